@@ -1,0 +1,368 @@
+"""Pins for the oracle's quantizers and dequantizers.
+
+The pages print no worked example for any of these formats, so each quantizer
+is pinned by what the formats and the mathematics fix: the amax element lands
+on the format maximum, codes are the nearest representable values of x/s
+(checked against an exact-rational search over all codes), powers of two
+scale through exactly, granules are independent, the packing layout is read
+back with an unpacker written from the format description, and
+dequant(quant(x)) stays within half a code step of x.
+"""
+import math
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+from serving_amax_reduce_gb300 import inputs
+
+
+def bf16_bits(t: torch.Tensor) -> np.ndarray:
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def vals(bits: np.ndarray) -> np.ndarray:
+    return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+E4M3_POS = None
+
+
+def e4m3_grid(orc):
+    global E4M3_POS
+    if E4M3_POS is None:
+        E4M3_POS = np.array(sorted({abs(orc.dec_e4m3(c)) for c in range(256)
+                                    if not math.isnan(orc.dec_e4m3(c))}))
+    return E4M3_POS
+
+
+E2M1_POS = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6], np.float64)
+
+
+def half_step(grid: np.ndarray, a: np.ndarray) -> np.ndarray:
+    """Half the distance between the two grid points around |a| (saturating)."""
+    a = np.minimum(np.abs(a), grid[-1])
+    i = np.clip(np.searchsorted(grid, a, side="right"), 1, len(grid) - 1)
+    return (grid[i] - grid[i - 1]) / 2
+
+
+def assert_nearest(dec_codes, target, grid, slack=1e-6):
+    """Each decoded code is within half a step of the (unsaturated) target."""
+    err = np.abs(dec_codes - np.clip(target, -grid[-1], grid[-1]))
+    bound = half_step(grid, target) * (1 + slack) + 1e-300
+    bad = err > bound
+    assert not bad.any(), (np.argwhere(bad)[:5], dec_codes[bad][:5], target[bad][:5])
+
+
+def dec_vec(fn, codes):
+    lut = np.array([fn(c) for c in range(256)], np.float64)
+    return lut[codes]
+
+
+def rand_bits(shape, seed, std=1.0):
+    return bf16_bits(inputs.normal_bf16(shape, std, seed))
+
+
+# ------------------------------------------------------------------ FP8 scaled
+@pytest.mark.parametrize("kind", ["tensor", "token", "block128"])
+def test_fp8_amax_maps_to_448_and_codes_are_nearest(orc, kind):
+    R, K = 256, 384
+    x = bf16_bits(inputs.outlier_channel_bf16(R, K, 77))
+    xv = vals(x)
+    q = {"tensor": orc.quant_fp8_tensor, "token": orc.quant_fp8_token,
+         "block128": orc.quant_fp8_block128}[kind]
+    codes, s = q(x)
+    if kind == "tensor":
+        s_full = np.full((R, K), float(s))
+        gran = [(slice(0, R), slice(0, K))]
+    elif kind == "token":
+        s_full = np.repeat(np.asarray(s, np.float64)[:, None], K, 1)
+        gran = [(slice(i, i + 1), slice(0, K)) for i in range(R)]
+    else:
+        s_full = np.kron(np.asarray(s, np.float64), np.ones((128, 128)))
+        gran = [(slice(i, i + 128), slice(j, j + 128)) for i in range(0, R, 128) for j in range(0, K, 128)]
+    d = dec_vec(orc.dec_e4m3, codes)
+    for g in gran:
+        a = np.abs(xv[g]).max()
+        sg = s_full[g].flat[0]
+        assert abs(sg * 448 - a) <= a * 2.0 ** -22            # s = amax/448 to binary32 rounding
+        at = np.abs(xv[g]) == a
+        assert np.all(np.abs(d[g][at]) == 448.0)
+    assert_nearest(d, xv / s_full, e4m3_grid(orc), slack=1e-5)
+
+
+@pytest.mark.parametrize("kind", ["tensor", "token", "block128"])
+def test_fp8_sign_symmetry_power_of_two_and_zero(orc, kind):
+    q = {"tensor": orc.quant_fp8_tensor, "token": orc.quant_fp8_token,
+         "block128": orc.quant_fp8_block128}[kind]
+    t = inputs.normal_bf16((128, 256), 0.02, 5)
+    c1, s1 = q(bf16_bits(t))
+    c2, s2 = q(bf16_bits(-t))
+    assert np.array_equal(c2, c1 ^ 0x80) and np.array_equal(s1, s2)
+    c3, s3 = q(bf16_bits(t * 4))
+    assert np.array_equal(c3, c1) and np.array_equal(np.asarray(s3), np.asarray(s1) * 4)
+    cz, sz = q(np.zeros((128, 256), np.uint16))
+    assert not cz.any() and np.all(np.asarray(sz) == 1.0)
+
+
+def test_fp8_block_granules_are_independent(orc):
+    w = rand_bits((256, 384), 9, 0.02)
+    c1, s1 = orc.quant_fp8_block128(w)
+    w2 = w.copy()
+    w2[128:256, 256:384] = bf16_bits(inputs.normal_bf16((128, 128), 50.0, 10))
+    c2, s2 = orc.quant_fp8_block128(w2)
+    changed = np.zeros((2, 3), bool)
+    changed[1, 2] = True
+    assert np.array_equal(s1[~changed], s2[~changed]) and s1[1, 2] != s2[1, 2]
+    mask = np.ones((256, 384), bool)
+    mask[128:, 256:] = False
+    assert np.array_equal(c1[mask], c2[mask])
+
+
+def test_fp8_token_rows_are_independent(orc):
+    x = rand_bits((8, 512), 12)
+    c1, s1 = orc.quant_fp8_token(x)
+    x2 = x.copy()
+    x2[3] = bf16_bits(inputs.normal_bf16((1, 512), 100.0, 13))[0]
+    c2, s2 = orc.quant_fp8_token(x2)
+    keep = np.arange(8) != 3
+    assert np.array_equal(c1[keep], c2[keep]) and np.array_equal(s1[keep], s2[keep])
+
+
+@pytest.mark.parametrize("kind", ["tensor", "token", "block128"])
+def test_fp8_dequant_close_and_index_layout(orc, kind):
+    """dequant(quant(x)) within half an E4M3 step of x; with granules of very
+    different magnitude a transposed scale index would miss by orders of magnitude."""
+    R, K = 256, 384
+    x = vals(rand_bits((R, K), 21))
+    x *= np.kron(10.0 ** np.arange(6).reshape(2, 3), np.ones((128, 128)))
+    xb = bf16_bits(torch.from_numpy(x).to(torch.bfloat16))
+    xv = vals(xb)
+    if kind == "tensor":
+        c, s = orc.quant_fp8_tensor(xb)
+        xh = orc.dequant_fp8_tensor(c, s)
+        sf = float(s)
+    elif kind == "token":
+        c, s = orc.quant_fp8_token(xb)
+        xh = orc.dequant_fp8_token(c, s)
+        sf = np.asarray(s, np.float64)[:, None]
+    else:
+        c, s = orc.quant_fp8_block128(xb)
+        xh = orc.dequant_fp8_block128(c, s)
+        sf = np.kron(np.asarray(s, np.float64), np.ones((128, 128)))
+    err = np.abs(xh - xv)
+    bound = half_step(e4m3_grid(orc), xv / sf) * sf * (1 + 1e-5)
+    assert np.all(err <= bound)
+
+
+# ------------------------------------------------------------------ MXFP8
+def test_mxfp8_shared_exponent_rule(orc):
+    x = bf16_bits(inputs.outlier_channel_bf16(64, 512, 31))
+    xv = vals(x)
+    codes, sc = orc.quant_mxfp8(x)
+    scale = np.vectorize(orc.dec_e8m0)(sc)
+    amax = np.abs(xv).reshape(64, 16, 32).max(-1)
+    # largest power of two <= amax, divided by 2^8 (the largest E4M3 power of two)
+    p2 = np.array([[2.0 ** (math.frexp(a)[1] - 1) for a in row] for row in amax])
+    assert np.array_equal(scale, p2 / 256)
+    assert np.all(np.log2(scale) == np.round(np.log2(scale)))          # powers of two
+    d = dec_vec(orc.dec_e4m3, codes)
+    target = xv / np.repeat(scale, 32, 1)                               # exact: power-of-two scaling
+    assert_nearest(d, target, e4m3_grid(orc))
+    # the amax element lands in [256, 448]
+    at = np.abs(xv).reshape(64, 16, 32) == amax[..., None]
+    dm = np.abs(d).reshape(64, 16, 32)[at]
+    assert np.all((dm >= 256) & (dm <= 448))
+
+
+def test_mxfp8_exact_bruteforce_small(orc):
+    from test_oracle_codecs import brute_nearest
+    table = [(c, orc.dec_e4m3(c)) for c in range(256) if not math.isnan(orc.dec_e4m3(c))]
+    x = bf16_bits(inputs.normal_bf16((2, 64), 3.0, 41))
+    codes, sc = orc.quant_mxfp8(x)
+    xv = vals(x)
+    for i in range(2):
+        for k in range(64):
+            v = xv[i, k] / orc.dec_e8m0(int(sc[i, k // 32]))
+            assert codes[i, k] == brute_nearest(v, table, 448.0, 3)
+
+
+def test_mxfp8_scale_by_two_and_zero(orc):
+    t = inputs.normal_bf16((16, 256), 1.0, 43)
+    c1, s1 = orc.quant_mxfp8(bf16_bits(t))
+    c2, s2 = orc.quant_mxfp8(bf16_bits(t * 2))
+    assert np.array_equal(c1, c2) and np.array_equal(s2.astype(int), s1.astype(int) + 1)
+    z = np.zeros((4, 64), np.uint16)
+    cz, sz = orc.quant_mxfp8(z)
+    assert not cz.any() and not sz.any()
+
+
+# ------------------------------------------------------------------ NVFP4
+def unpack_e2m1(packed: np.ndarray) -> np.ndarray:
+    """Two 4-bit codes per byte, the lower K index in the low nibble."""
+    out = np.empty((packed.shape[0], packed.shape[1] * 2), np.uint8)
+    out[:, 0::2] = packed & 0xF
+    out[:, 1::2] = packed >> 4
+    return out
+
+
+def test_nvfp4_two_level_scales(orc):
+    x = bf16_bits(inputs.outlier_channel_bf16(64, 256, 51))
+    xv = vals(x)
+    packed, sc, g = orc.quant_nvfp4(x)
+    A = np.abs(xv).max()
+    assert abs(float(g) * 2688 - A) <= A * 2.0 ** -22
+    dsb = dec_vec(orc.dec_e4m3, sc)
+    bmax = np.abs(xv).reshape(64, 16, 16).max(-1)
+    assert_nearest(dsb, bmax / 6 / float(g), e4m3_grid(orc), slack=1e-4)
+    codes = unpack_e2m1(packed)
+    d = np.array([orc.dec_e2m1(c) for c in range(16)])[codes]
+    denom = np.repeat(dsb, 16, 1) * float(g)
+    ok = denom > 0
+    assert_nearest(d[ok], xv[ok] / denom[ok], E2M1_POS, slack=1e-4)
+    assert np.all(codes[~ok] & 0x7 == 0)
+    # the tensor-amax element: block scale 448, code +-6
+    i, k = np.unravel_index(np.argmax(np.abs(xv)), xv.shape)
+    assert sc[i, k // 16] == 0x7E and abs(d[i, k]) == 6
+
+
+def test_nvfp4_packing_nibble_order(orc):
+    x = np.zeros((1, 16), np.uint16)
+    x[0, 0] = bf16_bits(torch.tensor([[6.0]], dtype=torch.bfloat16))[0, 0]
+    x[0, 3] = bf16_bits(torch.tensor([[-3.0]], dtype=torch.bfloat16))[0, 0]
+    packed, sc, g = orc.quant_nvfp4(x)
+    assert packed[0, 0] == 0x07            # k=0 -> low nibble (+6), k=1 -> high nibble (0)
+    assert packed[0, 1] == 0xD0            # k=2 low (0), k=3 high (-3 = 0b1101)
+    assert not packed[0, 2:].any()
+
+
+def test_nvfp4_dequant_close(orc):
+    x = bf16_bits(inputs.normal_bf16((32, 128), 1.0, 53))
+    xv = vals(x)
+    packed, sc, g = orc.quant_nvfp4(x)
+    xh = orc.dequant_nvfp4(packed, sc, g)
+    unit = np.repeat(dec_vec(orc.dec_e4m3, sc), 16, 1) * float(g)
+    bound = half_step(E2M1_POS, xv / unit) * unit * (1 + 1e-4)
+    assert np.all(np.abs(xh - xv) <= bound)
+
+
+# ------------------------------------------------------------------ int4
+def unpack_int4(qweight, qzeros, N, K):
+    """GPTQ-style layout: k = 8i + j in bits [4j, 4j+4) of qweight[i, n];
+    n = 8i + j in bits [4j, 4j+4) of qzeros[g, i]."""
+    qw = qweight.view(np.uint32)
+    q = np.empty((K, N), np.int64)
+    for j in range(8):
+        q[j::8, :] = (qw >> (4 * j)) & 0xF
+    qz = qzeros.view(np.uint32)
+    z = np.empty((K // 128, N), np.int64)
+    for j in range(8):
+        z[:, j::8] = (qz >> (4 * j)) & 0xF
+    return q, z
+
+
+def test_int4_rtn_invariants(orc):
+    N, K = 64, 384
+    w = bf16_bits(inputs.normal_bf16((N, K), 0.02, 61))
+    w[5, :128] = bf16_bits(torch.from_numpy(np.abs(vals(w[5:6, :128]))).to(torch.bfloat16))[0]  # all >= 0
+    w[6, 128:256] = 0                                                                        # all zero
+    wv = vals(w)
+    qw, sc, qz = orc.quant_int4_g128(w)
+    q, z = unpack_int4(qw, qz, N, K)
+    s = vals(sc)                                 # [K/128, N]
+    for n in range(N):
+        for g in range(K // 128):
+            grp = wv[n, g * 128:(g + 1) * 128]
+            qq = q[g * 128:(g + 1) * 128, n]
+            mn, mx = min(0.0, grp.min()), max(0.0, grp.max())
+            sg, zg = s[g, n], z[g, n]
+            if mx == mn:
+                assert sg == 1.0 and zg == 0 and not qq.any()
+                continue
+            assert abs(sg - (mx - mn) / 15) <= (mx - mn) / 15 * 2.0 ** -8
+            assert 0 <= zg <= 15 and np.all((qq >= 0) & (qq <= 15))
+            if mn < 0:
+                assert qq[np.argmin(grp)] == 0
+            if mn == 0:
+                assert zg == 0
+            # zero maps exactly: q == z wherever w == 0
+            assert np.all(qq[grp == 0] == zg)
+            deq = (qq - zg) * sg
+            inside = (grp / sg + zg >= -0.5) & (grp / sg + zg <= 15.5)
+            assert np.all(np.abs(deq - grp)[inside] <= sg / 2 * (1 + 1e-3))
+
+
+def test_int4_dequant_and_layout(orc):
+    N, K = 16, 256
+    w = bf16_bits(inputs.normal_bf16((N, K), 0.02, 63))
+    wv = vals(w)
+    wv_scaled = wv * np.array([1.0, 100.0])[np.arange(K) // 128][None, :] * (1 + np.arange(N))[:, None]
+    wb = bf16_bits(torch.from_numpy(wv_scaled).to(torch.bfloat16))
+    wv = vals(wb)
+    qw, sc, qz = orc.quant_int4_g128(wb)
+    assert qw.shape == (K // 8, N) and sc.shape == (K // 128, N) and qz.shape == (K // 128, N // 8)
+    wh = orc.dequant_int4_g128(qw, sc, qz)
+    s = vals(sc)
+    assert np.all(np.abs(wh - wv) <= np.repeat(s.T, 128, 1) * 0.5 * (1 + 1e-3) + 1e-30)
+    q, z = unpack_int4(qw, qz, N, K)
+    assert np.array_equal(wh, ((q - np.repeat(z, 128, 0)) * np.repeat(s, 128, 0)).T)
+
+
+def test_int4_exhaustive_code_roundtrip(orc):
+    """Every (q, z) pair survives pack -> unpack: build a weight whose RTN codes
+    are known (values already on the grid of a fixed scale) and read them back."""
+    N, K = 16, 128
+    sgrid = 2.0 ** -6
+    rng = np.random.default_rng(0)
+    # per column n choose z in 0..15, per k a code q; values (q - z) * s are exact
+    z = np.arange(N) % 16
+    q = np.array([[(k + 3 * n) % 16 for n in range(N)] for k in range(K)])
+    q[0, :] = 0
+    q[1, :] = 15                            # force range [(0-z)s, (15-z)s] so s = sgrid
+    w = ((q - z[None, :]) * sgrid).T         # [N, K]
+    zero_col = z == 0
+    wb = bf16_bits(torch.from_numpy(w).to(torch.bfloat16))
+    qw, sc, qz = orc.quant_int4_g128(wb)
+    qq, zz = unpack_int4(qw, qz, N, K)
+    assert np.all(vals(sc) == sgrid)
+    assert np.array_equal(zz[0], z)
+    assert np.array_equal(qq, q)
+    del rng, zero_col
+
+
+# ------------------------------------------------------------------ GEMM reference
+def test_gemm_ref_exact_rational_tiny(orc):
+    rng = np.random.default_rng(1)
+    for (M, N, K) in [(1, 1, 1), (3, 5, 7), (17, 9, 32), (32, 32, 32)]:
+        xb = bf16_bits(inputs.normal_bf16((M, K), 1.0, 100 + M))
+        wb = bf16_bits(inputs.normal_bf16((N, K), 1.0, 200 + N))
+        cx, sx = orc.quant_fp8_token(xb)
+        xh = orc.dequant_fp8_token(cx, sx)
+        wh = vals(wb)
+        alpha = 0.75
+        bias = rng.standard_normal(N)
+        y = orc.gemm_ref(xh, wh, alpha=alpha, bias=bias)
+        for m in range(M):
+            for n in range(N):
+                exact = Fraction(alpha) * sum(Fraction(float(xh[m, k])) * Fraction(float(wh[n, k]))
+                                              for k in range(K)) + Fraction(float(bias[n]))
+                assert abs(Fraction(float(y[m, n])) - exact) <= abs(exact) * Fraction(1, 2 ** 40) + Fraction(1, 2 ** 60)
+
+
+def test_gemm_ref_orientation(orc):
+    """Y = X W^T: Y[m, n] pairs row m of X with row n of W (nn.Linear layout)."""
+    X = np.zeros((2, 3)); X[1, 2] = 1.0
+    W = np.zeros((4, 3)); W[3, 2] = 5.0
+    Y = orc.gemm_ref(X, W)
+    assert Y.shape == (2, 4) and Y[1, 3] == 5.0 and np.count_nonzero(Y) == 1
+
+
+def test_gemm_metrics_and_pass_rule(orc):
+    rng = np.random.default_rng(2)
+    y = rng.standard_normal((64, 64))
+    ok, m = orc.gemm_pass(orc.bf16_round(y), y)
+    assert ok and m["relative_l2"] == pytest.approx(m["bf16_floor"])
+    ok, m = orc.gemm_pass(y * (1 + 5e-3), y)
+    assert not ok and m["relative_l2"] == pytest.approx(5e-3)
+    assert m["cosine"] == pytest.approx(1.0)
