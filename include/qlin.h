@@ -1,0 +1,191 @@
+/*
+ * qlin.h -- C ABI of the GB300 (sm_103a) quantized-linear library.
+ *
+ * The operations are the online-quantization linear method of
+ * "vLLM-Omni 在线量化（Online Quantization）完全指南：加载期动态量化 FP8 / Int8 /
+ * MXFP8 / MXFP4", section "在线量化的底层工作原理":
+ *   stage 2  the BF16 weight is quantized once after loading
+ *            (process_weights_after_loading)        -> qlin_quantize_weight
+ *   stage 3  every call quantizes the activation dynamically
+ *            (_quantize_activation)                 -> qlin_quantize_act
+ *            and runs the quantized matmul
+ *            (_quant_matmul)                        -> qlin_gemm
+ * The callers flatten 3-D activations to 2-D first, as the same stage's
+ * apply() skeleton does.  Formats and granularities:
+ *   FP8 per-tensor / per-token / 128x128 block: "[vLLM] 기타 양자화: FP8,
+ *     ModelOpt, INC, TorchAO, Quark", section "FP8: vLLM의 핵심 양자화".
+ *   MXFP8 (E8M0 scale per 32 K elements): stage 2 of the section above.
+ *   NVFP4 (mixed FP8/NVFP4 linears): "vLLM-Omni 量化推理实践", Table 1.
+ *   int4 asymmetric, group 128, auto_gptq packing, round-to-nearest
+ *     ("--iters 0"): "vLLM-Omni는 AutoRound 양자화로 추론을 가속화합니다",
+ *     section "새로운 모델 양자화".
+ *
+ * Conventions for every entry point:
+ *   - Pointers named *_dev are device pointers; the caller owns all memory
+ *     (inputs, outputs, workspace).  Entry points that take a stream never
+ *     allocate, never synchronize and never fall back to another path; they
+ *     enqueue kernels on `stream` and return.
+ *   - Matrices are row-major with the leading dimension in ELEMENTS.  X is
+ *     [M, K] (activations), W is [N, K] (nn.Linear weight), Y is [M, N].
+ *   - The return value covers host-side validation and launch errors only.
+ *     `dev_status_dev` (optional, may be NULL) is a device int that the
+ *     caller zeroes; a kernel writes QLIN_ERR_DEVICE_TIMEOUT into it if one
+ *     of its bounded waits gives up.  Such a kernel leaves its outputs
+ *     unspecified but returns, and the context stays usable.
+ *   - Inputs are finite.  NaN or Inf inputs give unspecified codes.
+ *
+ * Numeric rules (bit-exact; the pages name the formats but print no formula,
+ * so these are the plainest readings of the public format definitions):
+ *   FP8 (tensor, token, block): s = amax/448, code = E4M3(x * (448/amax)),
+ *     s = 1 and multiplier 1 when amax == 0.
+ *   MXFP8: e = clamp(floor(log2 amax) - 8, -127, 127); scale code e + 127;
+ *     code = E4M3(x * 2^-e).
+ *   NVFP4: g = A/2688 (A = tensor amax); block scale sb = UE4M3(b * (448/A));
+ *     code = E2M1(x * ((2688/A)/dec(sb))), 0 when dec(sb) == 0.
+ *   INT4: per (n, group of 128 k): range [min(0,min), max(0,max)],
+ *     s = bf16((max-min)/15) (1 if 0), z = clamp(rint(-min/s)), q =
+ *     clamp(rint(x/s) + z) with 1/s computed once in fp32.
+ *   Conversions round to nearest even and saturate (satfinite); a zero keeps
+ *   its sign.  Every fp32 operation is a single correctly rounded op.
+ */
+#ifndef QLIN_H
+#define QLIN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *qlin_stream_t;   /* same handle as cudaStream_t */
+
+typedef enum {
+    QLIN_FP8_TENSOR = 0,     /* E4M3 codes, one fp32 scale for the tensor          */
+    QLIN_FP8_TOKEN = 1,      /* E4M3 codes, one fp32 scale per row                 */
+    QLIN_FP8_BLOCK128 = 2,   /* E4M3 codes, one fp32 scale per 128x128 tile        */
+    QLIN_MXFP8 = 3,          /* E4M3 codes, one E8M0 scale byte per 32 along K     */
+    QLIN_NVFP4 = 4,          /* E2M1 codes 2/byte, UE4M3 per 16, fp32 per tensor   */
+    QLIN_INT4_G128_ASYM = 5, /* uint4 codes 8/int32, bf16 scale + uint4 zero / 128 */
+    QLIN_BF16 = 6            /* unquantized bf16 (the activation side of W4A16)    */
+} qlin_format;
+
+typedef enum {
+    /* Row-major [rows, K/G] scale tensor (G = 32 MXFP8, 16 NVFP4).            */
+    QLIN_SCALE_CANONICAL = 0,
+    /* Tensor-core-ready tiling, MXFP8 and NVFP4 only: for each 128-row tile
+     * (rows padded up to a multiple of 128 with scale code 0) and each chunk
+     * of 4 consecutive scales along K, 512 contiguous bytes; the scale of
+     * row r (r < 128 within the tile) and chunk position j (0..3) sits at
+     * byte 16*(r % 32) + 4*(r / 32) + j.  Tiles are ordered
+     * [row_tile][k_chunk].  This is the layout qlin_gemm consumes.            */
+    QLIN_SCALE_MMA = 1
+} qlin_scale_layout;
+
+typedef enum {
+    QLIN_OK = 0,
+    QLIN_ERR_INVALID_ARG = 1,    /* null pointer, bad size or leading dimension */
+    QLIN_ERR_UNSUPPORTED = 2,    /* format / layout / pair not provided          */
+    QLIN_ERR_ALIGNMENT = 3,      /* a pointer or stride breaks the 16-byte rule  */
+    QLIN_ERR_WORKSPACE = 4,      /* workspace missing or smaller than required   */
+    QLIN_ERR_CUDA = 5,           /* a CUDA call or launch failed                 */
+    QLIN_ERR_DEVICE_TIMEOUT = 6  /* written to dev_status by a kernel whose bounded wait expired */
+} qlin_status;
+
+const char *qlin_status_string(qlin_status s);
+
+/* ---------------------------------------------------------------- sizes
+ * Byte sizes of the buffers the quantizers write, for `rows` rows of K
+ * elements (rows = N for weights, M for activations).  0 means "not used by
+ * this format" or invalid arguments.                                        */
+
+/* Codes: FP8 formats rows*K; NVFP4 rows*K/2 (lower k in the low nibble);
+ * INT4 (K/8)*rows*4 as int32 [K/8, rows], k = 8i+j in bits [4j,4j+4).       */
+size_t qlin_codes_bytes(qlin_format fmt, int64_t rows, int64_t K);
+
+/* Scales: FP8_TENSOR 4 (one float); FP8_TOKEN rows*4; FP8_BLOCK128
+ * (rows/128)*(K/128)*4 row-major; MXFP8 rows*K/32 (canonical) or
+ * ceil(rows/128)*128*K/32 (MMA); NVFP4 rows*K/16 or ceil(rows/128)*128*K/16;
+ * INT4 (K/128)*rows*2, bf16 [K/128, rows].                                  */
+size_t qlin_scales_bytes(qlin_format fmt, qlin_scale_layout layout, int64_t rows, int64_t K);
+
+/* Zero points: INT4 only, (K/128)*(rows/8)*4 as int32 [K/128, rows/8],
+ * n = 8i+j in bits [4j,4j+4); no "-1" offset is applied.                     */
+size_t qlin_zeros_bytes(qlin_format fmt, int64_t rows, int64_t K);
+
+/* Workspace (device scratch) a quantizer call needs: the per-tensor
+ * formats (FP8_TENSOR, NVFP4) keep one float per reduction block; others 0. */
+size_t qlin_quant_workspace_bytes(qlin_format fmt, int64_t rows, int64_t K);
+
+/* Workspace a qlin_gemm call needs for this pair and shape (split-K partial
+ * sums and tile counters for the W4A16 decode GEMM; 0 for the others).      */
+size_t qlin_gemm_workspace_bytes(qlin_format w_fmt, qlin_format x_fmt,
+                                 int64_t M, int64_t N, int64_t K);
+
+/* ---------------------------------------------------------------- quantizers
+ * Quantize a bf16 matrix src[rows, K] (leading dimension ld >= K, elements)
+ * into caller-owned buffers, on `stream`.
+ *   codes_dev          qlin_codes_bytes(fmt, rows, K) bytes, 16-byte aligned
+ *   scales_dev         qlin_scales_bytes(fmt, layout, rows, K) bytes
+ *   zeros_dev          INT4 only (else NULL)
+ *   global_dev         NVFP4 only: one float, the per-tensor scale g
+ *   layout             QLIN_SCALE_MMA is accepted for MXFP8 and NVFP4 only
+ *   workspace_dev      qlin_quant_workspace_bytes(...) bytes (NULL if 0)
+ * Requirements: src and ld*2 bytes 16-byte aligned; K % 8 == 0;
+ *   FP8_BLOCK128: rows % 128 == 0 and K % 128 == 0; MXFP8: K % 32 == 0
+ *   (K % 128 == 0 for the MMA layout); NVFP4: K % 16 == 0 (K % 64 for MMA);
+ *   INT4: rows % 8 == 0 and K % 128 == 0.
+ * Errors: QLIN_ERR_INVALID_ARG, QLIN_ERR_ALIGNMENT, QLIN_ERR_UNSUPPORTED
+ *   (QLIN_BF16, or INT4 through qlin_quantize_act), QLIN_ERR_WORKSPACE,
+ *   QLIN_ERR_CUDA.                                                          */
+qlin_status qlin_quantize_weight(qlin_format fmt, const void *w_bf16_dev, int64_t N, int64_t K,
+                                 int64_t ldw, void *codes_dev, void *scales_dev, void *zeros_dev,
+                                 float *global_dev, qlin_scale_layout layout, void *workspace_dev,
+                                 size_t workspace_bytes, int *dev_status_dev, qlin_stream_t stream);
+
+qlin_status qlin_quantize_act(qlin_format fmt, const void *x_bf16_dev, int64_t M, int64_t K,
+                              int64_t ldx, void *codes_dev, void *scales_dev, float *global_dev,
+                              qlin_scale_layout layout, void *workspace_dev, size_t workspace_bytes,
+                              int *dev_status_dev, qlin_stream_t stream);
+
+/* ---------------------------------------------------------------- GEMM
+ * Y[M, N] (bf16, leading dimension ldy) = sum over k of dequant(X)[m,k] *
+ * dequant(W)[n,k], fp32 accumulation, optional bf16 bias[N] added before the
+ * final round to bf16 (the fused alpha*(A@B)+bias epilogue of
+ * "vLLM-Omni 在线量化（Online Quantization）完全指南" section
+ * "在线量化的底层工作原理", FP8 paragraph).
+ * Supported (w_fmt, x_fmt) pairs and their operands:
+ *   FP8_TENSOR, FP8_TENSOR : x = codes [M,K]; x_scales, w_scales = one float each
+ *   FP8_BLOCK128, FP8_TOKEN: x_scales float [M]; w_scales float [N/128, K/128]
+ *                            (N % 128 == 0, K % 128 == 0)
+ *   MXFP8, MXFP8           : scales in QLIN_SCALE_MMA layout (K % 128 == 0)
+ *   NVFP4, NVFP4           : scales in QLIN_SCALE_MMA layout, x_global and
+ *                            w_global one float each (K % 256 == 0)
+ *   INT4_G128_ASYM, BF16   : x = bf16 activations [M,K] row-major; w_codes
+ *                            qweight, w_scales bf16, w_zeros qzeros (K % 128 == 0,
+ *                            N % 8 == 0); workspace per qlin_gemm_workspace_bytes
+ * Other pairs return QLIN_ERR_UNSUPPORTED.  All operand rows are contiguous
+ * (leading dimension K, or K/2 bytes for NVFP4 codes); ldy >= N and ldy*2
+ * bytes 16-byte aligned.  M may be any value >= 1 (the row tail is handled
+ * in the kernels; buffers are not padded).                                  */
+qlin_status qlin_gemm(qlin_format w_fmt, qlin_format x_fmt, int64_t M, int64_t N, int64_t K,
+                      const void *x_dev, const void *x_scales_dev, const float *x_global_dev,
+                      const void *w_codes_dev, const void *w_scales_dev, const void *w_zeros_dev,
+                      const float *w_global_dev, const void *bias_bf16_dev, void *y_bf16_dev,
+                      int64_t ldy, qlin_scale_layout layout, void *workspace_dev,
+                      size_t workspace_bytes, int *dev_status_dev, qlin_stream_t stream);
+
+/* ---------------------------------------------------------------- diagnostics
+ * Runs the library's bounded device wait on an mbarrier that nothing ever
+ * completes, with at most `max_polls` polls, then writes
+ * QLIN_ERR_DEVICE_TIMEOUT into *dev_status_dev.  Exists so that the timeout
+ * path can be exercised without hanging or faulting a GPU.                  */
+qlin_status qlin_debug_expire_wait(int *dev_status_dev, uint32_t max_polls, qlin_stream_t stream);
+
+/* Library version string, e.g. "qlin 0.1 sm_103a". */
+const char *qlin_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* QLIN_H */

@@ -1,0 +1,219 @@
+// C ABI: argument validation, buffer-size queries and dispatch to the
+// kernels.  Nothing here allocates, synchronizes or falls back to another
+// path: a call that cannot run returns an error code before any launch.
+#include <cuda_runtime.h>
+
+#include "qlin_internal.h"
+
+using namespace qlin;
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool is_quant_format(qlin_format f) { return f >= QLIN_FP8_TENSOR && f <= QLIN_INT4_G128_ASYM; }
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+qlin_status launch_status(cudaError_t e) { return e == cudaSuccess ? QLIN_OK : QLIN_ERR_CUDA; }
+
+// Shape rules per format (see qlin.h).
+qlin_status check_quant_shape(qlin_format fmt, qlin_scale_layout layout, int64_t rows, int64_t K) {
+    if (rows < 1 || K < 8 || (K & 7) || rows > 0x7FFFFFFFll) return QLIN_ERR_INVALID_ARG;
+    if (layout != QLIN_SCALE_CANONICAL && layout != QLIN_SCALE_MMA) return QLIN_ERR_INVALID_ARG;
+    if (layout == QLIN_SCALE_MMA && fmt != QLIN_MXFP8 && fmt != QLIN_NVFP4) return QLIN_ERR_UNSUPPORTED;
+    switch (fmt) {
+        case QLIN_FP8_TENSOR:
+        case QLIN_FP8_TOKEN: return QLIN_OK;
+        case QLIN_FP8_BLOCK128: return (rows % 128 || K % 128) ? QLIN_ERR_INVALID_ARG : QLIN_OK;
+        case QLIN_MXFP8:
+            if (K % 32) return QLIN_ERR_INVALID_ARG;
+            return (layout == QLIN_SCALE_MMA && K % 128) ? QLIN_ERR_INVALID_ARG : QLIN_OK;
+        case QLIN_NVFP4:
+            if (K % 16) return QLIN_ERR_INVALID_ARG;
+            return (layout == QLIN_SCALE_MMA && K % 64) ? QLIN_ERR_INVALID_ARG : QLIN_OK;
+        case QLIN_INT4_G128_ASYM: return (rows % 8 || K % 128) ? QLIN_ERR_INVALID_ARG : QLIN_OK;
+        default: return QLIN_ERR_UNSUPPORTED;
+    }
+}
+
+qlin_status quantize(qlin_format fmt, const void* src, int64_t rows, int64_t K, int64_t ld, void* codes,
+                     void* scales, void* zeros, float* global, qlin_scale_layout layout, void* ws,
+                     size_t ws_bytes, cudaStream_t st) {
+    if (!is_quant_format(fmt)) return QLIN_ERR_UNSUPPORTED;
+    qlin_status s = check_quant_shape(fmt, layout, rows, K);
+    if (s != QLIN_OK) return s;
+    if (!src || !codes || !scales || ld < K) return QLIN_ERR_INVALID_ARG;
+    if (fmt == QLIN_INT4_G128_ASYM && !zeros) return QLIN_ERR_INVALID_ARG;
+    if (fmt == QLIN_NVFP4 && !global) return QLIN_ERR_INVALID_ARG;
+    if (!aligned16(src) || (ld * 2) % 16 || !aligned16(codes)) return QLIN_ERR_ALIGNMENT;
+    if (fmt == QLIN_FP8_TOKEN || fmt == QLIN_FP8_BLOCK128 || fmt == QLIN_FP8_TENSOR) {
+        if (reinterpret_cast<uintptr_t>(scales) & 3u) return QLIN_ERR_ALIGNMENT;
+    }
+    if (fmt == QLIN_INT4_G128_ASYM &&
+        ((reinterpret_cast<uintptr_t>(scales) & 1u) || (reinterpret_cast<uintptr_t>(zeros) & 3u)))
+        return QLIN_ERR_ALIGNMENT;
+    const size_t need = qlin_quant_workspace_bytes(fmt, rows, K);
+    if (need && (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 3u))) return QLIN_ERR_WORKSPACE;
+
+    const uint16_t* x = static_cast<const uint16_t*>(src);
+    uint8_t* c = static_cast<uint8_t*>(codes);
+    const bool mma = layout == QLIN_SCALE_MMA;
+    switch (fmt) {
+        case QLIN_FP8_TENSOR:
+            return launch_status(launch_fp8_tensor(x, rows, K, ld, c, static_cast<float*>(scales),
+                                                   static_cast<float*>(ws), amax_partials(rows, K), st));
+        case QLIN_FP8_TOKEN:
+            return launch_status(launch_fp8_rowwise(x, rows, K, ld, c, static_cast<float*>(scales), st));
+        case QLIN_FP8_BLOCK128:
+            return launch_status(launch_fp8_block128(x, rows, K, ld, c, static_cast<float*>(scales), st));
+        case QLIN_MXFP8:
+            return launch_status(launch_mxfp8(x, rows, K, ld, c, static_cast<uint8_t*>(scales), mma, st));
+        case QLIN_NVFP4:
+            return launch_status(launch_nvfp4(x, rows, K, ld, c, static_cast<uint8_t*>(scales), global, mma,
+                                              static_cast<float*>(ws), amax_partials(rows, K), st));
+        case QLIN_INT4_G128_ASYM:
+            return launch_status(launch_int4_g128(x, rows, K, ld, reinterpret_cast<int32_t*>(codes),
+                                                  static_cast<uint16_t*>(scales), static_cast<int32_t*>(zeros),
+                                                  st));
+        default: return QLIN_ERR_UNSUPPORTED;
+    }
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* qlin_status_string(qlin_status s) {
+    switch (s) {
+        case QLIN_OK: return "ok";
+        case QLIN_ERR_INVALID_ARG: return "invalid argument (null pointer, size or leading dimension)";
+        case QLIN_ERR_UNSUPPORTED: return "unsupported format, layout or format pair";
+        case QLIN_ERR_ALIGNMENT: return "pointer or stride not 16-byte aligned";
+        case QLIN_ERR_WORKSPACE: return "workspace missing or too small";
+        case QLIN_ERR_CUDA: return "CUDA launch or call failed";
+        case QLIN_ERR_DEVICE_TIMEOUT: return "a bounded device wait expired";
+        default: return "unknown status";
+    }
+}
+
+const char* qlin_version(void) { return "qlin 0.1 sm_103a"; }
+
+size_t qlin_codes_bytes(qlin_format fmt, int64_t rows, int64_t K) {
+    if (rows < 1 || K < 1) return 0;
+    switch (fmt) {
+        case QLIN_FP8_TENSOR:
+        case QLIN_FP8_TOKEN:
+        case QLIN_FP8_BLOCK128:
+        case QLIN_MXFP8: return (size_t)(rows * K);
+        case QLIN_NVFP4: return (size_t)(rows * (K / 2));
+        case QLIN_INT4_G128_ASYM: return (size_t)((K / 8) * rows * 4);
+        default: return 0;
+    }
+}
+
+size_t qlin_scales_bytes(qlin_format fmt, qlin_scale_layout layout, int64_t rows, int64_t K) {
+    if (rows < 1 || K < 1) return 0;
+    const int64_t rows_pad = ceil_div(rows, 128) * 128;
+    switch (fmt) {
+        case QLIN_FP8_TENSOR: return 4;
+        case QLIN_FP8_TOKEN: return (size_t)(rows * 4);
+        case QLIN_FP8_BLOCK128: return (size_t)((rows / 128) * (K / 128) * 4);
+        case QLIN_MXFP8: return (size_t)((layout == QLIN_SCALE_MMA ? rows_pad : rows) * (K / 32));
+        case QLIN_NVFP4: return (size_t)((layout == QLIN_SCALE_MMA ? rows_pad : rows) * (K / 16));
+        case QLIN_INT4_G128_ASYM: return (size_t)((K / 128) * rows * 2);
+        default: return 0;
+    }
+}
+
+size_t qlin_zeros_bytes(qlin_format fmt, int64_t rows, int64_t K) {
+    if (fmt != QLIN_INT4_G128_ASYM || rows < 1 || K < 1) return 0;
+    return (size_t)((K / 128) * (rows / 8) * 4);
+}
+
+size_t qlin_quant_workspace_bytes(qlin_format fmt, int64_t rows, int64_t K) {
+    if (rows < 1 || K < 1) return 0;
+    if (fmt == QLIN_FP8_TENSOR || fmt == QLIN_NVFP4) return (size_t)amax_partials(rows, K) * sizeof(float);
+    return 0;
+}
+
+size_t qlin_gemm_workspace_bytes(qlin_format w_fmt, qlin_format x_fmt, int64_t M, int64_t N, int64_t K) {
+    if (M < 1 || N < 1 || K < 1) return 0;
+    if (w_fmt == QLIN_INT4_G128_ASYM && x_fmt == QLIN_BF16) return w4a16_workspace_bytes(M, N, K);
+    return 0;
+}
+
+qlin_status qlin_quantize_weight(qlin_format fmt, const void* w_bf16_dev, int64_t N, int64_t K, int64_t ldw,
+                                 void* codes_dev, void* scales_dev, void* zeros_dev, float* global_dev,
+                                 qlin_scale_layout layout, void* workspace_dev, size_t workspace_bytes,
+                                 int* dev_status_dev, qlin_stream_t stream) {
+    (void)dev_status_dev;   // the quantizers have no device-side waits
+    return quantize(fmt, w_bf16_dev, N, K, ldw, codes_dev, scales_dev, zeros_dev, global_dev, layout,
+                    workspace_dev, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+qlin_status qlin_quantize_act(qlin_format fmt, const void* x_bf16_dev, int64_t M, int64_t K, int64_t ldx,
+                              void* codes_dev, void* scales_dev, float* global_dev, qlin_scale_layout layout,
+                              void* workspace_dev, size_t workspace_bytes, int* dev_status_dev,
+                              qlin_stream_t stream) {
+    (void)dev_status_dev;
+    if (fmt == QLIN_INT4_G128_ASYM) return QLIN_ERR_UNSUPPORTED;   // int4 is weight-only (W4A16)
+    return quantize(fmt, x_bf16_dev, M, K, ldx, codes_dev, scales_dev, nullptr, global_dev, layout,
+                    workspace_dev, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+qlin_status qlin_gemm(qlin_format w_fmt, qlin_format x_fmt, int64_t M, int64_t N, int64_t K, const void* x_dev,
+                      const void* x_scales_dev, const float* x_global_dev, const void* w_codes_dev,
+                      const void* w_scales_dev, const void* w_zeros_dev, const float* w_global_dev,
+                      const void* bias_bf16_dev, void* y_bf16_dev, int64_t ldy, qlin_scale_layout layout,
+                      void* workspace_dev, size_t workspace_bytes, int* dev_status_dev, qlin_stream_t stream) {
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (M < 1 || N < 1 || K < 1 || M > 0x7FFFFFFFll || N > 0x7FFFFFFFll || ldy < N) return QLIN_ERR_INVALID_ARG;
+    if (!x_dev || !w_codes_dev || !y_bf16_dev) return QLIN_ERR_INVALID_ARG;
+    if (!aligned16(x_dev) || !aligned16(w_codes_dev) || !aligned16(y_bf16_dev) || (ldy * 2) % 16 ||
+        (bias_bf16_dev && !aligned16(bias_bf16_dev)))
+        return QLIN_ERR_ALIGNMENT;
+    GemmArgs a{M, N, K, ldy, x_dev, x_scales_dev, x_global_dev, w_codes_dev, w_scales_dev, w_zeros_dev,
+               w_global_dev, static_cast<const uint16_t*>(bias_bf16_dev), static_cast<uint16_t*>(y_bf16_dev),
+               workspace_dev, workspace_bytes, dev_status_dev};
+    if (w_fmt == QLIN_FP8_TENSOR && x_fmt == QLIN_FP8_TENSOR) {
+        if (!x_scales_dev || !w_scales_dev) return QLIN_ERR_INVALID_ARG;
+        if (K % 16) return QLIN_ERR_INVALID_ARG;
+        return launch_status(launch_gemm_fp8_tensor(a, st));
+    }
+    if (w_fmt == QLIN_FP8_BLOCK128 && x_fmt == QLIN_FP8_TOKEN) {
+        if (!x_scales_dev || !w_scales_dev) return QLIN_ERR_INVALID_ARG;
+        if (N % 128 || K % 128) return QLIN_ERR_INVALID_ARG;
+        return launch_status(launch_gemm_fp8_block(a, st));
+    }
+    if (w_fmt == QLIN_MXFP8 && x_fmt == QLIN_MXFP8) {
+        if (layout != QLIN_SCALE_MMA) return QLIN_ERR_UNSUPPORTED;
+        if (!x_scales_dev || !w_scales_dev) return QLIN_ERR_INVALID_ARG;
+        if (K % 128) return QLIN_ERR_INVALID_ARG;
+        if (!aligned16(x_scales_dev) || !aligned16(w_scales_dev)) return QLIN_ERR_ALIGNMENT;
+        return launch_status(launch_gemm_mxfp8(a, st));
+    }
+    if (w_fmt == QLIN_NVFP4 && x_fmt == QLIN_NVFP4) {
+        if (layout != QLIN_SCALE_MMA) return QLIN_ERR_UNSUPPORTED;
+        if (!x_scales_dev || !w_scales_dev || !x_global_dev || !w_global_dev) return QLIN_ERR_INVALID_ARG;
+        if (K % 256) return QLIN_ERR_INVALID_ARG;
+        if (!aligned16(x_scales_dev) || !aligned16(w_scales_dev)) return QLIN_ERR_ALIGNMENT;
+        return launch_status(launch_gemm_nvfp4(a, st));
+    }
+    if (w_fmt == QLIN_INT4_G128_ASYM && x_fmt == QLIN_BF16) {
+        if (!w_scales_dev || !w_zeros_dev) return QLIN_ERR_INVALID_ARG;
+        if (K % 128 || N % 8) return QLIN_ERR_INVALID_ARG;
+        const size_t need = w4a16_workspace_bytes(M, N, K);
+        if (need && (!workspace_dev || workspace_bytes < need || !aligned16(workspace_dev)))
+            return QLIN_ERR_WORKSPACE;
+        return launch_status(launch_gemm_w4a16(a, st));
+    }
+    return QLIN_ERR_UNSUPPORTED;
+}
+
+qlin_status qlin_debug_expire_wait(int* dev_status_dev, uint32_t max_polls, qlin_stream_t stream) {
+    if (!dev_status_dev) return QLIN_ERR_INVALID_ARG;
+    return launch_status(launch_debug_expire_wait(dev_status_dev, max_polls, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,494 @@
+// Scaled low-precision GEMMs on the sm_103a tensor cores (tcgen05 + TMEM).
+//
+//   Y[m, n] = bf16( epilogue( sum_k Xq[m, k] * Wq[n, k] ) )
+//
+// The quantized matmul of "vLLM-Omni 在线量化（Online Quantization）完全指南"
+// section "在线量化的底层工作原理" stage 3, for the formats of
+// "[vLLM] 기타 양자화: FP8, ModelOpt, INC, TorchAO, Quark" section
+// "FP8: vLLM의 핵심 양자화" (per-tensor; per-token x 128x128 block),
+// stage 2 of the first page (MXFP8, E8M0 per 32 along K) and
+// "vLLM-Omni 量化推理实践" Table 1 (NVFP4 attention projections of the mixed
+// FP8/NVFP4 model).  The optional bias epilogue is the fused
+// alpha * (A @ B) + bias the first page mentions for Blackwell FP8.
+//
+// One CTA computes a 128 x 256 output tile with a warp-specialized pipeline:
+//   warp 0   one lane issues TMA loads of the X and W tiles (128-byte
+//            swizzle, zero fill past M) and the scale chunks into a
+//            4-stage shared-memory ring;
+//   warp 1   allocates TMEM; one lane issues tcgen05.mma into the TMEM
+//            accumulator and tcgen05.commit to release each stage;
+//   warps 2+ drain TMEM with tcgen05.ld, apply the scales and write bf16.
+// Variants:
+//   FP8 per-tensor  kind::f8f6f4, alpha = s_x * s_w in the epilogue.
+//   FP8 block       kind::f8f6f4 into one of two TMEM partial buffers per
+//                   128-wide K block; eight epilogue warps promote each
+//                   partial with its fp32 weight-block scale into register
+//                   accumulators (fp32 block scales are not an MMA scale
+//                   type), then multiply by the per-token scale.
+//   MXFP8           kind::mxf8f6f4.block_scale.scale_vec::1X, UE8M0 scales
+//                   copied smem -> TMEM with tcgen05.cp.
+//   NVFP4           kind::mxf4nvf4.block_scale.scale_vec::4X, UE4M3 scales,
+//                   alpha = g_x * g_w.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "qlin_internal.h"
+#include "tc_ptx.cuh"
+
+namespace qlin {
+namespace {
+
+using namespace ptx;
+
+enum Kind { kFp8Tensor = 0, kFp8Block = 1, kMxfp8 = 2, kNvfp4 = 3 };
+
+constexpr int BM = 128;              // tile rows (X rows) = MMA M
+constexpr int BKB = 128;             // K bytes per stage: 128 fp8 or 256 fp4 (one swizzle row)
+constexpr uint64_t kWaitLimitNs = 1000000000ull;   // bounded waits give up after 1 s
+
+template <int KIND>
+struct Cfg {
+    static constexpr int BN = 256;
+    static constexpr int STAGES = 4;
+    static constexpr int EPI_WARPS = (KIND == kFp8Block) ? 8 : 4;
+    static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+    static constexpr int A_BYTES = BM * BKB;
+    static constexpr int B_BYTES = BN * BKB;
+    // 512-byte scale chunks (128 rows x 4 scales) per 128 rows per stage
+    static constexpr int SF_CHUNKS = (KIND == kMxfp8) ? 1 : (KIND == kNvfp4 ? 4 : 0);
+    static constexpr int SFA_BYTES = SF_CHUNKS * 512;
+    static constexpr int SFB_BYTES = SF_CHUNKS * 512 * (BN / 128);
+    static constexpr int KSTEPS = BKB / 32;          // each MMA consumes 32 bytes of K
+    static constexpr int OFF_A = 0;
+    static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
+    static constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
+    static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
+    static constexpr int OFF_BAR = OFF_SFB + STAGES * SFB_BYTES;
+    static constexpr int NBAR = 2 * STAGES + 6;      // full[S], empty[S], acc, pfull[2], pempty[2], drain
+    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+    static constexpr int SMEM = OFF_MISC + 64 + 1024; // + slack for 1024-byte alignment
+    static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr int SFA_COL = 256;
+    static constexpr int SFA_COLS = 4 * SF_CHUNKS;             // per stage
+    static constexpr int SFB_COL = SFA_COL + STAGES * SFA_COLS;
+    static constexpr int SFB_COLS = 4 * SF_CHUNKS * (BN / 128); // per stage
+    static_assert(SFB_COL + STAGES * SFB_COLS <= 512, "TMEM budget");
+    static_assert(SMEM <= 232448, "shared memory budget");
+};
+
+// Instruction descriptors (M = 128, N = BN, both operands K-major).
+template <int KIND>
+__host__ __device__ constexpr uint32_t idesc_for() {
+    constexpr uint32_t n = (uint32_t)(Cfg<KIND>::BN >> 3) << 17;
+    constexpr uint32_t m = (uint32_t)(BM >> 4) << 24;
+    if (KIND == kFp8Tensor || KIND == kFp8Block)
+        return (1u << 4) /* D f32 */ | (0u << 7) /* A e4m3 */ | (0u << 10) /* B e4m3 */ | n | m;
+    if (KIND == kMxfp8)
+        return (0u << 7) | (0u << 10) | n | (1u << 23) /* UE8M0 scales */ | m;
+    return (1u << 7) /* A e2m1 */ | (1u << 10) /* B e2m1 */ | n | (0u << 23) /* UE4M3 scales */ | m;
+}
+
+struct TcParams {
+    int M, N, K, nk;
+    int64_t ldy;
+    const float* x_scale;    // tensor: [1]; block: per-token [M]
+    const float* w_scale;    // tensor: [1]; block: [N/128, K/128]
+    const float* x_global;   // NVFP4
+    const float* w_global;
+    const uint8_t* sfa;      // MXFP8 / NVFP4 scales, tensor-core tiling
+    const uint8_t* sfb;
+    int64_t sf_chunks_per_row;
+    const uint16_t* bias;
+    uint16_t* y;
+    int* status;
+};
+
+__device__ __forceinline__ void record_timeout(int* status, volatile uint32_t* abort_flag) {
+    *abort_flag = 1u;
+    if (status) atomicExch(status, (int)QLIN_ERR_DEVICE_TIMEOUT);
+}
+
+// Wait with the wall-clock bound; also gives up early once another role of
+// this CTA has aborted.
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile uint32_t* abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 32; i++)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    }
+}
+
+// Warp-uniform variant for the epilogue warps: lane 0 polls, the verdict is
+// broadcast so that the following .sync.aligned TMEM loads stay converged.
+__device__ __forceinline__ bool warp_wait_or_abort(uint64_t* bar, uint32_t parity, volatile uint32_t* abort_flag) {
+    bool ok = true;
+    if ((threadIdx.x & 31) == 0) ok = wait_or_abort(bar, parity, abort_flag);
+    return __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Write 32 consecutive outputs of one row (values already scaled).
+__device__ __forceinline__ void store_row32(const TcParams& p, int row, int n, const float (&v)[32]) {
+    uint16_t* dst = p.y + (int64_t)row * p.ldy + n;
+    if (n + 32 <= p.N) {
+        uint32_t w[16];
+#pragma unroll
+        for (int i = 0; i < 16; i++) {
+            float a = v[2 * i], b = v[2 * i + 1];
+            if (p.bias) {
+                a += __bfloat162float(__ushort_as_bfloat16(p.bias[n + 2 * i]));
+                b += __bfloat162float(__ushort_as_bfloat16(p.bias[n + 2 * i + 1]));
+            }
+            w[i] = pack_bf16x2(a, b);
+        }
+        uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+        for (int i = 0; i < 4; i++) d4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+    } else {
+        for (int i = 0; i < 32 && n + i < p.N; i++) {
+            float a = v[i];
+            if (p.bias) a += __bfloat162float(__ushort_as_bfloat16(p.bias[n + i]));
+            dst[i] = __bfloat16_as_ushort(__float2bfloat16_rn(a));
+        }
+    }
+}
+
+template <int KIND>
+__global__ void __launch_bounds__(Cfg<KIND>::THREADS, 1)
+    k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const TcParams p) {
+    using C = Cfg<KIND>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+    uint64_t* empty = full + C::STAGES;
+    uint64_t* accf = empty + C::STAGES;
+    uint64_t* pfull = accf + 1;
+    uint64_t* pempty = pfull + 2;
+    uint64_t* drain = pempty + 2;
+    uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);   // tmem base, abort, consumed, issued
+    volatile uint32_t* abort_flag = misc + 1;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n0 = blockIdx.x * C::BN, m0 = blockIdx.y * BM;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::STAGES; s++) {
+            mbar_init(full + s, 1);
+            mbar_init(empty + s, 1);
+        }
+        mbar_init(accf, 1);
+        mbar_init(pfull + 0, 1);
+        mbar_init(pfull + 1, 1);
+        mbar_init(pempty + 0, C::EPI_WARPS);
+        mbar_init(pempty + 1, C::EPI_WARPS);
+        mbar_init(drain, 1);
+        fence_mbar_init();
+        // a launch that follows an expired wait does no work
+        misc[1] = (p.status && *reinterpret_cast<volatile int*>(p.status) != 0) ? 1u : 0u;
+        misc[2] = 0;
+        misc[3] = 0;
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmB);
+    }
+    if (warp == 1) tmem_alloc(misc, C::TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = misc[0];
+    const bool skip = misc[1] != 0;
+
+    if (!skip && warp == 0 && lane == 0) {
+        // ------------------------------------------------ TMA producer
+        int issued = 0;
+        const int ntiles_b = (p.N + 127) / 128;
+        for (int kb = 0; kb < p.nk; kb++) {
+            const int s = kb % C::STAGES;
+            const uint32_t ph = (uint32_t)(kb / C::STAGES) & 1u;
+            if (!wait_or_abort(empty + s, ph ^ 1u, abort_flag)) {
+                record_timeout(p.status, abort_flag);
+                break;
+            }
+            uint32_t bytes = C::A_BYTES + C::B_BYTES;
+            if (C::SF_CHUNKS) {
+                bytes += C::SFA_BYTES;
+                for (int j = 0; j < C::BN / 128; j++)
+                    if ((n0 >> 7) + j < ntiles_b) bytes += C::SF_CHUNKS * 512;
+            }
+            mbar_arrive_expect_tx(full + s, bytes);
+            tma_load_2d(smem + C::OFF_A + s * C::A_BYTES, &tmA, kb * BKB, m0, full + s);
+            tma_load_2d(smem + C::OFF_B + s * C::B_BYTES, &tmB, kb * BKB, n0, full + s);
+            if (C::SF_CHUNKS) {
+                const int64_t cpr = p.sf_chunks_per_row;
+                bulk_load(smem + C::OFF_SFA + s * C::SFA_BYTES,
+                          p.sfa + (((int64_t)(m0 >> 7) * cpr + (int64_t)kb * C::SF_CHUNKS) << 9), C::SFA_BYTES,
+                          full + s);
+                for (int j = 0; j < C::BN / 128; j++) {
+                    const int nt = (n0 >> 7) + j;
+                    if (nt < ntiles_b)
+                        bulk_load(smem + C::OFF_SFB + s * C::SFB_BYTES + j * C::SF_CHUNKS * 512,
+                                  p.sfb + (((int64_t)nt * cpr + (int64_t)kb * C::SF_CHUNKS) << 9),
+                                  C::SF_CHUNKS * 512, full + s);
+                }
+            }
+            issued = kb + 1;
+        }
+        misc[3] = (uint32_t)issued;
+    } else if (!skip && warp == 1 && lane == 0) {
+        // ------------------------------------------------ MMA issuer
+        constexpr uint32_t idesc = idesc_for<KIND>();
+        for (int kb = 0; kb < p.nk; kb++) {
+            const int s = kb % C::STAGES;
+            const uint32_t ph = (uint32_t)(kb / C::STAGES) & 1u;
+            if (!wait_or_abort(full + s, ph, abort_flag)) {
+                record_timeout(p.status, abort_flag);
+                break;
+            }
+            uint32_t d = tmem;
+            if (KIND == kFp8Block) {
+                const int b = kb & 1;
+                if (!wait_or_abort(pempty + b, ((uint32_t)(kb >> 1) & 1u) ^ 1u, abort_flag)) {
+                    record_timeout(p.status, abort_flag);
+                    break;
+                }
+                d = tmem + (uint32_t)(b * C::BN);
+            }
+            tc_fence_after();
+            const uint32_t a_base = smem_u32(smem + C::OFF_A + s * C::A_BYTES);
+            const uint32_t b_base = smem_u32(smem + C::OFF_B + s * C::B_BYTES);
+            const uint32_t sfa_base = smem_u32(smem + C::OFF_SFA + s * C::SFA_BYTES);
+            const uint32_t sfb_base = smem_u32(smem + C::OFF_SFB + s * C::SFB_BYTES);
+            if (KIND == kMxfp8) {
+                tmem_cp_32x128b_x4(tmem + C::SFA_COL + s * C::SFA_COLS, sdesc_sf(sfa_base));
+#pragma unroll
+                for (int j = 0; j < C::BN / 128; j++)
+                    tmem_cp_32x128b_x4(tmem + C::SFB_COL + s * C::SFB_COLS + j * 4, sdesc_sf(sfb_base + j * 512));
+            }
+            if (KIND == kNvfp4) {
+#pragma unroll
+                for (int c = 0; c < 4; c++) {
+                    tmem_cp_32x128b_x4(tmem + C::SFA_COL + s * C::SFA_COLS + c * 4, sdesc_sf(sfa_base + c * 512));
+#pragma unroll
+                    for (int j = 0; j < C::BN / 128; j++)
+                        tmem_cp_32x128b_x4(tmem + C::SFB_COL + s * C::SFB_COLS + c * 4 * (C::BN / 128) + j * 4,
+                                           sdesc_sf(sfb_base + (j * 4 + c) * 512));
+                }
+            }
+#pragma unroll
+            for (int c = 0; c < C::KSTEPS; c++) {
+                const uint64_t ad = sdesc_sw128(a_base + c * 32);
+                const uint64_t bd = sdesc_sw128(b_base + c * 32);
+                const uint32_t acc = (KIND == kFp8Block) ? (c > 0) : (kb > 0 || c > 0);
+                if (KIND == kFp8Tensor || KIND == kFp8Block) {
+                    mma_f8f6f4(d, ad, bd, idesc, acc);
+                } else if (KIND == kMxfp8) {
+                    const uint32_t id = idesc | ((uint32_t)c << 4) | ((uint32_t)c << 29);
+                    mma_mxf8(d, ad, bd, id, tmem + C::SFA_COL + s * C::SFA_COLS,
+                             tmem + C::SFB_COL + s * C::SFB_COLS, acc);
+                } else {
+                    mma_nvf4(d, ad, bd, idesc, tmem + C::SFA_COL + s * C::SFA_COLS + c * 4,
+                             tmem + C::SFB_COL + s * C::SFB_COLS + c * 4 * (C::BN / 128), acc);
+                }
+            }
+            tc_commit(empty + s);
+            if (KIND == kFp8Block) tc_commit(pfull + (kb & 1));
+            misc[2] = (uint32_t)(kb + 1);
+        }
+        // Completes once every MMA issued above has finished (also after an abort).
+        if (KIND != kFp8Block) tc_commit(accf);
+    } else if (!skip && warp >= 2) {
+        // ------------------------------------------------ epilogue
+        const int q = warp & 3;                 // TMEM lane quadrant this warp may read
+        const int row = m0 + q * 32 + lane;
+        const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
+        if (KIND != kFp8Block) {
+            if (!warp_wait_or_abort(accf, 0, abort_flag)) {
+                if (lane == 0) record_timeout(p.status, abort_flag);
+            } else {
+                tc_fence_after();
+                float alpha = 1.0f;
+                if (KIND == kFp8Tensor) alpha = __fmul_rn(__ldg(p.x_scale), __ldg(p.w_scale));
+                if (KIND == kNvfp4) alpha = __fmul_rn(__ldg(p.x_global), __ldg(p.w_global));
+#pragma unroll 1
+                for (int c = 0; c < C::BN / 32; c++) {
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(tmem + lane_addr + (uint32_t)(c * 32), r);
+                    tmem_ld_wait();
+                    const int n = n0 + c * 32;
+                    if (row < p.M && n < p.N) {
+                        float v[32];
+#pragma unroll
+                        for (int i = 0; i < 32; i++) v[i] = __uint_as_float(r[i]) * alpha;
+                        store_row32(p, row, n, v);
+                    }
+                }
+            }
+        } else {
+            const int h = (warp - 2) >> 2;      // which 128-column half of the tile
+            const int kblocks = p.K >> 7;
+            const int nt = (n0 >> 7) + h;
+            const bool col_ok = nt * 128 < p.N;
+            float acc[128];
+#pragma unroll
+            for (int i = 0; i < 128; i++) acc[i] = 0.0f;
+            bool ok = true;
+            for (int kb = 0; kb < p.nk; kb++) {
+                const int b = kb & 1;
+                if (!warp_wait_or_abort(pfull + b, (uint32_t)(kb >> 1) & 1u, abort_flag)) {
+                    if (lane == 0) record_timeout(p.status, abort_flag);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const float sw = col_ok ? __ldg(p.w_scale + (int64_t)nt * kblocks + kb) : 0.0f;
+#pragma unroll
+                for (int c = 0; c < 4; c++) {
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(tmem + lane_addr + (uint32_t)(b * C::BN + h * 128 + c * 32), r);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 32; i++) acc[c * 32 + i] = fmaf(sw, __uint_as_float(r[i]), acc[c * 32 + i]);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(pempty + b);
+            }
+            if (ok && row < p.M && col_ok) {
+                const float sx = __ldg(p.x_scale + row);
+#pragma unroll
+                for (int c = 0; c < 4; c++) {
+                    float v[32];
+#pragma unroll
+                    for (int i = 0; i < 32; i++) v[i] = acc[c * 32 + i] * sx;
+                    store_row32(p, row, n0 + h * 128 + c * 32, v);
+                }
+            }
+        }
+    }
+
+    // ---------------------------------------------------- teardown
+    tc_fence_before();
+    __syncthreads();
+    if (*abort_flag && warp == 0 && lane == 0) {
+        // Let every TMA copy this CTA issued land before its shared memory is
+        // released: wait (bounded) on the stages issued but not consumed.
+        const int issued = (int)misc[3], consumed = (int)misc[2];
+        for (int kb = consumed; kb < issued; kb++) {
+            uint64_t* bar = full + (kb % C::STAGES);
+            mbar_wait(bar, (uint32_t)(kb / C::STAGES) & 1u, kWaitLimitNs);
+        }
+    }
+    if (*abort_flag && warp == 1 && lane == 0) {
+        // ... and every MMA / scale copy it issued has finished reading
+        // shared memory (a commit with nothing outstanding arrives at once).
+        tc_commit(drain);
+        mbar_wait(drain, 0, kWaitLimitNs);
+    }
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
+// ---------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+// Byte matrix [rows, inner_bytes] with row pitch `pitch` bytes, 128-byte
+// swizzled box of box_rows x 128 bytes, zero fill outside the matrix.
+bool make_tmap_u8(CUtensorMap* m, const void* base, uint64_t inner_bytes, uint64_t rows, uint64_t pitch,
+                  uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {inner_bytes, rows};
+    cuuint64_t strides[1] = {pitch};
+    cuuint32_t box[2] = {(cuuint32_t)BKB, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int KIND>
+cudaError_t launch_tc(const GemmArgs& a, cudaStream_t st) {
+    using C = Cfg<KIND>;
+    const uint64_t kbytes = (KIND == kNvfp4) ? (uint64_t)a.K / 2 : (uint64_t)a.K;
+    CUtensorMap tmA, tmB;
+    if (!make_tmap_u8(&tmA, a.x, kbytes, (uint64_t)a.M, kbytes, BM)) return cudaErrorInvalidValue;
+    if (!make_tmap_u8(&tmB, a.w, kbytes, (uint64_t)a.N, kbytes, C::BN)) return cudaErrorInvalidValue;
+    TcParams p{};
+    p.M = (int)a.M;
+    p.N = (int)a.N;
+    p.K = (int)a.K;
+    p.nk = (int)((kbytes + BKB - 1) / BKB);
+    p.ldy = a.ldy;
+    p.x_scale = static_cast<const float*>(a.x_scales);
+    p.w_scale = static_cast<const float*>(a.w_scales);
+    p.x_global = a.x_global;
+    p.w_global = a.w_global;
+    p.sfa = static_cast<const uint8_t*>(a.x_scales);
+    p.sfb = static_cast<const uint8_t*>(a.w_scales);
+    p.sf_chunks_per_row = (KIND == kMxfp8) ? a.K / 128 : a.K / 64;
+    p.bias = a.bias;
+    p.y = a.y;
+    p.status = a.dev_status;
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(k_gemm_tc<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    dim3 grid((unsigned)((a.N + C::BN - 1) / C::BN), (unsigned)((a.M + BM - 1) / BM));
+    k_gemm_tc<KIND><<<grid, C::THREADS, C::SMEM, st>>>(tmA, tmB, p);
+    return cudaGetLastError();
+}
+
+__global__ void k_expire_wait(int* status, uint32_t max_polls) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        bool done = false;
+        for (uint32_t i = 0; i < max_polls && !done; i++) done = mbar_try_wait(&bar, 0);
+        if (!done) atomicExch(status, (int)QLIN_ERR_DEVICE_TIMEOUT);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_fp8_tensor(const GemmArgs& a, cudaStream_t st) { return launch_tc<kFp8Tensor>(a, st); }
+cudaError_t launch_gemm_fp8_block(const GemmArgs& a, cudaStream_t st) { return launch_tc<kFp8Block>(a, st); }
+cudaError_t launch_gemm_mxfp8(const GemmArgs& a, cudaStream_t st) { return launch_tc<kMxfp8>(a, st); }
+cudaError_t launch_gemm_nvfp4(const GemmArgs& a, cudaStream_t st) { return launch_tc<kNvfp4>(a, st); }
+
+cudaError_t launch_debug_expire_wait(int* dev_status, uint32_t max_polls, cudaStream_t st) {
+    k_expire_wait<<<1, 32, 0, st>>>(dev_status, max_polls);
+    return cudaGetLastError();
+}
+
+}  // namespace qlin

@@ -1,0 +1,452 @@
+// Online quantizers: bf16 -> FP8 E4M3 (tensor / token / 128x128 block),
+// MXFP8, NVFP4 and int4 g128.  Each reads its bf16 input once from HBM in
+// 16-byte vectors, reduces amax (or min/max) with warp shuffles, and writes
+// codes and scales in the same pass.  The per-tensor formats need the tensor
+// amax before any code exists, so they add one read-only amax pass.
+//
+// Formats: "[vLLM] 기타 양자화: FP8, ModelOpt, INC, TorchAO, Quark" section
+// "FP8: vLLM의 핵심 양자화" (tensor/token/block-128 dynamic scales);
+// "vLLM-Omni 在线量化（Online Quantization）完全指南" section
+// "在线量化的底层工作原理" stage 2 (E4M3 + float8_e8m0fnu per 32 along K);
+// "vLLM-Omni 量化推理实践" Table 1 (NVFP4 in the mixed FP8/NVFP4 model);
+// "vLLM-Omni는 AutoRound 양자화로 추론을 가속화합니다" section "새로운 모델
+// 양자화" (int4, group_size 128, auto_round:auto_gptq packing, --iters 0).
+//
+// Bit-exactness: every fp32 step is one explicitly rounded intrinsic
+// (__fmul_rn, __fdiv_rn, __fsub_rn), this file is compiled with
+// -fmad=false -ftz=false -prec-div=true, and the E4M3/E2M1 conversions are
+// the hardware cvt.rn.satfinite instructions.
+#include <cuda_bf16.h>
+
+#include "qlin_internal.h"
+
+namespace qlin {
+namespace {
+
+constexpr float kE4M3Max = 448.0f;
+constexpr float kNvfp4Global = 2688.0f;   // 448 (E4M3 max) * 6 (E2M1 max)
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__device__ __forceinline__ uint4 ld16(const void* p) { return __ldg(reinterpret_cast<const uint4*>(p)); }
+
+__device__ __forceinline__ float absmax8(const uint4& v) {
+    float a = fmaxf(fabsf(bf16_lo(v.x)), fabsf(bf16_hi(v.x)));
+    a = fmaxf(a, fmaxf(fabsf(bf16_lo(v.y)), fabsf(bf16_hi(v.y))));
+    a = fmaxf(a, fmaxf(fabsf(bf16_lo(v.z)), fabsf(bf16_hi(v.z))));
+    a = fmaxf(a, fmaxf(fabsf(bf16_lo(v.w)), fabsf(bf16_hi(v.w))));
+    return a;
+}
+
+// Two fp32 -> two E4M3 codes, round to nearest even, saturating; `lo` lands
+// in bits 0..7.
+__device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Two fp32 -> two E2M1 codes in one byte, `lo` in the low nibble.
+__device__ __forceinline__ uint32_t cvt_e2m1x2(float lo, float hi) {
+    uint32_t r;
+    asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u32.u8 %0, t;\n}"
+        : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// One E4M3 code -> its value (exact: every E4M3 value is an fp16 value).
+__device__ __forceinline__ float e4m3_value(uint32_t code) {
+    uint32_t h2;
+    uint16_t in = (uint16_t)(code & 0xFFu);
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(in));
+    float f;
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tcvt.f32.f16 %0, lo;\n}" : "=f"(f) : "r"(h2));
+    return f;
+}
+
+// 8 bf16 (one 16-byte vector) times r -> 8 E4M3 codes.
+__device__ __forceinline__ uint2 enc8_e4m3(const uint4& v, float r) {
+    uint32_t c0 = cvt_e4m3x2(__fmul_rn(bf16_lo(v.x), r), __fmul_rn(bf16_hi(v.x), r));
+    uint32_t c1 = cvt_e4m3x2(__fmul_rn(bf16_lo(v.y), r), __fmul_rn(bf16_hi(v.y), r));
+    uint32_t c2 = cvt_e4m3x2(__fmul_rn(bf16_lo(v.z), r), __fmul_rn(bf16_hi(v.z), r));
+    uint32_t c3 = cvt_e4m3x2(__fmul_rn(bf16_lo(v.w), r), __fmul_rn(bf16_hi(v.w), r));
+    return make_uint2(c0 | (c1 << 16), c2 | (c3 << 16));
+}
+
+// 8 bf16 times r -> 8 E2M1 codes packed in 4 bytes.
+__device__ __forceinline__ uint32_t enc8_e2m1(const uint4& v, float r) {
+    uint32_t b0 = cvt_e2m1x2(__fmul_rn(bf16_lo(v.x), r), __fmul_rn(bf16_hi(v.x), r));
+    uint32_t b1 = cvt_e2m1x2(__fmul_rn(bf16_lo(v.y), r), __fmul_rn(bf16_hi(v.y), r));
+    uint32_t b2 = cvt_e2m1x2(__fmul_rn(bf16_lo(v.z), r), __fmul_rn(bf16_hi(v.z), r));
+    uint32_t b3 = cvt_e2m1x2(__fmul_rn(bf16_lo(v.w), r), __fmul_rn(bf16_hi(v.w), r));
+    return b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    return v;
+}
+
+// Max over the block; every thread receives the result.
+template <int T>
+__device__ __forceinline__ float block_max(float v, float* red) {
+    v = warp_max(v);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+        float w = lane < T / 32 ? red[lane] : 0.0f;
+        w = warp_max(w);
+        if (lane == 0) red[32] = w;
+    }
+    __syncthreads();
+    return red[32];
+}
+
+// FP8 granule: s = amax/448 and encode multiplier 448/amax (1, 1 for amax 0).
+__device__ __forceinline__ void fp8_params(float amax, float& s, float& r) {
+    if (amax == 0.0f) { s = 1.0f; r = 1.0f; return; }
+    s = __fdiv_rn(amax, kE4M3Max);
+    r = __fdiv_rn(kE4M3Max, amax);
+}
+
+// Byte offset of scale (row, j) in the tensor-core tiling (see qlin.h):
+// 512-byte chunks of 128 rows x 4 scales, ordered [row_tile][chunk].
+__device__ __forceinline__ int64_t mma_scale_offset(int64_t row, int64_t j, int64_t chunks_per_row) {
+    const int64_t tile = row >> 7, rr = row & 127;
+    return ((tile * chunks_per_row + (j >> 2)) << 9) + ((rr & 31) << 4) + ((rr >> 5) << 2) + (j & 3);
+}
+
+// ---------------------------------------------------------------- per row
+// One CTA per row; each thread keeps VPT 16-byte vectors in registers so the
+// row is read from HBM once.
+template <int T, int VPT>
+__global__ void __launch_bounds__(T) k_fp8_rows(const uint16_t* __restrict__ x, int64_t K, int64_t ld,
+                                                uint8_t* __restrict__ codes, float* __restrict__ scales) {
+    __shared__ float red[33];
+    const int64_t row = blockIdx.x;
+    const uint16_t* src = x + row * ld;
+    const int nv = (int)(K >> 3);
+    uint4 v[VPT];
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < VPT; i++) {
+        const int j = threadIdx.x + i * T;
+        if (j < nv) {
+            v[i] = ld16(src + 8 * j);
+            amax = fmaxf(amax, absmax8(v[i]));
+        }
+    }
+    amax = block_max<T>(amax, red);
+    float s, r;
+    fp8_params(amax, s, r);
+    uint2* dst = reinterpret_cast<uint2*>(codes + row * K);
+#pragma unroll
+    for (int i = 0; i < VPT; i++) {
+        const int j = threadIdx.x + i * T;
+        if (j < nv) dst[j] = enc8_e4m3(v[i], r);
+    }
+    if (threadIdx.x == 0) scales[row] = s;
+}
+
+// Rows too long for registers: amax pass then encode pass (second read hits L2).
+__global__ void __launch_bounds__(256) k_fp8_rows_long(const uint16_t* __restrict__ x, int64_t K, int64_t ld,
+                                                       uint8_t* __restrict__ codes, float* __restrict__ scales) {
+    __shared__ float red[33];
+    const int64_t row = blockIdx.x;
+    const uint16_t* src = x + row * ld;
+    const int64_t nv = K >> 3;
+    float amax = 0.0f;
+    for (int64_t j = threadIdx.x; j < nv; j += 256) amax = fmaxf(amax, absmax8(ld16(src + 8 * j)));
+    amax = block_max<256>(amax, red);
+    float s, r;
+    fp8_params(amax, s, r);
+    uint2* dst = reinterpret_cast<uint2*>(codes + row * K);
+    for (int64_t j = threadIdx.x; j < nv; j += 256) dst[j] = enc8_e4m3(ld16(src + 8 * j), r);
+    if (threadIdx.x == 0) scales[row] = s;
+}
+
+// ---------------------------------------------------------------- per tensor
+// Pass 1: partial amax per CTA into partials[blockIdx.x].
+__global__ void __launch_bounds__(256) k_amax_partial(const uint16_t* __restrict__ x, int64_t rows, int64_t K,
+                                                      int64_t ld, float* __restrict__ partials) {
+    __shared__ float red[33];
+    const int64_t nvr = K >> 3, total = rows * nvr;
+    float amax = 0.0f;
+    for (int64_t v = blockIdx.x * 256ll + threadIdx.x; v < total; v += (int64_t)gridDim.x * 256) {
+        const int64_t row = v / nvr, c = v - row * nvr;
+        amax = fmaxf(amax, absmax8(ld16(x + row * ld + 8 * c)));
+    }
+    amax = block_max<256>(amax, red);
+    if (threadIdx.x == 0) partials[blockIdx.x] = amax;
+}
+
+__device__ __forceinline__ float reduce_partials(const float* __restrict__ partials, int nparts, float* red) {
+    float a = 0.0f;
+    for (int i = threadIdx.x; i < nparts; i += 256) a = fmaxf(a, partials[i]);
+    return block_max<256>(a, red);
+}
+
+// Pass 2: every CTA folds the partials (a few KB from L2), then encodes.
+__global__ void __launch_bounds__(256) k_fp8_tensor_encode(const uint16_t* __restrict__ x, int64_t rows, int64_t K,
+                                                           int64_t ld, uint8_t* __restrict__ codes,
+                                                           float* __restrict__ scale,
+                                                           const float* __restrict__ partials, int nparts) {
+    __shared__ float red[33];
+    const float amax = reduce_partials(partials, nparts, red);
+    float s, r;
+    fp8_params(amax, s, r);
+    if (blockIdx.x == 0 && threadIdx.x == 0) *scale = s;
+    const int64_t nvr = K >> 3, total = rows * nvr;
+    for (int64_t v = blockIdx.x * 256ll + threadIdx.x; v < total; v += (int64_t)gridDim.x * 256) {
+        const int64_t row = v / nvr, c = v - row * nvr;
+        reinterpret_cast<uint2*>(codes + row * K)[c] = enc8_e4m3(ld16(x + row * ld + 8 * c), r);
+    }
+}
+
+// ---------------------------------------------------------------- 128x128 block
+// One CTA per 128x128 tile: 256 threads x 8 vectors; thread t covers rows
+// t/16 + 16i and the 16-byte column t%16 (256-byte coalesced row segments).
+__global__ void __launch_bounds__(256) k_fp8_block128(const uint16_t* __restrict__ x, int64_t K, int64_t ld,
+                                                      uint8_t* __restrict__ codes, float* __restrict__ scales) {
+    __shared__ float red[33];
+    const int64_t bi = blockIdx.y, bj = blockIdx.x;
+    const int r0 = threadIdx.x >> 4, cv = threadIdx.x & 15;
+    const uint16_t* src = x + (bi * 128 + r0) * ld + bj * 128 + cv * 8;
+    uint4 v[8];
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+        v[i] = ld16(src + (int64_t)(16 * i) * ld);
+        amax = fmaxf(amax, absmax8(v[i]));
+    }
+    amax = block_max<256>(amax, red);
+    float s, r;
+    fp8_params(amax, s, r);
+    uint8_t* dst = codes + (bi * 128 + r0) * K + bj * 128 + cv * 8;
+#pragma unroll
+    for (int i = 0; i < 8; i++) *reinterpret_cast<uint2*>(dst + (int64_t)(16 * i) * K) = enc8_e4m3(v[i], r);
+    if (threadIdx.x == 0) scales[bi * (K >> 7) + bj] = s;
+}
+
+// ---------------------------------------------------------------- MXFP8
+// Four consecutive lanes own one 32-element granule (8 elements each).  Rows
+// from `rows` up to `rows_pad` exist only in the MMA scale layout: they get
+// scale code 0 and no codes.
+__global__ void __launch_bounds__(256) k_mxfp8(const uint16_t* __restrict__ x, int64_t rows, int64_t rows_pad,
+                                               int64_t K, int64_t ld, uint8_t* __restrict__ codes,
+                                               uint8_t* __restrict__ scales, int mma) {
+    const int64_t nvr = K >> 3, total = rows_pad * nvr;
+    const int64_t chunks = K >> 7;
+    const int lane = threadIdx.x & 31;
+    // Warp-uniform trip count (the shuffles below use the full mask); total is
+    // a multiple of 4, so a granule's four lanes are all in or all out.
+    for (int64_t vb = blockIdx.x * 256ll + (threadIdx.x & ~31); vb < total; vb += (int64_t)gridDim.x * 256) {
+        const int64_t v = vb + lane;
+        const bool in = v < total;
+        const int64_t row = in ? v / nvr : rows_pad, c = in ? v - row * nvr : 0;
+        const bool valid = row < rows;
+        uint4 w = make_uint4(0, 0, 0, 0);
+        if (valid) w = ld16(x + row * ld + 8 * c);
+        float a = absmax8(w);
+        a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
+        a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 2));
+        // e = clamp(floor(log2 a) - 8, -127, 127); subnormal a lands below -127.
+        const int biased = (int)(__float_as_uint(a) >> 23);
+        int e = (a == 0.0f || biased == 0) ? -127 : max(biased - 127 - 8, -127);
+        e = min(e, 127);
+        const float mult = __uint_as_float((uint32_t)(127 - e) << 23);   // 2^-e, e <= 126 here
+        if (valid) reinterpret_cast<uint2*>(codes + row * K)[c] = enc8_e4m3(w, mult);
+        if (in && (c & 3) == 0) {
+            const int64_t j = c >> 2;
+            const int64_t off = mma ? mma_scale_offset(row, j, chunks) : row * (K >> 5) + j;
+            scales[off] = (uint8_t)(e + 127);
+        }
+    }
+}
+
+// ---------------------------------------------------------------- NVFP4
+// After the amax pass: two consecutive lanes own one 16-element block.
+__global__ void __launch_bounds__(256) k_nvfp4_encode(const uint16_t* __restrict__ x, int64_t rows,
+                                                      int64_t rows_pad, int64_t K, int64_t ld,
+                                                      uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
+                                                      float* __restrict__ global,
+                                                      const float* __restrict__ partials, int nparts, int mma) {
+    __shared__ float red[33];
+    const float A = reduce_partials(partials, nparts, red);
+    float g = 1.0f, q = 1.0f, rg = 1.0f;
+    if (A != 0.0f) {
+        g = __fdiv_rn(A, kNvfp4Global);
+        q = __fdiv_rn(kE4M3Max, A);
+        rg = __fdiv_rn(kNvfp4Global, A);
+    }
+    if (blockIdx.x == 0 && threadIdx.x == 0) *global = g;
+    const int64_t nvr = K >> 3, total = rows_pad * nvr;
+    const int64_t chunks = K >> 6;
+    const int lane = threadIdx.x & 31;
+    for (int64_t vb = blockIdx.x * 256ll + (threadIdx.x & ~31); vb < total; vb += (int64_t)gridDim.x * 256) {
+        const int64_t v = vb + lane;
+        const bool in = v < total;
+        const int64_t row = in ? v / nvr : rows_pad, c = in ? v - row * nvr : 0;
+        const bool valid = row < rows;
+        uint4 w = make_uint4(0, 0, 0, 0);
+        if (valid) w = ld16(x + row * ld + 8 * c);
+        float b = absmax8(w);
+        b = fmaxf(b, __shfl_xor_sync(0xFFFFFFFFu, b, 1));
+        const uint32_t sb = cvt_e4m3x2(__fmul_rn(b, q), 0.0f) & 0xFFu;   // non-negative: UE4M3
+        const float dsb = e4m3_value(sb);
+        const float rb = (dsb == 0.0f) ? 0.0f : __fdiv_rn(rg, dsb);
+        if (valid) reinterpret_cast<uint32_t*>(codes + row * (K >> 1))[c] = enc8_e2m1(w, rb);
+        if (in && (c & 1) == 0) {
+            const int64_t j = c >> 1;
+            const int64_t off = mma ? mma_scale_offset(row, j, chunks) : row * (K >> 4) + j;
+            scales[off] = (uint8_t)sb;
+        }
+    }
+}
+
+// ---------------------------------------------------------------- int4 g128
+// CTA = 64 output channels x one group of 128 k.  Thread t handles rows
+// t/16 + 16i and k-octet t%16; the row's 16 lanes reduce min/max by shuffles.
+// Packed words are transposed through shared memory so that qweight rows
+// (fixed k-octet, consecutive n) are written coalesced.
+__global__ void __launch_bounds__(256) k_int4_g128(const uint16_t* __restrict__ w, int64_t N, int64_t K,
+                                                   int64_t ld, int32_t* __restrict__ qweight,
+                                                   uint16_t* __restrict__ scales, int32_t* __restrict__ qzeros) {
+    __shared__ uint32_t words[16][65];
+    __shared__ uint32_t zs[64];
+    const int64_t n0 = (int64_t)blockIdx.x * 64, g = blockIdx.y, k0 = g * 128;
+    const int rl = threadIdx.x >> 4, oc = threadIdx.x & 15;
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        const int nl = rl + 16 * i;
+        const int64_t n = n0 + nl;
+        const bool valid = n < N;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (valid) v = ld16(w + n * ld + k0 + oc * 8);
+        float e[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
+                      bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
+        float mn = 0.0f, mx = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 8; j++) { mn = fminf(mn, e[j]); mx = fmaxf(mx, e[j]); }
+#pragma unroll
+        for (int o = 1; o < 16; o <<= 1) {
+            mn = fminf(mn, __shfl_xor_sync(0xFFFFFFFFu, mn, o));
+            mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+        }
+        const __nv_bfloat16 sb = __float2bfloat16_rn(__fdiv_rn(__fsub_rn(mx, mn), 15.0f));
+        float s = __bfloat162float(sb);
+        uint16_t sbits = __bfloat16_as_ushort(sb);
+        if (s == 0.0f) { s = 1.0f; sbits = 0x3F80u; }
+        const float r = __fdiv_rn(1.0f, s);
+        const int z = min(max(__float2int_rn(__fmul_rn(-mn, r)), 0), 15);
+        uint32_t word = 0;
+#pragma unroll
+        for (int j = 0; j < 8; j++) {
+            const int q = min(max(__float2int_rn(__fmul_rn(e[j], r)) + z, 0), 15);
+            word |= (uint32_t)q << (4 * j);
+        }
+        words[oc][nl] = word;
+        if (oc == 0) {
+            zs[nl] = (uint32_t)z;
+            if (valid) scales[g * N + n] = sbits;
+        }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int p = 0; p < 4; p++) {
+        const int idx = threadIdx.x + 256 * p, o = idx >> 6, nl = idx & 63;
+        if (n0 + nl < N) qweight[(k0 / 8 + o) * N + n0 + nl] = (int32_t)words[o][nl];
+    }
+    if (threadIdx.x < 8 && n0 + 8 * threadIdx.x < N) {
+        uint32_t zw = 0;
+#pragma unroll
+        for (int j = 0; j < 8; j++) zw |= zs[8 * threadIdx.x + j] << (4 * j);
+        qzeros[g * (N / 8) + n0 / 8 + threadIdx.x] = (int32_t)zw;
+    }
+}
+
+int grid_for(int64_t work, int per_block) {
+    int64_t b = (work + per_block - 1) / per_block;
+    if (b > (int64_t)kNumSMs * 8) b = (int64_t)kNumSMs * 8;
+    return (int)(b < 1 ? 1 : b);
+}
+
+template <int T>
+cudaError_t rows_dispatch(int vpt, const uint16_t* x, int64_t rows, int64_t K, int64_t ld, uint8_t* codes,
+                          float* scales, cudaStream_t st) {
+    dim3 grid((unsigned)rows);
+    switch (vpt) {
+        case 1: k_fp8_rows<T, 1><<<grid, T, 0, st>>>(x, K, ld, codes, scales); break;
+        case 2: k_fp8_rows<T, 2><<<grid, T, 0, st>>>(x, K, ld, codes, scales); break;
+        case 3: k_fp8_rows<T, 3><<<grid, T, 0, st>>>(x, K, ld, codes, scales); break;
+        case 4: k_fp8_rows<T, 4><<<grid, T, 0, st>>>(x, K, ld, codes, scales); break;
+        case 5: k_fp8_rows<T, 5><<<grid, T, 0, st>>>(x, K, ld, codes, scales); break;
+        case 6: k_fp8_rows<T, 6><<<grid, T, 0, st>>>(x, K, ld, codes, scales); break;
+        case 7: k_fp8_rows<T, 7><<<grid, T, 0, st>>>(x, K, ld, codes, scales); break;
+        default: k_fp8_rows<T, 8><<<grid, T, 0, st>>>(x, K, ld, codes, scales); break;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int amax_partials(int64_t rows, int64_t K) {
+    const int64_t nv = rows * (K >> 3);
+    int64_t p = (nv + 1023) / 1024;
+    if (p > 1024) p = 1024;
+    return (int)(p < 1 ? 1 : p);
+}
+
+cudaError_t launch_fp8_rowwise(const uint16_t* x, int64_t rows, int64_t K, int64_t ld, uint8_t* codes,
+                               float* scales, cudaStream_t st) {
+    const int64_t nv = K >> 3;
+    if (nv <= 128 * 8) return rows_dispatch<128>((int)((nv + 127) / 128), x, rows, K, ld, codes, scales, st);
+    if (nv <= 256 * 8) return rows_dispatch<256>((int)((nv + 255) / 256), x, rows, K, ld, codes, scales, st);
+    k_fp8_rows_long<<<(unsigned)rows, 256, 0, st>>>(x, K, ld, codes, scales);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_fp8_tensor(const uint16_t* x, int64_t rows, int64_t K, int64_t ld, uint8_t* codes,
+                              float* scale, float* partials, int nparts, cudaStream_t st) {
+    k_amax_partial<<<nparts, 256, 0, st>>>(x, rows, K, ld, partials);
+    k_fp8_tensor_encode<<<grid_for(rows * (K >> 3), 256 * 4), 256, 0, st>>>(x, rows, K, ld, codes, scale,
+                                                                             partials, nparts);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_fp8_block128(const uint16_t* x, int64_t rows, int64_t K, int64_t ld, uint8_t* codes,
+                                float* scales, cudaStream_t st) {
+    dim3 grid((unsigned)(K / 128), (unsigned)(rows / 128));
+    k_fp8_block128<<<grid, 256, 0, st>>>(x, K, ld, codes, scales);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_mxfp8(const uint16_t* x, int64_t rows, int64_t K, int64_t ld, uint8_t* codes,
+                         uint8_t* scales, bool mma_layout, cudaStream_t st) {
+    const int64_t rows_pad = mma_layout ? (rows + 127) / 128 * 128 : rows;
+    k_mxfp8<<<grid_for(rows_pad * (K >> 3), 256 * 4), 256, 0, st>>>(x, rows, rows_pad, K, ld, codes, scales,
+                                                                      mma_layout ? 1 : 0);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_nvfp4(const uint16_t* x, int64_t rows, int64_t K, int64_t ld, uint8_t* codes,
+                         uint8_t* scales, float* global, bool mma_layout, float* partials, int nparts,
+                         cudaStream_t st) {
+    const int64_t rows_pad = mma_layout ? (rows + 127) / 128 * 128 : rows;
+    k_amax_partial<<<nparts, 256, 0, st>>>(x, rows, K, ld, partials);
+    k_nvfp4_encode<<<grid_for(rows_pad * (K >> 3), 256 * 4), 256, 0, st>>>(
+        x, rows, rows_pad, K, ld, codes, scales, global, partials, nparts, mma_layout ? 1 : 0);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_int4_g128(const uint16_t* w, int64_t N, int64_t K, int64_t ld, int32_t* qweight,
+                             uint16_t* scales, int32_t* qzeros, cudaStream_t st) {
+    dim3 grid((unsigned)((N + 63) / 64), (unsigned)(K / 128));
+    k_int4_g128<<<grid, 256, 0, st>>>(w, N, K, ld, qweight, scales, qzeros);
+    return cudaGetLastError();
+}
+
+}  // namespace qlin

@@ -1,0 +1,139 @@
+"""Host-side checks of the C-ABI library: it builds for sm_103a, loads without
+a GPU, exports every entry point include/qlin.h declares, answers size
+queries, and rejects bad arguments before any launch."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def q():
+    from serving_amax_reduce_gb300 import build
+    build.build()
+    from serving_amax_reduce_gb300 import qlin
+    return qlin
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "qlin.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(qlin_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(q):
+    names = declared_functions()
+    assert len(names) >= 11
+    lib = ctypes.CDLL(q.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_version_and_status_strings(q):
+    assert "sm_103a" in q.qlin_version()
+    for s in q.Status:
+        assert q.qlin_status_string(s)
+
+
+def test_size_queries(q):
+    F, L = q.Fmt, q.Layout
+    assert q.qlin_codes_bytes(F.FP8_TOKEN, 20280, 5120) == 20280 * 5120
+    assert q.qlin_codes_bytes(F.NVFP4, 32768, 3072) == 32768 * 1536
+    assert q.qlin_codes_bytes(F.INT4_G128_ASYM, 4096, 12288) == 12288 // 8 * 4096 * 4
+    assert q.qlin_scales_bytes(F.FP8_TENSOR, L.CANONICAL, 128, 1024) == 4
+    assert q.qlin_scales_bytes(F.FP8_BLOCK128, L.CANONICAL, 12288, 3072) == 96 * 24 * 4
+    assert q.qlin_scales_bytes(F.MXFP8, L.CANONICAL, 20280, 5120) == 20280 * 160
+    assert q.qlin_scales_bytes(F.MXFP8, L.MMA, 20280, 5120) == 20352 * 160
+    assert q.qlin_scales_bytes(F.NVFP4, L.MMA, 200, 3072) == 256 * 192
+    assert q.qlin_scales_bytes(F.INT4_G128_ASYM, L.CANONICAL, 4096, 12288) == 96 * 4096 * 2
+    assert q.qlin_zeros_bytes(F.INT4_G128_ASYM, 4096, 12288) == 96 * 512 * 4
+    assert q.qlin_zeros_bytes(F.FP8_TOKEN, 4096, 12288) == 0
+    assert q.qlin_quant_workspace_bytes(F.FP8_TENSOR, 128, 1024) > 0
+    assert q.qlin_quant_workspace_bytes(F.FP8_TOKEN, 128, 1024) == 0
+
+
+FAKE = 1 << 20          # a 16-byte aligned non-null value; never dereferenced by these calls
+
+
+def test_quantize_rejects_bad_arguments(q):
+    F, L, S = q.Fmt, q.Layout, q.Status
+    ws = q.qlin_quant_workspace_bytes(F.FP8_TENSOR, 128, 1024)
+    # null source / outputs
+    assert q.qlin_quantize_act(F.FP8_TOKEN, None, 128, 1024, 1024, FAKE, FAKE, None, L.CANONICAL, None, 0, None,
+                               None) == S.INVALID_ARG
+    assert q.qlin_quantize_act(F.FP8_TOKEN, FAKE, 128, 1024, 1024, None, FAKE, None, L.CANONICAL, None, 0, None,
+                               None) == S.INVALID_ARG
+    # K not a multiple of 8, ld < K, empty
+    assert q.qlin_quantize_act(F.FP8_TOKEN, FAKE, 128, 1020, 1024, FAKE, FAKE, None, L.CANONICAL, None, 0, None,
+                               None) == S.INVALID_ARG
+    assert q.qlin_quantize_act(F.FP8_TOKEN, FAKE, 128, 1024, 512, FAKE, FAKE, None, L.CANONICAL, None, 0, None,
+                               None) == S.INVALID_ARG
+    assert q.qlin_quantize_act(F.FP8_TOKEN, FAKE, 0, 1024, 1024, FAKE, FAKE, None, L.CANONICAL, None, 0, None,
+                               None) == S.INVALID_ARG
+    # misaligned source
+    assert q.qlin_quantize_act(F.FP8_TOKEN, FAKE + 2, 128, 1024, 1024, FAKE, FAKE, None, L.CANONICAL, None, 0,
+                               None, None) == S.ALIGNMENT
+    # per-tensor without workspace
+    assert q.qlin_quantize_act(F.FP8_TENSOR, FAKE, 128, 1024, 1024, FAKE, FAKE, None, L.CANONICAL, None, 0, None,
+                               None) == S.WORKSPACE
+    assert q.qlin_quantize_act(F.FP8_TENSOR, FAKE, 128, 1024, 1024, FAKE, FAKE, None, L.CANONICAL, FAKE, ws - 4,
+                               None, None) == S.WORKSPACE
+    # block-128 shape rules
+    assert q.qlin_quantize_weight(F.FP8_BLOCK128, FAKE, 200, 1024, 1024, FAKE, FAKE, None, None, L.CANONICAL,
+                                  None, 0, None, None) == S.INVALID_ARG
+    # MMA layout only for MX / NVFP4; MX MMA layout needs K % 128
+    assert q.qlin_quantize_act(F.FP8_TOKEN, FAKE, 128, 1024, 1024, FAKE, FAKE, None, L.MMA, None, 0, None,
+                               None) == S.UNSUPPORTED
+    assert q.qlin_quantize_act(F.MXFP8, FAKE, 128, 96, 96, FAKE, FAKE, None, L.MMA, None, 0, None,
+                               None) == S.INVALID_ARG
+    # NVFP4 needs the global-scale output
+    assert q.qlin_quantize_act(F.NVFP4, FAKE, 128, 1024, 1024, FAKE, FAKE, None, L.CANONICAL, FAKE, 1 << 20,
+                               None, None) == S.INVALID_ARG
+    # int4 is weight-only, and needs zeros
+    assert q.qlin_quantize_act(F.INT4_G128_ASYM, FAKE, 128, 1024, 1024, FAKE, FAKE, None, L.CANONICAL, None, 0,
+                               None, None) == S.UNSUPPORTED
+    assert q.qlin_quantize_weight(F.INT4_G128_ASYM, FAKE, 128, 1024, 1024, FAKE, FAKE, None, None, L.CANONICAL,
+                                  None, 0, None, None) == S.INVALID_ARG
+    assert q.qlin_quantize_weight(F.BF16, FAKE, 128, 1024, 1024, FAKE, FAKE, None, None, L.CANONICAL, None, 0,
+                                  None, None) == S.UNSUPPORTED
+
+
+def test_gemm_rejects_bad_arguments(q):
+    F, L, S = q.Fmt, q.Layout, q.Status
+
+    def g(wf, xf, M, N, K, layout=L.CANONICAL, x=FAKE, y=FAKE, ldy=None, xs=FAKE, ws=FAKE, xg=FAKE, wg=FAKE,
+          wz=FAKE, work=None, work_bytes=0):
+        return q.qlin_gemm(wf, xf, M, N, K, x, xs, xg, FAKE, ws, wz, wg, None, y, N if ldy is None else ldy, layout,
+                           work, work_bytes, None, None)
+
+    assert g(F.FP8_TENSOR, F.FP8_TENSOR, 0, 1024, 1024) == S.INVALID_ARG
+    assert g(F.FP8_TENSOR, F.FP8_TENSOR, 128, 1024, 1024, x=None) == S.INVALID_ARG
+    assert g(F.FP8_TENSOR, F.FP8_TENSOR, 128, 1024, 1024, y=FAKE + 8) == S.ALIGNMENT
+    assert g(F.FP8_TENSOR, F.FP8_TENSOR, 128, 1024, 1024, ldy=1000) == S.INVALID_ARG
+    assert g(F.FP8_TENSOR, F.FP8_TENSOR, 128, 1024, 1024, xs=None) == S.INVALID_ARG
+    assert g(F.FP8_BLOCK128, F.FP8_TOKEN, 128, 1000, 1024) == S.INVALID_ARG
+    assert g(F.MXFP8, F.MXFP8, 128, 1024, 1024) == S.UNSUPPORTED          # canonical scales
+    assert g(F.MXFP8, F.MXFP8, 128, 1024, 1056, layout=L.MMA) == S.INVALID_ARG
+    assert g(F.NVFP4, F.NVFP4, 128, 1024, 1024, layout=L.MMA, xg=None) == S.INVALID_ARG
+    assert g(F.NVFP4, F.FP8_TOKEN, 128, 1024, 1024, layout=L.MMA) == S.UNSUPPORTED
+    assert g(F.FP8_TENSOR, F.FP8_TOKEN, 128, 1024, 1024) == S.UNSUPPORTED
+    assert g(F.INT4_G128_ASYM, F.BF16, 16, 4096, 4000) == S.INVALID_ARG
+    need = q.qlin_gemm_workspace_bytes(F.INT4_G128_ASYM, F.BF16, 16, 4096, 4096)
+    if need:
+        assert g(F.INT4_G128_ASYM, F.BF16, 16, 4096, 4096, work=None) == S.WORKSPACE
+
+
+def test_mma_layout_reader_matches_the_documented_formula():
+    from layouts import mma_to_canonical
+    rows, nsc = 200, 8
+    buf = np.zeros(2 * 2 * 512, np.uint8)
+    canon = (np.arange(rows * nsc) % 251).astype(np.uint8).reshape(rows, nsc)
+    for r in range(rows):
+        for j in range(nsc):
+            tile, rr, chunk, jj = r // 128, r % 128, j // 4, j % 4
+            buf[(tile * 2 + chunk) * 512 + 16 * (rr % 32) + 4 * (rr // 32) + jj] = canon[r, j]
+    assert np.array_equal(mma_to_canonical(buf, rows, nsc), canon)

@@ -1,0 +1,169 @@
+"""GPU quantized GEMMs against the fp64 oracle on identical quantized inputs.
+
+Pass rule: relative Frobenius error <= 2e-3 + the relative error of rounding
+the oracle's own result to bf16.  Each case also checks that the output is
+not the unquantized bf16 product (the quantized path really ran).
+"""
+import numpy as np
+import pytest
+import torch
+
+from gpu_util import bits, np_f32, np_u8, require_gpu
+from layouts import mma_to_canonical
+from serving_amax_reduce_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def q():
+    return require_gpu()
+
+
+def y_np(y: torch.Tensor) -> np.ndarray:
+    return y.float().cpu().numpy().astype(np.float64)
+
+
+def check(orc, y_gpu, y_ref, x=None, w=None, rows=None):
+    from serving_amax_reduce_gb300 import qlin
+    assert qlin.read_device_status() == 0, "a bounded device wait expired"
+    ok, m = orc.gemm_pass(y_gpu, y_ref)
+    assert ok, m
+    assert np.isfinite(y_gpu).all()
+    if x is not None:
+        xb = x.float() if rows is None else x[rows].float()
+        plain = (xb.double() @ w.double().T).numpy()
+        d = np.linalg.norm(y_gpu - plain) / np.linalg.norm(plain)
+        assert d > 1e-5, "output equals the unquantized product"
+    return m
+
+
+def sample_rows(M, n, seed=0):
+    if M <= n:
+        return np.arange(M)
+    return np.sort(np.random.default_rng(seed).choice(M, n, replace=False))
+
+
+# ------------------------------------------------------------------ FP8 per-tensor
+@pytest.mark.parametrize("M,N,K", [(128, 1024, 1024), (200, 512, 384), (1, 256, 128), (333, 1040, 1040)])
+def test_fp8_tensor_gemm(q, orc, M, N, K):
+    lin = inputs.fp8_tensor_linear(M, K, N)
+    x, w = lin.make_x(), lin.make_w()
+    F = q.Fmt
+    bx = q.quantize_act(F.FP8_TENSOR, x.cuda())
+    bw = q.quantize_weight(F.FP8_TENSOR, w.cuda())
+    y = q.gemm(F.FP8_TENSOR, F.FP8_TENSOR, M, N, K, bx["codes"], bx["scales"], bw["codes"], bw["scales"])
+    torch.cuda.synchronize()
+    xh = orc.dequant_fp8_tensor(np_u8(bx["codes"]).reshape(M, K), np_f32(bx["scales"])[0])
+    wh = orc.dequant_fp8_tensor(np_u8(bw["codes"]).reshape(N, K), np_f32(bw["scales"])[0])
+    check(orc, y_np(y), orc.gemm_ref(xh, wh), x, w)
+
+
+def test_fp8_tensor_gemm_bias(q, orc):
+    M, N, K = 200, 512, 256
+    lin = inputs.fp8_tensor_linear(M, K, N)
+    x, w = lin.make_x(), lin.make_w()
+    bias = inputs.normal_bf16((1, N), 0.05, 99)[0]
+    F = q.Fmt
+    bx = q.quantize_act(F.FP8_TENSOR, x.cuda())
+    bw = q.quantize_weight(F.FP8_TENSOR, w.cuda())
+    y = q.gemm(F.FP8_TENSOR, F.FP8_TENSOR, M, N, K, bx["codes"], bx["scales"], bw["codes"], bw["scales"],
+               bias=bias.cuda())
+    torch.cuda.synchronize()
+    xh = orc.dequant_fp8_tensor(np_u8(bx["codes"]).reshape(M, K), np_f32(bx["scales"])[0])
+    wh = orc.dequant_fp8_tensor(np_u8(bw["codes"]).reshape(N, K), np_f32(bw["scales"])[0])
+    check(orc, y_np(y), orc.gemm_ref(xh, wh, bias=orc.bf16_values(bits(bias)[None, :])[0]))
+
+
+# ------------------------------------------------------------------ FP8 token x block-128
+def fp8_block_case(q, orc, M, N, K, nrows=None):
+    lin = inputs.fp8_block_linear(1, K, N, M=M)
+    x, w = lin.make_x(), lin.make_w()
+    F = q.Fmt
+    bx = q.quantize_act(F.FP8_TOKEN, x.cuda())
+    bw = q.quantize_weight(F.FP8_BLOCK128, w.cuda())
+    y = q.gemm(F.FP8_BLOCK128, F.FP8_TOKEN, M, N, K, bx["codes"], bx["scales"], bw["codes"], bw["scales"])
+    torch.cuda.synchronize()
+    rows = sample_rows(M, nrows or M)
+    xc = np_u8(bx["codes"]).reshape(M, K)[rows]
+    xs = np_f32(bx["scales"])[:M][rows]
+    xh = orc.dequant_fp8_token(xc, xs)
+    wh = orc.dequant_fp8_block128(np_u8(bw["codes"]).reshape(N, K), np_f32(bw["scales"]).reshape(N // 128, K // 128))
+    return check(orc, y_np(y)[rows], orc.gemm_ref(xh, wh), x, w, rows=torch.from_numpy(rows))
+
+
+@pytest.mark.parametrize("M,N,K", [(200, 512, 384), (128, 256, 128), (1, 384, 256), (513, 1280, 1152)])
+def test_fp8_block_gemm(q, orc, M, N, K):
+    fp8_block_case(q, orc, M, N, K)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("B,K,N", [(1, 3072, 12288), (1, 12288, 3072)])
+def test_fp8_block_gemm_full_size(q, orc, B, K, N):
+    fp8_block_case(q, orc, 4096 * B, N, K, nrows=256)
+
+
+# ------------------------------------------------------------------ MXFP8
+def mxfp8_case(q, orc, M, N, K, nrows=None):
+    lin = inputs.mxfp8_linear(K, N, M=M)
+    x, w = lin.make_x(), lin.make_w()
+    F, L = q.Fmt, q.Layout
+    bx = q.quantize_act(F.MXFP8, x.cuda(), L.MMA)
+    bw = q.quantize_weight(F.MXFP8, w.cuda(), L.MMA)
+    y = q.gemm(F.MXFP8, F.MXFP8, M, N, K, bx["codes"], bx["scales"], bw["codes"], bw["scales"], layout=L.MMA)
+    torch.cuda.synchronize()
+    rows = sample_rows(M, nrows or M)
+    xs = mma_to_canonical(np_u8(bx["scales"]), M, K // 32)[rows]
+    xh = orc.dequant_mxfp8(np_u8(bx["codes"]).reshape(M, K)[rows], xs)
+    wh = orc.dequant_mxfp8(np_u8(bw["codes"]).reshape(N, K), mma_to_canonical(np_u8(bw["scales"]), N, K // 32))
+    return check(orc, y_np(y)[rows], orc.gemm_ref(xh, wh), x, w, rows=torch.from_numpy(rows))
+
+
+@pytest.mark.parametrize("M,N,K", [(200, 512, 512), (128, 256, 128), (1, 256, 256), (300, 640, 1152)])
+def test_mxfp8_gemm(q, orc, M, N, K):
+    mxfp8_case(q, orc, M, N, K)
+
+
+@pytest.mark.slow
+def test_mxfp8_gemm_full_size(q, orc):
+    mxfp8_case(q, orc, 20280, 5120, 5120, nrows=256)
+
+
+# ------------------------------------------------------------------ NVFP4
+def nvfp4_case(q, orc, M, N, K, nrows=None):
+    lin = inputs.mixed_stack(M=M, d=K)[0]
+    x = lin.make_x()
+    w = inputs.normal_bf16((N, K), 0.02, lin.w_seed)
+    F, L = q.Fmt, q.Layout
+    bx = q.quantize_act(F.NVFP4, x.cuda(), L.MMA)
+    bw = q.quantize_weight(F.NVFP4, w.cuda(), L.MMA)
+    y = q.gemm(F.NVFP4, F.NVFP4, M, N, K, bx["codes"], bx["scales"], bw["codes"], bw["scales"], layout=L.MMA,
+               x_global=bx["global"], w_global=bw["global"])
+    torch.cuda.synchronize()
+    rows = sample_rows(M, nrows or M)
+    xs = mma_to_canonical(np_u8(bx["scales"]), M, K // 16)[rows]
+    xh = orc.dequant_nvfp4(np_u8(bx["codes"]).reshape(M, K // 2)[rows], xs, np_f32(bx["global"])[0])
+    wh = orc.dequant_nvfp4(np_u8(bw["codes"]).reshape(N, K // 2), mma_to_canonical(np_u8(bw["scales"]), N, K // 16),
+                           np_f32(bw["global"])[0])
+    return check(orc, y_np(y)[rows], orc.gemm_ref(xh, wh), x, w, rows=torch.from_numpy(rows))
+
+
+@pytest.mark.parametrize("M,N,K", [(200, 512, 512), (128, 256, 256), (1, 256, 256), (300, 640, 1280)])
+def test_nvfp4_gemm(q, orc, M, N, K):
+    nvfp4_case(q, orc, M, N, K)
+
+
+@pytest.mark.slow
+def test_nvfp4_gemm_full_size(q, orc):
+    nvfp4_case(q, orc, 32768, 3072, 3072, nrows=256)
+
+
+# ------------------------------------------------------------------ device timeout path
+def test_bounded_wait_expires_with_status(q):
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = q.qlin_debug_expire_wait(st.data_ptr(), 1000, torch.cuda.current_stream().cuda_stream)
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert int(st.item()) == int(q.Status.DEVICE_TIMEOUT)
+    # the context is still usable afterwards
+    assert float(torch.ones(4, device="cuda").sum()) == 4.0

@@ -1,0 +1,142 @@
+"""GPU quantizers against the CPU oracle: codes and scales bit for bit."""
+import numpy as np
+import pytest
+import torch
+
+from gpu_util import bits, edge_bf16, np_f32, np_u8, require_gpu
+from layouts import mma_padding_rows, mma_to_canonical
+from serving_amax_reduce_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def q():
+    return require_gpu()
+
+
+def run(q, fmt, x, layout=None, weight=False):
+    L = q.Layout.CANONICAL if layout is None else layout
+    xd = x.cuda()
+    b = (q.quantize_weight if weight else q.quantize_act)(fmt, xd, L)
+    torch.cuda.synchronize()
+    return b
+
+
+def make(kind, rows, K, seed):
+    if kind == "outlier":
+        return inputs.outlier_channel_bf16(rows, K, seed)
+    if kind == "edge":
+        return edge_bf16(rows, K, seed)
+    return inputs.normal_bf16((rows, K), 0.02, seed)
+
+
+SHAPES_ROW = [(1, 1024), (200, 3072), (64, 12288), (3, 24576), (129, 1040), (37, 8)]
+
+
+@pytest.mark.parametrize("rows,K", SHAPES_ROW)
+@pytest.mark.parametrize("kind", ["outlier", "edge"])
+def test_fp8_token(q, orc, rows, K, kind):
+    x = make(kind, rows, K, rows + K)
+    b = run(q, q.Fmt.FP8_TOKEN, x)
+    codes, scales = orc.quant_fp8_token(bits(x))
+    assert np.array_equal(np_u8(b["codes"]).reshape(rows, K), codes)
+    assert np.array_equal(np_f32(b["scales"])[:rows].view(np.uint32), scales.view(np.uint32))
+
+
+@pytest.mark.parametrize("rows,K", [(128, 1024), (1024, 1024), (333, 520), (4096, 4096), (1, 8)])
+@pytest.mark.parametrize("kind", ["normal", "edge"])
+def test_fp8_tensor(q, orc, rows, K, kind):
+    x = make(kind, rows, K, 7 * rows + K)
+    b = run(q, q.Fmt.FP8_TENSOR, x)
+    codes, s = orc.quant_fp8_tensor(bits(x))
+    assert np.array_equal(np_u8(b["codes"]).reshape(rows, K), codes)
+    assert np_f32(b["scales"])[0].view(np.uint32) == np.float32(s).view(np.uint32)
+
+
+@pytest.mark.parametrize("rows,K", [(128, 128), (256, 384), (1024, 3072), (12288, 3072)])
+@pytest.mark.parametrize("kind", ["normal", "edge"])
+def test_fp8_block128(q, orc, rows, K, kind):
+    x = make(kind, rows, K, 3 * rows + K)
+    b = run(q, q.Fmt.FP8_BLOCK128, x, weight=True)
+    codes, s = orc.quant_fp8_block128(bits(x))
+    assert np.array_equal(np_u8(b["codes"]).reshape(rows, K), codes)
+    assert np.array_equal(np_f32(b["scales"]).reshape(s.shape).view(np.uint32), s.view(np.uint32))
+
+
+@pytest.mark.parametrize("rows,K", [(1, 128), (200, 5120), (128, 13824), (77, 96)])
+@pytest.mark.parametrize("kind", ["normal", "edge"])
+@pytest.mark.parametrize("mma", [False, True])
+def test_mxfp8(q, orc, rows, K, kind, mma):
+    if mma and K % 128:
+        pytest.skip("MMA layout needs K % 128 == 0")
+    x = make(kind, rows, K, 5 * rows + K) if kind == "edge" else inputs.normal_bf16((rows, K), 1.0, rows + K)
+    b = run(q, q.Fmt.MXFP8, x, q.Layout.MMA if mma else None)
+    codes, sc = orc.quant_mxfp8(bits(x))
+    assert np.array_equal(np_u8(b["codes"]).reshape(rows, K), codes)
+    got = np_u8(b["scales"])
+    if mma:
+        assert np.array_equal(mma_to_canonical(got, rows, K // 32), sc)
+        assert not mma_padding_rows(got, rows, K // 32).any()
+    else:
+        assert np.array_equal(got[: rows * K // 32].reshape(rows, K // 32), sc)
+
+
+@pytest.mark.parametrize("rows,K", [(1, 64), (200, 3072), (300, 12288), (5, 80)])
+@pytest.mark.parametrize("kind", ["outlier", "edge"])
+@pytest.mark.parametrize("mma", [False, True])
+def test_nvfp4(q, orc, rows, K, kind, mma):
+    if mma and K % 64:
+        pytest.skip("MMA layout needs K % 64 == 0")
+    x = make(kind, rows, K, 11 * rows + K)
+    b = run(q, q.Fmt.NVFP4, x, q.Layout.MMA if mma else None)
+    packed, sc, g = orc.quant_nvfp4(bits(x))
+    assert np.array_equal(np_u8(b["codes"]).reshape(rows, K // 2), packed)
+    assert np_f32(b["global"])[0].view(np.uint32) == np.float32(g).view(np.uint32)
+    got = np_u8(b["scales"])
+    if mma:
+        assert np.array_equal(mma_to_canonical(got, rows, K // 16), sc)
+        assert not mma_padding_rows(got, rows, K // 16).any()
+    else:
+        assert np.array_equal(got[: rows * K // 16].reshape(rows, K // 16), sc)
+
+
+@pytest.mark.parametrize("N,K", [(72, 256), (4096, 4096), (12288, 4096), (64, 12288)])
+@pytest.mark.parametrize("kind", ["normal", "edge"])
+def test_int4_g128(q, orc, N, K, kind):
+    w = make(kind, N, K, 13 * N + K)
+    b = run(q, q.Fmt.INT4_G128_ASYM, w, weight=True)
+    qw, sc, qz = orc.quant_int4_g128(bits(w))
+    assert np.array_equal(b["codes"].cpu().numpy().view(np.int32).reshape(K // 8, N), qw)
+    assert np.array_equal(b["scales"].cpu().numpy().view(np.uint16).reshape(K // 128, N), sc)
+    assert np.array_equal(b["zeros"].cpu().numpy().view(np.int32).reshape(K // 128, N // 8), qz)
+
+
+def test_leading_dimension_is_honoured(q, orc):
+    """A strided view (ld > K) quantizes exactly like its contiguous copy."""
+    big = inputs.outlier_channel_bf16(96, 4096, 5)
+    x = big[:, 1024:3072]
+    xd = big.cuda()[:, 1024:3072]
+    for fmt, ref in [(q.Fmt.FP8_TOKEN, orc.quant_fp8_token), (q.Fmt.MXFP8, orc.quant_mxfp8)]:
+        b = q.quantize_act(fmt, xd)
+        torch.cuda.synchronize()
+        codes, sc = ref(bits(x.contiguous()))
+        assert np.array_equal(np_u8(b["codes"]).reshape(96, 2048), codes)
+
+
+@pytest.mark.slow
+def test_full_size_activation_quantizers(q, orc):
+    """The workloads' largest activations: MXFP8 X [20280, 13824] and NVFP4 X
+    [32768, 3072] (per-tensor amax over 100 M elements), compared in full."""
+    x = inputs.mxfp8_linear(13824, 5120).make_x()
+    b = run(q, q.Fmt.MXFP8, x, q.Layout.MMA)
+    codes, sc = orc.quant_mxfp8(bits(x))
+    assert np.array_equal(np_u8(b["codes"]).reshape(codes.shape), codes)
+    assert np.array_equal(mma_to_canonical(np_u8(b["scales"]), x.shape[0], x.shape[1] // 32), sc)
+    del b, codes, sc
+    x = inputs.mixed_stack()[0].make_x()
+    b = run(q, q.Fmt.NVFP4, x, q.Layout.MMA)
+    packed, sc, g = orc.quant_nvfp4(bits(x))
+    assert np.array_equal(np_u8(b["codes"]).reshape(packed.shape), packed)
+    assert np.array_equal(mma_to_canonical(np_u8(b["scales"]), x.shape[0], x.shape[1] // 16), sc)
+    assert np_f32(b["global"])[0] == g
