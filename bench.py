@@ -1,0 +1,518 @@
+#!/usr/bin/env python
+"""Throughput of the quantized-linear hot path on GB300.
+
+One step = one pass of every hot-path operation over all five synthetic
+workloads, each linear doing: weight quantization (load-time, once per
+distinct weight), dynamic activation quantization, and the quantized GEMM
+("vLLM-Omni 在线量化（Online Quantization）完全指南", section
+"在线量化的底层工作原理", stages 2 and 3):
+
+  fp8_tensor   FP8 per-tensor W8A8, M=128, K=N=1024
+  w4a16        int4 g128 decode, M in {1,16,64} x (K,N) in {(4096,4096),(4096,12288),(12288,4096)}
+  fp8_block    per-token x 128x128-block FP8 DiT MLP, M=4096*B (B in {1,4,8}), (K,N) in {(3072,12288),(12288,3072)}
+  mxfp8        MXFP8 video DiT, M=20280, (K,N) in {(5120,13824),(13824,5120),(5120,5120)}
+  mixed        4 NVFP4 attention projections (3072x3072) + 4 FP8 block-128 MLP linears, M=32768
+
+value = GEMM FLOPs of the step / device time of the step (TFLOP/s), inputs
+resident in HBM.  Every step streams several GB, far more than the 126 MB L2,
+so each input is evicted between its uses.
+
+--impl reference times the CPU oracle (the slow reference implementation) on
+a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "quant-GEMM TFLOPS (% of format tensor peak); quantizer GB/s (% of HBM peak)"
+WORKLOAD = "qlin-5-workloads"
+FP8_RATIO, FP4_RATIO = 2.0, 6.0          # nominal dense tensor rates relative to bf16
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--rows-json", default=None, help="also write the per-row breakdown here")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------- workload description
+def workload_linears():
+    from serving_amax_reduce_gb300 import inputs as I
+    lins = [("fp8_tensor", I.fp8_tensor_linear())]
+    for (K, N) in I.W4A16_SHAPES:
+        for M in I.W4A16_M:
+            lins.append(("w4a16", I.w4a16_linear(M, K, N)))
+    for B in I.FP8_MLP_B:
+        for (K, N) in I.FP8_MLP_SHAPES:
+            lins.append(("fp8_block", I.fp8_block_linear(B, K, N)))
+    for (K, N) in I.MXFP8_SHAPES:
+        lins.append(("mxfp8", I.mxfp8_linear(K, N)))
+    for lin in I.mixed_stack():
+        lins.append(("mixed", lin))
+    return lins
+
+
+def config_block(args):
+    return {
+        "workload": WORKLOAD,
+        "workloads": ["fp8_tensor M128 K1024 N1024",
+                      "w4a16 M{1,16,64} (K,N){(4096,4096),(4096,12288),(12288,4096)}",
+                      "fp8_block M4096*{1,4,8} (K,N){(3072,12288),(12288,3072)}",
+                      "mxfp8 M20280 (K,N){(5120,13824),(13824,5120),(5120,5120)}",
+                      "mixed M32768: 4x nvfp4 3072x3072 + 4x fp8_block (3072<->12288)"],
+        "step": "per linear: weight quantize + activation quantize + quantized GEMM",
+        "l2": "inputs larger than L2: each step streams several GB through the 126 MB L2 between reuses",
+        "parallelism": f"replicas x{args.gpus}",
+    }
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        pw = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows), "power_w_max": max(pw) if pw else None}
+
+
+# ---------------------------------------------------------------- native arm
+class Job:
+    """One linear: device inputs, pre-allocated quantized buffers and output."""
+
+    def __init__(self, group, lin, dev, q):
+        import torch
+        F, L = q.Fmt, q.Layout
+        self.group, self.lin = group, lin
+        self.x = lin.make_x(device=dev)
+        self.w = lin.make_w(device=dev)
+        wf = {"fp8_tensor": F.FP8_TENSOR, "fp8_block128": F.FP8_BLOCK128, "mxfp8": F.MXFP8, "nvfp4": F.NVFP4,
+              "int4_g128": F.INT4_G128_ASYM}[lin.w_fmt]
+        xf = {"fp8_tensor": F.FP8_TENSOR, "fp8_token": F.FP8_TOKEN, "mxfp8": F.MXFP8, "nvfp4": F.NVFP4,
+              "bf16": F.BF16}[lin.x_fmt]
+        self.wf, self.xf = wf, xf
+        self.layout = L.MMA if wf in (F.MXFP8, F.NVFP4) else L.CANONICAL
+        self.wb = q.alloc_quant(wf, lin.N, lin.K, self.layout, dev)
+        self.xb = q.alloc_quant(xf, lin.M, lin.K, self.layout, dev) if xf != F.BF16 else None
+        self.y = torch.empty(lin.M, lin.N, dtype=torch.bfloat16, device=dev)
+        self.q = q
+
+    def launches(self) -> int:
+        F = self.q.Fmt
+        two = (F.FP8_TENSOR, F.NVFP4)
+        n = (2 if self.wf in two else 1) + 1
+        if self.xf != F.BF16:
+            n += 2 if self.xf in two else 1
+        return n
+
+    def quant_w(self):
+        self.q.quantize_weight(self.wf, self.w, self.layout, bufs=self.wb)
+
+    def quant_x(self):
+        if self.xb is not None:
+            self.q.quantize_act(self.xf, self.x, self.layout, bufs=self.xb)
+
+    def gemm(self):
+        q, lin = self.q, self.lin
+        if self.xb is None:
+            q.gemm(self.wf, self.xf, lin.M, lin.N, lin.K, self.x, None, self.wb["codes"], self.wb["scales"],
+                   w_zeros=self.wb["zeros"], y=self.y)
+        else:
+            q.gemm(self.wf, self.xf, lin.M, lin.N, lin.K, self.xb["codes"], self.xb["scales"], self.wb["codes"],
+                   self.wb["scales"], x_global=self.xb.get("global"), w_global=self.wb.get("global"), y=self.y,
+                   layout=self.layout)
+
+    def bytes_w_quant(self) -> int:
+        lin, q = self.lin, self.q
+        return (lin.N * lin.K * 2 + q.qlin_codes_bytes(self.wf, lin.N, lin.K)
+                + q.qlin_scales_bytes(self.wf, self.layout, lin.N, lin.K) + q.qlin_zeros_bytes(self.wf, lin.N, lin.K))
+
+    def bytes_x_quant(self) -> int:
+        lin, q = self.lin, self.q
+        if self.xb is None:
+            return 0
+        return (lin.M * lin.K * 2 + q.qlin_codes_bytes(self.xf, lin.M, lin.K)
+                + q.qlin_scales_bytes(self.xf, self.layout, lin.M, lin.K))
+
+    def gemm_bytes(self) -> int:
+        """Algorithmic HBM bytes of the GEMM: operands once + output once."""
+        lin, q = self.lin, self.q
+        xb = lin.M * lin.K * 2 if self.xb is None else (q.qlin_codes_bytes(self.xf, lin.M, lin.K)
+                                                          + q.qlin_scales_bytes(self.xf, self.layout, lin.M, lin.K))
+        wb = (q.qlin_codes_bytes(self.wf, lin.N, lin.K) + q.qlin_scales_bytes(self.wf, self.layout, lin.N, lin.K)
+              + q.qlin_zeros_bytes(self.wf, lin.N, lin.K))
+        return xb + wb + lin.M * lin.N * 2
+
+
+def kernel_name(job, op):
+    F = job.q.Fmt
+    if op == "gemm":
+        return {F.FP8_TENSOR: "gemm_fp8_tensor", F.FP8_BLOCK128: "gemm_fp8_block", F.MXFP8: "gemm_mxfp8",
+                F.NVFP4: "gemm_nvfp4", F.INT4_G128_ASYM: "gemm_w4a16"}[job.wf]
+    fmt = job.wf if op == "quant_w" else job.xf
+    return "quant_" + {F.FP8_TENSOR: "fp8_tensor", F.FP8_TOKEN: "fp8_token", F.FP8_BLOCK128: "fp8_block128",
+                       F.MXFP8: "mxfp8", F.NVFP4: "nvfp4", F.INT4_G128_ASYM: "int4_g128"}[fmt]
+
+
+def tensor_peak(peaks, wf, q, sustained=True):
+    bf16 = peaks.get("bf16_tflops_sustained" if sustained else "bf16_tflops") or (1700.0 if sustained else 1900.0)
+    ratio = FP4_RATIO if wf == q.Fmt.NVFP4 else (1.0 if wf == q.Fmt.INT4_G128_ASYM else FP8_RATIO)
+    return bf16 * ratio
+
+
+def run_native(args, rank, world, local_rank):
+    import torch
+    from serving_amax_reduce_gb300 import build as qbuild
+    qbuild.build()
+    from serving_amax_reduce_gb300 import qlin as q
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    peaks = {}
+    pp = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(pp):
+        peaks = json.load(open(pp))
+    peak_src = "measured" if peaks else "fallback"
+    hbm_peak = peaks.get("hbm_gbs", 6800.0)
+
+    jobs = [Job(g, lin, dev, q) for g, lin in workload_linears()]
+    # distinct weights are quantized once per step (several linears may share a W shape but not a W)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+
+    def step(events=None):
+        for j in jobs:
+            for op in ("quant_w", "quant_x", "gemm"):
+                if op == "quant_x" and j.xb is None:
+                    continue
+                if events is not None:
+                    e0 = torch.cuda.Event(enable_timing=True)
+                    e1 = torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                getattr(j, op)()
+                if events is not None:
+                    e1.record(stream)
+                    events.append((j, op, e0, e1))
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    if q.read_device_status(dev) != 0:
+        raise RuntimeError("a bounded device wait expired during warm-up")
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    # ---- timed region (device time of whole steps, per-call events inside)
+    sampler = ClockSampler(local_rank if os.environ.get("CUDA_VISIBLE_DEVICES") is None else 0)
+    events = []
+    barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        step(events)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clocks = sampler.stop()
+    ms_total = t0.elapsed_time(t1)
+    if q.read_device_status(dev) != 0:
+        raise RuntimeError("a bounded device wait expired in the timed region")
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_total = float(tt.item())
+
+    flops_step = sum(j.lin.flops() for j in jobs)
+    ms_step = ms_total / args.steps
+    value = flops_step * args.steps * world / (ms_total * 1e-3) / 1e12
+
+    # ---- per-row breakdown from the per-call events
+    rows = {}
+    for j, op, e0, e1 in events:
+        name = kernel_name(j, op)
+        r = rows.setdefault(name, {"launches_per_step": 0, "ms": 0.0, "flops": 0, "bytes": 0, "wf": j.wf})
+        r["ms"] += e0.elapsed_time(e1)
+        r["launches_per_step"] += 1
+        if op == "gemm":
+            r["flops"] += j.lin.flops()
+            r["bytes"] += j.gemm_bytes()
+        else:
+            r["bytes"] += j.bytes_w_quant() if op == "quant_w" else j.bytes_x_quant()
+    out_rows = {}
+    for name, r in rows.items():
+        ms = r["ms"] / args.steps                     # device ms per step spent in this row
+        d = {"calls_per_step": r["launches_per_step"] // args.steps, "ms_per_step": round(ms, 4),
+             "gbs": round((r["bytes"] / args.steps) / (ms * 1e-3) / 1e9, 1)}
+        d["hbm_frac"] = round(d["gbs"] / hbm_peak, 3)
+        if r["flops"]:
+            tf = (r["flops"] / args.steps) / (ms * 1e-3) / 1e12
+            d["tflops"] = round(tf, 1)
+            d["tensor_frac"] = round(tf / tensor_peak(peaks, r["wf"], q), 3)
+        out_rows[name] = d
+
+    # dominant kernel: the row with the largest share of the step
+    dom = max(rows, key=lambda k: rows[k]["ms"])
+    dr = rows[dom]
+    dom_ms_per_launch = dr["ms"] / dr["launches_per_step"]
+    if dr["flops"]:
+        per_launch = dr["flops"] / dr["launches_per_step"]
+        peak = tensor_peak(peaks, dr["wf"], q)
+        achieved = per_launch / (dom_ms_per_launch * 1e-3) / 1e12
+        roofline = {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 1), "peak": round(peak, 1),
+                    "unit": "TFLOP/s", "frac": round(achieved / peak, 3), "traffic": None,
+                    "peak_source": f"{peak_src} bf16 sustained x nominal format ratio",
+                    "algorithmic_per_launch": per_launch}
+    else:
+        per_launch = dr["bytes"] / dr["launches_per_step"]
+        achieved = per_launch / (dom_ms_per_launch * 1e-3) / 1e9
+        roofline = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": hbm_peak,
+                    "unit": "GB/s", "frac": round(achieved / hbm_peak, 3), "traffic": None,
+                    "peak_source": peak_src, "algorithmic_per_launch": per_launch}
+
+    launches = sum(j.launches() for j in jobs) * args.steps
+
+    # ---- end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, jobs, stream, flops_step, world, dev)
+
+    res = {"metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+           "warmup": max(args.warmup, 3), "ms_per_step": round(ms_step, 3), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "e4m3/e2m1/int4 operands, f32 accumulate, bf16 out",
+           "data": "synthetic (seeded; shapes and distributions of the five workloads)",
+           "config": config_block(args), "clocks": clocks, "gpu_launches": launches, "roofline": roofline,
+           "rows": out_rows}
+    if e2e:
+        res["e2e"] = e2e
+    return res, jobs
+
+
+def run_e2e(args, jobs, stream, flops_step, world, dev):
+    import torch
+    host_in = []
+    h2d = d2h = 0
+    for j in jobs:
+        hx = torch.empty_like(j.x, device="cpu").pin_memory()
+        hx.copy_(j.x)
+        hw = torch.empty_like(j.w, device="cpu").pin_memory()
+        hw.copy_(j.w)
+        hy = torch.empty_like(j.y, device="cpu").pin_memory()
+        host_in.append((j, hx, hw, hy))
+        h2d += hx.numel() * 2 + hw.numel() * 2
+        d2h += hy.numel() * 2
+
+    def step():
+        for j, hx, hw, hy in host_in:
+            j.x.copy_(hx, non_blocking=True)
+            j.w.copy_(hw, non_blocking=True)
+            j.quant_w()
+            j.quant_x()
+            j.gemm()
+            hy.copy_(j.y, non_blocking=True)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    n = max(1, min(args.steps, 5))
+    t0.record(stream)
+    for _ in range(n):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1)
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    return {"value": round(flops_step * n * world / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n,
+            "ms_per_step": round(ms / n, 3)}
+
+
+# ---------------------------------------------------------------- oracle timing
+def oracle_sample_step(rows_x: int, rows_w: int):
+    """The CPU oracle on a bounded sample of the workload: for one linear of
+    each workload, quantize rows_x rows of X and rows_w rows of W, dequantize,
+    and form the float64 product.  Returns (flops, seconds)."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from serving_amax_reduce_gb300 import inputs as I
+
+    picks = [I.fp8_tensor_linear(), I.w4a16_linear(16, 4096, 4096), I.fp8_block_linear(1, 3072, 12288),
+             I.mxfp8_linear(5120, 13824), I.mixed_stack()[0]]
+    flops, secs = 0, 0.0
+    for lin in picks:
+        Ms = min(rows_x, lin.M)
+        Ns = min(rows_w, lin.N)
+        Ns -= Ns % 128 if lin.w_fmt in ("fp8_block128",) else Ns % 8
+        x = lin.make_x()[:Ms].contiguous()
+        w = lin.make_w()[:Ns].contiguous()
+        xb = x.view(torch.int16).numpy().view(np.uint16)
+        wb = w.view(torch.int16).numpy().view(np.uint16)
+        t = time.perf_counter()
+        if lin.w_fmt == "fp8_tensor":
+            cx, sx = oracle.quant_fp8_tensor(xb); cw, sw = oracle.quant_fp8_tensor(wb)
+            xh, wh = oracle.dequant_fp8_tensor(cx, sx), oracle.dequant_fp8_tensor(cw, sw)
+        elif lin.w_fmt == "int4_g128":
+            qw, sc, qz = oracle.quant_int4_g128(wb)
+            xh, wh = oracle.bf16_values(xb), oracle.dequant_int4_g128(qw, sc, qz)
+        elif lin.w_fmt == "fp8_block128":
+            cx, sx = oracle.quant_fp8_token(xb); cw, sw = oracle.quant_fp8_block128(wb)
+            xh, wh = oracle.dequant_fp8_token(cx, sx), oracle.dequant_fp8_block128(cw, sw)
+        elif lin.w_fmt == "mxfp8":
+            cx, sx = oracle.quant_mxfp8(xb); cw, sw = oracle.quant_mxfp8(wb)
+            xh, wh = oracle.dequant_mxfp8(cx, sx), oracle.dequant_mxfp8(cw, sw)
+        else:
+            cx, sx, gx = oracle.quant_nvfp4(xb); cw, sw, gw = oracle.quant_nvfp4(wb)
+            xh, wh = oracle.dequant_nvfp4(cx, sx, gx), oracle.dequant_nvfp4(cw, sw, gw)
+        oracle.gemm_ref(xh, wh)
+        secs += time.perf_counter() - t
+        flops += 2 * Ms * Ns * lin.K
+    return flops, secs
+
+
+SAMPLE_BASELINE = (512, 1024)      # rows of X, rows of W per linear (cpu_baseline leg)
+SAMPLE_REFERENCE = (256, 512)      # per step of the --impl reference arm
+
+
+def blas_threads():
+    try:
+        import numpy as np  # noqa: F401
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count()
+
+
+def cpu_baseline():
+    import oracle
+    oracle.build()
+    flops, secs = oracle_sample_step(*SAMPLE_BASELINE)
+    return {"value": round(flops / secs / 1e12, 6), "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
+            "sample": (f"one linear per workload, X[:{SAMPLE_BASELINE[0]}] x W[:{SAMPLE_BASELINE[1]}] full K: "
+                       "scalar C quantizers (1 thread) + float64 numpy matmul (BLAS threads)"),
+            "seconds": round(secs, 2)}
+
+
+def run_reference(args, rank, world):
+    import oracle
+    oracle.build()
+    if rank != 0:
+        return None
+    for _ in range(args.warmup):
+        oracle_sample_step(*SAMPLE_REFERENCE)
+    flops = secs = 0
+    for _ in range(args.steps):
+        f, s = oracle_sample_step(*SAMPLE_REFERENCE)
+        flops += f
+        secs += s
+    v = flops / secs / 1e12
+    return {"impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(secs / args.steps * 1e3, 1),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded; bounded sample of the five workloads)", "config": config_block(args),
+            "cpu_baseline": {"value": round(v, 6), "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
+                             "sample": (f"per step: one linear per workload, X[:{SAMPLE_REFERENCE[0]}] x "
+                                        f"W[:{SAMPLE_REFERENCE[1]}] at full K")},
+            "e2e": {"value": round(v, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse_args()
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    local_rank = int(os.environ.get("LOCAL_RANK", 0))
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    res, _ = run_native(args, rank, world, local_rank)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline()
+    if args.rows_json and rank == 0:
+        json.dump(res, open(args.rows_json, "w"), indent=1)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

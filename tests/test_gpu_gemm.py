@@ -158,6 +158,34 @@ def test_nvfp4_gemm_full_size(q, orc):
     nvfp4_case(q, orc, 32768, 3072, 3072, nrows=256)
 
 
+# ------------------------------------------------------------------ W4A16 decode
+def w4a16_case(q, orc, M, K, N):
+    lin = inputs.w4a16_linear(M, K, N)
+    x, w = lin.make_x(), lin.make_w()
+    F = q.Fmt
+    bw = q.quantize_weight(F.INT4_G128_ASYM, w.cuda())
+    xd = x.cuda()
+    y = q.gemm(F.INT4_G128_ASYM, F.BF16, M, N, K, xd, None, bw["codes"], bw["scales"], w_zeros=bw["zeros"])
+    torch.cuda.synchronize()
+    wh = orc.dequant_int4_g128(bw["codes"].cpu().numpy().view(np.int32).reshape(K // 8, N),
+                               bw["scales"].cpu().numpy().view(np.uint16).reshape(K // 128, N),
+                               bw["zeros"].cpu().numpy().view(np.int32).reshape(K // 128, N // 8))
+    return check(orc, y_np(y), orc.gemm_ref(orc.bf16_values(bits(x)), wh), x, w)
+
+
+@pytest.mark.parametrize("M,K,N", [(1, 4096, 4096), (16, 4096, 12288), (64, 12288, 4096), (5, 256, 72),
+                                   (100, 512, 256), (200, 1024, 384), (33, 128, 136)])
+def test_w4a16_gemm(q, orc, M, K, N):
+    w4a16_case(q, orc, M, K, N)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("M", [1, 16, 64])
+@pytest.mark.parametrize("K,N", [(4096, 4096), (4096, 12288), (12288, 4096)])
+def test_w4a16_gemm_all_decode_shapes(q, orc, M, K, N):
+    w4a16_case(q, orc, M, K, N)
+
+
 # ------------------------------------------------------------------ device timeout path
 def test_bounded_wait_expires_with_status(q):
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
