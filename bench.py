@@ -50,6 +50,8 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--rows-json", default=None, help="also write the per-row breakdown here")
+    ap.add_argument("--eager", action="store_true", help="launch call by call instead of replaying a CUDA graph")
+    ap.add_argument("--only", default=None, help="keep only linears whose name contains this string")
     return ap.parse_args()
 
 
@@ -230,23 +232,24 @@ def run_native(args, rank, world, local_rank):
     peak_src = "measured" if peaks else "fallback"
     hbm_peak = peaks.get("hbm_gbs", 6800.0)
 
-    jobs = [Job(g, lin, dev, q) for g, lin in workload_linears()]
+    jobs = [Job(g, lin, dev, q) for g, lin in workload_linears() if not args.only or args.only in lin.name]
+    if not jobs:
+        raise SystemExit(f"--only {args.only!r} matches no linear")
     # distinct weights are quantized once per step (several linears may share a W shape but not a W)
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
 
-    def step(events=None):
+    def step(events=None, make_event=None):
         for j in jobs:
             for op in ("quant_w", "quant_x", "gemm"):
                 if op == "quant_x" and j.xb is None:
                     continue
                 if events is not None:
-                    e0 = torch.cuda.Event(enable_timing=True)
-                    e1 = torch.cuda.Event(enable_timing=True)
-                    e0.record(stream)
+                    e0, e1 = make_event(), make_event()
+                    e0.record(torch.cuda.current_stream())
                 getattr(j, op)()
                 if events is not None:
-                    e1.record(stream)
+                    e1.record(torch.cuda.current_stream())
                     events.append((j, op, e0, e1))
 
     for _ in range(max(args.warmup, 3)):
@@ -260,7 +263,23 @@ def run_native(args, rank, world, local_rank):
             import torch.distributed as dist
             dist.barrier()
 
-    # ---- timed region (device time of whole steps, per-call events inside)
+    # The step is captured once as a CUDA graph (about 80 library launches);
+    # per-call timing events become event-record nodes of the same graph.
+    graph, gevents, mode = None, [], "eager"
+    if not args.eager:
+        try:
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                step(gevents, lambda: torch.cuda.Event(enable_timing=True, external=True))
+            graph.replay()
+            torch.cuda.synchronize()
+            mode = "cuda-graph"
+        except (TypeError, RuntimeError) as exc:      # no graph-capturable timing events here
+            print(f"bench: graph capture unavailable ({exc}); timing eagerly", file=sys.stderr)
+            graph, gevents = None, []
+            torch.cuda.synchronize()
+
+    # ---- timed region (device time of whole steps)
     sampler = ClockSampler(local_rank if os.environ.get("CUDA_VISIBLE_DEVICES") is None else 0)
     events = []
     barrier()
@@ -270,7 +289,10 @@ def run_native(args, rank, world, local_rank):
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
     for _ in range(args.steps):
-        step(events)
+        if graph is not None:
+            graph.replay()
+        else:
+            step(events, lambda: torch.cuda.Event(enable_timing=True))
     t1.record(stream)
     torch.cuda.synchronize()
     barrier()
@@ -278,6 +300,19 @@ def run_native(args, rank, world, local_rank):
     ms_total = t0.elapsed_time(t1)
     if q.read_device_status(dev) != 0:
         raise RuntimeError("a bounded device wait expired in the timed region")
+    if graph is not None:
+        # the graph's event nodes hold the last timed replay; add a few more
+        # replays (each read back) so that per-call times are averaged
+        events = [(j, op, e0.elapsed_time(e1)) for j, op, e0, e1 in gevents]
+        n_extra = max(1, min(args.steps, 4))
+        for _ in range(n_extra):
+            graph.replay()
+            torch.cuda.synchronize()
+            events += [(j, op, e0.elapsed_time(e1)) for j, op, e0, e1 in gevents]
+        per_call_steps = 1 + n_extra
+    else:
+        events = [(j, op, e0.elapsed_time(e1)) for j, op, e0, e1 in events]
+        per_call_steps = args.steps
     if world > 1:
         import torch.distributed as dist
         tt = torch.tensor([ms_total], device=dev)
@@ -290,11 +325,11 @@ def run_native(args, rank, world, local_rank):
 
     # ---- per-row breakdown from the per-call events
     rows = {}
-    for j, op, e0, e1 in events:
+    for j, op, ms in events:
         name = kernel_name(j, op)
-        r = rows.setdefault(name, {"launches_per_step": 0, "ms": 0.0, "flops": 0, "bytes": 0, "wf": j.wf})
-        r["ms"] += e0.elapsed_time(e1)
-        r["launches_per_step"] += 1
+        r = rows.setdefault(name, {"launches": 0, "ms": 0.0, "flops": 0, "bytes": 0, "wf": j.wf})
+        r["ms"] += ms
+        r["launches"] += 1
         if op == "gemm":
             r["flops"] += j.lin.flops()
             r["bytes"] += j.gemm_bytes()
@@ -302,12 +337,12 @@ def run_native(args, rank, world, local_rank):
             r["bytes"] += j.bytes_w_quant() if op == "quant_w" else j.bytes_x_quant()
     out_rows = {}
     for name, r in rows.items():
-        ms = r["ms"] / args.steps                     # device ms per step spent in this row
-        d = {"calls_per_step": r["launches_per_step"] // args.steps, "ms_per_step": round(ms, 4),
-             "gbs": round((r["bytes"] / args.steps) / (ms * 1e-3) / 1e9, 1)}
+        ms = r["ms"] / per_call_steps                 # device ms per step spent in this row
+        d = {"calls_per_step": r["launches"] // per_call_steps, "ms_per_step": round(ms, 4),
+             "gbs": round((r["bytes"] / per_call_steps) / (ms * 1e-3) / 1e9, 1)}
         d["hbm_frac"] = round(d["gbs"] / hbm_peak, 3)
         if r["flops"]:
-            tf = (r["flops"] / args.steps) / (ms * 1e-3) / 1e12
+            tf = (r["flops"] / per_call_steps) / (ms * 1e-3) / 1e12
             d["tflops"] = round(tf, 1)
             d["tensor_frac"] = round(tf / tensor_peak(peaks, r["wf"], q), 3)
         out_rows[name] = d
@@ -315,9 +350,9 @@ def run_native(args, rank, world, local_rank):
     # dominant kernel: the row with the largest share of the step
     dom = max(rows, key=lambda k: rows[k]["ms"])
     dr = rows[dom]
-    dom_ms_per_launch = dr["ms"] / dr["launches_per_step"]
+    dom_ms_per_launch = dr["ms"] / dr["launches"]
     if dr["flops"]:
-        per_launch = dr["flops"] / dr["launches_per_step"]
+        per_launch = dr["flops"] / dr["launches"]
         peak = tensor_peak(peaks, dr["wf"], q)
         achieved = per_launch / (dom_ms_per_launch * 1e-3) / 1e12
         roofline = {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 1), "peak": round(peak, 1),
@@ -325,7 +360,7 @@ def run_native(args, rank, world, local_rank):
                     "peak_source": f"{peak_src} bf16 sustained x nominal format ratio",
                     "algorithmic_per_launch": per_launch}
     else:
-        per_launch = dr["bytes"] / dr["launches_per_step"]
+        per_launch = dr["bytes"] / dr["launches"]
         achieved = per_launch / (dom_ms_per_launch * 1e-3) / 1e9
         roofline = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": hbm_peak,
                     "unit": "GB/s", "frac": round(achieved / hbm_peak, 3), "traffic": None,
@@ -343,7 +378,7 @@ def run_native(args, rank, world, local_rank):
            "scaling": "weak", "vs_baseline": None, "dtype": "e4m3/e2m1/int4 operands, f32 accumulate, bf16 out",
            "data": "synthetic (seeded; shapes and distributions of the five workloads)",
            "config": config_block(args), "clocks": clocks, "gpu_launches": launches, "roofline": roofline,
-           "rows": out_rows}
+           "rows": out_rows, "launch_mode": mode}
     if e2e:
         res["e2e"] = e2e
     return res, jobs
@@ -375,12 +410,26 @@ def run_e2e(args, jobs, stream, flops_step, world, dev):
     for _ in range(2):
         step()
     torch.cuda.synchronize()
+    graph = None
+    if not args.eager:
+        try:
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                step()
+            graph.replay()
+            torch.cuda.synchronize()
+        except RuntimeError:
+            graph = None
+            torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     n = max(1, min(args.steps, 5))
     t0.record(stream)
     for _ in range(n):
-        step()
+        if graph is not None:
+            graph.replay()
+        else:
+            step()
     t1.record(stream)
     torch.cuda.synchronize()
     ms = t0.elapsed_time(t1)

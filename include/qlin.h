@@ -117,8 +117,9 @@ size_t qlin_zeros_bytes(qlin_format fmt, int64_t rows, int64_t K);
  * formats (FP8_TENSOR, NVFP4) keep one float per reduction block; others 0. */
 size_t qlin_quant_workspace_bytes(qlin_format fmt, int64_t rows, int64_t K);
 
-/* Workspace a qlin_gemm call needs for this pair and shape (split-K partial
- * sums and tile counters for the W4A16 decode GEMM; 0 for the others).      */
+/* Workspace a qlin_gemm call needs for this pair and shape.  Every GEMM
+ * here returns 0: the W4A16 split-K reduction runs through distributed
+ * shared memory inside a thread-block cluster.                             */
 size_t qlin_gemm_workspace_bytes(qlin_format w_fmt, qlin_format x_fmt,
                                  int64_t M, int64_t N, int64_t K);
 
