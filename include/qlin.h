@@ -176,6 +176,34 @@ qlin_status qlin_gemm(qlin_format w_fmt, qlin_format x_fmt, int64_t M, int64_t N
                       int64_t ldy, qlin_scale_layout layout, void *workspace_dev,
                       size_t workspace_bytes, int *dev_status_dev, qlin_stream_t stream);
 
+/* ---------------------------------------------------------------- no-allocation variant
+ * The pages have no counterpart to this entry point.
+ *
+ * Per-tensor FP8 quantization (QLIN_FP8_TENSOR rules, same codes and scale
+ * as qlin_quantize_act / qlin_quantize_weight) for callers that cannot
+ * allocate device memory or hand over a workspace -- for example a plugin
+ * inside a serving engine that has already reserved the device memory for its
+ * own pool, or code that must keep the memory footprint fixed after start-up.
+ * The per-tensor amax partials live in a fixed device array inside the
+ * library (QLIN_NOALLOC_MAX_PARTIALS floats, 16 KB), which every device that
+ * loads the library holds until exit.  One partial covers 16384 elements, so
+ * rows*K may be at most QLIN_NOALLOC_MAX_ELEMENTS; larger tensors return
+ * QLIN_ERR_WORKSPACE before any launch.
+ *   x_bf16_dev  [rows, K] bf16, leading dimension ld (elements), 16-byte aligned
+ *   codes_dev   rows*K E4M3 codes, row-major, 16-byte aligned
+ *   scale_dev   one float, the tensor scale s = amax/448
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current, so make the first call
+ * before any stream capture, and call with the stream's device current.
+ * The array is shared by all calls on a device and keeps the last call's
+ * contents (each call rewrites the slots it reads, nothing needs clearing);
+ * calls that overlap on the GPU race on it.  Allocates nothing; errors as
+ * qlin_quantize_act.                                                        */
+#define QLIN_NOALLOC_MAX_PARTIALS 4096
+#define QLIN_NOALLOC_MAX_ELEMENTS (4096LL * 16384LL)
+qlin_status qlin_quantize_fp8_tensor_noalloc(const void *x_bf16_dev, int64_t rows, int64_t K, int64_t ld,
+                                             void *codes_dev, float *scale_dev, qlin_stream_t stream);
+
 /* ---------------------------------------------------------------- diagnostics
  * Runs the library's bounded device wait on an mbarrier that nothing ever
  * completes, with at most `max_polls` polls, then writes

@@ -26,6 +26,7 @@ UNITS = {
     "gemm_tc.cu": [],
     "gemm_w4a16.cu": [],
     "api.cu": [],
+    "noalloc.cu": [],
 }
 
 

@@ -76,6 +76,7 @@ def _load():
         "qlin_gemm": ([_I, _I, _I64, _I64, _I64, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I, _P, _SZ, _P, _P],
                       _I),
         "qlin_debug_expire_wait": ([_P, ctypes.c_uint32, _P], _I),
+        "qlin_quantize_fp8_tensor_noalloc": ([_P, _I64, _I64, _I64, _P, _P, _P], _I),
     }
     for name, (args, res) in sigs.items():
         fn = getattr(lib, name)
@@ -137,6 +138,15 @@ def qlin_gemm(w_fmt, x_fmt, M, N, K, x, x_scales, x_global, w_codes, w_scales, w
 
 def qlin_debug_expire_wait(status, max_polls, stream) -> int:
     return _load().qlin_debug_expire_wait(status, max_polls, stream)
+
+
+NOALLOC_MAX_ELEMENTS = 4096 * 16384
+
+
+def qlin_quantize_fp8_tensor_noalloc(x, rows, K, ld, codes, scale, stream) -> int:
+    """Per-tensor FP8 quantization that allocates nothing and takes no
+    workspace (for callers that cannot allocate device memory); see qlin.h."""
+    return _load().qlin_quantize_fp8_tensor_noalloc(x, rows, K, ld, codes, scale, stream)
 
 
 # ------------------------------------------------------------------ torch marshalling
