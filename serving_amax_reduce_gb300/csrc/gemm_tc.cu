@@ -11,18 +11,22 @@
 // FP8/NVFP4 model).  The optional bias epilogue is the fused
 // alpha * (A @ B) + bias the first page mentions for Blackwell FP8.
 //
-// One CTA computes a 128 x 256 output tile with a warp-specialized pipeline:
+// Persistent CTAs (one per SM) walk 128 x 256 output tiles in a grouped
+// raster; each CTA runs a warp-specialized pipeline:
 //   warp 0   one lane issues TMA loads of the X and W tiles (128-byte
 //            swizzle, zero fill past M) and the scale chunks into a
 //            4-stage shared-memory ring;
 //   warp 1   allocates TMEM; one lane issues tcgen05.mma into the TMEM
 //            accumulator and tcgen05.commit to release each stage;
-//   warps 2+ drain TMEM with tcgen05.ld, apply the scales and write bf16.
+//   warps 2-9 copy the accumulator TMEM -> registers with tcgen05.ld,
+//            release it to the next tile's MMAs at once, then apply the
+//            scales and write bf16 while that tile's mainloop runs.
 // Variants:
 //   FP8 per-tensor  kind::f8f6f4, alpha = s_x * s_w in the epilogue.
 //   FP8 block       kind::f8f6f4 into one of two TMEM partial buffers per
-//                   128-wide K block; eight epilogue warps promote each
-//                   partial with its fp32 weight-block scale into register
+//                   128-wide K block; the eight epilogue warps promote each
+//                   partial with its fp32 weight-block scale (prefetched
+//                   into registers at tile start) into register
 //                   accumulators (fp32 block scales are not an MMA scale
 //                   type), then multiply by the per-token scale.
 //   MXFP8           kind::mxf8f6f4.block_scale.scale_vec::1X, UE8M0 scales
@@ -52,7 +56,7 @@ template <int KIND>
 struct Cfg {
     static constexpr int BN = 256;
     static constexpr int STAGES = 4;
-    static constexpr int EPI_WARPS = (KIND == kFp8Block) ? 8 : 4;
+    static constexpr int EPI_WARPS = 8;              // two per TMEM lane quadrant, 128 columns each
     static constexpr int THREADS = 64 + 32 * EPI_WARPS;
     static constexpr int A_BYTES = BM * BKB;
     static constexpr int B_BYTES = BN * BKB;
@@ -66,7 +70,7 @@ struct Cfg {
     static constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
     static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
     static constexpr int OFF_BAR = OFF_SFB + STAGES * SFB_BYTES;
-    static constexpr int NBAR = 2 * STAGES + 6;      // full[S], empty[S], acc, pfull[2], pempty[2], drain
+    static constexpr int NBAR = 2 * STAGES + 7;      // full[S], empty[S], accf, acce, pfull[2], pempty[2], drain
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int SMEM = OFF_MISC + 64 + 1024; // + slack for 1024-byte alignment
     static constexpr uint32_t TMEM_COLS = 512;
@@ -155,12 +159,29 @@ __device__ __forceinline__ void store_row32(const TcParams& p, int row, int n, c
 #pragma unroll
         for (int i = 0; i < 4; i++) d4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
     } else {
-        for (int i = 0; i < 32 && n + i < p.N; i++) {
-            float a = v[i];
-            if (p.bias) a += __bfloat162float(__ushort_as_bfloat16(p.bias[n + i]));
-            dst[i] = __bfloat16_as_ushort(__float2bfloat16_rn(a));
+#pragma unroll
+        for (int i = 0; i < 32; i++) {
+            if (n + i < p.N) {
+                float a = v[i];
+                if (p.bias) a += __bfloat162float(__ushort_as_bfloat16(p.bias[n + i]));
+                dst[i] = __bfloat16_as_ushort(__float2bfloat16_rn(a));
+            }
         }
     }
+}
+
+// Grouped raster: bands of 16 row blocks; inside a band, consecutive tile
+// indices walk down the rows first, so the CTAs running at the same time
+// share A row blocks and B column blocks in L2.
+template <int BN>
+__device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int& m0, int& n0) {
+    constexpr int GM = 16;
+    const int band = t / (GM * tiles_n);
+    const int first_m = band * GM;
+    const int gm = min(GM, tiles_m - first_m);
+    const int idx = t - band * GM * tiles_n;
+    m0 = (first_m + idx % gm) * BM;
+    n0 = (idx / gm) * BN;
 }
 
 template <int KIND>
@@ -171,15 +192,17 @@ __global__ void __launch_bounds__(Cfg<KIND>::THREADS, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
     uint64_t* empty = full + C::STAGES;
-    uint64_t* accf = empty + C::STAGES;
-    uint64_t* pfull = accf + 1;
-    uint64_t* pempty = pfull + 2;
+    uint64_t* accf = empty + C::STAGES;     // accumulator ready (non-block kinds)
+    uint64_t* acce = accf + 1;              // accumulator drained into registers
+    uint64_t* pfull = acce + 1;             // FP8 block: partial buffer b ready
+    uint64_t* pempty = pfull + 2;           // FP8 block: partial buffer b drained
     uint64_t* drain = pempty + 2;
     uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);   // tmem base, abort, consumed, issued
     volatile uint32_t* abort_flag = misc + 1;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n0 = blockIdx.x * C::BN, m0 = blockIdx.y * BM;
+    const int tiles_m = (p.M + BM - 1) / BM, tiles_n = (p.N + C::BN - 1) / C::BN;
+    const int ntiles = tiles_m * tiles_n;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; s++) {
@@ -187,6 +210,7 @@ __global__ void __launch_bounds__(Cfg<KIND>::THREADS, 1)
             mbar_init(empty + s, 1);
         }
         mbar_init(accf, 1);
+        mbar_init(acce, C::EPI_WARPS);
         mbar_init(pfull + 0, 1);
         mbar_init(pfull + 1, 1);
         mbar_init(pempty + 0, C::EPI_WARPS);
@@ -209,167 +233,215 @@ __global__ void __launch_bounds__(Cfg<KIND>::THREADS, 1)
 
     if (!skip && warp == 0 && lane == 0) {
         // ------------------------------------------------ TMA producer
-        int issued = 0;
+        uint32_t kg = 0;
         const int ntiles_b = (p.N + 127) / 128;
-        for (int kb = 0; kb < p.nk; kb++) {
-            const int s = kb % C::STAGES;
-            const uint32_t ph = (uint32_t)(kb / C::STAGES) & 1u;
-            if (!wait_or_abort(empty + s, ph ^ 1u, abort_flag)) {
-                record_timeout(p.status, abort_flag);
-                break;
-            }
+        const int64_t cpr = p.sf_chunks_per_row;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+            int m0, n0;
+            tile_coords<C::BN>(tile, tiles_m, tiles_n, m0, n0);
             uint32_t bytes = C::A_BYTES + C::B_BYTES;
             if (C::SF_CHUNKS) {
                 bytes += C::SFA_BYTES;
                 for (int j = 0; j < C::BN / 128; j++)
                     if ((n0 >> 7) + j < ntiles_b) bytes += C::SF_CHUNKS * 512;
             }
-            mbar_arrive_expect_tx(full + s, bytes);
-            tma_load_2d(smem + C::OFF_A + s * C::A_BYTES, &tmA, kb * BKB, m0, full + s);
-            tma_load_2d(smem + C::OFF_B + s * C::B_BYTES, &tmB, kb * BKB, n0, full + s);
-            if (C::SF_CHUNKS) {
-                const int64_t cpr = p.sf_chunks_per_row;
-                bulk_load(smem + C::OFF_SFA + s * C::SFA_BYTES,
-                          p.sfa + (((int64_t)(m0 >> 7) * cpr + (int64_t)kb * C::SF_CHUNKS) << 9), C::SFA_BYTES,
-                          full + s);
-                for (int j = 0; j < C::BN / 128; j++) {
-                    const int nt = (n0 >> 7) + j;
-                    if (nt < ntiles_b)
-                        bulk_load(smem + C::OFF_SFB + s * C::SFB_BYTES + j * C::SF_CHUNKS * 512,
-                                  p.sfb + (((int64_t)nt * cpr + (int64_t)kb * C::SF_CHUNKS) << 9),
-                                  C::SF_CHUNKS * 512, full + s);
-                }
-            }
-            issued = kb + 1;
-        }
-        misc[3] = (uint32_t)issued;
-    } else if (!skip && warp == 1 && lane == 0) {
-        // ------------------------------------------------ MMA issuer
-        constexpr uint32_t idesc = idesc_for<KIND>();
-        for (int kb = 0; kb < p.nk; kb++) {
-            const int s = kb % C::STAGES;
-            const uint32_t ph = (uint32_t)(kb / C::STAGES) & 1u;
-            if (!wait_or_abort(full + s, ph, abort_flag)) {
-                record_timeout(p.status, abort_flag);
-                break;
-            }
-            uint32_t d = tmem;
-            if (KIND == kFp8Block) {
-                const int b = kb & 1;
-                if (!wait_or_abort(pempty + b, ((uint32_t)(kb >> 1) & 1u) ^ 1u, abort_flag)) {
+            for (int kb = 0; kb < p.nk; kb++, kg++) {
+                const int s = (int)(kg % C::STAGES);
+                const uint32_t ph = (kg / C::STAGES) & 1u;
+                if (!wait_or_abort(empty + s, ph ^ 1u, abort_flag)) {
                     record_timeout(p.status, abort_flag);
-                    break;
-                }
-                d = tmem + (uint32_t)(b * C::BN);
-            }
-            tc_fence_after();
-            const uint32_t a_base = smem_u32(smem + C::OFF_A + s * C::A_BYTES);
-            const uint32_t b_base = smem_u32(smem + C::OFF_B + s * C::B_BYTES);
-            const uint32_t sfa_base = smem_u32(smem + C::OFF_SFA + s * C::SFA_BYTES);
-            const uint32_t sfb_base = smem_u32(smem + C::OFF_SFB + s * C::SFB_BYTES);
-            if (KIND == kMxfp8) {
-                tmem_cp_32x128b_x4(tmem + C::SFA_COL + s * C::SFA_COLS, sdesc_sf(sfa_base));
-#pragma unroll
-                for (int j = 0; j < C::BN / 128; j++)
-                    tmem_cp_32x128b_x4(tmem + C::SFB_COL + s * C::SFB_COLS + j * 4, sdesc_sf(sfb_base + j * 512));
-            }
-            if (KIND == kNvfp4) {
-#pragma unroll
-                for (int c = 0; c < 4; c++) {
-                    tmem_cp_32x128b_x4(tmem + C::SFA_COL + s * C::SFA_COLS + c * 4, sdesc_sf(sfa_base + c * 512));
-#pragma unroll
-                    for (int j = 0; j < C::BN / 128; j++)
-                        tmem_cp_32x128b_x4(tmem + C::SFB_COL + s * C::SFB_COLS + c * 4 * (C::BN / 128) + j * 4,
-                                           sdesc_sf(sfb_base + (j * 4 + c) * 512));
-                }
-            }
-#pragma unroll
-            for (int c = 0; c < C::KSTEPS; c++) {
-                const uint64_t ad = sdesc_sw128(a_base + c * 32);
-                const uint64_t bd = sdesc_sw128(b_base + c * 32);
-                const uint32_t acc = (KIND == kFp8Block) ? (c > 0) : (kb > 0 || c > 0);
-                if (KIND == kFp8Tensor || KIND == kFp8Block) {
-                    mma_f8f6f4(d, ad, bd, idesc, acc);
-                } else if (KIND == kMxfp8) {
-                    const uint32_t id = idesc | ((uint32_t)c << 4) | ((uint32_t)c << 29);
-                    mma_mxf8(d, ad, bd, id, tmem + C::SFA_COL + s * C::SFA_COLS,
-                             tmem + C::SFB_COL + s * C::SFB_COLS, acc);
-                } else {
-                    mma_nvf4(d, ad, bd, idesc, tmem + C::SFA_COL + s * C::SFA_COLS + c * 4,
-                             tmem + C::SFB_COL + s * C::SFB_COLS + c * 4 * (C::BN / 128), acc);
-                }
-            }
-            tc_commit(empty + s);
-            if (KIND == kFp8Block) tc_commit(pfull + (kb & 1));
-            misc[2] = (uint32_t)(kb + 1);
-        }
-        // Completes once every MMA issued above has finished (also after an abort).
-        if (KIND != kFp8Block) tc_commit(accf);
-    } else if (!skip && warp >= 2) {
-        // ------------------------------------------------ epilogue
-        const int q = warp & 3;                 // TMEM lane quadrant this warp may read
-        const int row = m0 + q * 32 + lane;
-        const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
-        if (KIND != kFp8Block) {
-            if (!warp_wait_or_abort(accf, 0, abort_flag)) {
-                if (lane == 0) record_timeout(p.status, abort_flag);
-            } else {
-                tc_fence_after();
-                float alpha = 1.0f;
-                if (KIND == kFp8Tensor) alpha = __fmul_rn(__ldg(p.x_scale), __ldg(p.w_scale));
-                if (KIND == kNvfp4) alpha = __fmul_rn(__ldg(p.x_global), __ldg(p.w_global));
-#pragma unroll 1
-                for (int c = 0; c < C::BN / 32; c++) {
-                    uint32_t r[32];
-                    tmem_ld_32x32b_x32(tmem + lane_addr + (uint32_t)(c * 32), r);
-                    tmem_ld_wait();
-                    const int n = n0 + c * 32;
-                    if (row < p.M && n < p.N) {
-                        float v[32];
-#pragma unroll
-                        for (int i = 0; i < 32; i++) v[i] = __uint_as_float(r[i]) * alpha;
-                        store_row32(p, row, n, v);
-                    }
-                }
-            }
-        } else {
-            const int h = (warp - 2) >> 2;      // which 128-column half of the tile
-            const int kblocks = p.K >> 7;
-            const int nt = (n0 >> 7) + h;
-            const bool col_ok = nt * 128 < p.N;
-            float acc[128];
-#pragma unroll
-            for (int i = 0; i < 128; i++) acc[i] = 0.0f;
-            bool ok = true;
-            for (int kb = 0; kb < p.nk; kb++) {
-                const int b = kb & 1;
-                if (!warp_wait_or_abort(pfull + b, (uint32_t)(kb >> 1) & 1u, abort_flag)) {
-                    if (lane == 0) record_timeout(p.status, abort_flag);
                     ok = false;
                     break;
                 }
-                tc_fence_after();
-                const float sw = col_ok ? __ldg(p.w_scale + (int64_t)nt * kblocks + kb) : 0.0f;
-#pragma unroll
-                for (int c = 0; c < 4; c++) {
-                    uint32_t r[32];
-                    tmem_ld_32x32b_x32(tmem + lane_addr + (uint32_t)(b * C::BN + h * 128 + c * 32), r);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int i = 0; i < 32; i++) acc[c * 32 + i] = fmaf(sw, __uint_as_float(r[i]), acc[c * 32 + i]);
+                mbar_arrive_expect_tx(full + s, bytes);
+                tma_load_2d(smem + C::OFF_A + s * C::A_BYTES, &tmA, kb * BKB, m0, full + s);
+                tma_load_2d(smem + C::OFF_B + s * C::B_BYTES, &tmB, kb * BKB, n0, full + s);
+                if (C::SF_CHUNKS) {
+                    bulk_load(smem + C::OFF_SFA + s * C::SFA_BYTES,
+                              p.sfa + (((int64_t)(m0 >> 7) * cpr + (int64_t)kb * C::SF_CHUNKS) << 9), C::SFA_BYTES,
+                              full + s);
+                    for (int j = 0; j < C::BN / 128; j++) {
+                        const int nt = (n0 >> 7) + j;
+                        if (nt < ntiles_b)
+                            bulk_load(smem + C::OFF_SFB + s * C::SFB_BYTES + j * C::SF_CHUNKS * 512,
+                                      p.sfb + (((int64_t)nt * cpr + (int64_t)kb * C::SF_CHUNKS) << 9),
+                                      C::SF_CHUNKS * 512, full + s);
+                    }
                 }
+                misc[3] = kg + 1;
+            }
+        }
+    } else if (!skip && warp == 1 && lane == 0) {
+        // ------------------------------------------------ MMA issuer
+        constexpr uint32_t idesc = idesc_for<KIND>();
+        uint32_t kg = 0, kbg = 0, it = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, it++) {
+            if (KIND != kFp8Block) {
+                if (!wait_or_abort(acce, (it & 1u) ^ 1u, abort_flag)) {
+                    record_timeout(p.status, abort_flag);
+                    break;
+                }
+            }
+            for (int kb = 0; kb < p.nk; kb++, kg++) {
+                const int s = (int)(kg % C::STAGES);
+                const uint32_t ph = (kg / C::STAGES) & 1u;
+                if (!wait_or_abort(full + s, ph, abort_flag)) {
+                    record_timeout(p.status, abort_flag);
+                    ok = false;
+                    break;
+                }
+                uint32_t d = tmem;
+                if (KIND == kFp8Block) {
+                    const int b = (int)(kbg & 1u);
+                    if (!wait_or_abort(pempty + b, ((kbg >> 1) & 1u) ^ 1u, abort_flag)) {
+                        record_timeout(p.status, abort_flag);
+                        ok = false;
+                        break;
+                    }
+                    d = tmem + (uint32_t)(b * C::BN);
+                }
+                tc_fence_after();
+                const uint32_t a_base = smem_u32(smem + C::OFF_A + s * C::A_BYTES);
+                const uint32_t b_base = smem_u32(smem + C::OFF_B + s * C::B_BYTES);
+                const uint32_t sfa_base = smem_u32(smem + C::OFF_SFA + s * C::SFA_BYTES);
+                const uint32_t sfb_base = smem_u32(smem + C::OFF_SFB + s * C::SFB_BYTES);
+                if (KIND == kMxfp8) {
+                    tmem_cp_32x128b_x4(tmem + C::SFA_COL + s * C::SFA_COLS, sdesc_sf(sfa_base));
+#pragma unroll
+                    for (int j = 0; j < C::BN / 128; j++)
+                        tmem_cp_32x128b_x4(tmem + C::SFB_COL + s * C::SFB_COLS + j * 4, sdesc_sf(sfb_base + j * 512));
+                }
+                if (KIND == kNvfp4) {
+#pragma unroll
+                    for (int c = 0; c < 4; c++) {
+                        tmem_cp_32x128b_x4(tmem + C::SFA_COL + s * C::SFA_COLS + c * 4, sdesc_sf(sfa_base + c * 512));
+#pragma unroll
+                        for (int j = 0; j < C::BN / 128; j++)
+                            tmem_cp_32x128b_x4(tmem + C::SFB_COL + s * C::SFB_COLS + c * 4 * (C::BN / 128) + j * 4,
+                                               sdesc_sf(sfb_base + (j * 4 + c) * 512));
+                    }
+                }
+#pragma unroll
+                for (int c = 0; c < C::KSTEPS; c++) {
+                    const uint64_t ad = sdesc_sw128(a_base + c * 32);
+                    const uint64_t bd = sdesc_sw128(b_base + c * 32);
+                    const uint32_t acc = (KIND == kFp8Block) ? (c > 0) : (kb > 0 || c > 0);
+                    if (KIND == kFp8Tensor || KIND == kFp8Block) {
+                        mma_f8f6f4(d, ad, bd, idesc, acc);
+                    } else if (KIND == kMxfp8) {
+                        const uint32_t id = idesc | ((uint32_t)c << 4) | ((uint32_t)c << 29);
+                        mma_mxf8(d, ad, bd, id, tmem + C::SFA_COL + s * C::SFA_COLS,
+                                 tmem + C::SFB_COL + s * C::SFB_COLS, acc);
+                    } else {
+                        mma_nvf4(d, ad, bd, idesc, tmem + C::SFA_COL + s * C::SFA_COLS + c * 4,
+                                 tmem + C::SFB_COL + s * C::SFB_COLS + c * 4 * (C::BN / 128), acc);
+                    }
+                }
+                tc_commit(empty + s);
+                if (KIND == kFp8Block) {
+                    tc_commit(pfull + (kbg & 1u));
+                    kbg++;
+                }
+                misc[2] = kg + 1;
+            }
+            if (ok && KIND != kFp8Block) tc_commit(accf);
+        }
+    } else if (!skip && warp >= 2) {
+        // ------------------------------------------------ epilogue (8 warps)
+        const int q = warp & 3;                 // TMEM lane quadrant this warp may read
+        const int h = (warp - 2) >> 2;          // which 128-column half of the tile
+        const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
+        float alpha = 1.0f;
+        if (KIND == kFp8Tensor) alpha = __fmul_rn(__ldg(p.x_scale), __ldg(p.w_scale));
+        if (KIND == kNvfp4) alpha = __fmul_rn(__ldg(p.x_global), __ldg(p.w_global));
+        uint32_t it = 0, kbg = 0;
+        for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, it++) {
+            int m0, n0;
+            tile_coords<C::BN>(tile, tiles_m, tiles_n, m0, n0);
+            const int row = m0 + q * 32 + lane;
+            const int ncol = n0 + h * 128;
+            bool ok = true;
+            if (KIND != kFp8Block) {
+                if (!warp_wait_or_abort(accf, it & 1u, abort_flag)) {
+                    if (lane == 0) record_timeout(p.status, abort_flag);
+                    break;
+                }
+                tc_fence_after();
+                uint32_t r[4][32];
+#pragma unroll
+                for (int c = 0; c < 4; c++)
+                    tmem_ld_32x32b_x32(tmem + lane_addr + (uint32_t)(h * 128 + c * 32), r[c]);
+                tmem_ld_wait();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(pempty + b);
-            }
-            if (ok && row < p.M && col_ok) {
-                const float sx = __ldg(p.x_scale + row);
+                if (lane == 0) mbar_arrive(acce);     // the MMA may start the next tile
+                if (row < p.M) {
 #pragma unroll
-                for (int c = 0; c < 4; c++) {
-                    float v[32];
+                    for (int c = 0; c < 4; c++) {
+                        if (ncol + c * 32 < p.N) {
+                            float v[32];
 #pragma unroll
-                    for (int i = 0; i < 32; i++) v[i] = acc[c * 32 + i] * sx;
-                    store_row32(p, row, n0 + h * 128 + c * 32, v);
+                            for (int i = 0; i < 32; i++) v[i] = __uint_as_float(r[c][i]) * alpha;
+                            store_row32(p, row, ncol + c * 32, v);
+                        }
+                    }
+                }
+            } else {
+                const int nt = ncol >> 7;
+                const bool col_ok = ncol < p.N;
+                const int kblocks = p.K >> 7;
+                const float sx = (row < p.M) ? __ldg(p.x_scale + row) : 0.0f;
+                // this half-tile's weight-block scales, 32 per register, fetched by shuffle
+                float sreg[4];
+                float acc[128];
+#pragma unroll
+                for (int i = 0; i < 128; i++) acc[i] = 0.0f;
+                for (int kb = 0; kb < p.nk; kb++, kbg++) {
+                    if ((kb & 127) == 0) {
+#pragma unroll
+                        for (int j = 0; j < 4; j++) {
+                            const int kk = kb + j * 32 + lane;
+                            sreg[j] = (col_ok && kk < kblocks) ? __ldg(p.w_scale + (int64_t)nt * kblocks + kk) : 0.0f;
+                        }
+                    }
+                    const int b = (int)(kbg & 1u);
+                    if (!warp_wait_or_abort(pfull + b, (kbg >> 1) & 1u, abort_flag)) {
+                        if (lane == 0) record_timeout(p.status, abort_flag);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const int kr = kb & 127;
+                    float sw = __shfl_sync(0xFFFFFFFFu, sreg[0], kr & 31);
+                    const float sw1 = __shfl_sync(0xFFFFFFFFu, sreg[1], kr & 31);
+                    const float sw2 = __shfl_sync(0xFFFFFFFFu, sreg[2], kr & 31);
+                    const float sw3 = __shfl_sync(0xFFFFFFFFu, sreg[3], kr & 31);
+                    sw = (kr < 32) ? sw : (kr < 64) ? sw1 : (kr < 96) ? sw2 : sw3;
+#pragma unroll
+                    for (int c = 0; c < 8; c++) {
+                        uint32_t r[16];
+                        tmem_ld_32x32b_x16(tmem + lane_addr + (uint32_t)(b * C::BN + h * 128 + c * 16), r);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 16; i++) acc[c * 16 + i] = fmaf(sw, __uint_as_float(r[i]), acc[c * 16 + i]);
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(pempty + b);
+                }
+                if (!ok) break;
+                if (row < p.M && col_ok) {
+#pragma unroll
+                    for (int c = 0; c < 4; c++) {
+                        if (ncol + c * 32 < p.N) {
+                            float v[32];
+#pragma unroll
+                            for (int i = 0; i < 32; i++) v[i] = acc[c * 32 + i] * sx;
+                            store_row32(p, row, ncol + c * 32, v);
+                        }
+                    }
                 }
             }
         }
@@ -381,11 +453,9 @@ __global__ void __launch_bounds__(Cfg<KIND>::THREADS, 1)
     if (*abort_flag && warp == 0 && lane == 0) {
         // Let every TMA copy this CTA issued land before its shared memory is
         // released: wait (bounded) on the stages issued but not consumed.
-        const int issued = (int)misc[3], consumed = (int)misc[2];
-        for (int kb = consumed; kb < issued; kb++) {
-            uint64_t* bar = full + (kb % C::STAGES);
-            mbar_wait(bar, (uint32_t)(kb / C::STAGES) & 1u, kWaitLimitNs);
-        }
+        const uint32_t issued = misc[3], consumed = misc[2];
+        for (uint32_t kg = consumed; kg < issued; kg++)
+            mbar_wait(full + (kg % C::STAGES), (kg / C::STAGES) & 1u, kWaitLimitNs);
     }
     if (*abort_flag && warp == 1 && lane == 0) {
         // ... and every MMA / scale copy it issued has finished reading
@@ -402,6 +472,19 @@ __global__ void __launch_bounds__(Cfg<KIND>::THREADS, 1)
 }
 
 // ---------------------------------------------------------------- host side
+int num_sms() {
+    static int n = 0;
+    if (!n) {
+        int dev = 0, v = 0;
+        if (cudaGetDevice(&dev) == cudaSuccess &&
+            cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
+            n = v;
+        else
+            n = kNumSMs;
+    }
+    return n;
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     if (!fn) {
@@ -460,7 +543,8 @@ cudaError_t launch_tc(const GemmArgs& a, cudaStream_t st) {
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    dim3 grid((unsigned)((a.N + C::BN - 1) / C::BN), (unsigned)((a.M + BM - 1) / BM));
+    const int64_t ntiles = ((a.N + C::BN - 1) / C::BN) * ((a.M + BM - 1) / BM);
+    const int grid = (int)(ntiles < num_sms() ? ntiles : num_sms());   // persistent: one CTA per SM
     k_gemm_tc<KIND><<<grid, C::THREADS, C::SMEM, st>>>(tmA, tmB, p);
     return cudaGetLastError();
 }

@@ -7,17 +7,21 @@
 //
 // Decode has few tokens, so the output channels take the MMA's M side
 // ("swap AB"): a CTA owns 128 channels and MP tokens (MP = 16, 32, 64 or 128,
-// zero-filled past M by TMA).  Per 64-K sub-tile:
-//   warp 0    TMA: the packed int4 words (8 k-octets x 128 channels) and the
-//             X tile (MP x 64 bf16, 128-byte swizzle);
+// zero-filled past M by TMA).  Per 128-K group:
+//   warp 0    TMA: the packed int4 words (16 k-octets x 128 channels, 8 KB)
+//             into a deep ring, so that enough HBM reads are in flight;
+//   warp 10   TMA: the X tile (MP x 128 bf16, two 128-byte-swizzled boxes)
+//             into its own ring (X is re-read by every CTA and sits in L2);
 //   warps 2-5 dequantize each word into exact bf16 (q - z) values (small
 //             integers, so no rounding) and store them in the 128-byte
-//             swizzled K-major layout the MMA reads;
+//             swizzled K-major layout the MMA reads; the zero points of 32
+//             groups are prefetched into registers;
 //   warp 1    one lane issues tcgen05.mma kind::f16 into one of two TMEM
 //             partial buffers per 128-K group;
-//   warps 6-9 multiply each group's partial by its fp32-converted bf16 scale
-//             and accumulate in registers (the scale varies per group and
-//             channel, so it cannot be folded into either operand exactly).
+//   warps 6-9 multiply each group's partial by its bf16 scale (32 groups
+//             prefetched into registers) and accumulate in registers (the
+//             scale varies per group and channel, so it cannot be folded
+//             into either operand exactly).
 // Split-K: the CTAs of one thread-block cluster share an output tile and
 // each take a contiguous range of groups; their fp32 partial tiles are summed
 // through distributed shared memory, so the kernel needs no global scratch.
@@ -35,19 +39,22 @@ namespace {
 using namespace ptx;
 
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
-constexpr int SQ = 8;            // TMA stages (one 64-K sub-tile each)
-constexpr int SA = 4;            // dequantized A buffers
-constexpr int QW_BYTES = 8 * 128 * 4;      // 8 k-octets x 128 channels int32
-constexpr int A_BYTES = 128 * 128;         // 128 channels x 64 bf16
+constexpr int QW_BYTES = 16 * 128 * 4;     // one 128-K group: 16 k-octets x 128 channels int32
+constexpr int A_BYTES = 2 * 128 * 128;     // one group dequantized: two 64-K sub-tiles of 128 x 64 bf16
+constexpr int SA = 2;                      // dequantized groups in flight
+constexpr int CHUNK = 32;                  // groups whose zero points / scales sit in registers
 
 template <int MP>
 struct W4Cfg {
-    static constexpr int X_BYTES = MP * 128;
-    static constexpr int OFF_A = 0;                                  // SA x 16 KB (reused for the reduction)
-    static constexpr int OFF_X = OFF_A + SA * A_BYTES;               // SQ x X tiles (1024-aligned sizes)
-    static constexpr int OFF_QW = OFF_X + SQ * X_BYTES;              // SQ x 4 KB
-    static constexpr int OFF_BAR = OFF_QW + SQ * QW_BYTES;
-    static constexpr int NBAR = 2 * SQ + 2 * SA + 5;                 // qfull, qempty, afull, aempty, pfull[2], pempty[2], drain
+    static constexpr int XSUB = MP * 128;                           // one 64-K X sub-tile
+    static constexpr int X_BYTES = 2 * XSUB;                        // one group of X
+    static constexpr int XS = (MP <= 16) ? 8 : (MP <= 64 ? 4 : 2);  // X ring depth (groups)
+    static constexpr int QS = (MP <= 32) ? 14 : (MP == 64 ? 10 : 6);// weight ring depth (groups)
+    static constexpr int OFF_A = 0;                                  // SA groups (reused for the reduction)
+    static constexpr int OFF_X = OFF_A + SA * A_BYTES;
+    static constexpr int OFF_QW = OFF_X + XS * X_BYTES;
+    static constexpr int OFF_BAR = OFF_QW + QS * QW_BYTES;
+    static constexpr int NBAR = 2 * QS + 2 * XS + 2 * SA + 5;        // q/x/a full+empty, pfull[2], pempty[2], drain
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int SMEM = OFF_MISC + 64 + 1024;
     static constexpr uint32_t TMEM_COLS = (2 * MP < 32) ? 32 : 2 * MP;
@@ -91,16 +98,6 @@ __device__ __forceinline__ void record_timeout(int* status, volatile uint32_t* a
     if (status) atomicExch(status, (int)QLIN_ERR_DEVICE_TIMEOUT);
 }
 
-__device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[16]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr)
-        : "memory");
-}
-
 // Generic-proxy smem writes -> visible to the tensor core's async proxy.
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -139,20 +136,48 @@ __device__ __forceinline__ uint4 dequant8(uint32_t w, __nv_bfloat162 bias2) {
     return make_uint4(h[0], h[1], h[2], h[3]);
 }
 
+// Zero points of this thread's channel for CHUNK groups starting at g:
+// eight 4-bit values per register.
+__device__ __forceinline__ void load_zero_chunk(const W4Params& p, int ng, int g, int g_end, uint32_t (&zr)[4]) {
+#pragma unroll
+    for (int j = 0; j < 4; j++) zr[j] = 0;
+    if (ng >= p.N) return;
+#pragma unroll
+    for (int i = 0; i < CHUNK; i++) {
+        if (g + i < g_end) {
+            const uint32_t w = (uint32_t)__ldg(p.qzeros + (int64_t)(g + i) * (p.N >> 3) + (ng >> 3));
+            zr[i >> 3] |= ((w >> (4 * (ng & 7))) & 0xFu) << (4 * (i & 7));
+        }
+    }
+}
+
+// bf16 scales of this thread's channel for CHUNK groups starting at g, two per register.
+__device__ __forceinline__ void load_scale_chunk(const W4Params& p, int ng, int g, int g_end, uint32_t (&sr)[16]) {
+#pragma unroll
+    for (int j = 0; j < 16; j++) sr[j] = 0;
+    if (ng >= p.N) return;
+#pragma unroll
+    for (int i = 0; i < CHUNK; i++)
+        if (g + i < g_end) sr[i >> 1] |= (uint32_t)__ldg(p.scales + (int64_t)(g + i) * p.N + ng) << (16 * (i & 1));
+}
+
 template <int MP>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(352, 1)
     k_w4a16(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmX, const W4Params p) {
     using C = W4Cfg<MP>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* qfull = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
-    uint64_t* qempty = qfull + SQ;
-    uint64_t* afull = qempty + SQ;
+    uint64_t* qempty = qfull + C::QS;
+    uint64_t* xfull = qempty + C::QS;
+    uint64_t* xempty = xfull + C::XS;
+    uint64_t* afull = xempty + C::XS;
     uint64_t* aempty = afull + SA;
     uint64_t* pfull = aempty + SA;
     uint64_t* pempty = pfull + 2;
     uint64_t* drain = pempty + 2;
-    uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);   // tmem, abort, consumed, issued
+    // tmem, abort, MMA-consumed groups, weight groups issued, X groups issued, dequant-consumed groups
+    uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
     volatile uint32_t* abort_flag = misc + 1;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -160,12 +185,16 @@ __global__ void __launch_bounds__(320, 1)
     const int rank = (int)cluster_rank();
     const int n0 = blockIdx.y * 128, m0 = blockIdx.z * MP;
     const int g0 = (int)((int64_t)p.groups * rank / cs), g1 = (int)((int64_t)p.groups * (rank + 1) / cs);
-    const int nsub = 2 * (g1 - g0);                // 64-K sub-tiles of this CTA
+    const int ng_cta = g1 - g0;                    // 128-K groups of this CTA
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < SQ; s++) {
+        for (int s = 0; s < C::QS; s++) {
             mbar_init(qfull + s, 1);
-            mbar_init(qempty + s, 4 + 1);         // four dequant warps + the MMA commit
+            mbar_init(qempty + s, 4);             // the four dequant warps
+        }
+        for (int s = 0; s < C::XS; s++) {
+            mbar_init(xfull + s, 1);
+            mbar_init(xempty + s, 1);             // the MMA commit
         }
         for (int s = 0; s < SA; s++) {
             mbar_init(afull + s, 4);
@@ -178,8 +207,7 @@ __global__ void __launch_bounds__(320, 1)
         mbar_init(drain, 1);
         fence_mbar_init();
         misc[1] = (p.status && *reinterpret_cast<volatile int*>(p.status) != 0) ? 1u : 0u;
-        misc[2] = 0;
-        misc[3] = 0;
+        for (int i = 2; i < 6; i++) misc[i] = 0;
         prefetch_tmap(&tmQ);
         prefetch_tmap(&tmX);
     }
@@ -196,42 +224,54 @@ __global__ void __launch_bounds__(320, 1)
     bool epi_ok = false;
 
     if (!skip && warp == 0 && lane == 0) {
-        // ------------------------------------------------ producer
-        int issued = 0;
-        for (int t = 0; t < nsub; t++) {
-            const int s = t % SQ;
-            if (!wait_or_abort(qempty + s, ((uint32_t)(t / SQ) & 1u) ^ 1u, abort_flag)) {
+        // ------------------------------------------------ weight producer (HBM stream)
+        for (int t = 0; t < ng_cta; t++) {
+            const int s = t % C::QS;
+            if (!wait_or_abort(qempty + s, ((uint32_t)(t / C::QS) & 1u) ^ 1u, abort_flag)) {
                 record_timeout(p.status, abort_flag);
                 break;
             }
-            const int k = g0 * 128 + t * 64;
-            mbar_arrive_expect_tx(qfull + s, QW_BYTES + C::X_BYTES);
-            tma_load_2d(smem + C::OFF_QW + s * QW_BYTES, &tmQ, n0, k / 8, qfull + s);
-            tma_load_2d(smem + C::OFF_X + s * C::X_BYTES, &tmX, k, m0, qfull + s);
-            issued = t + 1;
+            mbar_arrive_expect_tx(qfull + s, QW_BYTES);
+            tma_load_2d(smem + C::OFF_QW + s * QW_BYTES, &tmQ, n0, (g0 + t) * 16, qfull + s);
+            misc[3] = (uint32_t)(t + 1);
         }
-        misc[3] = (uint32_t)issued;
+    } else if (!skip && warp == 10 && lane == 0) {
+        // ------------------------------------------------ activation producer (L2)
+        for (int t = 0; t < ng_cta; t++) {
+            const int s = t % C::XS;
+            if (!wait_or_abort(xempty + s, ((uint32_t)(t / C::XS) & 1u) ^ 1u, abort_flag)) {
+                record_timeout(p.status, abort_flag);
+                break;
+            }
+            const int k = (g0 + t) * 128;
+            mbar_arrive_expect_tx(xfull + s, C::X_BYTES);
+            tma_load_2d(smem + C::OFF_X + s * C::X_BYTES, &tmX, k, m0, xfull + s);
+            tma_load_2d(smem + C::OFF_X + s * C::X_BYTES + C::XSUB, &tmX, k + 64, m0, xfull + s);
+            misc[4] = (uint32_t)(t + 1);
+        }
     } else if (!skip && warp == 1 && lane == 0) {
         // ------------------------------------------------ MMA issuer
-        for (int t = 0; t < nsub; t++) {
-            const int s = t % SQ, sa = t % SA, b = (t >> 1) & 1;
-            if (!wait_or_abort(qfull + s, (uint32_t)(t / SQ) & 1u, abort_flag) ||
+        for (int t = 0; t < ng_cta; t++) {
+            const int sx = t % C::XS, sa = t % SA, b = t & 1;
+            if (!wait_or_abort(xfull + sx, (uint32_t)(t / C::XS) & 1u, abort_flag) ||
                 !wait_or_abort(afull + sa, (uint32_t)(t / SA) & 1u, abort_flag) ||
-                ((t & 1) == 0 && !wait_or_abort(pempty + b, ((uint32_t)(t >> 2) & 1u) ^ 1u, abort_flag))) {
+                !wait_or_abort(pempty + b, ((uint32_t)(t >> 1) & 1u) ^ 1u, abort_flag)) {
                 record_timeout(p.status, abort_flag);
                 break;
             }
             tc_fence_after();
             const uint32_t a_base = smem_u32(smem + C::OFF_A + sa * A_BYTES);
-            const uint32_t x_base = smem_u32(smem + C::OFF_X + s * C::X_BYTES);
+            const uint32_t x_base = smem_u32(smem + C::OFF_X + sx * C::X_BYTES);
             const uint32_t d = tmem + (uint32_t)(b * MP);
 #pragma unroll
-            for (int c = 0; c < 4; c++)
-                mma_f16(d, sdesc_sw128(a_base + c * 32), sdesc_sw128(x_base + c * 32), C::IDESC,
-                        ((t & 1) || c > 0) ? 1u : 0u);
+            for (int j = 0; j < 2; j++)
+#pragma unroll
+                for (int c = 0; c < 4; c++)
+                    mma_f16(d, sdesc_sw128(a_base + j * (A_BYTES / 2) + c * 32),
+                            sdesc_sw128(x_base + j * C::XSUB + c * 32), C::IDESC, (j > 0 || c > 0) ? 1u : 0u);
             tc_commit(aempty + sa);
-            tc_commit(qempty + s);
-            if (t & 1) tc_commit(pfull + b);
+            tc_commit(xempty + sx);
+            tc_commit(pfull + b);
             misc[2] = (uint32_t)(t + 1);
         }
     } else if (!skip && warp >= 2 && warp < 6) {
@@ -239,25 +279,31 @@ __global__ void __launch_bounds__(320, 1)
         const int n = threadIdx.x - 64;            // channel within the tile (0..127)
         const int ng = n0 + n;
         uint8_t* const a_ring = smem + C::OFF_A;
-        for (int t = 0; t < nsub; t++) {
-            const int s = t % SQ, sa = t % SA;
-            if (!warp_wait(qfull + s, (uint32_t)(t / SQ) & 1u, abort_flag) ||
+        uint32_t zr[4];
+        load_zero_chunk(p, ng, g0, g1, zr);
+        for (int t = 0; t < ng_cta; t++) {
+            const int s = t % C::QS, sa = t % SA;
+            if ((t % CHUNK) == 0 && t > 0) load_zero_chunk(p, ng, g0 + t, g1, zr);
+            if (!warp_wait(qfull + s, (uint32_t)(t / C::QS) & 1u, abort_flag) ||
                 !warp_wait(aempty + sa, ((uint32_t)(t / SA) & 1u) ^ 1u, abort_flag)) {
                 if (lane == 0) record_timeout(p.status, abort_flag);
                 break;
             }
-            const int g = g0 + (t >> 1);
-            uint32_t z = 0;
-            if (ng < p.N) z = ((uint32_t)__ldg(p.qzeros + (int64_t)g * (p.N >> 3) + (ng >> 3)) >> (4 * (ng & 7))) & 0xFu;
-            const uint32_t zb = 0x4300u | z;
+            const int ti = t % CHUNK;
+            uint32_t zw = zr[0];
+#pragma unroll
+            for (int j = 1; j < 4; j++)
+                if ((ti >> 3) == j) zw = zr[j];
+            const uint32_t zb = 0x4300u | ((zw >> (4 * (ti & 7))) & 0xFu);
             __nv_bfloat162 bias2;
             *reinterpret_cast<uint32_t*>(&bias2) = zb | (zb << 16);
             const uint32_t* qw = reinterpret_cast<const uint32_t*>(smem + C::OFF_QW + s * QW_BYTES);
             uint8_t* arow = a_ring + sa * A_BYTES + n * 128;
 #pragma unroll
-            for (int o = 0; o < 8; o++) {
+            for (int o = 0; o < 16; o++) {
                 const uint32_t w = qw[o * 128 + n];
-                *reinterpret_cast<uint4*>(arow + ((o ^ (n & 7)) << 4)) = dequant8(w, bias2);
+                *reinterpret_cast<uint4*>(arow + (o >> 3) * (A_BYTES / 2) + (((o & 7) ^ (n & 7)) << 4)) =
+                    dequant8(w, bias2);
             }
             fence_proxy_async_smem();
             __syncwarp();
@@ -265,25 +311,32 @@ __global__ void __launch_bounds__(320, 1)
                 mbar_arrive(afull + sa);
                 mbar_arrive(qempty + s);
             }
+            if (threadIdx.x == 64) misc[5] = (uint32_t)(t + 1);
         }
-    } else if (!skip && warp >= 6) {
+    } else if (!skip && warp >= 6 && warp < 10) {
         // ------------------------------------------------ epilogue (scale promotion)
         const int q = warp & 3;
         const int n = q * 32 + lane;
         const int ng = n0 + n;
         const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
+        uint32_t sr[16];
+        load_scale_chunk(p, ng, g0, g1, sr);
         epi_ok = true;
-        for (int gi = 0; gi < g1 - g0; gi++) {
+        for (int gi = 0; gi < ng_cta; gi++) {
             const int b = gi & 1;
+            if ((gi % CHUNK) == 0 && gi > 0) load_scale_chunk(p, ng, g0 + gi, g1, sr);
             if (!warp_wait(pfull + b, (uint32_t)(gi >> 1) & 1u, abort_flag)) {
                 if (lane == 0) record_timeout(p.status, abort_flag);
                 epi_ok = false;
                 break;
             }
             tc_fence_after();
-            const float sc = (ng < p.N)
-                                 ? __bfloat162float(__ushort_as_bfloat16(__ldg(p.scales + (int64_t)(g0 + gi) * p.N + ng)))
-                                 : 0.0f;
+            const int ti = gi % CHUNK;
+            uint32_t sw = sr[0];
+#pragma unroll
+            for (int j = 1; j < 16; j++)
+                if ((ti >> 1) == j) sw = sr[j];
+            const float sc = __uint_as_float((ti & 1) ? (sw & 0xFFFF0000u) : (sw << 16));
 #pragma unroll
             for (int c = 0; c < MP / 16; c++) {
                 uint32_t r[16];
@@ -302,8 +355,11 @@ __global__ void __launch_bounds__(320, 1)
     tc_fence_before();
     __syncthreads();
     if (*abort_flag && warp == 0 && lane == 0) {
-        const int issued = (int)misc[3], consumed = (int)misc[2];
-        for (int t = consumed; t < issued; t++) mbar_wait(qfull + (t % SQ), (uint32_t)(t / SQ) & 1u, kWaitLimitNs);
+        // every TMA copy this CTA issued must land before its shared memory goes
+        for (uint32_t t = misc[5]; t < misc[3]; t++)
+            mbar_wait(qfull + (t % C::QS), (t / C::QS) & 1u, kWaitLimitNs);
+        for (uint32_t t = misc[2]; t < misc[4]; t++)
+            mbar_wait(xfull + (t % C::XS), (t / C::XS) & 1u, kWaitLimitNs);
     }
     if (*abort_flag && warp == 1 && lane == 0) {
         tc_commit(drain);
@@ -315,7 +371,7 @@ __global__ void __launch_bounds__(320, 1)
     const bool ok = !*abort_flag;
     float* red = reinterpret_cast<float*>(smem + C::OFF_A);    // [MP][128] fp32, reuses the A ring
     if (cs == 1) {
-        if (warp >= 6 && epi_ok && ok) {
+        if (warp >= 6 && warp < 10 && epi_ok && ok) {
             const int ng = n0 + (warp & 3) * 32 + lane;
             if (ng < p.N) {
 #pragma unroll
@@ -325,7 +381,7 @@ __global__ void __launch_bounds__(320, 1)
             }
         }
     } else {
-        if (warp >= 6) {
+        if (warp >= 6 && warp < 10) {
             const int n = (warp & 3) * 32 + lane;
 #pragma unroll
             for (int m = 0; m < MP; m++) red[m * 128 + n] = (epi_ok && ok) ? acc[m] : 0.0f;
@@ -386,7 +442,7 @@ cudaError_t launch_mp(const GemmArgs& a, cudaStream_t st) {
     {
         cuuint64_t dims[2] = {(cuuint64_t)a.N, (cuuint64_t)(a.K / 8)};
         cuuint64_t strides[1] = {(cuuint64_t)a.N * 4};
-        cuuint32_t box[2] = {128, 8};
+        cuuint32_t box[2] = {128, 16};
         cuuint32_t estr[2] = {1, 1};
         if (fn(&tmQ, CU_TENSOR_MAP_DATA_TYPE_INT32, 2, const_cast<void*>(a.w), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -424,7 +480,7 @@ cudaError_t launch_mp(const GemmArgs& a, cudaStream_t st) {
     const int cs = pick_split(ntiles * mtiles, p.groups);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)cs, (unsigned)ntiles, (unsigned)mtiles);
-    cfg.blockDim = dim3(320);
+    cfg.blockDim = dim3(352);
     cfg.dynamicSmemBytes = C::SMEM;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
