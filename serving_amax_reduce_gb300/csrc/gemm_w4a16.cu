@@ -6,20 +6,21 @@
 //   Y[m, n] = sum_g s[g, n] * sum_{k in g} x[m, k] * (q[k, n] - z[g, n])
 //
 // Decode has few tokens, so the output channels take the MMA's M side
-// ("swap AB"): a CTA owns 128 channels and MP tokens (MP = 16, 32, 64 or 128,
-// zero-filled past M by TMA).  Per 128-K group:
+// ("swap AB"): a CTA owns 128 channels and MP tokens (MP = 16, 32 or 64,
+// zero-filled past M by TMA; larger M runs as several token tiles).
+// Per 128-K group:
 //   warp 0    TMA: the packed int4 words (16 k-octets x 128 channels, 8 KB)
 //             into a deep ring, so that enough HBM reads are in flight;
-//   warp 10   TMA: the X tile (MP x 128 bf16, two 128-byte-swizzled boxes)
+//   warp 14   TMA: the X tile (MP x 128 bf16, two 128-byte-swizzled boxes)
 //             into its own ring (X is re-read by every CTA and sits in L2);
-//   warps 2-5 dequantize each word into exact bf16 (q - z) values (small
+//   warps 2-9 dequantize each word into exact bf16 (q - z) values (small
 //             integers, so no rounding) and store them in the 128-byte
-//             swizzled K-major layout the MMA reads; the zero points of 32
-//             groups are prefetched into registers;
-//   warp 1    one lane issues tcgen05.mma kind::f16 into one of two TMEM
+//             swizzled K-major layout the MMA reads, three groups deep; the
+//             zero points of 32 groups are staged in shared memory;
+//   warp 1    one lane issues tcgen05.mma kind::f16 into one of four TMEM
 //             partial buffers per 128-K group;
-//   warps 6-9 multiply each group's partial by its bf16 scale (32 groups
-//             prefetched into registers) and accumulate in registers (the
+//   warps 10-13 multiply each group's partial by its bf16 scale (32 groups
+//             staged in shared memory) and accumulate in registers (the
 //             scale varies per group and channel, so it cannot be folded
 //             into either operand exactly).
 // Split-K: the CTAs of one thread-block cluster share an output tile and
@@ -41,23 +42,27 @@ using namespace ptx;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 constexpr int QW_BYTES = 16 * 128 * 4;     // one 128-K group: 16 k-octets x 128 channels int32
 constexpr int A_BYTES = 2 * 128 * 128;     // one group dequantized: two 64-K sub-tiles of 128 x 64 bf16
-constexpr int SA = 2;                      // dequantized groups in flight
-constexpr int CHUNK = 32;                  // groups whose zero points / scales sit in registers
+constexpr int CHUNK = 32;                  // groups whose zero points / scales are staged at a time
+constexpr int NP = 4;                      // TMEM partial buffers (groups the MMA may run ahead)
+constexpr int THREADS = 480;               // 15 warps, see the role map in k_w4a16
 
 template <int MP>
 struct W4Cfg {
     static constexpr int XSUB = MP * 128;                           // one 64-K X sub-tile
     static constexpr int X_BYTES = 2 * XSUB;                        // one group of X
-    static constexpr int XS = (MP <= 16) ? 8 : (MP <= 64 ? 4 : 2);  // X ring depth (groups)
-    static constexpr int QS = (MP <= 32) ? 14 : (MP == 64 ? 10 : 6);// weight ring depth (groups)
+    static constexpr int SA = 3;                                    // dequantized groups in flight
+    static constexpr int XS = (MP <= 32) ? 4 : 3;                   // X ring depth (groups)
+    static constexpr int QS = (MP <= 32) ? 9 : 7;                   // weight ring depth (groups)
     static constexpr int OFF_A = 0;                                  // SA groups (reused for the reduction)
     static constexpr int OFF_X = OFF_A + SA * A_BYTES;
     static constexpr int OFF_QW = OFF_X + XS * X_BYTES;
-    static constexpr int OFF_BAR = OFF_QW + QS * QW_BYTES;
-    static constexpr int NBAR = 2 * QS + 2 * XS + 2 * SA + 5;        // q/x/a full+empty, pfull[2], pempty[2], drain
+    static constexpr int OFF_ZT = OFF_QW + QS * QW_BYTES;           // zero points [CHUNK][256] bytes
+    static constexpr int OFF_ST = OFF_ZT + CHUNK * 256;             // scales [CHUNK][128] floats
+    static constexpr int OFF_BAR = OFF_ST + CHUNK * 128 * 4;
+    static constexpr int NBAR = 2 * QS + 2 * XS + 2 * SA + 2 * NP + 1;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int SMEM = OFF_MISC + 64 + 1024;
-    static constexpr uint32_t TMEM_COLS = (2 * MP < 32) ? 32 : 2 * MP;
+    static constexpr uint32_t TMEM_COLS = (NP * MP < 32) ? 32 : NP * MP;
     static constexpr int RED_BYTES = MP * 128 * 4;
     static_assert(RED_BYTES <= SA * A_BYTES, "reduction tile must fit in the A ring");
     static_assert(SMEM <= 232448, "shared memory budget");
@@ -136,34 +141,12 @@ __device__ __forceinline__ uint4 dequant8(uint32_t w, __nv_bfloat162 bias2) {
     return make_uint4(h[0], h[1], h[2], h[3]);
 }
 
-// Zero points of this thread's channel for CHUNK groups starting at g:
-// eight 4-bit values per register.
-__device__ __forceinline__ void load_zero_chunk(const W4Params& p, int ng, int g, int g_end, uint32_t (&zr)[4]) {
-#pragma unroll
-    for (int j = 0; j < 4; j++) zr[j] = 0;
-    if (ng >= p.N) return;
-#pragma unroll
-    for (int i = 0; i < CHUNK; i++) {
-        if (g + i < g_end) {
-            const uint32_t w = (uint32_t)__ldg(p.qzeros + (int64_t)(g + i) * (p.N >> 3) + (ng >> 3));
-            zr[i >> 3] |= ((w >> (4 * (ng & 7))) & 0xFu) << (4 * (i & 7));
-        }
-    }
-}
-
-// bf16 scales of this thread's channel for CHUNK groups starting at g, two per register.
-__device__ __forceinline__ void load_scale_chunk(const W4Params& p, int ng, int g, int g_end, uint32_t (&sr)[16]) {
-#pragma unroll
-    for (int j = 0; j < 16; j++) sr[j] = 0;
-    if (ng >= p.N) return;
-#pragma unroll
-    for (int i = 0; i < CHUNK; i++)
-        if (g + i < g_end) sr[i >> 1] |= (uint32_t)__ldg(p.scales + (int64_t)(g + i) * p.N + ng) << (16 * (i & 1));
-}
-
 template <int MP>
-__global__ void __launch_bounds__(352, 1)
+__global__ void __launch_bounds__(THREADS, 1)
     k_w4a16(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmX, const W4Params p) {
+    // Role map: warp 0 weight TMA, warp 1 MMA (and TMEM owner), warps 2-9
+    // dequantize (thread d: channel d % 128, sub-tile d / 128 of each group),
+    // warps 10-13 epilogue (TMEM lane quadrant = warp % 4), warp 14 X TMA.
     using C = W4Cfg<MP>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -172,10 +155,10 @@ __global__ void __launch_bounds__(352, 1)
     uint64_t* xfull = qempty + C::QS;
     uint64_t* xempty = xfull + C::XS;
     uint64_t* afull = xempty + C::XS;
-    uint64_t* aempty = afull + SA;
-    uint64_t* pfull = aempty + SA;
-    uint64_t* pempty = pfull + 2;
-    uint64_t* drain = pempty + 2;
+    uint64_t* aempty = afull + C::SA;
+    uint64_t* pfull = aempty + C::SA;
+    uint64_t* pempty = pfull + NP;
+    uint64_t* drain = pempty + NP;
     // tmem, abort, MMA-consumed groups, weight groups issued, X groups issued, dequant-consumed groups
     uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
     volatile uint32_t* abort_flag = misc + 1;
@@ -190,20 +173,20 @@ __global__ void __launch_bounds__(352, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::QS; s++) {
             mbar_init(qfull + s, 1);
-            mbar_init(qempty + s, 4);             // the four dequant warps
+            mbar_init(qempty + s, 8);             // the eight dequant warps
         }
         for (int s = 0; s < C::XS; s++) {
             mbar_init(xfull + s, 1);
             mbar_init(xempty + s, 1);             // the MMA commit
         }
-        for (int s = 0; s < SA; s++) {
-            mbar_init(afull + s, 4);
+        for (int s = 0; s < C::SA; s++) {
+            mbar_init(afull + s, 8);
             mbar_init(aempty + s, 1);
         }
-        mbar_init(pfull + 0, 1);
-        mbar_init(pfull + 1, 1);
-        mbar_init(pempty + 0, 4);
-        mbar_init(pempty + 1, 4);
+        for (int s = 0; s < NP; s++) {
+            mbar_init(pfull + s, 1);
+            mbar_init(pempty + s, 4);             // the four epilogue warps
+        }
         mbar_init(drain, 1);
         fence_mbar_init();
         misc[1] = (p.status && *reinterpret_cast<volatile int*>(p.status) != 0) ? 1u : 0u;
@@ -235,7 +218,7 @@ __global__ void __launch_bounds__(352, 1)
             tma_load_2d(smem + C::OFF_QW + s * QW_BYTES, &tmQ, n0, (g0 + t) * 16, qfull + s);
             misc[3] = (uint32_t)(t + 1);
         }
-    } else if (!skip && warp == 10 && lane == 0) {
+    } else if (!skip && warp == 14 && lane == 0) {
         // ------------------------------------------------ activation producer (L2)
         for (int t = 0; t < ng_cta; t++) {
             const int s = t % C::XS;
@@ -252,10 +235,10 @@ __global__ void __launch_bounds__(352, 1)
     } else if (!skip && warp == 1 && lane == 0) {
         // ------------------------------------------------ MMA issuer
         for (int t = 0; t < ng_cta; t++) {
-            const int sx = t % C::XS, sa = t % SA, b = t & 1;
+            const int sx = t % C::XS, sa = t % C::SA, b = t % NP;
             if (!wait_or_abort(xfull + sx, (uint32_t)(t / C::XS) & 1u, abort_flag) ||
-                !wait_or_abort(afull + sa, (uint32_t)(t / SA) & 1u, abort_flag) ||
-                !wait_or_abort(pempty + b, ((uint32_t)(t >> 1) & 1u) ^ 1u, abort_flag)) {
+                !wait_or_abort(afull + sa, (uint32_t)(t / C::SA) & 1u, abort_flag) ||
+                !wait_or_abort(pempty + b, ((uint32_t)(t / NP) & 1u) ^ 1u, abort_flag)) {
                 record_timeout(p.status, abort_flag);
                 break;
             }
@@ -274,37 +257,39 @@ __global__ void __launch_bounds__(352, 1)
             tc_commit(pfull + b);
             misc[2] = (uint32_t)(t + 1);
         }
-    } else if (!skip && warp >= 2 && warp < 6) {
+    } else if (!skip && warp >= 2 && warp < 10) {
         // ------------------------------------------------ dequantizers
-        const int n = threadIdx.x - 64;            // channel within the tile (0..127)
+        const int d = threadIdx.x - 64;            // 0..255
+        const int n = d & 127, half = d >> 7;      // channel, 64-K sub-tile of each group
         const int ng = n0 + n;
+        uint8_t* const zt = smem + C::OFF_ZT;      // this thread's column d of [CHUNK][256]
         uint8_t* const a_ring = smem + C::OFF_A;
-        uint32_t zr[4];
-        load_zero_chunk(p, ng, g0, g1, zr);
         for (int t = 0; t < ng_cta; t++) {
-            const int s = t % C::QS, sa = t % SA;
-            if ((t % CHUNK) == 0 && t > 0) load_zero_chunk(p, ng, g0 + t, g1, zr);
+            const int s = t % C::QS, sa = t % C::SA;
+            if ((t % CHUNK) == 0) {
+                for (int i = 0; i < CHUNK && t + i < ng_cta; i++) {
+                    uint32_t z = 0;
+                    if (ng < p.N)
+                        z = ((uint32_t)__ldg(p.qzeros + (int64_t)(g0 + t + i) * (p.N >> 3) + (ng >> 3)) >> (4 * (ng & 7))) & 0xFu;
+                    zt[i * 256 + d] = (uint8_t)z;
+                }
+            }
             if (!warp_wait(qfull + s, (uint32_t)(t / C::QS) & 1u, abort_flag) ||
-                !warp_wait(aempty + sa, ((uint32_t)(t / SA) & 1u) ^ 1u, abort_flag)) {
+                !warp_wait(aempty + sa, ((uint32_t)(t / C::SA) & 1u) ^ 1u, abort_flag)) {
                 if (lane == 0) record_timeout(p.status, abort_flag);
                 break;
             }
-            const int ti = t % CHUNK;
-            uint32_t zw = zr[0];
-#pragma unroll
-            for (int j = 1; j < 4; j++)
-                if ((ti >> 3) == j) zw = zr[j];
-            const uint32_t zb = 0x4300u | ((zw >> (4 * (ti & 7))) & 0xFu);
+            const uint32_t zb = 0x4300u | zt[(t % CHUNK) * 256 + d];
             __nv_bfloat162 bias2;
             *reinterpret_cast<uint32_t*>(&bias2) = zb | (zb << 16);
-            const uint32_t* qw = reinterpret_cast<const uint32_t*>(smem + C::OFF_QW + s * QW_BYTES);
-            uint8_t* arow = a_ring + sa * A_BYTES + n * 128;
+            const uint32_t* qw = reinterpret_cast<const uint32_t*>(smem + C::OFF_QW + s * QW_BYTES) + half * 8 * 128;
+            uint8_t* arow = a_ring + sa * A_BYTES + half * (A_BYTES / 2) + n * 128;
+            uint32_t w[8];
 #pragma unroll
-            for (int o = 0; o < 16; o++) {
-                const uint32_t w = qw[o * 128 + n];
-                *reinterpret_cast<uint4*>(arow + (o >> 3) * (A_BYTES / 2) + (((o & 7) ^ (n & 7)) << 4)) =
-                    dequant8(w, bias2);
-            }
+            for (int o = 0; o < 8; o++) w[o] = qw[o * 128 + n];
+#pragma unroll
+            for (int o = 0; o < 8; o++)
+                *reinterpret_cast<uint4*>(arow + ((o ^ (n & 7)) << 4)) = dequant8(w[o], bias2);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
@@ -313,30 +298,29 @@ __global__ void __launch_bounds__(352, 1)
             }
             if (threadIdx.x == 64) misc[5] = (uint32_t)(t + 1);
         }
-    } else if (!skip && warp >= 6 && warp < 10) {
+    } else if (!skip && warp >= 10 && warp < 14) {
         // ------------------------------------------------ epilogue (scale promotion)
         const int q = warp & 3;
         const int n = q * 32 + lane;
         const int ng = n0 + n;
         const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
-        uint32_t sr[16];
-        load_scale_chunk(p, ng, g0, g1, sr);
+        float* const st = reinterpret_cast<float*>(smem + C::OFF_ST);   // this thread's column n of [CHUNK][128]
         epi_ok = true;
-        for (int gi = 0; gi < ng_cta; gi++) {
-            const int b = gi & 1;
-            if ((gi % CHUNK) == 0 && gi > 0) load_scale_chunk(p, ng, g0 + gi, g1, sr);
-            if (!warp_wait(pfull + b, (uint32_t)(gi >> 1) & 1u, abort_flag)) {
+        for (int t = 0; t < ng_cta; t++) {
+            const int b = t % NP;
+            if ((t % CHUNK) == 0) {
+                for (int i = 0; i < CHUNK && t + i < ng_cta; i++)
+                    st[i * 128 + n] = (ng < p.N) ? __bfloat162float(__ushort_as_bfloat16(
+                                                       __ldg(p.scales + (int64_t)(g0 + t + i) * p.N + ng)))
+                                                 : 0.0f;
+            }
+            if (!warp_wait(pfull + b, (uint32_t)(t / NP) & 1u, abort_flag)) {
                 if (lane == 0) record_timeout(p.status, abort_flag);
                 epi_ok = false;
                 break;
             }
             tc_fence_after();
-            const int ti = gi % CHUNK;
-            uint32_t sw = sr[0];
-#pragma unroll
-            for (int j = 1; j < 16; j++)
-                if ((ti >> 1) == j) sw = sr[j];
-            const float sc = __uint_as_float((ti & 1) ? (sw & 0xFFFF0000u) : (sw << 16));
+            const float sc = st[(t % CHUNK) * 128 + n];
 #pragma unroll
             for (int c = 0; c < MP / 16; c++) {
                 uint32_t r[16];
@@ -371,7 +355,7 @@ __global__ void __launch_bounds__(352, 1)
     const bool ok = !*abort_flag;
     float* red = reinterpret_cast<float*>(smem + C::OFF_A);    // [MP][128] fp32, reuses the A ring
     if (cs == 1) {
-        if (warp >= 6 && warp < 10 && epi_ok && ok) {
+        if (warp >= 10 && warp < 14 && epi_ok && ok) {
             const int ng = n0 + (warp & 3) * 32 + lane;
             if (ng < p.N) {
 #pragma unroll
@@ -381,7 +365,7 @@ __global__ void __launch_bounds__(352, 1)
             }
         }
     } else {
-        if (warp >= 6 && warp < 10) {
+        if (warp >= 10 && warp < 14) {
             const int n = (warp & 3) * 32 + lane;
 #pragma unroll
             for (int m = 0; m < MP; m++) red[m * 128 + n] = (epi_ok && ok) ? acc[m] : 0.0f;
@@ -422,8 +406,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 int pick_mp(int64_t M) {
     if (M <= 16) return 16;
     if (M <= 32) return 32;
-    if (M <= 64) return 64;
-    return 128;
+    return 64;                       // larger M runs as several 64-token tiles
 }
 
 // Split-K ways (cluster size) so that the grid is about one wave of SMs.
@@ -480,7 +463,7 @@ cudaError_t launch_mp(const GemmArgs& a, cudaStream_t st) {
     const int cs = pick_split(ntiles * mtiles, p.groups);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)cs, (unsigned)ntiles, (unsigned)mtiles);
-    cfg.blockDim = dim3(352);
+    cfg.blockDim = dim3(THREADS);
     cfg.dynamicSmemBytes = C::SMEM;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
@@ -501,8 +484,7 @@ cudaError_t launch_gemm_w4a16(const GemmArgs& a, cudaStream_t st) {
     switch (pick_mp(a.M)) {
         case 16: return launch_mp<16>(a, st);
         case 32: return launch_mp<32>(a, st);
-        case 64: return launch_mp<64>(a, st);
-        default: return launch_mp<128>(a, st);
+        default: return launch_mp<64>(a, st);
     }
 }
 
