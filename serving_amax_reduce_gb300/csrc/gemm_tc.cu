@@ -18,7 +18,8 @@
 //            4-stage shared-memory ring;
 //   warp 1   allocates TMEM; one lane issues tcgen05.mma into the TMEM
 //            accumulator and tcgen05.commit to release each stage;
-//   warps 2-9 copy the accumulator TMEM -> registers with tcgen05.ld,
+//   warps 4-11 (two warpgroups, raised to 232 registers with setmaxnreg)
+//            copy the accumulator TMEM -> registers with tcgen05.ld,
 //            release it to the next tile's MMAs at once, then apply the
 //            scales and write bf16 while that tile's mainloop runs.
 // Variants:
@@ -57,7 +58,11 @@ struct Cfg {
     static constexpr int BN = 256;
     static constexpr int STAGES = 4;
     static constexpr int EPI_WARPS = 8;              // two per TMEM lane quadrant, 128 columns each
-    static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+    static constexpr int THREADS = 384;               // warpgroup 0: TMA + MMA; warpgroups 1-2: epilogue
+    // setmaxnreg split: 128 x 40 + 256 x 232 = 64512 = 384 threads x 168
+    // registers, the launch allocation (checked on the host before launch).
+    static constexpr int REGS_LAUNCH = 168, REGS_CTRL = 40, REGS_EPI = 232;
+    static_assert(128 * REGS_CTRL + 256 * REGS_EPI <= THREADS * REGS_LAUNCH, "register split");
     static constexpr int A_BYTES = BM * BKB;
     static constexpr int B_BYTES = BN * BKB;
     // 512-byte scale chunks (128 rows x 4 scales) per 128 rows per stage
@@ -69,7 +74,9 @@ struct Cfg {
     static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
     static constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
     static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
-    static constexpr int OFF_BAR = OFF_SFB + STAGES * SFB_BYTES;
+    static constexpr int STG_BYTES = 32 * 16 * 2;    // per epilogue warp: 32 rows x 16 bf16 output staging
+    static constexpr int OFF_STG = OFF_SFB + STAGES * SFB_BYTES;
+    static constexpr int OFF_BAR = OFF_STG + EPI_WARPS * STG_BYTES;
     static constexpr int NBAR = 2 * STAGES + 7;      // full[S], empty[S], accf, acce, pfull[2], pempty[2], drain
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int SMEM = OFF_MISC + 64 + 1024; // + slack for 1024-byte alignment
@@ -141,31 +148,36 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// Write 32 consecutive outputs of one row (values already scaled).
-__device__ __forceinline__ void store_row32(const TcParams& p, int row, int n, const float (&v)[32]) {
-    uint16_t* dst = p.y + (int64_t)row * p.ldy + n;
-    if (n + 32 <= p.N) {
-        uint32_t w[16];
+// Write this warp's 32 rows x 32 columns (row = lane, values already scaled)
+// at output (m, n) through the warp's shared-memory staging buffer: two
+// 32 x 16 bf16 boxes stored by TMA.  Bias (if any) is added here; rows and
+// columns outside Y are clipped by the tensor map.
+__device__ __forceinline__ void store_block32(const TcParams& p, const CUtensorMap* tmY, uint8_t* stg, int m, int n,
+                                              const float (&v)[32]) {
+    const int lane = threadIdx.x & 31;
 #pragma unroll
-        for (int i = 0; i < 16; i++) {
-            float a = v[2 * i], b = v[2 * i + 1];
+    for (int hh = 0; hh < 2; hh++) {
+        uint32_t w[8];
+#pragma unroll
+        for (int i = 0; i < 8; i++) {
+            float a = v[hh * 16 + 2 * i], b = v[hh * 16 + 2 * i + 1];
             if (p.bias) {
-                a += __bfloat162float(__ushort_as_bfloat16(p.bias[n + 2 * i]));
-                b += __bfloat162float(__ushort_as_bfloat16(p.bias[n + 2 * i + 1]));
+                const int c = n + hh * 16 + 2 * i;
+                if (c < p.N) a += __bfloat162float(__ushort_as_bfloat16(p.bias[c]));
+                if (c + 1 < p.N) b += __bfloat162float(__ushort_as_bfloat16(p.bias[c + 1]));
             }
             w[i] = pack_bf16x2(a, b);
         }
-        uint4* d4 = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-        for (int i = 0; i < 4; i++) d4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-    } else {
-#pragma unroll
-        for (int i = 0; i < 32; i++) {
-            if (n + i < p.N) {
-                float a = v[i];
-                if (p.bias) a += __bfloat162float(__ushort_as_bfloat16(p.bias[n + i]));
-                dst[i] = __bfloat16_as_ushort(__float2bfloat16_rn(a));
-            }
+        if (lane == 0) bulk_wait_read_all();         // the previous box has left the staging buffer
+        __syncwarp();
+        uint4* dst = reinterpret_cast<uint4*>(stg + lane * 32);
+        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_2d(tmY, n + hh * 16, m, stg);
+            bulk_commit_group();
         }
     }
 }
@@ -186,7 +198,8 @@ __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int
 
 template <int KIND>
 __global__ void __launch_bounds__(Cfg<KIND>::THREADS, 1)
-    k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const TcParams p) {
+    k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+              const __grid_constant__ CUtensorMap tmY, const TcParams p) {
     using C = Cfg<KIND>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -223,6 +236,7 @@ __global__ void __launch_bounds__(Cfg<KIND>::THREADS, 1)
         misc[3] = 0;
         prefetch_tmap(&tmA);
         prefetch_tmap(&tmB);
+        prefetch_tmap(&tmY);
     }
     if (warp == 1) tmem_alloc(misc, C::TMEM_COLS);
     tc_fence_before();
@@ -230,7 +244,10 @@ __global__ void __launch_bounds__(Cfg<KIND>::THREADS, 1)
     tc_fence_after();
     const uint32_t tmem = misc[0];
     const bool skip = misc[1] != 0;
-
+    // Warpgroup 0 (TMA, MMA, two idle warps) gives registers to the two
+    // epilogue warpgroups, which hold a 128-column fp32 tile row each.
+    if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::REGS_CTRL));
     if (!skip && warp == 0 && lane == 0) {
         // ------------------------------------------------ TMA producer
         uint32_t kg = 0;
@@ -348,10 +365,13 @@ __global__ void __launch_bounds__(Cfg<KIND>::THREADS, 1)
             }
             if (ok && KIND != kFp8Block) tc_commit(accf);
         }
-    } else if (!skip && warp >= 2) {
+    }
+    } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::REGS_EPI));
+    if (!skip) {
         // ------------------------------------------------ epilogue (8 warps)
         const int q = warp & 3;                 // TMEM lane quadrant this warp may read
-        const int h = (warp - 2) >> 2;          // which 128-column half of the tile
+        const int h = (warp - 4) >> 2;          // which 128-column half of the tile
         const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
         float alpha = 1.0f;
         if (KIND == kFp8Tensor) alpha = __fmul_rn(__ldg(p.x_scale), __ldg(p.w_scale));
@@ -377,15 +397,14 @@ __global__ void __launch_bounds__(Cfg<KIND>::THREADS, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(acce);     // the MMA may start the next tile
-                if (row < p.M) {
+                uint8_t* stg = smem + C::OFF_STG + (warp - 4) * C::STG_BYTES;
 #pragma unroll
-                    for (int c = 0; c < 4; c++) {
-                        if (ncol + c * 32 < p.N) {
-                            float v[32];
+                for (int c = 0; c < 4; c++) {
+                    if (ncol + c * 32 < p.N) {
+                        float v[32];
 #pragma unroll
-                            for (int i = 0; i < 32; i++) v[i] = __uint_as_float(r[c][i]) * alpha;
-                            store_row32(p, row, ncol + c * 32, v);
-                        }
+                        for (int i = 0; i < 32; i++) v[i] = __uint_as_float(r[c][i]) * alpha;
+                        store_block32(p, &tmY, stg, m0 + q * 32, ncol + c * 32, v);
                     }
                 }
             } else {
@@ -395,9 +414,9 @@ __global__ void __launch_bounds__(Cfg<KIND>::THREADS, 1)
                 const float sx = (row < p.M) ? __ldg(p.x_scale + row) : 0.0f;
                 // this half-tile's weight-block scales, 32 per register, fetched by shuffle
                 float sreg[4];
-                float acc[128];
+                uint64_t acc2[64];                  // 128 fp32 accumulators as (lo, hi) pairs
 #pragma unroll
-                for (int i = 0; i < 128; i++) acc[i] = 0.0f;
+                for (int i = 0; i < 64; i++) acc2[i] = 0ull;
                 for (int kb = 0; kb < p.nk; kb++, kbg++) {
                     if ((kb & 127) == 0) {
 #pragma unroll
@@ -419,32 +438,51 @@ __global__ void __launch_bounds__(Cfg<KIND>::THREADS, 1)
                     const float sw2 = __shfl_sync(0xFFFFFFFFu, sreg[2], kr & 31);
                     const float sw3 = __shfl_sync(0xFFFFFFFFu, sreg[3], kr & 31);
                     sw = (kr < 32) ? sw : (kr < 64) ? sw1 : (kr < 96) ? sw2 : sw3;
+                    // 4 chunks of 32 columns; the load of chunk c+1 is in flight
+                    // while chunk c is accumulated.
+                    const uint32_t pbase = tmem + lane_addr + (uint32_t)(b * C::BN + h * 128);
+                    uint32_t ra[32], rb[32];
+                    tmem_ld_32x32b_x32(pbase, ra);
+                    tmem_ld_wait();
 #pragma unroll
-                    for (int c = 0; c < 8; c++) {
-                        uint32_t r[16];
-                        tmem_ld_32x32b_x16(tmem + lane_addr + (uint32_t)(b * C::BN + h * 128 + c * 16), r);
-                        tmem_ld_wait();
+                    for (int c = 0; c < 4; c++) {
+                        if (c + 1 < 4) {
+                            if (c & 1) tmem_ld_32x32b_x32(pbase + (uint32_t)((c + 1) * 32), ra);
+                            else tmem_ld_32x32b_x32(pbase + (uint32_t)((c + 1) * 32), rb);
+                        }
+                        const uint64_t sw2 = pack_f32x2(__float_as_uint(sw), __float_as_uint(sw));
 #pragma unroll
-                        for (int i = 0; i < 16; i++) acc[c * 16 + i] = fmaf(sw, __uint_as_float(r[i]), acc[c * 16 + i]);
+                        for (int i = 0; i < 16; i++) {
+                            const uint64_t pv = (c & 1) ? pack_f32x2(rb[2 * i], rb[2 * i + 1])
+                                                        : pack_f32x2(ra[2 * i], ra[2 * i + 1]);
+                            acc2[c * 16 + i] = ffma2(sw2, pv, acc2[c * 16 + i]);
+                        }
+                        if (c + 1 < 4) tmem_ld_wait();
                     }
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(pempty + b);
                 }
                 if (!ok) break;
-                if (row < p.M && col_ok) {
+                uint8_t* stg = smem + C::OFF_STG + (warp - 4) * C::STG_BYTES;
 #pragma unroll
-                    for (int c = 0; c < 4; c++) {
-                        if (ncol + c * 32 < p.N) {
-                            float v[32];
+                for (int c = 0; c < 4; c++) {
+                    if (ncol + c * 32 < p.N) {
+                        float v[32];
 #pragma unroll
-                            for (int i = 0; i < 32; i++) v[i] = acc[c * 32 + i] * sx;
-                            store_row32(p, row, ncol + c * 32, v);
+                        for (int i = 0; i < 16; i++) {
+                            unpack_f32x2(acc2[c * 16 + i], v[2 * i], v[2 * i + 1]);
+                            v[2 * i] *= sx;
+                            v[2 * i + 1] *= sx;
                         }
+                        store_block32(p, &tmY, stg, m0 + q * 32, ncol + c * 32, v);
                     }
                 }
             }
         }
+    }
+
+    if (lane == 0) bulk_wait_all();              // this warp's output stores have completed
     }
 
     // ---------------------------------------------------- teardown
@@ -521,6 +559,18 @@ cudaError_t launch_tc(const GemmArgs& a, cudaStream_t st) {
     CUtensorMap tmA, tmB;
     if (!make_tmap_u8(&tmA, a.x, kbytes, (uint64_t)a.M, kbytes, BM)) return cudaErrorInvalidValue;
     if (!make_tmap_u8(&tmB, a.w, kbytes, (uint64_t)a.N, kbytes, C::BN)) return cudaErrorInvalidValue;
+    CUtensorMap tmY;
+    {
+        auto fn = encode_fn();
+        cuuint64_t dims[2] = {(cuuint64_t)a.N, (cuuint64_t)a.M};
+        cuuint64_t strides[1] = {(cuuint64_t)a.ldy * 2};
+        cuuint32_t box[2] = {16, 32};
+        cuuint32_t estr[2] = {1, 1};
+        if (!fn || fn(&tmY, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.y, dims, strides, box, estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
     TcParams p{};
     p.M = (int)a.M;
     p.N = (int)a.N;
@@ -539,13 +589,19 @@ cudaError_t launch_tc(const GemmArgs& a, cudaStream_t st) {
     p.status = a.dev_status;
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(k_gemm_tc<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        // The in-kernel setmaxnreg split assumes the launch allocation of
+        // REGS_LAUNCH registers per thread; refuse to launch otherwise.
+        cudaFuncAttributes fa;
+        cudaError_t e = cudaFuncGetAttributes(&fa, k_gemm_tc<KIND>);
+        if (e != cudaSuccess) return e;
+        if (fa.numRegs != C::REGS_LAUNCH) return cudaErrorInvalidConfiguration;
+        e = cudaFuncSetAttribute(k_gemm_tc<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
     const int64_t ntiles = ((a.N + C::BN - 1) / C::BN) * ((a.M + BM - 1) / BM);
     const int grid = (int)(ntiles < num_sms() ? ntiles : num_sms());   // persistent: one CTA per SM
-    k_gemm_tc<KIND><<<grid, C::THREADS, C::SMEM, st>>>(tmA, tmB, p);
+    k_gemm_tc<KIND><<<grid, C::THREADS, C::SMEM, st>>>(tmA, tmB, tmY, p);
     return cudaGetLastError();
 }
 

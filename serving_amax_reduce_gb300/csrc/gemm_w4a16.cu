@@ -103,11 +103,6 @@ __device__ __forceinline__ void record_timeout(int* status, volatile uint32_t* a
     if (status) atomicExch(status, (int)QLIN_ERR_DEVICE_TIMEOUT);
 }
 
-// Generic-proxy smem writes -> visible to the tensor core's async proxy.
-__device__ __forceinline__ void fence_proxy_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
