@@ -74,7 +74,9 @@ struct Cfg {
     static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
     static constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
     static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
-    static constexpr int STG_BYTES = 32 * 16 * 2;    // per epilogue warp: 32 rows x 16 bf16 output staging
+    static constexpr int STG_BOX = 32 * 16 * 2;      // one 32 x 16 bf16 output box
+    static constexpr int STG_BUFS = (KIND == kNvfp4) ? 1 : 2;   // staging boxes per epilogue warp
+    static constexpr int STG_BYTES = STG_BOX * STG_BUFS;
     static constexpr int OFF_STG = OFF_SFB + STAGES * SFB_BYTES;
     static constexpr int OFF_BAR = OFF_STG + EPI_WARPS * STG_BYTES;
     static constexpr int NBAR = 2 * STAGES + 7;      // full[S], empty[S], accf, acce, pfull[2], pempty[2], drain
@@ -152,11 +154,13 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
 // at output (m, n) through the warp's shared-memory staging buffer: two
 // 32 x 16 bf16 boxes stored by TMA.  Bias (if any) is added here; rows and
 // columns outside Y are clipped by the tensor map.
+template <int NBUF>
 __device__ __forceinline__ void store_block32(const TcParams& p, const CUtensorMap* tmY, uint8_t* stg, int m, int n,
                                               const float (&v)[32]) {
     const int lane = threadIdx.x & 31;
 #pragma unroll
     for (int hh = 0; hh < 2; hh++) {
+        uint8_t* box = stg + (hh % NBUF) * (32 * 16 * 2);
         uint32_t w[8];
 #pragma unroll
         for (int i = 0; i < 8; i++) {
@@ -168,15 +172,19 @@ __device__ __forceinline__ void store_block32(const TcParams& p, const CUtensorM
             }
             w[i] = pack_bf16x2(a, b);
         }
-        if (lane == 0) bulk_wait_read_all();         // the previous box has left the staging buffer
+        // the box stored NBUF boxes ago has left this staging buffer
+        if (lane == 0) {
+            if (NBUF == 1) bulk_wait_read_all();
+            else asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+        }
         __syncwarp();
-        uint4* dst = reinterpret_cast<uint4*>(stg + lane * 32);
+        uint4* dst = reinterpret_cast<uint4*>(box + lane * 32);
         dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
         dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-            tma_store_2d(tmY, n + hh * 16, m, stg);
+            tma_store_2d(tmY, n + hh * 16, m, box);
             bulk_commit_group();
         }
     }
@@ -404,7 +412,7 @@ __global__ void __launch_bounds__(Cfg<KIND>::THREADS, 1)
                         float v[32];
 #pragma unroll
                         for (int i = 0; i < 32; i++) v[i] = __uint_as_float(r[c][i]) * alpha;
-                        store_block32(p, &tmY, stg, m0 + q * 32, ncol + c * 32, v);
+                        store_block32<C::STG_BUFS>(p, &tmY, stg, m0 + q * 32, ncol + c * 32, v);
                     }
                 }
             } else {
@@ -438,30 +446,23 @@ __global__ void __launch_bounds__(Cfg<KIND>::THREADS, 1)
                     const float sw2 = __shfl_sync(0xFFFFFFFFu, sreg[2], kr & 31);
                     const float sw3 = __shfl_sync(0xFFFFFFFFu, sreg[3], kr & 31);
                     sw = (kr < 32) ? sw : (kr < 64) ? sw1 : (kr < 96) ? sw2 : sw3;
-                    // 4 chunks of 32 columns; the load of chunk c+1 is in flight
-                    // while chunk c is accumulated.
+                    // two 64-column loads; the buffer is released after the second
                     const uint32_t pbase = tmem + lane_addr + (uint32_t)(b * C::BN + h * 128);
-                    uint32_t ra[32], rb[32];
-                    tmem_ld_32x32b_x32(pbase, ra);
-                    tmem_ld_wait();
+                    const uint64_t swp = pack_f32x2(__float_as_uint(sw), __float_as_uint(sw));
 #pragma unroll
-                    for (int c = 0; c < 4; c++) {
-                        if (c + 1 < 4) {
-                            if (c & 1) tmem_ld_32x32b_x32(pbase + (uint32_t)((c + 1) * 32), ra);
-                            else tmem_ld_32x32b_x32(pbase + (uint32_t)((c + 1) * 32), rb);
+                    for (int c = 0; c < 2; c++) {
+                        uint32_t r[64];
+                        tmem_ld_32x32b_x64(pbase + (uint32_t)(c * 64), r);
+                        tmem_ld_wait();
+                        if (c == 1) {
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(pempty + b);
                         }
-                        const uint64_t sw2 = pack_f32x2(__float_as_uint(sw), __float_as_uint(sw));
 #pragma unroll
-                        for (int i = 0; i < 16; i++) {
-                            const uint64_t pv = (c & 1) ? pack_f32x2(rb[2 * i], rb[2 * i + 1])
-                                                        : pack_f32x2(ra[2 * i], ra[2 * i + 1]);
-                            acc2[c * 16 + i] = ffma2(sw2, pv, acc2[c * 16 + i]);
-                        }
-                        if (c + 1 < 4) tmem_ld_wait();
+                        for (int i = 0; i < 32; i++)
+                            acc2[c * 32 + i] = ffma2(swp, pack_f32x2(r[2 * i], r[2 * i + 1]), acc2[c * 32 + i]);
                     }
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(pempty + b);
                 }
                 if (!ok) break;
                 uint8_t* stg = smem + C::OFF_STG + (warp - 4) * C::STG_BYTES;
@@ -475,7 +476,7 @@ __global__ void __launch_bounds__(Cfg<KIND>::THREADS, 1)
                             v[2 * i] *= sx;
                             v[2 * i + 1] *= sx;
                         }
-                        store_block32(p, &tmY, stg, m0 + q * 32, ncol + c * 32, v);
+                        store_block32<C::STG_BUFS>(p, &tmY, stg, m0 + q * 32, ncol + c * 32, v);
                     }
                 }
             }
