@@ -1,5 +1,5 @@
-// W4A16 decode GEMM: Y[M, N] = X[M, K] (bf16) . dequant(W)^T with W stored as
-// int4 asymmetric codes, group 128 along K, GPTQ-style packing
+// W4A16 decode GEMM: Y[M, N] = X[M, K] (bf16) . dequant(W)^T (+ bias) with W
+// stored as int4 asymmetric codes, group 128 along K, GPTQ-style packing
 // ("vLLM-Omni는 AutoRound 양자화로 추론을 가속화합니다", section "새로운 모델
 // 양자화": bits 4, group_size 128, packing auto_round:auto_gptq).
 //
@@ -13,16 +13,21 @@
 //             into a deep ring, so that enough HBM reads are in flight;
 //   warp 14   TMA: the X tile (MP x 128 bf16, two 128-byte-swizzled boxes)
 //             into its own ring (X is re-read by every CTA and sits in L2);
-//   warps 2-9 dequantize each word into exact bf16 (q - z) values (small
-//             integers, so no rounding) and store them in the 128-byte
-//             swizzled K-major layout the MMA reads, three groups deep; the
-//             zero points of 32 groups are staged in shared memory;
-//   warp 1    one lane issues tcgen05.mma kind::f16 into one of four TMEM
-//             partial buffers per 128-K group;
-//   warps 10-13 multiply each group's partial by its bf16 scale (32 groups
-//             staged in shared memory) and accumulate in registers (the
-//             scale varies per group and channel, so it cannot be folded
-//             into either operand exactly).
+//   warps 2-9 dequantize, in two sets of four warps that take alternate
+//             groups: each thread owns one channel, turns its 16 words into
+//             128 exact bf16 (q - z) values (small integers, so no rounding)
+//             and writes them with one tcgen05.st into the group's tensor
+//             memory stage, which the MMA reads as its A operand; the set
+//             also permutes the group's X tile within 8-element K chunks to
+//             the order in which the dequantized pairs come out;
+//   warps 1, 15 one lane each issues the group's tcgen05.mma kind::f16 (A from
+//             tensor memory, X from shared memory) into the group's TMEM
+//             partial buffer; the two issuers take alternate groups, which
+//             doubles the rate at which small MMAs enter the tensor pipe;
+//   warps 10-13 multiply each group's partial by its bf16 scale (staged in
+//             shared memory) and accumulate in registers: the scale varies per
+//             group and channel, so it cannot be folded into either operand
+//             exactly.
 // Split-K: the CTAs of one thread-block cluster share an output tile and
 // each take a contiguous range of groups; their fp32 partial tiles are summed
 // through distributed shared memory, so the kernel needs no global scratch.
@@ -41,30 +46,36 @@ using namespace ptx;
 
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 constexpr int QW_BYTES = 16 * 128 * 4;     // one 128-K group: 16 k-octets x 128 channels int32
-constexpr int A_BYTES = 2 * 128 * 128;     // one group dequantized: two 64-K sub-tiles of 128 x 64 bf16
-constexpr int CHUNK = 32;                  // groups whose zero points / scales are staged at a time
-constexpr int NP = 4;                      // TMEM partial buffers (groups the MMA may run ahead)
-constexpr int THREADS = 480;               // 15 warps, see the role map in k_w4a16
+constexpr int A_COLS = 64;                 // TMEM columns per dequantized group (128 K as bf16 pairs)
+constexpr int ZCH = 16;                    // groups of one dequant set whose zero points are staged at a time
+constexpr int SCH = 16;                    // groups whose scales are staged at a time (epilogue)
+constexpr int THREADS = 512;               // 16 warps, see the role map in k_w4a16
+constexpr uint32_t TMEM_COLS = 512;
 
 template <int MP>
 struct W4Cfg {
     static constexpr int XSUB = MP * 128;                           // one 64-K X sub-tile
     static constexpr int X_BYTES = 2 * XSUB;                        // one group of X
-    static constexpr int SA = 3;                                    // dequantized groups in flight
-    static constexpr int XS = (MP <= 32) ? 4 : 3;                   // X ring depth (groups)
-    static constexpr int QS = (MP <= 32) ? 9 : 7;                   // weight ring depth (groups)
-    static constexpr int OFF_A = 0;                                  // SA groups (reused for the reduction)
-    static constexpr int OFF_X = OFF_A + SA * A_BYTES;
-    static constexpr int OFF_QW = OFF_X + XS * X_BYTES;
-    static constexpr int OFF_ZT = OFF_QW + QS * QW_BYTES;           // zero points [CHUNK][256] bytes
-    static constexpr int OFF_ST = OFF_ZT + CHUNK * 256;             // scales [CHUNK][128] floats
-    static constexpr int OFF_BAR = OFF_ST + CHUNK * 128 * 4;
-    static constexpr int NBAR = 2 * QS + 2 * XS + 2 * SA + 2 * NP + 1;
+    // A stages in TMEM = X slots in shared memory (both freed by the same MMA
+    // completion); partial buffers in TMEM.  Both even: each stage always
+    // belongs to the same one of the two MMA issuers.
+    static constexpr int RA = (MP <= 32) ? 6 : 4;
+    static constexpr int RP = 4;
+    static constexpr int XS = RA;
+    static constexpr int QS = (MP <= 32) ? 16 : 12;                 // weight ring depth (groups)
+    static constexpr int OFF_QW = 0;                                // weight ring
+    static constexpr int OFF_X = OFF_QW + QS * QW_BYTES;
+    static constexpr int OFF_ZT = OFF_X + XS * X_BYTES;             // zero points [2 sets][ZCH][128] bytes
+    static constexpr int OFF_ST = OFF_ZT + 2 * ZCH * 128;           // scales [SCH][128] floats
+    static constexpr int OFF_RED = OFF_ST + SCH * 128 * 4;          // split-K partial tile [MP][128] fp32
+    static constexpr int OFF_BAR = OFF_RED + MP * 128 * 4;
+    static constexpr int NBAR = 2 * QS + 3 * RA + 2 * RP + 1;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int SMEM = OFF_MISC + 64 + 1024;
-    static constexpr uint32_t TMEM_COLS = (NP * MP < 32) ? 32 : NP * MP;
-    static constexpr int RED_BYTES = MP * 128 * 4;
-    static_assert(RED_BYTES <= SA * A_BYTES, "reduction tile must fit in the A ring");
+    static constexpr uint32_t P_COL = RA * A_COLS;                  // partial buffers follow the A stages
+    static_assert(P_COL + RP * MP <= TMEM_COLS, "tensor memory budget");
+    static_assert(RA % 2 == 0 && RP % 2 == 0, "stages alternate between the two issuers");
+    static_assert(X_BYTES % 1024 == 0 && OFF_X % 1024 == 0, "128-byte-swizzled tiles need 1 KB alignment");
     static_assert(SMEM <= 232448, "shared memory budget");
     // kind::f16: D f32, A bf16, B bf16, K-major, N = MP, M = 128
     static constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(MP >> 3) << 17) |
@@ -76,11 +87,13 @@ struct W4Params {
     int64_t ldy;
     const uint16_t* scales;   // bf16 [K/128, N]
     const int32_t* qzeros;    // [K/128, N/8]
+    const uint16_t* bias;     // bf16 [N] or null
     uint16_t* y;
     int* status;
 };
 
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile uint32_t* abort_flag) {
+    if (mbar_test_wait(bar, parity)) return true;          // usually complete already: no suspend
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
@@ -113,48 +126,62 @@ __device__ __forceinline__ uint32_t cluster_rank() {
     return r;
 }
 
+// Load from the shared memory of CTA `rank` of this cluster (ordered by the
+// cluster barrier that precedes the reduction, so independent loads may overlap).
 __device__ __forceinline__ float ld_peer_f32(uint32_t local_saddr, uint32_t rank) {
     uint32_t remote;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_saddr), "r"(rank));
+    asm("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_saddr), "r"(rank));
     float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote));
     return v;
 }
 
 // Eight 4-bit codes (k = 8o .. 8o+7 in bits [4j, 4j+4)) minus the zero point,
 // as eight exact bf16 values: 0x4300 | q is the bf16 for 128 + q, and
-// (128 + q) - (128 + z) is an exact small integer.
-__device__ __forceinline__ uint4 dequant8(uint32_t w, __nv_bfloat162 bias2) {
-    uint32_t h[4];
+// (128 + q) - (128 + z) is an exact small integer.  The codes are taken two at
+// a time from bits [4j, 4j+4) and [4j+16, 4j+20), so the pairs come out as
+// (k0, k4), (k1, k5), (k2, k6), (k3, k7): every 8-element K chunk of the A
+// operand is in the order 0 4 1 5 2 6 3 7, and the X tile is permuted the
+// same way (permute_x_chunk), which leaves each dot product unchanged.
+__device__ __forceinline__ void dequant8(uint32_t w, __nv_bfloat162 bias2, uint32_t* out) {
+    constexpr uint32_t kMask = 0x000F000Fu, kMagic = 0x43004300u;
+    uint32_t v[4];
+    v[0] = lop3_and_or(w, kMask, kMagic);
+    v[1] = lop3_and_or(w >> 4, kMask, kMagic);
+    v[2] = lop3_and_or(w >> 8, kMask, kMagic);
+    v[3] = lop3_and_or(w >> 12, kMask, kMagic);
 #pragma unroll
-    for (int p = 0; p < 4; p++) {
-        const uint32_t t = ((w >> (8 * p)) & 0xFu) | (((w >> (8 * p + 4)) & 0xFu) << 16) | 0x43004300u;
-        __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(&t);
-        v = __hsub2(v, bias2);
-        h[p] = *reinterpret_cast<uint32_t*>(&v);
+    for (int i = 0; i < 4; i++) {
+        __nv_bfloat162 h = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&v[i]), bias2);
+        out[i] = *reinterpret_cast<uint32_t*>(&h);
     }
-    return make_uint4(h[0], h[1], h[2], h[3]);
+}
+
+// One 16-byte chunk of X (k0 .. k7, bf16) into the order 0 4 1 5 2 6 3 7.
+__device__ __forceinline__ uint4 permute_x_chunk(uint4 c) {
+    return make_uint4(prmt(c.x, c.z, 0x5410u), prmt(c.x, c.z, 0x7632u), prmt(c.y, c.w, 0x5410u),
+                      prmt(c.y, c.w, 0x7632u));
 }
 
 template <int MP>
 __global__ void __launch_bounds__(THREADS, 1)
     k_w4a16(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmX, const W4Params p) {
-    // Role map: warp 0 weight TMA, warp 1 MMA (and TMEM owner), warps 2-9
-    // dequantize (thread d: channel d % 128, sub-tile d / 128 of each group),
-    // warps 10-13 epilogue (TMEM lane quadrant = warp % 4), warp 14 X TMA.
+    // Role map: warp 0 weight TMA, warp 1 MMA for even groups (and TMEM owner),
+    // warps 2-5 / 6-9 dequantize even / odd groups (TMEM lane quadrant =
+    // warp % 4), warps 10-13 epilogue (quadrant = warp % 4), warp 14 X TMA,
+    // warp 15 MMA for odd groups.
     using C = W4Cfg<MP>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* qfull = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
     uint64_t* qempty = qfull + C::QS;
-    uint64_t* xfull = qempty + C::QS;
-    uint64_t* xempty = xfull + C::XS;
-    uint64_t* afull = xempty + C::XS;
-    uint64_t* aempty = afull + C::SA;
-    uint64_t* pfull = aempty + C::SA;
-    uint64_t* pempty = pfull + NP;
-    uint64_t* drain = pempty + NP;
-    // tmem, abort, MMA-consumed groups, weight groups issued, X groups issued, dequant-consumed groups
+    uint64_t* xfull = qempty + C::QS;    // X slot a loaded (TMA)
+    uint64_t* afull = xfull + C::RA;     // A stage a written and X slot a permuted
+    uint64_t* mdone = afull + C::RA;     // the MMAs of stage a finished: A stage and X slot free
+    uint64_t* pfull = mdone + C::RA;     // partial p ready
+    uint64_t* pempty = pfull + C::RP;    // the epilogue has read partial p
+    uint64_t* drain = pempty + C::RP;
+    // tmem, abort, -, weight groups issued, X groups issued
     uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
     volatile uint32_t* abort_flag = misc + 1;
 
@@ -168,38 +195,30 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::QS; s++) {
             mbar_init(qfull + s, 1);
-            mbar_init(qempty + s, 8);             // the eight dequant warps
+            mbar_init(qempty + s, 4);             // the four warps of one dequant set
         }
-        for (int s = 0; s < C::XS; s++) {
+        for (int s = 0; s < C::RA; s++) {
             mbar_init(xfull + s, 1);
-            mbar_init(xempty + s, 1);             // the MMA commit
+            mbar_init(afull + s, 4);              // the four warps of one dequant set
+            mbar_init(mdone + s, 1);              // an MMA commit
         }
-        for (int s = 0; s < C::SA; s++) {
-            mbar_init(afull + s, 8);
-            mbar_init(aempty + s, 1);
-        }
-        for (int s = 0; s < NP; s++) {
-            mbar_init(pfull + s, 1);
+        for (int s = 0; s < C::RP; s++) {
+            mbar_init(pfull + s, 1);              // an MMA commit
             mbar_init(pempty + s, 4);             // the four epilogue warps
         }
-        mbar_init(drain, 1);
+        mbar_init(drain, 2);                      // both MMA issuers
         fence_mbar_init();
         misc[1] = (p.status && *reinterpret_cast<volatile int*>(p.status) != 0) ? 1u : 0u;
         for (int i = 2; i < 6; i++) misc[i] = 0;
         prefetch_tmap(&tmQ);
         prefetch_tmap(&tmX);
     }
-    if (warp == 1) tmem_alloc(misc, C::TMEM_COLS);
+    if (warp == 1) tmem_alloc(misc, TMEM_COLS);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = misc[0];
     const bool skip = misc[1] != 0;
-
-    float acc[MP];
-#pragma unroll
-    for (int i = 0; i < MP; i++) acc[i] = 0.0f;
-    bool epi_ok = false;
 
     if (!skip && warp == 0 && lane == 0) {
         // ------------------------------------------------ weight producer (HBM stream)
@@ -216,8 +235,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     } else if (!skip && warp == 14 && lane == 0) {
         // ------------------------------------------------ activation producer (L2)
         for (int t = 0; t < ng_cta; t++) {
-            const int s = t % C::XS;
-            if (!wait_or_abort(xempty + s, ((uint32_t)(t / C::XS) & 1u) ^ 1u, abort_flag)) {
+            const int s = t % C::RA;
+            if (!wait_or_abort(mdone + s, ((uint32_t)(t / C::RA) & 1u) ^ 1u, abort_flag)) {
                 record_timeout(p.status, abort_flag);
                 break;
             }
@@ -227,71 +246,87 @@ __global__ void __launch_bounds__(THREADS, 1)
             tma_load_2d(smem + C::OFF_X + s * C::X_BYTES + C::XSUB, &tmX, k + 64, m0, xfull + s);
             misc[4] = (uint32_t)(t + 1);
         }
-    } else if (!skip && warp == 1 && lane == 0) {
-        // ------------------------------------------------ MMA issuer
-        for (int t = 0; t < ng_cta; t++) {
-            const int sx = t % C::XS, sa = t % C::SA, b = t % NP;
-            if (!wait_or_abort(xfull + sx, (uint32_t)(t / C::XS) & 1u, abort_flag) ||
-                !wait_or_abort(afull + sa, (uint32_t)(t / C::SA) & 1u, abort_flag) ||
-                !wait_or_abort(pempty + b, ((uint32_t)(t / NP) & 1u) ^ 1u, abort_flag)) {
+    } else if (!skip && (warp == 1 || warp == 15) && lane == 0) {
+        // ------------------------------------------------ MMA issuers (even / odd groups)
+        for (int t = (warp == 1) ? 0 : 1; t < ng_cta; t += 2) {
+            const int a = t % C::RA, pb = t % C::RP;
+            // afull: the dequant set has written A and permuted this group's X tile
+            if (!wait_or_abort(afull + a, (uint32_t)(t / C::RA) & 1u, abort_flag) ||
+                !wait_or_abort(pempty + pb, ((uint32_t)(t / C::RP) & 1u) ^ 1u, abort_flag)) {
                 record_timeout(p.status, abort_flag);
                 break;
             }
             tc_fence_after();
-            const uint32_t a_base = smem_u32(smem + C::OFF_A + sa * A_BYTES);
-            const uint32_t x_base = smem_u32(smem + C::OFF_X + sx * C::X_BYTES);
-            const uint32_t d = tmem + (uint32_t)(b * MP);
+            const uint32_t a_t = tmem + (uint32_t)(a * A_COLS);
+            const uint32_t x_base = smem_u32(smem + C::OFF_X + a * C::X_BYTES);
+            const uint32_t d = tmem + C::P_COL + (uint32_t)(pb * MP);
 #pragma unroll
             for (int j = 0; j < 2; j++)
 #pragma unroll
                 for (int c = 0; c < 4; c++)
-                    mma_f16(d, sdesc_sw128(a_base + j * (A_BYTES / 2) + c * 32),
-                            sdesc_sw128(x_base + j * C::XSUB + c * 32), C::IDESC, (j > 0 || c > 0) ? 1u : 0u);
-            tc_commit(aempty + sa);
-            tc_commit(xempty + sx);
-            tc_commit(pfull + b);
-            misc[2] = (uint32_t)(t + 1);
+                    mma_f16_ta(d, a_t + (uint32_t)((j * 4 + c) * 8), sdesc_sw128(x_base + j * C::XSUB + c * 32),
+                               C::IDESC, (j > 0 || c > 0) ? 1u : 0u);
+            tc_commit(mdone + a);
+            tc_commit(pfull + pb);
         }
     } else if (!skip && warp >= 2 && warp < 10) {
         // ------------------------------------------------ dequantizers
-        const int d = threadIdx.x - 64;            // 0..255
-        const int n = d & 127, half = d >> 7;      // channel, 64-K sub-tile of each group
+        const int set = (warp - 2) >> 2;           // 0: even groups, 1: odd groups
+        const int quad = warp & 3;                 // the TMEM lanes this warp may write
+        const int n = quad * 32 + lane;            // channel of the tile = TMEM lane = row of A
         const int ng = n0 + n;
-        uint8_t* const zt = smem + C::OFF_ZT;      // this thread's column d of [CHUNK][256]
-        uint8_t* const a_ring = smem + C::OFF_A;
-        for (int t = 0; t < ng_cta; t++) {
-            const int s = t % C::QS, sa = t % C::SA;
-            if ((t % CHUNK) == 0) {
-                for (int i = 0; i < CHUNK && t + i < ng_cta; i++) {
-                    uint32_t z = 0;
-                    if (ng < p.N)
-                        z = ((uint32_t)__ldg(p.qzeros + (int64_t)(g0 + t + i) * (p.N >> 3) + (ng >> 3)) >> (4 * (ng & 7))) & 0xFu;
-                    zt[i * 256 + d] = (uint8_t)z;
-                }
+        uint8_t* const zt = smem + C::OFF_ZT + set * (ZCH * 128);   // column n of [ZCH][128]
+        const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
+        int u = 0;                                 // index of t among this set's groups
+        for (int t = set; t < ng_cta; t += 2, u++) {
+            if ((u % ZCH) == 0) {
+                // the zero points of this set's next ZCH groups, all loads in flight at once
+                uint32_t zw[ZCH];
+#pragma unroll
+                for (int i = 0; i < ZCH; i++)
+                    zw[i] = (ng < p.N && t + 2 * i < ng_cta)
+                                ? (uint32_t)__ldg(p.qzeros + (int64_t)(g0 + t + 2 * i) * (p.N >> 3) + (ng >> 3))
+                                : 0u;
+#pragma unroll
+                for (int i = 0; i < ZCH; i++) zt[i * 128 + n] = (uint8_t)((zw[i] >> (4 * (ng & 7))) & 0xFu);
             }
-            if (!warp_wait(qfull + s, (uint32_t)(t / C::QS) & 1u, abort_flag) ||
-                !warp_wait(aempty + sa, ((uint32_t)(t / C::SA) & 1u) ^ 1u, abort_flag)) {
+            const int s = t % C::QS, a = t % C::RA;
+            if (!warp_wait(xfull + a, (uint32_t)(t / C::RA) & 1u, abort_flag) ||
+                !warp_wait(qfull + s, (uint32_t)(t / C::QS) & 1u, abort_flag)) {
                 if (lane == 0) record_timeout(p.status, abort_flag);
                 break;
             }
-            const uint32_t zb = 0x4300u | zt[(t % CHUNK) * 256 + d];
+            {
+                // this group's X tile (MP x 128 bf16 = MP * 16 chunks), permuted in place
+                uint4* xc = reinterpret_cast<uint4*>(smem + C::OFF_X + a * C::X_BYTES);
+#pragma unroll
+                for (int i = 0; i < MP / 8; i++) xc[i * 128 + n] = permute_x_chunk(xc[i * 128 + n]);
+                fence_proxy_async_smem();            // the MMA reads X through the async proxy
+            }
+            const uint32_t zb = 0x4300u | zt[(u % ZCH) * 128 + n];
             __nv_bfloat162 bias2;
             *reinterpret_cast<uint32_t*>(&bias2) = zb | (zb << 16);
-            const uint32_t* qw = reinterpret_cast<const uint32_t*>(smem + C::OFF_QW + s * QW_BYTES) + half * 8 * 128;
-            uint8_t* arow = a_ring + sa * A_BYTES + half * (A_BYTES / 2) + n * 128;
-            uint32_t w[8];
+            const uint32_t* qw = reinterpret_cast<const uint32_t*>(smem + C::OFF_QW + s * QW_BYTES);
+            uint32_t w[16];
 #pragma unroll
-            for (int o = 0; o < 8; o++) w[o] = qw[o * 128 + n];
-#pragma unroll
-            for (int o = 0; o < 8; o++)
-                *reinterpret_cast<uint4*>(arow + ((o ^ (n & 7)) << 4)) = dequant8(w[o], bias2);
-            fence_proxy_async_smem();
+            for (int o = 0; o < 16; o++) w[o] = qw[o * 128 + n];
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(afull + sa);
-                mbar_arrive(qempty + s);
+            if (lane == 0) mbar_arrive(qempty + s);   // the words are in registers: the slot may refill
+            uint32_t av[64];
+#pragma unroll
+            for (int o = 0; o < 16; o++) dequant8(w[o], bias2, av + 4 * o);
+            // only the TMEM write waits for the stage's previous MMAs, so the
+            // loads and the arithmetic above overlap them
+            if (!warp_wait(mdone + a, ((uint32_t)(t / C::RA) & 1u) ^ 1u, abort_flag)) {
+                if (lane == 0) record_timeout(p.status, abort_flag);
+                break;
             }
-            if (threadIdx.x == 64) misc[5] = (uint32_t)(t + 1);
+            tc_fence_after();
+            tmem_st_32x32b_x64(tmem + lane_addr + (uint32_t)(a * A_COLS), av);
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(afull + a);
         }
     } else if (!skip && warp >= 10 && warp < 14) {
         // ------------------------------------------------ epilogue (scale promotion)
@@ -299,34 +334,61 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int n = q * 32 + lane;
         const int ng = n0 + n;
         const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
-        float* const st = reinterpret_cast<float*>(smem + C::OFF_ST);   // this thread's column n of [CHUNK][128]
-        epi_ok = true;
+        float* const st = reinterpret_cast<float*>(smem + C::OFF_ST);   // this thread's column n of [SCH][128]
+        float acc[MP];
+#pragma unroll
+        for (int i = 0; i < MP; i++) acc[i] = 0.0f;
+        bool epi_ok = true;
         for (int t = 0; t < ng_cta; t++) {
-            const int b = t % NP;
-            if ((t % CHUNK) == 0) {
-                for (int i = 0; i < CHUNK && t + i < ng_cta; i++)
-                    st[i * 128 + n] = (ng < p.N) ? __bfloat162float(__ushort_as_bfloat16(
-                                                       __ldg(p.scales + (int64_t)(g0 + t + i) * p.N + ng)))
-                                                 : 0.0f;
+            const int pb = t % C::RP;
+            if ((t % SCH) == 0) {
+                // batches of loads in flight at once (smaller batches where acc is large)
+                constexpr int SB = (MP >= 64) ? 8 : SCH;
+#pragma unroll
+                for (int i0 = 0; i0 < SCH; i0 += SB) {
+                    uint16_t sw[SB];
+#pragma unroll
+                    for (int i = 0; i < SB; i++)
+                        sw[i] = (ng < p.N && t + i0 + i < ng_cta)
+                                    ? __ldg(p.scales + (int64_t)(g0 + t + i0 + i) * p.N + ng)
+                                    : (uint16_t)0;
+#pragma unroll
+                    for (int i = 0; i < SB; i++)
+                        st[(i0 + i) * 128 + n] = __bfloat162float(__ushort_as_bfloat16(sw[i]));
+                }
             }
-            if (!warp_wait(pfull + b, (uint32_t)(t / NP) & 1u, abort_flag)) {
+            if (!warp_wait(pfull + pb, (uint32_t)(t / C::RP) & 1u, abort_flag)) {
                 if (lane == 0) record_timeout(p.status, abort_flag);
                 epi_ok = false;
                 break;
             }
             tc_fence_after();
-            const float sc = st[(t % CHUNK) * 128 + n];
+            const float sc = st[(t % SCH) * 128 + n];
 #pragma unroll
             for (int c = 0; c < MP / 16; c++) {
-                uint32_t r[16];
-                tmem_ld_32x32b_x16(tmem + lane_addr + (uint32_t)(b * MP + c * 16), r);
+                uint32_t v[16];
+                tmem_ld_32x32b_x16(tmem + lane_addr + C::P_COL + (uint32_t)(pb * MP + c * 16), v);
                 tmem_ld_wait();
 #pragma unroll
-                for (int i = 0; i < 16; i++) acc[c * 16 + i] = fmaf(sc, __uint_as_float(r[i]), acc[c * 16 + i]);
+                for (int i = 0; i < 16; i++) acc[c * 16 + i] = fmaf(sc, __uint_as_float(v[i]), acc[c * 16 + i]);
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(pempty + b);
+            if (lane == 0) mbar_arrive(pempty + pb);
+        }
+        // every group of this CTA is in acc once the loop ran to the end
+        if (cs == 1) {
+            if (epi_ok && ng < p.N) {
+                const float b = p.bias ? __bfloat162float(__ushort_as_bfloat16(p.bias[ng])) : 0.0f;
+#pragma unroll
+                for (int m = 0; m < MP; m++)
+                    if (m0 + m < p.M)
+                        p.y[(int64_t)(m0 + m) * p.ldy + ng] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[m] + b));
+            }
+        } else {
+            float* const red = reinterpret_cast<float*>(smem + C::OFF_RED);
+#pragma unroll
+            for (int m = 0; m < MP; m++) red[m * 128 + n] = epi_ok ? acc[m] : 0.0f;
         }
     }
 
@@ -334,54 +396,48 @@ __global__ void __launch_bounds__(THREADS, 1)
     tc_fence_before();
     __syncthreads();
     if (*abort_flag && warp == 0 && lane == 0) {
-        // every TMA copy this CTA issued must land before its shared memory goes
-        for (uint32_t t = misc[5]; t < misc[3]; t++)
-            mbar_wait(qfull + (t % C::QS), (t / C::QS) & 1u, kWaitLimitNs);
-        for (uint32_t t = misc[2]; t < misc[4]; t++)
-            mbar_wait(xfull + (t % C::XS), (t / C::XS) & 1u, kWaitLimitNs);
+        // every TMA copy this CTA issued must land before its shared memory goes;
+        // a ring slot's latest phase covers every earlier copy into it
+        const int wq = (int)misc[3], wx = (int)misc[4];
+        for (int t = (wq > C::QS ? wq - C::QS : 0); t < wq; t++)
+            mbar_wait(qfull + (t % C::QS), (uint32_t)(t / C::QS) & 1u, kWaitLimitNs);
+        for (int t = (wx > C::RA ? wx - C::RA : 0); t < wx; t++)
+            mbar_wait(xfull + (t % C::RA), (uint32_t)(t / C::RA) & 1u, kWaitLimitNs);
     }
-    if (*abort_flag && warp == 1 && lane == 0) {
-        tc_commit(drain);
+    if (*abort_flag && (warp == 1 || warp == 15) && lane == 0) {
+        tc_commit(drain);                          // each issuer's own MMAs
         mbar_wait(drain, 0, kWaitLimitNs);
     }
     __syncthreads();
 
-    // ---------------------------------------------------- output
+    // ---------------------------------------------------- split-K reduction over the cluster
     const bool ok = !*abort_flag;
-    float* red = reinterpret_cast<float*>(smem + C::OFF_A);    // [MP][128] fp32, reuses the A ring
-    if (cs == 1) {
-        if (warp >= 10 && warp < 14 && epi_ok && ok) {
-            const int ng = n0 + (warp & 3) * 32 + lane;
-            if (ng < p.N) {
-#pragma unroll
-                for (int m = 0; m < MP; m++)
-                    if (m0 + m < p.M)
-                        p.y[(int64_t)(m0 + m) * p.ldy + ng] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[m]));
-            }
-        }
-    } else {
-        if (warp >= 10 && warp < 14) {
-            const int n = (warp & 3) * 32 + lane;
-#pragma unroll
-            for (int m = 0; m < MP; m++) red[m * 128 + n] = (epi_ok && ok) ? acc[m] : 0.0f;
-        }
+    if (cs > 1) {
+        const float* red = reinterpret_cast<const float*>(smem + C::OFF_RED);
         cluster_sync_all();
         // CTA `rank` sums columns [rank*128/cs, (rank+1)*128/cs) over the cluster.
         const int c0 = rank * 128 / cs, c1 = (rank + 1) * 128 / cs, width = c1 - c0;
         const uint32_t red_s = smem_u32(red);
         for (int idx = threadIdx.x; idx < MP * width; idx += blockDim.x) {
             const int m = idx / width, n = c0 + idx % width;
+            const uint32_t off = red_s + (uint32_t)((m * 128 + n) * 4);
+            float part[8];
+#pragma unroll
+            for (int r = 0; r < 8; r++) part[r] = (r < cs) ? ld_peer_f32(off, (uint32_t)r) : 0.0f;
             float v = 0.0f;
-            for (int r = 0; r < cs; r++) v += ld_peer_f32(red_s + (uint32_t)((m * 128 + n) * 4), (uint32_t)r);
-            if (m0 + m < p.M && n0 + n < p.N && ok)
-                p.y[(int64_t)(m0 + m) * p.ldy + n0 + n] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+#pragma unroll
+            for (int r = 0; r < 8; r++) v += part[r];
+            if (m0 + m < p.M && n0 + n < p.N && ok) {
+                const float b = p.bias ? __bfloat162float(__ushort_as_bfloat16(p.bias[n0 + n])) : 0.0f;
+                p.y[(int64_t)(m0 + m) * p.ldy + n0 + n] = __bfloat16_as_ushort(__float2bfloat16_rn(v + b));
+            }
         }
         cluster_sync_all();
     }
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
-        tmem_dealloc(tmem, C::TMEM_COLS);
+        tmem_dealloc(tmem, TMEM_COLS);
     }
 }
 
@@ -445,6 +501,7 @@ cudaError_t launch_mp(const GemmArgs& a, cudaStream_t st) {
     p.ldy = a.ldy;
     p.scales = static_cast<const uint16_t*>(a.w_scales);
     p.qzeros = static_cast<const int32_t*>(a.w_zeros);
+    p.bias = a.bias;
     p.y = a.y;
     p.status = a.dev_status;
 

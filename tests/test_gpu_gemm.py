@@ -159,24 +159,33 @@ def test_nvfp4_gemm_full_size(q, orc):
 
 
 # ------------------------------------------------------------------ W4A16 decode
-def w4a16_case(q, orc, M, K, N):
+def w4a16_case(q, orc, M, K, N, with_bias=False):
     lin = inputs.w4a16_linear(M, K, N)
     x, w = lin.make_x(), lin.make_w()
     F = q.Fmt
     bw = q.quantize_weight(F.INT4_G128_ASYM, w.cuda())
     xd = x.cuda()
-    y = q.gemm(F.INT4_G128_ASYM, F.BF16, M, N, K, xd, None, bw["codes"], bw["scales"], w_zeros=bw["zeros"])
+    bias = inputs.normal_bf16((1, N), 0.05, 77)[0] if with_bias else None
+    y = q.gemm(F.INT4_G128_ASYM, F.BF16, M, N, K, xd, None, bw["codes"], bw["scales"], w_zeros=bw["zeros"],
+               bias=bias.cuda() if with_bias else None)
     torch.cuda.synchronize()
     wh = orc.dequant_int4_g128(bw["codes"].cpu().numpy().view(np.int32).reshape(K // 8, N),
                                bw["scales"].cpu().numpy().view(np.uint16).reshape(K // 128, N),
                                bw["zeros"].cpu().numpy().view(np.int32).reshape(K // 128, N // 8))
-    return check(orc, y_np(y), orc.gemm_ref(orc.bf16_values(bits(x)), wh), x, w)
+    b = orc.bf16_values(bits(bias)[None, :])[0] if with_bias else None
+    return check(orc, y_np(y), orc.gemm_ref(orc.bf16_values(bits(x)), wh, bias=b), x, w)
 
 
 @pytest.mark.parametrize("M,K,N", [(1, 4096, 4096), (16, 4096, 12288), (64, 12288, 4096), (5, 256, 72),
                                    (100, 512, 256), (200, 1024, 384), (33, 128, 136)])
 def test_w4a16_gemm(q, orc, M, K, N):
     w4a16_case(q, orc, M, K, N)
+
+
+@pytest.mark.parametrize("M,K,N", [(1, 4096, 4096), (3, 256, 72), (70, 1024, 256)])
+def test_w4a16_gemm_bias(q, orc, M, K, N):
+    # (1, 4096, 4096) takes the split-K cluster path, (3, 256, 72) a single CTA
+    w4a16_case(q, orc, M, K, N, with_bias=True)
 
 
 @pytest.mark.slow
