@@ -420,19 +420,16 @@ __global__ void __launch_bounds__(Cfg<KIND>::THREADS, 1)
                 const bool col_ok = ncol < p.N;
                 const int kblocks = p.K >> 7;
                 const float sx = (row < p.M) ? __ldg(p.x_scale + row) : 0.0f;
-                // this half-tile's weight-block scales, 32 per register, fetched by shuffle
-                float sreg[4];
+                // this half-tile's weight-block scales: one uniform load per block,
+                // issued a block ahead so that its latency is hidden
+                const float* const swrow = p.w_scale + (int64_t)(col_ok ? nt : 0) * kblocks;
+                float sw_next = col_ok ? __ldg(swrow) : 0.0f;
                 uint64_t acc2[64];                  // 128 fp32 accumulators as (lo, hi) pairs
 #pragma unroll
                 for (int i = 0; i < 64; i++) acc2[i] = 0ull;
                 for (int kb = 0; kb < p.nk; kb++, kbg++) {
-                    if ((kb & 127) == 0) {
-#pragma unroll
-                        for (int j = 0; j < 4; j++) {
-                            const int kk = kb + j * 32 + lane;
-                            sreg[j] = (col_ok && kk < kblocks) ? __ldg(p.w_scale + (int64_t)nt * kblocks + kk) : 0.0f;
-                        }
-                    }
+                    const float sw = sw_next;
+                    if (col_ok && kb + 1 < kblocks) sw_next = __ldg(swrow + kb + 1);
                     const int b = (int)(kbg & 1u);
                     if (!warp_wait_or_abort(pfull + b, (kbg >> 1) & 1u, abort_flag)) {
                         if (lane == 0) record_timeout(p.status, abort_flag);
@@ -440,12 +437,6 @@ __global__ void __launch_bounds__(Cfg<KIND>::THREADS, 1)
                         break;
                     }
                     tc_fence_after();
-                    const int kr = kb & 127;
-                    float sw = __shfl_sync(0xFFFFFFFFu, sreg[0], kr & 31);
-                    const float sw1 = __shfl_sync(0xFFFFFFFFu, sreg[1], kr & 31);
-                    const float sw2 = __shfl_sync(0xFFFFFFFFu, sreg[2], kr & 31);
-                    const float sw3 = __shfl_sync(0xFFFFFFFFu, sreg[3], kr & 31);
-                    sw = (kr < 32) ? sw : (kr < 64) ? sw1 : (kr < 96) ? sw2 : sw3;
                     // two 64-column loads; the buffer is released after the second
                     const uint32_t pbase = tmem + lane_addr + (uint32_t)(b * C::BN + h * 128);
                     const uint64_t swp = pack_f32x2(__float_as_uint(sw), __float_as_uint(sw));
