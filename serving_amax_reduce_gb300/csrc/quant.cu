@@ -119,6 +119,30 @@ __device__ __forceinline__ int64_t mma_scale_offset(int64_t row, int64_t j, int6
     return ((tile * chunks_per_row + (j >> 2)) << 9) + ((rr & 31) << 4) + ((rr >> 5) << 2) + (j & 3);
 }
 
+// ---------------------------------------------------------------- row tasks
+// The element-wise formats walk "tasks": 32 consecutive 16-byte vectors
+// (256 elements) of one row, one task per warp and one vector per lane, so
+// each row is read in 512-byte coalesced segments.  A warp keeps kUnroll tasks
+// in flight; row and column come from one 32-bit division per task.  The
+// task count fits in 32 bits for any tensor that fits in device memory (the
+// host checks).
+constexpr int kUnroll = 4;
+
+struct TaskPos {
+    uint32_t row, c;   // c: 16-byte vector index within the row
+    bool in;           // the task exists and c < vectors per row
+};
+
+__device__ __forceinline__ TaskPos task_pos(uint32_t t, uint32_t total, uint32_t tpr, uint32_t nvr, int lane) {
+    TaskPos q{0, 0, false};
+    if (t < total) {
+        q.row = t / tpr;
+        q.c = (t - q.row * tpr) * 32 + (uint32_t)lane;
+        q.in = q.c < nvr;
+    }
+    return q;
+}
+
 // ---------------------------------------------------------------- per row
 // One CTA per row; each thread keeps VPT 16-byte vectors in registers so the
 // row is read from HBM once.
@@ -173,11 +197,19 @@ __global__ void __launch_bounds__(256) k_fp8_rows_long(const uint16_t* __restric
 __global__ void __launch_bounds__(256) k_amax_partial(const uint16_t* __restrict__ x, int64_t rows, int64_t K,
                                                       int64_t ld, float* __restrict__ partials) {
     __shared__ float red[33];
-    const int64_t nvr = K >> 3, total = rows * nvr;
+    const uint32_t nvr = (uint32_t)(K >> 3), tpr = (nvr + 31) / 32, total = (uint32_t)rows * tpr;
+    const uint32_t warps = gridDim.x * 8, w0 = blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
     float amax = 0.0f;
-    for (int64_t v = blockIdx.x * 256ll + threadIdx.x; v < total; v += (int64_t)gridDim.x * 256) {
-        const int64_t row = v / nvr, c = v - row * nvr;
-        amax = fmaxf(amax, absmax8(ld16(x + row * ld + 8 * c)));
+    for (uint32_t t = w0; t < total; t += warps * kUnroll) {
+        uint4 v[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; u++) {
+            const TaskPos q = task_pos(t + u * warps, total, tpr, nvr, lane);
+            v[u] = q.in ? ld16(x + (int64_t)q.row * ld + 8 * q.c) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; u++) amax = fmaxf(amax, absmax8(v[u]));
     }
     amax = block_max<256>(amax, red);
     if (threadIdx.x == 0) partials[blockIdx.x] = amax;
@@ -199,10 +231,20 @@ __global__ void __launch_bounds__(256) k_fp8_tensor_encode(const uint16_t* __res
     float s, r;
     fp8_params(amax, s, r);
     if (blockIdx.x == 0 && threadIdx.x == 0) *scale = s;
-    const int64_t nvr = K >> 3, total = rows * nvr;
-    for (int64_t v = blockIdx.x * 256ll + threadIdx.x; v < total; v += (int64_t)gridDim.x * 256) {
-        const int64_t row = v / nvr, c = v - row * nvr;
-        reinterpret_cast<uint2*>(codes + row * K)[c] = enc8_e4m3(ld16(x + row * ld + 8 * c), r);
+    const uint32_t nvr = (uint32_t)(K >> 3), tpr = (nvr + 31) / 32, total = (uint32_t)rows * tpr;
+    const uint32_t warps = gridDim.x * 8, w0 = blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    for (uint32_t t = w0; t < total; t += warps * kUnroll) {
+        uint4 v[kUnroll];
+        TaskPos q[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; u++) {
+            q[u] = task_pos(t + u * warps, total, tpr, nvr, lane);
+            if (q[u].in) v[u] = ld16(x + (int64_t)q[u].row * ld + 8 * q[u].c);
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; u++)
+            if (q[u].in) reinterpret_cast<uint2*>(codes + (int64_t)q[u].row * K)[q[u].c] = enc8_e4m3(v[u], r);
     }
 }
 
@@ -234,75 +276,96 @@ __global__ void __launch_bounds__(256) k_fp8_block128(const uint16_t* __restrict
 // ---------------------------------------------------------------- MXFP8
 // Four consecutive lanes own one 32-element granule (8 elements each).  Rows
 // from `rows` up to `rows_pad` exist only in the MMA scale layout: they get
-// scale code 0 and no codes.
+// scale code 0 and no codes.  Every lane of a warp runs the same trip count
+// (the shuffles use the full mask); a task never splits a granule.
 __global__ void __launch_bounds__(256) k_mxfp8(const uint16_t* __restrict__ x, int64_t rows, int64_t rows_pad,
                                                int64_t K, int64_t ld, uint8_t* __restrict__ codes,
                                                uint8_t* __restrict__ scales, int mma) {
-    const int64_t nvr = K >> 3, total = rows_pad * nvr;
+    const uint32_t nvr = (uint32_t)(K >> 3), tpr = (nvr + 31) / 32, total = (uint32_t)rows_pad * tpr;
+    const uint32_t warps = gridDim.x * 8, w0 = blockIdx.x * 8 + (threadIdx.x >> 5);
     const int64_t chunks = K >> 7;
     const int lane = threadIdx.x & 31;
-    // Warp-uniform trip count (the shuffles below use the full mask); total is
-    // a multiple of 4, so a granule's four lanes are all in or all out.
-    for (int64_t vb = blockIdx.x * 256ll + (threadIdx.x & ~31); vb < total; vb += (int64_t)gridDim.x * 256) {
-        const int64_t v = vb + lane;
-        const bool in = v < total;
-        const int64_t row = in ? v / nvr : rows_pad, c = in ? v - row * nvr : 0;
-        const bool valid = row < rows;
-        uint4 w = make_uint4(0, 0, 0, 0);
-        if (valid) w = ld16(x + row * ld + 8 * c);
-        float a = absmax8(w);
-        a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
-        a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 2));
-        // e = clamp(floor(log2 a) - 8, -127, 127); subnormal a lands below -127.
-        const int biased = (int)(__float_as_uint(a) >> 23);
-        int e = (a == 0.0f || biased == 0) ? -127 : max(biased - 127 - 8, -127);
-        e = min(e, 127);
-        const float mult = __uint_as_float((uint32_t)(127 - e) << 23);   // 2^-e, e <= 126 here
-        if (valid) reinterpret_cast<uint2*>(codes + row * K)[c] = enc8_e4m3(w, mult);
-        if (in && (c & 3) == 0) {
-            const int64_t j = c >> 2;
-            const int64_t off = mma ? mma_scale_offset(row, j, chunks) : row * (K >> 5) + j;
-            scales[off] = (uint8_t)(e + 127);
+    for (uint32_t t = w0; t < total; t += warps * kUnroll) {
+        uint4 v[kUnroll];
+        TaskPos q[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; u++) {
+            q[u] = task_pos(t + u * warps, total, tpr, nvr, lane);
+            v[u] = (q[u].in && q[u].row < rows) ? ld16(x + (int64_t)q[u].row * ld + 8 * q[u].c)
+                                                : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; u++) {
+            float a = absmax8(v[u]);
+            a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
+            a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 2));
+            // e = clamp(floor(log2 a) - 8, -127, 127); subnormal a lands below -127.
+            const int biased = (int)(__float_as_uint(a) >> 23);
+            int e = (a == 0.0f || biased == 0) ? -127 : max(biased - 127 - 8, -127);
+            e = min(e, 127);
+            const float mult = __uint_as_float((uint32_t)(127 - e) << 23);   // 2^-e, e <= 126 here
+            if (!q[u].in) continue;
+            const int64_t row = q[u].row, c = q[u].c;
+            if (row < rows) reinterpret_cast<uint2*>(codes + row * K)[c] = enc8_e4m3(v[u], mult);
+            if ((c & 3) == 0) {
+                const int64_t j = c >> 2;
+                const int64_t off = mma ? mma_scale_offset(row, j, chunks) : row * (K >> 5) + j;
+                scales[off] = (uint8_t)(e + 127);
+            }
         }
     }
 }
 
 // ---------------------------------------------------------------- NVFP4
-// After the amax pass: two consecutive lanes own one 16-element block.
+// After the amax pass: two consecutive lanes own one 16-element block.  The
+// code multiplier rg / dsb depends only on the block's UE4M3 scale code, so
+// each CTA tabulates it once for all 256 codes (same division, same bits).
 __global__ void __launch_bounds__(256) k_nvfp4_encode(const uint16_t* __restrict__ x, int64_t rows,
                                                       int64_t rows_pad, int64_t K, int64_t ld,
                                                       uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
                                                       float* __restrict__ global,
                                                       const float* __restrict__ partials, int nparts, int mma) {
     __shared__ float red[33];
+    __shared__ float rb_of[256];
     const float A = reduce_partials(partials, nparts, red);
-    float g = 1.0f, q = 1.0f, rg = 1.0f;
+    float g = 1.0f, qm = 1.0f, rg = 1.0f;
     if (A != 0.0f) {
         g = __fdiv_rn(A, kNvfp4Global);
-        q = __fdiv_rn(kE4M3Max, A);
+        qm = __fdiv_rn(kE4M3Max, A);
         rg = __fdiv_rn(kNvfp4Global, A);
     }
+    {
+        const float dsb = e4m3_value((uint32_t)threadIdx.x);
+        rb_of[threadIdx.x] = (dsb == 0.0f) ? 0.0f : __fdiv_rn(rg, dsb);
+    }
+    __syncthreads();
     if (blockIdx.x == 0 && threadIdx.x == 0) *global = g;
-    const int64_t nvr = K >> 3, total = rows_pad * nvr;
+    const uint32_t nvr = (uint32_t)(K >> 3), tpr = (nvr + 31) / 32, total = (uint32_t)rows_pad * tpr;
+    const uint32_t warps = gridDim.x * 8, w0 = blockIdx.x * 8 + (threadIdx.x >> 5);
     const int64_t chunks = K >> 6;
     const int lane = threadIdx.x & 31;
-    for (int64_t vb = blockIdx.x * 256ll + (threadIdx.x & ~31); vb < total; vb += (int64_t)gridDim.x * 256) {
-        const int64_t v = vb + lane;
-        const bool in = v < total;
-        const int64_t row = in ? v / nvr : rows_pad, c = in ? v - row * nvr : 0;
-        const bool valid = row < rows;
-        uint4 w = make_uint4(0, 0, 0, 0);
-        if (valid) w = ld16(x + row * ld + 8 * c);
-        float b = absmax8(w);
-        b = fmaxf(b, __shfl_xor_sync(0xFFFFFFFFu, b, 1));
-        const uint32_t sb = cvt_e4m3x2(__fmul_rn(b, q), 0.0f) & 0xFFu;   // non-negative: UE4M3
-        const float dsb = e4m3_value(sb);
-        const float rb = (dsb == 0.0f) ? 0.0f : __fdiv_rn(rg, dsb);
-        if (valid) reinterpret_cast<uint32_t*>(codes + row * (K >> 1))[c] = enc8_e2m1(w, rb);
-        if (in && (c & 1) == 0) {
-            const int64_t j = c >> 1;
-            const int64_t off = mma ? mma_scale_offset(row, j, chunks) : row * (K >> 4) + j;
-            scales[off] = (uint8_t)sb;
+    for (uint32_t t = w0; t < total; t += warps * kUnroll) {
+        uint4 v[kUnroll];
+        TaskPos q[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; u++) {
+            q[u] = task_pos(t + u * warps, total, tpr, nvr, lane);
+            v[u] = (q[u].in && q[u].row < rows) ? ld16(x + (int64_t)q[u].row * ld + 8 * q[u].c)
+                                                : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; u++) {
+            float b = absmax8(v[u]);
+            b = fmaxf(b, __shfl_xor_sync(0xFFFFFFFFu, b, 1));
+            const uint32_t sb = cvt_e4m3x2(__fmul_rn(b, qm), 0.0f) & 0xFFu;   // non-negative: UE4M3
+            if (!q[u].in) continue;
+            const int64_t row = q[u].row, c = q[u].c;
+            if (row < rows) reinterpret_cast<uint32_t*>(codes + row * (K >> 1))[c] = enc8_e2m1(v[u], rb_of[sb]);
+            if ((c & 1) == 0) {
+                const int64_t j = c >> 1;
+                const int64_t off = mma ? mma_scale_offset(row, j, chunks) : row * (K >> 4) + j;
+                scales[off] = (uint8_t)sb;
+            }
         }
     }
 }
@@ -374,6 +437,14 @@ int grid_for(int64_t work, int per_block) {
     return (int)(b < 1 ? 1 : b);
 }
 
+// Tasks of one tensor, or -1 when their count does not fit the 32-bit walk.
+int64_t task_count(int64_t rows, int64_t K) {
+    const int64_t t = rows * (((K >> 3) + 31) / 32);
+    return t > 0x7FFFFFFFll ? -1 : t;
+}
+
+int task_grid(int64_t tasks) { return grid_for(tasks, 8 * kUnroll); }
+
 template <int T>
 cudaError_t rows_dispatch(int vpt, const uint16_t* x, int64_t rows, int64_t K, int64_t ld, uint8_t* codes,
                           float* scales, cudaStream_t st) {
@@ -411,9 +482,10 @@ cudaError_t launch_fp8_rowwise(const uint16_t* x, int64_t rows, int64_t K, int64
 
 cudaError_t launch_fp8_tensor(const uint16_t* x, int64_t rows, int64_t K, int64_t ld, uint8_t* codes,
                               float* scale, float* partials, int nparts, cudaStream_t st) {
+    const int64_t tasks = task_count(rows, K);
+    if (tasks < 0) return cudaErrorInvalidValue;
     k_amax_partial<<<nparts, 256, 0, st>>>(x, rows, K, ld, partials);
-    k_fp8_tensor_encode<<<grid_for(rows * (K >> 3), 256 * 4), 256, 0, st>>>(x, rows, K, ld, codes, scale,
-                                                                             partials, nparts);
+    k_fp8_tensor_encode<<<task_grid(tasks), 256, 0, st>>>(x, rows, K, ld, codes, scale, partials, nparts);
     return cudaGetLastError();
 }
 
@@ -427,8 +499,9 @@ cudaError_t launch_fp8_block128(const uint16_t* x, int64_t rows, int64_t K, int6
 cudaError_t launch_mxfp8(const uint16_t* x, int64_t rows, int64_t K, int64_t ld, uint8_t* codes,
                          uint8_t* scales, bool mma_layout, cudaStream_t st) {
     const int64_t rows_pad = mma_layout ? (rows + 127) / 128 * 128 : rows;
-    k_mxfp8<<<grid_for(rows_pad * (K >> 3), 256 * 4), 256, 0, st>>>(x, rows, rows_pad, K, ld, codes, scales,
-                                                                      mma_layout ? 1 : 0);
+    const int64_t tasks = task_count(rows_pad, K);
+    if (tasks < 0) return cudaErrorInvalidValue;
+    k_mxfp8<<<task_grid(tasks), 256, 0, st>>>(x, rows, rows_pad, K, ld, codes, scales, mma_layout ? 1 : 0);
     return cudaGetLastError();
 }
 
@@ -436,9 +509,11 @@ cudaError_t launch_nvfp4(const uint16_t* x, int64_t rows, int64_t K, int64_t ld,
                          uint8_t* scales, float* global, bool mma_layout, float* partials, int nparts,
                          cudaStream_t st) {
     const int64_t rows_pad = mma_layout ? (rows + 127) / 128 * 128 : rows;
+    const int64_t tasks = task_count(rows_pad, K);
+    if (tasks < 0) return cudaErrorInvalidValue;
     k_amax_partial<<<nparts, 256, 0, st>>>(x, rows, K, ld, partials);
-    k_nvfp4_encode<<<grid_for(rows_pad * (K >> 3), 256 * 4), 256, 0, st>>>(
-        x, rows, rows_pad, K, ld, codes, scales, global, partials, nparts, mma_layout ? 1 : 0);
+    k_nvfp4_encode<<<task_grid(tasks), 256, 0, st>>>(x, rows, rows_pad, K, ld, codes, scales, global, partials,
+                                                     nparts, mma_layout ? 1 : 0);
     return cudaGetLastError();
 }
 
