@@ -116,16 +116,6 @@ __device__ __forceinline__ void record_timeout(int* status, volatile uint32_t* a
     if (status) atomicExch(status, (int)QLIN_ERR_DEVICE_TIMEOUT);
 }
 
-__device__ __forceinline__ void cluster_sync_all() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ uint32_t cluster_rank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
 // Load from the shared memory of CTA `rank` of this cluster (ordered by the
 // cluster barrier that precedes the reduction, so independent loads may overlap).
 __device__ __forceinline__ float ld_peer_f32(uint32_t local_saddr, uint32_t rank) {
@@ -187,7 +177,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int cs = (int)gridDim.x;                 // cluster size = split-K ways
-    const int rank = (int)cluster_rank();
+    const int rank = (int)cluster_ctarank();
     const int n0 = blockIdx.y * 128, m0 = blockIdx.z * MP;
     const int g0 = (int)((int64_t)p.groups * rank / cs), g1 = (int)((int64_t)p.groups * (rank + 1) / cs);
     const int ng_cta = g1 - g0;                    // 128-K groups of this CTA
