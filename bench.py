@@ -201,6 +201,33 @@ class Job:
         return xb + wb + lin.M * lin.N * 2
 
 
+# DRAM traffic (read + write bytes) of one captured launch of the dominant
+# kernel, from the ncu summary in profiles/gemm_fp8_block_M4096_K3072_N12288.md.
+# It is scaled to the step's average launch by algorithmic bytes, and reported
+# as null once the kernel's source differs from the one the counters came from.
+MEASURED_TRAFFIC = {
+    "gemm_fp8_block": {
+        "dram_bytes": 80784128 + 58381056,
+        "alg_bytes": 4096 * 3072 + 4096 * 4 + 12288 * 3072 + 96 * 24 * 4 + 4096 * 12288 * 2,
+        "source": "serving_amax_reduce_gb300/csrc/gemm_tc.cu",
+        "sha256": "7c80333d773b7dc87e0b495c0573fcd031a24ab82ba204790e9feb543f127d7d",
+        "captured": "M4096 K3072 N12288 (one bench launch)",
+    },
+}
+
+
+def measured_traffic(kernel, alg_bytes_per_launch):
+    import hashlib
+    m = MEASURED_TRAFFIC.get(kernel)
+    if not m:
+        return None, None
+    path = os.path.join(ROOT, m["source"])
+    if not os.path.exists(path) or hashlib.sha256(open(path, "rb").read()).hexdigest() != m["sha256"]:
+        return None, "kernel changed since the counters were taken"
+    return int(round(m["dram_bytes"] * alg_bytes_per_launch / m["alg_bytes"])), \
+        f"ncu capture of {m['captured']}, scaled by algorithmic bytes"
+
+
 def kernel_name(job, op):
     F = job.q.Fmt
     if op == "gemm":
@@ -355,8 +382,10 @@ def run_native(args, rank, world, local_rank):
         per_launch = dr["flops"] / dr["launches"]
         peak = tensor_peak(peaks, dr["wf"], q)
         achieved = per_launch / (dom_ms_per_launch * 1e-3) / 1e12
+        traffic, traffic_src = measured_traffic(dom, dr["bytes"] / dr["launches"])
         roofline = {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 1), "peak": round(peak, 1),
-                    "unit": "TFLOP/s", "frac": round(achieved / peak, 3), "traffic": None,
+                    "unit": "TFLOP/s", "frac": round(achieved / peak, 3), "traffic": traffic,
+                    "traffic_source": traffic_src, "algorithmic_bytes_per_launch": round(dr["bytes"] / dr["launches"]),
                     "peak_source": f"{peak_src} bf16 sustained x nominal format ratio",
                     "algorithmic_per_launch": per_launch}
     else:
