@@ -18,6 +18,9 @@
 //            4-stage shared-memory ring;
 //   warp 1   allocates TMEM; one lane issues tcgen05.mma into the TMEM
 //            accumulator and tcgen05.commit to release each stage;
+//   warps 2-3 NVFP4 only: one lane each copies the stage's X / W scale
+//            chunks smem -> TMEM with tcgen05.cp (12 copies per stage would
+//            otherwise serialize with the MMAs on one issuing thread);
 //   warps 4-11 (two warpgroups, raised to 232 registers with setmaxnreg)
 //            copy the accumulator TMEM -> registers with tcgen05.ld,
 //            release it to the next tile's MMAs at once, then apply the
@@ -26,10 +29,10 @@
 //   FP8 per-tensor  kind::f8f6f4, alpha = s_x * s_w in the epilogue.
 //   FP8 block       kind::f8f6f4 into one of two TMEM partial buffers per
 //                   128-wide K block; the eight epilogue warps promote each
-//                   partial with its fp32 weight-block scale (prefetched
-//                   into registers at tile start) into register
-//                   accumulators (fp32 block scales are not an MMA scale
-//                   type), then multiply by the per-token scale.
+//                   partial with its fp32 weight-block scale (one uniform
+//                   load, a block ahead) into register accumulators (fp32
+//                   block scales are not an MMA scale type), then multiply
+//                   by the per-token scale.
 //   MXFP8           kind::mxf8f6f4.block_scale.scale_vec::1X, UE8M0 scales
 //                   copied smem -> TMEM with tcgen05.cp.
 //   NVFP4           kind::mxf4nvf4.block_scale.scale_vec::4X, UE4M3 scales,
@@ -67,6 +70,9 @@ struct Cfg {
     static constexpr int B_BYTES = BN * BKB;
     // 512-byte scale chunks (128 rows x 4 scales) per 128 rows per stage
     static constexpr int SF_CHUNKS = (KIND == kMxfp8) ? 1 : (KIND == kNvfp4 ? 4 : 0);
+    // NVFP4 has 12 scale-chunk copies per stage: two threads issue them off the
+    // MMA thread; MXFP8's 3 copies stay with the MMA issuer
+    static constexpr bool SPLIT_CP = (KIND == kNvfp4);
     static constexpr int SFA_BYTES = SF_CHUNKS * 512;
     static constexpr int SFB_BYTES = SF_CHUNKS * 512 * (BN / 128);
     static constexpr int KSTEPS = BKB / 32;          // each MMA consumes 32 bytes of K
@@ -79,7 +85,8 @@ struct Cfg {
     static constexpr int STG_BYTES = STG_BOX * STG_BUFS;
     static constexpr int OFF_STG = OFF_SFB + STAGES * SFB_BYTES;
     static constexpr int OFF_BAR = OFF_STG + EPI_WARPS * STG_BYTES;
-    static constexpr int NBAR = 2 * STAGES + 7;      // full[S], empty[S], accf, acce, pfull[2], pempty[2], drain
+    // full[S], empty[S], accf, acce, pfull[2], pempty[2], drain, sfready[S]
+    static constexpr int NBAR = 3 * STAGES + 7;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int SMEM = OFF_MISC + 64 + 1024; // + slack for 1024-byte alignment
     static constexpr uint32_t TMEM_COLS = 512;
@@ -218,6 +225,7 @@ __global__ void __launch_bounds__(Cfg<KIND>::THREADS, 1)
     uint64_t* pfull = acce + 1;             // FP8 block: partial buffer b ready
     uint64_t* pempty = pfull + 2;           // FP8 block: partial buffer b drained
     uint64_t* drain = pempty + 2;
+    uint64_t* sfready = drain + 1;          // MX / NVFP4: stage s's scale factors are in TMEM
     uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);   // tmem base, abort, consumed, issued
     volatile uint32_t* abort_flag = misc + 1;
 
@@ -236,7 +244,8 @@ __global__ void __launch_bounds__(Cfg<KIND>::THREADS, 1)
         mbar_init(pfull + 1, 1);
         mbar_init(pempty + 0, C::EPI_WARPS);
         mbar_init(pempty + 1, C::EPI_WARPS);
-        mbar_init(drain, 1);
+        mbar_init(drain, C::SPLIT_CP ? 3 : 1);   // the MMA issuer (+ the two scale-copy threads)
+        for (int s = 0; s < C::STAGES; s++) mbar_init(sfready + s, 2);
         fence_mbar_init();
         // a launch that follows an expired wait does no work
         misc[1] = (p.status && *reinterpret_cast<volatile int*>(p.status) != 0) ? 1u : 0u;
@@ -327,26 +336,21 @@ __global__ void __launch_bounds__(Cfg<KIND>::THREADS, 1)
                     }
                     d = tmem + (uint32_t)(b * C::BN);
                 }
+                if (C::SPLIT_CP && !wait_or_abort(sfready + s, ph, abort_flag)) {
+                    record_timeout(p.status, abort_flag);
+                    ok = false;
+                    break;
+                }
                 tc_fence_after();
                 const uint32_t a_base = smem_u32(smem + C::OFF_A + s * C::A_BYTES);
                 const uint32_t b_base = smem_u32(smem + C::OFF_B + s * C::B_BYTES);
-                const uint32_t sfa_base = smem_u32(smem + C::OFF_SFA + s * C::SFA_BYTES);
-                const uint32_t sfb_base = smem_u32(smem + C::OFF_SFB + s * C::SFB_BYTES);
                 if (KIND == kMxfp8) {
+                    const uint32_t sfa_base = smem_u32(smem + C::OFF_SFA + s * C::SFA_BYTES);
+                    const uint32_t sfb_base = smem_u32(smem + C::OFF_SFB + s * C::SFB_BYTES);
                     tmem_cp_32x128b_x4(tmem + C::SFA_COL + s * C::SFA_COLS, sdesc_sf(sfa_base));
 #pragma unroll
                     for (int j = 0; j < C::BN / 128; j++)
                         tmem_cp_32x128b_x4(tmem + C::SFB_COL + s * C::SFB_COLS + j * 4, sdesc_sf(sfb_base + j * 512));
-                }
-                if (KIND == kNvfp4) {
-#pragma unroll
-                    for (int c = 0; c < 4; c++) {
-                        tmem_cp_32x128b_x4(tmem + C::SFA_COL + s * C::SFA_COLS + c * 4, sdesc_sf(sfa_base + c * 512));
-#pragma unroll
-                        for (int j = 0; j < C::BN / 128; j++)
-                            tmem_cp_32x128b_x4(tmem + C::SFB_COL + s * C::SFB_COLS + c * 4 * (C::BN / 128) + j * 4,
-                                               sdesc_sf(sfb_base + (j * 4 + c) * 512));
-                    }
                 }
 #pragma unroll
                 for (int c = 0; c < C::KSTEPS; c++) {
@@ -372,6 +376,40 @@ __global__ void __launch_bounds__(Cfg<KIND>::THREADS, 1)
                 misc[2] = kg + 1;
             }
             if (ok && KIND != kFp8Block) tc_commit(accf);
+        }
+    } else if (!skip && C::SPLIT_CP && (warp == 2 || warp == 3) && lane == 0) {
+        // ------------------------------------------------ scale-factor copies (NVFP4)
+        // smem -> TMEM with tcgen05.cp, off the MMA thread: warp 2 copies the
+        // X scales, warp 3 the W scales, into the stage's TMEM slot; the MMA
+        // thread waits for both commits.  A slot is rewritten only after the
+        // stage's TMA has landed again, i.e. after the MMAs that read it ended.
+        uint32_t kg = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+            for (int kb = 0; kb < p.nk; kb++, kg++) {
+                const int s = (int)(kg % C::STAGES);
+                const uint32_t ph = (kg / C::STAGES) & 1u;
+                if (!wait_or_abort(full + s, ph, abort_flag)) {
+                    record_timeout(p.status, abort_flag);
+                    ok = false;
+                    break;
+                }
+                const uint32_t sfa_base = smem_u32(smem + C::OFF_SFA + s * C::SFA_BYTES);
+                const uint32_t sfb_base = smem_u32(smem + C::OFF_SFB + s * C::SFB_BYTES);
+                if (warp == 2) {
+#pragma unroll
+                    for (int c = 0; c < C::SF_CHUNKS; c++)
+                        tmem_cp_32x128b_x4(tmem + C::SFA_COL + s * C::SFA_COLS + c * 4, sdesc_sf(sfa_base + c * 512));
+                } else {
+#pragma unroll
+                    for (int c = 0; c < C::SF_CHUNKS; c++)
+#pragma unroll
+                        for (int j = 0; j < C::BN / 128; j++)
+                            tmem_cp_32x128b_x4(tmem + C::SFB_COL + s * C::SFB_COLS + c * 4 * (C::BN / 128) + j * 4,
+                                               sdesc_sf(sfb_base + (j * C::SF_CHUNKS + c) * 512));
+                }
+                tc_commit(sfready + s);
+            }
         }
     }
     } else {
@@ -487,11 +525,11 @@ __global__ void __launch_bounds__(Cfg<KIND>::THREADS, 1)
         for (uint32_t kg = consumed; kg < issued; kg++)
             mbar_wait(full + (kg % C::STAGES), (kg / C::STAGES) & 1u, kWaitLimitNs);
     }
-    if (*abort_flag && warp == 1 && lane == 0) {
-        // ... and every MMA / scale copy it issued has finished reading
-        // shared memory (a commit with nothing outstanding arrives at once).
+    if (*abort_flag && lane == 0 && (warp == 1 || (C::SPLIT_CP && (warp == 2 || warp == 3)))) {
+        // ... and every MMA / scale copy issued has finished reading shared
+        // memory (a commit with nothing outstanding arrives at once)
         tc_commit(drain);
-        mbar_wait(drain, 0, kWaitLimitNs);
+        if (warp == 1) mbar_wait(drain, 0, kWaitLimitNs);
     }
     __syncthreads();
     if (warp == 1) {
