@@ -371,64 +371,67 @@ __global__ void __launch_bounds__(256) k_nvfp4_encode(const uint16_t* __restrict
 }
 
 // ---------------------------------------------------------------- int4 g128
-// CTA = 64 output channels x one group of 128 k.  Thread t handles rows
-// t/16 + 16i and k-octet t%16; the row's 16 lanes reduce min/max by shuffles.
-// Packed words are transposed through shared memory so that qweight rows
-// (fixed k-octet, consecutive n) are written coalesced.
-__global__ void __launch_bounds__(256) k_int4_g128(const uint16_t* __restrict__ w, int64_t N, int64_t K,
+// One thread per output channel and 128-K group: it reads the group's 256
+// contiguous bytes of its weight row (16 vectors), so min/max, the scale, the
+// zero point and the 16 packed words are all computed once, by one thread.
+// A warp covers 32 consecutive channels, so each qweight row store (fixed
+// k-octet, consecutive n) and each scale store is coalesced; the zero points
+// of 8 channels are OR-ed into one word across 8 lanes.
+__global__ void __launch_bounds__(128) k_int4_g128(const uint16_t* __restrict__ w, int64_t N, int64_t K,
                                                    int64_t ld, int32_t* __restrict__ qweight,
                                                    uint16_t* __restrict__ scales, int32_t* __restrict__ qzeros) {
-    __shared__ uint32_t words[16][65];
-    __shared__ uint32_t zs[64];
-    const int64_t n0 = (int64_t)blockIdx.x * 64, g = blockIdx.y, k0 = g * 128;
-    const int rl = threadIdx.x >> 4, oc = threadIdx.x & 15;
+    const int64_t g = blockIdx.y, k0 = g * 128;
+    const int64_t n = (int64_t)blockIdx.x * 128 + threadIdx.x;
+    const int lane = threadIdx.x & 31;
+    const bool valid = n < N;
+    uint4 v[16];
 #pragma unroll
-    for (int i = 0; i < 4; i++) {
-        const int nl = rl + 16 * i;
-        const int64_t n = n0 + nl;
-        const bool valid = n < N;
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (valid) v = ld16(w + n * ld + k0 + oc * 8);
-        float e[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
-                      bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
-        float mn = 0.0f, mx = 0.0f;
+    for (int o = 0; o < 16; o++) v[o] = valid ? ld16(w + n * ld + k0 + 8 * o) : make_uint4(0, 0, 0, 0);
+    // four independent min/max chains (short dependency chains), then combined
+    float mnv[4] = {0.0f, 0.0f, 0.0f, 0.0f}, mxv[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-        for (int j = 0; j < 8; j++) { mn = fminf(mn, e[j]); mx = fmaxf(mx, e[j]); }
+    for (int o = 0; o < 16; o++) {
+        const uint32_t u[4] = {v[o].x, v[o].y, v[o].z, v[o].w};
 #pragma unroll
-        for (int o = 1; o < 16; o <<= 1) {
-            mn = fminf(mn, __shfl_xor_sync(0xFFFFFFFFu, mn, o));
-            mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+        for (int i = 0; i < 4; i++) {
+            const float a = bf16_lo(u[i]), b = bf16_hi(u[i]);
+            mnv[i] = fminf(mnv[i], fminf(a, b));
+            mxv[i] = fmaxf(mxv[i], fmaxf(a, b));
         }
-        const __nv_bfloat16 sb = __float2bfloat16_rn(__fdiv_rn(__fsub_rn(mx, mn), 15.0f));
-        float s = __bfloat162float(sb);
-        uint16_t sbits = __bfloat16_as_ushort(sb);
-        if (s == 0.0f) { s = 1.0f; sbits = 0x3F80u; }
-        const float r = __fdiv_rn(1.0f, s);
-        const int z = min(max(__float2int_rn(__fmul_rn(-mn, r)), 0), 15);
+    }
+    const float mn = fminf(fminf(mnv[0], mnv[1]), fminf(mnv[2], mnv[3]));
+    const float mx = fmaxf(fmaxf(mxv[0], mxv[1]), fmaxf(mxv[2], mxv[3]));
+    const __nv_bfloat16 sb = __float2bfloat16_rn(__fdiv_rn(__fsub_rn(mx, mn), 15.0f));
+    float s = __bfloat162float(sb);
+    uint16_t sbits = __bfloat16_as_ushort(sb);
+    if (s == 0.0f) { s = 1.0f; sbits = 0x3F80u; }
+    const float r = __fdiv_rn(1.0f, s);
+    const int z = min(max(__float2int_rn(__fmul_rn(-mn, r)), 0), 15);
+    // rint(x*r) + z without a float->int conversion per element: |x*r| <= 15,
+    // and adding 1.5 * 2^23 rounds it to an integer (nearest even) in the low
+    // mantissa bits, so bits(x*r + 1.5*2^23) - bits(1.5*2^23) = rint(x*r).
+    constexpr float kRound = 12582912.0f;
+    const int zoff = (int)0x4B400000 - z;
+#pragma unroll
+    for (int o = 0; o < 16; o++) {
+        const uint32_t u[4] = {v[o].x, v[o].y, v[o].z, v[o].w};
         uint32_t word = 0;
 #pragma unroll
-        for (int j = 0; j < 8; j++) {
-            const int q = min(max(__float2int_rn(__fmul_rn(e[j], r)) + z, 0), 15);
-            word |= (uint32_t)q << (4 * j);
+        for (int i = 0; i < 4; i++) {
+            const int ta = (int)__float_as_uint(__fadd_rn(__fmul_rn(bf16_lo(u[i]), r), kRound)) - zoff;
+            const int tb = (int)__float_as_uint(__fadd_rn(__fmul_rn(bf16_hi(u[i]), r), kRound)) - zoff;
+            const int qa = min(max(ta, 0), 15), qb = min(max(tb, 0), 15);
+            word |= ((uint32_t)qa << (8 * i)) | ((uint32_t)qb << (8 * i + 4));
         }
-        words[oc][nl] = word;
-        if (oc == 0) {
-            zs[nl] = (uint32_t)z;
-            if (valid) scales[g * N + n] = sbits;
-        }
+        if (valid) qweight[(k0 / 8 + o) * N + n] = (int32_t)word;
     }
-    __syncthreads();
-#pragma unroll
-    for (int p = 0; p < 4; p++) {
-        const int idx = threadIdx.x + 256 * p, o = idx >> 6, nl = idx & 63;
-        if (n0 + nl < N) qweight[(k0 / 8 + o) * N + n0 + nl] = (int32_t)words[o][nl];
-    }
-    if (threadIdx.x < 8 && n0 + 8 * threadIdx.x < N) {
-        uint32_t zw = 0;
-#pragma unroll
-        for (int j = 0; j < 8; j++) zw |= zs[8 * threadIdx.x + j] << (4 * j);
-        qzeros[g * (N / 8) + n0 / 8 + threadIdx.x] = (int32_t)zw;
-    }
+    if (valid) scales[g * N + n] = sbits;
+    // N is a multiple of 8, so an aligned group of 8 lanes is all valid or all not
+    uint32_t zw = (uint32_t)z << (4 * (lane & 7));
+    zw |= __shfl_xor_sync(0xFFFFFFFFu, zw, 1);
+    zw |= __shfl_xor_sync(0xFFFFFFFFu, zw, 2);
+    zw |= __shfl_xor_sync(0xFFFFFFFFu, zw, 4);
+    if (valid && (lane & 7) == 0) qzeros[g * (N / 8) + n / 8] = (int32_t)zw;
 }
 
 int grid_for(int64_t work, int per_block) {
@@ -519,8 +522,8 @@ cudaError_t launch_nvfp4(const uint16_t* x, int64_t rows, int64_t K, int64_t ld,
 
 cudaError_t launch_int4_g128(const uint16_t* w, int64_t N, int64_t K, int64_t ld, int32_t* qweight,
                              uint16_t* scales, int32_t* qzeros, cudaStream_t st) {
-    dim3 grid((unsigned)((N + 63) / 64), (unsigned)(K / 128));
-    k_int4_g128<<<grid, 256, 0, st>>>(w, N, K, ld, qweight, scales, qzeros);
+    dim3 grid((unsigned)((N + 127) / 128), (unsigned)(K / 128));
+    k_int4_g128<<<grid, 128, 0, st>>>(w, N, K, ld, qweight, scales, qzeros);
     return cudaGetLastError();
 }
 
