@@ -76,12 +76,14 @@ def _load():
             "oracle_quant_fp8_block128": ([P, I64, I64, I64, P, P], None),
             "oracle_quant_mxfp8": ([P, I64, I64, I64, P, P], None),
             "oracle_quant_nvfp4": ([P, I64, I64, I64, P, P, P], None),
+            "oracle_quant_mxfp4": ([P, I64, I64, I64, P, P], None),
             "oracle_quant_int4_g128": ([P, I64, I64, I64, P, P, P], None),
             "oracle_dequant_fp8_tensor": ([P, I64, I64, F, P], None),
             "oracle_dequant_fp8_token": ([P, I64, I64, P, P], None),
             "oracle_dequant_fp8_block128": ([P, I64, I64, P, P], None),
             "oracle_dequant_mxfp8": ([P, I64, I64, P, P], None),
             "oracle_dequant_nvfp4": ([P, I64, I64, P, F, P], None),
+            "oracle_dequant_mxfp4": ([P, I64, I64, P, P], None),
             "oracle_dequant_int4_g128": ([P, P, P, I64, I64, P], None),
         }
         for name, (args, res) in sig.items():
@@ -198,6 +200,18 @@ def quant_nvfp4(x):
     return packed, sc, g[0]
 
 
+def quant_mxfp4(x):
+    """MXFP4 -> (packed E2M1 uint8 [R,K/2], E8M0 scale codes uint8 [R,K/32])."""
+    x = _bf16_bits(x)
+    R, K = x.shape
+    if K % 32:
+        raise ValueError("MXFP4 needs K multiple of 32")
+    packed = np.empty((R, K // 2), np.uint8)
+    sc = np.empty((R, K // 32), np.uint8)
+    _load().oracle_quant_mxfp4(_p(x), R, K, K, _p(packed), _p(sc))
+    return packed, sc
+
+
 def quant_int4_g128(w):
     """int4 asymmetric g128 RTN of W [N,K] -> (qweight int32 [K/8,N],
     scales bf16 bits uint16 [K/128,N], qzeros int32 [K/128,N/8])."""
@@ -254,6 +268,15 @@ def dequant_nvfp4(packed, scale_codes, global_scale):
     R, K = packed.shape[0], packed.shape[1] * 2
     out = _f64((R, K))
     _load().oracle_dequant_nvfp4(_p(packed), R, K, _p(scale_codes), float(global_scale), _p(out))
+    return out
+
+
+def dequant_mxfp4(packed, scale_codes):
+    packed = np.ascontiguousarray(packed, np.uint8)
+    scale_codes = np.ascontiguousarray(scale_codes, np.uint8)
+    R, K = packed.shape[0], packed.shape[1] * 2
+    out = _f64((R, K))
+    _load().oracle_dequant_mxfp4(_p(packed), R, K, _p(scale_codes), _p(out))
     return out
 
 

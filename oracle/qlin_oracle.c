@@ -42,6 +42,12 @@
  *       q = clamp(rint(x*r) + z); z stored without the "-1" offset.
  *   R5  conversions to E4M3/E2M1 round to nearest, ties to the even code,
  *       saturate to the largest finite magnitude and keep the sign of zero.
+ *   R6  MXFP4 (the same page and section: the online MXFP4 path mirrors
+ *       MXFP8 with float4_e2m1fn_x2 codes, two per byte): the R2 rule with
+ *       the E2M1 exponent, e = clamp(floor(log2 amax) - 2, -127, 127)
+ *       (2 = exponent of 6, the largest E2M1 power-of-two range), codes =
+ *       E2M1(x * 2^-e) packed two per byte, lower K index in the low nibble;
+ *       amax == 0 gives scale code 0.
  */
 #include <math.h>
 #include <stdint.h>
@@ -240,6 +246,35 @@ void oracle_quant_mxfp8(const uint16_t *x, int64_t rows, int64_t K, int64_t ld,
 
 /* K multiple of 16.  packed codes: rows x (K/2) bytes (lower K index in the
  * low nibble); block scale codes: rows x (K/16); global: one float. */
+/* MXFP4: E2M1 codes + E8M0 exponent per 32 along K (R6)               */
+void oracle_quant_mxfp4(const uint16_t *x, int64_t rows, int64_t K, int64_t ld,
+                        uint8_t *packed, uint8_t *scale_codes)
+{
+    int64_t nb = K / 32;
+    for (int64_t i = 0; i < rows; i++)
+        for (int64_t b = 0; b < nb; b++) {
+            const uint16_t *g = x + i * ld + b * 32;
+            float amax = 0.0f;
+            for (int k = 0; k < 32; k++)
+                amax = fmaxf(amax, fabsf(oracle_bf16_to_f32(g[k])));
+            int e;
+            if (amax == 0.0f) {
+                e = -127;
+            } else {
+                e = oracle_floor_log2(amax) - 2;
+                if (e < -127) e = -127;
+                if (e > 127) e = 127;
+            }
+            float mult = ldexpf(1.0f, -e);                /* 2^-e, exact */
+            for (int k = 0; k < 32; k += 2) {
+                uint8_t lo = oracle_enc_e2m1(oracle_bf16_to_f32(g[k]) * mult);
+                uint8_t hi = oracle_enc_e2m1(oracle_bf16_to_f32(g[k + 1]) * mult);
+                packed[i * (K / 2) + (b * 32 + k) / 2] = (uint8_t)(lo | (hi << 4));
+            }
+            scale_codes[i * nb + b] = (uint8_t)(e + 127);
+        }
+}
+
 void oracle_quant_nvfp4(const uint16_t *x, int64_t rows, int64_t K, int64_t ld,
                         uint8_t *packed, uint8_t *scale_codes, float *global)
 {
@@ -353,6 +388,17 @@ void oracle_dequant_mxfp8(const uint8_t *codes, int64_t rows, int64_t K,
         for (int64_t k = 0; k < K; k++)
             out[i * K + k] = oracle_dec_e4m3(codes[i * K + k])
                              * oracle_dec_e8m0(scale_codes[i * (K / 32) + k / 32]);
+}
+
+void oracle_dequant_mxfp4(const uint8_t *packed, int64_t rows, int64_t K,
+                          const uint8_t *scale_codes, double *out)
+{
+    for (int64_t i = 0; i < rows; i++)
+        for (int64_t k = 0; k < K; k++) {
+            uint8_t byte = packed[i * (K / 2) + k / 2];
+            uint8_t c = (k % 2) ? (byte >> 4) : (byte & 0xF);
+            out[i * K + k] = oracle_dec_e2m1(c) * oracle_dec_e8m0(scale_codes[i * (K / 32) + k / 32]);
+        }
 }
 
 void oracle_dequant_nvfp4(const uint8_t *packed, int64_t rows, int64_t K,

@@ -247,6 +247,87 @@ def test_nvfp4_dequant_close(orc):
     assert np.all(np.abs(xh - xv) <= bound)
 
 
+# ------------------------------------------------------------------ MXFP4
+def test_mxfp4_shared_exponent_rule(orc):
+    # OCP MX rule with the E2M1 element: scale = largest power of two <= amax,
+    # divided by 4 (2^2, the exponent of 6, the largest E2M1 binade)
+    x = bf16_bits(inputs.outlier_channel_bf16(64, 512, 31))
+    xv = vals(x)
+    packed, sc = orc.quant_mxfp4(x)
+    scale = np.vectorize(orc.dec_e8m0)(sc)
+    amax = np.abs(xv).reshape(64, 16, 32).max(-1)
+    p2 = np.array([[2.0 ** (math.frexp(a)[1] - 1) for a in row] for row in amax])
+    assert np.array_equal(scale, p2 / 4)
+    d = dec_vec(orc.dec_e2m1, unpack_e2m1(packed))
+    target = xv / np.repeat(scale, 32, 1)                               # exact: power-of-two scaling
+    assert_nearest(d, target, E2M1_POS)
+    # the amax element lands in [4, 6] (saturating from [6, 8))
+    at = np.abs(xv).reshape(64, 16, 32) == amax[..., None]
+    dm = np.abs(d).reshape(64, 16, 32)[at]
+    assert np.all((dm >= 4) & (dm <= 6))
+
+
+def test_mxfp4_exact_bruteforce_small(orc):
+    from test_oracle_codecs import brute_nearest
+    table = [(c, orc.dec_e2m1(c)) for c in range(16)]
+    x = bf16_bits(inputs.normal_bf16((2, 64), 3.0, 45))
+    packed, sc = orc.quant_mxfp4(x)
+    codes = unpack_e2m1(packed)
+    xv = vals(x)
+    for i in range(2):
+        for k in range(64):
+            v = xv[i, k] / orc.dec_e8m0(int(sc[i, k // 32]))
+            assert codes[i, k] == brute_nearest(v, table, 6.0, 1)
+
+
+def test_mxfp4_worked_block(orc):
+    # a block of exactly representable values at scale 2^3: amax 48 -> floor(log2) 5 -> e = 3;
+    # codes are the E2M1 table itself, ties round to the even code, 7 saturates to 6
+    vals_ = [48, 32, 24, 16, 12, 8, 4, 0, -48, -4, 20, 40, 2, 6, 56, 1] + [0] * 16
+    x = bf16_bits(torch.tensor([vals_], dtype=torch.bfloat16))
+    packed, sc = orc.quant_mxfp4(x)
+    assert sc[0, 0] == 127 + 3
+    codes = unpack_e2m1(packed)[0]
+    # 20/8 = 2.5 -> tie between 2 (code 4) and 3 (code 5) -> 4; 40/8 = 5 -> tie 4|6 -> 4 (code 6)
+    # 2/8 = 0.25 -> tie 0|0.5 -> 0; 6/8 = 0.75 -> tie 0.5|1 -> 1 (code 2); 56/8 = 7 -> saturates to 6
+    # 1/8 = 0.125 -> 0
+    want = [0x7, 0x6, 0x5, 0x4, 0x3, 0x2, 0x1, 0x0, 0xF, 0x9, 0x4, 0x6, 0x0, 0x2, 0x7, 0x0] + [0] * 16
+    assert list(codes) == want
+    assert packed[0, 0] == 0x67            # k=0 -> low nibble (6 -> 0x7), k=1 -> high nibble (4 -> 0x6)
+    dq = orc.dequant_mxfp4(packed, sc)[0]
+    assert list(dq[:8]) == [48, 32, 24, 16, 12, 8, 4, 0]
+
+
+def test_mxfp4_scale_offset_from_mxfp8(orc):
+    # same MX rule, element exponents 2 (E2M1) and 8 (E4M3): the scale codes differ by 6
+    x = bf16_bits(inputs.normal_bf16((8, 256), 1.0, 47))
+    _, s4 = orc.quant_mxfp4(x)
+    _, s8 = orc.quant_mxfp8(x)
+    assert np.array_equal(s4.astype(int), s8.astype(int) + 6)
+
+
+def test_mxfp4_scale_by_two_and_zero(orc):
+    t = inputs.normal_bf16((16, 256), 1.0, 49)
+    p1, s1 = orc.quant_mxfp4(bf16_bits(t))
+    p2, s2 = orc.quant_mxfp4(bf16_bits(t * 2))
+    assert np.array_equal(p1, p2) and np.array_equal(s2.astype(int), s1.astype(int) + 1)
+    z = np.zeros((4, 64), np.uint16)
+    pz, sz = orc.quant_mxfp4(z)
+    assert not pz.any() and not sz.any()
+
+
+def test_mxfp4_dequant_close(orc):
+    x = bf16_bits(inputs.normal_bf16((32, 128), 1.0, 51))
+    xv = vals(x)
+    packed, sc = orc.quant_mxfp4(x)
+    xh = orc.dequant_mxfp4(packed, sc)
+    unit = np.repeat(np.vectorize(orc.dec_e8m0)(sc), 32, 1)
+    bound = half_step(E2M1_POS, xv / unit) * unit * (1 + 1e-9)
+    sat = np.abs(xv / unit) > 6                                        # saturated: off by up to 2 units
+    assert np.all(np.abs(xh - xv)[~sat] <= bound[~sat])
+    assert np.all(np.abs(xh - xv)[sat] <= 2 * unit[sat])
+
+
 # ------------------------------------------------------------------ int4
 def unpack_int4(qweight, qzeros, N, K):
     """GPTQ-style layout: k = 8i + j in bits [4j, 4j+4) of qweight[i, n];
