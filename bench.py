@@ -52,12 +52,16 @@ def parse_args():
     ap.add_argument("--rows-json", default=None, help="also write the per-row breakdown here")
     ap.add_argument("--eager", action="store_true", help="launch call by call instead of replaying a CUDA graph")
     ap.add_argument("--only", default=None, help="keep only linears whose name contains this string")
+    ap.add_argument("--next", action="store_true",
+                    help="measure the next rows instead (MXFP4 W4A4 on the MXFP8 workload's shapes)")
     return ap.parse_args()
 
 
 # ---------------------------------------------------------------- workload description
-def workload_linears():
+def workload_linears(next_rows: bool = False):
     from serving_amax_reduce_gb300 import inputs as I
+    if next_rows:
+        return [("mxfp4", I.mxfp4_linear(K, N)) for (K, N) in I.MXFP8_SHAPES]
     lins = [("fp8_tensor", I.fp8_tensor_linear())]
     for (K, N) in I.W4A16_SHAPES:
         for M in I.W4A16_M:
@@ -73,6 +77,11 @@ def workload_linears():
 
 
 def config_block(args):
+    if args.next:
+        return {"workload": "next-rows-mxfp4-w4a4",
+                "workloads": ["mxfp4 W4A4 M20280 (K,N){(5120,13824),(13824,5120),(5120,5120)}"],
+                "step": "per linear: weight quantize + activation quantize + quantized GEMM",
+                "l2": "inputs larger than L2", "parallelism": f"replicas x{args.gpus}"}
     return {
         "workload": WORKLOAD,
         "workloads": ["fp8_tensor M128 K1024 N1024",
@@ -144,11 +153,11 @@ class Job:
         self.x = lin.make_x(device=dev)
         self.w = lin.make_w(device=dev)
         wf = {"fp8_tensor": F.FP8_TENSOR, "fp8_block128": F.FP8_BLOCK128, "mxfp8": F.MXFP8, "nvfp4": F.NVFP4,
-              "int4_g128": F.INT4_G128_ASYM}[lin.w_fmt]
+              "int4_g128": F.INT4_G128_ASYM, "mxfp4": F.MXFP4}[lin.w_fmt]
         xf = {"fp8_tensor": F.FP8_TENSOR, "fp8_token": F.FP8_TOKEN, "mxfp8": F.MXFP8, "nvfp4": F.NVFP4,
-              "bf16": F.BF16}[lin.x_fmt]
+              "bf16": F.BF16, "mxfp4": F.MXFP4}[lin.x_fmt]
         self.wf, self.xf = wf, xf
-        self.layout = L.MMA if wf in (F.MXFP8, F.NVFP4) else L.CANONICAL
+        self.layout = L.MMA if wf in (F.MXFP8, F.NVFP4, F.MXFP4) else L.CANONICAL
         self.wb = q.alloc_quant(wf, lin.N, lin.K, self.layout, dev)
         self.xb = q.alloc_quant(xf, lin.M, lin.K, self.layout, dev) if xf != F.BF16 else None
         self.y = torch.empty(lin.M, lin.N, dtype=torch.bfloat16, device=dev)
@@ -232,15 +241,15 @@ def kernel_name(job, op):
     F = job.q.Fmt
     if op == "gemm":
         return {F.FP8_TENSOR: "gemm_fp8_tensor", F.FP8_BLOCK128: "gemm_fp8_block", F.MXFP8: "gemm_mxfp8",
-                F.NVFP4: "gemm_nvfp4", F.INT4_G128_ASYM: "gemm_w4a16"}[job.wf]
+                F.NVFP4: "gemm_nvfp4", F.INT4_G128_ASYM: "gemm_w4a16", F.MXFP4: "gemm_mxfp4"}[job.wf]
     fmt = job.wf if op == "quant_w" else job.xf
     return "quant_" + {F.FP8_TENSOR: "fp8_tensor", F.FP8_TOKEN: "fp8_token", F.FP8_BLOCK128: "fp8_block128",
-                       F.MXFP8: "mxfp8", F.NVFP4: "nvfp4", F.INT4_G128_ASYM: "int4_g128"}[fmt]
+                       F.MXFP8: "mxfp8", F.NVFP4: "nvfp4", F.INT4_G128_ASYM: "int4_g128", F.MXFP4: "mxfp4"}[fmt]
 
 
 def tensor_peak(peaks, wf, q, sustained=True):
     bf16 = peaks.get("bf16_tflops_sustained" if sustained else "bf16_tflops") or (1700.0 if sustained else 1900.0)
-    ratio = FP4_RATIO if wf == q.Fmt.NVFP4 else (1.0 if wf == q.Fmt.INT4_G128_ASYM else FP8_RATIO)
+    ratio = FP4_RATIO if wf in (q.Fmt.NVFP4, q.Fmt.MXFP4) else (1.0 if wf == q.Fmt.INT4_G128_ASYM else FP8_RATIO)
     return bf16 * ratio
 
 
@@ -259,7 +268,8 @@ def run_native(args, rank, world, local_rank):
     peak_src = "measured" if peaks else "fallback"
     hbm_peak = peaks.get("hbm_gbs", 6800.0)
 
-    jobs = [Job(g, lin, dev, q) for g, lin in workload_linears() if not args.only or args.only in lin.name]
+    jobs = [Job(g, lin, dev, q) for g, lin in workload_linears(args.next)
+            if not args.only or args.only in lin.name]
     if not jobs:
         raise SystemExit(f"--only {args.only!r} matches no linear")
     # distinct weights are quantized once per step (several linears may share a W shape but not a W)
@@ -605,7 +615,7 @@ def main():
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl")
     res, _ = run_native(args, rank, world, local_rank)
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.next:
         res["cpu_baseline"] = cpu_baseline()
     if args.rows_json and rank == 0:
         json.dump(res, open(args.rows_json, "w"), indent=1)

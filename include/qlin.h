@@ -67,13 +67,19 @@ typedef enum {
     QLIN_MXFP8 = 3,          /* E4M3 codes, one E8M0 scale byte per 32 along K     */
     QLIN_NVFP4 = 4,          /* E2M1 codes 2/byte, UE4M3 per 16, fp32 per tensor   */
     QLIN_INT4_G128_ASYM = 5, /* uint4 codes 8/int32, bf16 scale + uint4 zero / 128 */
-    QLIN_BF16 = 6            /* unquantized bf16 (the activation side of W4A16)    */
+    QLIN_BF16 = 6,           /* unquantized bf16 (the activation side of W4A16)    */
+    /* E2M1 codes 2/byte (lower k in the low nibble), one E8M0 scale byte per
+     * 32 along K by the MX shared-exponent rule with the E2M1 element:
+     * "vLLM-Omni 在线量化（Online Quantization）完全指南", section
+     * "在线量化的底层工作原理" (the online MXFP4 path mirrors MXFP8 with
+     * float4_e2m1fn_x2 codes; W4A4).                                          */
+    QLIN_MXFP4 = 7
 } qlin_format;
 
 typedef enum {
-    /* Row-major [rows, K/G] scale tensor (G = 32 MXFP8, 16 NVFP4).            */
+    /* Row-major [rows, K/G] scale tensor (G = 32 MXFP8 / MXFP4, 16 NVFP4).   */
     QLIN_SCALE_CANONICAL = 0,
-    /* Tensor-core-ready tiling, MXFP8 and NVFP4 only: for each 128-row tile
+    /* Tensor-core-ready tiling, MXFP8, MXFP4 and NVFP4 only: for each 128-row tile
      * (rows padded up to a multiple of 128 with scale code 0) and each chunk
      * of 4 consecutive scales along K, 512 contiguous bytes; the scale of
      * row r (r < 128 within the tile) and chunk position j (0..3) sits at
@@ -99,13 +105,14 @@ const char *qlin_status_string(qlin_status s);
  * elements (rows = N for weights, M for activations).  0 means "not used by
  * this format" or invalid arguments.                                        */
 
-/* Codes: FP8 formats rows*K; NVFP4 rows*K/2 (lower k in the low nibble);
+/* Codes: FP8 formats rows*K; NVFP4 and MXFP4 rows*K/2 (lower k in the low nibble);
  * INT4 (K/8)*rows*4 as int32 [K/8, rows], k = 8i+j in bits [4j,4j+4).       */
 size_t qlin_codes_bytes(qlin_format fmt, int64_t rows, int64_t K);
 
 /* Scales: FP8_TENSOR 4 (one float); FP8_TOKEN rows*4; FP8_BLOCK128
  * (rows/128)*(K/128)*4 row-major; MXFP8 rows*K/32 (canonical) or
- * ceil(rows/128)*128*K/32 (MMA); NVFP4 rows*K/16 or ceil(rows/128)*128*K/16;
+ * ceil(rows/128)*128*K/32 (MMA), the same for MXFP4; NVFP4 rows*K/16 or
+ * ceil(rows/128)*128*K/16;
  * INT4 (K/128)*rows*2, bf16 [K/128, rows].                                  */
 size_t qlin_scales_bytes(qlin_format fmt, qlin_scale_layout layout, int64_t rows, int64_t K);
 
@@ -130,11 +137,12 @@ size_t qlin_gemm_workspace_bytes(qlin_format w_fmt, qlin_format x_fmt,
  *   scales_dev         qlin_scales_bytes(fmt, layout, rows, K) bytes
  *   zeros_dev          INT4 only (else NULL)
  *   global_dev         NVFP4 only: one float, the per-tensor scale g
- *   layout             QLIN_SCALE_MMA is accepted for MXFP8 and NVFP4 only
+ *   layout             QLIN_SCALE_MMA is accepted for MXFP8, MXFP4 and NVFP4 only
  *   workspace_dev      qlin_quant_workspace_bytes(...) bytes (NULL if 0)
  * Requirements: src and ld*2 bytes 16-byte aligned; K % 8 == 0;
  *   FP8_BLOCK128: rows % 128 == 0 and K % 128 == 0; MXFP8: K % 32 == 0
- *   (K % 128 == 0 for the MMA layout); NVFP4: K % 16 == 0 (K % 64 for MMA);
+ *   (K % 128 == 0 for the MMA layout), the same for MXFP4; NVFP4: K % 16 == 0
+ *   (K % 64 for MMA);
  *   INT4: rows % 8 == 0 and K % 128 == 0.
  * Errors: QLIN_ERR_INVALID_ARG, QLIN_ERR_ALIGNMENT, QLIN_ERR_UNSUPPORTED
  *   (QLIN_BF16, or INT4 through qlin_quantize_act), QLIN_ERR_WORKSPACE,
@@ -162,11 +170,12 @@ qlin_status qlin_quantize_act(qlin_format fmt, const void *x_bf16_dev, int64_t M
  *   MXFP8, MXFP8           : scales in QLIN_SCALE_MMA layout (K % 128 == 0)
  *   NVFP4, NVFP4           : scales in QLIN_SCALE_MMA layout, x_global and
  *                            w_global one float each (K % 256 == 0)
+ *   MXFP4, MXFP4           : scales in QLIN_SCALE_MMA layout (K % 256 == 0)
  *   INT4_G128_ASYM, BF16   : x = bf16 activations [M,K] row-major; w_codes
  *                            qweight, w_scales bf16, w_zeros qzeros (K % 128 == 0,
  *                            N % 8 == 0); workspace per qlin_gemm_workspace_bytes
  * Other pairs return QLIN_ERR_UNSUPPORTED.  All operand rows are contiguous
- * (leading dimension K, or K/2 bytes for NVFP4 codes); ldy >= N and ldy*2
+ * (leading dimension K, or K/2 bytes for NVFP4 / MXFP4 codes); ldy >= N and ldy*2
  * bytes 16-byte aligned.  M may be any value >= 1 (the row tail is handled
  * in the kernels; buffers are not padded).                                  */
 qlin_status qlin_gemm(qlin_format w_fmt, qlin_format x_fmt, int64_t M, int64_t N, int64_t K,

@@ -11,7 +11,9 @@ namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-bool is_quant_format(qlin_format f) { return f >= QLIN_FP8_TENSOR && f <= QLIN_INT4_G128_ASYM; }
+bool is_quant_format(qlin_format f) {
+    return (f >= QLIN_FP8_TENSOR && f <= QLIN_INT4_G128_ASYM) || f == QLIN_MXFP4;
+}
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
@@ -21,12 +23,14 @@ qlin_status launch_status(cudaError_t e) { return e == cudaSuccess ? QLIN_OK : Q
 qlin_status check_quant_shape(qlin_format fmt, qlin_scale_layout layout, int64_t rows, int64_t K) {
     if (rows < 1 || K < 8 || (K & 7) || rows > 0x7FFFFFFFll) return QLIN_ERR_INVALID_ARG;
     if (layout != QLIN_SCALE_CANONICAL && layout != QLIN_SCALE_MMA) return QLIN_ERR_INVALID_ARG;
-    if (layout == QLIN_SCALE_MMA && fmt != QLIN_MXFP8 && fmt != QLIN_NVFP4) return QLIN_ERR_UNSUPPORTED;
+    if (layout == QLIN_SCALE_MMA && fmt != QLIN_MXFP8 && fmt != QLIN_MXFP4 && fmt != QLIN_NVFP4)
+        return QLIN_ERR_UNSUPPORTED;
     switch (fmt) {
         case QLIN_FP8_TENSOR:
         case QLIN_FP8_TOKEN: return QLIN_OK;
         case QLIN_FP8_BLOCK128: return (rows % 128 || K % 128) ? QLIN_ERR_INVALID_ARG : QLIN_OK;
         case QLIN_MXFP8:
+        case QLIN_MXFP4:
             if (K % 32) return QLIN_ERR_INVALID_ARG;
             return (layout == QLIN_SCALE_MMA && K % 128) ? QLIN_ERR_INVALID_ARG : QLIN_OK;
         case QLIN_NVFP4:
@@ -69,6 +73,8 @@ qlin_status quantize(qlin_format fmt, const void* src, int64_t rows, int64_t K, 
             return launch_status(launch_fp8_block128(x, rows, K, ld, c, static_cast<float*>(scales), st));
         case QLIN_MXFP8:
             return launch_status(launch_mxfp8(x, rows, K, ld, c, static_cast<uint8_t*>(scales), mma, st));
+        case QLIN_MXFP4:
+            return launch_status(launch_mxfp4(x, rows, K, ld, c, static_cast<uint8_t*>(scales), mma, st));
         case QLIN_NVFP4:
             return launch_status(launch_nvfp4(x, rows, K, ld, c, static_cast<uint8_t*>(scales), global, mma,
                                               static_cast<float*>(ws), amax_partials(rows, K), st));
@@ -106,7 +112,8 @@ size_t qlin_codes_bytes(qlin_format fmt, int64_t rows, int64_t K) {
         case QLIN_FP8_TOKEN:
         case QLIN_FP8_BLOCK128:
         case QLIN_MXFP8: return (size_t)(rows * K);
-        case QLIN_NVFP4: return (size_t)(rows * (K / 2));
+        case QLIN_NVFP4:
+        case QLIN_MXFP4: return (size_t)(rows * (K / 2));
         case QLIN_INT4_G128_ASYM: return (size_t)((K / 8) * rows * 4);
         default: return 0;
     }
@@ -119,7 +126,8 @@ size_t qlin_scales_bytes(qlin_format fmt, qlin_scale_layout layout, int64_t rows
         case QLIN_FP8_TENSOR: return 4;
         case QLIN_FP8_TOKEN: return (size_t)(rows * 4);
         case QLIN_FP8_BLOCK128: return (size_t)((rows / 128) * (K / 128) * 4);
-        case QLIN_MXFP8: return (size_t)((layout == QLIN_SCALE_MMA ? rows_pad : rows) * (K / 32));
+        case QLIN_MXFP8:
+        case QLIN_MXFP4: return (size_t)((layout == QLIN_SCALE_MMA ? rows_pad : rows) * (K / 32));
         case QLIN_NVFP4: return (size_t)((layout == QLIN_SCALE_MMA ? rows_pad : rows) * (K / 16));
         case QLIN_INT4_G128_ASYM: return (size_t)((K / 128) * rows * 2);
         default: return 0;
@@ -192,6 +200,13 @@ qlin_status qlin_gemm(qlin_format w_fmt, qlin_format x_fmt, int64_t M, int64_t N
         if (K % 128) return QLIN_ERR_INVALID_ARG;
         if (!aligned16(x_scales_dev) || !aligned16(w_scales_dev)) return QLIN_ERR_ALIGNMENT;
         return launch_status(launch_gemm_mxfp8(a, st));
+    }
+    if (w_fmt == QLIN_MXFP4 && x_fmt == QLIN_MXFP4) {
+        if (layout != QLIN_SCALE_MMA) return QLIN_ERR_UNSUPPORTED;
+        if (!x_scales_dev || !w_scales_dev) return QLIN_ERR_INVALID_ARG;
+        if (K % 256) return QLIN_ERR_INVALID_ARG;
+        if (!aligned16(x_scales_dev) || !aligned16(w_scales_dev)) return QLIN_ERR_ALIGNMENT;
+        return launch_status(launch_gemm_mxfp4(a, st));
     }
     if (w_fmt == QLIN_NVFP4 && x_fmt == QLIN_NVFP4) {
         if (layout != QLIN_SCALE_MMA) return QLIN_ERR_UNSUPPORTED;

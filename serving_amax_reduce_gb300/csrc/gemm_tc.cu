@@ -18,9 +18,9 @@
 //            4-stage shared-memory ring;
 //   warp 1   allocates TMEM; one lane issues tcgen05.mma into the TMEM
 //            accumulator and tcgen05.commit to release each stage;
-//   warps 2-3 NVFP4 only: one lane each copies the stage's X / W scale
-//            chunks smem -> TMEM with tcgen05.cp (12 copies per stage would
-//            otherwise serialize with the MMAs on one issuing thread);
+//   warps 2-3 NVFP4 / MXFP4: one lane each copies the stage's X / W scale
+//            chunks smem -> TMEM with tcgen05.cp (12 / 6 copies per stage
+//            would otherwise serialize with the MMAs on one issuing thread);
 //   warps 4-11 (two warpgroups, raised to 232 registers with setmaxnreg)
 //            copy the accumulator TMEM -> registers with tcgen05.ld,
 //            release it to the next tile's MMAs at once, then apply the
@@ -37,6 +37,8 @@
 //                   copied smem -> TMEM with tcgen05.cp.
 //   NVFP4           kind::mxf4nvf4.block_scale.scale_vec::4X, UE4M3 scales,
 //                   alpha = g_x * g_w.
+//   MXFP4 (W4A4)    kind::mxf4nvf4.block_scale.scale_vec::2X, UE8M0 scales
+//                   (the online MXFP4 path of the same page).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -50,7 +52,7 @@ namespace {
 
 using namespace ptx;
 
-enum Kind { kFp8Tensor = 0, kFp8Block = 1, kMxfp8 = 2, kNvfp4 = 3 };
+enum Kind { kFp8Tensor = 0, kFp8Block = 1, kMxfp8 = 2, kNvfp4 = 3, kMxfp4 = 4 };
 
 constexpr int BM = 128;              // tile rows (X rows) = MMA M
 constexpr int BKB = 128;             // K bytes per stage: 128 fp8 or 256 fp4 (one swizzle row)
@@ -69,10 +71,10 @@ struct Cfg {
     static constexpr int A_BYTES = BM * BKB;
     static constexpr int B_BYTES = BN * BKB;
     // 512-byte scale chunks (128 rows x 4 scales) per 128 rows per stage
-    static constexpr int SF_CHUNKS = (KIND == kMxfp8) ? 1 : (KIND == kNvfp4 ? 4 : 0);
+    static constexpr int SF_CHUNKS = (KIND == kMxfp8) ? 1 : (KIND == kNvfp4 ? 4 : (KIND == kMxfp4 ? 2 : 0));
     // NVFP4 has 12 scale-chunk copies per stage: two threads issue them off the
     // MMA thread; MXFP8's 3 copies stay with the MMA issuer
-    static constexpr bool SPLIT_CP = (KIND == kNvfp4);
+    static constexpr bool SPLIT_CP = (KIND == kNvfp4 || KIND == kMxfp4);
     static constexpr int SFA_BYTES = SF_CHUNKS * 512;
     static constexpr int SFB_BYTES = SF_CHUNKS * 512 * (BN / 128);
     static constexpr int KSTEPS = BKB / 32;          // each MMA consumes 32 bytes of K
@@ -107,6 +109,8 @@ __host__ __device__ constexpr uint32_t idesc_for() {
         return (1u << 4) /* D f32 */ | (0u << 7) /* A e4m3 */ | (0u << 10) /* B e4m3 */ | n | m;
     if (KIND == kMxfp8)
         return (0u << 7) | (0u << 10) | n | (1u << 23) /* UE8M0 scales */ | m;
+    if (KIND == kMxfp4)
+        return (1u << 7) /* A e2m1 */ | (1u << 10) /* B e2m1 */ | n | (1u << 23) /* UE8M0 scales */ | m;
     return (1u << 7) /* A e2m1 */ | (1u << 10) /* B e2m1 */ | n | (0u << 23) /* UE4M3 scales */ | m;
 }
 
@@ -363,6 +367,12 @@ __global__ void __launch_bounds__(Cfg<KIND>::THREADS, 1)
                         const uint32_t id = idesc | ((uint32_t)c << 4) | ((uint32_t)c << 29);
                         mma_mxf8(d, ad, bd, id, tmem + C::SFA_COL + s * C::SFA_COLS,
                                  tmem + C::SFB_COL + s * C::SFB_COLS, acc);
+                    } else if (KIND == kMxfp4) {
+                        // chunk c/2 holds the scales of two MMAs; the ids 0 / 2 select the pair
+                        const uint32_t sf = (uint32_t)(c & 1) * 2u;
+                        const uint32_t id = idesc | (sf << 4) | (sf << 29);
+                        mma_mxf4(d, ad, bd, id, tmem + C::SFA_COL + s * C::SFA_COLS + (c >> 1) * 4,
+                                 tmem + C::SFB_COL + s * C::SFB_COLS + (c >> 1) * 4 * (C::BN / 128), acc);
                     } else {
                         mma_nvf4(d, ad, bd, idesc, tmem + C::SFA_COL + s * C::SFA_COLS + c * 4,
                                  tmem + C::SFB_COL + s * C::SFB_COLS + c * 4 * (C::BN / 128), acc);
@@ -585,7 +595,7 @@ bool make_tmap_u8(CUtensorMap* m, const void* base, uint64_t inner_bytes, uint64
 template <int KIND>
 cudaError_t launch_tc(const GemmArgs& a, cudaStream_t st) {
     using C = Cfg<KIND>;
-    const uint64_t kbytes = (KIND == kNvfp4) ? (uint64_t)a.K / 2 : (uint64_t)a.K;
+    const uint64_t kbytes = (KIND == kNvfp4 || KIND == kMxfp4) ? (uint64_t)a.K / 2 : (uint64_t)a.K;
     CUtensorMap tmA, tmB;
     if (!make_tmap_u8(&tmA, a.x, kbytes, (uint64_t)a.M, kbytes, BM)) return cudaErrorInvalidValue;
     if (!make_tmap_u8(&tmB, a.w, kbytes, (uint64_t)a.N, kbytes, C::BN)) return cudaErrorInvalidValue;
@@ -613,7 +623,7 @@ cudaError_t launch_tc(const GemmArgs& a, cudaStream_t st) {
     p.w_global = a.w_global;
     p.sfa = static_cast<const uint8_t*>(a.x_scales);
     p.sfb = static_cast<const uint8_t*>(a.w_scales);
-    p.sf_chunks_per_row = (KIND == kMxfp8) ? a.K / 128 : a.K / 64;
+    p.sf_chunks_per_row = (KIND == kMxfp8 || KIND == kMxfp4) ? a.K / 128 : a.K / 64;
     p.bias = a.bias;
     p.y = a.y;
     p.status = a.dev_status;
@@ -655,6 +665,7 @@ cudaError_t launch_gemm_fp8_tensor(const GemmArgs& a, cudaStream_t st) { return 
 cudaError_t launch_gemm_fp8_block(const GemmArgs& a, cudaStream_t st) { return launch_tc<kFp8Block>(a, st); }
 cudaError_t launch_gemm_mxfp8(const GemmArgs& a, cudaStream_t st) { return launch_tc<kMxfp8>(a, st); }
 cudaError_t launch_gemm_nvfp4(const GemmArgs& a, cudaStream_t st) { return launch_tc<kNvfp4>(a, st); }
+cudaError_t launch_gemm_mxfp4(const GemmArgs& a, cudaStream_t st) { return launch_tc<kMxfp4>(a, st); }
 
 cudaError_t launch_debug_expire_wait(int* dev_status, uint32_t max_polls, cudaStream_t st) {
     k_expire_wait<<<1, 32, 0, st>>>(dev_status, max_polls);

@@ -20,6 +20,8 @@ cudaError_t launch_fp8_block128(const uint16_t* x, int64_t rows, int64_t K, int6
                                 uint8_t* codes, float* scales, cudaStream_t st);
 cudaError_t launch_mxfp8(const uint16_t* x, int64_t rows, int64_t K, int64_t ld, uint8_t* codes,
                          uint8_t* scales, bool mma_layout, cudaStream_t st);
+cudaError_t launch_mxfp4(const uint16_t* x, int64_t rows, int64_t K, int64_t ld, uint8_t* codes,
+                         uint8_t* scales, bool mma_layout, cudaStream_t st);
 cudaError_t launch_nvfp4(const uint16_t* x, int64_t rows, int64_t K, int64_t ld, uint8_t* codes,
                          uint8_t* scales, float* global, bool mma_layout, float* partials,
                          int nparts, cudaStream_t st);
@@ -50,6 +52,7 @@ cudaError_t launch_gemm_fp8_tensor(const GemmArgs& a, cudaStream_t st);
 cudaError_t launch_gemm_fp8_block(const GemmArgs& a, cudaStream_t st);
 cudaError_t launch_gemm_mxfp8(const GemmArgs& a, cudaStream_t st);
 cudaError_t launch_gemm_nvfp4(const GemmArgs& a, cudaStream_t st);
+cudaError_t launch_gemm_mxfp4(const GemmArgs& a, cudaStream_t st);
 cudaError_t launch_gemm_w4a16(const GemmArgs& a, cudaStream_t st);
 size_t w4a16_workspace_bytes(int64_t M, int64_t N, int64_t K);
 

@@ -1,5 +1,5 @@
 // Online quantizers: bf16 -> FP8 E4M3 (tensor / token / 128x128 block),
-// MXFP8, NVFP4 and int4 g128.  Each reads its bf16 input once from HBM in
+// MXFP8, MXFP4, NVFP4 and int4 g128.  Each reads its bf16 input once from HBM in
 // 16-byte vectors, reduces amax (or min/max) with warp shuffles, and writes
 // codes and scales in the same pass.  The per-tensor formats need the tensor
 // amax before any code exists, so they add one read-only amax pass.
@@ -273,14 +273,18 @@ __global__ void __launch_bounds__(256) k_fp8_block128(const uint16_t* __restrict
     if (threadIdx.x == 0) scales[bi * (K >> 7) + bj] = s;
 }
 
-// ---------------------------------------------------------------- MXFP8
-// Four consecutive lanes own one 32-element granule (8 elements each).  Rows
-// from `rows` up to `rows_pad` exist only in the MMA scale layout: they get
-// scale code 0 and no codes.  Every lane of a warp runs the same trip count
-// (the shuffles use the full mask); a task never splits a granule.
-__global__ void __launch_bounds__(256) k_mxfp8(const uint16_t* __restrict__ x, int64_t rows, int64_t rows_pad,
-                                               int64_t K, int64_t ld, uint8_t* __restrict__ codes,
-                                               uint8_t* __restrict__ scales, int mma) {
+// ---------------------------------------------------------------- MXFP8 / MXFP4
+// The MX rule with the element format's largest power-of-two exponent: 8 for
+// E4M3 (MXFP8), 2 for E2M1 (MXFP4, codes two per byte).  Four consecutive
+// lanes own one 32-element granule (8 elements each).  Rows from `rows` up to
+// `rows_pad` exist only in the MMA scale layout: they get scale code 0 and no
+// codes.  Every lane of a warp runs the same trip count (the shuffles use the
+// full mask); a task never splits a granule.
+template <bool FP4>
+__global__ void __launch_bounds__(256) k_mx(const uint16_t* __restrict__ x, int64_t rows, int64_t rows_pad,
+                                            int64_t K, int64_t ld, uint8_t* __restrict__ codes,
+                                            uint8_t* __restrict__ scales, int mma) {
+    constexpr int kEmax = FP4 ? 2 : 8;
     const uint32_t nvr = (uint32_t)(K >> 3), tpr = (nvr + 31) / 32, total = (uint32_t)rows_pad * tpr;
     const uint32_t warps = gridDim.x * 8, w0 = blockIdx.x * 8 + (threadIdx.x >> 5);
     const int64_t chunks = K >> 7;
@@ -299,14 +303,17 @@ __global__ void __launch_bounds__(256) k_mxfp8(const uint16_t* __restrict__ x, i
             float a = absmax8(v[u]);
             a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
             a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 2));
-            // e = clamp(floor(log2 a) - 8, -127, 127); subnormal a lands below -127.
+            // e = clamp(floor(log2 a) - kEmax, -127, 127); subnormal a lands below -127.
             const int biased = (int)(__float_as_uint(a) >> 23);
-            int e = (a == 0.0f || biased == 0) ? -127 : max(biased - 127 - 8, -127);
+            int e = (a == 0.0f || biased == 0) ? -127 : max(biased - 127 - kEmax, -127);
             e = min(e, 127);
             const float mult = __uint_as_float((uint32_t)(127 - e) << 23);   // 2^-e, e <= 126 here
             if (!q[u].in) continue;
             const int64_t row = q[u].row, c = q[u].c;
-            if (row < rows) reinterpret_cast<uint2*>(codes + row * K)[c] = enc8_e4m3(v[u], mult);
+            if (row < rows) {
+                if (FP4) reinterpret_cast<uint32_t*>(codes + row * (K >> 1))[c] = enc8_e2m1(v[u], mult);
+                else reinterpret_cast<uint2*>(codes + row * K)[c] = enc8_e4m3(v[u], mult);
+            }
             if ((c & 3) == 0) {
                 const int64_t j = c >> 2;
                 const int64_t off = mma ? mma_scale_offset(row, j, chunks) : row * (K >> 5) + j;
@@ -504,7 +511,16 @@ cudaError_t launch_mxfp8(const uint16_t* x, int64_t rows, int64_t K, int64_t ld,
     const int64_t rows_pad = mma_layout ? (rows + 127) / 128 * 128 : rows;
     const int64_t tasks = task_count(rows_pad, K);
     if (tasks < 0) return cudaErrorInvalidValue;
-    k_mxfp8<<<task_grid(tasks), 256, 0, st>>>(x, rows, rows_pad, K, ld, codes, scales, mma_layout ? 1 : 0);
+    k_mx<false><<<task_grid(tasks), 256, 0, st>>>(x, rows, rows_pad, K, ld, codes, scales, mma_layout ? 1 : 0);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_mxfp4(const uint16_t* x, int64_t rows, int64_t K, int64_t ld, uint8_t* codes,
+                         uint8_t* scales, bool mma_layout, cudaStream_t st) {
+    const int64_t rows_pad = mma_layout ? (rows + 127) / 128 * 128 : rows;
+    const int64_t tasks = task_count(rows_pad, K);
+    if (tasks < 0) return cudaErrorInvalidValue;
+    k_mx<true><<<task_grid(tasks), 256, 0, st>>>(x, rows, rows_pad, K, ld, codes, scales, mma_layout ? 1 : 0);
     return cudaGetLastError();
 }
 

@@ -127,6 +127,14 @@ def mxfp8_linear(K: int, N: int, M: int = MXFP8_M) -> Linear:
                   _seed(4, 2 * v), _seed(4, 2 * v + 1), "normal", x_std=1.0, w_std=0.015)
 
 
+def mxfp4_linear(K: int, N: int, M: int = MXFP8_M) -> Linear:
+    """MXFP4 W4A4 (the next format of the online MXFP4 path) on the video-DiT
+    shapes and distributions of the MXFP8 workload: X N(0,1), W N(0, 0.015^2)."""
+    v = MXFP8_SHAPES.index((K, N)) if (K, N) in MXFP8_SHAPES else 7
+    return Linear(f"mxfp4_K{K}_N{N}", M, K, N, "mxfp4", "mxfp4",
+                  _seed(6, 2 * v), _seed(6, 2 * v + 1), "normal", x_std=1.0, w_std=0.015)
+
+
 def mixed_stack(M: int = 32768, d: int = 3072, ff: int = 12288) -> list[Linear]:
     """Eight linears: NVFP4 W4A4 q/k/v/out projections (d x d) and FP8 block-128
     MLP linears (two d->ff, two ff->d); activations as the DiT MLP workload."""

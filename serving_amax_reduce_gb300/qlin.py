@@ -27,6 +27,7 @@ class Fmt(enum.IntEnum):
     NVFP4 = 4
     INT4_G128_ASYM = 5
     BF16 = 6
+    MXFP4 = 7
 
 
 class Layout(enum.IntEnum):

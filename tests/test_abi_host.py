@@ -54,6 +54,11 @@ def test_size_queries(q):
     assert q.qlin_zeros_bytes(F.FP8_TOKEN, 4096, 12288) == 0
     assert q.qlin_quant_workspace_bytes(F.FP8_TENSOR, 128, 1024) > 0
     assert q.qlin_quant_workspace_bytes(F.FP8_TOKEN, 128, 1024) == 0
+    # MXFP4: E2M1 codes two per byte, one E8M0 byte per 32, no workspace
+    assert q.qlin_codes_bytes(F.MXFP4, 20280, 5120) == 20280 * 2560
+    assert q.qlin_scales_bytes(F.MXFP4, L.CANONICAL, 20280, 5120) == 20280 * 160
+    assert q.qlin_scales_bytes(F.MXFP4, L.MMA, 20280, 5120) == 20352 * 160
+    assert q.qlin_quant_workspace_bytes(F.MXFP4, 20280, 5120) == 0
 
 
 FAKE = 1 << 20          # a 16-byte aligned non-null value; never dereferenced by these calls
@@ -90,6 +95,10 @@ def test_quantize_rejects_bad_arguments(q):
                                None) == S.UNSUPPORTED
     assert q.qlin_quantize_act(F.MXFP8, FAKE, 128, 96, 96, FAKE, FAKE, None, L.MMA, None, 0, None,
                                None) == S.INVALID_ARG
+    assert q.qlin_quantize_act(F.MXFP4, FAKE, 128, 96, 96, FAKE, FAKE, None, L.MMA, None, 0, None,
+                               None) == S.INVALID_ARG
+    assert q.qlin_quantize_act(F.MXFP4, FAKE, 128, 80, 80, FAKE, FAKE, None, L.CANONICAL, None, 0, None,
+                               None) == S.INVALID_ARG                  # K % 32
     # NVFP4 needs the global-scale output
     assert q.qlin_quantize_act(F.NVFP4, FAKE, 128, 1024, 1024, FAKE, FAKE, None, L.CANONICAL, FAKE, 1 << 20,
                                None, None) == S.INVALID_ARG
@@ -120,6 +129,9 @@ def test_gemm_rejects_bad_arguments(q):
     assert g(F.MXFP8, F.MXFP8, 128, 1024, 1056, layout=L.MMA) == S.INVALID_ARG
     assert g(F.NVFP4, F.NVFP4, 128, 1024, 1024, layout=L.MMA, xg=None) == S.INVALID_ARG
     assert g(F.NVFP4, F.FP8_TOKEN, 128, 1024, 1024, layout=L.MMA) == S.UNSUPPORTED
+    assert g(F.MXFP4, F.MXFP4, 128, 1024, 1024) == S.UNSUPPORTED          # canonical scales
+    assert g(F.MXFP4, F.MXFP4, 128, 1024, 1152, layout=L.MMA) == S.INVALID_ARG   # K % 256
+    assert g(F.MXFP4, F.MXFP8, 128, 1024, 1024, layout=L.MMA) == S.UNSUPPORTED
     assert g(F.FP8_TENSOR, F.FP8_TOKEN, 128, 1024, 1024) == S.UNSUPPORTED
     assert g(F.INT4_G128_ASYM, F.BF16, 16, 4096, 4000) == S.INVALID_ARG
     need = q.qlin_gemm_workspace_bytes(F.INT4_G128_ASYM, F.BF16, 16, 4096, 4096)

@@ -166,6 +166,39 @@ def test_nvfp4_gemm_full_size(q, orc):
     nvfp4_case(q, orc, 32768, 3072, 3072, nrows=256)
 
 
+# ------------------------------------------------------------------ MXFP4 (W4A4)
+def mxfp4_case(q, orc, M, N, K, nrows=None, with_bias=False):
+    lin = inputs.mxfp8_linear(K, N, M=M)          # the MXFP8 workload's distributions, W4A4 formats
+    x, w = lin.make_x(), lin.make_w()
+    F, L = q.Fmt, q.Layout
+    bx = q.quantize_act(F.MXFP4, x.cuda(), L.MMA)
+    bw = q.quantize_weight(F.MXFP4, w.cuda(), L.MMA)
+    bias = inputs.normal_bf16((1, N), 0.05, 79)[0] if with_bias else None
+    y = q.gemm(F.MXFP4, F.MXFP4, M, N, K, bx["codes"], bx["scales"], bw["codes"], bw["scales"], layout=L.MMA,
+               bias=bias.cuda() if with_bias else None)
+    torch.cuda.synchronize()
+    rows = sample_rows(M, nrows or M)
+    xs = mma_to_canonical(np_u8(bx["scales"]), M, K // 32)[rows]
+    xh = orc.dequant_mxfp4(np_u8(bx["codes"]).reshape(M, K // 2)[rows], xs)
+    wh = orc.dequant_mxfp4(np_u8(bw["codes"]).reshape(N, K // 2), mma_to_canonical(np_u8(bw["scales"]), N, K // 32))
+    b = orc.bf16_values(bits(bias)[None, :])[0] if with_bias else None
+    return check(orc, y_np(y)[rows], orc.gemm_ref(xh, wh, bias=b), x, w, rows=torch.from_numpy(rows))
+
+
+@pytest.mark.parametrize("M,N,K", [(200, 512, 512), (128, 256, 256), (1, 256, 768), (300, 640, 1280)])
+def test_mxfp4_gemm(q, orc, M, N, K):
+    mxfp4_case(q, orc, M, N, K)
+
+
+def test_mxfp4_gemm_bias(q, orc):
+    mxfp4_case(q, orc, 130, 384, 512, with_bias=True)
+
+
+@pytest.mark.slow
+def test_mxfp4_gemm_full_size(q, orc):
+    mxfp4_case(q, orc, 20280, 5120, 5120, nrows=256)
+
+
 # ------------------------------------------------------------------ W4A16 decode
 def w4a16_case(q, orc, M, K, N, with_bias=False):
     lin = inputs.w4a16_linear(M, K, N)

@@ -101,6 +101,24 @@ def test_nvfp4(q, orc, rows, K, kind, mma):
         assert np.array_equal(got[: rows * K // 16].reshape(rows, K // 16), sc)
 
 
+@pytest.mark.parametrize("rows,K", [(1, 128), (200, 5120), (128, 13824), (77, 96)])
+@pytest.mark.parametrize("kind", ["normal", "edge"])
+@pytest.mark.parametrize("mma", [False, True])
+def test_mxfp4(q, orc, rows, K, kind, mma):
+    if mma and K % 128:
+        pytest.skip("MMA layout needs K % 128 == 0")
+    x = make(kind, rows, K, 7 * rows + K) if kind == "edge" else inputs.normal_bf16((rows, K), 1.0, rows + 2 * K)
+    b = run(q, q.Fmt.MXFP4, x, q.Layout.MMA if mma else None)
+    packed, sc = orc.quant_mxfp4(bits(x))
+    assert np.array_equal(np_u8(b["codes"]).reshape(rows, K // 2), packed)
+    got = np_u8(b["scales"])
+    if mma:
+        assert np.array_equal(mma_to_canonical(got, rows, K // 32), sc)
+        assert not mma_padding_rows(got, rows, K // 32).any()
+    else:
+        assert np.array_equal(got[: rows * K // 32].reshape(rows, K // 32), sc)
+
+
 @pytest.mark.parametrize("N,K", [(72, 256), (4096, 4096), (12288, 4096), (64, 12288)])
 @pytest.mark.parametrize("kind", ["normal", "edge"])
 def test_int4_g128(q, orc, N, K, kind):
