@@ -74,6 +74,7 @@ def _load():
             "oracle_quant_fp8_tensor": ([P, I64, I64, I64, P, P], None),
             "oracle_quant_fp8_token": ([P, I64, I64, I64, P, P], None),
             "oracle_quant_fp8_block128": ([P, I64, I64, I64, P, P], None),
+            "oracle_quant_fp8_group128": ([P, I64, I64, I64, P, P], None),
             "oracle_quant_mxfp8": ([P, I64, I64, I64, P, P], None),
             "oracle_quant_nvfp4": ([P, I64, I64, I64, P, P, P], None),
             "oracle_quant_mxfp4": ([P, I64, I64, I64, P, P], None),
@@ -81,6 +82,7 @@ def _load():
             "oracle_dequant_fp8_tensor": ([P, I64, I64, F, P], None),
             "oracle_dequant_fp8_token": ([P, I64, I64, P, P], None),
             "oracle_dequant_fp8_block128": ([P, I64, I64, P, P], None),
+            "oracle_dequant_fp8_group128": ([P, I64, I64, P, P], None),
             "oracle_dequant_mxfp8": ([P, I64, I64, P, P], None),
             "oracle_dequant_nvfp4": ([P, I64, I64, P, F, P], None),
             "oracle_dequant_mxfp4": ([P, I64, I64, P, P], None),
@@ -160,6 +162,18 @@ def quant_fp8_token(x):
     codes = np.empty((R, K), np.uint8)
     s = np.empty(R, np.float32)
     _load().oracle_quant_fp8_token(_p(x), R, K, K, _p(codes), _p(s))
+    return codes, s
+
+
+def quant_fp8_group128(x):
+    """Dynamic E4M3 per 1 x 128 group -> (codes uint8 [R,K], scales float32 [R, K/128])."""
+    x = _bf16_bits(x)
+    R, K = x.shape
+    if K % 128:
+        raise ValueError("FP8 group-128 needs K multiple of 128")
+    codes = np.empty((R, K), np.uint8)
+    s = np.empty((R, K // 128), np.float32)
+    _load().oracle_quant_fp8_group128(_p(x), R, K, K, _p(codes), _p(s))
     return codes, s
 
 
@@ -243,6 +257,14 @@ def dequant_fp8_token(codes, scales):
     scales = np.ascontiguousarray(scales, np.float32)
     out = _f64(codes.shape)
     _load().oracle_dequant_fp8_token(_p(codes), codes.shape[0], codes.shape[1], _p(scales), _p(out))
+    return out
+
+
+def dequant_fp8_group128(codes, scales):
+    codes = np.ascontiguousarray(codes, np.uint8)
+    scales = np.ascontiguousarray(scales, np.float32)
+    out = _f64(codes.shape)
+    _load().oracle_dequant_fp8_group128(_p(codes), codes.shape[0], codes.shape[1], _p(scales), _p(out))
     return out
 
 

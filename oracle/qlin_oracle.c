@@ -48,6 +48,10 @@
  *       (2 = exponent of 6, the largest E2M1 power-of-two range), codes =
  *       E2M1(x * 2^-e) packed two per byte, lower K index in the low nibble;
  *       amax == 0 gives scale code 0.
+ *   R7  dynamic FP8 128-group activations ("[vLLM] 기타 양자화", section
+ *       "FP8: vLLM의 핵심 양자화", the block-128 dynamic symmetric scheme
+ *       applied to activations): the R1 granule is 1 x 128, one token times
+ *       128 consecutive K elements, with one fp32 scale per (row, K/128).
  */
 #include <math.h>
 #include <stdint.h>
@@ -192,6 +196,24 @@ void oracle_quant_fp8_token(const uint16_t *x, int64_t rows, int64_t K, int64_t 
 
 /* One scale per 128 x 128 tile.  rows, K multiples of 128.
  * scales: (rows/128) x (K/128), row-major. */
+/* FP8 E4M3 with one dynamic scale per 1 x 128 group along K (R7)       */
+void oracle_quant_fp8_group128(const uint16_t *x, int64_t rows, int64_t K, int64_t ld,
+                               uint8_t *codes, float *scales)
+{
+    int64_t ng = K / 128;
+    for (int64_t i = 0; i < rows; i++)
+        for (int64_t g = 0; g < ng; g++) {
+            const uint16_t *grp = x + i * ld + g * 128;
+            float amax = 0.0f, s, r;
+            for (int k = 0; k < 128; k++)
+                amax = fmaxf(amax, fabsf(oracle_bf16_to_f32(grp[k])));
+            fp8_granule(amax, &s, &r);
+            for (int k = 0; k < 128; k++)
+                codes[i * K + g * 128 + k] = oracle_enc_e4m3(oracle_bf16_to_f32(grp[k]) * r);
+            scales[i * ng + g] = s;
+        }
+}
+
 void oracle_quant_fp8_block128(const uint16_t *x, int64_t rows, int64_t K, int64_t ld,
                                uint8_t *codes, float *scales)
 {
@@ -370,6 +392,14 @@ void oracle_dequant_fp8_token(const uint8_t *codes, int64_t rows, int64_t K,
     for (int64_t i = 0; i < rows; i++)
         for (int64_t k = 0; k < K; k++)
             out[i * K + k] = oracle_dec_e4m3(codes[i * K + k]) * (double)scales[i];
+}
+
+void oracle_dequant_fp8_group128(const uint8_t *codes, int64_t rows, int64_t K,
+                                 const float *scales, double *out)
+{
+    for (int64_t i = 0; i < rows; i++)
+        for (int64_t k = 0; k < K; k++)
+            out[i * K + k] = oracle_dec_e4m3(codes[i * K + k]) * (double)scales[i * (K / 128) + k / 128];
 }
 
 void oracle_dequant_fp8_block128(const uint8_t *codes, int64_t rows, int64_t K,

@@ -120,6 +120,53 @@ def test_fp8_block_granules_are_independent(orc):
     assert np.array_equal(c1[mask], c2[mask])
 
 
+def test_fp8_group128_amax_maps_to_448_and_codes_are_nearest(orc):
+    R, K = 64, 512
+    x = bf16_bits(inputs.outlier_channel_bf16(R, K, 81))
+    xv = vals(x)
+    codes, s = orc.quant_fp8_group128(x)
+    assert s.shape == (R, K // 128)
+    s_full = np.repeat(np.asarray(s, np.float64), 128, 1)
+    d = dec_vec(orc.dec_e4m3, codes)
+    for i in range(R):
+        for g in range(K // 128):
+            blk = np.abs(xv[i, g * 128:(g + 1) * 128])
+            a = blk.max()
+            assert abs(s[i, g] * 448 - a) <= a * 2.0 ** -22    # s = amax/448 to binary32 rounding
+            assert np.all(np.abs(d[i, g * 128:(g + 1) * 128][blk == a]) == 448.0)
+    assert_nearest(d, xv / s_full, e4m3_grid(orc), slack=1e-5)
+
+
+def test_fp8_group128_reduces_to_token_when_k_is_128(orc):
+    # with K = 128 a row is one group: the same codes and scales as per-token quantization
+    x = rand_bits((96, 128), 83)
+    c1, s1 = orc.quant_fp8_group128(x)
+    c2, s2 = orc.quant_fp8_token(x)
+    assert np.array_equal(c1, c2) and np.array_equal(s1[:, 0].view(np.uint32), s2.view(np.uint32))
+
+
+def test_fp8_group128_groups_are_independent_and_dequant_close(orc):
+    x = rand_bits((8, 512), 85)
+    c1, s1 = orc.quant_fp8_group128(x)
+    x2 = x.copy()
+    x2[5, 256:384] = bf16_bits(inputs.normal_bf16((1, 128), 1000.0, 86))[0]
+    c2, s2 = orc.quant_fp8_group128(x2)
+    changed = np.zeros((8, 4), bool)
+    changed[5, 2] = True
+    assert np.array_equal(s1[~changed], s2[~changed]) and s1[5, 2] != s2[5, 2]
+    keep = np.ones((8, 512), bool)
+    keep[5, 256:384] = False
+    assert np.array_equal(c1[keep], c2[keep])
+    # groups 10^k apart: a transposed scale index would miss by orders of magnitude
+    xv = vals(x) * np.repeat(10.0 ** np.arange(4)[None, :], 128, 1)
+    xb = bf16_bits(torch.from_numpy(xv).to(torch.bfloat16))
+    c, sc = orc.quant_fp8_group128(xb)
+    xh = orc.dequant_fp8_group128(c, sc)
+    unit = np.repeat(np.asarray(sc, np.float64), 128, 1)
+    bound = half_step(e4m3_grid(orc), vals(xb) / unit) * unit * (1 + 1e-5)
+    assert np.all(np.abs(xh - vals(xb)) <= bound)
+
+
 def test_fp8_token_rows_are_independent(orc):
     x = rand_bits((8, 512), 12)
     c1, s1 = orc.quant_fp8_token(x)
