@@ -61,7 +61,8 @@ def parse_args():
 def workload_linears(next_rows: bool = False):
     from serving_amax_reduce_gb300 import inputs as I
     if next_rows:
-        return [("mxfp4", I.mxfp4_linear(K, N)) for (K, N) in I.MXFP8_SHAPES]
+        return ([("mxfp4", I.mxfp4_linear(K, N)) for (K, N) in I.MXFP8_SHAPES]
+                + [("fp8_group", I.fp8_group_linear(K, N)) for (K, N) in I.FP8_MLP_SHAPES])
     lins = [("fp8_tensor", I.fp8_tensor_linear())]
     for (K, N) in I.W4A16_SHAPES:
         for M in I.W4A16_M:
@@ -78,8 +79,9 @@ def workload_linears(next_rows: bool = False):
 
 def config_block(args):
     if args.next:
-        return {"workload": "next-rows-mxfp4-w4a4",
-                "workloads": ["mxfp4 W4A4 M20280 (K,N){(5120,13824),(13824,5120),(5120,5120)}"],
+        return {"workload": "next-rows",
+                "workloads": ["mxfp4 W4A4 M20280 (K,N){(5120,13824),(13824,5120),(5120,5120)}",
+                              "fp8 1x128-group X x 128x128-block W, M4096 (K,N){(3072,12288),(12288,3072)}"],
                 "step": "per linear: weight quantize + activation quantize + quantized GEMM",
                 "l2": "inputs larger than L2", "parallelism": f"replicas x{args.gpus}"}
     return {
@@ -155,7 +157,7 @@ class Job:
         wf = {"fp8_tensor": F.FP8_TENSOR, "fp8_block128": F.FP8_BLOCK128, "mxfp8": F.MXFP8, "nvfp4": F.NVFP4,
               "int4_g128": F.INT4_G128_ASYM, "mxfp4": F.MXFP4}[lin.w_fmt]
         xf = {"fp8_tensor": F.FP8_TENSOR, "fp8_token": F.FP8_TOKEN, "mxfp8": F.MXFP8, "nvfp4": F.NVFP4,
-              "bf16": F.BF16, "mxfp4": F.MXFP4}[lin.x_fmt]
+              "bf16": F.BF16, "mxfp4": F.MXFP4, "fp8_group128": F.FP8_GROUP128}[lin.x_fmt]
         self.wf, self.xf = wf, xf
         self.layout = L.MMA if wf in (F.MXFP8, F.NVFP4, F.MXFP4) else L.CANONICAL
         self.wb = q.alloc_quant(wf, lin.N, lin.K, self.layout, dev)
@@ -240,11 +242,14 @@ def measured_traffic(kernel, alg_bytes_per_launch):
 def kernel_name(job, op):
     F = job.q.Fmt
     if op == "gemm":
+        if job.xf == F.FP8_GROUP128:
+            return "gemm_fp8_block_x_group128"
         return {F.FP8_TENSOR: "gemm_fp8_tensor", F.FP8_BLOCK128: "gemm_fp8_block", F.MXFP8: "gemm_mxfp8",
                 F.NVFP4: "gemm_nvfp4", F.INT4_G128_ASYM: "gemm_w4a16", F.MXFP4: "gemm_mxfp4"}[job.wf]
     fmt = job.wf if op == "quant_w" else job.xf
     return "quant_" + {F.FP8_TENSOR: "fp8_tensor", F.FP8_TOKEN: "fp8_token", F.FP8_BLOCK128: "fp8_block128",
-                       F.MXFP8: "mxfp8", F.NVFP4: "nvfp4", F.INT4_G128_ASYM: "int4_g128", F.MXFP4: "mxfp4"}[fmt]
+                       F.MXFP8: "mxfp8", F.NVFP4: "nvfp4", F.INT4_G128_ASYM: "int4_g128", F.MXFP4: "mxfp4",
+                       F.FP8_GROUP128: "fp8_group128"}[fmt]
 
 
 def tensor_peak(peaks, wf, q, sustained=True):

@@ -73,7 +73,12 @@ typedef enum {
      * "vLLM-Omni 在线量化（Online Quantization）完全指南", section
      * "在线量化的底层工作原理" (the online MXFP4 path mirrors MXFP8 with
      * float4_e2m1fn_x2 codes; W4A4).                                          */
-    QLIN_MXFP4 = 7
+    QLIN_MXFP4 = 7,
+    /* E4M3 codes, one fp32 scale per row and 128 consecutive K (1 x 128
+     * groups): the block-128 dynamic symmetric FP8 scheme of "[vLLM] 기타
+     * 양자화: FP8, ModelOpt, INC, TorchAO, Quark", section "FP8: vLLM의 핵심
+     * 양자화", on activations; pairs with FP8_BLOCK128 weights in qlin_gemm.   */
+    QLIN_FP8_GROUP128 = 8
 } qlin_format;
 
 typedef enum {
@@ -109,7 +114,8 @@ const char *qlin_status_string(qlin_status s);
  * INT4 (K/8)*rows*4 as int32 [K/8, rows], k = 8i+j in bits [4j,4j+4).       */
 size_t qlin_codes_bytes(qlin_format fmt, int64_t rows, int64_t K);
 
-/* Scales: FP8_TENSOR 4 (one float); FP8_TOKEN rows*4; FP8_BLOCK128
+/* Scales: FP8_TENSOR 4 (one float); FP8_TOKEN rows*4; FP8_GROUP128
+ * rows*(K/128)*4, float [rows, K/128] row-major; FP8_BLOCK128
  * (rows/128)*(K/128)*4 row-major; MXFP8 rows*K/32 (canonical) or
  * ceil(rows/128)*128*K/32 (MMA), the same for MXFP4; NVFP4 rows*K/16 or
  * ceil(rows/128)*128*K/16;
@@ -140,7 +146,8 @@ size_t qlin_gemm_workspace_bytes(qlin_format w_fmt, qlin_format x_fmt,
  *   layout             QLIN_SCALE_MMA is accepted for MXFP8, MXFP4 and NVFP4 only
  *   workspace_dev      qlin_quant_workspace_bytes(...) bytes (NULL if 0)
  * Requirements: src and ld*2 bytes 16-byte aligned; K % 8 == 0;
- *   FP8_BLOCK128: rows % 128 == 0 and K % 128 == 0; MXFP8: K % 32 == 0
+ *   FP8_BLOCK128: rows % 128 == 0 and K % 128 == 0; FP8_GROUP128: K % 128 == 0;
+ *   MXFP8: K % 32 == 0
  *   (K % 128 == 0 for the MMA layout), the same for MXFP4; NVFP4: K % 16 == 0
  *   (K % 64 for MMA);
  *   INT4: rows % 8 == 0 and K % 128 == 0.
@@ -167,6 +174,7 @@ qlin_status qlin_quantize_act(qlin_format fmt, const void *x_bf16_dev, int64_t M
  *   FP8_TENSOR, FP8_TENSOR : x = codes [M,K]; x_scales, w_scales = one float each
  *   FP8_BLOCK128, FP8_TOKEN: x_scales float [M]; w_scales float [N/128, K/128]
  *                            (N % 128 == 0, K % 128 == 0)
+ *   FP8_BLOCK128, FP8_GROUP128: x_scales float [M, K/128]; otherwise as above
  *   MXFP8, MXFP8           : scales in QLIN_SCALE_MMA layout (K % 128 == 0)
  *   NVFP4, NVFP4           : scales in QLIN_SCALE_MMA layout, x_global and
  *                            w_global one float each (K % 256 == 0)

@@ -12,7 +12,7 @@ namespace {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 bool is_quant_format(qlin_format f) {
-    return (f >= QLIN_FP8_TENSOR && f <= QLIN_INT4_G128_ASYM) || f == QLIN_MXFP4;
+    return (f >= QLIN_FP8_TENSOR && f <= QLIN_INT4_G128_ASYM) || f == QLIN_MXFP4 || f == QLIN_FP8_GROUP128;
 }
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -29,6 +29,7 @@ qlin_status check_quant_shape(qlin_format fmt, qlin_scale_layout layout, int64_t
         case QLIN_FP8_TENSOR:
         case QLIN_FP8_TOKEN: return QLIN_OK;
         case QLIN_FP8_BLOCK128: return (rows % 128 || K % 128) ? QLIN_ERR_INVALID_ARG : QLIN_OK;
+        case QLIN_FP8_GROUP128: return (K % 128) ? QLIN_ERR_INVALID_ARG : QLIN_OK;
         case QLIN_MXFP8:
         case QLIN_MXFP4:
             if (K % 32) return QLIN_ERR_INVALID_ARG;
@@ -51,7 +52,7 @@ qlin_status quantize(qlin_format fmt, const void* src, int64_t rows, int64_t K, 
     if (fmt == QLIN_INT4_G128_ASYM && !zeros) return QLIN_ERR_INVALID_ARG;
     if (fmt == QLIN_NVFP4 && !global) return QLIN_ERR_INVALID_ARG;
     if (!aligned16(src) || (ld * 2) % 16 || !aligned16(codes)) return QLIN_ERR_ALIGNMENT;
-    if (fmt == QLIN_FP8_TOKEN || fmt == QLIN_FP8_BLOCK128 || fmt == QLIN_FP8_TENSOR) {
+    if (fmt == QLIN_FP8_TOKEN || fmt == QLIN_FP8_BLOCK128 || fmt == QLIN_FP8_TENSOR || fmt == QLIN_FP8_GROUP128) {
         if (reinterpret_cast<uintptr_t>(scales) & 3u) return QLIN_ERR_ALIGNMENT;
     }
     if (fmt == QLIN_INT4_G128_ASYM &&
@@ -71,6 +72,8 @@ qlin_status quantize(qlin_format fmt, const void* src, int64_t rows, int64_t K, 
             return launch_status(launch_fp8_rowwise(x, rows, K, ld, c, static_cast<float*>(scales), st));
         case QLIN_FP8_BLOCK128:
             return launch_status(launch_fp8_block128(x, rows, K, ld, c, static_cast<float*>(scales), st));
+        case QLIN_FP8_GROUP128:
+            return launch_status(launch_fp8_group128(x, rows, K, ld, c, static_cast<float*>(scales), st));
         case QLIN_MXFP8:
             return launch_status(launch_mxfp8(x, rows, K, ld, c, static_cast<uint8_t*>(scales), mma, st));
         case QLIN_MXFP4:
@@ -111,6 +114,7 @@ size_t qlin_codes_bytes(qlin_format fmt, int64_t rows, int64_t K) {
         case QLIN_FP8_TENSOR:
         case QLIN_FP8_TOKEN:
         case QLIN_FP8_BLOCK128:
+        case QLIN_FP8_GROUP128:
         case QLIN_MXFP8: return (size_t)(rows * K);
         case QLIN_NVFP4:
         case QLIN_MXFP4: return (size_t)(rows * (K / 2));
@@ -126,6 +130,7 @@ size_t qlin_scales_bytes(qlin_format fmt, qlin_scale_layout layout, int64_t rows
         case QLIN_FP8_TENSOR: return 4;
         case QLIN_FP8_TOKEN: return (size_t)(rows * 4);
         case QLIN_FP8_BLOCK128: return (size_t)((rows / 128) * (K / 128) * 4);
+        case QLIN_FP8_GROUP128: return (size_t)(rows * (K / 128) * 4);
         case QLIN_MXFP8:
         case QLIN_MXFP4: return (size_t)((layout == QLIN_SCALE_MMA ? rows_pad : rows) * (K / 32));
         case QLIN_NVFP4: return (size_t)((layout == QLIN_SCALE_MMA ? rows_pad : rows) * (K / 16));
@@ -189,9 +194,10 @@ qlin_status qlin_gemm(qlin_format w_fmt, qlin_format x_fmt, int64_t M, int64_t N
         if (K % 16) return QLIN_ERR_INVALID_ARG;
         return launch_status(launch_gemm_fp8_tensor(a, st));
     }
-    if (w_fmt == QLIN_FP8_BLOCK128 && x_fmt == QLIN_FP8_TOKEN) {
+    if (w_fmt == QLIN_FP8_BLOCK128 && (x_fmt == QLIN_FP8_TOKEN || x_fmt == QLIN_FP8_GROUP128)) {
         if (!x_scales_dev || !w_scales_dev) return QLIN_ERR_INVALID_ARG;
         if (N % 128 || K % 128) return QLIN_ERR_INVALID_ARG;
+        a.x_group128 = (x_fmt == QLIN_FP8_GROUP128);
         return launch_status(launch_gemm_fp8_block(a, st));
     }
     if (w_fmt == QLIN_MXFP8 && x_fmt == QLIN_MXFP8) {

@@ -32,7 +32,8 @@
 //                   partial with its fp32 weight-block scale (one uniform
 //                   load, a block ahead) into register accumulators (fp32
 //                   block scales are not an MMA scale type), then multiply
-//                   by the per-token scale.
+//                   by the per-token scale (or, for 1 x 128 activation
+//                   groups, fold each block's X scale into its multiplier).
 //   MXFP8           kind::mxf8f6f4.block_scale.scale_vec::1X, UE8M0 scales
 //                   copied smem -> TMEM with tcgen05.cp.
 //   NVFP4           kind::mxf4nvf4.block_scale.scale_vec::4X, UE4M3 scales,
@@ -127,6 +128,7 @@ struct TcParams {
     const uint16_t* bias;
     uint16_t* y;
     int* status;
+    int x_group;             // FP8 block: x_scale is [M, K/128] (1 x 128 groups) instead of [M]
 };
 
 __device__ __forceinline__ void record_timeout(int* status, volatile uint32_t* abort_flag) {
@@ -467,7 +469,12 @@ __global__ void __launch_bounds__(Cfg<KIND>::THREADS, 1)
                 const int nt = ncol >> 7;
                 const bool col_ok = ncol < p.N;
                 const int kblocks = p.K >> 7;
-                const float sx = (row < p.M) ? __ldg(p.x_scale + row) : 0.0f;
+                // per-token X scale (applied once at the end), or with 1 x 128 groups
+                // one X scale per block, folded into that block's multiplier
+                const bool xg = p.x_group != 0, row_ok = row < p.M;
+                const float sx = xg ? 1.0f : (row_ok ? __ldg(p.x_scale + row) : 0.0f);
+                const float* const sxrow = p.x_scale + (int64_t)(row_ok ? row : 0) * kblocks;
+                float sxg_next = xg ? (row_ok ? __ldg(sxrow) : 0.0f) : 1.0f;
                 // this half-tile's weight-block scales: one uniform load per block,
                 // issued a block ahead so that its latency is hidden
                 const float* const swrow = p.w_scale + (int64_t)(col_ok ? nt : 0) * kblocks;
@@ -476,8 +483,9 @@ __global__ void __launch_bounds__(Cfg<KIND>::THREADS, 1)
 #pragma unroll
                 for (int i = 0; i < 64; i++) acc2[i] = 0ull;
                 for (int kb = 0; kb < p.nk; kb++, kbg++) {
-                    const float sw = sw_next;
+                    const float sw = sw_next * sxg_next;
                     if (col_ok && kb + 1 < kblocks) sw_next = __ldg(swrow + kb + 1);
+                    if (xg && row_ok && kb + 1 < kblocks) sxg_next = __ldg(sxrow + kb + 1);
                     const int b = (int)(kbg & 1u);
                     if (!warp_wait_or_abort(pfull + b, (kbg >> 1) & 1u, abort_flag)) {
                         if (lane == 0) record_timeout(p.status, abort_flag);
@@ -627,6 +635,7 @@ cudaError_t launch_tc(const GemmArgs& a, cudaStream_t st) {
     p.bias = a.bias;
     p.y = a.y;
     p.status = a.dev_status;
+    p.x_group = a.x_group128 ? 1 : 0;
     static bool attr_set = false;
     if (!attr_set) {
         // The in-kernel setmaxnreg split assumes the launch allocation of

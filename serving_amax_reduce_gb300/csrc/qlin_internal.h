@@ -18,6 +18,8 @@ cudaError_t launch_fp8_tensor(const uint16_t* x, int64_t rows, int64_t K, int64_
                               cudaStream_t st);
 cudaError_t launch_fp8_block128(const uint16_t* x, int64_t rows, int64_t K, int64_t ld,
                                 uint8_t* codes, float* scales, cudaStream_t st);
+cudaError_t launch_fp8_group128(const uint16_t* x, int64_t rows, int64_t K, int64_t ld,
+                                uint8_t* codes, float* scales, cudaStream_t st);
 cudaError_t launch_mxfp8(const uint16_t* x, int64_t rows, int64_t K, int64_t ld, uint8_t* codes,
                          uint8_t* scales, bool mma_layout, cudaStream_t st);
 cudaError_t launch_mxfp4(const uint16_t* x, int64_t rows, int64_t K, int64_t ld, uint8_t* codes,
@@ -46,6 +48,7 @@ struct GemmArgs {
     void* workspace;
     size_t workspace_bytes;
     int* dev_status;
+    bool x_group128;          // FP8 block GEMM: x_scales per (row, 128-K group) instead of per row
 };
 
 cudaError_t launch_gemm_fp8_tensor(const GemmArgs& a, cudaStream_t st);

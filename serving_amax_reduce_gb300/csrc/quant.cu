@@ -1,5 +1,5 @@
-// Online quantizers: bf16 -> FP8 E4M3 (tensor / token / 128x128 block),
-// MXFP8, MXFP4, NVFP4 and int4 g128.  Each reads its bf16 input once from HBM in
+// Online quantizers: bf16 -> FP8 E4M3 (tensor / token / 1x128 group /
+// 128x128 block), MXFP8, MXFP4, NVFP4 and int4 g128.  Each reads its bf16 input once from HBM in
 // 16-byte vectors, reduces amax (or min/max) with warp shuffles, and writes
 // codes and scales in the same pass.  The per-tensor formats need the tensor
 // amax before any code exists, so they add one read-only amax pass.
@@ -273,6 +273,39 @@ __global__ void __launch_bounds__(256) k_fp8_block128(const uint16_t* __restrict
     if (threadIdx.x == 0) scales[bi * (K >> 7) + bj] = s;
 }
 
+// ---------------------------------------------------------------- 1 x 128 groups
+// Row tasks: a task's 32 vectors are two 128-element groups of one row, 16
+// lanes each; the group amax comes from four xor-shuffles inside the 16 lanes.
+// K % 128 == 0, so a group is entirely inside or outside the row.
+__global__ void __launch_bounds__(256) k_fp8_group128(const uint16_t* __restrict__ x, int64_t rows, int64_t K,
+                                                      int64_t ld, uint8_t* __restrict__ codes,
+                                                      float* __restrict__ scales) {
+    const uint32_t nvr = (uint32_t)(K >> 3), tpr = (nvr + 31) / 32, total = (uint32_t)rows * tpr;
+    const uint32_t warps = gridDim.x * 8, w0 = blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    for (uint32_t t = w0; t < total; t += warps * kUnroll) {
+        uint4 v[kUnroll];
+        TaskPos q[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; u++) {
+            q[u] = task_pos(t + u * warps, total, tpr, nvr, lane);
+            v[u] = q[u].in ? ld16(x + (int64_t)q[u].row * ld + 8 * q[u].c) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; u++) {
+            float a = absmax8(v[u]);
+#pragma unroll
+            for (int o = 1; o < 16; o <<= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
+            float sc, r;
+            fp8_params(a, sc, r);
+            if (!q[u].in) continue;
+            const int64_t row = q[u].row, c = q[u].c;
+            reinterpret_cast<uint2*>(codes + row * K)[c] = enc8_e4m3(v[u], r);
+            if ((c & 15) == 0) scales[row * (K >> 7) + (c >> 4)] = sc;
+        }
+    }
+}
+
 // ---------------------------------------------------------------- MXFP8 / MXFP4
 // The MX rule with the element format's largest power-of-two exponent: 8 for
 // E4M3 (MXFP8), 2 for E2M1 (MXFP4, codes two per byte).  Four consecutive
@@ -503,6 +536,14 @@ cudaError_t launch_fp8_block128(const uint16_t* x, int64_t rows, int64_t K, int6
                                 float* scales, cudaStream_t st) {
     dim3 grid((unsigned)(K / 128), (unsigned)(rows / 128));
     k_fp8_block128<<<grid, 256, 0, st>>>(x, K, ld, codes, scales);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_fp8_group128(const uint16_t* x, int64_t rows, int64_t K, int64_t ld, uint8_t* codes,
+                                float* scales, cudaStream_t st) {
+    const int64_t tasks = task_count(rows, K);
+    if (tasks < 0) return cudaErrorInvalidValue;
+    k_fp8_group128<<<task_grid(tasks), 256, 0, st>>>(x, rows, K, ld, codes, scales);
     return cudaGetLastError();
 }
 

@@ -127,6 +127,14 @@ def mxfp8_linear(K: int, N: int, M: int = MXFP8_M) -> Linear:
                   _seed(4, 2 * v), _seed(4, 2 * v + 1), "normal", x_std=1.0, w_std=0.015)
 
 
+def fp8_group_linear(K: int, N: int, M: int = 4096) -> Linear:
+    """FP8 1 x 128 dynamic activation groups x 128x128-block weights on the DiT MLP
+    shapes and distributions of the FP8 block workload (1% outlier channels)."""
+    v = FP8_MLP_SHAPES.index((K, N)) if (K, N) in FP8_MLP_SHAPES else 5
+    return Linear(f"fp8_group_K{K}_N{N}", M, K, N, "fp8_group128", "fp8_block128",
+                  _seed(7, 2 * v), _seed(7, 2 * v + 1), "outlier", x_std=1.0, w_std=0.02)
+
+
 def mxfp4_linear(K: int, N: int, M: int = MXFP8_M) -> Linear:
     """MXFP4 W4A4 (the next format of the online MXFP4 path) on the video-DiT
     shapes and distributions of the MXFP8 workload: X N(0,1), W N(0, 0.015^2)."""

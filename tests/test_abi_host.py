@@ -59,6 +59,9 @@ def test_size_queries(q):
     assert q.qlin_scales_bytes(F.MXFP4, L.CANONICAL, 20280, 5120) == 20280 * 160
     assert q.qlin_scales_bytes(F.MXFP4, L.MMA, 20280, 5120) == 20352 * 160
     assert q.qlin_quant_workspace_bytes(F.MXFP4, 20280, 5120) == 0
+    # FP8 1 x 128 groups: one float per row and 128 K
+    assert q.qlin_codes_bytes(F.FP8_GROUP128, 4096, 3072) == 4096 * 3072
+    assert q.qlin_scales_bytes(F.FP8_GROUP128, L.CANONICAL, 4096, 3072) == 4096 * 24 * 4
 
 
 FAKE = 1 << 20          # a 16-byte aligned non-null value; never dereferenced by these calls
@@ -99,6 +102,10 @@ def test_quantize_rejects_bad_arguments(q):
                                None) == S.INVALID_ARG
     assert q.qlin_quantize_act(F.MXFP4, FAKE, 128, 80, 80, FAKE, FAKE, None, L.CANONICAL, None, 0, None,
                                None) == S.INVALID_ARG                  # K % 32
+    assert q.qlin_quantize_act(F.FP8_GROUP128, FAKE, 128, 96, 96, FAKE, FAKE, None, L.CANONICAL, None, 0, None,
+                               None) == S.INVALID_ARG                  # K % 128
+    assert q.qlin_quantize_act(F.FP8_GROUP128, FAKE, 128, 128, 128, FAKE, FAKE, None, L.MMA, None, 0, None,
+                               None) == S.UNSUPPORTED                  # no tensor-core scale layout
     # NVFP4 needs the global-scale output
     assert q.qlin_quantize_act(F.NVFP4, FAKE, 128, 1024, 1024, FAKE, FAKE, None, L.CANONICAL, FAKE, 1 << 20,
                                None, None) == S.INVALID_ARG
@@ -132,6 +139,9 @@ def test_gemm_rejects_bad_arguments(q):
     assert g(F.MXFP4, F.MXFP4, 128, 1024, 1024) == S.UNSUPPORTED          # canonical scales
     assert g(F.MXFP4, F.MXFP4, 128, 1024, 1152, layout=L.MMA) == S.INVALID_ARG   # K % 256
     assert g(F.MXFP4, F.MXFP8, 128, 1024, 1024, layout=L.MMA) == S.UNSUPPORTED
+    assert g(F.FP8_BLOCK128, F.FP8_GROUP128, 128, 1024, 1000) == S.INVALID_ARG   # K % 128
+    assert g(F.FP8_BLOCK128, F.FP8_GROUP128, 128, 1024, 1024, xs=None) == S.INVALID_ARG
+    assert g(F.FP8_TENSOR, F.FP8_GROUP128, 128, 1024, 1024) == S.UNSUPPORTED
     assert g(F.FP8_TENSOR, F.FP8_TOKEN, 128, 1024, 1024) == S.UNSUPPORTED
     assert g(F.INT4_G128_ASYM, F.BF16, 16, 4096, 4000) == S.INVALID_ARG
     need = q.qlin_gemm_workspace_bytes(F.INT4_G128_ASYM, F.BF16, 16, 4096, 4096)

@@ -111,6 +111,39 @@ def test_fp8_block_gemm_full_size(q, orc, B, K, N):
     fp8_block_case(q, orc, 4096 * B, N, K, nrows=256)
 
 
+# ------------------------------------------------------------------ FP8 128x128 block W x 1x128 group X
+def fp8_group_case(q, orc, M, N, K, nrows=None, with_bias=False):
+    lin = inputs.fp8_block_linear(1, K, N, M=M)
+    x, w = lin.make_x(), lin.make_w()
+    F = q.Fmt
+    bx = q.quantize_act(F.FP8_GROUP128, x.cuda())
+    bw = q.quantize_weight(F.FP8_BLOCK128, w.cuda())
+    bias = inputs.normal_bf16((1, N), 0.05, 80)[0] if with_bias else None
+    y = q.gemm(F.FP8_BLOCK128, F.FP8_GROUP128, M, N, K, bx["codes"], bx["scales"], bw["codes"], bw["scales"],
+               bias=bias.cuda() if with_bias else None)
+    torch.cuda.synchronize()
+    rows = sample_rows(M, nrows or M)
+    xh = orc.dequant_fp8_group128(np_u8(bx["codes"]).reshape(M, K)[rows],
+                                  np_f32(bx["scales"]).reshape(M, K // 128)[rows])
+    wh = orc.dequant_fp8_block128(np_u8(bw["codes"]).reshape(N, K), np_f32(bw["scales"]).reshape(N // 128, K // 128))
+    b = orc.bf16_values(bits(bias)[None, :])[0] if with_bias else None
+    return check(orc, y_np(y)[rows], orc.gemm_ref(xh, wh, bias=b), x, w, rows=torch.from_numpy(rows))
+
+
+@pytest.mark.parametrize("M,N,K", [(200, 512, 384), (128, 256, 128), (1, 384, 256), (513, 1280, 1152)])
+def test_fp8_group128_gemm(q, orc, M, N, K):
+    fp8_group_case(q, orc, M, N, K)
+
+
+def test_fp8_group128_gemm_bias(q, orc):
+    fp8_group_case(q, orc, 130, 640, 256, with_bias=True)
+
+
+@pytest.mark.slow
+def test_fp8_group128_gemm_full_size(q, orc):
+    fp8_group_case(q, orc, 4096, 12288, 3072, nrows=256)
+
+
 # ------------------------------------------------------------------ MXFP8
 def mxfp8_case(q, orc, M, N, K, nrows=None):
     lin = inputs.mxfp8_linear(K, N, M=M)

@@ -101,6 +101,16 @@ def test_nvfp4(q, orc, rows, K, kind, mma):
         assert np.array_equal(got[: rows * K // 16].reshape(rows, K // 16), sc)
 
 
+@pytest.mark.parametrize("rows,K", [(1, 128), (200, 3072), (300, 12288), (7, 384)])
+@pytest.mark.parametrize("kind", ["outlier", "edge"])
+def test_fp8_group128(q, orc, rows, K, kind):
+    x = make(kind, rows, K, 17 * rows + K)
+    b = run(q, q.Fmt.FP8_GROUP128, x)
+    codes, s = orc.quant_fp8_group128(bits(x))
+    assert np.array_equal(np_u8(b["codes"]).reshape(rows, K), codes)
+    assert np.array_equal(np_f32(b["scales"]).reshape(rows, K // 128).view(np.uint32), s.view(np.uint32))
+
+
 @pytest.mark.parametrize("rows,K", [(1, 128), (200, 5120), (128, 13824), (77, 96)])
 @pytest.mark.parametrize("kind", ["normal", "edge"])
 @pytest.mark.parametrize("mma", [False, True])
