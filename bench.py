@@ -57,6 +57,24 @@ def parse_args():
     return ap.parse_args()
 
 
+# ---------------------------------------------------------------- ranks
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """The largest value over all ranks: a job's time is its slowest rank's."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 # ---------------------------------------------------------------- workload description
 def workload_linears(next_rows: bool = False):
     from serving_amax_reduce_gb300 import inputs as I
@@ -300,11 +318,6 @@ def run_native(args, rank, world, local_rank):
     if q.read_device_status(dev) != 0:
         raise RuntimeError("a bounded device wait expired during warm-up")
 
-    def barrier():
-        if world > 1:
-            import torch.distributed as dist
-            dist.barrier()
-
     # The step is captured once as a CUDA graph (about 80 library launches);
     # per-call timing events become event-record nodes of the same graph.
     graph, gevents, mode = None, [], "eager"
@@ -324,7 +337,7 @@ def run_native(args, rank, world, local_rank):
     # ---- timed region (device time of whole steps)
     sampler = ClockSampler(local_rank if os.environ.get("CUDA_VISIBLE_DEVICES") is None else 0)
     events = []
-    barrier()
+    barrier(world)
     torch.cuda.synchronize()
     sampler.start()
     t0 = torch.cuda.Event(enable_timing=True)
@@ -337,7 +350,7 @@ def run_native(args, rank, world, local_rank):
             step(events, lambda: torch.cuda.Event(enable_timing=True))
     t1.record(stream)
     torch.cuda.synchronize()
-    barrier()
+    barrier(world)
     clocks = sampler.stop()
     ms_total = t0.elapsed_time(t1)
     if q.read_device_status(dev) != 0:
@@ -355,11 +368,7 @@ def run_native(args, rank, world, local_rank):
     else:
         events = [(j, op, e0.elapsed_time(e1)) for j, op, e0, e1 in events]
         per_call_steps = args.steps
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_total = float(tt.item())
+    ms_total = max_over_ranks(ms_total, world, dev)
 
     flops_step = sum(j.lin.flops() for j in jobs)
     ms_step = ms_total / args.steps
@@ -501,11 +510,7 @@ def run_e2e(args, jobs, stream, flops_step, world, dev):
     t1.record(stream)
     torch.cuda.synchronize()
     ms = t0.elapsed_time(t1)
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(ms, world, dev)
     return {"value": round(flops_step * n * world / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n,
             "ms_per_step": round(ms / n, 3)}
