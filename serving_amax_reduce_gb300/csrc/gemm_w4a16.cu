@@ -49,27 +49,33 @@ constexpr int QW_BYTES = 16 * 128 * 4;     // one 128-K group: 16 k-octets x 128
 constexpr int A_COLS = 64;                 // TMEM columns per dequantized group (128 K as bf16 pairs)
 constexpr int ZCH = 16;                    // groups of one dequant set whose zero points are staged at a time
 constexpr int SCH = 16;                    // groups whose scales are staged at a time (epilogue)
-constexpr int THREADS = 512;               // 16 warps, see the role map in k_w4a16
 constexpr uint32_t TMEM_COLS = 512;
 
 template <int MP>
 struct W4Cfg {
+    // Dequant sets of four warps take groups in turn.  (Four sets measured no
+    // faster than two: the tensor pipe's small-MMA rate and the handoffs bound
+    // a group, not the dequant arithmetic.)
+    static constexpr int NSETS = 2;
+    static constexpr int E0 = 2 + 4 * NSETS;                        // first epilogue warp
+    static constexpr int THREADS = 32 * (E0 + 6);                   // + 4 epilogue, X producer, odd MMA issuer
     static constexpr int XSUB = MP * 128;                           // one 64-K X sub-tile
     static constexpr int X_BYTES = 2 * XSUB;                        // one group of X
-    // A stages in TMEM = X slots in shared memory (both freed by the same MMA
-    // completion); partial buffers in TMEM.  Both even: each stage always
-    // belongs to the same one of the two MMA issuers.
-    static constexpr int RA = (MP <= 32) ? 6 : 4;
-    static constexpr int RP = 4;
-    static constexpr int XS = RA;
+    // One ring of R group slots: a TMEM A stage, an X slot in shared memory and
+    // a TMEM partial buffer move together, so that one commit per group frees
+    // the A stage and the X slot and announces the partial (the tensor pipe
+    // takes a commit about as slowly as a small MMA).  R is even, so that each
+    // slot always belongs to the same one of the two MMA issuers.
+    static constexpr int R = (MP == 16) ? 6 : 4;
+    static constexpr int RA = R, RP = R, XS = R;
     static constexpr int QS = (MP <= 32) ? 16 : 12;                 // weight ring depth (groups)
     static constexpr int OFF_QW = 0;                                // weight ring
     static constexpr int OFF_X = OFF_QW + QS * QW_BYTES;
     static constexpr int OFF_ZT = OFF_X + XS * X_BYTES;             // zero points [2 sets][ZCH][128] bytes
-    static constexpr int OFF_ST = OFF_ZT + 2 * ZCH * 128;           // scales [SCH][128] floats
+    static constexpr int OFF_ST = OFF_ZT + NSETS * ZCH * 128;       // scales [SCH][128] floats
     static constexpr int OFF_RED = OFF_ST + SCH * 128 * 4;          // split-K partial tile [MP][128] fp32
     static constexpr int OFF_BAR = OFF_RED + MP * 128 * 4;
-    static constexpr int NBAR = 2 * QS + 3 * RA + 2 * RP + 1;
+    static constexpr int NBAR = 2 * QS + 4 * R + 1;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int SMEM = OFF_MISC + 64 + 1024;
     static constexpr uint32_t P_COL = RA * A_COLS;                  // partial buffers follow the A stages
@@ -154,23 +160,22 @@ __device__ __forceinline__ uint4 permute_x_chunk(uint4 c) {
 }
 
 template <int MP>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(W4Cfg<MP>::THREADS, 1)
     k_w4a16(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmX, const W4Params p) {
     // Role map: warp 0 weight TMA, warp 1 MMA for even groups (and TMEM owner),
-    // warps 2-5 / 6-9 dequantize even / odd groups (TMEM lane quadrant =
-    // warp % 4), warps 10-13 epilogue (quadrant = warp % 4), warp 14 X TMA,
-    // warp 15 MMA for odd groups.
+    // warps 2 .. E0-1 dequantize in NSETS sets of four (set s takes the groups
+    // t % NSETS == s; TMEM lane quadrant = warp % 4), warps E0 .. E0+3 epilogue
+    // (quadrant = warp % 4), warp E0+4 X TMA, warp E0+5 MMA for odd groups.
     using C = W4Cfg<MP>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* qfull = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
     uint64_t* qempty = qfull + C::QS;
-    uint64_t* xfull = qempty + C::QS;    // X slot a loaded (TMA)
-    uint64_t* afull = xfull + C::RA;     // A stage a written and X slot a permuted
-    uint64_t* mdone = afull + C::RA;     // the MMAs of stage a finished: A stage and X slot free
-    uint64_t* pfull = mdone + C::RA;     // partial p ready
-    uint64_t* pempty = pfull + C::RP;    // the epilogue has read partial p
-    uint64_t* drain = pempty + C::RP;
+    uint64_t* xfull = qempty + C::QS;    // slot r: X loaded (TMA)
+    uint64_t* afull = xfull + C::R;      // slot r: A stage written and X permuted
+    uint64_t* done = afull + C::R;       // slot r: its MMAs finished (A stage, X slot free; partial ready)
+    uint64_t* pempty = done + C::R;      // slot r: the epilogue has read the partial
+    uint64_t* drain = pempty + C::R;
     // tmem, abort, -, weight groups issued, X groups issued
     uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
     volatile uint32_t* abort_flag = misc + 1;
@@ -187,13 +192,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(qfull + s, 1);
             mbar_init(qempty + s, 4);             // the four warps of one dequant set
         }
-        for (int s = 0; s < C::RA; s++) {
+        for (int s = 0; s < C::R; s++) {
             mbar_init(xfull + s, 1);
             mbar_init(afull + s, 4);              // the four warps of one dequant set
-            mbar_init(mdone + s, 1);              // an MMA commit
-        }
-        for (int s = 0; s < C::RP; s++) {
-            mbar_init(pfull + s, 1);              // an MMA commit
+            mbar_init(done + s, 1);               // one MMA commit per group
             mbar_init(pempty + s, 4);             // the four epilogue warps
         }
         mbar_init(drain, 2);                      // both MMA issuers
@@ -222,11 +224,11 @@ __global__ void __launch_bounds__(THREADS, 1)
             tma_load_2d(smem + C::OFF_QW + s * QW_BYTES, &tmQ, n0, (g0 + t) * 16, qfull + s);
             misc[3] = (uint32_t)(t + 1);
         }
-    } else if (!skip && warp == 14 && lane == 0) {
+    } else if (!skip && warp == C::E0 + 4 && lane == 0) {
         // ------------------------------------------------ activation producer (L2)
         for (int t = 0; t < ng_cta; t++) {
-            const int s = t % C::RA;
-            if (!wait_or_abort(mdone + s, ((uint32_t)(t / C::RA) & 1u) ^ 1u, abort_flag)) {
+            const int s = t % C::R;
+            if (!wait_or_abort(done + s, ((uint32_t)(t / C::R) & 1u) ^ 1u, abort_flag)) {
                 record_timeout(p.status, abort_flag);
                 break;
             }
@@ -236,10 +238,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             tma_load_2d(smem + C::OFF_X + s * C::X_BYTES + C::XSUB, &tmX, k + 64, m0, xfull + s);
             misc[4] = (uint32_t)(t + 1);
         }
-    } else if (!skip && (warp == 1 || warp == 15) && lane == 0) {
+    } else if (!skip && (warp == 1 || warp == C::E0 + 5) && lane == 0) {
         // ------------------------------------------------ MMA issuers (even / odd groups)
         for (int t = (warp == 1) ? 0 : 1; t < ng_cta; t += 2) {
-            const int a = t % C::RA, pb = t % C::RP;
+            const int a = t % C::RA, pb = t % C::RP, sx = t % C::XS;
             // afull: the dequant set has written A and permuted this group's X tile
             if (!wait_or_abort(afull + a, (uint32_t)(t / C::RA) & 1u, abort_flag) ||
                 !wait_or_abort(pempty + pb, ((uint32_t)(t / C::RP) & 1u) ^ 1u, abort_flag)) {
@@ -248,7 +250,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             tc_fence_after();
             const uint32_t a_t = tmem + (uint32_t)(a * A_COLS);
-            const uint32_t x_base = smem_u32(smem + C::OFF_X + a * C::X_BYTES);
+            const uint32_t x_base = smem_u32(smem + C::OFF_X + sx * C::X_BYTES);
             const uint32_t d = tmem + C::P_COL + (uint32_t)(pb * MP);
 #pragma unroll
             for (int j = 0; j < 2; j++)
@@ -256,39 +258,38 @@ __global__ void __launch_bounds__(THREADS, 1)
                 for (int c = 0; c < 4; c++)
                     mma_f16_ta(d, a_t + (uint32_t)((j * 4 + c) * 8), sdesc_sw128(x_base + j * C::XSUB + c * 32),
                                C::IDESC, (j > 0 || c > 0) ? 1u : 0u);
-            tc_commit(mdone + a);
-            tc_commit(pfull + pb);
+            tc_commit(done + a);
         }
-    } else if (!skip && warp >= 2 && warp < 10) {
+    } else if (!skip && warp >= 2 && warp < C::E0) {
         // ------------------------------------------------ dequantizers
-        const int set = (warp - 2) >> 2;           // 0: even groups, 1: odd groups
+        const int set = (warp - 2) >> 2;           // takes groups t with t % NSETS == set
         const int quad = warp & 3;                 // the TMEM lanes this warp may write
         const int n = quad * 32 + lane;            // channel of the tile = TMEM lane = row of A
         const int ng = n0 + n;
         uint8_t* const zt = smem + C::OFF_ZT + set * (ZCH * 128);   // column n of [ZCH][128]
         const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
         int u = 0;                                 // index of t among this set's groups
-        for (int t = set; t < ng_cta; t += 2, u++) {
+        for (int t = set; t < ng_cta; t += C::NSETS, u++) {
             if ((u % ZCH) == 0) {
                 // the zero points of this set's next ZCH groups, all loads in flight at once
                 uint32_t zw[ZCH];
 #pragma unroll
                 for (int i = 0; i < ZCH; i++)
-                    zw[i] = (ng < p.N && t + 2 * i < ng_cta)
-                                ? (uint32_t)__ldg(p.qzeros + (int64_t)(g0 + t + 2 * i) * (p.N >> 3) + (ng >> 3))
+                    zw[i] = (ng < p.N && t + C::NSETS * i < ng_cta)
+                                ? (uint32_t)__ldg(p.qzeros + (int64_t)(g0 + t + C::NSETS * i) * (p.N >> 3) + (ng >> 3))
                                 : 0u;
 #pragma unroll
                 for (int i = 0; i < ZCH; i++) zt[i * 128 + n] = (uint8_t)((zw[i] >> (4 * (ng & 7))) & 0xFu);
             }
-            const int s = t % C::QS, a = t % C::RA;
-            if (!warp_wait(xfull + a, (uint32_t)(t / C::RA) & 1u, abort_flag) ||
+            const int s = t % C::QS, a = t % C::RA, sx = t % C::XS;
+            if (!warp_wait(xfull + sx, (uint32_t)(t / C::XS) & 1u, abort_flag) ||
                 !warp_wait(qfull + s, (uint32_t)(t / C::QS) & 1u, abort_flag)) {
                 if (lane == 0) record_timeout(p.status, abort_flag);
                 break;
             }
             {
                 // this group's X tile (MP x 128 bf16 = MP * 16 chunks), permuted in place
-                uint4* xc = reinterpret_cast<uint4*>(smem + C::OFF_X + a * C::X_BYTES);
+                uint4* xc = reinterpret_cast<uint4*>(smem + C::OFF_X + sx * C::X_BYTES);
 #pragma unroll
                 for (int i = 0; i < MP / 8; i++) xc[i * 128 + n] = permute_x_chunk(xc[i * 128 + n]);
                 fence_proxy_async_smem();            // the MMA reads X through the async proxy
@@ -305,9 +306,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             uint32_t av[64];
 #pragma unroll
             for (int o = 0; o < 16; o++) dequant8(w[o], bias2, av + 4 * o);
-            // only the TMEM write waits for the stage's previous MMAs, so the
+            // only the TMEM write waits for the slot's previous MMAs, so the
             // loads and the arithmetic above overlap them
-            if (!warp_wait(mdone + a, ((uint32_t)(t / C::RA) & 1u) ^ 1u, abort_flag)) {
+            if (!warp_wait(done + a, ((uint32_t)(t / C::RA) & 1u) ^ 1u, abort_flag)) {
                 if (lane == 0) record_timeout(p.status, abort_flag);
                 break;
             }
@@ -318,7 +319,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(afull + a);
         }
-    } else if (!skip && warp >= 10 && warp < 14) {
+    } else if (!skip && warp >= C::E0 && warp < C::E0 + 4) {
         // ------------------------------------------------ epilogue (scale promotion)
         const int q = warp & 3;
         const int n = q * 32 + lane;
@@ -347,7 +348,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                         st[(i0 + i) * 128 + n] = __bfloat162float(__ushort_as_bfloat16(sw[i]));
                 }
             }
-            if (!warp_wait(pfull + pb, (uint32_t)(t / C::RP) & 1u, abort_flag)) {
+            if (!warp_wait(done + pb, (uint32_t)(t / C::RP) & 1u, abort_flag)) {
                 if (lane == 0) record_timeout(p.status, abort_flag);
                 epi_ok = false;
                 break;
@@ -391,10 +392,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int wq = (int)misc[3], wx = (int)misc[4];
         for (int t = (wq > C::QS ? wq - C::QS : 0); t < wq; t++)
             mbar_wait(qfull + (t % C::QS), (uint32_t)(t / C::QS) & 1u, kWaitLimitNs);
-        for (int t = (wx > C::RA ? wx - C::RA : 0); t < wx; t++)
-            mbar_wait(xfull + (t % C::RA), (uint32_t)(t / C::RA) & 1u, kWaitLimitNs);
+        for (int t = (wx > C::XS ? wx - C::XS : 0); t < wx; t++)
+            mbar_wait(xfull + (t % C::XS), (uint32_t)(t / C::XS) & 1u, kWaitLimitNs);
     }
-    if (*abort_flag && (warp == 1 || warp == 15) && lane == 0) {
+    if (*abort_flag && (warp == 1 || warp == C::E0 + 5) && lane == 0) {
         tc_commit(drain);                          // each issuer's own MMAs
         mbar_wait(drain, 0, kWaitLimitNs);
     }
@@ -505,7 +506,7 @@ cudaError_t launch_mp(const GemmArgs& a, cudaStream_t st) {
     const int cs = pick_split(ntiles * mtiles, p.groups);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)cs, (unsigned)ntiles, (unsigned)mtiles);
-    cfg.blockDim = dim3(THREADS);
+    cfg.blockDim = dim3(C::THREADS);
     cfg.dynamicSmemBytes = C::SMEM;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
