@@ -236,10 +236,10 @@ class Job:
 # as null once the kernel's source differs from the one the counters came from.
 MEASURED_TRAFFIC = {
     "gemm_fp8_block": {
-        "dram_bytes": 80784128 + 58381056,
+        "dram_bytes": 78276864 + 57034496,
         "alg_bytes": 4096 * 3072 + 4096 * 4 + 12288 * 3072 + 96 * 24 * 4 + 4096 * 12288 * 2,
         "source": "serving_amax_reduce_gb300/csrc/gemm_tc.cu",
-        "sha256": "7c80333d773b7dc87e0b495c0573fcd031a24ab82ba204790e9feb543f127d7d",
+        "sha256": "d2682fd0443500a01999d35bc09ab22ddc8fd183823f3e96b94d8a1bdcb8e4da",
         "captured": "M4096 K3072 N12288 (one bench launch)",
     },
 }
@@ -517,27 +517,37 @@ def run_e2e(args, jobs, stream, flops_step, world, dev):
 
 
 # ---------------------------------------------------------------- oracle timing
-def oracle_sample_step(rows_x: int, rows_w: int):
-    """The CPU oracle on a bounded sample of the workload: for one linear of
-    each workload, quantize rows_x rows of X and rows_w rows of W, dequantize,
-    and form the float64 product.  Returns (flops, seconds)."""
+def oracle_sample_inputs(rows_x: int, rows_w: int):
+    """A bounded sample of the workload for the CPU oracle: one linear of each
+    workload, cut to its first rows_x rows of X and rows_w rows of W (full K).
+    Returns (linear, X bits, W bits, rows of X, rows of W) per linear; the
+    bf16 bits are produced here, outside any timed region."""
     import numpy as np
     import torch
 
-    import oracle
     from serving_amax_reduce_gb300 import inputs as I
 
     picks = [I.fp8_tensor_linear(), I.w4a16_linear(16, 4096, 4096), I.fp8_block_linear(1, 3072, 12288),
              I.mxfp8_linear(5120, 13824), I.mixed_stack()[0]]
-    flops, secs = 0, 0.0
+    out = []
     for lin in picks:
         Ms = min(rows_x, lin.M)
         Ns = min(rows_w, lin.N)
         Ns -= Ns % 128 if lin.w_fmt in ("fp8_block128",) else Ns % 8
         x = lin.make_x()[:Ms].contiguous()
         w = lin.make_w()[:Ns].contiguous()
-        xb = x.view(torch.int16).numpy().view(np.uint16)
-        wb = w.view(torch.int16).numpy().view(np.uint16)
+        out.append((lin, x.view(torch.int16).numpy().view(np.uint16), w.view(torch.int16).numpy().view(np.uint16),
+                    Ms, Ns))
+    return out
+
+
+def oracle_sample_pass(sample):
+    """One timed pass of the CPU oracle over a prepared sample: quantize X and
+    W, dequantize, and form the float64 product.  Returns (flops, seconds)."""
+    import oracle
+
+    flops, secs = 0, 0.0
+    for lin, xb, wb, Ms, Ns in sample:
         t = time.perf_counter()
         if lin.w_fmt == "fp8_tensor":
             cx, sx = oracle.quant_fp8_tensor(xb); cw, sw = oracle.quant_fp8_tensor(wb)
@@ -560,8 +570,9 @@ def oracle_sample_step(rows_x: int, rows_w: int):
     return flops, secs
 
 
-SAMPLE_BASELINE = (512, 1024)      # rows of X, rows of W per linear (cpu_baseline leg)
-SAMPLE_REFERENCE = (256, 512)      # per step of the --impl reference arm
+SAMPLE_BASELINE = (2048, 4096)     # rows of X, rows of W per linear (cpu_baseline leg)
+BASELINE_MIN_SECONDS = 12.0        # cpu_baseline repeats passes until this much oracle time
+SAMPLE_REFERENCE = (1024, 2048)    # per step of the --impl reference arm
 
 
 def blas_threads():
@@ -579,10 +590,18 @@ def blas_threads():
 def cpu_baseline():
     import oracle
     oracle.build()
-    flops, secs = oracle_sample_step(*SAMPLE_BASELINE)
+    sample = oracle_sample_inputs(*SAMPLE_BASELINE)
+    flops = secs = 0
+    passes = 0
+    while secs < BASELINE_MIN_SECONDS:
+        f, t = oracle_sample_pass(sample)
+        flops += f
+        secs += t
+        passes += 1
     return {"value": round(flops / secs / 1e12, 6), "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
-            "sample": (f"one linear per workload, X[:{SAMPLE_BASELINE[0]}] x W[:{SAMPLE_BASELINE[1]}] full K: "
-                       "scalar C quantizers (1 thread) + float64 numpy matmul (BLAS threads)"),
+            "sample": (f"{passes} passes over one linear per workload, X[:{SAMPLE_BASELINE[0]}] x "
+                       f"W[:{SAMPLE_BASELINE[1]}] at full K ({flops / passes / 1e9:.0f} GFLOP per pass): scalar C "
+                       "quantizers (1 thread) + float64 numpy matmul (BLAS threads)"),
             "seconds": round(secs, 2)}
 
 
@@ -591,11 +610,12 @@ def run_reference(args, rank, world):
     oracle.build()
     if rank != 0:
         return None
+    sample = oracle_sample_inputs(*SAMPLE_REFERENCE)
     for _ in range(args.warmup):
-        oracle_sample_step(*SAMPLE_REFERENCE)
+        oracle_sample_pass(sample)
     flops = secs = 0
     for _ in range(args.steps):
-        f, s = oracle_sample_step(*SAMPLE_REFERENCE)
+        f, s = oracle_sample_pass(sample)
         flops += f
         secs += s
     v = flops / secs / 1e12

@@ -3,8 +3,8 @@
 The data path has no collective (each rank is an independent replica), so
 what the ranks share is the timing: a barrier around the timed region and the
 maximum of the ranks' times.  These run as two gloo processes.  The reference
-arm is also launched the way the driver launches it, under
-torch.distributed.run with two ranks: rank 0 alone works and prints one line.
+arm is also launched under torch.distributed.run with two ranks, as a
+multi-GPU bench run is: rank 0 alone works and prints one line.
 """
 import json
 import os
