@@ -9,7 +9,7 @@ Two layers:
 * ``qlin_oracle.c`` (built here into ``_build/liboracle.so`` with gcc, strict
   IEEE binary32, no contraction): scalar codecs and quantizers, written one
   element at a time from the format definitions.  See its header for the
-  readings R1..R5 taken where the pages name a format but print no formula.
+  readings R1..R8 taken where the pages name a format but print no formula.
 * this module: numpy marshalling, and the GEMM reference, which is the plain
   definition Y = Xhat @ What^T evaluated in float64 over the dequantized
   operands (``numpy.matmul`` as the one library step).
@@ -79,6 +79,7 @@ def _load():
             "oracle_quant_nvfp4": ([P, I64, I64, I64, P, P, P], None),
             "oracle_quant_mxfp4": ([P, I64, I64, I64, P, P], None),
             "oracle_quant_int4_g128": ([P, I64, I64, I64, P, P, P], None),
+            "oracle_quant_int8_row": ([P, I64, I64, I64, P, P], None),
             "oracle_dequant_fp8_tensor": ([P, I64, I64, F, P], None),
             "oracle_dequant_fp8_token": ([P, I64, I64, P, P], None),
             "oracle_dequant_fp8_block128": ([P, I64, I64, P, P], None),
@@ -87,6 +88,7 @@ def _load():
             "oracle_dequant_nvfp4": ([P, I64, I64, P, F, P], None),
             "oracle_dequant_mxfp4": ([P, I64, I64, P, P], None),
             "oracle_dequant_int4_g128": ([P, P, P, I64, I64, P], None),
+            "oracle_dequant_int8_row": ([P, I64, I64, P, P], None),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
@@ -162,6 +164,17 @@ def quant_fp8_token(x):
     codes = np.empty((R, K), np.uint8)
     s = np.empty(R, np.float32)
     _load().oracle_quant_fp8_token(_p(x), R, K, K, _p(codes), _p(s))
+    return codes, s
+
+
+def quant_int8_row(x):
+    """Symmetric INT8, one scale per row (a token of X or a channel of W)
+    -> (codes int8 [R,K], scales float32 [R])."""
+    x = _bf16_bits(x)
+    R, K = x.shape
+    codes = np.empty((R, K), np.int8)
+    s = np.empty(R, np.float32)
+    _load().oracle_quant_int8_row(_p(x), R, K, K, _p(codes), _p(s))
     return codes, s
 
 
@@ -257,6 +270,14 @@ def dequant_fp8_token(codes, scales):
     scales = np.ascontiguousarray(scales, np.float32)
     out = _f64(codes.shape)
     _load().oracle_dequant_fp8_token(_p(codes), codes.shape[0], codes.shape[1], _p(scales), _p(out))
+    return out
+
+
+def dequant_int8_row(codes, scales):
+    codes = np.ascontiguousarray(codes, np.int8)
+    scales = np.ascontiguousarray(scales, np.float32)
+    out = _f64(codes.shape)
+    _load().oracle_dequant_int8_row(_p(codes), codes.shape[0], codes.shape[1], _p(scales), _p(out))
     return out
 
 

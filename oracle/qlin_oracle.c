@@ -52,6 +52,14 @@
  *       "FP8: vLLM의 핵심 양자화", the block-128 dynamic symmetric scheme
  *       applied to activations): the R1 granule is 1 x 128, one token times
  *       128 consecutive K elements, with one fp32 scale per (row, K/128).
+ *   R8  INT8 W8A8 ("vLLM-Omni 在线量化（Online Quantization）完全指南",
+ *       section "在线量化的底层工作原理": the CUDA online INT8 path makes
+ *       the weight codes and their scales with a scaled int8 quantizer;
+ *       section "核心参数详解": activations are dynamic only): symmetric
+ *       per-row granule, one fp32 scale per weight output channel and one
+ *       per activation token, s = amax/127, codes = clamp(rint(x * (127/amax)),
+ *       -127, 127) as two's-complement bytes; amax == 0 gives s = 1 and
+ *       multiplier 1.
  */
 #include <math.h>
 #include <stdint.h>
@@ -376,6 +384,33 @@ void oracle_quant_int4_g128(const uint16_t *w, int64_t N, int64_t K, int64_t ld,
 }
 
 /* ------------------------------------------------------------------ */
+/* INT8 symmetric, one fp32 scale per row (R8)                          */
+/* ------------------------------------------------------------------ */
+
+/* codes: rows x K int8, row-major; scales: rows.  A row is one token of X or
+ * one output channel of W. */
+void oracle_quant_int8_row(const uint16_t *x, int64_t rows, int64_t K, int64_t ld,
+                           int8_t *codes, float *scales)
+{
+    for (int64_t i = 0; i < rows; i++) {
+        float amax = 0.0f, s = 1.0f, r = 1.0f;
+        for (int64_t k = 0; k < K; k++)
+            amax = fmaxf(amax, fabsf(oracle_bf16_to_f32(x[i * ld + k])));
+        if (amax != 0.0f) {
+            s = amax / 127.0f;
+            r = 127.0f / amax;
+        }
+        for (int64_t k = 0; k < K; k++) {
+            float q = rintf(oracle_bf16_to_f32(x[i * ld + k]) * r);
+            if (q > 127.0f) q = 127.0f;
+            if (q < -127.0f) q = -127.0f;
+            codes[i * K + k] = (int8_t)(int)q;
+        }
+        scales[i] = s;
+    }
+}
+
+/* ------------------------------------------------------------------ */
 /* dequantizers: codes + scales -> exact values in binary64            */
 /* ------------------------------------------------------------------ */
 
@@ -455,4 +490,12 @@ void oracle_dequant_int4_g128(const int32_t *qweight, const uint16_t *scales,
             double s = (double)oracle_bf16_to_f32(scales[g * N + n]);
             out[n * K + k] = (double)(q - z) * s;
         }
+}
+
+void oracle_dequant_int8_row(const int8_t *codes, int64_t rows, int64_t K, const float *scales,
+                             double *out)
+{
+    for (int64_t i = 0; i < rows; i++)
+        for (int64_t k = 0; k < K; k++)
+            out[i * K + k] = (double)codes[i * K + k] * (double)scales[i];
 }

@@ -459,6 +459,77 @@ def test_int4_exhaustive_code_roundtrip(orc):
     del rng, zero_col
 
 
+# ------------------------------------------------------------------ INT8 per row
+def test_int8_worked_rows_ties_and_saturation(orc):
+    """Rows chosen so that 127/amax is a power of two: x * r is exact and the
+    expected codes follow from the definition by hand (ties to even)."""
+    row1 = [127.0, 0.5, 1.5, 2.5, -0.5, -1.5, 126.5, -127.0]      # amax 127: r = 1
+    row2 = [254.0, 3.0, 5.0, -7.0, 1.0, -254.0, 0.0, 253.0]       # amax 254: r = 1/2
+    x = bf16_bits(torch.tensor([row1, row2], dtype=torch.bfloat16))
+    codes, s = orc.quant_int8_row(x)
+    assert codes.dtype == np.int8
+    assert codes[0].tolist() == [127, 0, 2, 2, 0, -2, 126, -127]
+    assert codes[1].tolist() == [127, 2, 2, -4, 0, -127, 0, 126]
+    assert s.tolist() == [1.0, 2.0]
+
+
+def test_int8_amax_maps_to_127_and_codes_are_nearest(orc):
+    R, K = 48, 384
+    x = bf16_bits(inputs.outlier_channel_bf16(R, K, 91))
+    xv = vals(x)
+    codes, s = orc.quant_int8_row(x)
+    q = codes.astype(np.float64)
+    a = np.abs(xv).max(1)
+    assert np.all(np.abs(s.astype(np.float64) * 127 - a) <= a * 2.0 ** -22)   # s = amax/127 to binary32
+    for i in range(R):
+        assert np.all(np.abs(q[i][np.abs(xv[i]) == a[i]]) == 127)
+    target = xv * (127.0 / a)[:, None]
+    assert np.all(np.abs(q - target) <= 0.5 + 1e-4) and np.all(np.abs(q) <= 127)
+
+
+def test_int8_zero_row_scaling_and_sign(orc):
+    x = rand_bits((6, 256), 93)
+    x[2] = 0
+    c1, s1 = orc.quant_int8_row(x)
+    assert not c1[2].any() and s1[2] == 1.0
+    x2 = bf16_bits(torch.from_numpy(vals(x) * 2.0).to(torch.bfloat16))
+    c2, s2 = orc.quant_int8_row(x2)
+    keep = np.arange(6) != 2
+    assert np.array_equal(c1, c2) and np.array_equal(s2[keep], 2 * s1[keep])
+    c3, s3 = orc.quant_int8_row(x ^ np.uint16(0x8000))
+    assert np.array_equal(c3, -c1) and np.array_equal(s3, s1)
+
+
+def test_int8_rows_are_independent_and_dequant_close(orc):
+    x = rand_bits((8, 512), 95)
+    c1, s1 = orc.quant_int8_row(x)
+    x2 = x.copy()
+    x2[4] = bf16_bits(inputs.normal_bf16((1, 512), 50.0, 96))[0]
+    c2, s2 = orc.quant_int8_row(x2)
+    keep = np.arange(8) != 4
+    assert np.array_equal(c1[keep], c2[keep]) and np.array_equal(s1[keep], s2[keep]) and s1[4] != s2[4]
+    # rows 10^k apart: a scale applied to the wrong row misses by orders of magnitude
+    xv = vals(x) * (10.0 ** np.arange(8))[:, None]
+    xb = bf16_bits(torch.from_numpy(xv).to(torch.bfloat16))
+    c, sc = orc.quant_int8_row(xb)
+    xh = orc.dequant_int8_row(c, sc)
+    assert np.all(np.abs(xh - vals(xb)) <= sc.astype(np.float64)[:, None] * 0.5 * (1 + 1e-5))
+
+
+def test_int8_gemm_is_scaled_integer_product(orc):
+    """Over INT8 operands the GEMM reference (float64 matmul of dequantized
+    values) equals s_x[m] * s_w[n] times the exact int64 dot product of the codes."""
+    M, N, K = 24, 40, 256
+    cx, sx = orc.quant_int8_row(rand_bits((M, K), 97))
+    cw, sw = orc.quant_int8_row(rand_bits((N, K), 98, 0.02))
+    y = orc.gemm_ref(orc.dequant_int8_row(cx, sx), orc.dequant_int8_row(cw, sw))
+    ss = sx.astype(np.float64)[:, None] * sw.astype(np.float64)[None, :]
+    expect = ss * (cx.astype(np.int64) @ cw.astype(np.int64).T)
+    # each float64 product of two dequantized values rounds once (62 bits)
+    mag = ss * (np.abs(cx.astype(np.int64)) @ np.abs(cw.astype(np.int64)).T)
+    assert np.all(np.abs(y - expect) <= mag * K * 2.0 ** -52)
+
+
 # ------------------------------------------------------------------ GEMM reference
 def test_gemm_ref_exact_rational_tiny(orc):
     rng = np.random.default_rng(1)
