@@ -53,7 +53,8 @@ def parse_args():
     ap.add_argument("--eager", action="store_true", help="launch call by call instead of replaying a CUDA graph")
     ap.add_argument("--only", default=None, help="keep only linears whose name contains this string")
     ap.add_argument("--next", action="store_true",
-                    help="measure the next rows instead (MXFP4 W4A4 on the MXFP8 workload's shapes)")
+                    help="measure the next rows instead (MXFP4 W4A4 on the MXFP8 workload's shapes, FP8 "
+                         "1x128-group and INT8 W8A8 on the DiT MLP shapes)")
     return ap.parse_args()
 
 
@@ -80,7 +81,8 @@ def workload_linears(next_rows: bool = False):
     from serving_amax_reduce_gb300 import inputs as I
     if next_rows:
         return ([("mxfp4", I.mxfp4_linear(K, N)) for (K, N) in I.MXFP8_SHAPES]
-                + [("fp8_group", I.fp8_group_linear(K, N)) for (K, N) in I.FP8_MLP_SHAPES])
+                + [("fp8_group", I.fp8_group_linear(K, N)) for (K, N) in I.FP8_MLP_SHAPES]
+                + [("int8", I.int8_linear(K, N)) for (K, N) in I.FP8_MLP_SHAPES])
     lins = [("fp8_tensor", I.fp8_tensor_linear())]
     for (K, N) in I.W4A16_SHAPES:
         for M in I.W4A16_M:
@@ -99,7 +101,8 @@ def config_block(args):
     if args.next:
         return {"workload": "next-rows",
                 "workloads": ["mxfp4 W4A4 M20280 (K,N){(5120,13824),(13824,5120),(5120,5120)}",
-                              "fp8 1x128-group X x 128x128-block W, M4096 (K,N){(3072,12288),(12288,3072)}"],
+                              "fp8 1x128-group X x 128x128-block W, M4096 (K,N){(3072,12288),(12288,3072)}",
+                              "int8 W8A8 per-token X x per-channel W, M4096 (K,N){(3072,12288),(12288,3072)}"],
                 "step": "per linear: weight quantize + activation quantize + quantized GEMM",
                 "l2": "inputs larger than L2", "parallelism": f"replicas x{args.gpus}"}
     return {
@@ -173,9 +176,9 @@ class Job:
         self.x = lin.make_x(device=dev)
         self.w = lin.make_w(device=dev)
         wf = {"fp8_tensor": F.FP8_TENSOR, "fp8_block128": F.FP8_BLOCK128, "mxfp8": F.MXFP8, "nvfp4": F.NVFP4,
-              "int4_g128": F.INT4_G128_ASYM, "mxfp4": F.MXFP4}[lin.w_fmt]
+              "int4_g128": F.INT4_G128_ASYM, "mxfp4": F.MXFP4, "int8_row": F.INT8_ROW}[lin.w_fmt]
         xf = {"fp8_tensor": F.FP8_TENSOR, "fp8_token": F.FP8_TOKEN, "mxfp8": F.MXFP8, "nvfp4": F.NVFP4,
-              "bf16": F.BF16, "mxfp4": F.MXFP4, "fp8_group128": F.FP8_GROUP128}[lin.x_fmt]
+              "bf16": F.BF16, "mxfp4": F.MXFP4, "fp8_group128": F.FP8_GROUP128, "int8_row": F.INT8_ROW}[lin.x_fmt]
         self.wf, self.xf = wf, xf
         self.layout = L.MMA if wf in (F.MXFP8, F.NVFP4, F.MXFP4) else L.CANONICAL
         self.wb = q.alloc_quant(wf, lin.N, lin.K, self.layout, dev)
@@ -263,16 +266,19 @@ def kernel_name(job, op):
         if job.xf == F.FP8_GROUP128:
             return "gemm_fp8_block_x_group128"
         return {F.FP8_TENSOR: "gemm_fp8_tensor", F.FP8_BLOCK128: "gemm_fp8_block", F.MXFP8: "gemm_mxfp8",
-                F.NVFP4: "gemm_nvfp4", F.INT4_G128_ASYM: "gemm_w4a16", F.MXFP4: "gemm_mxfp4"}[job.wf]
+                F.NVFP4: "gemm_nvfp4", F.INT4_G128_ASYM: "gemm_w4a16", F.MXFP4: "gemm_mxfp4",
+                F.INT8_ROW: "gemm_int8"}[job.wf]
     fmt = job.wf if op == "quant_w" else job.xf
     return "quant_" + {F.FP8_TENSOR: "fp8_tensor", F.FP8_TOKEN: "fp8_token", F.FP8_BLOCK128: "fp8_block128",
                        F.MXFP8: "mxfp8", F.NVFP4: "nvfp4", F.INT4_G128_ASYM: "int4_g128", F.MXFP4: "mxfp4",
-                       F.FP8_GROUP128: "fp8_group128"}[fmt]
+                       F.FP8_GROUP128: "fp8_group128", F.INT8_ROW: "int8_row"}[fmt]
 
 
 def tensor_peak(peaks, wf, q, sustained=True):
     bf16 = peaks.get("bf16_tflops_sustained" if sustained else "bf16_tflops") or (1700.0 if sustained else 1900.0)
-    ratio = FP4_RATIO if wf in (q.Fmt.NVFP4, q.Fmt.MXFP4) else (1.0 if wf == q.Fmt.INT4_G128_ASYM else FP8_RATIO)
+    # W4A16 and INT8 (no integer MMA on sm_103a) run kind::f16, at the bf16 rate
+    ratio = FP4_RATIO if wf in (q.Fmt.NVFP4, q.Fmt.MXFP4) else (
+        1.0 if wf in (q.Fmt.INT4_G128_ASYM, q.Fmt.INT8_ROW) else FP8_RATIO)
     return bf16 * ratio
 
 

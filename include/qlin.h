@@ -45,6 +45,8 @@
  *   INT4: per (n, group of 128 k): range [min(0,min), max(0,max)],
  *     s = bf16((max-min)/15) (1 if 0), z = clamp(rint(-min/s)), q =
  *     clamp(rint(x/s) + z) with 1/s computed once in fp32.
+ *   INT8 (per row): s = amax/127, code = clamp(rint(x * (127/amax)), -127,
+ *     127), s = 1 and multiplier 1 when amax == 0.
  *   Conversions round to nearest even and saturate (satfinite); a zero keeps
  *   its sign.  Every fp32 operation is a single correctly rounded op.
  */
@@ -78,7 +80,14 @@ typedef enum {
      * groups): the block-128 dynamic symmetric FP8 scheme of "[vLLM] 기타
      * 양자화: FP8, ModelOpt, INC, TorchAO, Quark", section "FP8: vLLM의 핵심
      * 양자화", on activations; pairs with FP8_BLOCK128 weights in qlin_gemm.   */
-    QLIN_FP8_GROUP128 = 8
+    QLIN_FP8_GROUP128 = 8,
+    /* int8 codes (two's complement), one fp32 scale per row: per output
+     * channel for a weight, per token for an activation.  The CUDA online
+     * INT8 W8A8 path of "vLLM-Omni 在线量化（Online Quantization）完全指南",
+     * section "在线量化的底层工作原理" (weights and their scales from a scaled
+     * int8 quantizer), with the dynamic activation scheme of section
+     * "核心参数详解"; pairs with itself in qlin_gemm.                           */
+    QLIN_INT8_ROW = 9
 } qlin_format;
 
 typedef enum {
@@ -110,11 +119,11 @@ const char *qlin_status_string(qlin_status s);
  * elements (rows = N for weights, M for activations).  0 means "not used by
  * this format" or invalid arguments.                                        */
 
-/* Codes: FP8 formats rows*K; NVFP4 and MXFP4 rows*K/2 (lower k in the low nibble);
+/* Codes: FP8 formats and INT8_ROW rows*K; NVFP4 and MXFP4 rows*K/2 (lower k in the low nibble);
  * INT4 (K/8)*rows*4 as int32 [K/8, rows], k = 8i+j in bits [4j,4j+4).       */
 size_t qlin_codes_bytes(qlin_format fmt, int64_t rows, int64_t K);
 
-/* Scales: FP8_TENSOR 4 (one float); FP8_TOKEN rows*4; FP8_GROUP128
+/* Scales: FP8_TENSOR 4 (one float); FP8_TOKEN and INT8_ROW rows*4; FP8_GROUP128
  * rows*(K/128)*4, float [rows, K/128] row-major; FP8_BLOCK128
  * (rows/128)*(K/128)*4 row-major; MXFP8 rows*K/32 (canonical) or
  * ceil(rows/128)*128*K/32 (MMA), the same for MXFP4; NVFP4 rows*K/16 or
@@ -179,6 +188,12 @@ qlin_status qlin_quantize_act(qlin_format fmt, const void *x_bf16_dev, int64_t M
  *   NVFP4, NVFP4           : scales in QLIN_SCALE_MMA layout, x_global and
  *                            w_global one float each (K % 256 == 0)
  *   MXFP4, MXFP4           : scales in QLIN_SCALE_MMA layout (K % 256 == 0)
+ *   INT8_ROW, INT8_ROW     : x_scales float [M], w_scales float [N] (K % 16 == 0).
+ *                            sm_103a has no integer tensor-core MMA, so the
+ *                            kernel turns the codes into exact fp16 values on
+ *                            chip and multiplies them with fp32 accumulation:
+ *                            every product is exact, and so is every partial sum
+ *                            below 2^24 in magnitude.
  *   INT4_G128_ASYM, BF16   : x = bf16 activations [M,K] row-major; w_codes
  *                            qweight, w_scales bf16, w_zeros qzeros (K % 128 == 0,
  *                            N % 8 == 0); workspace per qlin_gemm_workspace_bytes

@@ -12,7 +12,8 @@ namespace {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 bool is_quant_format(qlin_format f) {
-    return (f >= QLIN_FP8_TENSOR && f <= QLIN_INT4_G128_ASYM) || f == QLIN_MXFP4 || f == QLIN_FP8_GROUP128;
+    return (f >= QLIN_FP8_TENSOR && f <= QLIN_INT4_G128_ASYM) || f == QLIN_MXFP4 || f == QLIN_FP8_GROUP128 ||
+           f == QLIN_INT8_ROW;
 }
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -27,7 +28,8 @@ qlin_status check_quant_shape(qlin_format fmt, qlin_scale_layout layout, int64_t
         return QLIN_ERR_UNSUPPORTED;
     switch (fmt) {
         case QLIN_FP8_TENSOR:
-        case QLIN_FP8_TOKEN: return QLIN_OK;
+        case QLIN_FP8_TOKEN:
+        case QLIN_INT8_ROW: return QLIN_OK;
         case QLIN_FP8_BLOCK128: return (rows % 128 || K % 128) ? QLIN_ERR_INVALID_ARG : QLIN_OK;
         case QLIN_FP8_GROUP128: return (K % 128) ? QLIN_ERR_INVALID_ARG : QLIN_OK;
         case QLIN_MXFP8:
@@ -52,7 +54,8 @@ qlin_status quantize(qlin_format fmt, const void* src, int64_t rows, int64_t K, 
     if (fmt == QLIN_INT4_G128_ASYM && !zeros) return QLIN_ERR_INVALID_ARG;
     if (fmt == QLIN_NVFP4 && !global) return QLIN_ERR_INVALID_ARG;
     if (!aligned16(src) || (ld * 2) % 16 || !aligned16(codes)) return QLIN_ERR_ALIGNMENT;
-    if (fmt == QLIN_FP8_TOKEN || fmt == QLIN_FP8_BLOCK128 || fmt == QLIN_FP8_TENSOR || fmt == QLIN_FP8_GROUP128) {
+    if (fmt == QLIN_FP8_TOKEN || fmt == QLIN_FP8_BLOCK128 || fmt == QLIN_FP8_TENSOR || fmt == QLIN_FP8_GROUP128 ||
+        fmt == QLIN_INT8_ROW) {
         if (reinterpret_cast<uintptr_t>(scales) & 3u) return QLIN_ERR_ALIGNMENT;
     }
     if (fmt == QLIN_INT4_G128_ASYM &&
@@ -70,6 +73,8 @@ qlin_status quantize(qlin_format fmt, const void* src, int64_t rows, int64_t K, 
                                                    static_cast<float*>(ws), amax_partials(rows, K), st));
         case QLIN_FP8_TOKEN:
             return launch_status(launch_fp8_rowwise(x, rows, K, ld, c, static_cast<float*>(scales), st));
+        case QLIN_INT8_ROW:
+            return launch_status(launch_int8_rowwise(x, rows, K, ld, c, static_cast<float*>(scales), st));
         case QLIN_FP8_BLOCK128:
             return launch_status(launch_fp8_block128(x, rows, K, ld, c, static_cast<float*>(scales), st));
         case QLIN_FP8_GROUP128:
@@ -115,6 +120,7 @@ size_t qlin_codes_bytes(qlin_format fmt, int64_t rows, int64_t K) {
         case QLIN_FP8_TOKEN:
         case QLIN_FP8_BLOCK128:
         case QLIN_FP8_GROUP128:
+        case QLIN_INT8_ROW:
         case QLIN_MXFP8: return (size_t)(rows * K);
         case QLIN_NVFP4:
         case QLIN_MXFP4: return (size_t)(rows * (K / 2));
@@ -128,7 +134,8 @@ size_t qlin_scales_bytes(qlin_format fmt, qlin_scale_layout layout, int64_t rows
     const int64_t rows_pad = ceil_div(rows, 128) * 128;
     switch (fmt) {
         case QLIN_FP8_TENSOR: return 4;
-        case QLIN_FP8_TOKEN: return (size_t)(rows * 4);
+        case QLIN_FP8_TOKEN:
+        case QLIN_INT8_ROW: return (size_t)(rows * 4);
         case QLIN_FP8_BLOCK128: return (size_t)((rows / 128) * (K / 128) * 4);
         case QLIN_FP8_GROUP128: return (size_t)(rows * (K / 128) * 4);
         case QLIN_MXFP8:
@@ -220,6 +227,11 @@ qlin_status qlin_gemm(qlin_format w_fmt, qlin_format x_fmt, int64_t M, int64_t N
         if (K % 256) return QLIN_ERR_INVALID_ARG;
         if (!aligned16(x_scales_dev) || !aligned16(w_scales_dev)) return QLIN_ERR_ALIGNMENT;
         return launch_status(launch_gemm_nvfp4(a, st));
+    }
+    if (w_fmt == QLIN_INT8_ROW && x_fmt == QLIN_INT8_ROW) {
+        if (!x_scales_dev || !w_scales_dev) return QLIN_ERR_INVALID_ARG;
+        if (K % 16) return QLIN_ERR_INVALID_ARG;
+        return launch_status(launch_gemm_int8(a, st));
     }
     if (w_fmt == QLIN_INT4_G128_ASYM && x_fmt == QLIN_BF16) {
         if (!w_scales_dev || !w_zeros_dev) return QLIN_ERR_INVALID_ARG;

@@ -40,6 +40,15 @@
 //                   alpha = g_x * g_w.
 //   MXFP4 (W4A4)    kind::mxf4nvf4.block_scale.scale_vec::2X, UE8M0 scales
 //                   (the online MXFP4 path of the same page).
+//   INT8 (W8A8)     the online INT8 path of the same page, per-token X and
+//                   per-channel W scales.  sm_103a has no integer MMA, so TMA
+//                   stages the int8 tiles (64 K per stage) in a ring of their
+//                   own and warps 12-15 (a fourth warpgroup) turn every code
+//                   into the fp16 value of the same integer (q ^ 0x80 placed
+//                   in the mantissa of 1024, minus 1152: exact) in the
+//                   128-byte-swizzled layout the MMA reads; kind::f16 then
+//                   multiplies exact integers with fp32 accumulation, and the
+//                   epilogue applies s_x[m] * s_w[n].
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -53,7 +62,7 @@ namespace {
 
 using namespace ptx;
 
-enum Kind { kFp8Tensor = 0, kFp8Block = 1, kMxfp8 = 2, kNvfp4 = 3, kMxfp4 = 4 };
+enum Kind { kFp8Tensor = 0, kFp8Block = 1, kMxfp8 = 2, kNvfp4 = 3, kMxfp4 = 4, kInt8 = 5 };
 
 constexpr int BM = 128;              // tile rows (X rows) = MMA M
 constexpr int BKB = 128;             // K bytes per stage: 128 fp8 or 256 fp4 (one swizzle row)
@@ -61,16 +70,27 @@ constexpr uint64_t kWaitLimitNs = 1000000000ull;   // bounded waits give up afte
 
 template <int KIND>
 struct Cfg {
+    // INT8: operands are converted on chip from an int8 staging ring
+    static constexpr bool CVT = (KIND == kInt8);
     static constexpr int BN = 256;
-    static constexpr int STAGES = 4;
+    static constexpr int STAGES = CVT ? 2 : 4;       // operand stages (converted fp16 for INT8)
+    static constexpr int S8 = CVT ? 4 : 0;           // int8 staging stages
     static constexpr int EPI_WARPS = 8;              // two per TMEM lane quadrant, 128 columns each
-    static constexpr int THREADS = 384;               // warpgroup 0: TMA + MMA; warpgroups 1-2: epilogue
-    // setmaxnreg split: 128 x 40 + 256 x 232 = 64512 = 384 threads x 168
-    // registers, the launch allocation (checked on the host before launch).
-    static constexpr int REGS_LAUNCH = 168, REGS_CTRL = 40, REGS_EPI = 232;
-    static_assert(128 * REGS_CTRL + 256 * REGS_EPI <= THREADS * REGS_LAUNCH, "register split");
+    static constexpr int CVT_WARPS = CVT ? 4 : 0;    // warpgroup 3 (INT8 only): int8 -> fp16
+    // warpgroup 0: TMA + MMA; warpgroups 1-2: epilogue; warpgroup 3: converters
+    static constexpr int THREADS = 384 + 32 * CVT_WARPS;
+    // setmaxnreg split, within the launch allocation (checked on the host
+    // before launch): 128 x 40 + 256 x 232 = 64512 <= 384 x 168, and for INT8
+    // 128 x 40 + 256 x 184 + 128 x 104 = 65536 = 512 x 128.
+    static constexpr int REGS_LAUNCH = CVT ? 128 : 168, REGS_CTRL = 40, REGS_EPI = CVT ? 184 : 232;
+    static constexpr int REGS_CVT = 104;
+    static_assert(128 * REGS_CTRL + 256 * REGS_EPI + 32 * CVT_WARPS * REGS_CVT <= THREADS * REGS_LAUNCH,
+                  "register split");
     static constexpr int A_BYTES = BM * BKB;
     static constexpr int B_BYTES = BN * BKB;
+    static constexpr int K8 = 64;                    // INT8: K per stage (64 fp16 = one 128-byte row)
+    static constexpr int A8_BYTES = CVT ? BM * K8 : 0;
+    static constexpr int B8_BYTES = CVT ? BN * K8 : 0;
     // 512-byte scale chunks (128 rows x 4 scales) per 128 rows per stage
     static constexpr int SF_CHUNKS = (KIND == kMxfp8) ? 1 : (KIND == kNvfp4 ? 4 : (KIND == kMxfp4 ? 2 : 0));
     // NVFP4 has 12 scale-chunk copies per stage: two threads issue them off the
@@ -86,10 +106,12 @@ struct Cfg {
     static constexpr int STG_BOX = 32 * 16 * 2;      // one 32 x 16 bf16 output box
     static constexpr int STG_BUFS = (KIND == kNvfp4) ? 1 : 2;   // staging boxes per epilogue warp
     static constexpr int STG_BYTES = STG_BOX * STG_BUFS;
-    static constexpr int OFF_STG = OFF_SFB + STAGES * SFB_BYTES;
+    static constexpr int OFF_A8 = OFF_SFB + STAGES * SFB_BYTES;
+    static constexpr int OFF_B8 = OFF_A8 + S8 * A8_BYTES;
+    static constexpr int OFF_STG = OFF_B8 + S8 * B8_BYTES;
     static constexpr int OFF_BAR = OFF_STG + EPI_WARPS * STG_BYTES;
-    // full[S], empty[S], accf, acce, pfull[2], pempty[2], drain, sfready[S]
-    static constexpr int NBAR = 3 * STAGES + 7;
+    // full[S], empty[S], accf, acce, pfull[2], pempty[2], drain, sfready[S], s8full[S8], s8empty[S8]
+    static constexpr int NBAR = 3 * STAGES + 7 + 2 * S8;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int SMEM = OFF_MISC + 64 + 1024; // + slack for 1024-byte alignment
     static constexpr uint32_t TMEM_COLS = 512;
@@ -108,6 +130,8 @@ __host__ __device__ constexpr uint32_t idesc_for() {
     constexpr uint32_t m = (uint32_t)(BM >> 4) << 24;
     if (KIND == kFp8Tensor || KIND == kFp8Block)
         return (1u << 4) /* D f32 */ | (0u << 7) /* A e4m3 */ | (0u << 10) /* B e4m3 */ | n | m;
+    if (KIND == kInt8)   // kind::f16
+        return (1u << 4) /* D f32 */ | (0u << 7) /* A f16 */ | (0u << 10) /* B f16 */ | n | m;
     if (KIND == kMxfp8)
         return (0u << 7) | (0u << 10) | n | (1u << 23) /* UE8M0 scales */ | m;
     if (KIND == kMxfp4)
@@ -156,6 +180,19 @@ __device__ __forceinline__ bool warp_wait_or_abort(uint64_t* bar, uint32_t parit
     bool ok = true;
     if ((threadIdx.x & 31) == 0) ok = wait_or_abort(bar, parity, abort_flag);
     return __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
+}
+
+// Four int8 codes (one word, lowest k in the low byte) -> the fp16 values of
+// the same four integers as two f16x2 words (lower k in the low half).
+// q ^ 0x80 = q + 128 in [0, 255]; as the low mantissa byte under 0x64 it
+// reads as the fp16 value 1024 + q + 128, and subtracting 1152 (0x6480)
+// leaves q exactly (every integer of magnitude below 2048 is an fp16 value).
+__device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    const uint32_t u = w ^ 0x80808080u;
+    const uint32_t a = prmt(u, 0x64646464u, 0x5140u);   // bytes u0, 0x64, u1, 0x64
+    const uint32_t b = prmt(u, 0x64646464u, 0x5342u);   // bytes u2, 0x64, u3, 0x64
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(a), "r"(0x64806480u));
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(0x64806480u));
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
@@ -232,6 +269,8 @@ __global__ void __launch_bounds__(Cfg<KIND>::THREADS, 1)
     uint64_t* pempty = pfull + 2;           // FP8 block: partial buffer b drained
     uint64_t* drain = pempty + 2;
     uint64_t* sfready = drain + 1;          // MX / NVFP4: stage s's scale factors are in TMEM
+    uint64_t* s8full = sfready + C::STAGES; // INT8: int8 staging slot landed (TMA)
+    uint64_t* s8empty = s8full + C::S8;     // INT8: int8 staging slot read by the converters
     uint32_t* misc = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);   // tmem base, abort, consumed, issued
     volatile uint32_t* abort_flag = misc + 1;
 
@@ -241,8 +280,12 @@ __global__ void __launch_bounds__(Cfg<KIND>::THREADS, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; s++) {
-            mbar_init(full + s, 1);
+            mbar_init(full + s, C::CVT ? C::CVT_WARPS : 1);   // TMA, or the converter warps
             mbar_init(empty + s, 1);
+        }
+        for (int s = 0; s < C::S8; s++) {
+            mbar_init(s8full + s, 1);
+            mbar_init(s8empty + s, C::CVT_WARPS);
         }
         mbar_init(accf, 1);
         mbar_init(acce, C::EPI_WARPS);
@@ -271,7 +314,29 @@ __global__ void __launch_bounds__(Cfg<KIND>::THREADS, 1)
     // epilogue warpgroups, which hold a 128-column fp32 tile row each.
     if (warp < 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::REGS_CTRL));
-    if (!skip && warp == 0 && lane == 0) {
+    if (C::CVT && !skip && warp == 0 && lane == 0) {
+        // ------------------------------------------------ TMA producer (INT8 staging ring)
+        if constexpr (C::CVT) {
+        uint32_t kg = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+            int m0, n0;
+            tile_coords<C::BN>(tile, tiles_m, tiles_n, m0, n0);
+            for (int kb = 0; kb < p.nk; kb++, kg++) {
+                const int j = (int)(kg % C::S8);
+                if (!wait_or_abort(s8empty + j, ((kg / C::S8) & 1u) ^ 1u, abort_flag)) {
+                    record_timeout(p.status, abort_flag);
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(s8full + j, C::A8_BYTES + C::B8_BYTES);
+                tma_load_2d(smem + C::OFF_A8 + j * C::A8_BYTES, &tmA, kb * C::K8, m0, s8full + j);
+                tma_load_2d(smem + C::OFF_B8 + j * C::B8_BYTES, &tmB, kb * C::K8, n0, s8full + j);
+                misc[3] = kg + 1;
+            }
+        }
+        }
+    } else if (!C::CVT && !skip && warp == 0 && lane == 0) {
         // ------------------------------------------------ TMA producer
         uint32_t kg = 0;
         const int ntiles_b = (p.N + 127) / 128;
@@ -365,6 +430,8 @@ __global__ void __launch_bounds__(Cfg<KIND>::THREADS, 1)
                     const uint32_t acc = (KIND == kFp8Block) ? (c > 0) : (kb > 0 || c > 0);
                     if (KIND == kFp8Tensor || KIND == kFp8Block) {
                         mma_f8f6f4(d, ad, bd, idesc, acc);
+                    } else if (KIND == kInt8) {
+                        mma_f16(d, ad, bd, idesc, acc);
                     } else if (KIND == kMxfp8) {
                         const uint32_t id = idesc | ((uint32_t)c << 4) | ((uint32_t)c << 29);
                         mma_mxf8(d, ad, bd, id, tmem + C::SFA_COL + s * C::SFA_COLS,
@@ -424,7 +491,7 @@ __global__ void __launch_bounds__(Cfg<KIND>::THREADS, 1)
             }
         }
     }
-    } else {
+    } else if (warp < 12) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::REGS_EPI));
     if (!skip) {
         // ------------------------------------------------ epilogue (8 warps)
@@ -456,12 +523,21 @@ __global__ void __launch_bounds__(Cfg<KIND>::THREADS, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(acce);     // the MMA may start the next tile
                 uint8_t* stg = smem + C::OFF_STG + (warp - 4) * C::STG_BYTES;
+                // INT8: s_x of this thread's row, s_w per column (one uniform load each)
+                const float sxr = (KIND == kInt8) ? (row < p.M ? __ldg(p.x_scale + row) : 0.0f) : alpha;
 #pragma unroll
                 for (int c = 0; c < 4; c++) {
                     if (ncol + c * 32 < p.N) {
                         float v[32];
 #pragma unroll
-                        for (int i = 0; i < 32; i++) v[i] = __uint_as_float(r[c][i]) * alpha;
+                        for (int i = 0; i < 32; i++) v[i] = __uint_as_float(r[c][i]) * sxr;
+                        if (KIND == kInt8) {
+#pragma unroll
+                            for (int i = 0; i < 32; i++) {
+                                const int col = ncol + c * 32 + i;
+                                v[i] *= col < p.N ? __ldg(p.w_scale + col) : 0.0f;
+                            }
+                        }
                         store_block32<C::STG_BUFS>(p, &tmY, stg, m0 + q * 32, ncol + c * 32, v);
                     }
                 }
@@ -531,6 +607,59 @@ __global__ void __launch_bounds__(Cfg<KIND>::THREADS, 1)
     }
 
     if (lane == 0) bulk_wait_all();              // this warp's output stores have completed
+    } else {
+        if constexpr (C::CVT) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::REGS_CVT));
+        if (!skip) {
+            // ------------------------------------------------ int8 -> fp16 converters (4 warps)
+            // A stage holds 384 rows (128 of X, 256 of W) of 64 int8 = 4 chunks
+            // of 16 codes; thread ct takes chunks ct, ct + 128, ... (8 rows per
+            // warp per round: 128 contiguous staging bytes per quarter warp).
+            // Chunk c of row r becomes 16-byte fp16 chunks 2c and 2c + 1 of the
+            // row's 128 bytes, stored at chunk position (2c [+1]) ^ (r & 7):
+            // the 128-byte swizzle the MMA descriptors expect (8-row atoms).
+            const int ct = (warp - 12) * 32 + lane;
+            uint32_t kg = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+                for (int kb = 0; kb < p.nk; kb++, kg++) {
+                    const int j = (int)(kg % C::S8), s = (int)(kg % C::STAGES);
+                    if (!warp_wait_or_abort(s8full + j, (kg / C::S8) & 1u, abort_flag) ||
+                        !warp_wait_or_abort(empty + s, ((kg / C::STAGES) & 1u) ^ 1u, abort_flag)) {
+                        if (lane == 0) record_timeout(p.status, abort_flag);
+                        ok = false;
+                        break;
+                    }
+                    const uint8_t* a8 = smem + C::OFF_A8 + j * C::A8_BYTES;
+                    const uint8_t* b8 = smem + C::OFF_B8 + j * C::B8_BYTES;
+                    uint8_t* a16 = smem + C::OFF_A + s * C::A_BYTES;
+                    uint8_t* b16 = smem + C::OFF_B + s * C::B_BYTES;
+#pragma unroll 4
+                    for (int i = 0; i < (BM + C::BN) * 4 / 128; i++) {
+                        const int id = i * 128 + ct, r = id >> 2, c = id & 3;
+                        const bool isa = r < BM;          // uniform per i
+                        const int rr = isa ? r : r - BM;
+                        const uint4 qv = *reinterpret_cast<const uint4*>((isa ? a8 : b8) + rr * C::K8 + c * 16);
+                        uint4 h0, h1;
+                        i8x4_to_f16x4(qv.x, h0.x, h0.y);
+                        i8x4_to_f16x4(qv.y, h0.z, h0.w);
+                        i8x4_to_f16x4(qv.z, h1.x, h1.y);
+                        i8x4_to_f16x4(qv.w, h1.z, h1.w);
+                        uint8_t* row = (isa ? a16 : b16) + rr * 128;
+                        const int sw = rr & 7;
+                        *reinterpret_cast<uint4*>(row + (((2 * c) ^ sw) << 4)) = h0;
+                        *reinterpret_cast<uint4*>(row + (((2 * c + 1) ^ sw) << 4)) = h1;
+                    }
+                    fence_proxy_async_smem();         // generic-proxy writes -> the MMA's async proxy
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(s8empty + j);
+                        mbar_arrive(full + s);
+                    }
+                }
+            }
+        }
+        }
     }
 
     // ---------------------------------------------------- teardown
@@ -539,9 +668,16 @@ __global__ void __launch_bounds__(Cfg<KIND>::THREADS, 1)
     if (*abort_flag && warp == 0 && lane == 0) {
         // Let every TMA copy this CTA issued land before its shared memory is
         // released: wait (bounded) on the stages issued but not consumed.
-        const uint32_t issued = misc[3], consumed = misc[2];
-        for (uint32_t kg = consumed; kg < issued; kg++)
-            mbar_wait(full + (kg % C::STAGES), (kg / C::STAGES) & 1u, kWaitLimitNs);
+        const uint32_t issued = misc[3];
+        if constexpr (C::CVT) {
+            // at most the last S8 staging loads can still be in flight; a
+            // load whose phase already completed passes at once
+            for (uint32_t kg = issued > (uint32_t)C::S8 ? issued - C::S8 : 0u; kg < issued; kg++)
+                mbar_wait(s8full + (kg % C::S8), (kg / C::S8) & 1u, kWaitLimitNs);
+        } else {
+            for (uint32_t kg = misc[2]; kg < issued; kg++)
+                mbar_wait(full + (kg % C::STAGES), (kg / C::STAGES) & 1u, kWaitLimitNs);
+        }
     }
     if (*abort_flag && lane == 0 && (warp == 1 || (C::SPLIT_CP && (warp == 2 || warp == 3)))) {
         // ... and every MMA / scale copy issued has finished reading shared
@@ -584,19 +720,20 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// Byte matrix [rows, inner_bytes] with row pitch `pitch` bytes, 128-byte
-// swizzled box of box_rows x 128 bytes, zero fill outside the matrix.
+// Byte matrix [rows, inner_bytes] with row pitch `pitch` bytes, box of
+// box_rows x box_inner bytes (128-byte swizzle for the MMA operand tiles, none
+// for the INT8 staging tiles), zero fill outside the matrix.
 bool make_tmap_u8(CUtensorMap* m, const void* base, uint64_t inner_bytes, uint64_t rows, uint64_t pitch,
-                  uint32_t box_rows) {
+                  uint32_t box_rows, uint32_t box_inner = BKB, bool swizzle = true) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[2] = {inner_bytes, rows};
     cuuint64_t strides[1] = {pitch};
-    cuuint32_t box[2] = {(cuuint32_t)BKB, box_rows};
+    cuuint32_t box[2] = {box_inner, box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
@@ -605,8 +742,14 @@ cudaError_t launch_tc(const GemmArgs& a, cudaStream_t st) {
     using C = Cfg<KIND>;
     const uint64_t kbytes = (KIND == kNvfp4 || KIND == kMxfp4) ? (uint64_t)a.K / 2 : (uint64_t)a.K;
     CUtensorMap tmA, tmB;
-    if (!make_tmap_u8(&tmA, a.x, kbytes, (uint64_t)a.M, kbytes, BM)) return cudaErrorInvalidValue;
-    if (!make_tmap_u8(&tmB, a.w, kbytes, (uint64_t)a.N, kbytes, C::BN)) return cudaErrorInvalidValue;
+    if (C::CVT) {
+        if (!make_tmap_u8(&tmA, a.x, kbytes, (uint64_t)a.M, kbytes, BM, C::K8, false) ||
+            !make_tmap_u8(&tmB, a.w, kbytes, (uint64_t)a.N, kbytes, C::BN, C::K8, false))
+            return cudaErrorInvalidValue;
+    } else {
+        if (!make_tmap_u8(&tmA, a.x, kbytes, (uint64_t)a.M, kbytes, BM)) return cudaErrorInvalidValue;
+        if (!make_tmap_u8(&tmB, a.w, kbytes, (uint64_t)a.N, kbytes, C::BN)) return cudaErrorInvalidValue;
+    }
     CUtensorMap tmY;
     {
         auto fn = encode_fn();
@@ -623,7 +766,7 @@ cudaError_t launch_tc(const GemmArgs& a, cudaStream_t st) {
     p.M = (int)a.M;
     p.N = (int)a.N;
     p.K = (int)a.K;
-    p.nk = (int)((kbytes + BKB - 1) / BKB);
+    p.nk = C::CVT ? (int)((a.K + C::K8 - 1) / C::K8) : (int)((kbytes + BKB - 1) / BKB);
     p.ldy = a.ldy;
     p.x_scale = static_cast<const float*>(a.x_scales);
     p.w_scale = static_cast<const float*>(a.w_scales);
@@ -675,6 +818,7 @@ cudaError_t launch_gemm_fp8_block(const GemmArgs& a, cudaStream_t st) { return l
 cudaError_t launch_gemm_mxfp8(const GemmArgs& a, cudaStream_t st) { return launch_tc<kMxfp8>(a, st); }
 cudaError_t launch_gemm_nvfp4(const GemmArgs& a, cudaStream_t st) { return launch_tc<kNvfp4>(a, st); }
 cudaError_t launch_gemm_mxfp4(const GemmArgs& a, cudaStream_t st) { return launch_tc<kMxfp4>(a, st); }
+cudaError_t launch_gemm_int8(const GemmArgs& a, cudaStream_t st) { return launch_tc<kInt8>(a, st); }
 
 cudaError_t launch_debug_expire_wait(int* dev_status, uint32_t max_polls, cudaStream_t st) {
     k_expire_wait<<<1, 32, 0, st>>>(dev_status, max_polls);

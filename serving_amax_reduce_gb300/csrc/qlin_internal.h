@@ -13,6 +13,8 @@ constexpr int kNumSMs = 152;   // GB300: grids are sized in multiples of this
 // All take the bf16 source [rows, K] with leading dimension ld (elements).
 cudaError_t launch_fp8_rowwise(const uint16_t* x, int64_t rows, int64_t K, int64_t ld,
                                uint8_t* codes, float* scales, cudaStream_t st);
+cudaError_t launch_int8_rowwise(const uint16_t* x, int64_t rows, int64_t K, int64_t ld,
+                                uint8_t* codes, float* scales, cudaStream_t st);
 cudaError_t launch_fp8_tensor(const uint16_t* x, int64_t rows, int64_t K, int64_t ld,
                               uint8_t* codes, float* scale, float* partials, int nparts,
                               cudaStream_t st);
@@ -56,6 +58,7 @@ cudaError_t launch_gemm_fp8_block(const GemmArgs& a, cudaStream_t st);
 cudaError_t launch_gemm_mxfp8(const GemmArgs& a, cudaStream_t st);
 cudaError_t launch_gemm_nvfp4(const GemmArgs& a, cudaStream_t st);
 cudaError_t launch_gemm_mxfp4(const GemmArgs& a, cudaStream_t st);
+cudaError_t launch_gemm_int8(const GemmArgs& a, cudaStream_t st);
 cudaError_t launch_gemm_w4a16(const GemmArgs& a, cudaStream_t st);
 size_t w4a16_workspace_bytes(int64_t M, int64_t N, int64_t K);
 

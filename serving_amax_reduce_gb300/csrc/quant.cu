@@ -1,5 +1,5 @@
 // Online quantizers: bf16 -> FP8 E4M3 (tensor / token / 1x128 group /
-// 128x128 block), MXFP8, MXFP4, NVFP4 and int4 g128.  Each reads its bf16 input once from HBM in
+// 128x128 block), MXFP8, MXFP4, NVFP4, int4 g128 and INT8 per row.  Each reads its bf16 input once from HBM in
 // 16-byte vectors, reduces amax (or min/max) with warp shuffles, and writes
 // codes and scales in the same pass.  The per-tensor formats need the tensor
 // amax before any code exists, so they add one read-only amax pass.
@@ -10,7 +10,10 @@
 // "在线量化的底层工作原理" stage 2 (E4M3 + float8_e8m0fnu per 32 along K);
 // "vLLM-Omni 量化推理实践" Table 1 (NVFP4 in the mixed FP8/NVFP4 model);
 // "vLLM-Omni는 AutoRound 양자화로 추론을 가속화합니다" section "새로운 모델
-// 양자화" (int4, group_size 128, auto_round:auto_gptq packing, --iters 0).
+// 양자화" (int4, group_size 128, auto_round:auto_gptq packing, --iters 0);
+// "vLLM-Omni 在线量化（Online Quantization）完全指南" sections "在线量化的底层
+// 工作原理" and "核心参数详解" (INT8 W8A8: per-channel weight scales, dynamic
+// per-token activation scales).
 //
 // Bit-exactness: every fp32 step is one explicitly rounded intrinsic
 // (__fmul_rn, __fdiv_rn, __fsub_rn), this file is compiled with
@@ -112,6 +115,44 @@ __device__ __forceinline__ void fp8_params(float amax, float& s, float& r) {
     r = __fdiv_rn(kE4M3Max, amax);
 }
 
+// INT8 granule: s = amax/127 and encode multiplier 127/amax (1, 1 for amax 0).
+__device__ __forceinline__ void int8_params(float amax, float& s, float& r) {
+    if (amax == 0.0f) { s = 1.0f; r = 1.0f; return; }
+    s = __fdiv_rn(amax, 127.0f);
+    r = __fdiv_rn(127.0f, amax);
+}
+
+// v * r -> int8 code clamp(rint(v * r), -127, 127) in the low byte.  |v * r|
+// <= 127 (up to one rounding), so adding 1.5 * 2^23 lands in [2^23, 2^24),
+// where the fp32 spacing is 1: the add rounds the product to an integer,
+// ties to even, and the bits minus those of 1.5 * 2^23 are that integer.
+__device__ __forceinline__ uint32_t int8_code(float v, float r) {
+    const int t = (int)__float_as_uint(__fadd_rn(__fmul_rn(v, r), 12582912.0f)) - 0x4B400000;
+    return (uint32_t)min(max(t, -127), 127) & 0xFFu;
+}
+
+// 8 bf16 (one 16-byte vector) times r -> 8 int8 codes.
+__device__ __forceinline__ uint2 enc8_int8(const uint4& v, float r) {
+    const uint32_t w0 = int8_code(bf16_lo(v.x), r) | (int8_code(bf16_hi(v.x), r) << 8) |
+                        (int8_code(bf16_lo(v.y), r) << 16) | (int8_code(bf16_hi(v.y), r) << 24);
+    const uint32_t w1 = int8_code(bf16_lo(v.z), r) | (int8_code(bf16_hi(v.z), r) << 8) |
+                        (int8_code(bf16_lo(v.w), r) << 16) | (int8_code(bf16_hi(v.w), r) << 24);
+    return make_uint2(w0, w1);
+}
+
+// One row granule, FP8 (s = amax/448, E4M3 codes) or INT8 (s = amax/127).
+template <bool INT8>
+__device__ __forceinline__ void row_params(float amax, float& s, float& r) {
+    if constexpr (INT8) int8_params(amax, s, r);
+    else fp8_params(amax, s, r);
+}
+
+template <bool INT8>
+__device__ __forceinline__ uint2 enc8_row(const uint4& v, float r) {
+    if constexpr (INT8) return enc8_int8(v, r);
+    else return enc8_e4m3(v, r);
+}
+
 // Byte offset of scale (row, j) in the tensor-core tiling (see qlin.h):
 // 512-byte chunks of 128 rows x 4 scales, ordered [row_tile][chunk].
 __device__ __forceinline__ int64_t mma_scale_offset(int64_t row, int64_t j, int64_t chunks_per_row) {
@@ -145,10 +186,11 @@ __device__ __forceinline__ TaskPos task_pos(uint32_t t, uint32_t total, uint32_t
 
 // ---------------------------------------------------------------- per row
 // One CTA per row; each thread keeps VPT 16-byte vectors in registers so the
-// row is read from HBM once.
-template <int T, int VPT>
-__global__ void __launch_bounds__(T) k_fp8_rows(const uint16_t* __restrict__ x, int64_t K, int64_t ld,
-                                                uint8_t* __restrict__ codes, float* __restrict__ scales) {
+// row is read from HBM once.  FP8 per-token and INT8 per-row (a token of X or
+// an output channel of W) share this body and differ in the granule rule.
+template <int T, int VPT, bool INT8>
+__device__ __forceinline__ void rows_body(const uint16_t* __restrict__ x, int64_t K, int64_t ld,
+                                          uint8_t* __restrict__ codes, float* __restrict__ scales) {
     __shared__ float red[33];
     const int64_t row = blockIdx.x;
     const uint16_t* src = x + row * ld;
@@ -165,19 +207,32 @@ __global__ void __launch_bounds__(T) k_fp8_rows(const uint16_t* __restrict__ x, 
     }
     amax = block_max<T>(amax, red);
     float s, r;
-    fp8_params(amax, s, r);
+    row_params<INT8>(amax, s, r);
     uint2* dst = reinterpret_cast<uint2*>(codes + row * K);
 #pragma unroll
     for (int i = 0; i < VPT; i++) {
         const int j = threadIdx.x + i * T;
-        if (j < nv) dst[j] = enc8_e4m3(v[i], r);
+        if (j < nv) dst[j] = enc8_row<INT8>(v[i], r);
     }
     if (threadIdx.x == 0) scales[row] = s;
 }
 
+template <int T, int VPT>
+__global__ void __launch_bounds__(T) k_fp8_rows(const uint16_t* __restrict__ x, int64_t K, int64_t ld,
+                                                uint8_t* __restrict__ codes, float* __restrict__ scales) {
+    rows_body<T, VPT, false>(x, K, ld, codes, scales);
+}
+
+template <int T, int VPT>
+__global__ void __launch_bounds__(T) k_int8_rows(const uint16_t* __restrict__ x, int64_t K, int64_t ld,
+                                                 uint8_t* __restrict__ codes, float* __restrict__ scales) {
+    rows_body<T, VPT, true>(x, K, ld, codes, scales);
+}
+
 // Rows too long for registers: amax pass then encode pass (second read hits L2).
-__global__ void __launch_bounds__(256) k_fp8_rows_long(const uint16_t* __restrict__ x, int64_t K, int64_t ld,
-                                                       uint8_t* __restrict__ codes, float* __restrict__ scales) {
+template <bool INT8>
+__device__ __forceinline__ void rows_long_body(const uint16_t* __restrict__ x, int64_t K, int64_t ld,
+                                               uint8_t* __restrict__ codes, float* __restrict__ scales) {
     __shared__ float red[33];
     const int64_t row = blockIdx.x;
     const uint16_t* src = x + row * ld;
@@ -186,10 +241,20 @@ __global__ void __launch_bounds__(256) k_fp8_rows_long(const uint16_t* __restric
     for (int64_t j = threadIdx.x; j < nv; j += 256) amax = fmaxf(amax, absmax8(ld16(src + 8 * j)));
     amax = block_max<256>(amax, red);
     float s, r;
-    fp8_params(amax, s, r);
+    row_params<INT8>(amax, s, r);
     uint2* dst = reinterpret_cast<uint2*>(codes + row * K);
-    for (int64_t j = threadIdx.x; j < nv; j += 256) dst[j] = enc8_e4m3(ld16(src + 8 * j), r);
+    for (int64_t j = threadIdx.x; j < nv; j += 256) dst[j] = enc8_row<INT8>(ld16(src + 8 * j), r);
     if (threadIdx.x == 0) scales[row] = s;
+}
+
+__global__ void __launch_bounds__(256) k_fp8_rows_long(const uint16_t* __restrict__ x, int64_t K, int64_t ld,
+                                                       uint8_t* __restrict__ codes, float* __restrict__ scales) {
+    rows_long_body<false>(x, K, ld, codes, scales);
+}
+
+__global__ void __launch_bounds__(256) k_int8_rows_long(const uint16_t* __restrict__ x, int64_t K, int64_t ld,
+                                                        uint8_t* __restrict__ codes, float* __restrict__ scales) {
+    rows_long_body<true>(x, K, ld, codes, scales);
 }
 
 // ---------------------------------------------------------------- per tensor
@@ -254,7 +319,7 @@ __global__ void __launch_bounds__(256) k_fp8_tensor_encode(const uint16_t* __res
 __global__ void __launch_bounds__(256) k_fp8_block128(const uint16_t* __restrict__ x, int64_t K, int64_t ld,
                                                       uint8_t* __restrict__ codes, float* __restrict__ scales) {
     __shared__ float red[33];
-    const int64_t bi = blockIdx.y, bj = blockIdx.x;
+    const int64_t kt = K >> 7, bi = (int64_t)blockIdx.x / kt, bj = (int64_t)blockIdx.x - bi * kt;
     const int r0 = threadIdx.x >> 4, cv = threadIdx.x & 15;
     const uint16_t* src = x + (bi * 128 + r0) * ld + bj * 128 + cv * 8;
     uint4 v[8];
@@ -420,27 +485,32 @@ __global__ void __launch_bounds__(256) k_nvfp4_encode(const uint16_t* __restrict
 __global__ void __launch_bounds__(128) k_int4_g128(const uint16_t* __restrict__ w, int64_t N, int64_t K,
                                                    int64_t ld, int32_t* __restrict__ qweight,
                                                    uint16_t* __restrict__ scales, int32_t* __restrict__ qzeros) {
-    const int64_t g = blockIdx.y, k0 = g * 128;
-    const int64_t n = (int64_t)blockIdx.x * 128 + threadIdx.x;
+    const int64_t nb = (N + 127) >> 7, g = (int64_t)blockIdx.x / nb, k0 = g * 128;
+    const int64_t n = ((int64_t)blockIdx.x - g * nb) * 128 + threadIdx.x;
     const int lane = threadIdx.x & 31;
     const bool valid = n < N;
     uint4 v[16];
 #pragma unroll
     for (int o = 0; o < 16; o++) v[o] = valid ? ld16(w + n * ld + k0 + 8 * o) : make_uint4(0, 0, 0, 0);
-    // four independent min/max chains (short dependency chains), then combined
-    float mnv[4] = {0.0f, 0.0f, 0.0f, 0.0f}, mxv[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    // min and max on bf16 pairs (exact), four independent chains of each,
+    // then combined
+    __nv_bfloat162 mn2[4], mx2[4];
+#pragma unroll
+    for (int i = 0; i < 4; i++) { mn2[i] = __floats2bfloat162_rn(0.0f, 0.0f); mx2[i] = mn2[i]; }
 #pragma unroll
     for (int o = 0; o < 16; o++) {
         const uint32_t u[4] = {v[o].x, v[o].y, v[o].z, v[o].w};
 #pragma unroll
         for (int i = 0; i < 4; i++) {
-            const float a = bf16_lo(u[i]), b = bf16_hi(u[i]);
-            mnv[i] = fminf(mnv[i], fminf(a, b));
-            mxv[i] = fmaxf(mxv[i], fmaxf(a, b));
+            const __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162*>(&u[i]);
+            mn2[i] = __hmin2(mn2[i], h);
+            mx2[i] = __hmax2(mx2[i], h);
         }
     }
-    const float mn = fminf(fminf(mnv[0], mnv[1]), fminf(mnv[2], mnv[3]));
-    const float mx = fmaxf(fmaxf(mxv[0], mxv[1]), fmaxf(mxv[2], mxv[3]));
+    const __nv_bfloat162 m0 = __hmin2(__hmin2(mn2[0], mn2[1]), __hmin2(mn2[2], mn2[3]));
+    const __nv_bfloat162 m1 = __hmax2(__hmax2(mx2[0], mx2[1]), __hmax2(mx2[2], mx2[3]));
+    const float mn = fminf(__low2float(m0), __high2float(m0));
+    const float mx = fmaxf(__low2float(m1), __high2float(m1));
     const __nv_bfloat16 sb = __float2bfloat16_rn(__fdiv_rn(__fsub_rn(mx, mn), 15.0f));
     float s = __bfloat162float(sb);
     uint16_t sbits = __bfloat16_as_ushort(sb);
@@ -474,34 +544,77 @@ __global__ void __launch_bounds__(128) k_int4_g128(const uint16_t* __restrict__ 
     if (valid && (lane & 7) == 0) qzeros[g * (N / 8) + n / 8] = (int32_t)zw;
 }
 
-int grid_for(int64_t work, int per_block) {
-    int64_t b = (work + per_block - 1) / per_block;
-    if (b > (int64_t)kNumSMs * 8) b = (int64_t)kNumSMs * 8;
-    return (int)(b < 1 ? 1 : b);
+int sm_count() {
+    static int n = 0;
+    if (!n) {
+        int dev = 0, v = 0;
+        if (cudaGetDevice(&dev) == cudaSuccess &&
+            cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
+            n = v;
+        else
+            n = kNumSMs;
+    }
+    return n;
 }
 
+// Grids of a task walk (8 warps per CTA, kUnroll tasks per warp per round).
+// Kernels without a per-CTA prologue launch one round per CTA: the block
+// scheduler refills an SM as its CTAs retire, so new loads start while older
+// CTAs encode and store.  The two encode passes that begin by folding the
+// partial maxima (and, for NVFP4, tabulating 256 divisions) stay persistent
+// with 8 CTAs per SM, so that prologue runs once per resident CTA.
 // Tasks of one tensor, or -1 when their count does not fit the 32-bit walk.
 int64_t task_count(int64_t rows, int64_t K) {
     const int64_t t = rows * (((K >> 3) + 31) / 32);
     return t > 0x7FFFFFFFll ? -1 : t;
 }
 
-int task_grid(int64_t tasks) { return grid_for(tasks, 8 * kUnroll); }
+int64_t task_rounds(int64_t tasks) { return (tasks + 8 * kUnroll - 1) / (8 * kUnroll); }
 
-template <int T>
+int task_grid_once(int64_t tasks) {
+    const int64_t b = task_rounds(tasks);
+    return (int)(b < 1 ? 1 : b);
+}
+
+int task_grid_persistent(int64_t tasks) {
+    int64_t b = task_rounds(tasks);
+    const int64_t cap = (int64_t)sm_count() * 8;
+    if (b > cap) b = cap;
+    return (int)(b < 1 ? 1 : b);
+}
+
+template <int T, bool INT8>
 cudaError_t rows_dispatch(int vpt, const uint16_t* x, int64_t rows, int64_t K, int64_t ld, uint8_t* codes,
                           float* scales, cudaStream_t st) {
     dim3 grid((unsigned)rows);
+#define QLIN_ROWS(V)                                                                              \
+    case V:                                                                                       \
+        if constexpr (INT8) k_int8_rows<T, V><<<grid, T, 0, st>>>(x, K, ld, codes, scales);        \
+        else k_fp8_rows<T, V><<<grid, T, 0, st>>>(x, K, ld, codes, scales);                        \
+        break;
     switch (vpt) {
-        case 1: k_fp8_rows<T, 1><<<grid, T, 0, st>>>(x, K, ld, codes, scales); break;
-        case 2: k_fp8_rows<T, 2><<<grid, T, 0, st>>>(x, K, ld, codes, scales); break;
-        case 3: k_fp8_rows<T, 3><<<grid, T, 0, st>>>(x, K, ld, codes, scales); break;
-        case 4: k_fp8_rows<T, 4><<<grid, T, 0, st>>>(x, K, ld, codes, scales); break;
-        case 5: k_fp8_rows<T, 5><<<grid, T, 0, st>>>(x, K, ld, codes, scales); break;
-        case 6: k_fp8_rows<T, 6><<<grid, T, 0, st>>>(x, K, ld, codes, scales); break;
-        case 7: k_fp8_rows<T, 7><<<grid, T, 0, st>>>(x, K, ld, codes, scales); break;
-        default: k_fp8_rows<T, 8><<<grid, T, 0, st>>>(x, K, ld, codes, scales); break;
+        QLIN_ROWS(1)
+        QLIN_ROWS(2)
+        QLIN_ROWS(3)
+        QLIN_ROWS(4)
+        QLIN_ROWS(5)
+        QLIN_ROWS(6)
+        QLIN_ROWS(7)
+        default:
+        QLIN_ROWS(8)
     }
+#undef QLIN_ROWS
+    return cudaGetLastError();
+}
+
+template <bool INT8>
+cudaError_t rowwise(const uint16_t* x, int64_t rows, int64_t K, int64_t ld, uint8_t* codes, float* scales,
+                    cudaStream_t st) {
+    const int64_t nv = K >> 3;
+    if (nv <= 128 * 8) return rows_dispatch<128, INT8>((int)((nv + 127) / 128), x, rows, K, ld, codes, scales, st);
+    if (nv <= 256 * 8) return rows_dispatch<256, INT8>((int)((nv + 255) / 256), x, rows, K, ld, codes, scales, st);
+    if constexpr (INT8) k_int8_rows_long<<<(unsigned)rows, 256, 0, st>>>(x, K, ld, codes, scales);
+    else k_fp8_rows_long<<<(unsigned)rows, 256, 0, st>>>(x, K, ld, codes, scales);
     return cudaGetLastError();
 }
 
@@ -516,11 +629,12 @@ int amax_partials(int64_t rows, int64_t K) {
 
 cudaError_t launch_fp8_rowwise(const uint16_t* x, int64_t rows, int64_t K, int64_t ld, uint8_t* codes,
                                float* scales, cudaStream_t st) {
-    const int64_t nv = K >> 3;
-    if (nv <= 128 * 8) return rows_dispatch<128>((int)((nv + 127) / 128), x, rows, K, ld, codes, scales, st);
-    if (nv <= 256 * 8) return rows_dispatch<256>((int)((nv + 255) / 256), x, rows, K, ld, codes, scales, st);
-    k_fp8_rows_long<<<(unsigned)rows, 256, 0, st>>>(x, K, ld, codes, scales);
-    return cudaGetLastError();
+    return rowwise<false>(x, rows, K, ld, codes, scales, st);
+}
+
+cudaError_t launch_int8_rowwise(const uint16_t* x, int64_t rows, int64_t K, int64_t ld, uint8_t* codes,
+                                float* scales, cudaStream_t st) {
+    return rowwise<true>(x, rows, K, ld, codes, scales, st);
 }
 
 cudaError_t launch_fp8_tensor(const uint16_t* x, int64_t rows, int64_t K, int64_t ld, uint8_t* codes,
@@ -528,14 +642,13 @@ cudaError_t launch_fp8_tensor(const uint16_t* x, int64_t rows, int64_t K, int64_
     const int64_t tasks = task_count(rows, K);
     if (tasks < 0) return cudaErrorInvalidValue;
     k_amax_partial<<<nparts, 256, 0, st>>>(x, rows, K, ld, partials);
-    k_fp8_tensor_encode<<<task_grid(tasks), 256, 0, st>>>(x, rows, K, ld, codes, scale, partials, nparts);
+    k_fp8_tensor_encode<<<task_grid_persistent(tasks), 256, 0, st>>>(x, rows, K, ld, codes, scale, partials, nparts);
     return cudaGetLastError();
 }
 
 cudaError_t launch_fp8_block128(const uint16_t* x, int64_t rows, int64_t K, int64_t ld, uint8_t* codes,
                                 float* scales, cudaStream_t st) {
-    dim3 grid((unsigned)(K / 128), (unsigned)(rows / 128));
-    k_fp8_block128<<<grid, 256, 0, st>>>(x, K, ld, codes, scales);
+    k_fp8_block128<<<(unsigned)((K / 128) * (rows / 128)), 256, 0, st>>>(x, K, ld, codes, scales);
     return cudaGetLastError();
 }
 
@@ -543,7 +656,7 @@ cudaError_t launch_fp8_group128(const uint16_t* x, int64_t rows, int64_t K, int6
                                 float* scales, cudaStream_t st) {
     const int64_t tasks = task_count(rows, K);
     if (tasks < 0) return cudaErrorInvalidValue;
-    k_fp8_group128<<<task_grid(tasks), 256, 0, st>>>(x, rows, K, ld, codes, scales);
+    k_fp8_group128<<<task_grid_once(tasks), 256, 0, st>>>(x, rows, K, ld, codes, scales);
     return cudaGetLastError();
 }
 
@@ -552,7 +665,7 @@ cudaError_t launch_mxfp8(const uint16_t* x, int64_t rows, int64_t K, int64_t ld,
     const int64_t rows_pad = mma_layout ? (rows + 127) / 128 * 128 : rows;
     const int64_t tasks = task_count(rows_pad, K);
     if (tasks < 0) return cudaErrorInvalidValue;
-    k_mx<false><<<task_grid(tasks), 256, 0, st>>>(x, rows, rows_pad, K, ld, codes, scales, mma_layout ? 1 : 0);
+    k_mx<false><<<task_grid_once(tasks), 256, 0, st>>>(x, rows, rows_pad, K, ld, codes, scales, mma_layout ? 1 : 0);
     return cudaGetLastError();
 }
 
@@ -561,7 +674,7 @@ cudaError_t launch_mxfp4(const uint16_t* x, int64_t rows, int64_t K, int64_t ld,
     const int64_t rows_pad = mma_layout ? (rows + 127) / 128 * 128 : rows;
     const int64_t tasks = task_count(rows_pad, K);
     if (tasks < 0) return cudaErrorInvalidValue;
-    k_mx<true><<<task_grid(tasks), 256, 0, st>>>(x, rows, rows_pad, K, ld, codes, scales, mma_layout ? 1 : 0);
+    k_mx<true><<<task_grid_once(tasks), 256, 0, st>>>(x, rows, rows_pad, K, ld, codes, scales, mma_layout ? 1 : 0);
     return cudaGetLastError();
 }
 
@@ -572,15 +685,14 @@ cudaError_t launch_nvfp4(const uint16_t* x, int64_t rows, int64_t K, int64_t ld,
     const int64_t tasks = task_count(rows_pad, K);
     if (tasks < 0) return cudaErrorInvalidValue;
     k_amax_partial<<<nparts, 256, 0, st>>>(x, rows, K, ld, partials);
-    k_nvfp4_encode<<<task_grid(tasks), 256, 0, st>>>(x, rows, rows_pad, K, ld, codes, scales, global, partials,
+    k_nvfp4_encode<<<task_grid_persistent(tasks), 256, 0, st>>>(x, rows, rows_pad, K, ld, codes, scales, global, partials,
                                                      nparts, mma_layout ? 1 : 0);
     return cudaGetLastError();
 }
 
 cudaError_t launch_int4_g128(const uint16_t* w, int64_t N, int64_t K, int64_t ld, int32_t* qweight,
                              uint16_t* scales, int32_t* qzeros, cudaStream_t st) {
-    dim3 grid((unsigned)((N + 127) / 128), (unsigned)(K / 128));
-    k_int4_g128<<<grid, 128, 0, st>>>(w, N, K, ld, qweight, scales, qzeros);
+    k_int4_g128<<<(unsigned)(((N + 127) / 128) * (K / 128)), 128, 0, st>>>(w, N, K, ld, qweight, scales, qzeros);
     return cudaGetLastError();
 }
 

@@ -135,6 +135,14 @@ def fp8_group_linear(K: int, N: int, M: int = 4096) -> Linear:
                   _seed(7, 2 * v), _seed(7, 2 * v + 1), "outlier", x_std=1.0, w_std=0.02)
 
 
+def int8_linear(K: int, N: int, M: int = 4096) -> Linear:
+    """INT8 W8A8 (per-token X, per-channel W) on the DiT MLP shapes and
+    distributions of the FP8 block workload (1% outlier channels in X)."""
+    v = FP8_MLP_SHAPES.index((K, N)) if (K, N) in FP8_MLP_SHAPES else 5
+    return Linear(f"int8_K{K}_N{N}", M, K, N, "int8_row", "int8_row",
+                  _seed(8, 2 * v), _seed(8, 2 * v + 1), "outlier", x_std=1.0, w_std=0.02)
+
+
 def mxfp4_linear(K: int, N: int, M: int = MXFP8_M) -> Linear:
     """MXFP4 W4A4 (the next format of the online MXFP4 path) on the video-DiT
     shapes and distributions of the MXFP8 workload: X N(0,1), W N(0, 0.015^2)."""

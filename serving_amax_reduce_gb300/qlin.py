@@ -29,6 +29,7 @@ class Fmt(enum.IntEnum):
     BF16 = 6
     MXFP4 = 7
     FP8_GROUP128 = 8
+    INT8_ROW = 9
 
 
 class Layout(enum.IntEnum):
@@ -197,7 +198,7 @@ def alloc_quant(fmt: Fmt, rows: int, K: int, layout: Layout, device) -> dict:
     """Torch buffers sized by the library's own size queries."""
     out = {"codes": _empty(qlin_codes_bytes(fmt, rows, K), device)}
     sb = qlin_scales_bytes(fmt, layout, rows, K)
-    if fmt in (Fmt.FP8_TENSOR, Fmt.FP8_TOKEN, Fmt.FP8_BLOCK128, Fmt.FP8_GROUP128):
+    if fmt in (Fmt.FP8_TENSOR, Fmt.FP8_TOKEN, Fmt.FP8_BLOCK128, Fmt.FP8_GROUP128, Fmt.INT8_ROW):
         out["scales"] = _empty(sb, device, torch.float32)
     elif fmt == Fmt.INT4_G128_ASYM:
         out["scales"] = _empty(sb, device, torch.int16)

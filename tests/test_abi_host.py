@@ -62,6 +62,11 @@ def test_size_queries(q):
     # FP8 1 x 128 groups: one float per row and 128 K
     assert q.qlin_codes_bytes(F.FP8_GROUP128, 4096, 3072) == 4096 * 3072
     assert q.qlin_scales_bytes(F.FP8_GROUP128, L.CANONICAL, 4096, 3072) == 4096 * 24 * 4
+    # INT8 per row: one byte per code, one float per row, no workspace
+    assert q.qlin_codes_bytes(F.INT8_ROW, 4096, 3072) == 4096 * 3072
+    assert q.qlin_scales_bytes(F.INT8_ROW, L.CANONICAL, 4096, 3072) == 4096 * 4
+    assert q.qlin_quant_workspace_bytes(F.INT8_ROW, 4096, 3072) == 0
+    assert q.qlin_gemm_workspace_bytes(F.INT8_ROW, F.INT8_ROW, 4096, 12288, 3072) == 0
 
 
 FAKE = 1 << 20          # a 16-byte aligned non-null value; never dereferenced by these calls
@@ -106,6 +111,12 @@ def test_quantize_rejects_bad_arguments(q):
                                None) == S.INVALID_ARG                  # K % 128
     assert q.qlin_quantize_act(F.FP8_GROUP128, FAKE, 128, 128, 128, FAKE, FAKE, None, L.MMA, None, 0, None,
                                None) == S.UNSUPPORTED                  # no tensor-core scale layout
+    assert q.qlin_quantize_act(F.INT8_ROW, FAKE, 128, 1020, 1024, FAKE, FAKE, None, L.CANONICAL, None, 0, None,
+                               None) == S.INVALID_ARG                  # K % 8
+    assert q.qlin_quantize_weight(F.INT8_ROW, FAKE, 128, 1024, 1024, FAKE, FAKE + 2, None, None, L.CANONICAL,
+                                  None, 0, None, None) == S.ALIGNMENT  # float scales
+    assert q.qlin_quantize_weight(F.INT8_ROW, FAKE, 128, 1024, 1024, FAKE, FAKE, None, None, L.MMA, None, 0,
+                                  None, None) == S.UNSUPPORTED
     # NVFP4 needs the global-scale output
     assert q.qlin_quantize_act(F.NVFP4, FAKE, 128, 1024, 1024, FAKE, FAKE, None, L.CANONICAL, FAKE, 1 << 20,
                                None, None) == S.INVALID_ARG
@@ -143,6 +154,10 @@ def test_gemm_rejects_bad_arguments(q):
     assert g(F.FP8_BLOCK128, F.FP8_GROUP128, 128, 1024, 1024, xs=None) == S.INVALID_ARG
     assert g(F.FP8_TENSOR, F.FP8_GROUP128, 128, 1024, 1024) == S.UNSUPPORTED
     assert g(F.FP8_TENSOR, F.FP8_TOKEN, 128, 1024, 1024) == S.UNSUPPORTED
+    assert g(F.INT8_ROW, F.INT8_ROW, 128, 1024, 1000) == S.INVALID_ARG         # K % 16
+    assert g(F.INT8_ROW, F.INT8_ROW, 128, 1024, 1024, ws=None) == S.INVALID_ARG
+    assert g(F.INT8_ROW, F.FP8_TOKEN, 128, 1024, 1024) == S.UNSUPPORTED
+    assert g(F.FP8_BLOCK128, F.INT8_ROW, 128, 1024, 1024) == S.UNSUPPORTED
     assert g(F.INT4_G128_ASYM, F.BF16, 16, 4096, 4000) == S.INVALID_ARG
     need = q.qlin_gemm_workspace_bytes(F.INT4_G128_ASYM, F.BF16, 16, 4096, 4096)
     if need:

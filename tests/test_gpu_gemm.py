@@ -144,6 +144,43 @@ def test_fp8_group128_gemm_full_size(q, orc):
     fp8_group_case(q, orc, 4096, 12288, 3072, nrows=256)
 
 
+# ------------------------------------------------------------------ INT8 W8A8
+def int8_case(q, orc, M, N, K, nrows=None, with_bias=False):
+    lin = inputs.int8_linear(K, N, M=M)
+    x, w = lin.make_x(), lin.make_w()
+    F = q.Fmt
+    bx = q.quantize_act(F.INT8_ROW, x.cuda())
+    bw = q.quantize_weight(F.INT8_ROW, w.cuda())
+    bias = inputs.normal_bf16((1, N), 0.05, 81)[0] if with_bias else None
+    y = q.gemm(F.INT8_ROW, F.INT8_ROW, M, N, K, bx["codes"], bx["scales"], bw["codes"], bw["scales"],
+               bias=bias.cuda() if with_bias else None)
+    torch.cuda.synchronize()
+    rows = sample_rows(M, nrows or M)
+    cx = np_u8(bx["codes"]).reshape(M, K).view(np.int8)
+    cw = np_u8(bw["codes"]).reshape(N, K).view(np.int8)
+    xh = orc.dequant_int8_row(cx[rows], np_f32(bx["scales"])[:M][rows])
+    wh = orc.dequant_int8_row(cw, np_f32(bw["scales"])[:N])
+    b = orc.bf16_values(bits(bias)[None, :])[0] if with_bias else None
+    return check(orc, y_np(y)[rows], orc.gemm_ref(xh, wh, bias=b), x, w, rows=torch.from_numpy(rows))
+
+
+# ragged M and N tiles, K not a multiple of the 64-wide stage, one row, one stage
+@pytest.mark.parametrize("M,N,K", [(200, 512, 384), (128, 256, 64), (1, 384, 256), (300, 640, 1040),
+                                   (513, 1280, 1152)])
+def test_int8_gemm(q, orc, M, N, K):
+    int8_case(q, orc, M, N, K)
+
+
+def test_int8_gemm_bias(q, orc):
+    int8_case(q, orc, 130, 640, 272, with_bias=True)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("K,N", [(3072, 12288), (12288, 3072)])
+def test_int8_gemm_full_size(q, orc, K, N):
+    int8_case(q, orc, 4096, N, K, nrows=256)
+
+
 # ------------------------------------------------------------------ MXFP8
 def mxfp8_case(q, orc, M, N, K, nrows=None):
     lin = inputs.mxfp8_linear(K, N, M=M)

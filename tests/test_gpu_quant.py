@@ -44,6 +44,27 @@ def test_fp8_token(q, orc, rows, K, kind):
     assert np.array_equal(np_f32(b["scales"])[:rows].view(np.uint32), scales.view(np.uint32))
 
 
+def int8_ties(rows, K, seed):
+    """Rows whose amax is 127 * 2^k, so that 127/amax = 2^-k exactly and
+    every x * 127/amax is a half-integer: each odd one is a rounding tie."""
+    g = torch.Generator().manual_seed(seed)
+    k = torch.randint(-8, 9, (rows, 1), generator=g).float()
+    n = torch.randint(-254, 255, (rows, K), generator=g).float()
+    n[:, 0] = 254
+    return ((n / 2) * torch.pow(2.0, k)).to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("rows,K", SHAPES_ROW)
+@pytest.mark.parametrize("kind", ["outlier", "edge", "ties"])
+@pytest.mark.parametrize("weight", [False, True])
+def test_int8_row(q, orc, rows, K, kind, weight):
+    x = int8_ties(rows, K, rows + 3 * K) if kind == "ties" else make(kind, rows, K, 5 * rows + K)
+    b = run(q, q.Fmt.INT8_ROW, x, weight=weight)
+    codes, scales = orc.quant_int8_row(bits(x))
+    assert np.array_equal(np_u8(b["codes"]).reshape(rows, K).view(np.int8), codes)
+    assert np.array_equal(np_f32(b["scales"])[:rows].view(np.uint32), scales.view(np.uint32))
+
+
 @pytest.mark.parametrize("rows,K", [(128, 1024), (1024, 1024), (333, 520), (4096, 4096), (1, 8)])
 @pytest.mark.parametrize("kind", ["normal", "edge"])
 def test_fp8_tensor(q, orc, rows, K, kind):
