@@ -76,14 +76,14 @@ struct Cfg {
     static constexpr int STAGES = CVT ? 2 : 4;       // operand stages (converted fp16 for INT8)
     static constexpr int S8 = CVT ? 4 : 0;           // int8 staging stages
     static constexpr int EPI_WARPS = 8;              // two per TMEM lane quadrant, 128 columns each
-    static constexpr int CVT_WARPS = CVT ? 4 : 0;    // warpgroup 3 (INT8 only): int8 -> fp16
-    // warpgroup 0: TMA + MMA; warpgroups 1-2: epilogue; warpgroup 3: converters
+    static constexpr int CVT_WARPS = CVT ? 8 : 0;    // warpgroups 3-4 (INT8 only): int8 -> fp16
+    // warpgroup 0: TMA + MMA; warpgroups 1-2: epilogue; warpgroups 3-4: converters
     static constexpr int THREADS = 384 + 32 * CVT_WARPS;
     // setmaxnreg split, within the launch allocation (checked on the host
     // before launch): 128 x 40 + 256 x 232 = 64512 <= 384 x 168, and for INT8
-    // 128 x 40 + 256 x 184 + 128 x 104 = 65536 = 512 x 128.
-    static constexpr int REGS_LAUNCH = CVT ? 128 : 168, REGS_CTRL = 40, REGS_EPI = CVT ? 184 : 232;
-    static constexpr int REGS_CVT = 104;
+    // 128 x 40 + 256 x 136 + 256 x 80 = 60416 <= 640 x 96.
+    static constexpr int REGS_LAUNCH = CVT ? 96 : 168, REGS_CTRL = 40, REGS_EPI = CVT ? 136 : 232;
+    static constexpr int REGS_CVT = 80;
     static_assert(128 * REGS_CTRL + 256 * REGS_EPI + 32 * CVT_WARPS * REGS_CVT <= THREADS * REGS_LAUNCH,
                   "register split");
     static constexpr int A_BYTES = BM * BKB;
@@ -383,7 +383,14 @@ __global__ void __launch_bounds__(Cfg<KIND>::THREADS, 1)
         uint32_t kg = 0, kbg = 0, it = 0;
         bool ok = true;
         for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, it++) {
-            if (KIND != kFp8Block) {
+            if (C::CVT) {
+                // INT8: two accumulator buffers (2 x 256 columns); wait until the
+                // epilogue has drained the one this tile reuses
+                if (!wait_or_abort(pempty + (it & 1u), ((it >> 1) & 1u) ^ 1u, abort_flag)) {
+                    record_timeout(p.status, abort_flag);
+                    break;
+                }
+            } else if (KIND != kFp8Block) {
                 if (!wait_or_abort(acce, (it & 1u) ^ 1u, abort_flag)) {
                     record_timeout(p.status, abort_flag);
                     break;
@@ -397,7 +404,7 @@ __global__ void __launch_bounds__(Cfg<KIND>::THREADS, 1)
                     ok = false;
                     break;
                 }
-                uint32_t d = tmem;
+                uint32_t d = C::CVT ? tmem + (it & 1u) * (uint32_t)C::BN : tmem;
                 if (KIND == kFp8Block) {
                     const int b = (int)(kbg & 1u);
                     if (!wait_or_abort(pempty + b, ((kbg >> 1) & 1u) ^ 1u, abort_flag)) {
@@ -454,7 +461,8 @@ __global__ void __launch_bounds__(Cfg<KIND>::THREADS, 1)
                 }
                 misc[2] = kg + 1;
             }
-            if (ok && KIND != kFp8Block) tc_commit(accf);
+            if (ok && C::CVT) tc_commit(pfull + (it & 1u));
+            else if (ok && KIND != kFp8Block) tc_commit(accf);
         }
     } else if (!skip && C::SPLIT_CP && (warp == 2 || warp == 3) && lane == 0) {
         // ------------------------------------------------ scale-factor copies (NVFP4)
@@ -508,7 +516,45 @@ __global__ void __launch_bounds__(Cfg<KIND>::THREADS, 1)
             const int row = m0 + q * 32 + lane;
             const int ncol = n0 + h * 128;
             bool ok = true;
-            if (KIND != kFp8Block) {
+            if constexpr (C::CVT) {
+                // INT8: accumulator buffer it & 1, read in two 64-column halves
+                // (fewer registers) and released after the second
+                const uint32_t b = it & 1u;
+                if (!warp_wait_or_abort(pfull + b, (it >> 1) & 1u, abort_flag)) {
+                    if (lane == 0) record_timeout(p.status, abort_flag);
+                    break;
+                }
+                tc_fence_after();
+                uint8_t* stg = smem + C::OFF_STG + (warp - 4) * C::STG_BYTES;
+                const float sxr = row < p.M ? __ldg(p.x_scale + row) : 0.0f;
+#pragma unroll
+                for (int hh = 0; hh < 2; hh++) {
+                    uint32_t r[2][32];
+#pragma unroll
+                    for (int c = 0; c < 2; c++)
+                        tmem_ld_32x32b_x32(tmem + lane_addr + b * (uint32_t)C::BN + (uint32_t)(h * 128 + (2 * hh + c) * 32),
+                                           r[c]);
+                    tmem_ld_wait();
+                    if (hh == 1) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(pempty + b);   // the MMA may reuse this buffer
+                    }
+#pragma unroll
+                    for (int c = 0; c < 2; c++) {
+                        const int col0 = ncol + (2 * hh + c) * 32;
+                        if (col0 < p.N) {
+                            float v[32];
+#pragma unroll
+                            for (int i = 0; i < 32; i++) {
+                                const int col = col0 + i;
+                                v[i] = __uint_as_float(r[c][i]) * sxr * (col < p.N ? __ldg(p.w_scale + col) : 0.0f);
+                            }
+                            store_block32<C::STG_BUFS>(p, &tmY, stg, m0 + q * 32, col0, v);
+                        }
+                    }
+                }
+            } else if (KIND != kFp8Block) {
                 if (!warp_wait_or_abort(accf, it & 1u, abort_flag)) {
                     if (lane == 0) record_timeout(p.status, abort_flag);
                     break;
@@ -523,21 +569,12 @@ __global__ void __launch_bounds__(Cfg<KIND>::THREADS, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(acce);     // the MMA may start the next tile
                 uint8_t* stg = smem + C::OFF_STG + (warp - 4) * C::STG_BYTES;
-                // INT8: s_x of this thread's row, s_w per column (one uniform load each)
-                const float sxr = (KIND == kInt8) ? (row < p.M ? __ldg(p.x_scale + row) : 0.0f) : alpha;
 #pragma unroll
                 for (int c = 0; c < 4; c++) {
                     if (ncol + c * 32 < p.N) {
                         float v[32];
 #pragma unroll
-                        for (int i = 0; i < 32; i++) v[i] = __uint_as_float(r[c][i]) * sxr;
-                        if (KIND == kInt8) {
-#pragma unroll
-                            for (int i = 0; i < 32; i++) {
-                                const int col = ncol + c * 32 + i;
-                                v[i] *= col < p.N ? __ldg(p.w_scale + col) : 0.0f;
-                            }
-                        }
+                        for (int i = 0; i < 32; i++) v[i] = __uint_as_float(r[c][i]) * alpha;
                         store_block32<C::STG_BUFS>(p, &tmY, stg, m0 + q * 32, ncol + c * 32, v);
                     }
                 }
@@ -613,8 +650,9 @@ __global__ void __launch_bounds__(Cfg<KIND>::THREADS, 1)
         if (!skip) {
             // ------------------------------------------------ int8 -> fp16 converters (4 warps)
             // A stage holds 384 rows (128 of X, 256 of W) of 64 int8 = 4 chunks
-            // of 16 codes; thread ct takes chunks ct, ct + 128, ... (8 rows per
-            // warp per round: 128 contiguous staging bytes per quarter warp).
+            // of 16 codes; thread ct (0..255) takes chunk ct & 3 of rows
+            // ct / 4 + 64 i, i = 0..5 (8 rows per warp per round: 128 contiguous
+            // staging bytes per quarter warp).
             // Chunk c of row r becomes 16-byte fp16 chunks 2c and 2c + 1 of the
             // row's 128 bytes, stored at chunk position (2c [+1]) ^ (r & 7):
             // the 128-byte swizzle the MMA descriptors expect (8-row atoms).
@@ -634,21 +672,33 @@ __global__ void __launch_bounds__(Cfg<KIND>::THREADS, 1)
                     const uint8_t* b8 = smem + C::OFF_B8 + j * C::B8_BYTES;
                     uint8_t* a16 = smem + C::OFF_A + s * C::A_BYTES;
                     uint8_t* b16 = smem + C::OFF_B + s * C::B_BYTES;
-#pragma unroll 4
-                    for (int i = 0; i < (BM + C::BN) * 4 / 128; i++) {
-                        const int id = i * 128 + ct, r = id >> 2, c = id & 3;
-                        const bool isa = r < BM;          // uniform per i
-                        const int rr = isa ? r : r - BM;
-                        const uint4 qv = *reinterpret_cast<const uint4*>((isa ? a8 : b8) + rr * C::K8 + c * 16);
-                        uint4 h0, h1;
-                        i8x4_to_f16x4(qv.x, h0.x, h0.y);
-                        i8x4_to_f16x4(qv.y, h0.z, h0.w);
-                        i8x4_to_f16x4(qv.z, h1.x, h1.y);
-                        i8x4_to_f16x4(qv.w, h1.z, h1.w);
-                        uint8_t* row = (isa ? a16 : b16) + rr * 128;
-                        const int sw = rr & 7;
-                        *reinterpret_cast<uint4*>(row + (((2 * c) ^ sw) << 4)) = h0;
-                        *reinterpret_cast<uint4*>(row + (((2 * c + 1) ^ sw) << 4)) = h1;
+                    // a batch of chunks is read before any is stored: stores may not
+                    // be ordered before loads the compiler cannot prove disjoint,
+                    // which would serialize load -> convert -> store chunk by chunk
+                    constexpr int TPR = 32 * C::CVT_WARPS / 4;   // rows per round
+                    constexpr int ROUNDS = (BM + C::BN) / TPR, BATCH = ROUNDS / 2;
+                    const int c = ct & 3, sw = (ct >> 2) & 7;   // same chunk and swizzle row every round
+#pragma unroll
+                    for (int i0 = 0; i0 < ROUNDS; i0 += BATCH) {
+                        uint4 qv[BATCH];
+#pragma unroll
+                        for (int i = 0; i < BATCH; i++) {
+                            const int r = (i0 + i) * TPR + (ct >> 2);  // rows < BM come from X
+                            const uint8_t* src = r < BM ? a8 + r * C::K8 : b8 + (r - BM) * C::K8;
+                            qv[i] = *reinterpret_cast<const uint4*>(src + c * 16);
+                        }
+#pragma unroll
+                        for (int i = 0; i < BATCH; i++) {
+                            const int r = (i0 + i) * TPR + (ct >> 2);
+                            uint8_t* row = r < BM ? a16 + r * 128 : b16 + (r - BM) * 128;
+                            uint4 h0, h1;
+                            i8x4_to_f16x4(qv[i].x, h0.x, h0.y);
+                            i8x4_to_f16x4(qv[i].y, h0.z, h0.w);
+                            i8x4_to_f16x4(qv[i].z, h1.x, h1.y);
+                            i8x4_to_f16x4(qv[i].w, h1.z, h1.w);
+                            *reinterpret_cast<uint4*>(row + (((2 * c) ^ sw) << 4)) = h0;
+                            *reinterpret_cast<uint4*>(row + (((2 * c + 1) ^ sw) << 4)) = h1;
+                        }
                     }
                     fence_proxy_async_smem();         // generic-proxy writes -> the MMA's async proxy
                     __syncwarp();
