@@ -54,7 +54,8 @@ def parse_args():
     ap.add_argument("--only", default=None, help="keep only linears whose name contains this string")
     ap.add_argument("--next", action="store_true",
                     help="measure the next rows instead (MXFP4 W4A4 on the MXFP8 workload's shapes, FP8 "
-                         "1x128-group and INT8 W8A8 on the DiT MLP shapes)")
+                         "1x128-group and INT8 W8A8 on the DiT MLP shapes, the per-tensor FP8 linear with "
+                         "its activation quantization fused into the GEMM)")
     return ap.parse_args()
 
 
@@ -82,7 +83,8 @@ def workload_linears(next_rows: bool = False):
     if next_rows:
         return ([("mxfp4", I.mxfp4_linear(K, N)) for (K, N) in I.MXFP8_SHAPES]
                 + [("fp8_group", I.fp8_group_linear(K, N)) for (K, N) in I.FP8_MLP_SHAPES]
-                + [("int8", I.int8_linear(K, N)) for (K, N) in I.FP8_MLP_SHAPES])
+                + [("int8", I.int8_linear(K, N)) for (K, N) in I.FP8_MLP_SHAPES]
+                + [("fp8_tensor_fused", I.fp8_tensor_fused_linear())])
     lins = [("fp8_tensor", I.fp8_tensor_linear())]
     for (K, N) in I.W4A16_SHAPES:
         for M in I.W4A16_M:
@@ -102,7 +104,8 @@ def config_block(args):
         return {"workload": "next-rows",
                 "workloads": ["mxfp4 W4A4 M20280 (K,N){(5120,13824),(13824,5120),(5120,5120)}",
                               "fp8 1x128-group X x 128x128-block W, M4096 (K,N){(3072,12288),(12288,3072)}",
-                              "int8 W8A8 per-token X x per-channel W, M4096 (K,N){(3072,12288),(12288,3072)}"],
+                              "int8 W8A8 per-token X x per-channel W, M4096 (K,N){(3072,12288),(12288,3072)}",
+                              "fp8 per-tensor with X quantized inside the GEMM, M128 K1024 N1024"],
                 "step": "per linear: weight quantize + activation quantize + quantized GEMM",
                 "l2": "inputs larger than L2", "parallelism": f"replicas x{args.gpus}"}
     return {
@@ -205,7 +208,7 @@ class Job:
         q, lin = self.q, self.lin
         if self.xb is None:
             q.gemm(self.wf, self.xf, lin.M, lin.N, lin.K, self.x, None, self.wb["codes"], self.wb["scales"],
-                   w_zeros=self.wb["zeros"], y=self.y)
+                   w_zeros=self.wb.get("zeros"), y=self.y)
         else:
             q.gemm(self.wf, self.xf, lin.M, lin.N, lin.K, self.xb["codes"], self.xb["scales"], self.wb["codes"],
                    self.wb["scales"], x_global=self.xb.get("global"), w_global=self.wb.get("global"), y=self.y,
@@ -265,6 +268,8 @@ def kernel_name(job, op):
     if op == "gemm":
         if job.xf == F.FP8_GROUP128:
             return "gemm_fp8_block_x_group128"
+        if job.xf == F.BF16 and job.wf == F.FP8_TENSOR:
+            return "gemm_fp8_tensor_fused_x"
         return {F.FP8_TENSOR: "gemm_fp8_tensor", F.FP8_BLOCK128: "gemm_fp8_block", F.MXFP8: "gemm_mxfp8",
                 F.NVFP4: "gemm_nvfp4", F.INT4_G128_ASYM: "gemm_w4a16", F.MXFP4: "gemm_mxfp4",
                 F.INT8_ROW: "gemm_int8"}[job.wf]

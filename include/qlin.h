@@ -181,6 +181,13 @@ qlin_status qlin_quantize_act(qlin_format fmt, const void *x_bf16_dev, int64_t M
  * "在线量化的底层工作原理", FP8 paragraph).
  * Supported (w_fmt, x_fmt) pairs and their operands:
  *   FP8_TENSOR, FP8_TENSOR : x = codes [M,K]; x_scales, w_scales = one float each
+ *   FP8_TENSOR, BF16       : activation quantization fused into the GEMM: x =
+ *                            bf16 activations [M,K] (M <= 128, else
+ *                            QLIN_ERR_UNSUPPORTED), quantized per tensor inside
+ *                            the kernel by the FP8_TENSOR rule; x_scales unused;
+ *                            w_scales one float; K % 16 == 0.  Y is bit-identical
+ *                            to qlin_quantize_act(FP8_TENSOR) followed by the
+ *                            FP8_TENSOR pair, in one launch.
  *   FP8_BLOCK128, FP8_TOKEN: x_scales float [M]; w_scales float [N/128, K/128]
  *                            (N % 128 == 0, K % 128 == 0)
  *   FP8_BLOCK128, FP8_GROUP128: x_scales float [M, K/128]; otherwise as above

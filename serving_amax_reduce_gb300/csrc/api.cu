@@ -228,6 +228,13 @@ qlin_status qlin_gemm(qlin_format w_fmt, qlin_format x_fmt, int64_t M, int64_t N
         if (!aligned16(x_scales_dev) || !aligned16(w_scales_dev)) return QLIN_ERR_ALIGNMENT;
         return launch_status(launch_gemm_nvfp4(a, st));
     }
+    if (w_fmt == QLIN_FP8_TENSOR && x_fmt == QLIN_BF16) {
+        // activation quantization fused into the GEMM: single-request row counts
+        if (!w_scales_dev) return QLIN_ERR_INVALID_ARG;
+        if (M > 128) return QLIN_ERR_UNSUPPORTED;
+        if (K % 16) return QLIN_ERR_INVALID_ARG;
+        return launch_status(launch_gemm_fp8_tensor_fused_x(a, st));
+    }
     if (w_fmt == QLIN_INT8_ROW && x_fmt == QLIN_INT8_ROW) {
         if (!x_scales_dev || !w_scales_dev) return QLIN_ERR_INVALID_ARG;
         if (K % 16) return QLIN_ERR_INVALID_ARG;

@@ -49,6 +49,16 @@
 //                   128-byte-swizzled layout the MMA reads; kind::f16 then
 //                   multiplies exact integers with fp32 accumulation, and the
 //                   epilogue applies s_x[m] * s_w[n].
+//   FP8 per-tensor  with the activation quantization fused into the GEMM (the
+//   fused X         producer quantizes the X tile): for M <= 128 (one row tile,
+//                   the single-request shapes) X arrives in bf16.  The eight
+//                   epilogue warps, idle during the mainloop, first take the
+//                   tensor amax of X (every CTA's A tile is all of X), then turn
+//                   each 128 x 128 bf16 block into E4M3 codes in the 128-byte-
+//                   swizzled A stage while TMA brings the W tile, and drain the
+//                   accumulator at the end of the tile.  Codes, s_x and the MMA
+//                   sequence equal those of qlin_quantize_act + the per-tensor
+//                   GEMM, so Y is the same bits; one launch instead of three.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -62,7 +72,7 @@ namespace {
 
 using namespace ptx;
 
-enum Kind { kFp8Tensor = 0, kFp8Block = 1, kMxfp8 = 2, kNvfp4 = 3, kMxfp4 = 4, kInt8 = 5 };
+enum Kind { kFp8Tensor = 0, kFp8Block = 1, kMxfp8 = 2, kNvfp4 = 3, kMxfp4 = 4, kInt8 = 5, kFp8QX = 6 };
 
 constexpr int BM = 128;              // tile rows (X rows) = MMA M
 constexpr int BKB = 128;             // K bytes per stage: 128 fp8 or 256 fp4 (one swizzle row)
@@ -72,6 +82,8 @@ template <int KIND>
 struct Cfg {
     // INT8: operands are converted on chip from an int8 staging ring
     static constexpr bool CVT = (KIND == kInt8);
+    // FP8 per-tensor with bf16 X: the epilogue warps quantize the A stages
+    static constexpr bool QX = (KIND == kFp8QX);
     static constexpr int BN = 256;
     static constexpr int STAGES = CVT ? 2 : 4;       // operand stages (converted fp16 for INT8)
     static constexpr int S8 = CVT ? 4 : 0;           // int8 staging stages
@@ -128,7 +140,7 @@ template <int KIND>
 __host__ __device__ constexpr uint32_t idesc_for() {
     constexpr uint32_t n = (uint32_t)(Cfg<KIND>::BN >> 3) << 17;
     constexpr uint32_t m = (uint32_t)(BM >> 4) << 24;
-    if (KIND == kFp8Tensor || KIND == kFp8Block)
+    if (KIND == kFp8Tensor || KIND == kFp8Block || KIND == kFp8QX)
         return (1u << 4) /* D f32 */ | (0u << 7) /* A e4m3 */ | (0u << 10) /* B e4m3 */ | n | m;
     if (KIND == kInt8)   // kind::f16
         return (1u << 4) /* D f32 */ | (0u << 7) /* A f16 */ | (0u << 10) /* B f16 */ | n | m;
@@ -153,6 +165,7 @@ struct TcParams {
     uint16_t* y;
     int* status;
     int x_group;             // FP8 block: x_scale is [M, K/128] (1 x 128 groups) instead of [M]
+    const uint16_t* xb;      // fused X (FP8 per-tensor): bf16 activations [M <= 128, K], row pitch K
 };
 
 __device__ __forceinline__ void record_timeout(int* status, volatile uint32_t* abort_flag) {
@@ -280,7 +293,8 @@ __global__ void __launch_bounds__(Cfg<KIND>::THREADS, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; s++) {
-            mbar_init(full + s, C::CVT ? C::CVT_WARPS : 1);   // TMA, or the converter warps
+            // TMA; or the converter warps (INT8); or TMA plus the epilogue warps (fused X)
+            mbar_init(full + s, C::CVT ? C::CVT_WARPS : (C::QX ? 1 + C::EPI_WARPS : 1));
             mbar_init(empty + s, 1);
         }
         for (int s = 0; s < C::S8; s++) {
@@ -345,7 +359,7 @@ __global__ void __launch_bounds__(Cfg<KIND>::THREADS, 1)
         for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
             int m0, n0;
             tile_coords<C::BN>(tile, tiles_m, tiles_n, m0, n0);
-            uint32_t bytes = C::A_BYTES + C::B_BYTES;
+            uint32_t bytes = (C::QX ? 0 : C::A_BYTES) + C::B_BYTES;   // fused X: the A stage is written on chip
             if (C::SF_CHUNKS) {
                 bytes += C::SFA_BYTES;
                 for (int j = 0; j < C::BN / 128; j++)
@@ -360,7 +374,7 @@ __global__ void __launch_bounds__(Cfg<KIND>::THREADS, 1)
                     break;
                 }
                 mbar_arrive_expect_tx(full + s, bytes);
-                tma_load_2d(smem + C::OFF_A + s * C::A_BYTES, &tmA, kb * BKB, m0, full + s);
+                if (!C::QX) tma_load_2d(smem + C::OFF_A + s * C::A_BYTES, &tmA, kb * BKB, m0, full + s);
                 tma_load_2d(smem + C::OFF_B + s * C::B_BYTES, &tmB, kb * BKB, n0, full + s);
                 if (C::SF_CHUNKS) {
                     bulk_load(smem + C::OFF_SFA + s * C::SFA_BYTES,
@@ -435,7 +449,7 @@ __global__ void __launch_bounds__(Cfg<KIND>::THREADS, 1)
                     const uint64_t ad = sdesc_sw128(a_base + c * 32);
                     const uint64_t bd = sdesc_sw128(b_base + c * 32);
                     const uint32_t acc = (KIND == kFp8Block) ? (c > 0) : (kb > 0 || c > 0);
-                    if (KIND == kFp8Tensor || KIND == kFp8Block) {
+                    if (KIND == kFp8Tensor || KIND == kFp8Block || KIND == kFp8QX) {
                         mma_f8f6f4(d, ad, bd, idesc, acc);
                     } else if (KIND == kInt8) {
                         mma_f16(d, ad, bd, idesc, acc);
@@ -509,13 +523,111 @@ __global__ void __launch_bounds__(Cfg<KIND>::THREADS, 1)
         float alpha = 1.0f;
         if (KIND == kFp8Tensor) alpha = __fmul_rn(__ldg(p.x_scale), __ldg(p.w_scale));
         if (KIND == kNvfp4) alpha = __fmul_rn(__ldg(p.x_global), __ldg(p.w_global));
-        uint32_t it = 0, kbg = 0;
+        const int et = (warp - 4) * 32 + lane;  // fused X: this thread among the 256 epilogue threads
+        float rx = 1.0f;                        // fused X: the code multiplier 448 / amax
+        if constexpr (C::QX) {
+            // Tensor amax of X (M <= 128 rows, all of them in this CTA's A tile),
+            // 32 vectors in flight per thread, then over the eight warps.
+            const uint32_t nvr = (uint32_t)(p.K >> 3), nvec = (uint32_t)p.M * nvr;
+            float a = 0.0f;
+            for (uint32_t v0 = (uint32_t)et; v0 < nvec; v0 += 256u * 32u) {
+                uint4 t[32];
+#pragma unroll
+                for (int j = 0; j < 32; j++) {
+                    const uint32_t v = v0 + (uint32_t)j * 256u;
+                    if (v < nvec) {
+                        const uint32_t r = v / nvr;
+                        t[j] = __ldg(reinterpret_cast<const uint4*>(p.xb + (int64_t)r * p.K + (int64_t)(v - r * nvr) * 8));
+                    } else {
+                        t[j] = make_uint4(0, 0, 0, 0);
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < 32; j++) {
+                    const uint32_t w[4] = {t[j].x, t[j].y, t[j].z, t[j].w};
+#pragma unroll
+                    for (int e = 0; e < 4; e++)
+                        a = fmaxf(a, fmaxf(fabsf(__uint_as_float(w[e] << 16)), fabsf(__uint_as_float(w[e] & 0xFFFF0000u))));
+                }
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
+            if (lane == 0) misc[4 + (warp - 4)] = __float_as_uint(a);
+            asm volatile("bar.sync 1, 256;" ::: "memory");   // the eight epilogue warps
+#pragma unroll
+            for (int w = 0; w < C::EPI_WARPS; w++) a = fmaxf(a, __uint_as_float(misc[4 + w]));
+            // the per-tensor FP8 granule: s = amax / 448, codes E4M3(x * (448 / amax))
+            float sx = 1.0f;
+            if (a != 0.0f) {
+                sx = __fdiv_rn(a, 448.0f);
+                rx = __fdiv_rn(448.0f, a);
+            }
+            alpha = __fmul_rn(sx, __ldg(p.w_scale));
+        }
+        uint32_t it = 0, kbg = 0, kq = 0;
         for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, it++) {
             int m0, n0;
             tile_coords<C::BN>(tile, tiles_m, tiles_n, m0, n0);
             const int row = m0 + q * 32 + lane;
             const int ncol = n0 + h * 128;
             bool ok = true;
+            if constexpr (C::QX) {
+                // Quantize this tile's X blocks (128 rows x 128 K bf16 -> E4M3) into
+                // the A stages: thread et takes 16-code chunk et & 7 of rows
+                // et / 8 + 32 i, i = 0..3, stored at chunk position c ^ (row & 7)
+                // (the 128-byte swizzle); the loads run two blocks ahead.
+                const int c = et & 7, sw = (et >> 3) & 7;
+                auto load_x = [&](int kb, uint4 (&d)[8]) {
+                    const int k = kb * 128 + c * 16;
+#pragma unroll
+                    for (int i = 0; i < 4; i++) {
+                        const int r = m0 + i * 32 + (et >> 3);
+                        const bool in = r < p.M && k < p.K;
+                        const uint16_t* src = p.xb + (int64_t)r * p.K + k;
+                        d[2 * i] = in ? __ldg(reinterpret_cast<const uint4*>(src)) : make_uint4(0, 0, 0, 0);
+                        d[2 * i + 1] = in ? __ldg(reinterpret_cast<const uint4*>(src + 8)) : make_uint4(0, 0, 0, 0);
+                    }
+                };
+                uint4 nv[8], nv2[8];
+                load_x(0, nv);
+                if (p.nk > 1) load_x(1, nv2);
+                for (int kb = 0; kb < p.nk; kb++, kq++) {
+                    uint4 cv[8];
+#pragma unroll
+                    for (int i = 0; i < 8; i++) {
+                        cv[i] = nv[i];
+                        nv[i] = nv2[i];
+                    }
+                    if (kb + 2 < p.nk) load_x(kb + 2, nv2);
+                    const int s = (int)(kq % C::STAGES);
+                    if (!warp_wait_or_abort(empty + s, ((kq / C::STAGES) & 1u) ^ 1u, abort_flag)) {
+                        if (lane == 0) record_timeout(p.status, abort_flag);
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* a_st = smem + C::OFF_A + s * C::A_BYTES;
+#pragma unroll
+                    for (int i = 0; i < 4; i++) {
+                        const uint32_t w[8] = {cv[2 * i].x, cv[2 * i].y, cv[2 * i].z, cv[2 * i].w,
+                                               cv[2 * i + 1].x, cv[2 * i + 1].y, cv[2 * i + 1].z, cv[2 * i + 1].w};
+                        uint32_t o[4];
+#pragma unroll
+                        for (int j = 0; j < 4; j++) {
+                            const uint32_t lo = cvt_e4m3x2(__fmul_rn(__uint_as_float(w[2 * j] << 16), rx),
+                                                           __fmul_rn(__uint_as_float(w[2 * j] & 0xFFFF0000u), rx));
+                            const uint32_t hi = cvt_e4m3x2(__fmul_rn(__uint_as_float(w[2 * j + 1] << 16), rx),
+                                                           __fmul_rn(__uint_as_float(w[2 * j + 1] & 0xFFFF0000u), rx));
+                            o[j] = lo | (hi << 16);
+                        }
+                        const int r = i * 32 + (et >> 3);
+                        *reinterpret_cast<uint4*>(a_st + r * 128 + ((c ^ sw) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+                    }
+                    fence_proxy_async_smem();         // generic-proxy writes -> the MMA's async proxy
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(full + s);
+                }
+                if (!ok) break;
+            }
             if constexpr (C::CVT) {
                 // INT8: accumulator buffer it & 1, read in two 64-column halves
                 // (fewer registers) and released after the second
@@ -796,6 +908,10 @@ cudaError_t launch_tc(const GemmArgs& a, cudaStream_t st) {
         if (!make_tmap_u8(&tmA, a.x, kbytes, (uint64_t)a.M, kbytes, BM, C::K8, false) ||
             !make_tmap_u8(&tmB, a.w, kbytes, (uint64_t)a.N, kbytes, C::BN, C::K8, false))
             return cudaErrorInvalidValue;
+    } else if (C::QX) {
+        // fused X: no A tiles are loaded; tmA is a valid copy of the W map (only prefetched)
+        if (!make_tmap_u8(&tmB, a.w, kbytes, (uint64_t)a.N, kbytes, C::BN)) return cudaErrorInvalidValue;
+        tmA = tmB;
     } else {
         if (!make_tmap_u8(&tmA, a.x, kbytes, (uint64_t)a.M, kbytes, BM)) return cudaErrorInvalidValue;
         if (!make_tmap_u8(&tmB, a.w, kbytes, (uint64_t)a.N, kbytes, C::BN)) return cudaErrorInvalidValue;
@@ -829,6 +945,7 @@ cudaError_t launch_tc(const GemmArgs& a, cudaStream_t st) {
     p.y = a.y;
     p.status = a.dev_status;
     p.x_group = a.x_group128 ? 1 : 0;
+    p.xb = static_cast<const uint16_t*>(a.x);
     static bool attr_set = false;
     if (!attr_set) {
         // The in-kernel setmaxnreg split assumes the launch allocation of
@@ -869,6 +986,7 @@ cudaError_t launch_gemm_mxfp8(const GemmArgs& a, cudaStream_t st) { return launc
 cudaError_t launch_gemm_nvfp4(const GemmArgs& a, cudaStream_t st) { return launch_tc<kNvfp4>(a, st); }
 cudaError_t launch_gemm_mxfp4(const GemmArgs& a, cudaStream_t st) { return launch_tc<kMxfp4>(a, st); }
 cudaError_t launch_gemm_int8(const GemmArgs& a, cudaStream_t st) { return launch_tc<kInt8>(a, st); }
+cudaError_t launch_gemm_fp8_tensor_fused_x(const GemmArgs& a, cudaStream_t st) { return launch_tc<kFp8QX>(a, st); }
 
 cudaError_t launch_debug_expire_wait(int* dev_status, uint32_t max_polls, cudaStream_t st) {
     k_expire_wait<<<1, 32, 0, st>>>(dev_status, max_polls);

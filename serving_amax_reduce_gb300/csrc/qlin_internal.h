@@ -59,6 +59,8 @@ cudaError_t launch_gemm_mxfp8(const GemmArgs& a, cudaStream_t st);
 cudaError_t launch_gemm_nvfp4(const GemmArgs& a, cudaStream_t st);
 cudaError_t launch_gemm_mxfp4(const GemmArgs& a, cudaStream_t st);
 cudaError_t launch_gemm_int8(const GemmArgs& a, cudaStream_t st);
+// FP8 per-tensor weights x bf16 activations quantized per tensor inside the GEMM (M <= 128)
+cudaError_t launch_gemm_fp8_tensor_fused_x(const GemmArgs& a, cudaStream_t st);
 cudaError_t launch_gemm_w4a16(const GemmArgs& a, cudaStream_t st);
 size_t w4a16_workspace_bytes(int64_t M, int64_t N, int64_t K);
 

@@ -313,6 +313,14 @@ __device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t
     return d;
 }
 
+// Two fp32 -> two E4M3 codes (round to nearest even, saturating), `lo` in
+// bits 0..7.
+__device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
 // Byte permute: byte i of the result is byte sel[4i..4i+3] of the pair {b, a} (a = bytes 0-3).
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     uint32_t d;

@@ -92,6 +92,13 @@ def fp8_tensor_linear(M=128, K=1024, N=1024) -> Linear:
                   _seed(1, 0), _seed(1, 1), "normal", x_std=0.02, w_std=0.02)
 
 
+def fp8_tensor_fused_linear(M=128, K=1024, N=1024) -> Linear:
+    """The per-tensor FP8 linear with its activation quantization fused into the
+    GEMM: the same X and W as fp8_tensor_linear, X handed over in bf16."""
+    return Linear("fp8_tensor_fused_x", M, K, N, "bf16", "fp8_tensor",
+                  _seed(1, 0), _seed(1, 1), "normal", x_std=0.02, w_std=0.02)
+
+
 W4A16_SHAPES = [(4096, 4096), (4096, 12288), (12288, 4096)]   # (K, N)
 W4A16_M = [1, 16, 64]
 

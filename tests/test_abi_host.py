@@ -154,6 +154,9 @@ def test_gemm_rejects_bad_arguments(q):
     assert g(F.FP8_BLOCK128, F.FP8_GROUP128, 128, 1024, 1024, xs=None) == S.INVALID_ARG
     assert g(F.FP8_TENSOR, F.FP8_GROUP128, 128, 1024, 1024) == S.UNSUPPORTED
     assert g(F.FP8_TENSOR, F.FP8_TOKEN, 128, 1024, 1024) == S.UNSUPPORTED
+    assert g(F.FP8_TENSOR, F.BF16, 129, 1024, 1024) == S.UNSUPPORTED           # fused X: M <= 128
+    assert g(F.FP8_TENSOR, F.BF16, 128, 1024, 1000) == S.INVALID_ARG           # K % 16
+    assert g(F.FP8_TENSOR, F.BF16, 128, 1024, 1024, ws=None) == S.INVALID_ARG
     assert g(F.INT8_ROW, F.INT8_ROW, 128, 1024, 1000) == S.INVALID_ARG         # K % 16
     assert g(F.INT8_ROW, F.INT8_ROW, 128, 1024, 1024, ws=None) == S.INVALID_ARG
     assert g(F.INT8_ROW, F.FP8_TOKEN, 128, 1024, 1024) == S.UNSUPPORTED

@@ -111,6 +111,47 @@ def test_fp8_block_gemm_full_size(q, orc, B, K, N):
     fp8_block_case(q, orc, 4096 * B, N, K, nrows=256)
 
 
+# ------------------------------------------------------------------ FP8 per-tensor, X quantized inside the GEMM
+def fused_x_case(q, orc, M, N, K, with_bias=False, zero_x=False):
+    lin = inputs.fp8_tensor_linear(M, K, N)
+    x, w = lin.make_x(), lin.make_w()
+    if zero_x:
+        x = torch.zeros_like(x)
+    F = q.Fmt
+    xd = x.cuda()
+    bw = q.quantize_weight(F.FP8_TENSOR, w.cuda())
+    bias = inputs.normal_bf16((1, N), 0.05, 82)[0] if with_bias else None
+    bd = bias.cuda() if with_bias else None
+    y = q.gemm(F.FP8_TENSOR, F.BF16, M, N, K, xd, None, bw["codes"], bw["scales"], bias=bd)
+    # the same linear in two steps: quantize X, then the per-tensor GEMM
+    bx = q.quantize_act(F.FP8_TENSOR, xd)
+    y2 = q.gemm(F.FP8_TENSOR, F.FP8_TENSOR, M, N, K, bx["codes"], bx["scales"], bw["codes"], bw["scales"], bias=bd)
+    torch.cuda.synchronize()
+    assert torch.equal(y.view(torch.int16), y2.view(torch.int16)), "fused and two-step results differ"
+    # and against the oracle's own quantization of X
+    cx, sx = orc.quant_fp8_tensor(bits(x))
+    wh = orc.dequant_fp8_tensor(np_u8(bw["codes"]).reshape(N, K), np_f32(bw["scales"])[0])
+    b = orc.bf16_values(bits(bias)[None, :])[0] if with_bias else None
+    ref = orc.gemm_ref(orc.dequant_fp8_tensor(cx, sx), wh, bias=b)
+    if zero_x:
+        assert np.array_equal(y_np(y), np.broadcast_to(orc.bf16_values(bits(bias)[None, :]) if with_bias else 0.0,
+                                                       (M, N)))
+        return None
+    return check(orc, y_np(y), ref, x, w)
+
+
+# one row tile at single-request row counts; ragged N and K; K of one block
+@pytest.mark.parametrize("M,N,K", [(128, 1024, 1024), (1, 256, 128), (77, 640, 1040), (128, 12288, 3072),
+                                   (5, 320, 2048)])
+def test_fp8_tensor_fused_x_gemm(q, orc, M, N, K):
+    fused_x_case(q, orc, M, N, K)
+
+
+def test_fp8_tensor_fused_x_gemm_bias_and_zero(q, orc):
+    fused_x_case(q, orc, 100, 512, 384, with_bias=True)
+    fused_x_case(q, orc, 16, 256, 256, with_bias=True, zero_x=True)
+
+
 # ------------------------------------------------------------------ FP8 128x128 block W x 1x128 group X
 def fp8_group_case(q, orc, M, N, K, nrows=None, with_bias=False):
     lin = inputs.fp8_block_linear(1, K, N, M=M)
