@@ -9,7 +9,8 @@ Two layers:
 * ``qlin_oracle.c`` (built here into ``_build/liboracle.so`` with gcc, strict
   IEEE binary32, no contraction): scalar codecs and quantizers, written one
   element at a time from the format definitions.  See its header for the
-  readings R1..R8 taken where the pages name a format but print no formula.
+  readings R1..R5 and R11..R13 taken where the pages name a format but print no
+  formula.
 * this module: numpy marshalling, and the GEMM reference, which is the plain
   definition Y = Xhat @ What^T evaluated in float64 over the dequantized
   operands (``numpy.matmul`` as the one library step).

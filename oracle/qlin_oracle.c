@@ -27,7 +27,8 @@
  * and no division is turned into a reciprocal multiply.
  *
  * Readings where the pages leave the rule open (all of them, since the pages
- * print no formula):
+ * print no formula; R6-R10 are not arithmetic readings, they fix inputs,
+ * layouts and the pass rule):
  *   R1  FP8 dynamic granule: s = amax/448, codes = E4M3(x * (448/amax));
  *       amax == 0 gives s = 1 and multiplier 1.
  *   R2  MX shared exponent: e = clamp(floor(log2 amax) - 8, -127, 127)
@@ -42,17 +43,17 @@
  *       q = clamp(rint(x*r) + z); z stored without the "-1" offset.
  *   R5  conversions to E4M3/E2M1 round to nearest, ties to the even code,
  *       saturate to the largest finite magnitude and keep the sign of zero.
- *   R6  MXFP4 (the same page and section: the online MXFP4 path mirrors
+ *   R11 MXFP4 (the same page and section: the online MXFP4 path mirrors
  *       MXFP8 with float4_e2m1fn_x2 codes, two per byte): the R2 rule with
  *       the E2M1 exponent, e = clamp(floor(log2 amax) - 2, -127, 127)
  *       (2 = exponent of 6, the largest E2M1 power-of-two range), codes =
  *       E2M1(x * 2^-e) packed two per byte, lower K index in the low nibble;
  *       amax == 0 gives scale code 0.
- *   R7  dynamic FP8 128-group activations ("[vLLM] 기타 양자화", section
+ *   R12 dynamic FP8 128-group activations ("[vLLM] 기타 양자화", section
  *       "FP8: vLLM의 핵심 양자화", the block-128 dynamic symmetric scheme
  *       applied to activations): the R1 granule is 1 x 128, one token times
  *       128 consecutive K elements, with one fp32 scale per (row, K/128).
- *   R8  INT8 W8A8 ("vLLM-Omni 在线量化（Online Quantization）完全指南",
+ *   R13 INT8 W8A8 ("vLLM-Omni 在线量化（Online Quantization）完全指南",
  *       section "在线量化的底层工作原理": the CUDA online INT8 path makes
  *       the weight codes and their scales with a scaled int8 quantizer;
  *       section "核心参数详解": activations are dynamic only): symmetric
@@ -204,7 +205,7 @@ void oracle_quant_fp8_token(const uint16_t *x, int64_t rows, int64_t K, int64_t 
 
 /* One scale per 128 x 128 tile.  rows, K multiples of 128.
  * scales: (rows/128) x (K/128), row-major. */
-/* FP8 E4M3 with one dynamic scale per 1 x 128 group along K (R7)       */
+/* FP8 E4M3 with one dynamic scale per 1 x 128 group along K (R12)      */
 void oracle_quant_fp8_group128(const uint16_t *x, int64_t rows, int64_t K, int64_t ld,
                                uint8_t *codes, float *scales)
 {
@@ -276,7 +277,7 @@ void oracle_quant_mxfp8(const uint16_t *x, int64_t rows, int64_t K, int64_t ld,
 
 /* K multiple of 16.  packed codes: rows x (K/2) bytes (lower K index in the
  * low nibble); block scale codes: rows x (K/16); global: one float. */
-/* MXFP4: E2M1 codes + E8M0 exponent per 32 along K (R6)               */
+/* MXFP4: E2M1 codes + E8M0 exponent per 32 along K (R11)              */
 void oracle_quant_mxfp4(const uint16_t *x, int64_t rows, int64_t K, int64_t ld,
                         uint8_t *packed, uint8_t *scale_codes)
 {
@@ -384,7 +385,7 @@ void oracle_quant_int4_g128(const uint16_t *w, int64_t N, int64_t K, int64_t ld,
 }
 
 /* ------------------------------------------------------------------ */
-/* INT8 symmetric, one fp32 scale per row (R8)                          */
+/* INT8 symmetric, one fp32 scale per row (R13)                         */
 /* ------------------------------------------------------------------ */
 
 /* codes: rows x K int8, row-major; scales: rows.  A row is one token of X or
