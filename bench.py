@@ -239,25 +239,36 @@ class Job:
 # DRAM traffic (read + write bytes) of one captured launch of the dominant
 # kernel, from the ncu summary in profiles/gemm_fp8_block_M4096_K3072_N12288.md.
 # It is scaled to the step's average launch by algorithmic bytes, and reported
-# as null once the kernel's source differs from the one the counters came from.
+# as null once the kernel's code (comments and whitespace aside) differs from
+# the code the counters came from.
 MEASURED_TRAFFIC = {
     "gemm_fp8_block": {
         "dram_bytes": 79162624 + 57511936,
         "alg_bytes": 4096 * 3072 + 4096 * 4 + 12288 * 3072 + 96 * 24 * 4 + 4096 * 12288 * 2,
         "source": "serving_amax_reduce_gb300/csrc/gemm_tc.cu",
-        "sha256": "0b6d8801f2c1049cfb3ae6dd9ad68419672912e375c7e4d707fa61b70e9fc970",
+        "code_sha256": "ae38fa4fbcc39dba74fdd5189f997f9cc49753a5628ae7a4e19fd92173096a58",
         "captured": "M4096 K3072 N12288 (one bench launch)",
     },
 }
 
 
-def measured_traffic(kernel, alg_bytes_per_launch):
+def code_fingerprint(path: str) -> str:
+    """sha256 of a C++/CUDA source with its comments and whitespace removed:
+    it changes when the code changes, not when a comment is edited."""
     import hashlib
+    import re
+    text = open(path, encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return hashlib.sha256(" ".join(text.split()).encode()).hexdigest()
+
+
+def measured_traffic(kernel, alg_bytes_per_launch):
     m = MEASURED_TRAFFIC.get(kernel)
     if not m:
         return None, None
     path = os.path.join(ROOT, m["source"])
-    if not os.path.exists(path) or hashlib.sha256(open(path, "rb").read()).hexdigest() != m["sha256"]:
+    if not os.path.exists(path) or code_fingerprint(path) != m["code_sha256"]:
         return None, "kernel changed since the counters were taken"
     return int(round(m["dram_bytes"] * alg_bytes_per_launch / m["alg_bytes"])), \
         f"ncu capture of {m['captured']}, scaled by algorithmic bytes"

@@ -43,12 +43,13 @@
 //   INT8 (W8A8)     the online INT8 path of the same page, per-token X and
 //                   per-channel W scales.  sm_103a has no integer MMA, so TMA
 //                   stages the int8 tiles (64 K per stage) in a ring of their
-//                   own and warps 12-15 (a fourth warpgroup) turn every code
+//                   own and warps 12-19 (two more warpgroups) turn every code
 //                   into the fp16 value of the same integer (q ^ 0x80 placed
 //                   in the mantissa of 1024, minus 1152: exact) in the
 //                   128-byte-swizzled layout the MMA reads; kind::f16 then
-//                   multiplies exact integers with fp32 accumulation, and the
-//                   epilogue applies s_x[m] * s_w[n].
+//                   multiplies exact integers with fp32 accumulation into one of
+//                   two TMEM accumulators, and the epilogue applies
+//                   s_x[m] * s_w[n].
 //   FP8 per-tensor  with the activation quantization fused into the GEMM (the
 //   fused X         producer quantizes the X tile): for M <= 128 (one row tile,
 //                   the single-request shapes) X arrives in bf16.  The eight
@@ -760,7 +761,7 @@ __global__ void __launch_bounds__(Cfg<KIND>::THREADS, 1)
         if constexpr (C::CVT) {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::REGS_CVT));
         if (!skip) {
-            // ------------------------------------------------ int8 -> fp16 converters (4 warps)
+            // ------------------------------------------------ int8 -> fp16 converters (8 warps)
             // A stage holds 384 rows (128 of X, 256 of W) of 64 int8 = 4 chunks
             // of 16 codes; thread ct (0..255) takes chunk ct & 3 of rows
             // ct / 4 + 64 i, i = 0..5 (8 rows per warp per round: 128 contiguous
