@@ -342,7 +342,7 @@ __global__ void __launch_bounds__(256) k_fp8_block128(const uint16_t* __restrict
 // Row tasks: a task's 32 vectors are two 128-element groups of one row, 16
 // lanes each; the group amax comes from four xor-shuffles inside the 16 lanes.
 // K % 128 == 0, so a group is entirely inside or outside the row.
-__global__ void __launch_bounds__(256) k_fp8_group128(const uint16_t* __restrict__ x, int64_t rows, int64_t K,
+__global__ void __launch_bounds__(256, 6) k_fp8_group128(const uint16_t* __restrict__ x, int64_t rows, int64_t K,
                                                       int64_t ld, uint8_t* __restrict__ codes,
                                                       float* __restrict__ scales) {
     const uint32_t nvr = (uint32_t)(K >> 3), tpr = (nvr + 31) / 32, total = (uint32_t)rows * tpr;
@@ -379,7 +379,7 @@ __global__ void __launch_bounds__(256) k_fp8_group128(const uint16_t* __restrict
 // codes.  Every lane of a warp runs the same trip count (the shuffles use the
 // full mask); a task never splits a granule.
 template <bool FP4>
-__global__ void __launch_bounds__(256) k_mx(const uint16_t* __restrict__ x, int64_t rows, int64_t rows_pad,
+__global__ void __launch_bounds__(256, 6) k_mx(const uint16_t* __restrict__ x, int64_t rows, int64_t rows_pad,
                                             int64_t K, int64_t ld, uint8_t* __restrict__ codes,
                                             uint8_t* __restrict__ scales, int mma) {
     constexpr int kEmax = FP4 ? 2 : 8;
@@ -558,6 +558,10 @@ int sm_count() {
 }
 
 // Grids of a task walk (8 warps per CTA, kUnroll tasks per warp per round).
+// k_mx and k_fp8_group128 are capped at 40 registers (6 CTAs per SM, a few
+// bytes of spill), which made them 1.5 % and 10 % faster than at 46-51
+// registers (4-5 CTAs per SM); the same cap made the NVFP4 encode pass 2 %
+// slower, so that one is not capped.
 // Kernels without a per-CTA prologue launch one round per CTA: the block
 // scheduler refills an SM as its CTAs retire, so new loads start while older
 // CTAs encode and store.  The two encode passes that begin by folding the
