@@ -432,6 +432,232 @@ __global__ void __launch_bounds__(W4Cfg<MP>::THREADS, 1)
     }
 }
 
+// ---------------------------------------------------------------- M <= 16: warp-level MMA
+// At 16 tokens each tcgen05 MMA of the kernel above has N = 16 and the tensor
+// pipe is bound by its per-instruction cost.  This variant keeps the weights in
+// registers: each lane turns int4 codes into exact bf16 (q - z) values (the
+// same 0x4300 trick) and feeds them straight to mma.sync.m16n8k16 (tokens =
+// the MMA's 16 rows, 8 channels per instruction), so no operand goes through
+// shared or tensor memory and no weight tile waits on a barrier.
+//
+// CTA = 128 channels x this cluster rank's 128-K groups; 8 warps: warp w takes
+// the 32 channels (w & 3) * 32 and the groups of parity w >> 2.  In a warp,
+// lane group c4 = lane / 4 owns the 4 consecutive channels 4 c4 + t, one per
+// n8 tile t (MMA column c4 of tile t), so its weights come as one 16-byte
+// load per 8-K octet.  For a 16-K step the B fragment of lane q = lane % 4
+// needs 4 codes: they are taken from octet q / 2 as the pairs (j, j + 4) and
+// (j + 1, j + 5), j = 2 (q % 2); X is staged with every 8-K octet in the order
+// 0 4 1 5 2 6 3 7, which puts the four matching A values of a row at positions
+// 4q .. 4q + 3 (one 8-byte load), the same logical K order on both sides.
+// Split-K runs over the cluster exactly as above.
+constexpr int kXRow = 144;          // bf16 per staged X row: 128 + 16 (8-byte A loads hit 32 banks)
+constexpr int kWRow = 136;          // 32-bit words per staged weight octet row: 128 + 8 (conflict-free 16-byte reads)
+constexpr int kWPairs = 3;          // weight ring depth, in pairs of groups
+constexpr int kMmaSmem = (2 * 2 * 16 * kXRow) * 2 + 16 * 128 * 4 + (2 * kWPairs) * 16 * kWRow * 4;
+
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                          uint32_t b0, uint32_t b1) {
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+                 "{%0,%1,%2,%3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// 16 bytes global -> shared, bypassing L1; src_bytes 0 fills zeros.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// Codes in bits [sh, sh + 4) and [sh + 16, sh + 20) minus the zero point: an
+// exact bf16 pair.
+__device__ __forceinline__ uint32_t dq_pair(uint32_t w, int sh, __nv_bfloat162 bias2) {
+    const uint32_t v = lop3_and_or(w >> sh, 0x000F000Fu, 0x43004300u);
+    __nv_bfloat162 h = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&v), bias2);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+struct W4MmaParams {
+    int M, N, K, groups;
+    int64_t ldy;
+    const int32_t* qweight;   // [K/8, N]
+    const uint16_t* x;        // bf16 [M, K]
+    const uint16_t* scales;   // bf16 [K/128, N]
+    const int32_t* qzeros;    // [K/128, N/8]
+    const uint16_t* bias;
+    uint16_t* y;
+};
+
+__global__ void __launch_bounds__(256, 2) k_w4a16_mma(const W4MmaParams p) {
+    extern __shared__ __align__(16) uint8_t smem_mma[];
+    uint16_t* xs = reinterpret_cast<uint16_t*>(smem_mma);                         // [2 buf][2 parity][16][kXRow]
+    float* red = reinterpret_cast<float*>(smem_mma + 2 * 2 * 16 * kXRow * 2);      // [16][128]
+    uint32_t* wsm = reinterpret_cast<uint32_t*>(smem_mma + 2 * 2 * 16 * kXRow * 2 + 16 * 128 * 4);  // [slot][16][kWRow]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
+    const int slice = warp & 3, par = warp >> 2, c4 = lane >> 2, q = lane & 3;
+    const int cs = (int)gridDim.x, rank = (int)cluster_ctarank();
+    const int n0 = (int)blockIdx.y * 128, m0 = (int)blockIdx.z * 16;
+    const int g0 = rank * p.groups / cs, g1 = (rank + 1) * p.groups / cs;
+    const int npairs = (g1 - g0 + 1) / 2;
+    const int chb = n0 + slice * 32 + 4 * c4;           // this lane's 4 B-fragment channels
+    const bool bok = chb < p.N;                          // N % 8 == 0: all 4 or none
+    const int chs = n0 + slice * 32 + 8 * q;             // the 8 channels of this lane's C columns
+    const int sh0 = 8 * (q & 1);                         // pair (j, j + 4), j = 2 (q % 2)
+
+    // X of a pair of groups (16 rows x 16 octets each), two octets per thread
+    auto load_x = [&](int pr, uint4 (&xv)[2]) {
+#pragma unroll
+        for (int j = 0; j < 2; j++) {
+            const int idx = tid + 256 * j, pa = idx >> 8, row = (idx >> 4) & 15, oct = idx & 15;
+            const int g = g0 + 2 * pr + pa;
+            const bool in = g < g1 && m0 + row < p.M;
+            xv[j] = in ? __ldg(reinterpret_cast<const uint4*>(p.x + (int64_t)(m0 + row) * p.K + g * 128 + oct * 8))
+                       : make_uint4(0, 0, 0, 0);
+        }
+    };
+    auto store_x = [&](int buf, const uint4 (&xv)[2]) {
+#pragma unroll
+        for (int j = 0; j < 2; j++) {
+            const int idx = tid + 256 * j, pa = idx >> 8, row = (idx >> 4) & 15, oct = idx & 15;
+            *reinterpret_cast<uint4*>(xs + ((buf * 2 + pa) * 16 + row) * kXRow + oct * 8) = permute_x_chunk(xv[j]);
+        }
+    };
+    // weights of a pair of groups into ring slots: 2 x 16 octet rows x 32 chunks of 16 bytes
+    auto issue_w = [&](int pp) {
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+            const int c = tid + 256 * j, pa = c >> 9, row = (c >> 5) & 15, cc = c & 31;
+            const int g = g0 + 2 * pp + pa, slot = 2 * (pp % kWPairs) + pa;
+            const bool in = g < g1 && n0 + cc * 4 < p.N;
+            const int32_t* src = p.qweight + (int64_t)(in ? g * 16 + row : 0) * p.N + (in ? n0 + cc * 4 : 0);
+            cp_async16(wsm + (slot * 16 + row) * kWRow + cc * 4, src, in ? 16u : 0u);
+        }
+        cp_async_commit();
+    };
+
+    float acc[4][4];
+#pragma unroll
+    for (int t = 0; t < 4; t++)
+#pragma unroll
+        for (int i = 0; i < 4; i++) acc[t][i] = 0.0f;
+
+#pragma unroll
+    for (int pp = 0; pp < kWPairs; pp++) issue_w(pp);   // empty pairs still commit, keeping the count
+    uint4 xv[2];
+    load_x(0, xv);
+    store_x(0, xv);
+    if (npairs > 1) load_x(1, xv);
+    for (int pr = 0; pr < npairs; pr++) {
+        const int g = g0 + 2 * pr + par;
+        const int buf = pr & 1;
+        cp_async_wait<kWPairs - 1>();                     // this pair's weights have landed
+        __syncthreads();
+        // this group's zero points (B channels) and scales (C columns)
+        __nv_bfloat162 zb[4];
+        float sc[8];
+        {
+            const bool gin = g < g1;
+            const uint32_t zw = (bok && gin) ? (uint32_t)__ldg(p.qzeros + (int64_t)g * (p.N / 8) + chb / 8) : 0u;
+#pragma unroll
+            for (int t = 0; t < 4; t++) {
+                const uint16_t zbits = (uint16_t)(0x4300u | ((zw >> (4 * ((chb & 7) + t))) & 0xFu));
+                zb[t] = __halves2bfloat162(__ushort_as_bfloat16(zbits), __ushort_as_bfloat16(zbits));
+            }
+            const uint4 sv = (gin && chs < p.N) ? __ldg(reinterpret_cast<const uint4*>(p.scales + (int64_t)g * p.N + chs))
+                                                : make_uint4(0, 0, 0, 0);
+            const uint32_t s2[4] = {sv.x, sv.y, sv.z, sv.w};
+#pragma unroll
+            for (int i = 0; i < 4; i++) {
+                sc[2 * i] = __uint_as_float(s2[i] << 16);
+                sc[2 * i + 1] = __uint_as_float(s2[i] & 0xFFFF0000u);
+            }
+        }
+        float cg[4][4];
+#pragma unroll
+        for (int t = 0; t < 4; t++)
+#pragma unroll
+            for (int i = 0; i < 4; i++) cg[t][i] = 0.0f;
+        const uint16_t* xr = xs + (buf * 2 + par) * 16 * kXRow;
+        const uint32_t* wr = wsm + (2 * (pr % kWPairs) + par) * 16 * kWRow + (slice * 32 + 4 * c4);
+#pragma unroll
+        for (int st = 0; st < 8; st++) {
+            const uint2 ar0 = *reinterpret_cast<const uint2*>(xr + c4 * kXRow + 16 * st + 4 * q);
+            const uint2 ar1 = *reinterpret_cast<const uint2*>(xr + (c4 + 8) * kXRow + 16 * st + 4 * q);
+            const uint4 wv = *reinterpret_cast<const uint4*>(wr + (2 * st + (q >> 1)) * kWRow);
+            const uint32_t w4[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+            for (int t = 0; t < 4; t++) {
+                const uint32_t b0 = dq_pair(w4[t], sh0, zb[t]);
+                const uint32_t b1 = dq_pair(w4[t], sh0 + 4, zb[t]);
+                mma_16816(cg[t], ar0.x, ar1.x, ar0.y, ar1.y, b0, b1);
+            }
+        }
+        // C columns 2q, 2q + 1 of tile t are channels chs + t and chs + 4 + t
+#pragma unroll
+        for (int t = 0; t < 4; t++) {
+            acc[t][0] += cg[t][0] * sc[t];
+            acc[t][1] += cg[t][1] * sc[4 + t];
+            acc[t][2] += cg[t][2] * sc[t];
+            acc[t][3] += cg[t][3] * sc[4 + t];
+        }
+        // stage the next pair's X (the buffer read two pairs ago is free since the barrier above)
+        if (pr + 1 < npairs) store_x(buf ^ 1, xv);
+        if (pr + 2 < npairs) load_x(pr + 2, xv);
+        __syncthreads();                                  // this pair's weight slots are free
+        issue_w(pr + kWPairs);
+    }
+    cp_async_wait<0>();
+
+    // the two group parities into one partial tile: rows c4 and c4 + 8
+    const int cb = slice * 32 + 8 * q;
+    if (par == 0) {
+#pragma unroll
+        for (int t = 0; t < 4; t++) {
+            red[c4 * 128 + cb + t] = acc[t][0];
+            red[c4 * 128 + cb + 4 + t] = acc[t][1];
+            red[(c4 + 8) * 128 + cb + t] = acc[t][2];
+            red[(c4 + 8) * 128 + cb + 4 + t] = acc[t][3];
+        }
+    }
+    __syncthreads();
+    if (par == 1) {
+#pragma unroll
+        for (int t = 0; t < 4; t++) {
+            red[c4 * 128 + cb + t] += acc[t][0];
+            red[c4 * 128 + cb + 4 + t] += acc[t][1];
+            red[(c4 + 8) * 128 + cb + t] += acc[t][2];
+            red[(c4 + 8) * 128 + cb + 4 + t] += acc[t][3];
+        }
+    }
+    __syncthreads();
+    // split-K over the cluster: CTA `rank` sums columns [rank*128/cs, (rank+1)*128/cs)
+    if (cs > 1) cluster_sync_all();
+    const int col0 = rank * 128 / cs, col1 = (rank + 1) * 128 / cs, width = col1 - col0;
+    const uint32_t red_s = smem_u32(red);
+    for (int idx = tid; idx < 16 * width; idx += 256) {
+        const int m = idx / width, n = col0 + idx % width;
+        float v = 0.0f;
+        if (cs > 1) {
+            const uint32_t off = red_s + (uint32_t)((m * 128 + n) * 4);
+            float part[8];
+#pragma unroll
+            for (int r = 0; r < 8; r++) part[r] = (r < cs) ? ld_peer_f32(off, (uint32_t)r) : 0.0f;
+#pragma unroll
+            for (int r = 0; r < 8; r++) v += part[r];
+        } else {
+            v = red[m * 128 + n];
+        }
+        if (m0 + m < p.M && n0 + n < p.N) {
+            const float b = p.bias ? __bfloat162float(__ushort_as_bfloat16(p.bias[n0 + n])) : 0.0f;
+            p.y[(int64_t)(m0 + m) * p.ldy + n0 + n] = __bfloat16_as_ushort(__float2bfloat16_rn(v + b));
+        }
+    }
+    if (cs > 1) cluster_sync_all();
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     if (!fn) {
@@ -523,7 +749,53 @@ cudaError_t launch_mp(const GemmArgs& a, cudaStream_t st) {
 
 size_t w4a16_workspace_bytes(int64_t, int64_t, int64_t) { return 0; }
 
+// Split-K ways (cluster size, 1..8, not only powers of two) for the warp-level
+// kernel: as many as fit one wave of two CTAs per SM, with at least two
+// 128-K groups per CTA.
+int pick_split_mma(int64_t tiles, int64_t groups) {
+    int cs = 1;
+    while (cs < 8 && tiles * (cs + 1) <= 2 * kNumSMs && groups >= 2 * (cs + 1)) cs++;
+    return cs;
+}
+
+cudaError_t launch_w4a16_mma(const GemmArgs& a, cudaStream_t st) {
+    W4MmaParams p{};
+    p.M = (int)a.M;
+    p.N = (int)a.N;
+    p.K = (int)a.K;
+    p.groups = (int)(a.K / 128);
+    p.ldy = a.ldy;
+    p.qweight = static_cast<const int32_t*>(a.w);
+    p.x = static_cast<const uint16_t*>(a.x);
+    p.scales = static_cast<const uint16_t*>(a.w_scales);
+    p.qzeros = static_cast<const int32_t*>(a.w_zeros);
+    p.bias = a.bias;
+    p.y = a.y;
+    const int64_t ntiles = (a.N + 127) / 128, mtiles = (a.M + 15) / 16;
+    const int cs = pick_split_mma(ntiles * mtiles, p.groups);
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(k_w4a16_mma, cudaFuncAttributeMaxDynamicSharedMemorySize, kMmaSmem);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)cs, (unsigned)ntiles, (unsigned)mtiles);
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = kMmaSmem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)cs;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k_w4a16_mma, p);
+}
+
 cudaError_t launch_gemm_w4a16(const GemmArgs& a, cudaStream_t st) {
+    if (a.M <= 16) return launch_w4a16_mma(a, st);
     switch (pick_mp(a.M)) {
         case 16: return launch_mp<16>(a, st);
         case 32: return launch_mp<32>(a, st);
