@@ -5,8 +5,11 @@
 //
 //   Y[m, n] = sum_g s[g, n] * sum_{k in g} x[m, k] * (q[k, n] - z[g, n])
 //
-// Decode has few tokens, so the output channels take the MMA's M side
-// ("swap AB"): a CTA owns 128 channels and MP tokens (MP = 16, 32 or 64,
+// Two kernels.  For M <= 16, k_w4a16_mma (further down) dequantizes in
+// registers and feeds warp-level mma.sync: at 16 tokens a tcgen05 MMA has
+// N = 16 and the tensor pipe is bound by its per-instruction cost.  For larger
+// M, k_w4a16 below runs tcgen05 with the output channels on the MMA's M side
+// ("swap AB"): a CTA owns 128 channels and MP tokens (MP = 32 or 64,
 // zero-filled past M by TMA; larger M runs as several token tiles).
 // Per 128-K group:
 //   warp 0    TMA: the packed int4 words (16 k-octets x 128 channels, 8 KB)
