@@ -69,7 +69,7 @@ struct W4Cfg {
     // the A stage and the X slot and announces the partial (the tensor pipe
     // takes a commit about as slowly as a small MMA).  R is even, so that each
     // slot always belongs to the same one of the two MMA issuers.
-    static constexpr int R = (MP == 16) ? 6 : 4;
+    static constexpr int R = 4;
     static constexpr int RA = R, RP = R, XS = R;
     static constexpr int QS = (MP <= 32) ? 16 : 12;                 // weight ring depth (groups)
     static constexpr int OFF_QW = 0;                                // weight ring
@@ -674,8 +674,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
+// Token tile of the tcgen05 kernel (M > 16; M <= 16 runs k_w4a16_mma).
 int pick_mp(int64_t M) {
-    if (M <= 16) return 16;
     if (M <= 32) return 32;
     return 64;                       // larger M runs as several 64-token tiles
 }
@@ -799,11 +799,7 @@ cudaError_t launch_w4a16_mma(const GemmArgs& a, cudaStream_t st) {
 
 cudaError_t launch_gemm_w4a16(const GemmArgs& a, cudaStream_t st) {
     if (a.M <= 16) return launch_w4a16_mma(a, st);
-    switch (pick_mp(a.M)) {
-        case 16: return launch_mp<16>(a, st);
-        case 32: return launch_mp<32>(a, st);
-        default: return launch_mp<64>(a, st);
-    }
+    return pick_mp(a.M) == 32 ? launch_mp<32>(a, st) : launch_mp<64>(a, st);
 }
 
 }  // namespace qlin
