@@ -437,17 +437,17 @@ __global__ void __launch_bounds__(W4Cfg<MP>::THREADS, 1)
 
 // ---------------------------------------------------------------- M <= 16: warp-level MMA
 // At 16 tokens each tcgen05 MMA of the kernel above has N = 16 and the tensor
-// pipe is bound by its per-instruction cost.  This variant keeps the weights in
-// registers: each lane turns int4 codes into exact bf16 (q - z) values (the
-// same 0x4300 trick) and feeds them straight to mma.sync.m16n8k16 (tokens =
-// the MMA's 16 rows, 8 channels per instruction), so no operand goes through
-// shared or tensor memory and no weight tile waits on a barrier.
+// pipe is bound by its per-instruction cost.  This variant dequantizes in
+// registers: the packed words stream through a cp.async ring in shared memory
+// (three pairs of groups ahead), each lane turns its int4 codes into exact
+// bf16 (q - z) values (the same 0x4300 trick) and feeds them straight to
+// mma.sync.m16n8k16 (tokens = the MMA's 16 rows, 8 channels per instruction).
 //
 // CTA = 128 channels x this cluster rank's 128-K groups; 8 warps: warp w takes
 // the 32 channels (w & 3) * 32 and the groups of parity w >> 2.  In a warp,
 // lane group c4 = lane / 4 owns the 4 consecutive channels 4 c4 + t, one per
 // n8 tile t (MMA column c4 of tile t), so its weights come as one 16-byte
-// load per 8-K octet.  For a 16-K step the B fragment of lane q = lane % 4
+// shared-memory read per 8-K octet.  For a 16-K step the B fragment of lane q = lane % 4
 // needs 4 codes: they are taken from octet q / 2 as the pairs (j, j + 4) and
 // (j + 1, j + 5), j = 2 (q % 2); X is staged with every 8-K octet in the order
 // 0 4 1 5 2 6 3 7, which puts the four matching A values of a row at positions
