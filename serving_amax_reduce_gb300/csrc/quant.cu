@@ -1,8 +1,9 @@
 // Online quantizers: bf16 -> FP8 E4M3 (tensor / token / 1x128 group /
 // 128x128 block), MXFP8, MXFP4, NVFP4, int4 g128 and INT8 per row.  Each
 // reads its bf16 input once from HBM in 16-byte vectors, reduces amax (or
-// min/max) with warp shuffles, and writes codes and scales in the same pass.  The per-tensor formats need the tensor
-// amax before any code exists, so they add one read-only amax pass.
+// min/max) with warp shuffles, and writes codes and scales in the same pass.
+// The per-tensor formats need the tensor amax before any code exists, so they
+// add one read-only amax pass.
 //
 // Formats: "[vLLM] 기타 양자화: FP8, ModelOpt, INC, TorchAO, Quark" section
 // "FP8: vLLM의 핵심 양자화" (tensor/token/block-128 dynamic scales);
