@@ -17,6 +17,10 @@ value = GEMM FLOPs of the step / device time of the step (TFLOP/s), inputs
 resident in HBM.  Every step streams several GB, far more than the 126 MB L2,
 so each input is evicted between its uses.
 
+--next measures the next rows instead: MXFP4 W4A4 on the mxfp8 shapes, FP8
+1x128-group activations and INT8 W8A8 on the fp8_block MLP shapes at M=4096,
+and the fp8_tensor linear with its activation quantization inside the GEMM.
+
 --impl reference times the CPU oracle (the slow reference implementation) on
 a bounded sample of the same workload.
 """
