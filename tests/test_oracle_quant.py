@@ -294,6 +294,36 @@ def test_nvfp4_dequant_close(orc):
     assert np.all(np.abs(xh - xv) <= bound)
 
 
+def test_nvfp4_worked_blocks(orc):
+    """Four blocks worked by hand.  The tensor amax is 448, so 448/A = 1 and
+    2688/A = 6 exactly, and g = fl(448/2688).
+    Block 0 holds the amax: scale E4M3(448) = 0x7E, multiplier fl(6/448); its
+    values sit far from E2M1 ties.  Block 1 (amax 12): scale E4M3(12) = 0x54,
+    multiplier 6/12 = 0.5 exactly, so every tie is a true tie and goes to the
+    even code; -0.5 -> -0.25 -> -0 keeps its sign.  Block 2 (amax 2^-20): the
+    scale rounds to 0 (below half the smallest UE4M3 subnormal), the
+    multiplier is 0 and the codes are signed zeros.  Block 3 (amax 2^-8): a
+    subnormal scale, code 0x02, multiplier 6/2^-8 = 1536."""
+    b0 = [448, 224, 112, -28, 0] + [0] * 11
+    b1 = [12, 5, -7, 1.5, 0.5, 10, -3, 2.5, -0.5] + [0] * 7
+    b2 = [2.0 ** -20, -2.0 ** -20] + [0] * 14
+    b3 = [2.0 ** -8, 2.0 ** -9, -2.0 ** -8] + [0] * 13
+    x = bf16_bits(torch.tensor([b0 + b1 + b2 + b3], dtype=torch.bfloat16))
+    packed, sc, g = orc.quant_nvfp4(x)
+    assert float(g) == float(np.float32(448) / np.float32(2688))
+    assert list(sc[0]) == [0x7E, 0x54, 0x00, 0x02]
+    codes = list(unpack_e2m1(packed)[0])
+    # block 0: 448 -> 6, 224 -> 3, 112 -> 1.5, -28 -> -0.375 -> nearest -0.5
+    assert codes[0:16] == [0x7, 0x5, 0x3, 0x9] + [0] * 12
+    # block 1 (x 0.5): 6; 2.5 tie 2|3 -> 2; -3.5 tie 3|4 -> 4; 0.75 tie 0.5|1 -> 1;
+    # 0.25 tie 0|0.5 -> 0; 5 tie 4|6 -> 4; -1.5; 1.25 tie 1|1.5 -> 1; -0.25 -> -0
+    assert codes[16:32] == [0x7, 0x4, 0xE, 0x2, 0x0, 0x6, 0xB, 0x2, 0x8] + [0] * 7
+    assert codes[32:48] == [0x0, 0x8] + [0] * 14
+    # block 3 (x 1536): 6, 3, -6
+    assert codes[48:64] == [0x7, 0x5, 0xF] + [0] * 13
+    assert packed[0, 8] == 0x4 << 4 | 0x7       # k = 16 low nibble, k = 17 high nibble
+
+
 # ------------------------------------------------------------------ MXFP4
 def test_mxfp4_shared_exponent_rule(orc):
     # OCP MX rule with the E2M1 element: scale = largest power of two <= amax,
@@ -459,6 +489,39 @@ def test_int4_exhaustive_code_roundtrip(orc):
     del rng, zero_col
 
 
+def test_int4_zero_point_and_codes_bruteforce(orc):
+    """Given the stored scale s (its value is pinned above), scan all 16
+    candidates for z and for every q: z is the candidate nearest to -min/s and
+    q - z the offset nearest to x/s, both with 1/s taken once in fp32, exact
+    rational distances, and ties to the even integer (-min/s and x/s)."""
+    N, K = 8, 256
+    w = bf16_bits(inputs.normal_bf16((N, K), 0.02, 65))
+    w[1, :128] = bf16_bits(torch.from_numpy(np.abs(vals(w[1:2, :128])) + 0.01).to(torch.bfloat16))[0]
+    w[2, 128:] = bf16_bits(torch.from_numpy(-np.abs(vals(w[2:3, 128:]))).to(torch.bfloat16))[0]
+    wv = vals(w)
+    qw, sc, qz = orc.quant_int4_g128(w)
+    q, z = unpack_int4(qw, qz, N, K)
+    s = vals(sc)
+
+    def nearest(t: Fraction, cands):
+        best = min(abs(c - t) for c in cands)
+        tied = [c for c in cands if abs(c - t) == best]
+        return tied[0] if len(tied) == 1 else [c for c in tied if c % 2 == 0][0]
+
+    for n in range(N):
+        for g in range(K // 128):
+            grp = wv[n, g * 128:(g + 1) * 128]
+            r = np.float32(1) / np.float32(s[g, n])
+            mn = min(0.0, grp.min())
+            zt = Fraction(float(np.float32(-mn) * r))
+            zb = nearest(zt, range(16))
+            assert z[g, n] == zb, (n, g)
+            for k in range(0, 128, 3):
+                # the offsets q - z that a code can take; outside them the nearest is the end (saturation)
+                t = Fraction(float(np.float32(grp[k]) * r))
+                assert q[g * 128 + k, n] == nearest(t, range(-zb, 16 - zb)) + zb, (n, g, k)
+
+
 # ------------------------------------------------------------------ INT8 per row
 def test_int8_worked_rows_ties_and_saturation(orc):
     """Rows chosen so that 127/amax is a power of two: x * r is exact and the
@@ -528,6 +591,39 @@ def test_int8_gemm_is_scaled_integer_product(orc):
     # each float64 product of two dequantized values rounds once (62 bits)
     mag = ss * (np.abs(cx.astype(np.int64)) @ np.abs(cw.astype(np.int64)).T)
     assert np.all(np.abs(y - expect) <= mag * K * 2.0 ** -52)
+
+
+# ------------------------------------------------------------------ every format
+MONOTONE_CASES = {
+    # name: (quantize, dequantize, length of the sorted runs along K)
+    "fp8_tensor": ("quant_fp8_tensor", "dequant_fp8_tensor", 64),
+    "fp8_token": ("quant_fp8_token", "dequant_fp8_token", 64),
+    "fp8_block128": ("quant_fp8_block128", "dequant_fp8_block128", 128),
+    "fp8_group128": ("quant_fp8_group128", "dequant_fp8_group128", 128),
+    "mxfp8": ("quant_mxfp8", "dequant_mxfp8", 32),
+    "mxfp4": ("quant_mxfp4", "dequant_mxfp4", 32),
+    "nvfp4": ("quant_nvfp4", "dequant_nvfp4", 16),
+    "int8_row": ("quant_int8_row", "dequant_int8_row", 64),
+    "int4_g128": ("quant_int4_g128", "dequant_int4_g128", 128),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MONOTONE_CASES))
+def test_dequant_of_quant_is_monotone(orc, name):
+    """Within one granule the scale is fixed and rounding to a grid is
+    monotone, so dequant(quant(x)) never decreases along sorted x.  Each run
+    is sorted in place: no granule's amax (nor min, for int4) changes.  A
+    wrong sign bit, a swapped nibble pair or a misplaced scale breaks it."""
+    qname, dname, run = MONOTONE_CASES[name]
+    R, K = 128, 512
+    x = bf16_bits(inputs.outlier_channel_bf16(R, K, 67))
+    order = np.argsort(vals(x).reshape(R, K // run, run), axis=-1, kind="stable")
+    xs = np.take_along_axis(x.reshape(R, K // run, run), order, axis=-1).reshape(R, K)
+    deq = getattr(orc, dname)(*getattr(orc, qname)(xs))
+    assert deq.shape == (R, K)
+    assert np.all(np.diff(deq.reshape(R, K // run, run), axis=-1) >= 0)
+    # and the runs hold values of both signs, so the check spans the sign boundary
+    assert (vals(xs) < 0).any() and (vals(xs) > 0).any()
 
 
 # ------------------------------------------------------------------ GEMM reference
