@@ -29,6 +29,7 @@ from __future__ import annotations
 import argparse
 import json
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -613,6 +614,28 @@ def blas_threads():
     return os.cpu_count()
 
 
+def host_cpu(cpuinfo: str = "/proc/cpuinfo") -> dict:
+    """The host the oracle ran on: logical CPUs and the CPU model as the
+    kernel reports it (x86 "model name"; on Arm the implementer and part
+    codes, e.g. 0x41 / 0xd4f for Arm Neoverse V2)."""
+    fields = {}
+    try:
+        with open(cpuinfo) as f:
+            for line in f:
+                if ":" in line:
+                    k, v = line.split(":", 1)
+                    fields.setdefault(k.strip(), v.strip())
+    except OSError:
+        pass
+    if fields.get("model name"):
+        model = fields["model name"]
+    elif "CPU implementer" in fields:
+        model = f"{platform.machine()} implementer {fields['CPU implementer']} part {fields.get('CPU part', '?')}"
+    else:
+        model = platform.processor() or platform.machine()
+    return {"cpu_count": os.cpu_count(), "cpu_model": model}
+
+
 def cpu_baseline():
     import oracle
     oracle.build()
@@ -628,7 +651,7 @@ def cpu_baseline():
             "sample": (f"{passes} passes over one linear per workload, X[:{SAMPLE_BASELINE[0]}] x "
                        f"W[:{SAMPLE_BASELINE[1]}] at full K ({flops / passes / 1e9:.0f} GFLOP per pass): scalar C "
                        "quantizers (1 thread) + float64 numpy matmul (BLAS threads)"),
-            "seconds": round(secs, 2)}
+            "seconds": round(secs, 2), "host": host_cpu()}
 
 
 def run_reference(args, rank, world):
@@ -651,7 +674,8 @@ def run_reference(args, rank, world):
             "data": "synthetic (seeded; bounded sample of the five workloads)", "config": config_block(args),
             "cpu_baseline": {"value": round(v, 6), "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
                              "sample": (f"per step: one linear per workload, X[:{SAMPLE_REFERENCE[0]}] x "
-                                        f"W[:{SAMPLE_REFERENCE[1]}] at full K")},
+                                        f"W[:{SAMPLE_REFERENCE[1]}] at full K"),
+                             "host": host_cpu()},
             "e2e": {"value": round(v, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 

@@ -25,3 +25,14 @@ def test_measured_traffic_matches_the_committed_kernel():
     assert bytes_ is not None, source
     assert 0 < bytes_ < 2 * 585209651
     assert bench.measured_traffic("no_such_kernel", 1) == (None, None)
+
+
+def test_host_cpu_reads_x86_and_arm_cpuinfo(tmp_path):
+    x86 = tmp_path / "x86"
+    x86.write_text("processor\t: 0\nmodel name\t: Some CPU @ 2.0GHz\n\nprocessor\t: 1\nmodel name\t: Some CPU @ 2.0GHz\n")
+    assert bench.host_cpu(str(x86))["cpu_model"] == "Some CPU @ 2.0GHz"
+    arm = tmp_path / "arm"
+    arm.write_text("processor\t: 0\nBogoMIPS\t: 2000.00\nCPU implementer\t: 0x41\nCPU part\t: 0xd4f\n")
+    got = bench.host_cpu(str(arm))
+    assert "implementer 0x41 part 0xd4f" in got["cpu_model"] and got["cpu_count"] >= 1
+    assert bench.host_cpu(str(tmp_path / "missing"))["cpu_model"]
