@@ -155,6 +155,8 @@ size_t qlin_gemm_workspace_bytes(qlin_format w_fmt, qlin_format x_fmt,
  *   layout             QLIN_SCALE_MMA is accepted for MXFP8, MXFP4 and NVFP4 only
  *   workspace_dev      qlin_quant_workspace_bytes(...) bytes (NULL if 0)
  * Requirements: src and ld*2 bytes 16-byte aligned; K % 8 == 0;
+ *   rows < 2^31, K < 2^31 and rows' * ceil(K/256) < 2^31, rows' being rows
+ *   rounded up to a multiple of 128 for the MMA layout (about 1 TB of bf16);
  *   FP8_BLOCK128: rows % 128 == 0 and K % 128 == 0; FP8_GROUP128: K % 128 == 0;
  *   MXFP8: K % 32 == 0
  *   (K % 128 == 0 for the MMA layout), the same for MXFP4; NVFP4: K % 16 == 0
@@ -203,11 +205,13 @@ qlin_status qlin_quantize_act(qlin_format fmt, const void *x_bf16_dev, int64_t M
  *                            below 2^24 in magnitude.
  *   INT4_G128_ASYM, BF16   : x = bf16 activations [M,K] row-major; w_codes
  *                            qweight, w_scales bf16, w_zeros qzeros (K % 128 == 0,
- *                            N % 8 == 0); workspace per qlin_gemm_workspace_bytes
+ *                            N % 8 == 0, N <= 65535*128, M <= 65535*64);
+ *                            workspace per qlin_gemm_workspace_bytes
  * Other pairs return QLIN_ERR_UNSUPPORTED.  All operand rows are contiguous
  * (leading dimension K, or K/2 bytes for NVFP4 / MXFP4 codes); ldy >= N and ldy*2
  * bytes 16-byte aligned.  M may be any value >= 1 (the row tail is handled
- * in the kernels; buffers are not padded).                                  */
+ * in the kernels; buffers are not padded).  M, N, K < 2^31 and
+ * ceil(M/128)*ceil(N/128) < 2^31; larger shapes return QLIN_ERR_INVALID_ARG. */
 qlin_status qlin_gemm(qlin_format w_fmt, qlin_format x_fmt, int64_t M, int64_t N, int64_t K,
                       const void *x_dev, const void *x_scales_dev, const float *x_global_dev,
                       const void *w_codes_dev, const void *w_scales_dev, const void *w_zeros_dev,

@@ -22,8 +22,11 @@ qlin_status launch_status(cudaError_t e) { return e == cudaSuccess ? QLIN_OK : Q
 
 // Shape rules per format (see qlin.h).
 qlin_status check_quant_shape(qlin_format fmt, qlin_scale_layout layout, int64_t rows, int64_t K) {
-    if (rows < 1 || K < 8 || (K & 7) || rows > 0x7FFFFFFFll) return QLIN_ERR_INVALID_ARG;
+    if (rows < 1 || K < 8 || (K & 7) || rows > 0x7FFFFFFFll || K > 0x7FFFFFFFll) return QLIN_ERR_INVALID_ARG;
     if (layout != QLIN_SCALE_CANONICAL && layout != QLIN_SCALE_MMA) return QLIN_ERR_INVALID_ARG;
+    // the element-wise walks number their 256-element row tasks in 32 bits
+    const int64_t rows_pad = layout == QLIN_SCALE_MMA ? ceil_div(rows, 128) * 128 : rows;
+    if (rows_pad * ceil_div(K, 256) > 0x7FFFFFFFll) return QLIN_ERR_INVALID_ARG;
     if (layout == QLIN_SCALE_MMA && fmt != QLIN_MXFP8 && fmt != QLIN_MXFP4 && fmt != QLIN_NVFP4)
         return QLIN_ERR_UNSUPPORTED;
     switch (fmt) {
@@ -188,7 +191,10 @@ qlin_status qlin_gemm(qlin_format w_fmt, qlin_format x_fmt, int64_t M, int64_t N
                       const void* bias_bf16_dev, void* y_bf16_dev, int64_t ldy, qlin_scale_layout layout,
                       void* workspace_dev, size_t workspace_bytes, int* dev_status_dev, qlin_stream_t stream) {
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if (M < 1 || N < 1 || K < 1 || M > 0x7FFFFFFFll || N > 0x7FFFFFFFll || ldy < N) return QLIN_ERR_INVALID_ARG;
+    if (M < 1 || N < 1 || K < 1 || M > 0x7FFFFFFFll || N > 0x7FFFFFFFll || K > 0x7FFFFFFFll || ldy < N)
+        return QLIN_ERR_INVALID_ARG;
+    // the kernels count K and the 128 x 128 output tiles in 32 bits
+    if (ceil_div(M, 128) * ceil_div(N, 128) > 0x7FFFFFFFll) return QLIN_ERR_INVALID_ARG;
     if (!x_dev || !w_codes_dev || !y_bf16_dev) return QLIN_ERR_INVALID_ARG;
     if (!aligned16(x_dev) || !aligned16(w_codes_dev) || !aligned16(y_bf16_dev) || (ldy * 2) % 16 ||
         (bias_bf16_dev && !aligned16(bias_bf16_dev)))
@@ -243,6 +249,8 @@ qlin_status qlin_gemm(qlin_format w_fmt, qlin_format x_fmt, int64_t M, int64_t N
     if (w_fmt == QLIN_INT4_G128_ASYM && x_fmt == QLIN_BF16) {
         if (!w_scales_dev || !w_zeros_dev) return QLIN_ERR_INVALID_ARG;
         if (K % 128 || N % 8) return QLIN_ERR_INVALID_ARG;
+        // 128-channel tiles and 64-token tiles run on grid dimensions y and z (at most 65535 each)
+        if (ceil_div(N, 128) > 65535 || ceil_div(M, 64) > 65535) return QLIN_ERR_INVALID_ARG;
         const size_t need = w4a16_workspace_bytes(M, N, K);
         if (need && (!workspace_dev || workspace_bytes < need || !aligned16(workspace_dev)))
             return QLIN_ERR_WORKSPACE;

@@ -167,6 +167,31 @@ def test_gemm_rejects_bad_arguments(q):
         assert g(F.INT4_G128_ASYM, F.BF16, 16, 4096, 4096, work=None) == S.WORKSPACE
 
 
+def test_shapes_past_the_32_bit_limits_are_rejected_before_any_launch(q):
+    F, L, S = q.Fmt, q.Layout, q.Status
+    big = 1 << 31
+    # quantizers: K, and rows x 256-element tasks, within 32 bits
+    assert q.qlin_quantize_act(F.FP8_TOKEN, FAKE, 1, big, big, FAKE, FAKE, None, L.CANONICAL, None, 0, None,
+                               None) == S.INVALID_ARG
+    for fmt in (F.FP8_TENSOR, F.MXFP8, F.NVFP4, F.FP8_GROUP128, F.INT8_ROW):
+        assert q.qlin_quantize_act(fmt, FAKE, 1 << 24, 1 << 16, 1 << 16, FAKE, FAKE, FAKE, L.CANONICAL, FAKE,
+                                   1 << 30, None, None) == S.INVALID_ARG, fmt
+    # rows padded to 128 for the MMA scale layout count too
+    rows = (1 << 31) - 1
+    assert q.qlin_quantize_act(F.MXFP8, FAKE, rows, 128, 128, FAKE, FAKE, None, L.MMA, None, 0, None,
+                               None) == S.INVALID_ARG
+
+    def g(wf, xf, M, N, K, layout=L.CANONICAL):
+        return q.qlin_gemm(wf, xf, M, N, K, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, N, layout, None,
+                           0, None, None)
+
+    assert g(F.FP8_TENSOR, F.FP8_TENSOR, 16, 16, big) == S.INVALID_ARG
+    assert g(F.FP8_BLOCK128, F.FP8_TOKEN, big - 1, big - 128, 128) == S.INVALID_ARG     # tiles past 2^31
+    # W4A16: 128-channel tiles and 64-token tiles on grid dimensions y and z
+    assert g(F.INT4_G128_ASYM, F.BF16, 65535 * 64 + 1, 4096, 4096) == S.INVALID_ARG
+    assert g(F.INT4_G128_ASYM, F.BF16, 16, 65535 * 128 + 8, 4096) == S.INVALID_ARG
+
+
 def test_mma_layout_reader_matches_the_documented_formula():
     from layouts import mma_to_canonical
     rows, nsc = 200, 8
