@@ -597,8 +597,8 @@ def oracle_sample_pass(sample):
     return flops, secs
 
 
-SAMPLE_BASELINE = (2048, 4096)     # rows of X, rows of W per linear (cpu_baseline leg)
-BASELINE_MIN_SECONDS = 12.0        # cpu_baseline repeats passes until this much oracle time
+SAMPLE_CPU = (2048, 4096)     # rows of X, rows of W per linear (cpu_baseline leg)
+CPU_MIN_SECONDS = 12.0        # cpu_baseline repeats passes until this much oracle time
 SAMPLE_REFERENCE = (1024, 2048)    # per step of the --impl reference arm
 
 
@@ -639,17 +639,17 @@ def host_cpu(cpuinfo: str = "/proc/cpuinfo") -> dict:
 def cpu_baseline():
     import oracle
     oracle.build()
-    sample = oracle_sample_inputs(*SAMPLE_BASELINE)
+    sample = oracle_sample_inputs(*SAMPLE_CPU)
     flops = secs = 0
     passes = 0
-    while secs < BASELINE_MIN_SECONDS:
+    while secs < CPU_MIN_SECONDS:
         f, t = oracle_sample_pass(sample)
         flops += f
         secs += t
         passes += 1
     return {"value": round(flops / secs / 1e12, 6), "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
-            "sample": (f"{passes} passes over one linear per workload, X[:{SAMPLE_BASELINE[0]}] x "
-                       f"W[:{SAMPLE_BASELINE[1]}] at full K ({flops / passes / 1e9:.0f} GFLOP per pass): scalar C "
+            "sample": (f"{passes} passes over one linear per workload, X[:{SAMPLE_CPU[0]}] x "
+                       f"W[:{SAMPLE_CPU[1]}] at full K ({flops / passes / 1e9:.0f} GFLOP per pass): scalar C "
                        "quantizers (1 thread) + float64 numpy matmul (BLAS threads)"),
             "seconds": round(secs, 2), "host": host_cpu()}
 
