@@ -33,6 +33,12 @@
  *     of its bounded waits gives up.  Such a kernel leaves its outputs
  *     unspecified but returns, and the context stays usable.
  *   - Inputs are finite.  NaN or Inf inputs give unspecified codes.
+ *   - One device per process.  The first qlin_gemm call of each format pair
+ *     sets that kernel's shared-memory size on the device current at the
+ *     time, and later calls skip the step.  A call on another device of the
+ *     same process then fails to launch and returns QLIN_ERR_CUDA; nothing is
+ *     written.  Make that first call on one thread; once each pair has run,
+ *     calls from several host threads (on their own streams) are safe.
  *
  * Numeric rules (bit-exact; the pages name the formats but print no formula,
  * so these are the plainest readings of the public format definitions):
