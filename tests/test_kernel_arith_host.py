@@ -7,8 +7,14 @@ the IEEE formats (numpy emulates the half-precision operations exactly).
   taken two at a time from bits [4j, 4j + 4) and [4j + 16, 4j + 20).
 - The warp-level W4A16 kernel: lane q's A-fragment positions and B-fragment
   positions name the same K index for every logical k of an m16n8k16 step.
+- The grids: the GEMM tile raster, the quantizers' task walks and tile grids,
+  the tensor-core scale tiling and the W4A16 split-K partitions each cover
+  their outputs exactly once.
 """
+from collections import Counter
+
 import numpy as np
+import pytest
 
 
 def f16(bits):
@@ -63,3 +69,162 @@ def test_warp_mma_k_order_matches_between_operands():
     # and the 16 logical k of a step cover the 16 physical k once
     covered = sorted(8 * (q // 2) + 2 * (q % 2) + d for q in range(4) for d in (0, 4, 1, 5))
     assert covered == list(range(16))
+
+
+# ---------------------------------------------------------------- grid coverage
+# The kernels' index math restated on the host (each function names the kernel
+# it follows): every output element, tile and K group is visited exactly once,
+# for the workloads' shapes and for ragged ones.
+SMS = 152
+
+
+def cdiv(a, b):
+    return -(-a // b)
+
+
+def tile_coords(t, tiles_m, tiles_n, BN, BM=128, GM=16):
+    """gemm_tc.cu, tile_coords: bands of 16 row blocks, rows first inside a band."""
+    band = t // (GM * tiles_n)
+    first_m = band * GM
+    gm = min(GM, tiles_m - first_m)
+    idx = t - band * GM * tiles_n
+    return (first_m + idx % gm) * BM, (idx // gm) * BN
+
+
+@pytest.mark.parametrize("M,N", [(128, 1024), (4096, 12288), (32768, 3072), (20280, 13824), (20280, 5120),
+                                 (333, 1040), (1, 72), (2100, 640)])
+def test_gemm_raster_visits_every_output_tile_once(M, N):
+    BN = 256
+    tm, tn = cdiv(M, 128), cdiv(N, BN)
+    got = [tile_coords(t, tm, tn, BN) for t in range(tm * tn)]
+    assert sorted(got) == [(i * 128, j * BN) for i in range(tm) for j in range(tn)]
+    # the persistent loop (tile = blockIdx.x; tile += gridDim.x) hands each index to one CTA
+    grid = min(tm * tn, SMS)
+    owners = Counter(t for b in range(grid) for t in range(b, tm * tn, grid))
+    assert set(owners.values()) == {1} and len(owners) == tm * tn
+
+
+def task_pos(t, total, tpr, nvr, lane):
+    """quant.cu, task_pos: task t is 32 consecutive 16-byte vectors of one row."""
+    if t >= total:
+        return None
+    row = t // tpr
+    c = (t - row * tpr) * 32 + lane
+    return (row, c) if c < nvr else None
+
+
+def task_walk(rows, K, grid, unroll=4):
+    """The walk of k_amax_partial, k_fp8_tensor_encode, k_mx, k_nvfp4_encode and
+    k_fp8_group128: warp w0 = 8 * block + warp takes tasks t + u * warps for
+    u < unroll, then steps by warps * unroll."""
+    nvr = K // 8
+    tpr = cdiv(nvr, 32)
+    total = rows * tpr
+    warps = grid * 8
+    seen = Counter()
+    for w0 in range(warps):
+        for t in range(w0, total, warps * unroll):
+            for u in range(unroll):
+                for lane in range(32):
+                    p = task_pos(t + u * warps, total, tpr, nvr, lane)
+                    if p is not None:
+                        seen[p] += 1
+    return seen, nvr
+
+
+def task_grid_once(rows, K, unroll=4):
+    return max(1, cdiv(rows * cdiv(K // 8, 32), 8 * unroll))
+
+
+def task_grid_persistent(rows, K, unroll=4):
+    return max(1, min(cdiv(rows * cdiv(K // 8, 32), 8 * unroll), SMS * 8))
+
+
+def amax_partials(rows, K):
+    return max(1, min(cdiv(rows * (K // 8), 1024), 1024))
+
+
+@pytest.mark.parametrize("rows,K", [(333, 1040), (128, 1024), (3, 8), (200, 512), (1, 20480), (130, 264)])
+def test_task_walks_cover_every_vector_once(rows, K):
+    for grid in {task_grid_once(rows, K), task_grid_persistent(rows, K), amax_partials(rows, K), 1, 3}:
+        seen, nvr = task_walk(rows, K, grid)
+        assert len(seen) == rows * nvr and set(seen.values()) == {1}, grid
+        assert all(r < rows and c < nvr for r, c in seen)
+    # the one-round grid needs no second round
+    g = task_grid_once(rows, K)
+    assert g * 8 * 4 >= rows * cdiv(K // 8, 32)
+
+
+def test_block128_and_int4_grids_cover_their_tiles():
+    # k_fp8_block128: CTA b -> tile (b // (K/128), b % (K/128)); thread t -> rows t/16 + 16 i, vector t % 16
+    rows, K = 384, 640
+    kt = K // 128
+    seen = Counter()
+    for b in range((rows // 128) * kt):
+        bi, bj = b // kt, b - (b // kt) * kt
+        for t in range(256):
+            for i in range(8):
+                seen[(bi * 128 + t // 16 + 16 * i, bj * 16 + t % 16)] += 1
+    assert len(seen) == rows * (K // 8) and set(seen.values()) == {1}
+    # k_int4_g128: CTA b -> group b // nb, channels (b % nb) * 128 + thread, those < N
+    for N in (72, 4096, 200):
+        nb = cdiv(N, 128)
+        pairs = Counter()
+        for b in range(nb * (K // 128)):
+            g = b // nb
+            for t in range(128):
+                n = (b - g * nb) * 128 + t
+                if n < N:
+                    pairs[(g, n)] += 1
+        assert len(pairs) == (K // 128) * N and set(pairs.values()) == {1}
+
+
+def mma_scale_offset(row, j, chunks):
+    """quant.cu, mma_scale_offset: the QLIN_SCALE_MMA tiling."""
+    tile, rr = row >> 7, row & 127
+    return ((tile * chunks + (j >> 2)) << 9) + ((rr & 31) << 4) + ((rr >> 5) << 2) + (j & 3)
+
+
+@pytest.mark.parametrize("rows,nsc", [(1, 4), (333, 16), (256, 40)])
+def test_mma_scale_tiling_is_a_bijection_onto_the_padded_buffer(rows, nsc):
+    rows_pad = cdiv(rows, 128) * 128
+    offs = [mma_scale_offset(r, j, nsc // 4) for r in range(rows_pad) for j in range(nsc)]
+    assert sorted(offs) == list(range(rows_pad * nsc))
+
+
+def pick_split_mma(tiles, groups):
+    """gemm_w4a16.cu, pick_split_mma (M <= 16)."""
+    cs = 1
+    while cs < 8 and tiles * (cs + 1) <= 2 * SMS and groups >= 2 * (cs + 1):
+        cs += 1
+    return cs
+
+
+def pick_split(tiles, groups):
+    """gemm_w4a16.cu, pick_split (the tcgen05 kernel, M > 16)."""
+    cs = 1
+    while cs < 8 and tiles * cs * 2 <= SMS and groups >= 2 * cs * 2:
+        cs *= 2
+    return cs
+
+
+@pytest.mark.parametrize("M,K,N", [(1, 4096, 4096), (16, 4096, 12288), (16, 12288, 4096), (64, 4096, 4096),
+                                   (64, 12288, 4096), (5, 256, 72), (33, 128, 136), (70, 1024, 256)])
+def test_w4a16_split_k_partitions_groups_and_columns(M, K, N):
+    groups = K // 128
+    if M <= 16:
+        tiles = cdiv(N, 128) * cdiv(M, 16)
+        cs = pick_split_mma(tiles, groups)
+        assert tiles * cs <= max(2 * SMS, tiles)        # about one wave of two CTAs per SM
+    else:
+        tiles = cdiv(N, 128) * cdiv(M, 64 if M > 32 else 32)
+        cs = pick_split(tiles, groups)
+    assert 1 <= cs <= 8
+    # rank r of the cluster takes groups [groups*r/cs, groups*(r+1)/cs): a partition, none empty
+    parts = [(groups * r // cs, groups * (r + 1) // cs) for r in range(cs)]
+    assert parts[0][0] == 0 and parts[-1][1] == groups
+    assert all(a[1] == b[0] for a, b in zip(parts, parts[1:]))
+    assert all(b - a >= (2 if cs > 1 else 1) for a, b in parts)
+    # and sums output columns [128*r/cs, 128*(r+1)/cs) of the tile over the cluster
+    cols = [(128 * r // cs, 128 * (r + 1) // cs) for r in range(cs)]
+    assert cols[0][0] == 0 and cols[-1][1] == 128 and all(a[1] == b[0] for a, b in zip(cols, cols[1:]))
