@@ -202,3 +202,21 @@ def test_mma_layout_reader_matches_the_documented_formula():
             tile, rr, chunk, jj = r // 128, r % 128, j // 4, j % 4
             buf[(tile * 2 + chunk) * 512 + 16 * (rr % 32) + 4 * (rr // 32) + jj] = canon[r, j]
     assert np.array_equal(mma_to_canonical(buf, rows, nsc), canon)
+
+
+def test_plain_c_consumer_compiles_links_and_passes(q, tmp_path):
+    """include/qlin.h is plain C99 (no C++ or CUDA headers) and libqlin.so links
+    into a C program; the program checks sizes and validation without a GPU."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    exe = str(tmp_path / "c_abi_check")
+    libdir = os.path.dirname(q.LIB_PATH)
+    cmd = [gcc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic", "-I", os.path.join(ROOT, "include"),
+           os.path.join(ROOT, "tests", "c_abi_check.c"), "-o", exe, q.LIB_PATH, f"-Wl,-rpath,{libdir}"]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0 and "c abi ok" in r.stdout, r.stdout + r.stderr
