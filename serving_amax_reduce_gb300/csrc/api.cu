@@ -201,7 +201,7 @@ qlin_status qlin_gemm(qlin_format w_fmt, qlin_format x_fmt, int64_t M, int64_t N
         return QLIN_ERR_ALIGNMENT;
     GemmArgs a{M, N, K, ldy, x_dev, x_scales_dev, x_global_dev, w_codes_dev, w_scales_dev, w_zeros_dev,
                w_global_dev, static_cast<const uint16_t*>(bias_bf16_dev), static_cast<uint16_t*>(y_bf16_dev),
-               workspace_dev, workspace_bytes, dev_status_dev};
+               workspace_dev, workspace_bytes, dev_status_dev, /*x_group128=*/false};
     if (w_fmt == QLIN_FP8_TENSOR && x_fmt == QLIN_FP8_TENSOR) {
         if (!x_scales_dev || !w_scales_dev) return QLIN_ERR_INVALID_ARG;
         if (K % 16) return QLIN_ERR_INVALID_ARG;
