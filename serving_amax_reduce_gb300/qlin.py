@@ -189,6 +189,30 @@ def _check(rc: int, where: str):
         raise QlinError(rc, where)
 
 
+def _need(t, nbytes: int, what: str):
+    """The library writes or reads `nbytes` bytes at t's address: refuse a
+    smaller or non-contiguous buffer before any pointer is handed over."""
+    if not nbytes:
+        return
+    if t is None:
+        raise ValueError(f"{what}: a buffer of {nbytes} bytes is required")
+    if not t.is_contiguous() or t.numel() * t.element_size() < nbytes:
+        raise ValueError(f"{what}: needs {nbytes} contiguous bytes, got {t.numel() * t.element_size()}"
+                         f"{'' if t.is_contiguous() else ' (not contiguous)'}")
+
+
+def _check_quant_bufs(fmt: Fmt, rows: int, K: int, layout: Layout, b: dict):
+    _need(b["codes"], qlin_codes_bytes(fmt, rows, K), "codes")
+    _need(b["scales"], qlin_scales_bytes(fmt, layout, rows, K), "scales")
+    _need(b.get("zeros"), qlin_zeros_bytes(fmt, rows, K), "zeros")
+    if fmt == Fmt.NVFP4:
+        _need(b.get("global"), 4, "global")
+    wsb = qlin_quant_workspace_bytes(fmt, rows, K)
+    _need(b.get("workspace"), wsb, "workspace")
+    if b.get("workspace_bytes", 0) < wsb:
+        raise ValueError(f"workspace_bytes: {wsb} required")
+
+
 def _empty(nbytes: int, device, dtype=torch.uint8):
     item = torch.empty((), dtype=dtype).element_size()
     return torch.empty(max(1, (nbytes + item - 1) // item), dtype=dtype, device=device)
@@ -218,6 +242,7 @@ def quantize_weight(fmt: Fmt, w: torch.Tensor, layout: Layout = Layout.CANONICAL
     assert w.dtype == torch.bfloat16 and w.dim() == 2 and w.stride(1) == 1
     N, K = w.shape
     b = bufs if bufs is not None else alloc_quant(fmt, N, K, layout, w.device)
+    _check_quant_bufs(fmt, N, K, layout, b)
     rc = qlin_quantize_weight(fmt, w.data_ptr(), N, K, w.stride(0), b["codes"].data_ptr(), b["scales"].data_ptr(),
                               _ptr(b.get("zeros")), _ptr(b.get("global")), layout, _ptr(b["workspace"]),
                               b["workspace_bytes"], _ptr(status if status is not None else device_status(w.device)),
@@ -231,6 +256,7 @@ def quantize_act(fmt: Fmt, x: torch.Tensor, layout: Layout = Layout.CANONICAL, b
     assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
     M, K = x.shape
     b = bufs if bufs is not None else alloc_quant(fmt, M, K, layout, x.device)
+    _check_quant_bufs(fmt, M, K, layout, b)
     rc = qlin_quantize_act(fmt, x.data_ptr(), M, K, x.stride(0), b["codes"].data_ptr(), b["scales"].data_ptr(),
                            _ptr(b.get("global")), layout, _ptr(b["workspace"]), b["workspace_bytes"],
                            _ptr(status if status is not None else device_status(x.device)), _stream(stream))
@@ -244,6 +270,20 @@ def gemm(w_fmt: Fmt, x_fmt: Fmt, M: int, N: int, K: int, x, x_scales, w_codes, w
     dev = w_codes.device
     if y is None:
         y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+    # the kernels write Y[M, N] with leading dimension y.stride(0) and read every operand in full
+    if y.dtype != torch.bfloat16 or tuple(y.shape) != (M, N) or y.stride(1) != 1:
+        raise ValueError(f"y: a bf16 [{M}, {N}] matrix with unit column stride is required")
+    if x_fmt == Fmt.BF16:
+        if x.dtype != torch.bfloat16 or tuple(x.shape) != (M, K) or not x.is_contiguous():
+            raise ValueError(f"x: contiguous bf16 [{M}, {K}] activations are required")
+    else:
+        _need(x, qlin_codes_bytes(x_fmt, M, K), "x codes")
+        _need(x_scales, qlin_scales_bytes(x_fmt, layout, M, K), "x_scales")
+    _need(w_codes, qlin_codes_bytes(w_fmt, N, K), "w_codes")
+    _need(w_scales, qlin_scales_bytes(w_fmt, layout, N, K), "w_scales")
+    _need(w_zeros, qlin_zeros_bytes(w_fmt, N, K), "w_zeros")
+    if bias is not None and (bias.dtype != torch.bfloat16 or bias.numel() < N or not bias.is_contiguous()):
+        raise ValueError(f"bias: {N} contiguous bf16 values are required")
     wsb = qlin_gemm_workspace_bytes(w_fmt, x_fmt, M, N, K)
     if wsb and workspace is None:
         workspace = _empty(wsb, dev)
