@@ -23,6 +23,15 @@ def run(q, fmt, x, layout=None, weight=False):
     return b
 
 
+def refused_before_launch(q, fmt, x):
+    """The tensor-core scale tiling needs whole 4-scale chunks along K; other K
+    are refused with INVALID_ARG before any launch (no output is written)."""
+    with pytest.raises(q.QlinError) as e:
+        run(q, fmt, x, q.Layout.MMA)
+    assert e.value.status == q.Status.INVALID_ARG
+    assert q.read_device_status() == 0
+
+
 def make(kind, rows, K, seed):
     if kind == "outlier":
         return inputs.outlier_channel_bf16(rows, K, seed)
@@ -89,9 +98,10 @@ def test_fp8_block128(q, orc, rows, K, kind):
 @pytest.mark.parametrize("kind", ["normal", "edge"])
 @pytest.mark.parametrize("mma", [False, True])
 def test_mxfp8(q, orc, rows, K, kind, mma):
-    if mma and K % 128:
-        pytest.skip("MMA layout needs K % 128 == 0")
     x = make(kind, rows, K, 5 * rows + K) if kind == "edge" else inputs.normal_bf16((rows, K), 1.0, rows + K)
+    if mma and K % 128:
+        refused_before_launch(q, q.Fmt.MXFP8, x)     # the tiling packs 4 scales (128 K) per chunk
+        return
     b = run(q, q.Fmt.MXFP8, x, q.Layout.MMA if mma else None)
     codes, sc = orc.quant_mxfp8(bits(x))
     assert np.array_equal(np_u8(b["codes"]).reshape(rows, K), codes)
@@ -107,9 +117,10 @@ def test_mxfp8(q, orc, rows, K, kind, mma):
 @pytest.mark.parametrize("kind", ["outlier", "edge"])
 @pytest.mark.parametrize("mma", [False, True])
 def test_nvfp4(q, orc, rows, K, kind, mma):
-    if mma and K % 64:
-        pytest.skip("MMA layout needs K % 64 == 0")
     x = make(kind, rows, K, 11 * rows + K)
+    if mma and K % 64:
+        refused_before_launch(q, q.Fmt.NVFP4, x)     # the tiling packs 4 scales (64 K) per chunk
+        return
     b = run(q, q.Fmt.NVFP4, x, q.Layout.MMA if mma else None)
     packed, sc, g = orc.quant_nvfp4(bits(x))
     assert np.array_equal(np_u8(b["codes"]).reshape(rows, K // 2), packed)
@@ -136,9 +147,10 @@ def test_fp8_group128(q, orc, rows, K, kind):
 @pytest.mark.parametrize("kind", ["normal", "edge"])
 @pytest.mark.parametrize("mma", [False, True])
 def test_mxfp4(q, orc, rows, K, kind, mma):
-    if mma and K % 128:
-        pytest.skip("MMA layout needs K % 128 == 0")
     x = make(kind, rows, K, 7 * rows + K) if kind == "edge" else inputs.normal_bf16((rows, K), 1.0, rows + 2 * K)
+    if mma and K % 128:
+        refused_before_launch(q, q.Fmt.MXFP4, x)
+        return
     b = run(q, q.Fmt.MXFP4, x, q.Layout.MMA if mma else None)
     packed, sc = orc.quant_mxfp4(bits(x))
     assert np.array_equal(np_u8(b["codes"]).reshape(rows, K // 2), packed)
