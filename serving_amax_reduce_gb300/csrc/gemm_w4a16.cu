@@ -9,8 +9,8 @@
 // registers and feeds warp-level mma.sync: at 16 tokens a tcgen05 MMA has
 // N = 16 and the tensor pipe is bound by its per-instruction cost.  For larger
 // M, k_w4a16 below runs tcgen05 with the output channels on the MMA's M side
-// ("swap AB"): a CTA owns 128 channels and MP tokens (MP = 32 or 64,
-// zero-filled past M by TMA; larger M runs as several token tiles).
+// ("swap AB"): a CTA owns 128 channels and MP = 64 tokens (zero-filled past M
+// by TMA; larger M runs as several token tiles).
 // Per 128-K group:
 //   warp 0    TMA: the packed int4 words (16 k-octets x 128 channels, 8 KB)
 //             into a deep ring, so that enough HBM reads are in flight;
@@ -674,12 +674,6 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// Token tile of the tcgen05 kernel (M > 16; M <= 16 runs k_w4a16_mma).
-int pick_mp(int64_t M) {
-    if (M <= 32) return 32;
-    return 64;                       // larger M runs as several 64-token tiles
-}
-
 // Split-K ways (cluster size) so that the grid is about one wave of SMs.
 int pick_split(int64_t tiles, int64_t groups) {
     int cs = 1;
@@ -799,7 +793,7 @@ cudaError_t launch_w4a16_mma(const GemmArgs& a, cudaStream_t st) {
 
 cudaError_t launch_gemm_w4a16(const GemmArgs& a, cudaStream_t st) {
     if (a.M <= 16) return launch_w4a16_mma(a, st);
-    return pick_mp(a.M) == 32 ? launch_mp<32>(a, st) : launch_mp<64>(a, st);
+    return launch_mp<64>(a, st);     // 64-token tiles, zero-filled past M; larger M runs several
 }
 
 }  // namespace qlin

@@ -329,7 +329,7 @@ def w4a16_case(q, orc, M, K, N, with_bias=False):
 
 
 @pytest.mark.parametrize("M,K,N", [(1, 4096, 4096), (16, 4096, 12288), (64, 12288, 4096), (5, 256, 72),
-                                   (100, 512, 256), (200, 1024, 384), (33, 128, 136)])
+                                   (100, 512, 256), (200, 1024, 384), (33, 128, 136), (24, 512, 136)])
 def test_w4a16_gemm(q, orc, M, K, N):
     w4a16_case(q, orc, M, K, N)
 

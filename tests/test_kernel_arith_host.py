@@ -209,7 +209,7 @@ def pick_split(tiles, groups):
 
 
 @pytest.mark.parametrize("M,K,N", [(1, 4096, 4096), (16, 4096, 12288), (16, 12288, 4096), (64, 4096, 4096),
-                                   (64, 12288, 4096), (5, 256, 72), (33, 128, 136), (70, 1024, 256)])
+                                   (64, 12288, 4096), (5, 256, 72), (24, 512, 136), (33, 128, 136), (70, 1024, 256)])
 def test_w4a16_split_k_partitions_groups_and_columns(M, K, N):
     groups = K // 128
     if M <= 16:
@@ -217,7 +217,7 @@ def test_w4a16_split_k_partitions_groups_and_columns(M, K, N):
         cs = pick_split_mma(tiles, groups)
         assert tiles * cs <= max(2 * SMS, tiles)        # about one wave of two CTAs per SM
     else:
-        tiles = cdiv(N, 128) * cdiv(M, 64 if M > 32 else 32)
+        tiles = cdiv(N, 128) * cdiv(M, 64)             # 64-token tiles
         cs = pick_split(tiles, groups)
     assert 1 <= cs <= 8
     # rank r of the cluster takes groups [groups*r/cs, groups*(r+1)/cs): a partition, none empty
