@@ -40,7 +40,11 @@ def make(kind, rows, K, seed):
     return inputs.normal_bf16((rows, K), 0.02, seed)
 
 
-SHAPES_ROW = [(1, 1024), (200, 3072), (64, 12288), (3, 24576), (129, 1040), (37, 8)]
+SHAPES_ROW = [(1, 1024), (200, 3072), (64, 12288), (3, 24576), (129, 1040), (37, 8),
+              # with the above, every register-resident (threads, vectors per thread) variant the
+              # per-row kernels dispatch to, and the first K past them
+              (9, 4096), (9, 5120), (9, 6144), (9, 7168), (9, 8192), (9, 9216), (9, 13312), (9, 16384),
+              (9, 16392)]
 
 
 @pytest.mark.parametrize("rows,K", SHAPES_ROW)

@@ -228,3 +228,23 @@ def test_w4a16_split_k_partitions_groups_and_columns(M, K, N):
     # and sums output columns [128*r/cs, 128*(r+1)/cs) of the tile over the cluster
     cols = [(128 * r // cs, 128 * (r + 1) // cs) for r in range(cs)]
     assert cols[0][0] == 0 and cols[-1][1] == 128 and all(a[1] == b[0] for a, b in zip(cols, cols[1:]))
+
+
+def rows_variant(K):
+    """quant.cu, rowwise: the per-row kernel a row of K elements runs."""
+    nv = K // 8
+    if nv <= 128 * 8:
+        return (128, cdiv(nv, 128))
+    if nv <= 256 * 8:
+        return (256, cdiv(nv, 256))
+    return "long"
+
+
+def test_row_quantizer_tests_reach_every_dispatched_variant():
+    import test_gpu_quant
+    reachable = {(128, v) for v in range(1, 9)} | {(256, v) for v in range(5, 9)} | {"long"}
+    assert {rows_variant(K) for _, K in test_gpu_quant.SHAPES_ROW} == reachable
+    for K in range(8, 20000, 8):
+        v = rows_variant(K)
+        if v != "long":
+            assert v in reachable and v[0] * v[1] * 8 >= K      # the CTA's vectors cover the row
