@@ -674,10 +674,12 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// Split-K ways (cluster size) so that the grid is about one wave of SMs.
+// Split-K ways (cluster size) so that the grid is about one wave of SMs.  At
+// most 4: each CTA holds most of an SM's shared memory, and clusters of up to
+// 4 such CTAs are the sizes this kernel has been run and checked with.
 int pick_split(int64_t tiles, int64_t groups) {
     int cs = 1;
-    while (cs < 8 && tiles * cs * 2 <= kNumSMs && groups >= 2 * cs * 2) cs *= 2;
+    while (cs < 4 && tiles * cs * 2 <= kNumSMs && groups >= 2 * cs * 2) cs *= 2;
     return cs;
 }
 

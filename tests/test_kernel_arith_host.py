@@ -201,15 +201,16 @@ def pick_split_mma(tiles, groups):
 
 
 def pick_split(tiles, groups):
-    """gemm_w4a16.cu, pick_split (the tcgen05 kernel, M > 16)."""
+    """gemm_w4a16.cu, pick_split (the tcgen05 kernel, M > 16): at most 4 ways."""
     cs = 1
-    while cs < 8 and tiles * cs * 2 <= SMS and groups >= 2 * cs * 2:
+    while cs < 4 and tiles * cs * 2 <= SMS and groups >= 2 * cs * 2:
         cs *= 2
     return cs
 
 
 @pytest.mark.parametrize("M,K,N", [(1, 4096, 4096), (16, 4096, 12288), (16, 12288, 4096), (64, 4096, 4096),
-                                   (64, 12288, 4096), (5, 256, 72), (24, 512, 136), (33, 128, 136), (70, 1024, 256)])
+                                   (64, 12288, 4096), (5, 256, 72), (24, 512, 136), (33, 128, 136), (70, 1024, 256),
+                                   (64, 2048, 1024)])
 def test_w4a16_split_k_partitions_groups_and_columns(M, K, N):
     groups = K // 128
     if M <= 16:
@@ -248,3 +249,16 @@ def test_row_quantizer_tests_reach_every_dispatched_variant():
         v = rows_variant(K)
         if v != "long":
             assert v in reachable and v[0] * v[1] * 8 >= K      # the CTA's vectors cover the row
+
+
+def test_w4a16_parity_cases_reach_every_cluster_size():
+    """The W4A16 parity shapes run the warp-level kernel with every split-K
+    cluster size it picks (1 to 8) and the tcgen05 kernel with 1, 2 and 4."""
+    import test_gpu_gemm
+    shapes = []
+    for mark in test_gpu_gemm.test_w4a16_gemm.pytestmark + test_gpu_gemm.test_w4a16_gemm_bias.pytestmark:
+        if mark.name == "parametrize":
+            shapes += list(mark.args[1])
+    mma = {pick_split_mma(cdiv(N, 128) * cdiv(M, 16), K // 128) for M, K, N in shapes if M <= 16}
+    tc = {pick_split(cdiv(N, 128) * cdiv(M, 64), K // 128) for M, K, N in shapes if M > 16}
+    assert mma == set(range(1, 9)) and tc == {1, 2, 4}
