@@ -294,6 +294,35 @@ def test_nvfp4_dequant_close(orc):
     assert np.all(np.abs(xh - xv) <= bound)
 
 
+def test_nvfp4_exact_bruteforce_small(orc):
+    """Every block scale and code against an exact-rational search over all
+    UE4M3 and E2M1 codes, on the fp32 values the NVFP4 rule defines:
+    q = 448/A and rg = 2688/A, block scale nearest to b*q, element value
+    x * (rg / dec(scale)) (0 when the scale decodes to 0), each product or
+    quotient one fp32 operation."""
+    from test_oracle_codecs import brute_nearest
+    e4m3 = [(c, orc.dec_e4m3(c)) for c in range(256) if not math.isnan(orc.dec_e4m3(c))]
+    e2m1 = [(c, orc.dec_e2m1(c)) for c in range(16)]
+    R, K = 6, 128
+    x = bf16_bits(inputs.outlier_channel_bf16(R, K, 57))
+    x[5] = bf16_bits(torch.from_numpy(vals(x[5:6]) * 1e-3).to(torch.bfloat16))[0]   # small blocks too
+    packed, sc, g = orc.quant_nvfp4(x)
+    xv = vals(x).astype(np.float32)                     # bf16 values are exact in fp32
+    A = np.float32(np.abs(xv).max())
+    q, rg = np.float32(448) / A, np.float32(2688) / A
+    assert float(g) == float(A / np.float32(2688))
+    codes = unpack_e2m1(packed)
+    for i in range(R):
+        for blk in range(K // 16):
+            seg = xv[i, 16 * blk:16 * blk + 16]
+            sb = brute_nearest(float(np.float32(np.abs(seg).max()) * q), e4m3, 448.0, 3)
+            assert sc[i, blk] == sb, (i, blk)
+            dsb = np.float32(orc.dec_e4m3(sb))
+            rb = np.float32(0) if dsb == 0 else rg / dsb
+            for k in range(16):
+                assert codes[i, 16 * blk + k] == brute_nearest(float(seg[k] * rb), e2m1, 6.0, 1), (i, blk, k)
+
+
 def test_nvfp4_worked_blocks(orc):
     """Four blocks worked by hand.  The tensor amax is 448, so 448/A = 1 and
     2688/A = 6 exactly, and g = fl(448/2688).
