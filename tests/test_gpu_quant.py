@@ -177,6 +177,26 @@ def test_int4_g128(q, orc, N, K, kind):
     assert np.array_equal(b["zeros"].cpu().numpy().view(np.int32).reshape(K // 128, N // 8), qz)
 
 
+def test_fp8_reciprocal_form_rows(q, orc):
+    """Rows on which x * fl(448 / amax) and x / fl(amax / 448) round to
+    different codes: the kernels follow the oracle (the reciprocal form) bit
+    for bit, per token, per 1 x 128 group and per tensor."""
+    from hard_cases import fp8_reciprocal_candidates, rows_of_pairs
+    rows = rows_of_pairs(fp8_reciprocal_candidates([orc.dec_e4m3(c) for c in range(256)]), 128)
+    x = torch.from_numpy(rows.view(np.int16)).view(torch.bfloat16)
+    for fmt, ref in [(q.Fmt.FP8_TOKEN, orc.quant_fp8_token), (q.Fmt.FP8_GROUP128, orc.quant_fp8_group128)]:
+        b = run(q, fmt, x)
+        codes, s = ref(rows)
+        s = np.asarray(s, np.float32)
+        assert np.array_equal(np_u8(b["codes"]).reshape(rows.shape), codes)
+        assert np.array_equal(np_f32(b["scales"]).reshape(s.shape).view(np.uint32), s.view(np.uint32))
+    for i in range(0, len(rows), max(1, len(rows) // 16)):
+        b = run(q, q.Fmt.FP8_TENSOR, x[i:i + 1])
+        codes, s = orc.quant_fp8_tensor(rows[i:i + 1])
+        assert np.array_equal(np_u8(b["codes"]).reshape(1, 128), codes)
+        assert np_f32(b["scales"])[0].view(np.uint32) == np.float32(s).view(np.uint32)
+
+
 def test_leading_dimension_is_honoured(q, orc):
     """A strided view (ld > K) quantizes exactly like its contiguous copy."""
     big = inputs.outlier_channel_bf16(96, 4096, 5)

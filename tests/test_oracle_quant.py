@@ -120,6 +120,34 @@ def test_fp8_block_granules_are_independent(orc):
     assert np.array_equal(c1[mask], c2[mask])
 
 
+def test_fp8_codes_follow_the_reciprocal_form(orc):
+    """Reading R1: code = E4M3(x * fl(448 / amax)), not E4M3(x / fl(amax / 448)).
+    On constructed rows where the two differ, every FP8 granule kind (token,
+    1 x 128 group, tensor) gives the reciprocal form's code, found by an
+    exact-rational search over all E4M3 codes."""
+    from hard_cases import fp8_reciprocal_candidates, rows_of_pairs
+    from test_oracle_codecs import brute_nearest
+    table = [(c, orc.dec_e4m3(c)) for c in range(256) if not math.isnan(orc.dec_e4m3(c))]
+    f32 = np.float32
+    pairs, want = [], []
+    for a, x in fp8_reciprocal_candidates([v for _, v in table]):
+        c_mul = brute_nearest(float(f32(x) * (f32(448) / f32(a))), table, 448.0, 3)
+        c_div = brute_nearest(float(f32(x) / (f32(a) / f32(448))), table, 448.0, 3)
+        if c_mul != c_div:
+            pairs.append((a, x))
+            want.append(c_mul)
+    assert len(pairs) >= 100                       # the readings really differ on these rows
+    rows = rows_of_pairs(pairs, 128)
+    codes, scales = orc.quant_fp8_token(rows)
+    assert list(codes[:, 1]) == want
+    assert np.array_equal(scales, np.array([f32(a) / f32(448) for a, _ in pairs], np.float32))
+    gcodes, _ = orc.quant_fp8_group128(rows)
+    assert list(gcodes[:, 1]) == want
+    for (a, x), w, row in list(zip(pairs, want, rows))[:20]:
+        tcodes, _ = orc.quant_fp8_tensor(row[None, :])
+        assert tcodes[0, 1] == w
+
+
 def test_fp8_group128_amax_maps_to_448_and_codes_are_nearest(orc):
     R, K = 64, 512
     x = bf16_bits(inputs.outlier_channel_bf16(R, K, 81))
