@@ -1,6 +1,12 @@
 """Constructed inputs on which two readings of a rounding rule give different
 codes (test inputs only: no expected values are computed here).
 
+NVFP4: `nvfp4_block_sweep` enumerates bf16 blocks under a fixed tensor amax,
+so that the block scale b * fl(448 / A) and the element value
+x * fl(fl(2688 / A) / dec(scale)) meet, somewhere in the sweep, the rare
+values where a variant of those steps (b / (6 g), x / (dec(scale) g)) rounds
+to another code.
+
 FP8 granules encode x * r with r = fl(448 / amax), one fp32 reciprocal per
 granule.  Dividing instead, x / fl(amax / 448), gives the same code almost
 everywhere; the pairs below are where it does not.  With amax = 7 t 2^j
@@ -42,3 +48,38 @@ def rows_of_pairs(pairs, K: int) -> np.ndarray:
     for i, (a, x) in enumerate(pairs):
         rows[i, 0], rows[i, 1] = a, x
     return (rows.view(np.uint32) >> 16).astype(np.uint16)
+
+
+def bf16_grid(lo_exp: int, hi_exp: int) -> np.ndarray:
+    """Every positive bf16 value in [2^lo_exp, 2^hi_exp), ascending, as float32."""
+    e = np.arange(lo_exp + 127, hi_exp + 127, dtype=np.uint32)
+    bits = ((e[:, None] << 7) | np.arange(128, dtype=np.uint32)[None, :]).ravel() << 16
+    return bits.view(np.float32)
+
+
+# tensor amaxes (bf16) under which the NVFP4 steps separate from their variants
+NVFP4_AMAXES = (13.0, 2.046875, 4.71875, 0.171875, 5.1875)
+
+
+def nvfp4_block_sweep(A: float, binades: int = 5, K: int = 256) -> np.ndarray:
+    """bf16 bits of one tensor whose amax is A: a block [A, 0, ...], then for
+    every bf16 b from 2^(floor(log2 A) - binades) up to A, blocks led by b and
+    filled with the bf16 values x <= b of that range in order, so that each
+    (b, x) pair appears once.  Rows of K elements (K / 16 blocks), padded with
+    zero blocks."""
+    lo = int(np.floor(np.log2(A))) - binades
+    grid = bf16_grid(lo, lo + binades + 1)
+    bs = grid[grid <= A]
+    blocks = [np.array([A] + [0.0] * 15, np.float32)]
+    for b in bs:
+        xs = grid[grid <= b]
+        for i in range(0, len(xs), 15):
+            chunk = xs[i:i + 15]
+            blk = np.zeros(16, np.float32)
+            blk[0], blk[1:1 + len(chunk)] = b, chunk
+            blocks.append(blk)
+    per_row = K // 16
+    n = -(-len(blocks) // per_row) * per_row
+    out = np.zeros((n, 16), np.float32)
+    out[:len(blocks)] = np.stack(blocks)
+    return (out.reshape(-1, K).view(np.uint32) >> 16).astype(np.uint16)

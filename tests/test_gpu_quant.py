@@ -197,6 +197,21 @@ def test_fp8_reciprocal_form_rows(q, orc):
         assert np_f32(b["scales"])[0].view(np.uint32) == np.float32(s).view(np.uint32)
 
 
+def test_nvfp4_step_sweeps(q, orc):
+    """Sweeps of bf16 blocks under fixed tensor amaxes, which put block and
+    element values within an ulp of code midpoints at both NVFP4 steps: the
+    kernel's codes, block scales and global scale equal the oracle's."""
+    from hard_cases import NVFP4_AMAXES, nvfp4_block_sweep
+    for A in NVFP4_AMAXES:
+        rows = nvfp4_block_sweep(A)
+        R, K = rows.shape
+        b = run(q, q.Fmt.NVFP4, torch.from_numpy(rows.view(np.int16)).view(torch.bfloat16))
+        packed, sc, g = orc.quant_nvfp4(rows)
+        assert np.array_equal(np_u8(b["codes"]).reshape(R, K // 2), packed), A
+        assert np.array_equal(np_u8(b["scales"])[: R * K // 16].reshape(R, K // 16), sc), A
+        assert np_f32(b["global"])[0].view(np.uint32) == np.float32(g).view(np.uint32), A
+
+
 def test_leading_dimension_is_honoured(q, orc):
     """A strided view (ld > K) quantizes exactly like its contiguous copy."""
     big = inputs.outlier_channel_bf16(96, 4096, 5)

@@ -351,6 +351,66 @@ def test_nvfp4_exact_bruteforce_small(orc):
                 assert codes[i, 16 * blk + k] == brute_nearest(float(seg[k] * rb), e2m1, 6.0, 1), (i, blk, k)
 
 
+def _straddle(lo, hi, mids):
+    """True where some midpoint m satisfies lo <= m <= hi (the codes may differ)."""
+    return np.searchsorted(mids, lo, "left") != np.searchsorted(mids, hi, "right")
+
+
+def _fragile(v, mids):
+    """True where v lies within two fp32 ulps of a code midpoint: there any
+    one-ulp change in the steps before the conversion can change the code."""
+    lo = np.nextafter(np.nextafter(v, np.float32(0)), np.float32(0))
+    hi = np.nextafter(np.nextafter(v, np.float32(np.inf)), np.float32(np.inf))
+    return _straddle(lo, hi, mids)
+
+
+def test_nvfp4_steps_on_fragile_values(orc):
+    """Reading R3's fp32 steps, on sweeps of bf16 blocks under fixed tensor
+    amaxes: wherever the block value b * fl(448/A) or the element value
+    x * fl(fl(2688/A) / dec(sb)) lies within two ulps of a code midpoint, the
+    oracle's code is the one an exact-rational search over all codes gives
+    for R3's value.  The sweeps include values where the variants b / fl(6 g)
+    and x / fl(dec(sb) g) round to another code, so either variant fails."""
+    from hard_cases import NVFP4_AMAXES, nvfp4_block_sweep
+    from test_oracle_codecs import brute_nearest
+    e4m3 = [(c, orc.dec_e4m3(c)) for c in range(256) if not math.isnan(orc.dec_e4m3(c))]
+    e2m1 = [(c, orc.dec_e2m1(c)) for c in range(16)]
+    pos4 = np.array(sorted({abs(v) for _, v in e4m3}))
+    mids4, mids2 = (pos4[1:] + pos4[:-1]) / 2, (E2M1_POS[1:] + E2M1_POS[:-1]) / 2
+    dec4 = np.array([orc.dec_e4m3(c) for c in range(256)], np.float32)
+    f32 = np.float32
+    n_sb = n_el = sep_sb = sep_el = 0
+    for A in NVFP4_AMAXES:
+        rows = nvfp4_block_sweep(A)
+        packed, sc, g = orc.quant_nvfp4(rows)
+        x = np.abs(vals(rows).astype(np.float32).reshape(-1, 16))
+        b = x.max(1)
+        q, rg, gg = f32(448) / f32(A), f32(2688) / f32(A), f32(A) / f32(2688)
+        assert f32(g) == gg
+        sc = sc.reshape(-1)
+        v1, v2 = b * q, b / (f32(6) * gg)
+        for i in np.nonzero(_fragile(v1, mids4) | ((v1 != v2) & _straddle(np.minimum(v1, v2),
+                                                                        np.maximum(v1, v2), mids4)))[0]:
+            c1 = brute_nearest(float(v1[i]), e4m3, 448.0, 3)
+            assert sc[i] == c1, (A, i, b[i])
+            n_sb += 1
+            sep_sb += c1 != brute_nearest(float(v2[i]), e4m3, 448.0, 3)
+        dsb = dec4[sc]
+        ok = dsb > 0
+        rb = np.where(ok, rg / np.where(ok, dsb, f32(1)), f32(0)).astype(np.float32)
+        e1 = x * rb[:, None]
+        e2 = x / np.where(ok, dsb * gg, f32(1))[:, None]
+        codes = unpack_e2m1(packed).reshape(-1, 16)
+        cand = ok[:, None] & (_fragile(e1, mids2) | ((e1 != e2) & _straddle(np.minimum(e1, e2),
+                                                                           np.maximum(e1, e2), mids2)))
+        for i, k in zip(*np.nonzero(cand)):
+            c1 = brute_nearest(float(e1[i, k]), e2m1, 6.0, 1)
+            assert codes[i, k] == c1, (A, i, k, x[i, k])
+            n_el += 1
+            sep_el += c1 != brute_nearest(float(e2[i, k]), e2m1, 6.0, 1)
+    assert sep_sb > 0 and sep_el > 0, (n_sb, n_el, sep_sb, sep_el)     # the sweeps separate R3 from both variants
+
+
 def test_nvfp4_worked_blocks(orc):
     """Four blocks worked by hand.  The tensor amax is 448, so 448/A = 1 and
     2688/A = 6 exactly, and g = fl(448/2688).
