@@ -83,3 +83,30 @@ def nvfp4_block_sweep(A: float, binades: int = 5, K: int = 256) -> np.ndarray:
     out = np.zeros((n, 16), np.float32)
     out[:len(blocks)] = np.stack(blocks)
     return (out.reshape(-1, K).view(np.uint32) >> 16).astype(np.uint16)
+
+
+def int4_half_step_weight(N: int = 64, s: float = 7.0 / 512) -> np.ndarray:
+    """bf16 bits of W [N, 256] (two groups of 128 per channel) in which every
+    group spans exactly 15 steps of s: its minimum is -z0 s with z0 in
+    {0, 1, 2, 4, 8} (even channels) or -(z0 + 1/2) s with z0 in
+    {3, 6, 9, 12, 14} (odd channels), and its maximum 15 steps above, so its
+    step is exactly s.  The other values are (k + 1/2) s for
+    every half step inside the range.  With s = 7 * 2^-9 all of them are bf16
+    values, and 1/s is inexact in fp32, so x * fl(1/s) often rounds to a value
+    next to the half-integer k + 1/2 instead of onto it."""
+    w = np.zeros((N, 256), np.float32)
+    for n in range(N):
+        for g in range(2):
+            if n % 2:
+                # the minimum itself half a step off the grid: -min / s = z0 + 1/2 sits next to a tie too
+                z0 = (6, 12, 14, 3, 9)[(n + 3 * g) % 5]
+                lo, hi = -(z0 + 0.5) * s, (14.5 - z0) * s
+            else:
+                z0 = (0, 1, 2, 4, 8)[(n + 3 * g) % 5]
+                lo, hi = -z0 * s, (15 - z0) * s
+            vals = [lo, hi] + [(k + 0.5) * s for k in range(-z0, 15 - z0) if lo <= (k + 0.5) * s <= hi]
+            row = np.resize(np.array(vals, np.float32), 128)
+            w[n, 128 * g:128 * g + 128] = row
+    bits = w.view(np.uint32)
+    assert not (bits & 0xFFFF).any()                    # every value is a bf16 value
+    return (bits >> 16).astype(np.uint16)

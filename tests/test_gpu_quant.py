@@ -177,6 +177,19 @@ def test_int4_g128(q, orc, N, K, kind):
     assert np.array_equal(b["zeros"].cpu().numpy().view(np.int32).reshape(K // 128, N // 8), qz)
 
 
+def test_int4_half_step_groups(q, orc):
+    """Groups whose values x * fl(1/s) and -min * fl(1/s) sit next to rounding
+    ties: the kernel's codes, scales and zero points equal the oracle's."""
+    from hard_cases import int4_half_step_weight
+    w = int4_half_step_weight()
+    N, K = w.shape
+    b = run(q, q.Fmt.INT4_G128_ASYM, torch.from_numpy(w.view(np.int16)).view(torch.bfloat16), weight=True)
+    qw, sc, qz = orc.quant_int4_g128(w)
+    assert np.array_equal(b["codes"].cpu().numpy().view(np.int32).reshape(K // 8, N), qw)
+    assert np.array_equal(b["scales"].cpu().numpy().view(np.uint16).reshape(K // 128, N), sc)
+    assert np.array_equal(b["zeros"].cpu().numpy().view(np.int32).reshape(K // 128, N // 8), qz)
+
+
 def test_fp8_reciprocal_form_rows(q, orc):
     """Rows on which x * fl(448 / amax) and x / fl(amax / 448) round to
     different codes: the kernels follow the oracle (the reciprocal form) bit

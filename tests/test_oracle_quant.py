@@ -639,6 +639,39 @@ def test_int4_zero_point_and_codes_bruteforce(orc):
                 assert q[g * 128 + k, n] == nearest(t, range(-zb, 16 - zb)) + zb, (n, g, k)
 
 
+def test_int4_codes_at_half_steps(orc):
+    """Reading R4: q = clamp(rint(x * fl(1/s)) + z) and z = clamp(rint(-min * fl(1/s))),
+    1/s taken once in fp32.  On groups of exact half steps (s = 7 * 2^-9, so
+    1/s is inexact) x * fl(1/s) lies within an ulp of k + 1/2, where the
+    division form x / s would tie to the even integer instead.  The oracle
+    follows R4, checked by exact rational distance (round half to even)."""
+    from hard_cases import int4_half_step_weight
+    w = int4_half_step_weight()
+    N, K = w.shape
+    qw, sc, qz = orc.quant_int4_g128(w)
+    q, z = unpack_int4(qw, qz, N, K)
+    f32 = np.float32
+    wv = vals(w).astype(np.float32)
+    s = vals(sc).astype(np.float32)
+    differ = z_differ = 0
+    for n in range(N):
+        for g in range(K // 128):
+            grp = wv[n, 128 * g:128 * g + 128]
+            sg = s[g, n]
+            assert sg == f32(7.0 / 512)
+            r = f32(1) / sg
+            mn = f32(-min(0.0, grp.min()))
+            zg = min(15, max(0, round(Fraction(float(mn * r)))))
+            assert z[g, n] == zg
+            z_differ += zg != min(15, max(0, round(Fraction(float(mn)) / Fraction(float(sg)))))
+            for k in range(128):
+                want = min(15, max(0, round(Fraction(float(grp[k] * r))) + zg))
+                assert q[128 * g + k, n] == want, (n, g, k)
+                alt = min(15, max(0, round(Fraction(float(grp[k])) / Fraction(float(sg))) + zg))
+                differ += want != alt
+    assert differ > 0 and z_differ > 0         # the groups do separate R4 from the division forms
+
+
 # ------------------------------------------------------------------ INT8 per row
 def test_int8_worked_rows_ties_and_saturation(orc):
     """Rows chosen so that 127/amax is a power of two: x * r is exact and the
