@@ -110,3 +110,21 @@ def int4_half_step_weight(N: int = 64, s: float = 7.0 / 512) -> np.ndarray:
     bits = w.view(np.uint32)
     assert not (bits & 0xFFFF).any()                    # every value is a bf16 value
     return (bits >> 16).astype(np.uint16)
+
+
+def row_amax_sweep(lo_exp: int = -4, hi_exp: int = 8, stride: int = 3, K: int = 256) -> np.ndarray:
+    """bf16 bits of rows that each start with their amax a and hold bf16 values
+    x <= a after it: for every `stride`-th bf16 a in [2^lo_exp, 2^hi_exp),
+    every bf16 x <= a of that range appears once (K - 1 per row).  Per-row
+    encoders multiply x by one rounded reciprocal of a, so the sweep meets the
+    values where that product sits next to a rounding tie."""
+    grid = bf16_grid(lo_exp, hi_exp)
+    rows = []
+    for a in grid[::stride]:
+        xs = grid[grid <= a]
+        for i in range(0, len(xs), K - 1):
+            row = np.zeros(K, np.float32)
+            chunk = xs[i:i + K - 1]
+            row[0], row[1:1 + len(chunk)] = a, chunk
+            rows.append(row)
+    return (np.stack(rows).view(np.uint32) >> 16).astype(np.uint16)

@@ -177,6 +177,20 @@ def test_int4_g128(q, orc, N, K, kind):
     assert np.array_equal(b["zeros"].cpu().numpy().view(np.int32).reshape(K // 128, N // 8), qz)
 
 
+def test_row_amax_sweep(q, orc):
+    """Rows led by their amax with every bf16 value below it: the per-row
+    encoders' products x * fl(c / amax) meet values next to rounding ties; the
+    INT8 and per-token FP8 kernels equal the oracle on every row."""
+    from hard_cases import row_amax_sweep
+    rows = row_amax_sweep()
+    x = torch.from_numpy(rows.view(np.int16)).view(torch.bfloat16)
+    for fmt, ref in [(q.Fmt.INT8_ROW, orc.quant_int8_row), (q.Fmt.FP8_TOKEN, orc.quant_fp8_token)]:
+        b = run(q, fmt, x)
+        codes, s = ref(rows)
+        assert np.array_equal(np_u8(b["codes"]).reshape(rows.shape), codes.view(np.uint8)), fmt
+        assert np.array_equal(np_f32(b["scales"]).view(np.uint32), np.asarray(s, np.float32).view(np.uint32)), fmt
+
+
 def test_int4_half_step_groups(q, orc):
     """Groups whose values x * fl(1/s) and -min * fl(1/s) sit next to rounding
     ties: the kernel's codes, scales and zero points equal the oracle's."""

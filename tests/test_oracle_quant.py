@@ -686,6 +686,35 @@ def test_int8_worked_rows_ties_and_saturation(orc):
     assert s.tolist() == [1.0, 2.0]
 
 
+def test_int8_codes_follow_the_reciprocal_form(orc):
+    """Reading R13: code = clamp(rint(x * fl(127 / amax))).  On a sweep of rows
+    led by their amax (tests/hard_cases.py), wherever x * fl(127/amax) lies
+    within two ulps of a half-integer the oracle's code is the nearest integer
+    (half to even) by exact rational distance; the sweep includes rows where
+    the division form x / fl(amax / 127) rounds to another integer."""
+    from hard_cases import row_amax_sweep
+    rows = row_amax_sweep()
+    codes, scales = orc.quant_int8_row(rows)
+    f32 = np.float32
+    x = vals(rows).astype(np.float32)
+    a = np.abs(x).max(1)
+    r = (f32(127) / a).astype(np.float32)
+    assert np.array_equal(scales, (a / f32(127)).astype(np.float32))
+    v = x * r[:, None]
+    lo = np.nextafter(np.nextafter(v, f32(-np.inf)), f32(-np.inf))
+    hi = np.nextafter(np.nextafter(v, f32(np.inf)), f32(np.inf))
+    fragile = np.floor(lo - f32(0.5)) != np.floor(hi - f32(0.5))        # a half-integer in [lo, hi]
+    alt = np.rint(x / (a / f32(127))[:, None])
+    checked = separated = 0
+    c = codes.view(np.int8).astype(np.int64)
+    for i, k in zip(*np.nonzero(fragile)):
+        want = min(127, max(-127, round(Fraction(float(v[i, k])))))
+        assert c[i, k] == want, (i, k, x[i, k])
+        checked += 1
+        separated += want != alt[i, k]
+    assert checked > 500 and separated > 0
+
+
 def test_int8_amax_maps_to_127_and_codes_are_nearest(orc):
     R, K = 48, 384
     x = bf16_bits(inputs.outlier_channel_bf16(R, K, 91))
