@@ -128,3 +128,13 @@ def row_amax_sweep(lo_exp: int = -4, hi_exp: int = 8, stride: int = 3, K: int = 
             row[0], row[1:1 + len(chunk)] = a, chunk
             rows.append(row)
     return (np.stack(rows).view(np.uint32) >> 16).astype(np.uint16)
+
+
+def tiles_of_pairs(pairs, n_tiles: int = 64) -> np.ndarray:
+    """bf16 bits of W [128, 128 * n] holding one pair per 128 x 128 tile:
+    amax at the tile's (0, 0) and x at (0, 1), zeros elsewhere."""
+    pairs = list(pairs)[:n_tiles]
+    w = np.zeros((128, 128 * len(pairs)), np.float32)
+    for t, (a, x) in enumerate(pairs):
+        w[0, 128 * t], w[0, 128 * t + 1] = a, x
+    return (w.view(np.uint32) >> 16).astype(np.uint16)

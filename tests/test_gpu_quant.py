@@ -217,6 +217,13 @@ def test_fp8_reciprocal_form_rows(q, orc):
         s = np.asarray(s, np.float32)
         assert np.array_equal(np_u8(b["codes"]).reshape(rows.shape), codes)
         assert np.array_equal(np_f32(b["scales"]).reshape(s.shape).view(np.uint32), s.view(np.uint32))
+    from hard_cases import tiles_of_pairs
+    pairs = fp8_reciprocal_candidates([orc.dec_e4m3(c) for c in range(256)])
+    tiles = tiles_of_pairs(pairs[::max(1, len(pairs) // 64)])
+    b = run(q, q.Fmt.FP8_BLOCK128, torch.from_numpy(tiles.view(np.int16)).view(torch.bfloat16), weight=True)
+    codes, s = orc.quant_fp8_block128(tiles)
+    assert np.array_equal(np_u8(b["codes"]).reshape(tiles.shape), codes)
+    assert np.array_equal(np_f32(b["scales"]).reshape(s.shape).view(np.uint32), s.view(np.uint32))
     for i in range(0, len(rows), max(1, len(rows) // 16)):
         b = run(q, q.Fmt.FP8_TENSOR, x[i:i + 1])
         codes, s = orc.quant_fp8_tensor(rows[i:i + 1])

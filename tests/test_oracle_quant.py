@@ -146,6 +146,11 @@ def test_fp8_codes_follow_the_reciprocal_form(orc):
     for (a, x), w, row in list(zip(pairs, want, rows))[:20]:
         tcodes, _ = orc.quant_fp8_tensor(row[None, :])
         assert tcodes[0, 1] == w
+    from hard_cases import tiles_of_pairs
+    stride = len(pairs) // 64
+    tiles = tiles_of_pairs(pairs[::stride])
+    bcodes, _ = orc.quant_fp8_block128(tiles)
+    assert list(bcodes[0, 1::128]) == want[::stride][:64]
 
 
 def test_fp8_group128_amax_maps_to_448_and_codes_are_nearest(orc):
