@@ -57,6 +57,8 @@ def parse_args():
     ap.add_argument("--rows-json", default=None, help="also write the per-row breakdown here")
     ap.add_argument("--eager", action="store_true", help="launch call by call instead of replaying a CUDA graph")
     ap.add_argument("--only", default=None, help="keep only linears whose name contains this string")
+    ap.add_argument("--no-cold", action="store_true", help="skip the cold-L2 timing of the HBM-bound calls")
+    ap.add_argument("--cold-iters", type=int, default=20)
     ap.add_argument("--next", action="store_true",
                     help="measure the next rows instead (MXFP4 W4A4 on the MXFP8 workload's shapes, FP8 "
                          "1x128-group and INT8 W8A8 on the DiT MLP shapes, the per-tensor FP8 linear with "
@@ -121,7 +123,8 @@ def config_block(args):
                       "mxfp8 M20280 (K,N){(5120,13824),(13824,5120),(5120,5120)}",
                       "mixed M32768: 4x nvfp4 3072x3072 + 4x fp8_block (3072<->12288)"],
         "step": "per linear: weight quantize + activation quantize + quantized GEMM",
-        "l2": "inputs larger than L2: each step streams several GB through the 126 MB L2 between reuses",
+        "l2": ("step: inputs larger than L2 (each step streams several GB through the 126 MB L2 between "
+               "reuses); HBM-bound rows also timed call by call after an L2 flush (rows.*.cold)"),
         "parallelism": f"replicas x{args.gpus}",
     }
 
@@ -241,11 +244,10 @@ class Job:
         return xb + wb + lin.M * lin.N * 2
 
 
-# DRAM traffic (read + write bytes) of one captured launch of the dominant
-# kernel, from the ncu summary in profiles/gemm_fp8_block_M4096_K3072_N12288.md.
-# It is scaled to the step's average launch by algorithmic bytes, and reported
-# as null once the kernel's code (comments and whitespace aside) differs from
-# the code the counters came from.
+# DRAM traffic (read + write bytes) of one ncu-captured launch of the dominant
+# kernel.  It is scaled to the step's average launch by algorithmic bytes, and
+# reported as null once the kernel's code (comments and whitespace aside)
+# differs from the code the counters came from.
 MEASURED_TRAFFIC = {
     "gemm_fp8_block": {
         "dram_bytes": 79162624 + 57511936,
@@ -295,7 +297,10 @@ def kernel_name(job, op):
                        F.FP8_GROUP128: "fp8_group128", F.INT8_ROW: "int8_row"}[fmt]
 
 
-def tensor_peak(peaks, wf, q, sustained=True):
+def tensor_peak(peaks, wf, q, sustained=False):
+    """The format's dense tensor peak: the measured bf16 rate (burst for a
+    timed region well under a second, as here; sustained for seconds-long
+    loops under the power cap) times the nominal format ratio."""
     bf16 = peaks.get("bf16_tflops_sustained" if sustained else "bf16_tflops") or (1700.0 if sustained else 1900.0)
     # W4A16 and INT8 (no integer MMA on sm_103a) run kind::f16, at the bf16 rate
     ratio = FP4_RATIO if wf in (q.Fmt.NVFP4, q.Fmt.MXFP4) else (
@@ -423,6 +428,7 @@ def run_native(args, rank, world, local_rank):
             tf = (r["flops"] / per_call_steps) / (ms * 1e-3) / 1e12
             d["tflops"] = round(tf, 1)
             d["tensor_frac"] = round(tf / tensor_peak(peaks, r["wf"], q), 3)
+            d["tensor_frac_of_sustained"] = round(tf / tensor_peak(peaks, r["wf"], q, sustained=True), 3)
         out_rows[name] = d
 
     # dominant kernel: the row with the largest share of the step
@@ -434,10 +440,13 @@ def run_native(args, rank, world, local_rank):
         peak = tensor_peak(peaks, dr["wf"], q)
         achieved = per_launch / (dom_ms_per_launch * 1e-3) / 1e12
         traffic, traffic_src = measured_traffic(dom, dr["bytes"] / dr["launches"])
+        peak_s = tensor_peak(peaks, dr["wf"], q, sustained=True)
         roofline = {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 1), "peak": round(peak, 1),
                     "unit": "TFLOP/s", "frac": round(achieved / peak, 3), "traffic": traffic,
                     "traffic_source": traffic_src, "algorithmic_bytes_per_launch": round(dr["bytes"] / dr["launches"]),
-                    "peak_source": f"{peak_src} bf16 sustained x nominal format ratio",
+                    "peak_source": (f"{peak_src} bf16 burst x nominal format ratio (the timed region lasts "
+                                    f"{ms_total / 1e3:.2f} s at the sampled clocks)"),
+                    "peak_sustained": round(peak_s, 1), "frac_of_sustained": round(achieved / peak_s, 3),
                     "algorithmic_per_launch": per_launch}
     else:
         per_launch = dr["bytes"] / dr["launches"]
@@ -447,6 +456,14 @@ def run_native(args, rank, world, local_rank):
                     "peak_source": peak_src, "algorithmic_per_launch": per_launch}
 
     launches = sum(j.launches() for j in jobs) * args.steps
+
+    # ---- the HBM-bound rows again, each call alone after an L2 flush
+    cold = None
+    if not args.no_cold:
+        cold = cold_rows(jobs, dev, hbm_peak, iters=args.cold_iters)
+        for name, c in cold["rows"].items():
+            if name in out_rows:
+                out_rows[name]["cold"] = c
 
     # ---- end to end through the public API with host buffers
     e2e = None
@@ -461,7 +478,62 @@ def run_native(args, rank, world, local_rank):
            "rows": out_rows, "launch_mode": mode}
     if e2e:
         res["e2e"] = e2e
+    if cold:
+        res["cold_l2"] = {"method": cold["method"], "w4a16_calls": cold["w4a16_calls"]}
     return res, jobs
+
+
+def cold_rows(jobs, dev, hbm_peak, iters=20, warm=3):
+    """Each HBM-bound call (every quantizer, the W4A16 GEMMs) timed alone with
+    a cold L2: before every timed call a 512 MiB buffer (over 4x the L2) is
+    read through, which leaves only its own clean lines in L2.  CUDA events
+    on the launching stream; the median over `iters` calls after `warm`."""
+    import torch
+    F = jobs[0].q.Fmt
+    flush = torch.ones(64 << 20, dtype=torch.int64, device=dev)      # 512 MiB, written once here
+    ops = []
+    for j in jobs:
+        ops.append((j, "quant_w"))
+        if j.xb is not None:
+            ops.append((j, "quant_x"))
+        if j.wf == F.INT4_G128_ASYM:
+            ops.append((j, "gemm"))
+    stream = torch.cuda.current_stream()
+    sink = torch.empty(1, dtype=torch.int64, device=dev)
+    meas = []
+    for j, op in ops:
+        fn = getattr(j, op)
+        evs = []
+        for it in range(warm + iters):
+            torch.sum(flush, out=sink)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            if it >= warm:
+                evs.append((e0, e1))
+        torch.cuda.synchronize()
+        meas.append((j, op, statistics.median(a.elapsed_time(b) for a, b in evs)))
+    rows, w4 = {}, []
+    for j, op, ms in meas:
+        name = kernel_name(j, op)
+        nbytes = j.gemm_bytes() if op == "gemm" else (j.bytes_w_quant() if op == "quant_w" else j.bytes_x_quant())
+        r = rows.setdefault(name, {"calls": 0, "ms": 0.0, "bytes": 0})
+        r["calls"] += 1
+        r["ms"] += ms
+        r["bytes"] += nbytes
+        if op == "gemm":
+            w4.append({"M": j.lin.M, "K": j.lin.K, "N": j.lin.N, "us": round(ms * 1e3, 2),
+                       "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1),
+                       "hbm_frac": round(nbytes / (ms * 1e-3) / 1e9 / hbm_peak, 3)})
+    out = {}
+    for name, r in rows.items():
+        gbs = r["bytes"] / (r["ms"] * 1e-3) / 1e9
+        out[name] = {"calls": r["calls"], "ms_sum_of_medians": round(r["ms"], 4), "gbs": round(gbs, 1),
+                     "hbm_frac": round(gbs / hbm_peak, 3)}
+    return {"rows": out, "w4a16_calls": w4,
+            "method": (f"each call alone, after reading a 512 MiB buffer (L2 about 126 MB); median of {iters} "
+                       f"calls after {warm}")}
 
 
 def run_e2e(args, jobs, stream, flops_step, world, dev):

@@ -49,8 +49,8 @@
  *   NVFP4: g = A/2688 (A = tensor amax); block scale sb = UE4M3(b * (448/A));
  *     code = E2M1(x * ((2688/A)/dec(sb))), 0 when dec(sb) == 0.
  *   INT4: per (n, group of 128 k): range [min(0,min), max(0,max)],
- *     s = bf16((max-min)/15) (1 if 0), z = clamp(rint(-min/s)), q =
- *     clamp(rint(x/s) + z) with 1/s computed once in fp32.
+ *     s = bf16((max-min)/15) (1 if 0), r = 1/s in fp32, z = clamp(rint(-min*r)),
+ *     q = clamp(rint(x*r) + z), clamps to [0, 15].
  *   INT8 (per row): s = amax/127, code = clamp(rint(x * (127/amax)), -127,
  *     127), s = 1 and multiplier 1 when amax == 0.
  *   Conversions round to nearest even and saturate (satfinite); a zero keeps
@@ -123,7 +123,10 @@ const char *qlin_status_string(qlin_status s);
 /* ---------------------------------------------------------------- sizes
  * Byte sizes of the buffers the quantizers write, for `rows` rows of K
  * elements (rows = N for weights, M for activations).  0 means "not used by
- * this format" or invalid arguments.                                        */
+ * this format" or invalid arguments.  The layouts are those of the formats'
+ * sources cited above (the GPTQ packing of the int4 page's
+ * auto_round:auto_gptq format; the E8M0 and UE4M3 scale bytes of the MX and
+ * NVFP4 formats).                                                           */
 
 /* Codes: FP8 formats and INT8_ROW rows*K; NVFP4 and MXFP4 rows*K/2 (lower k in the low nibble);
  * INT4 (K/8)*rows*4 as int32 [K/8, rows], k = 8i+j in bits [4j,4j+4).       */
@@ -153,7 +156,8 @@ size_t qlin_gemm_workspace_bytes(qlin_format w_fmt, qlin_format x_fmt,
 
 /* ---------------------------------------------------------------- quantizers
  * Quantize a bf16 matrix src[rows, K] (leading dimension ld >= K, elements)
- * into caller-owned buffers, on `stream`.
+ * into caller-owned buffers, on `stream`.  Both entry points apply the
+ * numeric rules above; they differ in where the pages place them (below).
  *   codes_dev          qlin_codes_bytes(fmt, rows, K) bytes, 16-byte aligned
  *   scales_dev         qlin_scales_bytes(fmt, layout, rows, K) bytes
  *   zeros_dev          INT4 only (else NULL)
@@ -171,11 +175,21 @@ size_t qlin_gemm_workspace_bytes(qlin_format w_fmt, qlin_format x_fmt,
  * Errors: QLIN_ERR_INVALID_ARG, QLIN_ERR_ALIGNMENT, QLIN_ERR_UNSUPPORTED
  *   (QLIN_BF16, or INT4 through qlin_quantize_act), QLIN_ERR_WORKSPACE,
  *   QLIN_ERR_CUDA.                                                          */
+/* Load-time weight quantization, once per weight: "vLLM-Omni 在线量化（Online
+ * Quantization）完全指南", section "在线量化的底层工作原理", stage 2 (the BF16
+ * weight is quantized after loading, process_weights_after_loading, and the
+ * original is released).  Every format except QLIN_BF16; rows = N output
+ * channels of W[N, K].                                                      */
 qlin_status qlin_quantize_weight(qlin_format fmt, const void *w_bf16_dev, int64_t N, int64_t K,
                                  int64_t ldw, void *codes_dev, void *scales_dev, void *zeros_dev,
                                  float *global_dev, qlin_scale_layout layout, void *workspace_dev,
                                  size_t workspace_bytes, int *dev_status_dev, qlin_stream_t stream);
 
+/* Dynamic activation quantization, every call: the same section, stage 3
+ * (_quantize_activation on the flattened input; activation scales are
+ * dynamic only, section "核心参数详解").  Every format except QLIN_BF16 and
+ * QLIN_INT4_G128_ASYM (int4 is weight-only: W4A16 takes bf16 activations);
+ * rows = M tokens of X[M, K].                                               */
 qlin_status qlin_quantize_act(qlin_format fmt, const void *x_bf16_dev, int64_t M, int64_t K,
                               int64_t ldx, void *codes_dev, void *scales_dev, float *global_dev,
                               qlin_scale_layout layout, void *workspace_dev, size_t workspace_bytes,
@@ -244,6 +258,8 @@ qlin_status qlin_gemm(qlin_format w_fmt, qlin_format x_fmt, int64_t M, int64_t N
  * The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current, so make the first call
  * before any stream capture, and call with the stream's device current.
+ * The address is kept per device and context; after cudaDeviceReset the next
+ * call looks it up again in the new context (again outside any capture).
  * The array is shared by all calls on a device and keeps the last call's
  * contents (each call rewrites the slots it reads, nothing needs clearing);
  * calls that overlap on the GPU race on it.  Allocates nothing; errors as

@@ -13,6 +13,7 @@
 // contents; each call overwrites exactly the slots it then reads, so nothing
 // has to be cleared.  Two calls that overlap on the GPU (different streams
 // without ordering) race on it.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -29,22 +30,57 @@ static __device__ __align__(256) float g_amax_partials[QLIN_NOALLOC_MAX_PARTIALS
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
-float* g_partials_ptr[kMaxDevices] = {};
+struct Cached {
+    unsigned long long ctx_id;   // the context the address belongs to (0: none yet)
+    float* ptr;
+};
+Cached g_partials[kMaxDevices] = {};
+
+// Unique id of the calling thread's current context, 0 if none is current or
+// the driver does not say.  Ids are never reused within a process, so a
+// context created after a device reset gets a new one.
+unsigned long long current_context_id() {
+    using GetCurrent = CUresult (*)(CUcontext*);
+    using GetId = CUresult (*)(CUcontext, unsigned long long*);
+    static GetCurrent get_current = nullptr;
+    static GetId get_id = nullptr;
+    static bool looked_up = false;
+    if (!looked_up) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<GetCurrent>(p);
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<GetId>(p);
+        looked_up = true;
+    }
+    CUcontext c = nullptr;
+    unsigned long long id = 0;
+    if (!get_current || !get_id || get_current(&c) != CUDA_SUCCESS || !c || get_id(c, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
 
 // Device address of g_amax_partials on the current device.  In host code the
-// symbol is only a stand-in; its device address has to be asked for, once
-// per device, with that device current.
+// symbol is only a stand-in; its device address has to be asked for with that
+// device current.  The answer is kept per device together with the id of the
+// context it came from, and asked for again when the device's context has
+// changed (after cudaDeviceReset the module is loaded anew, possibly
+// elsewhere).
 qlin_status partials_for_current_device(float** out) {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) return QLIN_ERR_CUDA;
     if (dev < 0 || dev >= kMaxDevices) return QLIN_ERR_UNSUPPORTED;
     std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_partials_ptr[dev]) {
+    const unsigned long long id = current_context_id();
+    if (!g_partials[dev].ptr || id == 0 || g_partials[dev].ctx_id != id) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_amax_partials) != cudaSuccess || !p) return QLIN_ERR_CUDA;
-        g_partials_ptr[dev] = static_cast<float*>(p);
+        g_partials[dev].ptr = static_cast<float*>(p);
+        g_partials[dev].ctx_id = current_context_id();   // the lookup makes the device's context current
     }
-    *out = g_partials_ptr[dev];
+    *out = g_partials[dev].ptr;
     return QLIN_OK;
 }
 

@@ -285,11 +285,15 @@ def gemm(w_fmt: Fmt, x_fmt: Fmt, M: int, N: int, K: int, x, x_scales, w_codes, w
     if bias is not None and (bias.dtype != torch.bfloat16 or bias.numel() < N or not bias.is_contiguous()):
         raise ValueError(f"bias: {N} contiguous bf16 values are required")
     wsb = qlin_gemm_workspace_bytes(w_fmt, x_fmt, M, N, K)
-    if wsb and workspace is None:
-        workspace = _empty(wsb, dev)
+    if workspace is None:
+        if wsb:
+            workspace = _empty(wsb, dev)
+    else:
+        _need(workspace, wsb, "workspace")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     rc = qlin_gemm(w_fmt, x_fmt, M, N, K, x.data_ptr(), _ptr(x_scales), _ptr(x_global), w_codes.data_ptr(),
                    _ptr(w_scales), _ptr(w_zeros), _ptr(w_global), _ptr(bias), y.data_ptr(), y.stride(0), layout,
-                   _ptr(workspace), wsb if workspace is not None else 0,
+                   _ptr(workspace), ws_bytes,
                    _ptr(status if status is not None else device_status(dev)), _stream(stream))
     _check(rc, "qlin_gemm")
     return y

@@ -138,3 +138,33 @@ def tiles_of_pairs(pairs, n_tiles: int = 64) -> np.ndarray:
     for t, (a, x) in enumerate(pairs):
         w[0, 128 * t], w[0, 128 * t + 1] = a, x
     return (w.view(np.uint32) >> 16).astype(np.uint16)
+
+
+def int4_scale_tie_weight(binades=(-20, -7, -3, 0, 4)) -> np.ndarray:
+    """bf16 bits of W [N, 128] (one int4 group per channel) whose range
+    D = max - min puts D / 15 on a bf16 rounding midpoint or within a few
+    fp32 ulps of one.  For a midpoint m = (257 + 2j) 2^(e-8) of binade e,
+    T = 15 (257 + 2j) has at most 13 significant bits; it is split into
+    hi = T with its low 5 bits cleared (at most 8 bits) and lo = T - hi (at
+    most 5 bits), both bf16 values once scaled by 2^(e-8).  Each (e, j) gives
+    six groups: max = hi and min = -lo, or max = lo and min = -hi, each with
+    lo as is (D / 15 = m exactly) or with lo * 8 -+ 1 in units of 2^(e-11)
+    (D / 15 = m -+ 2^(e-11) / 15, just off the midpoint).  The other values
+    of a group are zeros and min / 2."""
+    groups = []
+    for e in binades:
+        unit = 2.0 ** (e - 8)
+        for j in range(128):
+            T = 15 * (257 + 2 * j)
+            hi = T & ~0x1F
+            lo = T - hi
+            for lo_v in (lo * unit, (8 * lo - 1) * unit / 8, (8 * lo + 1) * unit / 8):
+                for mx, mn in ((hi * unit, -lo_v), (lo_v, -hi * unit)):
+                    g = np.zeros(128, np.float32)
+                    g[0], g[1], g[2] = mx, mn, mn / 2
+                    groups.append(g)
+    w = np.stack(groups)
+    w = np.concatenate([w, np.zeros(((-len(w)) % 8, 128), np.float32)])   # N multiple of 8
+    bits = w.view(np.uint32)
+    assert not (bits & 0xFFFF).any()                    # every value is a bf16 value
+    return (bits >> 16).astype(np.uint16)

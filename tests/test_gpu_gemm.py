@@ -106,7 +106,8 @@ def test_fp8_block_gemm_bias_ragged(q, orc):
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("B,K,N", [(1, 3072, 12288), (1, 12288, 3072)])
+@pytest.mark.parametrize("B", [1, 4, 8])
+@pytest.mark.parametrize("K,N", [(3072, 12288), (12288, 3072)])
 def test_fp8_block_gemm_full_size(q, orc, B, K, N):
     fp8_block_case(q, orc, 4096 * B, N, K, nrows=256)
 
@@ -244,8 +245,9 @@ def test_mxfp8_gemm(q, orc, M, N, K):
 
 
 @pytest.mark.slow
-def test_mxfp8_gemm_full_size(q, orc):
-    mxfp8_case(q, orc, 20280, 5120, 5120, nrows=256)
+@pytest.mark.parametrize("K,N", [(5120, 13824), (13824, 5120), (5120, 5120)])
+def test_mxfp8_gemm_full_size(q, orc, K, N):
+    mxfp8_case(q, orc, 20280, N, K, nrows=256)
 
 
 # ------------------------------------------------------------------ NVFP4

@@ -204,6 +204,20 @@ def test_int4_half_step_groups(q, orc):
     assert np.array_equal(b["zeros"].cpu().numpy().view(np.int32).reshape(K // 128, N // 8), qz)
 
 
+def test_int4_scale_tie_groups(q, orc):
+    """Groups whose (max - min) / 15 lies on a bf16 rounding midpoint or a few
+    fp32 ulps off one: the kernel's scales (and codes and zero points) equal
+    the oracle's, which rounds the range to nearest with ties to even."""
+    from hard_cases import int4_scale_tie_weight
+    w = int4_scale_tie_weight()
+    N, K = w.shape
+    b = run(q, q.Fmt.INT4_G128_ASYM, torch.from_numpy(w.view(np.int16)).view(torch.bfloat16), weight=True)
+    qw, sc, qz = orc.quant_int4_g128(w)
+    assert np.array_equal(b["scales"].cpu().numpy().view(np.uint16).reshape(K // 128, N), sc)
+    assert np.array_equal(b["codes"].cpu().numpy().view(np.int32).reshape(K // 8, N), qw)
+    assert np.array_equal(b["zeros"].cpu().numpy().view(np.int32).reshape(K // 128, N // 8), qz)
+
+
 def test_fp8_reciprocal_form_rows(q, orc):
     """Rows on which x * fl(448 / amax) and x / fl(amax / 448) round to
     different codes: the kernels follow the oracle (the reciprocal form) bit

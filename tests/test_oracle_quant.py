@@ -677,6 +677,88 @@ def test_int4_codes_at_half_steps(orc):
     assert differ > 0 and z_differ > 0         # the groups do separate R4 from the division forms
 
 
+def bf16_rne_exact(v: Fraction) -> Fraction:
+    """The bf16 value nearest to the exact rational v > 0, ties to an even
+    mantissa (8 significant bits), by integer arithmetic."""
+    unit = bf16_ulp(v)
+    n, rem = divmod(v, unit)
+    n = int(n)
+    if rem * 2 > unit or (rem * 2 == unit and n % 2):
+        n += 1
+    return n * unit
+
+
+def bf16_ulp(v: Fraction) -> Fraction:
+    """Spacing of the bf16 values in the binade of v > 0."""
+    e = v.numerator.bit_length() - v.denominator.bit_length()
+    if Fraction(2) ** e > v:
+        e -= 1
+    return Fraction(2) ** (e - 7)
+
+
+def _bf16_of_f32(a: np.ndarray, mode: str) -> np.ndarray:
+    """fp32 -> bf16 value by bits: 'rne', 'trunc' or 'half_away'."""
+    b = a.astype(np.float32).view(np.uint32).astype(np.uint64)
+    lo, kept = b & 0xFFFF, b >> 16
+    if mode == "rne":
+        kept += (lo > 0x8000) | ((lo == 0x8000) & (kept & 1 == 1))
+    elif mode == "half_away":
+        kept += lo >= 0x8000
+    return (kept.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def test_int4_scale_rounds_the_range_to_nearest_even(orc):
+    """Reading R4's scale step: s = bf16_RNE(fl((max - min) / 15)).  On groups
+    whose D / 15 is a bf16 rounding midpoint, or a few fp32 ulps off one
+    (tests/hard_cases.py), the oracle's stored scale is the bf16 value nearest
+    to the exact rational D / 15 with ties to even; the sweep separates that
+    from truncating to bf16, rounding ties away from zero, and multiplying by
+    fl(1/15) instead of dividing (each gives another scale on some group)."""
+    from hard_cases import int4_scale_tie_weight
+    w = int4_scale_tie_weight()
+    N, K = w.shape
+    qw, sc, qz = orc.quant_int4_g128(w)
+    s = vals(sc)[0]
+    wv = vals(w)
+    mx, mn = np.maximum(wv.max(1), 0.0), np.minimum(wv.min(1), 0.0)
+    live = mx > mn
+    assert live.sum() >= 3000
+    ties = 0
+    for n in np.flatnonzero(live):
+        d = Fraction(float(mx[n])) - Fraction(float(mn[n]))
+        want = bf16_rne_exact(d / 15)
+        assert Fraction(float(s[n])) == want, (n, float(mx[n]), float(mn[n]))
+        ties += abs(d / 15 - want) == bf16_ulp(d / 15) / 2
+    assert ties > 100                          # exact midpoints: the tie rule decides them
+    d32 = (mx.astype(np.float32) - mn.astype(np.float32)).astype(np.float32)
+    q32 = (d32 / np.float32(15)).astype(np.float32)
+    rcp = (d32 * (np.float32(1) / np.float32(15))).astype(np.float32)
+    for name, alt in [("trunc", _bf16_of_f32(q32, "trunc")), ("half_away", _bf16_of_f32(q32, "half_away")),
+                      ("reciprocal", _bf16_of_f32(rcp, "rne"))]:
+        assert (alt[live] != s[live]).any(), name
+
+
+def test_int4_scale_double_rounding_equals_single(orc):
+    """Why R4's scale step has no separate double-rounding reading:
+    bf16(fl32(D / 15)) equals bf16(D / 15) rounded once from the exact
+    quotient.  D = fl(max - min) and 15 m (m a bf16 midpoint) are both
+    multiples of the fp32 ulp of D, so a nonzero D - 15 m is at least that
+    ulp, and |D / 15 - m| >= ulp(D) / 15 > ulp(m) / 2: fl32(D / 15) never
+    lands on a midpoint that D / 15 itself is not on.  Checked exhaustively
+    on every pair of bf16 values max in [1, 4) and min in (-8, 0]."""
+    grid = np.concatenate([[0.0], np.arange(256, 512) / 256.0, np.arange(256, 512) / 128.0])
+    mxs = grid[grid >= 1]
+    mns = -np.concatenate([[0.0], grid[1:], np.arange(256, 512) / 64.0])
+    mx, mn = np.meshgrid(mxs, mns, indexing="ij")
+    d32 = (mx.astype(np.float32) - mn.astype(np.float32)).astype(np.float32)
+    assert np.array_equal(d32.astype(np.float64), mx - mn)          # the range itself is exact here
+    twice = _bf16_of_f32((d32 / np.float32(15)).astype(np.float32), "rne")
+    for i in range(0, mx.size, 7):
+        a, b = mx.flat[i], mn.flat[i]
+        assert Fraction(float(twice.flat[i])) == bf16_rne_exact((Fraction(a) - Fraction(b)) / 15), (a, b)
+    del orc
+
+
 # ------------------------------------------------------------------ INT8 per row
 def test_int8_worked_rows_ties_and_saturation(orc):
     """Rows chosen so that 127/amax is a power of two: x * r is exact and the

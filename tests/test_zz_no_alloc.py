@@ -47,6 +47,26 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls(q):
         assert scale.view(torch.int32).item() == ref["scales"][:1].view(torch.int32).item()
 
 
+def test_noalloc_at_its_largest_size(q):
+    """rows * K equal to the limit: every slot of the fixed array, the last
+    one included, is written and read; the result equals the workspace entry
+    point's bit for bit.  One row more at the same K is refused."""
+    K = 4096
+    rows = q.NOALLOC_MAX_ELEMENTS // K
+    x = inputs.normal_bf16((rows, K), 1.0, 73)
+    x[-1, -1] = 40.0                         # the tensor amax sits in the last partial's block
+    xd = x.cuda()
+    ref = q.quantize_act(q.Fmt.FP8_TENSOR, xd)
+    codes, scale = noalloc(q, xd)
+    torch.cuda.synchronize()
+    assert torch.equal(codes, ref["codes"][: codes.numel()])
+    assert scale.view(torch.int32).item() == ref["scales"][:1].view(torch.int32).item()
+    assert scale.view(torch.int32).item() == int(np.array([np.float32(40) / np.float32(448)]).view(np.int32)[0])
+    st = torch.cuda.current_stream().cuda_stream
+    assert q.qlin_quantize_fp8_tensor_noalloc(xd.data_ptr(), rows + 1, K, K, codes.data_ptr(), scale.data_ptr(),
+                                              st) == q.Status.WORKSPACE
+
+
 def test_noalloc_rejects_tensors_beyond_its_scratch(q):
     S = q.Status
     x = torch.zeros(16, dtype=torch.bfloat16, device="cuda")
