@@ -9,7 +9,7 @@ Two layers:
 * ``qlin_oracle.c`` (built here into ``_build/liboracle.so`` with gcc, strict
   IEEE binary32, no contraction): scalar codecs and quantizers, written one
   element at a time from the format definitions.  See its header for the
-  readings R1..R5 and R11..R13 taken where the pages name a format but print no
+  readings R1..R5, R11..R13 and R15 taken where the pages name a format but print no
   formula.
 * this module: numpy marshalling, and the GEMM reference, which is the plain
   definition Y = Xhat @ What^T evaluated in float64 over the dequantized
@@ -80,6 +80,7 @@ def _load():
             "oracle_quant_nvfp4": ([P, I64, I64, I64, P, P, P], None),
             "oracle_quant_mxfp4": ([P, I64, I64, I64, P, P], None),
             "oracle_quant_int4_g128": ([P, I64, I64, I64, P, P, P], None),
+            "oracle_quant_int4_g128_sym": ([P, I64, I64, I64, P, P, P], None),
             "oracle_quant_int8_row": ([P, I64, I64, I64, P, P], None),
             "oracle_dequant_fp8_tensor": ([P, I64, I64, F, P], None),
             "oracle_dequant_fp8_token": ([P, I64, I64, P, P], None),
@@ -251,6 +252,22 @@ def quant_int4_g128(w):
     sc = np.empty((K // 128, N), np.uint16)
     qz = np.empty((K // 128, N // 8), np.int32)
     _load().oracle_quant_int4_g128(_p(w), N, K, K, _p(qw), _p(sc), _p(qz))
+    return qw, sc, qz
+
+
+def quant_int4_g128_sym(w):
+    """int4 symmetric g128 RTN of W [N,K] (reading R15: range [-a, a], zero
+    point 8) -> (qweight int32 [K/8,N], scales bf16 bits uint16 [K/128,N],
+    qzeros int32 [K/128,N/8], every zero point 8).  Dequantize with
+    dequant_int4_g128."""
+    w = _bf16_bits(w)
+    N, K = w.shape
+    if N % 8 or K % 128:
+        raise ValueError("int4 g128 needs N multiple of 8 and K multiple of 128")
+    qw = np.empty((K // 8, N), np.int32)
+    sc = np.empty((K // 128, N), np.uint16)
+    qz = np.empty((K // 128, N // 8), np.int32)
+    _load().oracle_quant_int4_g128_sym(_p(w), N, K, K, _p(qw), _p(sc), _p(qz))
     return qw, sc, qz
 
 

@@ -61,6 +61,13 @@
  *       per activation token, s = amax/127, codes = clamp(rint(x * (127/amax)),
  *       -127, 127) as two's-complement bytes; amax == 0 gives s = 1 and
  *       multiplier 1.
+ *   R15 int4 symmetric ("vLLM-Omni는 AutoRound 양자화로 추론을 가속화합니다",
+ *       section "새로운 모델 양자화": the checkpoint's quantization_config
+ *       has "sym": true): the R4 group with its range taken symmetric,
+ *       [-a, a] with a = max |x| over the 128 elements, so s = bf16((a - (-a))/15)
+ *       (1 if that is 0) and r = 1/s as in R4; the zero point is the fixed
+ *       mid-code 8, not derived from the range, and q = clamp(rint(x*r) + 8)
+ *       in [0, 15].  Stored exactly like R4 (qzeros all 8).
  */
 #include <math.h>
 #include <stdint.h>
@@ -368,6 +375,41 @@ void oracle_quant_int4_g128(const uint16_t *w, int64_t N, int64_t K, int64_t ld,
             if (zf < 0.0f) zf = 0.0f;
             if (zf > 15.0f) zf = 15.0f;
             int z = (int)zf;
+            for (int k = 0; k < 128; k++) {
+                float qf = rintf(oracle_bf16_to_f32(grp[k]) * r) + (float)z;
+                if (qf < 0.0f) qf = 0.0f;
+                if (qf > 15.0f) qf = 15.0f;
+                int64_t kk = g * 128 + k;
+                uint32_t word = (uint32_t)qweight[(kk / 8) * N + n];
+                word |= (uint32_t)(int)qf << (4 * (kk % 8));
+                qweight[(kk / 8) * N + n] = (int32_t)word;
+            }
+            scales[g * N + n] = sbits;
+            uint32_t zw = (uint32_t)qzeros[g * (N / 8) + n / 8];
+            zw |= (uint32_t)z << (4 * (n % 8));
+            qzeros[g * (N / 8) + n / 8] = (int32_t)zw;
+        }
+}
+
+/* int4 symmetric, group 128 along K, round to nearest (R15).  Same
+ * layouts as oracle_quant_int4_g128; every stored zero point is 8. */
+void oracle_quant_int4_g128_sym(const uint16_t *w, int64_t N, int64_t K, int64_t ld,
+                                int32_t *qweight, uint16_t *scales, int32_t *qzeros)
+{
+    int64_t ng = K / 128;
+    memset(qweight, 0, sizeof(int32_t) * (size_t)(K / 8) * (size_t)N);
+    memset(qzeros, 0, sizeof(int32_t) * (size_t)ng * (size_t)(N / 8));
+    for (int64_t n = 0; n < N; n++)
+        for (int64_t g = 0; g < ng; g++) {
+            const uint16_t *grp = w + n * ld + g * 128;
+            float a = 0.0f;
+            for (int k = 0; k < 128; k++)
+                a = fmaxf(a, fabsf(oracle_bf16_to_f32(grp[k])));
+            uint16_t sbits = oracle_f32_to_bf16((a - (-a)) / 15.0f);
+            float s = oracle_bf16_to_f32(sbits);
+            if (s == 0.0f) { s = 1.0f; sbits = oracle_f32_to_bf16(1.0f); }
+            float r = 1.0f / s;
+            const int z = 8;
             for (int k = 0; k < 128; k++) {
                 float qf = rintf(oracle_bf16_to_f32(grp[k]) * r) + (float)z;
                 if (qf < 0.0f) qf = 0.0f;

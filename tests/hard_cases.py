@@ -168,3 +168,26 @@ def int4_scale_tie_weight(binades=(-20, -7, -3, 0, 4)) -> np.ndarray:
     bits = w.view(np.uint32)
     assert not (bits & 0xFFFF).any()                    # every value is a bf16 value
     return (bits >> 16).astype(np.uint16)
+
+
+def int4_sym_half_step_weight(N: int = 64, s: float = 7.0 / 512) -> np.ndarray:
+    """bf16 bits of W [N, 256] for the symmetric int4 rule: every group holds
+    its amax a = 7.5 s (so 2a / 15 = s exactly, a bf16 value, and 1/s is
+    inexact in fp32), with the sign of a alternating over channels, and
+    then the half steps (k + 1/2) s for k = -8 .. 7 and the whole steps k s
+    for k = -7 .. 7 in a per-group rotation.  x * fl(1/s) then often lands
+    next to the half-integer k + 1/2 instead of on it."""
+    w = np.zeros((N, 256), np.float32)
+    halves = [(k + 0.5) * s for k in range(-8, 8)]
+    wholes = [k * s for k in range(-7, 8)]
+    for n in range(N):
+        for g in range(2):
+            vals = halves + wholes
+            rot = (3 * n + 5 * g) % len(vals)
+            vals = vals[rot:] + vals[:rot]
+            row = np.resize(np.array(vals, np.float32), 128)
+            row[0] = 7.5 * s if (n + g) % 2 == 0 else -7.5 * s
+            w[n, 128 * g:128 * g + 128] = row
+    bits = w.view(np.uint32)
+    assert not (bits & 0xFFFF).any()                    # every value is a bf16 value
+    return (bits >> 16).astype(np.uint16)

@@ -759,6 +759,110 @@ def test_int4_scale_double_rounding_equals_single(orc):
     del orc
 
 
+# ------------------------------------------------------------------ int4 symmetric (R15)
+def test_int4_sym_scale_zero_point_and_range(orc):
+    """Reading R15: per group a = max |x|, s = bf16_RNE((a - (-a)) / 15) (the
+    bf16 value nearest to the exact 2a / 15, ties to even), zero point 8
+    everywhere, a zero group gets s = 1 and codes 8, and zero maps to 8."""
+    N, K = 64, 384
+    w = rand_bits((N, K), 91, 0.02)
+    w[3, 128:256] = 0                                                     # an all-zero group
+    w[4, :128] = bf16_bits(torch.from_numpy(np.abs(vals(w[4:5, :128]))).to(torch.bfloat16))[0]   # all >= 0
+    w[5, :64] = 0
+    qw, sc, qz = orc.quant_int4_g128_sym(w)
+    q, z = unpack_int4(qw, qz, N, K)
+    assert np.all(z == 8)
+    s = vals(sc)
+    wv = vals(w)
+    for n in range(N):
+        for g in range(K // 128):
+            grp = wv[n, 128 * g:128 * g + 128]
+            a = np.abs(grp).max()
+            if a == 0:
+                assert s[g, n] == 1.0 and np.all(q[128 * g:128 * g + 128, n] == 8)
+                continue
+            assert Fraction(float(s[g, n])) == bf16_rne_exact(Fraction(float(a)) * 2 / 15), (n, g)
+            qq = q[128 * g:128 * g + 128, n]
+            assert np.all(qq[grp == 0] == 8)
+            assert np.all((qq >= 0) & (qq <= 15))
+
+
+def test_int4_sym_codes_bruteforce_and_sign_symmetry(orc):
+    """Codes against a scan of the 16 offsets q - 8 in -8 .. 7 with exact
+    rational distances to x * fl(1/s) (ties to the even offset, the ends
+    saturating), and negating W maps q to 16 - q with the same scales where
+    neither side clamps (rint is odd-symmetric; offsets run -8 .. 7)."""
+    N, K = 16, 256
+    w = bf16_bits(inputs.outlier_channel_bf16(N, K, 93))
+    qw, sc, qz = orc.quant_int4_g128_sym(w)
+    q, _ = unpack_int4(qw, qz, N, K)
+    s = vals(sc).astype(np.float32)
+    wv = vals(w).astype(np.float32)
+
+    def nearest(t: Fraction):
+        cands = range(-8, 8)
+        best = min(abs(c - t) for c in cands)
+        tied = [c for c in cands if abs(c - t) == best]
+        return tied[0] if len(tied) == 1 else [c for c in tied if c % 2 == 0][0]
+
+    for n in range(N):
+        for g in range(K // 128):
+            r = np.float32(1) / s[g, n]
+            for k in range(0, 128, 5):
+                t = Fraction(float(wv[n, 128 * g + k] * r))
+                assert q[128 * g + k, n] == nearest(t) + 8, (n, g, k)
+    neg = w ^ np.uint16(0x8000)
+    qw2, sc2, qz2 = orc.quant_int4_g128_sym(neg)
+    q2, _ = unpack_int4(qw2, qz2, N, K)
+    assert np.array_equal(sc2, sc)
+    mid = (q >= 1) & (q <= 14)                 # rint(x r) in -7 .. 6: neither side clamps
+    assert np.array_equal(q2[mid], 16 - q[mid])
+    assert np.all(q2[q == 0] == 15)            # -8 turns into +8, which clamps to 7
+    assert np.all((q2[q == 15] == 1) | (q2[q == 15] == 0))   # +7, or +8 clamped, turns into -7 or -8
+
+
+def test_int4_sym_codes_at_half_steps(orc):
+    """Reading R15's fp32 steps: q = clamp(rint(x * fl(1/s)) + 8).  On groups
+    of exact half steps of s = 7 * 2^-9 (tests/hard_cases.py) x * fl(1/s)
+    lies next to k + 1/2; the oracle's codes are the exact nearest integers of
+    that product (ties to even) plus 8, and dividing, x / s, would give other
+    codes on some of them."""
+    from hard_cases import int4_sym_half_step_weight
+    w = int4_sym_half_step_weight()
+    N, K = w.shape
+    qw, sc, qz = orc.quant_int4_g128_sym(w)
+    q, z = unpack_int4(qw, qz, N, K)
+    assert np.all(z == 8)
+    s = vals(sc).astype(np.float32)
+    wv = vals(w).astype(np.float32)
+    differ = 0
+    for n in range(N):
+        for g in range(K // 128):
+            assert s[g, n] == np.float32(7.0 / 512)
+            r = np.float32(1) / s[g, n]
+            for k in range(128):
+                x = wv[n, 128 * g + k]
+                want = min(15, max(0, round(Fraction(float(x * r))) + 8))
+                assert q[128 * g + k, n] == want, (n, g, k)
+                differ += want != min(15, max(0, round(Fraction(float(x)) / Fraction(float(s[g, n]))) + 8))
+    assert differ > 0
+
+
+def test_int4_sym_dequant_within_half_step(orc):
+    """(q - 8) s is within s/2 of x wherever x / s + 8 is inside [-0.5, 15.5];
+    only the top end (x near +a, offset 7.5) can saturate, by one step."""
+    N, K = 32, 512
+    w = bf16_bits(inputs.normal_bf16((N, K), 0.02, 95))
+    qw, sc, qz = orc.quant_int4_g128_sym(w)
+    wh = orc.dequant_int4_g128(qw, sc, qz)
+    wv = vals(w)
+    s = np.repeat(vals(sc).T, 128, 1)
+    err = np.abs(wh - wv)
+    inside = (wv / s + 8 >= -0.5) & (wv / s + 8 <= 15.5)
+    assert np.all(err[inside] <= s[inside] / 2 * (1 + 1e-3))
+    assert np.all(err[~inside] <= s[~inside] * (1 + 1e-3))
+
+
 # ------------------------------------------------------------------ INT8 per row
 def test_int8_worked_rows_ties_and_saturation(orc):
     """Rows chosen so that 127/amax is a power of two: x * r is exact and the
@@ -871,6 +975,7 @@ MONOTONE_CASES = {
     "nvfp4": ("quant_nvfp4", "dequant_nvfp4", 16),
     "int8_row": ("quant_int8_row", "dequant_int8_row", 64),
     "int4_g128": ("quant_int4_g128", "dequant_int4_g128", 128),
+    "int4_g128_sym": ("quant_int4_g128_sym", "dequant_int4_g128", 128),
 }
 
 
