@@ -19,7 +19,8 @@ so each input is evicted between its uses.
 
 --next measures the next rows instead: MXFP4 W4A4 on the mxfp8 shapes, FP8
 1x128-group activations and INT8 W8A8 on the fp8_block MLP shapes at M=4096,
-and the fp8_tensor linear with its activation quantization inside the GEMM.
+the fp8_tensor linear with its activation quantization inside the GEMM, and
+symmetric int4 weights on the w4a16 decode shapes at M=1 and 16.
 
 --impl reference times the CPU oracle (the slow reference implementation) on
 a bounded sample of the same workload.
@@ -91,7 +92,8 @@ def workload_linears(next_rows: bool = False):
         return ([("mxfp4", I.mxfp4_linear(K, N)) for (K, N) in I.MXFP8_SHAPES]
                 + [("fp8_group", I.fp8_group_linear(K, N)) for (K, N) in I.FP8_MLP_SHAPES]
                 + [("int8", I.int8_linear(K, N)) for (K, N) in I.FP8_MLP_SHAPES]
-                + [("fp8_tensor_fused", I.fp8_tensor_fused_linear())])
+                + [("fp8_tensor_fused", I.fp8_tensor_fused_linear())]
+                + [("w4a16_sym", I.w4a16_sym_linear(M, K, N)) for (K, N) in I.W4A16_SHAPES for M in (1, 16)])
     lins = [("fp8_tensor", I.fp8_tensor_linear())]
     for (K, N) in I.W4A16_SHAPES:
         for M in I.W4A16_M:
@@ -112,7 +114,9 @@ def config_block(args):
                 "workloads": ["mxfp4 W4A4 M20280 (K,N){(5120,13824),(13824,5120),(5120,5120)}",
                               "fp8 1x128-group X x 128x128-block W, M4096 (K,N){(3072,12288),(12288,3072)}",
                               "int8 W8A8 per-token X x per-channel W, M4096 (K,N){(3072,12288),(12288,3072)}",
-                              "fp8 per-tensor with X quantized inside the GEMM, M128 K1024 N1024"],
+                              "fp8 per-tensor with X quantized inside the GEMM, M128 K1024 N1024",
+                              "w4a16 symmetric int4 (zero point 8) M{1,16} (K,N){(4096,4096),(4096,12288),"
+                              "(12288,4096)}"],
                 "step": "per linear: weight quantize + activation quantize + quantized GEMM",
                 "l2": "inputs larger than L2", "parallelism": f"replicas x{args.gpus}"}
     return {
@@ -187,7 +191,8 @@ class Job:
         self.x = lin.make_x(device=dev)
         self.w = lin.make_w(device=dev)
         wf = {"fp8_tensor": F.FP8_TENSOR, "fp8_block128": F.FP8_BLOCK128, "mxfp8": F.MXFP8, "nvfp4": F.NVFP4,
-              "int4_g128": F.INT4_G128_ASYM, "mxfp4": F.MXFP4, "int8_row": F.INT8_ROW}[lin.w_fmt]
+              "int4_g128": F.INT4_G128_ASYM, "mxfp4": F.MXFP4, "int8_row": F.INT8_ROW,
+              "int4_g128_sym": F.INT4_G128_SYM}[lin.w_fmt]
         xf = {"fp8_tensor": F.FP8_TENSOR, "fp8_token": F.FP8_TOKEN, "mxfp8": F.MXFP8, "nvfp4": F.NVFP4,
               "bf16": F.BF16, "mxfp4": F.MXFP4, "fp8_group128": F.FP8_GROUP128, "int8_row": F.INT8_ROW}[lin.x_fmt]
         self.wf, self.xf = wf, xf
@@ -290,11 +295,12 @@ def kernel_name(job, op):
             return "gemm_fp8_tensor_fused_x"
         return {F.FP8_TENSOR: "gemm_fp8_tensor", F.FP8_BLOCK128: "gemm_fp8_block", F.MXFP8: "gemm_mxfp8",
                 F.NVFP4: "gemm_nvfp4", F.INT4_G128_ASYM: "gemm_w4a16", F.MXFP4: "gemm_mxfp4",
-                F.INT8_ROW: "gemm_int8"}[job.wf]
+                F.INT8_ROW: "gemm_int8", F.INT4_G128_SYM: "gemm_w4a16_sym"}[job.wf]
     fmt = job.wf if op == "quant_w" else job.xf
     return "quant_" + {F.FP8_TENSOR: "fp8_tensor", F.FP8_TOKEN: "fp8_token", F.FP8_BLOCK128: "fp8_block128",
                        F.MXFP8: "mxfp8", F.NVFP4: "nvfp4", F.INT4_G128_ASYM: "int4_g128", F.MXFP4: "mxfp4",
-                       F.FP8_GROUP128: "fp8_group128", F.INT8_ROW: "int8_row"}[fmt]
+                       F.FP8_GROUP128: "fp8_group128", F.INT8_ROW: "int8_row",
+                       F.INT4_G128_SYM: "int4_g128_sym"}[fmt]
 
 
 def tensor_peak(peaks, wf, q, sustained=False):
@@ -304,7 +310,7 @@ def tensor_peak(peaks, wf, q, sustained=False):
     bf16 = peaks.get("bf16_tflops_sustained" if sustained else "bf16_tflops") or (1700.0 if sustained else 1900.0)
     # W4A16 and INT8 (no integer MMA on sm_103a) run kind::f16, at the bf16 rate
     ratio = FP4_RATIO if wf in (q.Fmt.NVFP4, q.Fmt.MXFP4) else (
-        1.0 if wf in (q.Fmt.INT4_G128_ASYM, q.Fmt.INT8_ROW) else FP8_RATIO)
+        1.0 if wf in (q.Fmt.INT4_G128_ASYM, q.Fmt.INT4_G128_SYM, q.Fmt.INT8_ROW) else FP8_RATIO)
     return bf16 * ratio
 
 
@@ -496,16 +502,15 @@ def cold_rows(jobs, dev, hbm_peak, iters=20, warm=3):
         ops.append((j, "quant_w"))
         if j.xb is not None:
             ops.append((j, "quant_x"))
-        if j.wf == F.INT4_G128_ASYM:
+        if j.wf in (F.INT4_G128_ASYM, F.INT4_G128_SYM):
             ops.append((j, "gemm"))
     stream = torch.cuda.current_stream()
-    sink = torch.empty(1, dtype=torch.int64, device=dev)
     meas = []
     for j, op in ops:
         fn = getattr(j, op)
         evs = []
         for it in range(warm + iters):
-            torch.sum(flush, out=sink)
+            flush.sum()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
             fn()

@@ -50,7 +50,8 @@
  *     code = E2M1(x * ((2688/A)/dec(sb))), 0 when dec(sb) == 0.
  *   INT4: per (n, group of 128 k): range [min(0,min), max(0,max)],
  *     s = bf16((max-min)/15) (1 if 0), r = 1/s in fp32, z = clamp(rint(-min*r)),
- *     q = clamp(rint(x*r) + z), clamps to [0, 15].
+ *     q = clamp(rint(x*r) + z), clamps to [0, 15].  INT4_SYM: the same with
+ *     max = a, min = -a (a = max |x|) and z = 8.
  *   INT8 (per row): s = amax/127, code = clamp(rint(x * (127/amax)), -127,
  *     127), s = 1 and multiplier 1 when amax == 0.
  *   Conversions round to nearest even and saturate (satfinite); a zero keeps
@@ -93,7 +94,14 @@ typedef enum {
      * section "在线量化的底层工作原理" (weights and their scales from a scaled
      * int8 quantizer), with the dynamic activation scheme of section
      * "核心参数详解"; pairs with itself in qlin_gemm.                           */
-    QLIN_INT8_ROW = 9
+    QLIN_INT8_ROW = 9,
+    /* int4 symmetric, group 128 along K: the "sym": true variant of the
+     * AutoRound page's checkpoint config ("vLLM-Omni는 AutoRound 양자화로
+     * 추론을 가속화합니다", section "새로운 모델 양자화").  Range [-a, a] with
+     * a = max |x| over the group, scale bf16(2a/15), zero point fixed at 8;
+     * stored exactly like QLIN_INT4_G128_ASYM (qzeros all 8), so qlin_gemm
+     * takes it with bf16 activations through the same W4A16 kernels.         */
+    QLIN_INT4_G128_SYM = 10
 } qlin_format;
 
 typedef enum {
@@ -129,7 +137,7 @@ const char *qlin_status_string(qlin_status s);
  * NVFP4 formats).                                                           */
 
 /* Codes: FP8 formats and INT8_ROW rows*K; NVFP4 and MXFP4 rows*K/2 (lower k in the low nibble);
- * INT4 (K/8)*rows*4 as int32 [K/8, rows], k = 8i+j in bits [4j,4j+4).       */
+ * INT4 (both variants) (K/8)*rows*4 as int32 [K/8, rows], k = 8i+j in bits [4j,4j+4). */
 size_t qlin_codes_bytes(qlin_format fmt, int64_t rows, int64_t K);
 
 /* Scales: FP8_TENSOR 4 (one float); FP8_TOKEN and INT8_ROW rows*4; FP8_GROUP128
@@ -171,7 +179,7 @@ size_t qlin_gemm_workspace_bytes(qlin_format w_fmt, qlin_format x_fmt,
  *   MXFP8: K % 32 == 0
  *   (K % 128 == 0 for the MMA layout), the same for MXFP4; NVFP4: K % 16 == 0
  *   (K % 64 for MMA);
- *   INT4: rows % 8 == 0 and K % 128 == 0.
+ *   INT4 (both variants): rows % 8 == 0 and K % 128 == 0.
  * Errors: QLIN_ERR_INVALID_ARG, QLIN_ERR_ALIGNMENT, QLIN_ERR_UNSUPPORTED
  *   (QLIN_BF16, or INT4 through qlin_quantize_act), QLIN_ERR_WORKSPACE,
  *   QLIN_ERR_CUDA.                                                          */
@@ -223,7 +231,8 @@ qlin_status qlin_quantize_act(qlin_format fmt, const void *x_bf16_dev, int64_t M
  *                            chip and multiplies them with fp32 accumulation:
  *                            every product is exact, and so is every partial sum
  *                            below 2^24 in magnitude.
- *   INT4_G128_ASYM, BF16   : x = bf16 activations [M,K] row-major; w_codes
+ *   INT4_G128_ASYM, BF16   : (and INT4_G128_SYM, BF16)
+ *                            x = bf16 activations [M,K] row-major; w_codes
  *                            qweight, w_scales bf16, w_zeros qzeros (K % 128 == 0,
  *                            N % 8 == 0, N <= 65535*128, M <= 65535*64);
  *                            workspace per qlin_gemm_workspace_bytes

@@ -13,7 +13,10 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 bool is_quant_format(qlin_format f) {
     return (f >= QLIN_FP8_TENSOR && f <= QLIN_INT4_G128_ASYM) || f == QLIN_MXFP4 || f == QLIN_FP8_GROUP128 ||
-           f == QLIN_INT8_ROW;
+           f == QLIN_INT8_ROW || f == QLIN_INT4_G128_SYM;
+}
+
+bool is_int4(qlin_format f) { return f == QLIN_INT4_G128_ASYM || f == QLIN_INT4_G128_SYM;
 }
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -42,7 +45,8 @@ qlin_status check_quant_shape(qlin_format fmt, qlin_scale_layout layout, int64_t
         case QLIN_NVFP4:
             if (K % 16) return QLIN_ERR_INVALID_ARG;
             return (layout == QLIN_SCALE_MMA && K % 64) ? QLIN_ERR_INVALID_ARG : QLIN_OK;
-        case QLIN_INT4_G128_ASYM: return (rows % 8 || K % 128) ? QLIN_ERR_INVALID_ARG : QLIN_OK;
+        case QLIN_INT4_G128_ASYM:
+        case QLIN_INT4_G128_SYM: return (rows % 8 || K % 128) ? QLIN_ERR_INVALID_ARG : QLIN_OK;
         default: return QLIN_ERR_UNSUPPORTED;
     }
 }
@@ -54,14 +58,14 @@ qlin_status quantize(qlin_format fmt, const void* src, int64_t rows, int64_t K, 
     qlin_status s = check_quant_shape(fmt, layout, rows, K);
     if (s != QLIN_OK) return s;
     if (!src || !codes || !scales || ld < K) return QLIN_ERR_INVALID_ARG;
-    if (fmt == QLIN_INT4_G128_ASYM && !zeros) return QLIN_ERR_INVALID_ARG;
+    if (is_int4(fmt) && !zeros) return QLIN_ERR_INVALID_ARG;
     if (fmt == QLIN_NVFP4 && !global) return QLIN_ERR_INVALID_ARG;
     if (!aligned16(src) || (ld * 2) % 16 || !aligned16(codes)) return QLIN_ERR_ALIGNMENT;
     if (fmt == QLIN_FP8_TOKEN || fmt == QLIN_FP8_BLOCK128 || fmt == QLIN_FP8_TENSOR || fmt == QLIN_FP8_GROUP128 ||
         fmt == QLIN_INT8_ROW) {
         if (reinterpret_cast<uintptr_t>(scales) & 3u) return QLIN_ERR_ALIGNMENT;
     }
-    if (fmt == QLIN_INT4_G128_ASYM &&
+    if (is_int4(fmt) &&
         ((reinterpret_cast<uintptr_t>(scales) & 1u) || (reinterpret_cast<uintptr_t>(zeros) & 3u)))
         return QLIN_ERR_ALIGNMENT;
     const size_t need = qlin_quant_workspace_bytes(fmt, rows, K);
@@ -90,9 +94,10 @@ qlin_status quantize(qlin_format fmt, const void* src, int64_t rows, int64_t K, 
             return launch_status(launch_nvfp4(x, rows, K, ld, c, static_cast<uint8_t*>(scales), global, mma,
                                               static_cast<float*>(ws), amax_partials(rows, K), st));
         case QLIN_INT4_G128_ASYM:
+        case QLIN_INT4_G128_SYM:
             return launch_status(launch_int4_g128(x, rows, K, ld, reinterpret_cast<int32_t*>(codes),
                                                   static_cast<uint16_t*>(scales), static_cast<int32_t*>(zeros),
-                                                  st));
+                                                  fmt == QLIN_INT4_G128_SYM, st));
         default: return QLIN_ERR_UNSUPPORTED;
     }
 }
@@ -127,7 +132,8 @@ size_t qlin_codes_bytes(qlin_format fmt, int64_t rows, int64_t K) {
         case QLIN_MXFP8: return (size_t)(rows * K);
         case QLIN_NVFP4:
         case QLIN_MXFP4: return (size_t)(rows * (K / 2));
-        case QLIN_INT4_G128_ASYM: return (size_t)((K / 8) * rows * 4);
+        case QLIN_INT4_G128_ASYM:
+        case QLIN_INT4_G128_SYM: return (size_t)((K / 8) * rows * 4);
         default: return 0;
     }
 }
@@ -144,13 +150,14 @@ size_t qlin_scales_bytes(qlin_format fmt, qlin_scale_layout layout, int64_t rows
         case QLIN_MXFP8:
         case QLIN_MXFP4: return (size_t)((layout == QLIN_SCALE_MMA ? rows_pad : rows) * (K / 32));
         case QLIN_NVFP4: return (size_t)((layout == QLIN_SCALE_MMA ? rows_pad : rows) * (K / 16));
-        case QLIN_INT4_G128_ASYM: return (size_t)((K / 128) * rows * 2);
+        case QLIN_INT4_G128_ASYM:
+        case QLIN_INT4_G128_SYM: return (size_t)((K / 128) * rows * 2);
         default: return 0;
     }
 }
 
 size_t qlin_zeros_bytes(qlin_format fmt, int64_t rows, int64_t K) {
-    if (fmt != QLIN_INT4_G128_ASYM || rows < 1 || K < 1) return 0;
+    if (!is_int4(fmt) || rows < 1 || K < 1) return 0;
     return (size_t)((K / 128) * (rows / 8) * 4);
 }
 
@@ -162,7 +169,7 @@ size_t qlin_quant_workspace_bytes(qlin_format fmt, int64_t rows, int64_t K) {
 
 size_t qlin_gemm_workspace_bytes(qlin_format w_fmt, qlin_format x_fmt, int64_t M, int64_t N, int64_t K) {
     if (M < 1 || N < 1 || K < 1) return 0;
-    if (w_fmt == QLIN_INT4_G128_ASYM && x_fmt == QLIN_BF16) return w4a16_workspace_bytes(M, N, K);
+    if (is_int4(w_fmt) && x_fmt == QLIN_BF16) return w4a16_workspace_bytes(M, N, K);
     return 0;
 }
 
@@ -180,7 +187,7 @@ qlin_status qlin_quantize_act(qlin_format fmt, const void* x_bf16_dev, int64_t M
                               void* workspace_dev, size_t workspace_bytes, int* dev_status_dev,
                               qlin_stream_t stream) {
     (void)dev_status_dev;
-    if (fmt == QLIN_INT4_G128_ASYM) return QLIN_ERR_UNSUPPORTED;   // int4 is weight-only (W4A16)
+    if (is_int4(fmt)) return QLIN_ERR_UNSUPPORTED;   // int4 is weight-only (W4A16)
     return quantize(fmt, x_bf16_dev, M, K, ldx, codes_dev, scales_dev, nullptr, global_dev, layout,
                     workspace_dev, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
@@ -246,7 +253,7 @@ qlin_status qlin_gemm(qlin_format w_fmt, qlin_format x_fmt, int64_t M, int64_t N
         if (K % 16) return QLIN_ERR_INVALID_ARG;
         return launch_status(launch_gemm_int8(a, st));
     }
-    if (w_fmt == QLIN_INT4_G128_ASYM && x_fmt == QLIN_BF16) {
+    if (is_int4(w_fmt) && x_fmt == QLIN_BF16) {      // the stored zero points serve both int4 variants
         if (!w_scales_dev || !w_zeros_dev) return QLIN_ERR_INVALID_ARG;
         if (K % 128 || N % 8) return QLIN_ERR_INVALID_ARG;
         // 128-channel tiles and 64-token tiles run on grid dimensions y and z (at most 65535 each)

@@ -30,7 +30,8 @@ cudaError_t launch_nvfp4(const uint16_t* x, int64_t rows, int64_t K, int64_t ld,
                          uint8_t* scales, float* global, bool mma_layout, float* partials,
                          int nparts, cudaStream_t st);
 cudaError_t launch_int4_g128(const uint16_t* w, int64_t N, int64_t K, int64_t ld,
-                             int32_t* qweight, uint16_t* scales, int32_t* qzeros, cudaStream_t st);
+                             int32_t* qweight, uint16_t* scales, int32_t* qzeros, bool sym,
+                             cudaStream_t st);
 
 // Number of partial-amax slots the per-tensor reductions use for a tensor.
 int amax_partials(int64_t rows, int64_t K);

@@ -11,7 +11,8 @@
 // "在线量化的底层工作原理" stage 2 (E4M3 + float8_e8m0fnu per 32 along K);
 // "vLLM-Omni 量化推理实践" Table 1 (NVFP4 in the mixed FP8/NVFP4 model);
 // "vLLM-Omni는 AutoRound 양자화로 추론을 가속화합니다" section "새로운 모델
-// 양자화" (int4, group_size 128, auto_round:auto_gptq packing, --iters 0);
+// 양자화" (int4, group_size 128, auto_round:auto_gptq packing, --iters 0;
+// the checkpoint config's "sym": true for the symmetric variant);
 // "vLLM-Omni 在线量化（Online Quantization）完全指南" sections "在线量化的底层
 // 工作原理" and "核心参数详解" (INT8 W8A8: per-channel weight scales, dynamic
 // per-token activation scales).
@@ -483,6 +484,10 @@ __global__ void __launch_bounds__(256) k_nvfp4_encode(const uint16_t* __restrict
 // A warp covers 32 consecutive channels, so each qweight row store (fixed
 // k-octet, consecutive n) and each scale store is coalesced; the zero points
 // of 8 channels are OR-ed into one word across 8 lanes.
+// SYM takes the range symmetric, [-a, a] with a = max |x|, and stores the
+// fixed zero point 8 (the "sym": true int4 variant); otherwise the range is
+// [min(0, min), max(0, max)] and the zero point is derived from it.
+template <bool SYM>
 __global__ void __launch_bounds__(128) k_int4_g128(const uint16_t* __restrict__ w, int64_t N, int64_t K,
                                                    int64_t ld, int32_t* __restrict__ qweight,
                                                    uint16_t* __restrict__ scales, int32_t* __restrict__ qzeros) {
@@ -510,14 +515,18 @@ __global__ void __launch_bounds__(128) k_int4_g128(const uint16_t* __restrict__ 
     }
     const __nv_bfloat162 m0 = __hmin2(__hmin2(mn2[0], mn2[1]), __hmin2(mn2[2], mn2[3]));
     const __nv_bfloat162 m1 = __hmax2(__hmax2(mx2[0], mx2[1]), __hmax2(mx2[2], mx2[3]));
-    const float mn = fminf(__low2float(m0), __high2float(m0));
-    const float mx = fmaxf(__low2float(m1), __high2float(m1));
+    float mn = fminf(__low2float(m0), __high2float(m0));
+    float mx = fmaxf(__low2float(m1), __high2float(m1));
+    if constexpr (SYM) {
+        mx = fmaxf(mx, -mn);          // a = max |x|; the range [-a, a]
+        mn = -mx;
+    }
     const __nv_bfloat16 sb = __float2bfloat16_rn(__fdiv_rn(__fsub_rn(mx, mn), 15.0f));
     float s = __bfloat162float(sb);
     uint16_t sbits = __bfloat16_as_ushort(sb);
     if (s == 0.0f) { s = 1.0f; sbits = 0x3F80u; }
     const float r = __fdiv_rn(1.0f, s);
-    const int z = min(max(__float2int_rn(__fmul_rn(-mn, r)), 0), 15);
+    const int z = SYM ? 8 : min(max(__float2int_rn(__fmul_rn(-mn, r)), 0), 15);
     // rint(x*r) + z without a float->int conversion per element: |x*r| <= 15,
     // and adding 1.5 * 2^23 rounds it to an integer (nearest even) in the low
     // mantissa bits, so bits(x*r + 1.5*2^23) - bits(1.5*2^23) = rint(x*r).
@@ -696,8 +705,10 @@ cudaError_t launch_nvfp4(const uint16_t* x, int64_t rows, int64_t K, int64_t ld,
 }
 
 cudaError_t launch_int4_g128(const uint16_t* w, int64_t N, int64_t K, int64_t ld, int32_t* qweight,
-                             uint16_t* scales, int32_t* qzeros, cudaStream_t st) {
-    k_int4_g128<<<(unsigned)(((N + 127) / 128) * (K / 128)), 128, 0, st>>>(w, N, K, ld, qweight, scales, qzeros);
+                             uint16_t* scales, int32_t* qzeros, bool sym, cudaStream_t st) {
+    const unsigned grid = (unsigned)(((N + 127) / 128) * (K / 128));
+    if (sym) k_int4_g128<true><<<grid, 128, 0, st>>>(w, N, K, ld, qweight, scales, qzeros);
+    else k_int4_g128<false><<<grid, 128, 0, st>>>(w, N, K, ld, qweight, scales, qzeros);
     return cudaGetLastError();
 }
 

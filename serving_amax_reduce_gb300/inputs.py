@@ -110,6 +110,14 @@ def w4a16_linear(M: int, K: int, N: int) -> Linear:
                   _seed(2, 2 * v), _seed(2, 2 * v + 1), "normal", x_std=1.0, w_std=0.02)
 
 
+def w4a16_sym_linear(M: int, K: int, N: int) -> Linear:
+    """The W4A16 decode shapes and distributions with symmetric int4 weights
+    (zero point 8), seeds of workload 9."""
+    v = W4A16_SHAPES.index((K, N)) if (K, N) in W4A16_SHAPES else 4
+    return Linear(f"w4a16_sym_M{M}_K{K}_N{N}", M, K, N, "bf16", "int4_g128_sym",
+                  _seed(9, 2 * v), _seed(9, 2 * v + 1), "normal", x_std=1.0, w_std=0.02)
+
+
 FP8_MLP_SHAPES = [(3072, 12288), (12288, 3072)]                # (K, N)
 FP8_MLP_B = [1, 4, 8]
 

@@ -30,6 +30,7 @@ class Fmt(enum.IntEnum):
     MXFP4 = 7
     FP8_GROUP128 = 8
     INT8_ROW = 9
+    INT4_G128_SYM = 10
 
 
 class Layout(enum.IntEnum):
@@ -224,7 +225,7 @@ def alloc_quant(fmt: Fmt, rows: int, K: int, layout: Layout, device) -> dict:
     sb = qlin_scales_bytes(fmt, layout, rows, K)
     if fmt in (Fmt.FP8_TENSOR, Fmt.FP8_TOKEN, Fmt.FP8_BLOCK128, Fmt.FP8_GROUP128, Fmt.INT8_ROW):
         out["scales"] = _empty(sb, device, torch.float32)
-    elif fmt == Fmt.INT4_G128_ASYM:
+    elif fmt in (Fmt.INT4_G128_ASYM, Fmt.INT4_G128_SYM):
         out["scales"] = _empty(sb, device, torch.int16)
         out["zeros"] = _empty(qlin_zeros_bytes(fmt, rows, K), device, torch.int32)
     else:

@@ -67,6 +67,11 @@ def test_size_queries(q):
     assert q.qlin_scales_bytes(F.INT8_ROW, L.CANONICAL, 4096, 3072) == 4096 * 4
     assert q.qlin_quant_workspace_bytes(F.INT8_ROW, 4096, 3072) == 0
     assert q.qlin_gemm_workspace_bytes(F.INT8_ROW, F.INT8_ROW, 4096, 12288, 3072) == 0
+    # symmetric int4: the asymmetric variant's layouts
+    for fn in (q.qlin_codes_bytes, q.qlin_zeros_bytes, q.qlin_quant_workspace_bytes):
+        assert fn(F.INT4_G128_SYM, 4096, 12288) == fn(F.INT4_G128_ASYM, 4096, 12288)
+    assert q.qlin_scales_bytes(F.INT4_G128_SYM, L.CANONICAL, 4096, 12288) == 96 * 4096 * 2
+    assert q.qlin_gemm_workspace_bytes(F.INT4_G128_SYM, F.BF16, 16, 4096, 4096) == 0
 
 
 FAKE = 1 << 20          # a 16-byte aligned non-null value; never dereferenced by these calls
@@ -127,6 +132,14 @@ def test_quantize_rejects_bad_arguments(q):
                                   None, 0, None, None) == S.INVALID_ARG
     assert q.qlin_quantize_weight(F.BF16, FAKE, 128, 1024, 1024, FAKE, FAKE, None, None, L.CANONICAL, None, 0,
                                   None, None) == S.UNSUPPORTED
+    assert q.qlin_quantize_act(F.INT4_G128_SYM, FAKE, 128, 1024, 1024, FAKE, FAKE, None, L.CANONICAL, None, 0,
+                               None, None) == S.UNSUPPORTED
+    assert q.qlin_quantize_weight(F.INT4_G128_SYM, FAKE, 128, 1024, 1024, FAKE, FAKE, None, None, L.CANONICAL,
+                                  None, 0, None, None) == S.INVALID_ARG                 # zeros missing
+    assert q.qlin_quantize_weight(F.INT4_G128_SYM, FAKE, 100, 1024, 1024, FAKE, FAKE, FAKE, None, L.CANONICAL,
+                                  None, 0, None, None) == S.INVALID_ARG                 # N % 8
+    assert q.qlin_quantize_weight(F.INT4_G128_SYM, FAKE, 128, 1024, 1024, FAKE, FAKE, FAKE, None, L.MMA,
+                                  None, 0, None, None) == S.UNSUPPORTED
 
 
 def test_gemm_rejects_bad_arguments(q):

@@ -51,6 +51,7 @@ PAIRS = [
     ("INT8_ROW", "INT8_ROW", "CANONICAL", (300, 640, 1040)),
     ("FP8_TENSOR", "BF16", "CANONICAL", (77, 640, 1040)),
     ("INT4_G128_ASYM", "BF16", "CANONICAL", (33, 136, 128)),
+    ("INT4_G128_SYM", "BF16", "CANONICAL", (16, 4096, 4096)),
 ]
 
 

@@ -313,14 +313,15 @@ def test_mxfp4_gemm_full_size(q, orc):
 
 
 # ------------------------------------------------------------------ W4A16 decode
-def w4a16_case(q, orc, M, K, N, with_bias=False):
+def w4a16_case(q, orc, M, K, N, with_bias=False, sym=False):
     lin = inputs.w4a16_linear(M, K, N)
     x, w = lin.make_x(), lin.make_w()
     F = q.Fmt
-    bw = q.quantize_weight(F.INT4_G128_ASYM, w.cuda())
+    wf = F.INT4_G128_SYM if sym else F.INT4_G128_ASYM
+    bw = q.quantize_weight(wf, w.cuda())
     xd = x.cuda()
     bias = inputs.normal_bf16((1, N), 0.05, 77)[0] if with_bias else None
-    y = q.gemm(F.INT4_G128_ASYM, F.BF16, M, N, K, xd, None, bw["codes"], bw["scales"], w_zeros=bw["zeros"],
+    y = q.gemm(wf, F.BF16, M, N, K, xd, None, bw["codes"], bw["scales"], w_zeros=bw["zeros"],
                bias=bias.cuda() if with_bias else None)
     torch.cuda.synchronize()
     wh = orc.dequant_int4_g128(bw["codes"].cpu().numpy().view(np.int32).reshape(K // 8, N),
@@ -351,6 +352,12 @@ def test_w4a16_gemm_bias(q, orc, M, K, N):
 @pytest.mark.parametrize("K,N", [(4096, 4096), (4096, 12288), (12288, 4096)])
 def test_w4a16_gemm_all_decode_shapes(q, orc, M, K, N):
     w4a16_case(q, orc, M, K, N)
+
+
+# the symmetric int4 weights (zero point 8) through the same kernels
+@pytest.mark.parametrize("M,K,N", [(1, 4096, 4096), (16, 4096, 12288), (64, 12288, 4096), (5, 256, 72)])
+def test_w4a16_sym_gemm(q, orc, M, K, N):
+    w4a16_case(q, orc, M, K, N, sym=True, with_bias=(M == 5))
 
 
 # ------------------------------------------------------------------ device timeout path

@@ -58,13 +58,14 @@ QUANT_CASES = [
     ("INT8_ROW", "CANONICAL", 333, 1040),
     ("INT8_ROW", "CANONICAL", 3, 20480),
     ("INT4_G128_ASYM", "CANONICAL", 200, 1024),
+    ("INT4_G128_SYM", "CANONICAL", 200, 1024),
 ]
 
 
 @pytest.mark.parametrize("fmt,layout,rows,K", QUANT_CASES)
 def test_quantizer_writes_only_its_outputs(q, fmt, layout, rows, K):
     f, lay = q.Fmt[fmt], q.Layout[layout]
-    quant = q.quantize_weight if f == q.Fmt.INT4_G128_ASYM else q.quantize_act
+    quant = q.quantize_weight if f in (q.Fmt.INT4_G128_ASYM, q.Fmt.INT4_G128_SYM) else q.quantize_act
     x = inputs.normal_bf16((rows, K), 1.0, 91).to(DEV)
     ref = quant(f, x, lay)
     bufs, raws = dict(ref), {}
@@ -139,7 +140,7 @@ def gemm_operands(q, name, M, N, K):
             kw["x_global"] = bx["global"]
     if wf == q.Fmt.NVFP4:
         kw["w_global"] = bw["global"]
-    if wf == q.Fmt.INT4_G128_ASYM:
+    if wf in (q.Fmt.INT4_G128_ASYM, q.Fmt.INT4_G128_SYM):
         kw["w_zeros"] = bw["zeros"]
     return (wf, xf, M, N, K, xa, xs, bw["codes"], bw["scales"]), kw
 

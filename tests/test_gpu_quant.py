@@ -177,6 +177,30 @@ def test_int4_g128(q, orc, N, K, kind):
     assert np.array_equal(b["zeros"].cpu().numpy().view(np.int32).reshape(K // 128, N // 8), qz)
 
 
+@pytest.mark.parametrize("N,K", [(72, 256), (4096, 4096), (12288, 4096), (64, 12288)])
+@pytest.mark.parametrize("kind", ["normal", "edge"])
+def test_int4_g128_sym(q, orc, N, K, kind):
+    w = make(kind, N, K, 19 * N + K)
+    b = run(q, q.Fmt.INT4_G128_SYM, w, weight=True)
+    qw, sc, qz = orc.quant_int4_g128_sym(bits(w))
+    assert np.array_equal(b["codes"].cpu().numpy().view(np.int32).reshape(K // 8, N), qw)
+    assert np.array_equal(b["scales"].cpu().numpy().view(np.uint16).reshape(K // 128, N), sc)
+    assert np.array_equal(b["zeros"].cpu().numpy().view(np.int32).reshape(K // 128, N // 8), qz)
+
+
+def test_int4_sym_half_step_groups(q, orc):
+    """Symmetric groups whose x * fl(1/s) sits next to rounding ties: the
+    kernel's codes, scales and zero points equal the oracle's."""
+    from hard_cases import int4_sym_half_step_weight
+    w = int4_sym_half_step_weight()
+    N, K = w.shape
+    b = run(q, q.Fmt.INT4_G128_SYM, torch.from_numpy(w.view(np.int16)).view(torch.bfloat16), weight=True)
+    qw, sc, qz = orc.quant_int4_g128_sym(w)
+    assert np.array_equal(b["codes"].cpu().numpy().view(np.int32).reshape(K // 8, N), qw)
+    assert np.array_equal(b["scales"].cpu().numpy().view(np.uint16).reshape(K // 128, N), sc)
+    assert np.array_equal(b["zeros"].cpu().numpy().view(np.int32).reshape(K // 128, N // 8), qz)
+
+
 def test_row_amax_sweep(q, orc):
     """Rows led by their amax with every bf16 value below it: the per-row
     encoders' products x * fl(c / amax) meet values next to rounding ties; the
