@@ -175,6 +175,7 @@ size_t qlin_gemm_workspace_bytes(qlin_format w_fmt, qlin_format x_fmt,
  * Requirements: src and ld*2 bytes 16-byte aligned; K % 8 == 0;
  *   rows < 2^31, K < 2^31 and rows' * ceil(K/256) < 2^31, rows' being rows
  *   rounded up to a multiple of 128 for the MMA layout (about 1 TB of bf16);
+ *   FP8_GROUP128, MXFP8, MXFP4 and NVFP4 also K <= 65535 * 1024;
  *   FP8_BLOCK128: rows % 128 == 0 and K % 128 == 0; FP8_GROUP128: K % 128 == 0;
  *   MXFP8: K % 32 == 0
  *   (K % 128 == 0 for the MMA layout), the same for MXFP4; NVFP4: K % 16 == 0

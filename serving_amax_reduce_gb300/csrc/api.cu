@@ -32,6 +32,10 @@ qlin_status check_quant_shape(qlin_format fmt, qlin_scale_layout layout, int64_t
     if (rows_pad * ceil_div(K, 256) > 0x7FFFFFFFll) return QLIN_ERR_INVALID_ARG;
     if (layout == QLIN_SCALE_MMA && fmt != QLIN_MXFP8 && fmt != QLIN_MXFP4 && fmt != QLIN_NVFP4)
         return QLIN_ERR_UNSUPPORTED;
+    // the row-chunk walks (1 x 128 groups, MX, NVFP4) put a row's 1024-element chunks on grid y
+    if ((fmt == QLIN_FP8_GROUP128 || fmt == QLIN_MXFP8 || fmt == QLIN_MXFP4 || fmt == QLIN_NVFP4) &&
+        ceil_div(K, 1024) > 65535)
+        return QLIN_ERR_INVALID_ARG;
     switch (fmt) {
         case QLIN_FP8_TENSOR:
         case QLIN_FP8_TOKEN:

@@ -44,6 +44,19 @@ __device__ __forceinline__ float absmax8(const uint4& v) {
     return a;
 }
 
+// The same maximum on bf16 pairs: clear the sign bits, three packed maxima
+// (exact: a max of bf16 values is one of them), then the last pair in fp32.
+__device__ __forceinline__ float absmax8_bf16x2(const uint4& v) {
+    const uint32_t u[4] = {v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu, v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu};
+    const __nv_bfloat162 a = __hmax2(*reinterpret_cast<const __nv_bfloat162*>(&u[0]),
+                                     *reinterpret_cast<const __nv_bfloat162*>(&u[1]));
+    const __nv_bfloat162 b = __hmax2(*reinterpret_cast<const __nv_bfloat162*>(&u[2]),
+                                     *reinterpret_cast<const __nv_bfloat162*>(&u[3]));
+    const __nv_bfloat162 m = __hmax2(a, b);
+    const uint32_t w = *reinterpret_cast<const uint32_t*>(&m);
+    return fmaxf(bf16_lo(w), bf16_hi(w));
+}
+
 // Two fp32 -> two E4M3 codes, round to nearest even, saturating; `lo` lands
 // in bits 0..7.
 __device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
@@ -340,36 +353,46 @@ __global__ void __launch_bounds__(256) k_fp8_block128(const uint16_t* __restrict
     if (threadIdx.x == 0) scales[bi * (K >> 7) + bj] = s;
 }
 
+// ---------------------------------------------------------------- row chunks
+// The 1 x 128-group, MX and NVFP4 quantizers walk "row chunks": warp w of a
+// CTA owns one row and kChunk = 32 * kChunkU consecutive 16-byte vectors of
+// it, kChunkU per lane (lane + 32 u), so each vector slot of the warp reads
+// 512 contiguous bytes and the row and column come from the block and warp
+// indices without a division.  Row blocks of 8 rows run along grid x, chunks
+// along grid y.  A granule (32, 16 or 128 elements: 4, 2 or 16 lanes) never
+// straddles a chunk, and every lane of a warp runs the same shuffles.
+constexpr int kChunkU = 4;
+constexpr int kChunk = 32 * kChunkU;           // vectors per warp chunk (1024 elements)
+
 // ---------------------------------------------------------------- 1 x 128 groups
-// Row tasks: a task's 32 vectors are two 128-element groups of one row, 16
-// lanes each; the group amax comes from four xor-shuffles inside the 16 lanes.
-// K % 128 == 0, so a group is entirely inside or outside the row.
-__global__ void __launch_bounds__(256, 6) k_fp8_group128(const uint16_t* __restrict__ x, int64_t rows, int64_t K,
-                                                      int64_t ld, uint8_t* __restrict__ codes,
-                                                      float* __restrict__ scales) {
-    const uint32_t nvr = (uint32_t)(K >> 3), tpr = (nvr + 31) / 32, total = (uint32_t)rows * tpr;
-    const uint32_t warps = gridDim.x * 8, w0 = blockIdx.x * 8 + (threadIdx.x >> 5);
+// Sixteen lanes own one 128-element group; the group amax comes from four
+// xor-shuffles inside the 16 lanes.  K % 128 == 0.
+__global__ void __launch_bounds__(256) k_fp8_group128(const uint16_t* __restrict__ x, int rows, int K, int64_t ld,
+                                                      uint8_t* __restrict__ codes, float* __restrict__ scales) {
     const int lane = threadIdx.x & 31;
-    for (uint32_t t = w0; t < total; t += warps * kUnroll) {
-        uint4 v[kUnroll];
-        TaskPos q[kUnroll];
+    const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (row >= rows) return;
+    const int nvr = K >> 3, c0 = blockIdx.y * kChunk + lane;
+    const uint16_t* src = x + (int64_t)row * ld;
+    uint4 v[kChunkU];
 #pragma unroll
-        for (int u = 0; u < kUnroll; u++) {
-            q[u] = task_pos(t + u * warps, total, tpr, nvr, lane);
-            v[u] = q[u].in ? ld16(x + (int64_t)q[u].row * ld + 8 * q[u].c) : make_uint4(0, 0, 0, 0);
-        }
+    for (int u = 0; u < kChunkU; u++) {
+        const int c = c0 + 32 * u;
+        v[u] = c < nvr ? ld16(src + 8 * c) : make_uint4(0, 0, 0, 0);
+    }
+    uint2* dst = reinterpret_cast<uint2*>(codes + (int64_t)row * K);
+    float* srow = scales + (int64_t)row * (K >> 7);
 #pragma unroll
-        for (int u = 0; u < kUnroll; u++) {
-            float a = absmax8(v[u]);
+    for (int u = 0; u < kChunkU; u++) {
+        const int c = c0 + 32 * u;
+        float a = absmax8_bf16x2(v[u]);
 #pragma unroll
-            for (int o = 1; o < 16; o <<= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
-            float sc, r;
-            fp8_params(a, sc, r);
-            if (!q[u].in) continue;
-            const int64_t row = q[u].row, c = q[u].c;
-            reinterpret_cast<uint2*>(codes + row * K)[c] = enc8_e4m3(v[u], r);
-            if ((c & 15) == 0) scales[row * (K >> 7) + (c >> 4)] = sc;
-        }
+        for (int o = 1; o < 16; o <<= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
+        if (c >= nvr) continue;
+        float sc, r;
+        fp8_params(a, sc, r);
+        dst[c] = enc8_e4m3(v[u], r);
+        if ((c & 15) == 0) srow[c >> 4] = sc;
     }
 }
 
@@ -378,47 +401,45 @@ __global__ void __launch_bounds__(256, 6) k_fp8_group128(const uint16_t* __restr
 // E4M3 (MXFP8), 2 for E2M1 (MXFP4, codes two per byte).  Four consecutive
 // lanes own one 32-element granule (8 elements each).  Rows from `rows` up to
 // `rows_pad` exist only in the MMA scale layout: they get scale code 0 and no
-// codes.  Every lane of a warp runs the same trip count (the shuffles use the
-// full mask); a task never splits a granule.
+// codes.
 template <bool FP4>
-__global__ void __launch_bounds__(256, 6) k_mx(const uint16_t* __restrict__ x, int64_t rows, int64_t rows_pad,
-                                            int64_t K, int64_t ld, uint8_t* __restrict__ codes,
-                                            uint8_t* __restrict__ scales, int mma) {
+__global__ void __launch_bounds__(256) k_mx(const uint16_t* __restrict__ x, int rows, int rows_pad, int K, int64_t ld,
+                                            uint8_t* __restrict__ codes, uint8_t* __restrict__ scales, int mma) {
     constexpr int kEmax = FP4 ? 2 : 8;
-    const uint32_t nvr = (uint32_t)(K >> 3), tpr = (nvr + 31) / 32, total = (uint32_t)rows_pad * tpr;
-    const uint32_t warps = gridDim.x * 8, w0 = blockIdx.x * 8 + (threadIdx.x >> 5);
-    const int64_t chunks = K >> 7;
     const int lane = threadIdx.x & 31;
-    for (uint32_t t = w0; t < total; t += warps * kUnroll) {
-        uint4 v[kUnroll];
-        TaskPos q[kUnroll];
+    const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (row >= rows_pad) return;
+    const bool live = row < rows;
+    const int nvr = K >> 3, c0 = blockIdx.y * kChunk + lane;
+    const uint16_t* src = x + (int64_t)row * ld;
+    uint4 v[kChunkU];
 #pragma unroll
-        for (int u = 0; u < kUnroll; u++) {
-            q[u] = task_pos(t + u * warps, total, tpr, nvr, lane);
-            v[u] = (q[u].in && q[u].row < rows) ? ld16(x + (int64_t)q[u].row * ld + 8 * q[u].c)
-                                                : make_uint4(0, 0, 0, 0);
+    for (int u = 0; u < kChunkU; u++) {
+        const int c = c0 + 32 * u;
+        v[u] = (live && c < nvr) ? ld16(src + 8 * c) : make_uint4(0, 0, 0, 0);
+    }
+    const int64_t chunks = K >> 7;
+    uint8_t* crow = codes + (int64_t)row * (FP4 ? (K >> 1) : K);
+#pragma unroll
+    for (int u = 0; u < kChunkU; u++) {
+        const int c = c0 + 32 * u;
+        float a = absmax8_bf16x2(v[u]);
+        a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
+        a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 2));
+        if (c >= nvr) continue;
+        // e = clamp(floor(log2 a) - kEmax, -127, 127); subnormal a lands below -127.
+        const int biased = (int)(__float_as_uint(a) >> 23);
+        int e = (a == 0.0f || biased == 0) ? -127 : max(biased - 127 - kEmax, -127);
+        e = min(e, 127);
+        const float mult = __uint_as_float((uint32_t)(127 - e) << 23);   // 2^-e, e <= 126 here
+        if (live) {
+            if (FP4) reinterpret_cast<uint32_t*>(crow)[c] = enc8_e2m1(v[u], mult);
+            else reinterpret_cast<uint2*>(crow)[c] = enc8_e4m3(v[u], mult);
         }
-#pragma unroll
-        for (int u = 0; u < kUnroll; u++) {
-            float a = absmax8(v[u]);
-            a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
-            a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 2));
-            // e = clamp(floor(log2 a) - kEmax, -127, 127); subnormal a lands below -127.
-            const int biased = (int)(__float_as_uint(a) >> 23);
-            int e = (a == 0.0f || biased == 0) ? -127 : max(biased - 127 - kEmax, -127);
-            e = min(e, 127);
-            const float mult = __uint_as_float((uint32_t)(127 - e) << 23);   // 2^-e, e <= 126 here
-            if (!q[u].in) continue;
-            const int64_t row = q[u].row, c = q[u].c;
-            if (row < rows) {
-                if (FP4) reinterpret_cast<uint32_t*>(codes + row * (K >> 1))[c] = enc8_e2m1(v[u], mult);
-                else reinterpret_cast<uint2*>(codes + row * K)[c] = enc8_e4m3(v[u], mult);
-            }
-            if ((c & 3) == 0) {
-                const int64_t j = c >> 2;
-                const int64_t off = mma ? mma_scale_offset(row, j, chunks) : row * (K >> 5) + j;
-                scales[off] = (uint8_t)(e + 127);
-            }
+        if ((c & 3) == 0) {
+            const int64_t j = c >> 2;
+            const int64_t off = mma ? mma_scale_offset(row, j, chunks) : (int64_t)row * (K >> 5) + j;
+            scales[off] = (uint8_t)(e + 127);
         }
     }
 }
@@ -427,10 +448,12 @@ __global__ void __launch_bounds__(256, 6) k_mx(const uint16_t* __restrict__ x, i
 // After the amax pass: two consecutive lanes own one 16-element block.  The
 // code multiplier rg / dsb depends only on the block's UE4M3 scale code, so
 // each CTA tabulates it once for all 256 codes (same division, same bits).
-__global__ void __launch_bounds__(256) k_nvfp4_encode(const uint16_t* __restrict__ x, int64_t rows,
-                                                      int64_t rows_pad, int64_t K, int64_t ld,
-                                                      uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
-                                                      float* __restrict__ global,
+// That prologue (and folding the partial maxima) makes the grid persistent:
+// a CTA takes the chunk ids blockIdx.x, blockIdx.x + gridDim.x, ..., chunk
+// id = row block * chunks per row + chunk (one division per id).
+__global__ void __launch_bounds__(256) k_nvfp4_encode(const uint16_t* __restrict__ x, int rows, int rows_pad, int K,
+                                                      int64_t ld, uint8_t* __restrict__ codes,
+                                                      uint8_t* __restrict__ scales, float* __restrict__ global,
                                                       const float* __restrict__ partials, int nparts, int mma) {
     __shared__ float red[33];
     __shared__ float rb_of[256];
@@ -447,30 +470,35 @@ __global__ void __launch_bounds__(256) k_nvfp4_encode(const uint16_t* __restrict
     }
     __syncthreads();
     if (blockIdx.x == 0 && threadIdx.x == 0) *global = g;
-    const uint32_t nvr = (uint32_t)(K >> 3), tpr = (nvr + 31) / 32, total = (uint32_t)rows_pad * tpr;
-    const uint32_t warps = gridDim.x * 8, w0 = blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nvr = K >> 3, nch = (nvr + kChunk - 1) / kChunk;
+    const uint32_t ids = (uint32_t)((rows_pad + 7) / 8) * (uint32_t)nch;
     const int64_t chunks = K >> 6;
-    const int lane = threadIdx.x & 31;
-    for (uint32_t t = w0; t < total; t += warps * kUnroll) {
-        uint4 v[kUnroll];
-        TaskPos q[kUnroll];
+    for (uint32_t id = blockIdx.x; id < ids; id += gridDim.x) {
+        const uint32_t rb = id / (uint32_t)nch;
+        const int row = (int)rb * 8 + warp;
+        if (row >= rows_pad) continue;                   // warp-uniform
+        const bool live = row < rows;
+        const int c0 = (int)(id - rb * (uint32_t)nch) * kChunk + lane;
+        const uint16_t* src = x + (int64_t)row * ld;
+        uint4 v[kChunkU];
 #pragma unroll
-        for (int u = 0; u < kUnroll; u++) {
-            q[u] = task_pos(t + u * warps, total, tpr, nvr, lane);
-            v[u] = (q[u].in && q[u].row < rows) ? ld16(x + (int64_t)q[u].row * ld + 8 * q[u].c)
-                                                : make_uint4(0, 0, 0, 0);
+        for (int u = 0; u < kChunkU; u++) {
+            const int c = c0 + 32 * u;
+            v[u] = (live && c < nvr) ? ld16(src + 8 * c) : make_uint4(0, 0, 0, 0);
         }
+        uint32_t* crow = reinterpret_cast<uint32_t*>(codes + (int64_t)row * (K >> 1));
 #pragma unroll
-        for (int u = 0; u < kUnroll; u++) {
-            float b = absmax8(v[u]);
+        for (int u = 0; u < kChunkU; u++) {
+            const int c = c0 + 32 * u;
+            float b = absmax8_bf16x2(v[u]);
             b = fmaxf(b, __shfl_xor_sync(0xFFFFFFFFu, b, 1));
+            if (c >= nvr) continue;
             const uint32_t sb = cvt_e4m3x2(__fmul_rn(b, qm), 0.0f) & 0xFFu;   // non-negative: UE4M3
-            if (!q[u].in) continue;
-            const int64_t row = q[u].row, c = q[u].c;
-            if (row < rows) reinterpret_cast<uint32_t*>(codes + row * (K >> 1))[c] = enc8_e2m1(v[u], rb_of[sb]);
+            if (live) crow[c] = enc8_e2m1(v[u], rb_of[sb]);
             if ((c & 1) == 0) {
                 const int64_t j = c >> 1;
-                const int64_t off = mma ? mma_scale_offset(row, j, chunks) : row * (K >> 4) + j;
+                const int64_t off = mma ? mma_scale_offset(row, j, chunks) : (int64_t)row * (K >> 4) + j;
                 scales[off] = (uint8_t)sb;
             }
         }
@@ -567,28 +595,17 @@ int sm_count() {
     return n;
 }
 
-// Grids of a task walk (8 warps per CTA, kUnroll tasks per warp per round).
-// k_mx and k_fp8_group128 are capped at 40 registers (6 CTAs per SM, a few
-// bytes of spill), which made them 1.5 % and 10 % faster than at 46-51
-// registers (4-5 CTAs per SM); the same cap made the NVFP4 encode pass 2 %
-// slower, so that one is not capped.
-// Kernels without a per-CTA prologue launch one round per CTA: the block
-// scheduler refills an SM as its CTAs retire, so new loads start while older
-// CTAs encode and store.  The two encode passes that begin by folding the
-// partial maxima (and, for NVFP4, tabulating 256 divisions) stay persistent
-// with 8 CTAs per SM, so that prologue runs once per resident CTA.
-// Tasks of one tensor, or -1 when their count does not fit the 32-bit walk.
+// Grid of the per-tensor task walks (8 warps per CTA, kUnroll tasks per warp
+// per round): the FP8 per-tensor encode pass begins by folding the partial
+// maxima, so it stays persistent with 8 CTAs per SM and that prologue runs
+// once per resident CTA.  Tasks of one tensor, or -1 when their count does
+// not fit the 32-bit walk.
 int64_t task_count(int64_t rows, int64_t K) {
     const int64_t t = rows * (((K >> 3) + 31) / 32);
     return t > 0x7FFFFFFFll ? -1 : t;
 }
 
 int64_t task_rounds(int64_t tasks) { return (tasks + 8 * kUnroll - 1) / (8 * kUnroll); }
-
-int task_grid_once(int64_t tasks) {
-    const int64_t b = task_rounds(tasks);
-    return (int)(b < 1 ? 1 : b);
-}
 
 int task_grid_persistent(int64_t tasks) {
     int64_t b = task_rounds(tasks);
@@ -666,29 +683,31 @@ cudaError_t launch_fp8_block128(const uint16_t* x, int64_t rows, int64_t K, int6
     return cudaGetLastError();
 }
 
+// Grid of a row-chunk walk: row blocks of 8 along x, chunks of a row along y.
+dim3 chunk_grid(int64_t rows, int64_t K) {
+    const int64_t nch = ((K >> 3) + kChunk - 1) / kChunk;
+    return dim3((unsigned)((rows + 7) / 8), (unsigned)nch);
+}
+
 cudaError_t launch_fp8_group128(const uint16_t* x, int64_t rows, int64_t K, int64_t ld, uint8_t* codes,
                                 float* scales, cudaStream_t st) {
-    const int64_t tasks = task_count(rows, K);
-    if (tasks < 0) return cudaErrorInvalidValue;
-    k_fp8_group128<<<task_grid_once(tasks), 256, 0, st>>>(x, rows, K, ld, codes, scales);
+    k_fp8_group128<<<chunk_grid(rows, K), 256, 0, st>>>(x, (int)rows, (int)K, ld, codes, scales);
     return cudaGetLastError();
 }
 
 cudaError_t launch_mxfp8(const uint16_t* x, int64_t rows, int64_t K, int64_t ld, uint8_t* codes,
                          uint8_t* scales, bool mma_layout, cudaStream_t st) {
     const int64_t rows_pad = mma_layout ? (rows + 127) / 128 * 128 : rows;
-    const int64_t tasks = task_count(rows_pad, K);
-    if (tasks < 0) return cudaErrorInvalidValue;
-    k_mx<false><<<task_grid_once(tasks), 256, 0, st>>>(x, rows, rows_pad, K, ld, codes, scales, mma_layout ? 1 : 0);
+    k_mx<false><<<chunk_grid(rows_pad, K), 256, 0, st>>>(x, (int)rows, (int)rows_pad, (int)K, ld, codes, scales,
+                                                         mma_layout ? 1 : 0);
     return cudaGetLastError();
 }
 
 cudaError_t launch_mxfp4(const uint16_t* x, int64_t rows, int64_t K, int64_t ld, uint8_t* codes,
                          uint8_t* scales, bool mma_layout, cudaStream_t st) {
     const int64_t rows_pad = mma_layout ? (rows + 127) / 128 * 128 : rows;
-    const int64_t tasks = task_count(rows_pad, K);
-    if (tasks < 0) return cudaErrorInvalidValue;
-    k_mx<true><<<task_grid_once(tasks), 256, 0, st>>>(x, rows, rows_pad, K, ld, codes, scales, mma_layout ? 1 : 0);
+    k_mx<true><<<chunk_grid(rows_pad, K), 256, 0, st>>>(x, (int)rows, (int)rows_pad, (int)K, ld, codes, scales,
+                                                        mma_layout ? 1 : 0);
     return cudaGetLastError();
 }
 
@@ -696,11 +715,13 @@ cudaError_t launch_nvfp4(const uint16_t* x, int64_t rows, int64_t K, int64_t ld,
                          uint8_t* scales, float* global, bool mma_layout, float* partials, int nparts,
                          cudaStream_t st) {
     const int64_t rows_pad = mma_layout ? (rows + 127) / 128 * 128 : rows;
-    const int64_t tasks = task_count(rows_pad, K);
-    if (tasks < 0) return cudaErrorInvalidValue;
+    const dim3 g = chunk_grid(rows_pad, K);
+    const int64_t ids = (int64_t)g.x * g.y;
+    int64_t grid = (int64_t)sm_count() * 8;
+    if (grid > ids) grid = ids;
     k_amax_partial<<<nparts, 256, 0, st>>>(x, rows, K, ld, partials);
-    k_nvfp4_encode<<<task_grid_persistent(tasks), 256, 0, st>>>(x, rows, rows_pad, K, ld, codes, scales, global, partials,
-                                                     nparts, mma_layout ? 1 : 0);
+    k_nvfp4_encode<<<(unsigned)grid, 256, 0, st>>>(x, (int)rows, (int)rows_pad, (int)K, ld, codes, scales, global,
+                                                  partials, nparts, mma_layout ? 1 : 0);
     return cudaGetLastError();
 }
 

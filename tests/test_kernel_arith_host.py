@@ -114,9 +114,9 @@ def task_pos(t, total, tpr, nvr, lane):
 
 
 def task_walk(rows, K, grid, unroll=4):
-    """The walk of k_amax_partial, k_fp8_tensor_encode, k_mx, k_nvfp4_encode and
-    k_fp8_group128: warp w0 = 8 * block + warp takes tasks t + u * warps for
-    u < unroll, then steps by warps * unroll."""
+    """The walk of k_amax_partial and k_fp8_tensor_encode: warp w0 = 8 * block
+    + warp takes tasks t + u * warps for u < unroll, then steps by warps *
+    unroll."""
     nvr = K // 8
     tpr = cdiv(nvr, 32)
     total = rows * tpr
@@ -153,6 +153,41 @@ def test_task_walks_cover_every_vector_once(rows, K):
     # the one-round grid needs no second round
     g = task_grid_once(rows, K)
     assert g * 8 * 4 >= rows * cdiv(K // 8, 32)
+
+
+CHUNK_U = 4
+CHUNK = 32 * CHUNK_U
+
+
+def chunk_grid(rows, K):
+    """quant.cu, chunk_grid: row blocks of 8 along x, 1024-element chunks along y."""
+    return cdiv(rows, 8), cdiv(K // 8, CHUNK)
+
+
+def chunk_vectors(bx, by, warp, lane, rows, K):
+    """k_fp8_group128 / k_mx: warp `warp` of CTA (bx, by) owns row 8 bx + warp and
+    the vectors by * CHUNK + lane + 32 u, u < CHUNK_U, that lie in the row."""
+    row = bx * 8 + warp
+    if row >= rows:
+        return []
+    nvr = K // 8
+    return [(row, c) for c in (by * CHUNK + lane + 32 * u for u in range(CHUNK_U)) if c < nvr]
+
+
+@pytest.mark.parametrize("rows,K", [(333, 1040), (128, 1024), (3, 32), (200, 512), (1, 20480), (130, 5120),
+                                    (20352, 128)])
+def test_chunk_walks_cover_every_vector_once(rows, K):
+    gx, gy = chunk_grid(rows, K)
+    seen = Counter(v for bx in range(gx) for by in range(gy) for w in range(8) for ln in range(32)
+                   for v in chunk_vectors(bx, by, w, ln, rows, K))
+    assert len(seen) == rows * (K // 8) and set(seen.values()) == {1}
+    # the persistent NVFP4 encode pass: CTA b takes ids b, b + grid, ...; id -> (id // gy, id % gy)
+    for grid in {1, 7, min(gx * gy, SMS * 8)}:
+        ids = Counter(i for b in range(grid) for i in range(b, gx * gy, grid))
+        assert set(ids.values()) == {1} and len(ids) == gx * gy
+        assert sorted(divmod(i, gy) for i in ids) == [(x, y) for x in range(gx) for y in range(gy)]
+    # a granule never straddles a chunk: 1024 elements hold whole 16-, 32- and 128-element granules
+    assert CHUNK * 8 % 128 == 0
 
 
 def test_block128_and_int4_grids_cover_their_tiles():
