@@ -286,6 +286,10 @@ qlin_status qlin_quantize_fp8_tensor_noalloc(const void *x_bf16_dev, int64_t row
  * path can be exercised without hanging or faulting a GPU.                  */
 qlin_status qlin_debug_expire_wait(int *dev_status_dev, uint32_t max_polls, qlin_stream_t stream);
 
+/* The cudaError_t value of the CUDA call that made this thread's most
+ * recent QLIN_ERR_CUDA return (0 if none has failed), for diagnostics. */
+int qlin_last_cuda_error(void);
+
 /* Library version string, e.g. "qlin 0.1 sm_103a". */
 const char *qlin_version(void);
 

@@ -21,7 +21,13 @@ bool is_int4(qlin_format f) { return f == QLIN_INT4_G128_ASYM || f == QLIN_INT4_
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-qlin_status launch_status(cudaError_t e) { return e == cudaSuccess ? QLIN_OK : QLIN_ERR_CUDA; }
+thread_local int g_last_cuda_error = 0;   // the calling thread's last failed CUDA call (cudaError_t)
+
+qlin_status launch_status(cudaError_t e) {
+    if (e == cudaSuccess) return QLIN_OK;
+    g_last_cuda_error = (int)e;
+    return QLIN_ERR_CUDA;
+}
 
 // Shape rules per format (see qlin.h).
 qlin_status check_quant_shape(qlin_format fmt, qlin_scale_layout layout, int64_t rows, int64_t K) {
@@ -124,6 +130,8 @@ const char* qlin_status_string(qlin_status s) {
 }
 
 const char* qlin_version(void) { return "qlin 0.1 sm_103a"; }
+
+int qlin_last_cuda_error(void) { return g_last_cuda_error; }
 
 size_t qlin_codes_bytes(qlin_format fmt, int64_t rows, int64_t K) {
     if (rows < 1 || K < 1) return 0;

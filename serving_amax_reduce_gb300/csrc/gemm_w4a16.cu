@@ -741,7 +741,9 @@ cudaError_t launch_mp(const GemmArgs& a, cudaStream_t st) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k_w4a16<MP>, tmQ, tmX, p);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, k_w4a16<MP>, tmQ, tmX, p);
+    if (e != cudaSuccess) (void)cudaGetLastError();   // a refused launch leaves no error for the next call
+    return e;
 }
 
 }  // namespace
@@ -790,7 +792,9 @@ cudaError_t launch_w4a16_mma(const GemmArgs& a, cudaStream_t st) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k_w4a16_mma, p);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, k_w4a16_mma, p);
+    if (e != cudaSuccess) (void)cudaGetLastError();   // a refused launch leaves no error for the next call
+    return e;
 }
 
 cudaError_t launch_gemm_w4a16(const GemmArgs& a, cudaStream_t st) {

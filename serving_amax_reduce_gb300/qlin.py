@@ -51,7 +51,8 @@ class Status(enum.IntEnum):
 class QlinError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = Status(status)
-        super().__init__(f"{where}: {self.status.name} ({qlin_status_string(status)})")
+        extra = f", cudaError {qlin_last_cuda_error()}" if self.status == Status.CUDA else ""
+        super().__init__(f"{where}: {self.status.name} ({qlin_status_string(status)}{extra})")
 
 
 _lib = None
@@ -70,6 +71,7 @@ def _load():
     sigs = {
         "qlin_status_string": ([_I], ctypes.c_char_p),
         "qlin_version": ([], ctypes.c_char_p),
+        "qlin_last_cuda_error": ([], _I),
         "qlin_codes_bytes": ([_I, _I64, _I64], _SZ),
         "qlin_scales_bytes": ([_I, _I, _I64, _I64], _SZ),
         "qlin_zeros_bytes": ([_I, _I64, _I64], _SZ),
@@ -101,6 +103,10 @@ def qlin_status_string(s: int) -> str:
 
 def qlin_version() -> str:
     return _load().qlin_version().decode()
+
+
+def qlin_last_cuda_error() -> int:
+    return _load().qlin_last_cuda_error()
 
 
 def qlin_codes_bytes(fmt, rows, K) -> int:

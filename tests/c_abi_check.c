@@ -29,6 +29,7 @@ int main(void) {
     int s;
 
     CHECK(strstr(qlin_version(), "sm_103a") != NULL);
+    CHECK(qlin_last_cuda_error() == 0);
     for (s = QLIN_OK; s <= QLIN_ERR_DEVICE_TIMEOUT; s++) CHECK(strlen(qlin_status_string((qlin_status)s)) > 0);
 
     /* sizes (rows = M or N, K along the row) */

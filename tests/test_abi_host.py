@@ -35,6 +35,7 @@ def test_every_declared_symbol_is_exported(q):
 
 def test_version_and_status_strings(q):
     assert "sm_103a" in q.qlin_version()
+    assert q.qlin_last_cuda_error() == 0
     for s in q.Status:
         assert q.qlin_status_string(s)
 
