@@ -9,7 +9,7 @@ Two layers:
 * ``qlin_oracle.c`` (built here into ``_build/liboracle.so`` with gcc, strict
   IEEE binary32, no contraction): scalar codecs and quantizers, written one
   element at a time from the format definitions.  See its header for the
-  readings R1..R5, R11..R13 and R15 taken where the pages name a format but print no
+  readings R1..R5, R11..R13, R15 and R16 taken where the pages name a format but print no
   formula.
 * this module: numpy marshalling, and the GEMM reference, which is the plain
   definition Y = Xhat @ What^T evaluated in float64 over the dequantized
@@ -81,6 +81,8 @@ def _load():
             "oracle_quant_mxfp4": ([P, I64, I64, I64, P, P], None),
             "oracle_quant_int4_g128": ([P, I64, I64, I64, P, P, P], None),
             "oracle_quant_int4_g128_sym": ([P, I64, I64, I64, P, P, P], None),
+            "oracle_quant_mxfp4_dual": ([P, I64, I64, I64, P, P, P], None),
+            "oracle_dequant_mxfp4_dual": ([P, I64, I64, P, P, P], None),
             "oracle_quant_int8_row": ([P, I64, I64, I64, P, P], None),
             "oracle_dequant_fp8_tensor": ([P, I64, I64, F, P], None),
             "oracle_dequant_fp8_token": ([P, I64, I64, P, P], None),
@@ -241,6 +243,20 @@ def quant_mxfp4(x):
     return packed, sc
 
 
+def quant_mxfp4_dual(x):
+    """MXFP4 dual-scale (reading R16) -> (packed E2M1 uint8 [R,K/2], fine E8M0
+    scale codes uint8 [R,K/32], coarse fp32 scales [R,K/512])."""
+    x = _bf16_bits(x)
+    R, K = x.shape
+    if K % 512:
+        raise ValueError("MXFP4 dual-scale needs K multiple of 512")
+    packed = np.empty((R, K // 2), np.uint8)
+    sc = np.empty((R, K // 32), np.uint8)
+    coarse = np.empty((R, K // 512), np.float32)
+    _load().oracle_quant_mxfp4_dual(_p(x), R, K, K, _p(packed), _p(sc), _p(coarse))
+    return packed, sc, coarse
+
+
 def quant_int4_g128(w):
     """int4 asymmetric g128 RTN of W [N,K] -> (qweight int32 [K/8,N],
     scales bf16 bits uint16 [K/128,N], qzeros int32 [K/128,N/8])."""
@@ -338,6 +354,16 @@ def dequant_mxfp4(packed, scale_codes):
     R, K = packed.shape[0], packed.shape[1] * 2
     out = _f64((R, K))
     _load().oracle_dequant_mxfp4(_p(packed), R, K, _p(scale_codes), _p(out))
+    return out
+
+
+def dequant_mxfp4_dual(packed, scale_codes, coarse):
+    packed = np.ascontiguousarray(packed, np.uint8)
+    scale_codes = np.ascontiguousarray(scale_codes, np.uint8)
+    coarse = np.ascontiguousarray(coarse, np.float32)
+    R, K = packed.shape[0], packed.shape[1] * 2
+    out = _f64((R, K))
+    _load().oracle_dequant_mxfp4_dual(_p(packed), R, K, _p(scale_codes), _p(coarse), _p(out))
     return out
 
 

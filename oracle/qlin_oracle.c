@@ -68,6 +68,16 @@
  *       (1 if that is 0) and r = 1/s as in R4; the zero point is the fixed
  *       mid-code 8, not derived from the range, and q = clamp(rint(x*r) + 8)
  *       in [0, 15].  Stored exactly like R4 (qzeros all 8).
+ *   R16 MXFP4 dual-scale online ("vLLM-Omni 在线量化（Online Quantization）完全指南",
+ *       section "在线量化的底层工作原理": the online mxfp4_dualscale path computes
+ *       a fine (per 32) and a coarse (per 512) scale level at run time and
+ *       fills the absent calibrated mul_scale with ones): per row and 512
+ *       consecutive K elements, A = max |x|, coarse fp32 scale c = A/6 and
+ *       multiplier r = 6/A (both 1 when A == 0); the block is normalized,
+ *       v = x * r (x * 1 for the all-ones mul_scale first, which is exact),
+ *       and the R11 MX rule runs on v per 32: e = clamp(floor(log2 max|v|) - 2,
+ *       -127, 127), codes E2M1(v * 2^-e) two per byte, scale byte e + 127.
+ *       Dequant: dec(code) * 2^e * c.
  */
 #include <math.h>
 #include <stdint.h>
@@ -342,6 +352,59 @@ void oracle_quant_nvfp4(const uint16_t *x, int64_t rows, int64_t K, int64_t ld,
             scale_codes[i * nb + b] = sb;
         }
     *global = g;
+}
+
+/* MXFP4 dual-scale (R16): K multiple of 512.  packed codes: rows x (K/2)
+ * bytes (lower K index in the low nibble); fine scale codes: rows x (K/32);
+ * coarse scales: rows x (K/512) floats. */
+void oracle_quant_mxfp4_dual(const uint16_t *x, int64_t rows, int64_t K, int64_t ld,
+                             uint8_t *packed, uint8_t *scale_codes, float *coarse)
+{
+    int64_t nc = K / 512, nb = K / 32;
+    for (int64_t i = 0; i < rows; i++)
+        for (int64_t cb = 0; cb < nc; cb++) {
+            const uint16_t *blk = x + i * ld + cb * 512;
+            float A = 0.0f, c = 1.0f, r = 1.0f;
+            for (int k = 0; k < 512; k++)
+                A = fmaxf(A, fabsf(oracle_bf16_to_f32(blk[k])));
+            if (A != 0.0f) { c = A / 6.0f; r = 6.0f / A; }
+            coarse[i * nc + cb] = c;
+            for (int f = 0; f < 16; f++) {
+                const uint16_t *g = blk + f * 32;
+                float v[32], a = 0.0f;
+                for (int k = 0; k < 32; k++) {
+                    v[k] = (oracle_bf16_to_f32(g[k]) * 1.0f) * r;     /* mul_scale = 1, then the coarse level */
+                    a = fmaxf(a, fabsf(v[k]));
+                }
+                int e;
+                if (a == 0.0f) {
+                    e = -127;
+                } else {
+                    e = oracle_floor_log2(a) - 2;
+                    if (e < -127) e = -127;
+                    if (e > 127) e = 127;
+                }
+                float mult = ldexpf(1.0f, -e);                 /* 2^-e, exact */
+                for (int k = 0; k < 32; k += 2) {
+                    uint8_t lo = oracle_enc_e2m1(v[k] * mult);
+                    uint8_t hi = oracle_enc_e2m1(v[k + 1] * mult);
+                    packed[i * (K / 2) + (cb * 512 + f * 32 + k) / 2] = (uint8_t)(lo | (hi << 4));
+                }
+                scale_codes[i * nb + cb * 16 + f] = (uint8_t)(e + 127);
+            }
+        }
+}
+
+void oracle_dequant_mxfp4_dual(const uint8_t *packed, int64_t rows, int64_t K,
+                               const uint8_t *scale_codes, const float *coarse, double *out)
+{
+    for (int64_t i = 0; i < rows; i++)
+        for (int64_t k = 0; k < K; k++) {
+            uint8_t byte = packed[i * (K / 2) + k / 2];
+            uint8_t c = (k % 2) ? (byte >> 4) : (byte & 0xF);
+            out[i * K + k] = oracle_dec_e2m1(c) * oracle_dec_e8m0(scale_codes[i * (K / 32) + k / 32])
+                             * (double)coarse[i * (K / 512) + k / 512];
+        }
 }
 
 /* ------------------------------------------------------------------ */

@@ -527,6 +527,120 @@ def test_mxfp4_dequant_close(orc):
     assert np.all(np.abs(xh - xv)[sat] <= 2 * unit[sat])
 
 
+# ------------------------------------------------------------------ MXFP4 dual-scale (R16)
+def _f32_floor_log2(v: float) -> int:
+    m, e = math.frexp(v)           # v = m 2^e, 0.5 <= m < 1
+    return e - 1
+
+
+def test_mxfp4_dual_coarse_and_fine_levels(orc):
+    """Reading R16: per 512 K the coarse scale is the binary32 nearest to A / 6
+    (A the block's amax; 1 for a zero block), and after normalizing by
+    fl(6 / A) every 32-element block's largest magnitude lands in [4, 8) times
+    its fine power of two (the MX floor rule with the E2M1 exponent 2); the
+    element at the block amax encodes to +-6 with fine exponent 0."""
+    R, K = 48, 1536
+    x = bf16_bits(inputs.outlier_channel_bf16(R, K, 97))
+    x[3, 512:1024] = 0                                            # a zero coarse block
+    packed, sc, coarse = orc.quant_mxfp4_dual(x)
+    assert packed.shape == (R, K // 2) and sc.shape == (R, K // 32) and coarse.shape == (R, K // 512)
+    xv = vals(x)
+    codes = unpack_e2m1(packed)
+    for i in range(R):
+        for cb in range(K // 512):
+            blk = xv[i, 512 * cb:512 * cb + 512]
+            A = np.abs(blk).max()
+            c = coarse[i, cb]
+            if A == 0:
+                assert c == 1.0 and not sc[i, 16 * cb:16 * cb + 16].any()
+                assert not (codes[i, 512 * cb:512 * cb + 512] & 7).any()
+                continue
+            assert Fraction(float(c)) == Fraction(float(np.float32(Fraction(float(A)) / 6)))   # nearest binary32
+            r = np.float32(6) / np.float32(A)
+            for f in range(16):
+                v = (blk[32 * f:32 * f + 32].astype(np.float32) * r).astype(np.float32)
+                a = float(np.abs(v).max())
+                e = int(sc[i, 16 * cb + f]) - 127
+                if a == 0:
+                    assert e == -127
+                    continue
+                assert 4.0 <= a * 2.0 ** -e < 8.0 or e == -127
+            k_at = int(np.argmax(np.abs(blk)))
+            assert int(sc[i, 16 * cb + k_at // 32]) == 127                  # fine exponent 0
+            assert codes[i, 512 * cb + k_at] & 7 == 7                       # |code| = 6
+
+
+def test_mxfp4_dual_codes_are_nearest_of_the_normalized_values(orc):
+    """Codes: the E2M1 value nearest (ties to even) to the exact rational
+    fl(x * fl(6 / A)) * 2^-e, saturating at 6, found by a scan of all codes."""
+    R, K = 6, 512
+    x = rand_bits((R, K), 99)
+    packed, sc, coarse = orc.quant_mxfp4_dual(x)
+    codes = unpack_e2m1(packed)
+    table = [(c, Fraction(orc.dec_e2m1(c))) for c in range(16)]
+    xv = vals(x).astype(np.float32)
+    for i in range(R):
+        r = np.float32(6) / np.float32(np.abs(xv[i]).max())
+        for k in range(0, K, 3):
+            e = int(sc[i, k // 32]) - 127
+            t = Fraction(float(np.float32(xv[i, k] * r))) * Fraction(2) ** -e
+            t = max(min(t, Fraction(6)), Fraction(-6))
+            best = min(abs(v - t) for _, v in table)
+            cands = [c for c, v in table if abs(v - t) == best]
+            if len(cands) > 1:
+                cands = [c for c in cands if (c & 1) == 0] or cands          # ties to the even mantissa
+                if t == 0:
+                    cands = [codes[i, k]] if codes[i, k] in (0, 8) else cands
+            assert codes[i, k] in cands, (i, k, codes[i, k], cands)
+
+
+def test_mxfp4_dual_reduces_to_mxfp4_when_the_coarse_scale_is_a_power_of_two(orc):
+    """With every 512-block's amax equal to 6 * 2^j the coarse multiplier
+    6 / A = 2^-j is exact, so the dual-scale codes are the single-level MXFP4
+    codes (reading R11) and every fine exponent is the MXFP4 one minus j."""
+    R, K = 16, 1024
+    x = rand_bits((R, K), 101)
+    xv = vals(x)
+    j = np.array([[(i + cb) % 5 - 2 for cb in range(K // 512)] for i in range(R)])
+    for i in range(R):
+        for cb in range(K // 512):
+            blk = xv[i, 512 * cb:512 * cb + 512]
+            blk = np.clip(blk, -5.9 * 2.0 ** j[i, cb], 5.9 * 2.0 ** j[i, cb])
+            blk[7] = 6.0 * 2.0 ** j[i, cb]
+            xv[i, 512 * cb:512 * cb + 512] = blk
+    x = bf16_bits(torch.from_numpy(xv).to(torch.bfloat16))
+    assert np.array_equal(np.abs(vals(x)).reshape(R, -1, 512).max(-1), 6.0 * 2.0 ** j)
+    packed, sc, coarse = orc.quant_mxfp4_dual(x)
+    p1, s1 = orc.quant_mxfp4(x)
+    assert np.array_equal(packed, p1)
+    assert np.array_equal(coarse, (2.0 ** j).astype(np.float32))
+    jj = np.repeat(j, 16, axis=1)
+    live = s1 > 0
+    assert np.array_equal(sc[live].astype(int), s1[live].astype(int) - jj[live])
+
+
+def test_mxfp4_dual_blocks_are_independent_and_dequant_close(orc):
+    R, K = 8, 1536
+    x = rand_bits((R, K), 103)
+    p1, s1, c1 = orc.quant_mxfp4_dual(x)
+    x2 = x.copy()
+    x2[5, 512:1024] = bf16_bits(inputs.normal_bf16((1, 512), 300.0, 104))[0]
+    p2, s2, c2 = orc.quant_mxfp4_dual(x2)
+    changed = np.zeros((R, K // 512), bool)
+    changed[5, 1] = True
+    assert np.array_equal(c1[~changed], c2[~changed]) and c1[5, 1] != c2[5, 1]
+    keep = np.ones((R, K), bool)
+    keep[5, 512:1024] = False
+    assert np.array_equal(unpack_e2m1(p1)[keep], unpack_e2m1(p2)[keep])
+    xh = orc.dequant_mxfp4_dual(p2, s2, c2)
+    xv = vals(x2)
+    unit = np.repeat(np.vectorize(orc.dec_e8m0)(s2), 32, 1) * np.repeat(c2.astype(np.float64), 512, 1)
+    bound = half_step(E2M1_POS, xv / unit) * unit * (1 + 1e-6)
+    sat = np.abs(xv / unit) > 6
+    assert np.all(np.abs(xh - xv)[~sat] <= bound[~sat])
+    assert np.all(np.abs(xh - xv)[sat] <= 2 * unit[sat])
+
+
 # ------------------------------------------------------------------ int4
 def unpack_int4(qweight, qzeros, N, K):
     """GPTQ-style layout: k = 8i + j in bits [4j, 4j+4) of qweight[i, n];
@@ -976,6 +1090,7 @@ MONOTONE_CASES = {
     "int8_row": ("quant_int8_row", "dequant_int8_row", 64),
     "int4_g128": ("quant_int4_g128", "dequant_int4_g128", 128),
     "int4_g128_sym": ("quant_int4_g128_sym", "dequant_int4_g128", 128),
+    "mxfp4_dual": ("quant_mxfp4_dual", "dequant_mxfp4_dual", 32),
 }
 
 
