@@ -93,7 +93,8 @@ def workload_linears(next_rows: bool = False):
                 + [("fp8_group", I.fp8_group_linear(K, N)) for (K, N) in I.FP8_MLP_SHAPES]
                 + [("int8", I.int8_linear(K, N)) for (K, N) in I.FP8_MLP_SHAPES]
                 + [("fp8_tensor_fused", I.fp8_tensor_fused_linear())]
-                + [("w4a16_sym", I.w4a16_sym_linear(M, K, N)) for (K, N) in I.W4A16_SHAPES for M in (1, 16)])
+                + [("w4a16_sym", I.w4a16_sym_linear(M, K, N)) for (K, N) in I.W4A16_SHAPES for M in (1, 16)]
+                + [("mxfp4_dual", I.mxfp4_dual_linear(K, N)) for (K, N) in I.MXFP8_SHAPES])
     lins = [("fp8_tensor", I.fp8_tensor_linear())]
     for (K, N) in I.W4A16_SHAPES:
         for M in I.W4A16_M:
@@ -116,7 +117,8 @@ def config_block(args):
                               "int8 W8A8 per-token X x per-channel W, M4096 (K,N){(3072,12288),(12288,3072)}",
                               "fp8 per-tensor with X quantized inside the GEMM, M128 K1024 N1024",
                               "w4a16 symmetric int4 (zero point 8) M{1,16} (K,N){(4096,4096),(4096,12288),"
-                              "(12288,4096)}"],
+                              "(12288,4096)}",
+                              "mxfp4 dual-scale W4A4 M20280 (K,N){(5120,13824),(13824,5120),(5120,5120)}"],
                 "step": "per linear: weight quantize + activation quantize + quantized GEMM",
                 "l2": "inputs larger than L2", "parallelism": f"replicas x{args.gpus}"}
     return {
@@ -192,11 +194,12 @@ class Job:
         self.w = lin.make_w(device=dev)
         wf = {"fp8_tensor": F.FP8_TENSOR, "fp8_block128": F.FP8_BLOCK128, "mxfp8": F.MXFP8, "nvfp4": F.NVFP4,
               "int4_g128": F.INT4_G128_ASYM, "mxfp4": F.MXFP4, "int8_row": F.INT8_ROW,
-              "int4_g128_sym": F.INT4_G128_SYM}[lin.w_fmt]
+              "int4_g128_sym": F.INT4_G128_SYM, "mxfp4_dual": F.MXFP4_DUAL}[lin.w_fmt]
         xf = {"fp8_tensor": F.FP8_TENSOR, "fp8_token": F.FP8_TOKEN, "mxfp8": F.MXFP8, "nvfp4": F.NVFP4,
-              "bf16": F.BF16, "mxfp4": F.MXFP4, "fp8_group128": F.FP8_GROUP128, "int8_row": F.INT8_ROW}[lin.x_fmt]
+              "bf16": F.BF16, "mxfp4": F.MXFP4, "fp8_group128": F.FP8_GROUP128, "int8_row": F.INT8_ROW,
+              "mxfp4_dual": F.MXFP4_DUAL}[lin.x_fmt]
         self.wf, self.xf = wf, xf
-        self.layout = L.MMA if wf in (F.MXFP8, F.NVFP4, F.MXFP4) else L.CANONICAL
+        self.layout = L.MMA if wf in (F.MXFP8, F.NVFP4, F.MXFP4, F.MXFP4_DUAL) else L.CANONICAL
         self.wb = q.alloc_quant(wf, lin.N, lin.K, self.layout, dev)
         self.xb = q.alloc_quant(xf, lin.M, lin.K, self.layout, dev) if xf != F.BF16 else None
         self.y = torch.empty(lin.M, lin.N, dtype=torch.bfloat16, device=dev)
@@ -230,22 +233,24 @@ class Job:
     def bytes_w_quant(self) -> int:
         lin, q = self.lin, self.q
         return (lin.N * lin.K * 2 + q.qlin_codes_bytes(self.wf, lin.N, lin.K)
-                + q.qlin_scales_bytes(self.wf, self.layout, lin.N, lin.K) + q.qlin_zeros_bytes(self.wf, lin.N, lin.K))
+                + q.qlin_scales_bytes(self.wf, self.layout, lin.N, lin.K) + q.qlin_zeros_bytes(self.wf, lin.N, lin.K)
+                + q.qlin_global_bytes(self.wf, lin.N, lin.K))
 
     def bytes_x_quant(self) -> int:
         lin, q = self.lin, self.q
         if self.xb is None:
             return 0
         return (lin.M * lin.K * 2 + q.qlin_codes_bytes(self.xf, lin.M, lin.K)
-                + q.qlin_scales_bytes(self.xf, self.layout, lin.M, lin.K))
+                + q.qlin_scales_bytes(self.xf, self.layout, lin.M, lin.K) + q.qlin_global_bytes(self.xf, lin.M, lin.K))
 
     def gemm_bytes(self) -> int:
         """Algorithmic HBM bytes of the GEMM: operands once + output once."""
         lin, q = self.lin, self.q
         xb = lin.M * lin.K * 2 if self.xb is None else (q.qlin_codes_bytes(self.xf, lin.M, lin.K)
-                                                          + q.qlin_scales_bytes(self.xf, self.layout, lin.M, lin.K))
+                                                          + q.qlin_scales_bytes(self.xf, self.layout, lin.M, lin.K)
+                                                          + q.qlin_global_bytes(self.xf, lin.M, lin.K))
         wb = (q.qlin_codes_bytes(self.wf, lin.N, lin.K) + q.qlin_scales_bytes(self.wf, self.layout, lin.N, lin.K)
-              + q.qlin_zeros_bytes(self.wf, lin.N, lin.K))
+              + q.qlin_zeros_bytes(self.wf, lin.N, lin.K) + q.qlin_global_bytes(self.wf, lin.N, lin.K))
         return xb + wb + lin.M * lin.N * 2
 
 
@@ -255,10 +260,10 @@ class Job:
 # differs from the code the counters came from.
 MEASURED_TRAFFIC = {
     "gemm_fp8_block": {
-        "dram_bytes": 79162624 + 57511936,
+        "dram_bytes": 78314240 + 57053952,
         "alg_bytes": 4096 * 3072 + 4096 * 4 + 12288 * 3072 + 96 * 24 * 4 + 4096 * 12288 * 2,
         "source": "serving_amax_reduce_gb300/csrc/gemm_tc.cu",
-        "code_sha256": "ae38fa4fbcc39dba74fdd5189f997f9cc49753a5628ae7a4e19fd92173096a58",
+        "code_sha256": "94df25cd32d726672027b2e4f9887380803dd05cacb4249e5c5460152f3a44df",
         "captured": "M4096 K3072 N12288 (one bench launch)",
     },
 }
@@ -295,12 +300,12 @@ def kernel_name(job, op):
             return "gemm_fp8_tensor_fused_x"
         return {F.FP8_TENSOR: "gemm_fp8_tensor", F.FP8_BLOCK128: "gemm_fp8_block", F.MXFP8: "gemm_mxfp8",
                 F.NVFP4: "gemm_nvfp4", F.INT4_G128_ASYM: "gemm_w4a16", F.MXFP4: "gemm_mxfp4",
-                F.INT8_ROW: "gemm_int8", F.INT4_G128_SYM: "gemm_w4a16_sym"}[job.wf]
+                F.INT8_ROW: "gemm_int8", F.INT4_G128_SYM: "gemm_w4a16_sym", F.MXFP4_DUAL: "gemm_mxfp4_dual"}[job.wf]
     fmt = job.wf if op == "quant_w" else job.xf
     return "quant_" + {F.FP8_TENSOR: "fp8_tensor", F.FP8_TOKEN: "fp8_token", F.FP8_BLOCK128: "fp8_block128",
                        F.MXFP8: "mxfp8", F.NVFP4: "nvfp4", F.INT4_G128_ASYM: "int4_g128", F.MXFP4: "mxfp4",
                        F.FP8_GROUP128: "fp8_group128", F.INT8_ROW: "int8_row",
-                       F.INT4_G128_SYM: "int4_g128_sym"}[fmt]
+                       F.INT4_G128_SYM: "int4_g128_sym", F.MXFP4_DUAL: "mxfp4_dual"}[fmt]
 
 
 def tensor_peak(peaks, wf, q, sustained=False):
@@ -309,7 +314,7 @@ def tensor_peak(peaks, wf, q, sustained=False):
     loops under the power cap) times the nominal format ratio."""
     bf16 = peaks.get("bf16_tflops_sustained" if sustained else "bf16_tflops") or (1700.0 if sustained else 1900.0)
     # W4A16 and INT8 (no integer MMA on sm_103a) run kind::f16, at the bf16 rate
-    ratio = FP4_RATIO if wf in (q.Fmt.NVFP4, q.Fmt.MXFP4) else (
+    ratio = FP4_RATIO if wf in (q.Fmt.NVFP4, q.Fmt.MXFP4, q.Fmt.MXFP4_DUAL) else (
         1.0 if wf in (q.Fmt.INT4_G128_ASYM, q.Fmt.INT4_G128_SYM, q.Fmt.INT8_ROW) else FP8_RATIO)
     return bf16 * ratio
 

@@ -54,6 +54,9 @@
  *     max = a, min = -a (a = max |x|) and z = 8.
  *   INT8 (per row): s = amax/127, code = clamp(rint(x * (127/amax)), -127,
  *     127), s = 1 and multiplier 1 when amax == 0.
+ *   MXFP4_DUAL: per 512 K, c = A/6 and r = 6/A (1, 1 when A == 0); v = x * r;
+ *     per 32, e = clamp(floor(log2 max|v|) - 2, -127, 127), code =
+ *     E2M1(v * 2^-e); dequant dec(code) * 2^e * c.
  *   Conversions round to nearest even and saturate (satfinite); a zero keeps
  *   its sign.  Every fp32 operation is a single correctly rounded op.
  */
@@ -101,7 +104,16 @@ typedef enum {
      * a = max |x| over the group, scale bf16(2a/15), zero point fixed at 8;
      * stored exactly like QLIN_INT4_G128_ASYM (qzeros all 8), so qlin_gemm
      * takes it with bf16 activations through the same W4A16 kernels.         */
-    QLIN_INT4_G128_SYM = 10
+    QLIN_INT4_G128_SYM = 10,
+    /* MXFP4 with two scale levels: a coarse fp32 scale per 512 consecutive K
+     * (A/6, A the amax of the 512) and, on the values divided by it, the MX
+     * shared exponent per 32 (E8M0 bytes, as QLIN_MXFP4); E2M1 codes two per
+     * byte.  The online mxfp4_dualscale path of "vLLM-Omni 在线量化（Online
+     * Quantization）完全指南", section "在线量化的底层工作原理" (per-32 fine and
+     * per-512 coarse levels computed at run time, the calibrated mul_scale
+     * absent and taken as ones).  The coarse scales go in the `global`
+     * buffer: float [rows, K/512].  Pairs with itself in qlin_gemm.           */
+    QLIN_MXFP4_DUAL = 11
 } qlin_format;
 
 typedef enum {
@@ -152,6 +164,11 @@ size_t qlin_scales_bytes(qlin_format fmt, qlin_scale_layout layout, int64_t rows
  * n = 8i+j in bits [4j,4j+4); no "-1" offset is applied.                     */
 size_t qlin_zeros_bytes(qlin_format fmt, int64_t rows, int64_t K);
 
+/* Second-level scale buffer (`global`): NVFP4 4 bytes (one float, the
+ * per-tensor scale); MXFP4_DUAL rows*(K/512)*4 (float [rows, K/512], the
+ * coarse scales); 0 otherwise.                                              */
+size_t qlin_global_bytes(qlin_format fmt, int64_t rows, int64_t K);
+
 /* Workspace (device scratch) a quantizer call needs: the per-tensor
  * formats (FP8_TENSOR, NVFP4) keep one float per reduction block; others 0. */
 size_t qlin_quant_workspace_bytes(qlin_format fmt, int64_t rows, int64_t K);
@@ -169,8 +186,9 @@ size_t qlin_gemm_workspace_bytes(qlin_format w_fmt, qlin_format x_fmt,
  *   codes_dev          qlin_codes_bytes(fmt, rows, K) bytes, 16-byte aligned
  *   scales_dev         qlin_scales_bytes(fmt, layout, rows, K) bytes
  *   zeros_dev          INT4 only (else NULL)
- *   global_dev         NVFP4 only: one float, the per-tensor scale g
- *   layout             QLIN_SCALE_MMA is accepted for MXFP8, MXFP4 and NVFP4 only
+ *   global_dev         NVFP4: one float, the per-tensor scale g; MXFP4_DUAL:
+ *                      the coarse scales, qlin_global_bytes(...) bytes
+ *   layout             QLIN_SCALE_MMA is accepted for MXFP8, MXFP4, MXFP4_DUAL and NVFP4 only
  *   workspace_dev      qlin_quant_workspace_bytes(...) bytes (NULL if 0)
  * Requirements: src and ld*2 bytes 16-byte aligned; K % 8 == 0;
  *   rows < 2^31, K < 2^31 and rows' * ceil(K/256) < 2^31, rows' being rows
@@ -178,7 +196,8 @@ size_t qlin_gemm_workspace_bytes(qlin_format w_fmt, qlin_format x_fmt,
  *   FP8_GROUP128, MXFP8, MXFP4 and NVFP4 also K <= 65535 * 1024;
  *   FP8_BLOCK128: rows % 128 == 0 and K % 128 == 0; FP8_GROUP128: K % 128 == 0;
  *   MXFP8: K % 32 == 0
- *   (K % 128 == 0 for the MMA layout), the same for MXFP4; NVFP4: K % 16 == 0
+ *   (K % 128 == 0 for the MMA layout), the same for MXFP4; MXFP4_DUAL: K % 512 == 0;
+ *   NVFP4: K % 16 == 0
  *   (K % 64 for MMA);
  *   INT4 (both variants): rows % 8 == 0 and K % 128 == 0.
  * Errors: QLIN_ERR_INVALID_ARG, QLIN_ERR_ALIGNMENT, QLIN_ERR_UNSUPPORTED
@@ -226,6 +245,10 @@ qlin_status qlin_quantize_act(qlin_format fmt, const void *x_bf16_dev, int64_t M
  *   NVFP4, NVFP4           : scales in QLIN_SCALE_MMA layout, x_global and
  *                            w_global one float each (K % 256 == 0)
  *   MXFP4, MXFP4           : scales in QLIN_SCALE_MMA layout (K % 256 == 0)
+ *   MXFP4_DUAL, MXFP4_DUAL : fine scales in QLIN_SCALE_MMA layout, x_global and
+ *                            w_global the coarse scales [M, K/512] and
+ *                            [N, K/512] (K % 512 == 0); each 512-K partial is
+ *                            scaled by x_global[m,b] * w_global[n,b] in fp32
  *   INT8_ROW, INT8_ROW     : x_scales float [M], w_scales float [N] (K % 16 == 0).
  *                            sm_103a has no integer tensor-core MMA, so the
  *                            kernel turns the codes into exact fp16 values on

@@ -13,7 +13,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 bool is_quant_format(qlin_format f) {
     return (f >= QLIN_FP8_TENSOR && f <= QLIN_INT4_G128_ASYM) || f == QLIN_MXFP4 || f == QLIN_FP8_GROUP128 ||
-           f == QLIN_INT8_ROW || f == QLIN_INT4_G128_SYM;
+           f == QLIN_INT8_ROW || f == QLIN_INT4_G128_SYM || f == QLIN_MXFP4_DUAL;
 }
 
 bool is_int4(qlin_format f) { return f == QLIN_INT4_G128_ASYM || f == QLIN_INT4_G128_SYM;
@@ -36,10 +36,12 @@ qlin_status check_quant_shape(qlin_format fmt, qlin_scale_layout layout, int64_t
     // the element-wise walks number their 256-element row tasks in 32 bits
     const int64_t rows_pad = layout == QLIN_SCALE_MMA ? ceil_div(rows, 128) * 128 : rows;
     if (rows_pad * ceil_div(K, 256) > 0x7FFFFFFFll) return QLIN_ERR_INVALID_ARG;
-    if (layout == QLIN_SCALE_MMA && fmt != QLIN_MXFP8 && fmt != QLIN_MXFP4 && fmt != QLIN_NVFP4)
+    if (layout == QLIN_SCALE_MMA && fmt != QLIN_MXFP8 && fmt != QLIN_MXFP4 && fmt != QLIN_NVFP4 &&
+        fmt != QLIN_MXFP4_DUAL)
         return QLIN_ERR_UNSUPPORTED;
     // the row-chunk walks (1 x 128 groups, MX, NVFP4) put a row's 1024-element chunks on grid y
-    if ((fmt == QLIN_FP8_GROUP128 || fmt == QLIN_MXFP8 || fmt == QLIN_MXFP4 || fmt == QLIN_NVFP4) &&
+    if ((fmt == QLIN_FP8_GROUP128 || fmt == QLIN_MXFP8 || fmt == QLIN_MXFP4 || fmt == QLIN_NVFP4 ||
+         fmt == QLIN_MXFP4_DUAL) &&
         ceil_div(K, 1024) > 65535)
         return QLIN_ERR_INVALID_ARG;
     switch (fmt) {
@@ -55,6 +57,7 @@ qlin_status check_quant_shape(qlin_format fmt, qlin_scale_layout layout, int64_t
         case QLIN_NVFP4:
             if (K % 16) return QLIN_ERR_INVALID_ARG;
             return (layout == QLIN_SCALE_MMA && K % 64) ? QLIN_ERR_INVALID_ARG : QLIN_OK;
+        case QLIN_MXFP4_DUAL: return (K % 512) ? QLIN_ERR_INVALID_ARG : QLIN_OK;
         case QLIN_INT4_G128_ASYM:
         case QLIN_INT4_G128_SYM: return (rows % 8 || K % 128) ? QLIN_ERR_INVALID_ARG : QLIN_OK;
         default: return QLIN_ERR_UNSUPPORTED;
@@ -69,7 +72,8 @@ qlin_status quantize(qlin_format fmt, const void* src, int64_t rows, int64_t K, 
     if (s != QLIN_OK) return s;
     if (!src || !codes || !scales || ld < K) return QLIN_ERR_INVALID_ARG;
     if (is_int4(fmt) && !zeros) return QLIN_ERR_INVALID_ARG;
-    if (fmt == QLIN_NVFP4 && !global) return QLIN_ERR_INVALID_ARG;
+    if ((fmt == QLIN_NVFP4 || fmt == QLIN_MXFP4_DUAL) && !global) return QLIN_ERR_INVALID_ARG;
+    if (fmt == QLIN_MXFP4_DUAL && (reinterpret_cast<uintptr_t>(global) & 3u)) return QLIN_ERR_ALIGNMENT;
     if (!aligned16(src) || (ld * 2) % 16 || !aligned16(codes)) return QLIN_ERR_ALIGNMENT;
     if (fmt == QLIN_FP8_TOKEN || fmt == QLIN_FP8_BLOCK128 || fmt == QLIN_FP8_TENSOR || fmt == QLIN_FP8_GROUP128 ||
         fmt == QLIN_INT8_ROW) {
@@ -100,6 +104,8 @@ qlin_status quantize(qlin_format fmt, const void* src, int64_t rows, int64_t K, 
             return launch_status(launch_mxfp8(x, rows, K, ld, c, static_cast<uint8_t*>(scales), mma, st));
         case QLIN_MXFP4:
             return launch_status(launch_mxfp4(x, rows, K, ld, c, static_cast<uint8_t*>(scales), mma, st));
+        case QLIN_MXFP4_DUAL:
+            return launch_status(launch_mxfp4_dual(x, rows, K, ld, c, static_cast<uint8_t*>(scales), global, mma, st));
         case QLIN_NVFP4:
             return launch_status(launch_nvfp4(x, rows, K, ld, c, static_cast<uint8_t*>(scales), global, mma,
                                               static_cast<float*>(ws), amax_partials(rows, K), st));
@@ -143,7 +149,8 @@ size_t qlin_codes_bytes(qlin_format fmt, int64_t rows, int64_t K) {
         case QLIN_INT8_ROW:
         case QLIN_MXFP8: return (size_t)(rows * K);
         case QLIN_NVFP4:
-        case QLIN_MXFP4: return (size_t)(rows * (K / 2));
+        case QLIN_MXFP4:
+        case QLIN_MXFP4_DUAL: return (size_t)(rows * (K / 2));
         case QLIN_INT4_G128_ASYM:
         case QLIN_INT4_G128_SYM: return (size_t)((K / 8) * rows * 4);
         default: return 0;
@@ -160,7 +167,8 @@ size_t qlin_scales_bytes(qlin_format fmt, qlin_scale_layout layout, int64_t rows
         case QLIN_FP8_BLOCK128: return (size_t)((rows / 128) * (K / 128) * 4);
         case QLIN_FP8_GROUP128: return (size_t)(rows * (K / 128) * 4);
         case QLIN_MXFP8:
-        case QLIN_MXFP4: return (size_t)((layout == QLIN_SCALE_MMA ? rows_pad : rows) * (K / 32));
+        case QLIN_MXFP4:
+        case QLIN_MXFP4_DUAL: return (size_t)((layout == QLIN_SCALE_MMA ? rows_pad : rows) * (K / 32));
         case QLIN_NVFP4: return (size_t)((layout == QLIN_SCALE_MMA ? rows_pad : rows) * (K / 16));
         case QLIN_INT4_G128_ASYM:
         case QLIN_INT4_G128_SYM: return (size_t)((K / 128) * rows * 2);
@@ -171,6 +179,13 @@ size_t qlin_scales_bytes(qlin_format fmt, qlin_scale_layout layout, int64_t rows
 size_t qlin_zeros_bytes(qlin_format fmt, int64_t rows, int64_t K) {
     if (!is_int4(fmt) || rows < 1 || K < 1) return 0;
     return (size_t)((K / 128) * (rows / 8) * 4);
+}
+
+size_t qlin_global_bytes(qlin_format fmt, int64_t rows, int64_t K) {
+    if (rows < 1 || K < 1) return 0;
+    if (fmt == QLIN_NVFP4) return 4;
+    if (fmt == QLIN_MXFP4_DUAL) return (size_t)(rows * (K / 512) * 4);
+    return 0;
 }
 
 size_t qlin_quant_workspace_bytes(qlin_format fmt, int64_t rows, int64_t K) {
@@ -245,6 +260,15 @@ qlin_status qlin_gemm(qlin_format w_fmt, qlin_format x_fmt, int64_t M, int64_t N
         if (K % 256) return QLIN_ERR_INVALID_ARG;
         if (!aligned16(x_scales_dev) || !aligned16(w_scales_dev)) return QLIN_ERR_ALIGNMENT;
         return launch_status(launch_gemm_mxfp4(a, st));
+    }
+    if (w_fmt == QLIN_MXFP4_DUAL && x_fmt == QLIN_MXFP4_DUAL) {
+        if (layout != QLIN_SCALE_MMA) return QLIN_ERR_UNSUPPORTED;
+        if (!x_scales_dev || !w_scales_dev || !x_global_dev || !w_global_dev) return QLIN_ERR_INVALID_ARG;
+        if (K % 512) return QLIN_ERR_INVALID_ARG;
+        if (!aligned16(x_scales_dev) || !aligned16(w_scales_dev) ||
+            (reinterpret_cast<uintptr_t>(x_global_dev) & 3u) || (reinterpret_cast<uintptr_t>(w_global_dev) & 3u))
+            return QLIN_ERR_ALIGNMENT;
+        return launch_status(launch_gemm_mxfp4_dual(a, st));
     }
     if (w_fmt == QLIN_NVFP4 && x_fmt == QLIN_NVFP4) {
         if (layout != QLIN_SCALE_MMA) return QLIN_ERR_UNSUPPORTED;

@@ -73,7 +73,7 @@ namespace {
 
 using namespace ptx;
 
-enum Kind { kFp8Tensor = 0, kFp8Block = 1, kMxfp8 = 2, kNvfp4 = 3, kMxfp4 = 4, kInt8 = 5, kFp8QX = 6 };
+enum Kind { kFp8Tensor = 0, kFp8Block = 1, kMxfp8 = 2, kNvfp4 = 3, kMxfp4 = 4, kInt8 = 5, kFp8QX = 6, kMx4Dual = 7 };
 
 constexpr int BM = 128;              // tile rows (X rows) = MMA M
 constexpr int BKB = 128;             // K bytes per stage: 128 fp8 or 256 fp4 (one swizzle row)
@@ -105,10 +105,12 @@ struct Cfg {
     static constexpr int A8_BYTES = CVT ? BM * K8 : 0;
     static constexpr int B8_BYTES = CVT ? BN * K8 : 0;
     // 512-byte scale chunks (128 rows x 4 scales) per 128 rows per stage
-    static constexpr int SF_CHUNKS = (KIND == kMxfp8) ? 1 : (KIND == kNvfp4 ? 4 : (KIND == kMxfp4 ? 2 : 0));
+    static constexpr bool DUAL = (KIND == kMx4Dual);  // MXFP4 dual-scale: per-512 partials promoted on chip
+    static constexpr int SF_CHUNKS =
+        (KIND == kMxfp8) ? 1 : (KIND == kNvfp4 ? 4 : ((KIND == kMxfp4 || KIND == kMx4Dual) ? 2 : 0));
     // NVFP4 has 12 scale-chunk copies per stage: two threads issue them off the
     // MMA thread; MXFP8's 3 copies stay with the MMA issuer
-    static constexpr bool SPLIT_CP = (KIND == kNvfp4 || KIND == kMxfp4);
+    static constexpr bool SPLIT_CP = (KIND == kNvfp4 || KIND == kMxfp4 || KIND == kMx4Dual);
     static constexpr int SFA_BYTES = SF_CHUNKS * 512;
     static constexpr int SFB_BYTES = SF_CHUNKS * 512 * (BN / 128);
     static constexpr int KSTEPS = BKB / 32;          // each MMA consumes 32 bytes of K
@@ -126,7 +128,10 @@ struct Cfg {
     // full[S], empty[S], accf, acce, pfull[2], pempty[2], drain, sfready[S], s8full[S8], s8empty[S8]
     static constexpr int NBAR = 3 * STAGES + 7 + 2 * S8;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-    static constexpr int SMEM = OFF_MISC + 64 + 1024; // + slack for 1024-byte alignment
+    // dual-scale: each epilogue warp stages its 128 columns' W coarse scales of a block
+    static constexpr int OFF_SWS = OFF_MISC + 64;
+    static constexpr int SWS_BYTES = DUAL ? EPI_WARPS * 128 * 4 : 0;
+    static constexpr int SMEM = OFF_SWS + SWS_BYTES + 1024; // + slack for 1024-byte alignment
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr int SFA_COL = 256;
     static constexpr int SFA_COLS = 4 * SF_CHUNKS;             // per stage
@@ -147,7 +152,7 @@ __host__ __device__ constexpr uint32_t idesc_for() {
         return (1u << 4) /* D f32 */ | (0u << 7) /* A f16 */ | (0u << 10) /* B f16 */ | n | m;
     if (KIND == kMxfp8)
         return (0u << 7) | (0u << 10) | n | (1u << 23) /* UE8M0 scales */ | m;
-    if (KIND == kMxfp4)
+    if (KIND == kMxfp4 || KIND == kMx4Dual)
         return (1u << 7) /* A e2m1 */ | (1u << 10) /* B e2m1 */ | n | (1u << 23) /* UE8M0 scales */ | m;
     return (1u << 7) /* A e2m1 */ | (1u << 10) /* B e2m1 */ | n | (0u << 23) /* UE4M3 scales */ | m;
 }
@@ -405,7 +410,7 @@ __global__ void __launch_bounds__(Cfg<KIND>::THREADS, 1)
                     record_timeout(p.status, abort_flag);
                     break;
                 }
-            } else if (KIND != kFp8Block) {
+            } else if (KIND != kFp8Block && !C::DUAL) {
                 if (!wait_or_abort(acce, (it & 1u) ^ 1u, abort_flag)) {
                     record_timeout(p.status, abort_flag);
                     break;
@@ -429,6 +434,15 @@ __global__ void __launch_bounds__(Cfg<KIND>::THREADS, 1)
                     }
                     d = tmem + (uint32_t)(b * C::BN);
                 }
+                if (C::DUAL && (kb & 1) == 0) {
+                    // one 512-K partial (two stages) at a time in columns [0, BN): wait until
+                    // the epilogue has read the previous one
+                    if (!wait_or_abort(pempty, (kbg & 1u) ^ 1u, abort_flag)) {
+                        record_timeout(p.status, abort_flag);
+                        ok = false;
+                        break;
+                    }
+                }
                 if (C::SPLIT_CP && !wait_or_abort(sfready + s, ph, abort_flag)) {
                     record_timeout(p.status, abort_flag);
                     ok = false;
@@ -449,7 +463,8 @@ __global__ void __launch_bounds__(Cfg<KIND>::THREADS, 1)
                 for (int c = 0; c < C::KSTEPS; c++) {
                     const uint64_t ad = sdesc_sw128(a_base + c * 32);
                     const uint64_t bd = sdesc_sw128(b_base + c * 32);
-                    const uint32_t acc = (KIND == kFp8Block) ? (c > 0) : (kb > 0 || c > 0);
+                    const uint32_t acc =
+                        (KIND == kFp8Block) ? (c > 0) : (C::DUAL ? ((kb & 1) || c > 0) : (kb > 0 || c > 0));
                     if (KIND == kFp8Tensor || KIND == kFp8Block || KIND == kFp8QX) {
                         mma_f8f6f4(d, ad, bd, idesc, acc);
                     } else if (KIND == kInt8) {
@@ -458,7 +473,7 @@ __global__ void __launch_bounds__(Cfg<KIND>::THREADS, 1)
                         const uint32_t id = idesc | ((uint32_t)c << 4) | ((uint32_t)c << 29);
                         mma_mxf8(d, ad, bd, id, tmem + C::SFA_COL + s * C::SFA_COLS,
                                  tmem + C::SFB_COL + s * C::SFB_COLS, acc);
-                    } else if (KIND == kMxfp4) {
+                    } else if (KIND == kMxfp4 || KIND == kMx4Dual) {
                         // chunk c/2 holds the scales of two MMAs; the ids 0 / 2 select the pair
                         const uint32_t sf = (uint32_t)(c & 1) * 2u;
                         const uint32_t id = idesc | (sf << 4) | (sf << 29);
@@ -474,10 +489,14 @@ __global__ void __launch_bounds__(Cfg<KIND>::THREADS, 1)
                     tc_commit(pfull + (kbg & 1u));
                     kbg++;
                 }
+                if (C::DUAL && (kb & 1) == 1) {
+                    tc_commit(pfull);
+                    kbg++;
+                }
                 misc[2] = kg + 1;
             }
             if (ok && C::CVT) tc_commit(pfull + (it & 1u));
-            else if (ok && KIND != kFp8Block) tc_commit(accf);
+            else if (ok && KIND != kFp8Block && !C::DUAL) tc_commit(accf);
         }
     } else if (!skip && C::SPLIT_CP && (warp == 2 || warp == 3) && lane == 0) {
         // ------------------------------------------------ scale-factor copies (NVFP4)
@@ -667,7 +686,7 @@ __global__ void __launch_bounds__(Cfg<KIND>::THREADS, 1)
                         }
                     }
                 }
-            } else if (KIND != kFp8Block) {
+            } else if (KIND != kFp8Block && !C::DUAL) {
                 if (!warp_wait_or_abort(accf, it & 1u, abort_flag)) {
                     if (lane == 0) record_timeout(p.status, abort_flag);
                     break;
@@ -688,6 +707,76 @@ __global__ void __launch_bounds__(Cfg<KIND>::THREADS, 1)
                         float v[32];
 #pragma unroll
                         for (int i = 0; i < 32; i++) v[i] = __uint_as_float(r[c][i]) * alpha;
+                        store_block32<C::STG_BUFS>(p, &tmY, stg, m0 + q * 32, ncol + c * 32, v);
+                    }
+                }
+            } else if constexpr (C::DUAL) {
+                // MXFP4 dual-scale: each 512-K partial (two stages), scaled by the row's and
+                // the column's coarse scales of that block.  The warp stages its 128 columns'
+                // W coarse scales of the block in its own shared slot (4 per lane, loaded a
+                // block ahead), so the multipliers come from broadcast reads.
+                const int nblk = p.K >> 9;
+                const bool row_ok = row < p.M;
+                const float* const sxrow = p.x_scale + (int64_t)(row_ok ? row : 0) * nblk;
+                float* const sws = reinterpret_cast<float*>(smem + C::OFF_SWS) + (warp - 4) * 128;
+                float sx_next = row_ok ? __ldg(sxrow) : 0.0f;
+                float swn[4];
+#pragma unroll
+                for (int i = 0; i < 4; i++) {
+                    const int col = ncol + lane + 32 * i;
+                    swn[i] = col < p.N ? __ldg(p.w_scale + (int64_t)col * nblk) : 0.0f;
+                }
+                uint64_t acc2[64];                  // 128 fp32 accumulators as (lo, hi) pairs
+#pragma unroll
+                for (int i = 0; i < 64; i++) acc2[i] = 0ull;
+                for (int b = 0; b < nblk; b++, kbg++) {
+                    const float sx = sx_next;
+                    __syncwarp();                   // every lane is done with the previous block's slot
+#pragma unroll
+                    for (int i = 0; i < 4; i++) sws[lane + 32 * i] = swn[i];
+                    __syncwarp();
+                    if (b + 1 < nblk) {
+                        sx_next = row_ok ? __ldg(sxrow + b + 1) : 0.0f;
+#pragma unroll
+                        for (int i = 0; i < 4; i++) {
+                            const int col = ncol + lane + 32 * i;
+                            swn[i] = col < p.N ? __ldg(p.w_scale + (int64_t)col * nblk + b + 1) : 0.0f;
+                        }
+                    }
+                    if (!warp_wait_or_abort(pfull, kbg & 1u, abort_flag)) {
+                        if (lane == 0) record_timeout(p.status, abort_flag);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    // two 64-column loads; the partial's columns are released after the second
+                    const uint32_t pbase = tmem + lane_addr + (uint32_t)(h * 128);
+#pragma unroll
+                    for (int c = 0; c < 2; c++) {
+                        uint32_t r[64];
+                        tmem_ld_32x32b_x64(pbase + (uint32_t)(c * 64), r);
+                        tmem_ld_wait();
+                        if (c == 1) {
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(pempty);
+                        }
+#pragma unroll
+                        for (int i = 0; i < 32; i++) {
+                            const float m0 = sx * sws[c * 64 + 2 * i], m1 = sx * sws[c * 64 + 2 * i + 1];
+                            acc2[c * 32 + i] = ffma2(pack_f32x2(__float_as_uint(m0), __float_as_uint(m1)),
+                                                     pack_f32x2(r[2 * i], r[2 * i + 1]), acc2[c * 32 + i]);
+                        }
+                    }
+                }
+                if (!ok) break;
+                uint8_t* stg = smem + C::OFF_STG + (warp - 4) * C::STG_BYTES;
+#pragma unroll
+                for (int c = 0; c < 4; c++) {
+                    if (ncol + c * 32 < p.N) {
+                        float v[32];
+#pragma unroll
+                        for (int i = 0; i < 16; i++) unpack_f32x2(acc2[c * 16 + i], v[2 * i], v[2 * i + 1]);
                         store_block32<C::STG_BUFS>(p, &tmY, stg, m0 + q * 32, ncol + c * 32, v);
                     }
                 }
@@ -903,7 +992,7 @@ bool make_tmap_u8(CUtensorMap* m, const void* base, uint64_t inner_bytes, uint64
 template <int KIND>
 cudaError_t launch_tc(const GemmArgs& a, cudaStream_t st) {
     using C = Cfg<KIND>;
-    const uint64_t kbytes = (KIND == kNvfp4 || KIND == kMxfp4) ? (uint64_t)a.K / 2 : (uint64_t)a.K;
+    const uint64_t kbytes = (KIND == kNvfp4 || KIND == kMxfp4 || KIND == kMx4Dual) ? (uint64_t)a.K / 2 : (uint64_t)a.K;
     CUtensorMap tmA, tmB;
     if (C::CVT) {
         if (!make_tmap_u8(&tmA, a.x, kbytes, (uint64_t)a.M, kbytes, BM, C::K8, false) ||
@@ -941,7 +1030,11 @@ cudaError_t launch_tc(const GemmArgs& a, cudaStream_t st) {
     p.w_global = a.w_global;
     p.sfa = static_cast<const uint8_t*>(a.x_scales);
     p.sfb = static_cast<const uint8_t*>(a.w_scales);
-    p.sf_chunks_per_row = (KIND == kMxfp8 || KIND == kMxfp4) ? a.K / 128 : a.K / 64;
+    p.sf_chunks_per_row = (KIND == kMxfp8 || KIND == kMxfp4 || KIND == kMx4Dual) ? a.K / 128 : a.K / 64;
+    if (KIND == kMx4Dual) {      // the coarse scales: [M, K/512] and [N, K/512]
+        p.x_scale = a.x_global;
+        p.w_scale = a.w_global;
+    }
     p.bias = a.bias;
     p.y = a.y;
     p.status = a.dev_status;
@@ -986,6 +1079,7 @@ cudaError_t launch_gemm_fp8_block(const GemmArgs& a, cudaStream_t st) { return l
 cudaError_t launch_gemm_mxfp8(const GemmArgs& a, cudaStream_t st) { return launch_tc<kMxfp8>(a, st); }
 cudaError_t launch_gemm_nvfp4(const GemmArgs& a, cudaStream_t st) { return launch_tc<kNvfp4>(a, st); }
 cudaError_t launch_gemm_mxfp4(const GemmArgs& a, cudaStream_t st) { return launch_tc<kMxfp4>(a, st); }
+cudaError_t launch_gemm_mxfp4_dual(const GemmArgs& a, cudaStream_t st) { return launch_tc<kMx4Dual>(a, st); }
 cudaError_t launch_gemm_int8(const GemmArgs& a, cudaStream_t st) { return launch_tc<kInt8>(a, st); }
 cudaError_t launch_gemm_fp8_tensor_fused_x(const GemmArgs& a, cudaStream_t st) { return launch_tc<kFp8QX>(a, st); }
 

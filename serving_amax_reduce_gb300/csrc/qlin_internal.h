@@ -26,6 +26,8 @@ cudaError_t launch_mxfp8(const uint16_t* x, int64_t rows, int64_t K, int64_t ld,
                          uint8_t* scales, bool mma_layout, cudaStream_t st);
 cudaError_t launch_mxfp4(const uint16_t* x, int64_t rows, int64_t K, int64_t ld, uint8_t* codes,
                          uint8_t* scales, bool mma_layout, cudaStream_t st);
+cudaError_t launch_mxfp4_dual(const uint16_t* x, int64_t rows, int64_t K, int64_t ld, uint8_t* codes,
+                              uint8_t* scales, float* coarse, bool mma_layout, cudaStream_t st);
 cudaError_t launch_nvfp4(const uint16_t* x, int64_t rows, int64_t K, int64_t ld, uint8_t* codes,
                          uint8_t* scales, float* global, bool mma_layout, float* partials,
                          int nparts, cudaStream_t st);
@@ -59,6 +61,7 @@ cudaError_t launch_gemm_fp8_block(const GemmArgs& a, cudaStream_t st);
 cudaError_t launch_gemm_mxfp8(const GemmArgs& a, cudaStream_t st);
 cudaError_t launch_gemm_nvfp4(const GemmArgs& a, cudaStream_t st);
 cudaError_t launch_gemm_mxfp4(const GemmArgs& a, cudaStream_t st);
+cudaError_t launch_gemm_mxfp4_dual(const GemmArgs& a, cudaStream_t st);
 cudaError_t launch_gemm_int8(const GemmArgs& a, cudaStream_t st);
 // FP8 per-tensor weights x bf16 activations quantized per tensor inside the GEMM (M <= 128)
 cudaError_t launch_gemm_fp8_tensor_fused_x(const GemmArgs& a, cudaStream_t st);

@@ -1,5 +1,6 @@
 // Online quantizers: bf16 -> FP8 E4M3 (tensor / token / 1x128 group /
-// 128x128 block), MXFP8, MXFP4, NVFP4, int4 g128 and INT8 per row.  Each
+// 128x128 block), MXFP8, MXFP4 (single and dual scale), NVFP4, int4 g128 and
+// INT8 per row.  Each
 // reads its bf16 input once from HBM in 16-byte vectors, reduces amax (or
 // min/max) with warp shuffles, and writes codes and scales in the same pass.
 // The per-tensor formats need the tensor amax before any code exists, so they
@@ -99,6 +100,18 @@ __device__ __forceinline__ uint32_t enc8_e2m1(const uint4& v, float r) {
     uint32_t b2 = cvt_e2m1x2(__fmul_rn(bf16_lo(v.z), r), __fmul_rn(bf16_hi(v.z), r));
     uint32_t b3 = cvt_e2m1x2(__fmul_rn(bf16_lo(v.w), r), __fmul_rn(bf16_hi(v.w), r));
     return b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
+}
+
+// 8 bf16 times r (rounded), then times the power of two m (exact) -> 8
+// E2M1 codes packed in 4 bytes: the two steps of the dual-scale rule.
+__device__ __forceinline__ uint32_t enc8_e2m1_2(const uint4& v, float r, float m) {
+    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+    uint32_t out = 0;
+#pragma unroll
+    for (int i = 0; i < 4; i++)
+        out |= cvt_e2m1x2(__fmul_rn(__fmul_rn(bf16_lo(u[i]), r), m), __fmul_rn(__fmul_rn(bf16_hi(u[i]), r), m))
+               << (8 * i);
+    return out;
 }
 
 __device__ __forceinline__ float warp_max(float v) {
@@ -444,6 +457,62 @@ __global__ void __launch_bounds__(256) k_mx(const uint16_t* __restrict__ x, int 
     }
 }
 
+// ---------------------------------------------------------------- MXFP4 dual-scale
+// A warp chunk (1024 elements of a row) holds two 512-element coarse blocks:
+// vector slots u = 0, 1 of every lane form the first, u = 2, 3 the second
+// (K % 512 == 0).  The coarse amax is a full-warp maximum, the coarse scale
+// A / 6 and multiplier 6 / A follow, and each 32-element granule (four lanes)
+// takes the MX rule on its normalized values: its amax times 6 / A, rounded,
+// is the maximum of the rounded products because rounding is monotone.
+__global__ void __launch_bounds__(256) k_mx_dual(const uint16_t* __restrict__ x, int rows, int rows_pad, int K,
+                                                 int64_t ld, uint8_t* __restrict__ codes,
+                                                 uint8_t* __restrict__ scales, float* __restrict__ coarse, int mma) {
+    const int lane = threadIdx.x & 31;
+    const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (row >= rows_pad) return;
+    const bool live = row < rows;
+    const int nvr = K >> 3, c0 = blockIdx.y * kChunk + lane;
+    const uint16_t* src = x + (int64_t)row * ld;
+    uint4 v[kChunkU];
+#pragma unroll
+    for (int u = 0; u < kChunkU; u++) {
+        const int c = c0 + 32 * u;
+        v[u] = (live && c < nvr) ? ld16(src + 8 * c) : make_uint4(0, 0, 0, 0);
+    }
+    const int64_t chunks = K >> 7;
+    uint32_t* crow = reinterpret_cast<uint32_t*>(codes + (int64_t)row * (K >> 1));
+#pragma unroll
+    for (int blk = 0; blk < 2; blk++) {
+        const float A = warp_max(fmaxf(absmax8_bf16x2(v[2 * blk]), absmax8_bf16x2(v[2 * blk + 1])));
+        float cs = 1.0f, rc = 1.0f;
+        if (A != 0.0f) {
+            cs = __fdiv_rn(A, 6.0f);
+            rc = __fdiv_rn(6.0f, A);
+        }
+        const int cb0 = blockIdx.y * kChunk + 64 * blk;          // first vector of this coarse block
+        if (cb0 >= nvr) break;                                    // K % 1024 == 512: the chunk's last block is absent
+        if (live && lane == 0) coarse[(int64_t)row * (K >> 9) + (cb0 >> 6)] = cs;
+#pragma unroll
+        for (int uu = 0; uu < 2; uu++) {
+            const int u = 2 * blk + uu, c = c0 + 32 * u;
+            float a = absmax8_bf16x2(v[u]);
+            a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
+            a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 2));
+            a = __fmul_rn(a, rc);
+            const int biased = (int)(__float_as_uint(a) >> 23);
+            int e = (a == 0.0f || biased == 0) ? -127 : max(biased - 127 - 2, -127);
+            e = min(e, 127);
+            const float mult = __uint_as_float((uint32_t)(127 - e) << 23);   // 2^-e, e <= 126 here
+            if (live) crow[c] = enc8_e2m1_2(v[u], rc, mult);
+            if ((c & 3) == 0) {
+                const int64_t j = c >> 2;
+                const int64_t off = mma ? mma_scale_offset(row, j, chunks) : (int64_t)row * (K >> 5) + j;
+                scales[off] = (uint8_t)(e + 127);
+            }
+        }
+    }
+}
+
 // ---------------------------------------------------------------- NVFP4
 // After the amax pass: two consecutive lanes own one 16-element block.  The
 // code multiplier rg / dsb depends only on the block's UE4M3 scale code, so
@@ -707,6 +776,14 @@ cudaError_t launch_mxfp4(const uint16_t* x, int64_t rows, int64_t K, int64_t ld,
                          uint8_t* scales, bool mma_layout, cudaStream_t st) {
     const int64_t rows_pad = mma_layout ? (rows + 127) / 128 * 128 : rows;
     k_mx<true><<<chunk_grid(rows_pad, K), 256, 0, st>>>(x, (int)rows, (int)rows_pad, (int)K, ld, codes, scales,
+                                                        mma_layout ? 1 : 0);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_mxfp4_dual(const uint16_t* x, int64_t rows, int64_t K, int64_t ld, uint8_t* codes,
+                              uint8_t* scales, float* coarse, bool mma_layout, cudaStream_t st) {
+    const int64_t rows_pad = mma_layout ? (rows + 127) / 128 * 128 : rows;
+    k_mx_dual<<<chunk_grid(rows_pad, K), 256, 0, st>>>(x, (int)rows, (int)rows_pad, (int)K, ld, codes, scales, coarse,
                                                         mma_layout ? 1 : 0);
     return cudaGetLastError();
 }

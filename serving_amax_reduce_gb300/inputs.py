@@ -142,6 +142,15 @@ def mxfp8_linear(K: int, N: int, M: int = MXFP8_M) -> Linear:
                   _seed(4, 2 * v), _seed(4, 2 * v + 1), "normal", x_std=1.0, w_std=0.015)
 
 
+def mxfp4_dual_linear(K: int, N: int, M: int = MXFP8_M) -> Linear:
+    """MXFP4 dual-scale W4A4 on the video-DiT shapes and distributions of the
+    MXFP8 workload, the same X and W as the single-scale MXFP4 row (seeds of
+    workload 6)."""
+    v = MXFP8_SHAPES.index((K, N)) if (K, N) in MXFP8_SHAPES else 7
+    return Linear(f"mxfp4_dual_K{K}_N{N}", M, K, N, "mxfp4_dual", "mxfp4_dual",
+                  _seed(6, 2 * v), _seed(6, 2 * v + 1), "normal", x_std=1.0, w_std=0.015)
+
+
 def fp8_group_linear(K: int, N: int, M: int = 4096) -> Linear:
     """FP8 1 x 128 dynamic activation groups x 128x128-block weights on the DiT MLP
     shapes and distributions of the FP8 block workload (1% outlier channels)."""

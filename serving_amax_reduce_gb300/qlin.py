@@ -31,6 +31,7 @@ class Fmt(enum.IntEnum):
     FP8_GROUP128 = 8
     INT8_ROW = 9
     INT4_G128_SYM = 10
+    MXFP4_DUAL = 11
 
 
 class Layout(enum.IntEnum):
@@ -75,6 +76,7 @@ def _load():
         "qlin_codes_bytes": ([_I, _I64, _I64], _SZ),
         "qlin_scales_bytes": ([_I, _I, _I64, _I64], _SZ),
         "qlin_zeros_bytes": ([_I, _I64, _I64], _SZ),
+        "qlin_global_bytes": ([_I, _I64, _I64], _SZ),
         "qlin_quant_workspace_bytes": ([_I, _I64, _I64], _SZ),
         "qlin_gemm_workspace_bytes": ([_I, _I, _I64, _I64, _I64], _SZ),
         "qlin_quantize_weight": ([_I, _P, _I64, _I64, _I64, _P, _P, _P, _P, _I, _P, _SZ, _P, _P], _I),
@@ -119,6 +121,10 @@ def qlin_scales_bytes(fmt, layout, rows, K) -> int:
 
 def qlin_zeros_bytes(fmt, rows, K) -> int:
     return _load().qlin_zeros_bytes(int(fmt), rows, K)
+
+
+def qlin_global_bytes(fmt, rows, K) -> int:
+    return _load().qlin_global_bytes(int(fmt), rows, K)
 
 
 def qlin_quant_workspace_bytes(fmt, rows, K) -> int:
@@ -212,8 +218,7 @@ def _check_quant_bufs(fmt: Fmt, rows: int, K: int, layout: Layout, b: dict):
     _need(b["codes"], qlin_codes_bytes(fmt, rows, K), "codes")
     _need(b["scales"], qlin_scales_bytes(fmt, layout, rows, K), "scales")
     _need(b.get("zeros"), qlin_zeros_bytes(fmt, rows, K), "zeros")
-    if fmt == Fmt.NVFP4:
-        _need(b.get("global"), 4, "global")
+    _need(b.get("global"), qlin_global_bytes(fmt, rows, K), "global")
     wsb = qlin_quant_workspace_bytes(fmt, rows, K)
     _need(b.get("workspace"), wsb, "workspace")
     if b.get("workspace_bytes", 0) < wsb:
@@ -236,8 +241,9 @@ def alloc_quant(fmt: Fmt, rows: int, K: int, layout: Layout, device) -> dict:
         out["zeros"] = _empty(qlin_zeros_bytes(fmt, rows, K), device, torch.int32)
     else:
         out["scales"] = _empty(sb, device)
-    if fmt == Fmt.NVFP4:
-        out["global"] = torch.empty(1, dtype=torch.float32, device=device)
+    gb = qlin_global_bytes(fmt, rows, K)
+    if gb:
+        out["global"] = _empty(gb, device, torch.float32)
     wsb = qlin_quant_workspace_bytes(fmt, rows, K)
     out["workspace"] = _empty(wsb, device, torch.float32) if wsb else None
     out["workspace_bytes"] = wsb
@@ -286,9 +292,11 @@ def gemm(w_fmt: Fmt, x_fmt: Fmt, M: int, N: int, K: int, x, x_scales, w_codes, w
     else:
         _need(x, qlin_codes_bytes(x_fmt, M, K), "x codes")
         _need(x_scales, qlin_scales_bytes(x_fmt, layout, M, K), "x_scales")
+        _need(x_global, qlin_global_bytes(x_fmt, M, K), "x_global")
     _need(w_codes, qlin_codes_bytes(w_fmt, N, K), "w_codes")
     _need(w_scales, qlin_scales_bytes(w_fmt, layout, N, K), "w_scales")
     _need(w_zeros, qlin_zeros_bytes(w_fmt, N, K), "w_zeros")
+    _need(w_global, qlin_global_bytes(w_fmt, N, K), "w_global")
     if bias is not None and (bias.dtype != torch.bfloat16 or bias.numel() < N or not bias.is_contiguous()):
         raise ValueError(f"bias: {N} contiguous bf16 values are required")
     wsb = qlin_gemm_workspace_bytes(w_fmt, x_fmt, M, N, K)

@@ -68,6 +68,11 @@ def test_size_queries(q):
     assert q.qlin_scales_bytes(F.INT8_ROW, L.CANONICAL, 4096, 3072) == 4096 * 4
     assert q.qlin_quant_workspace_bytes(F.INT8_ROW, 4096, 3072) == 0
     assert q.qlin_gemm_workspace_bytes(F.INT8_ROW, F.INT8_ROW, 4096, 12288, 3072) == 0
+    # MXFP4 dual-scale: MXFP4's codes and fine scales, coarse fp32 scales per 512 in `global`
+    assert q.qlin_codes_bytes(F.MXFP4_DUAL, 20280, 5120) == 20280 * 2560
+    assert q.qlin_scales_bytes(F.MXFP4_DUAL, L.MMA, 20280, 5120) == 20352 * 160
+    assert q.qlin_global_bytes(F.MXFP4_DUAL, 20280, 5120) == 20280 * 10 * 4
+    assert q.qlin_global_bytes(F.NVFP4, 20280, 5120) == 4 and q.qlin_global_bytes(F.MXFP4, 20280, 5120) == 0
     # symmetric int4: the asymmetric variant's layouts
     for fn in (q.qlin_codes_bytes, q.qlin_zeros_bytes, q.qlin_quant_workspace_bytes):
         assert fn(F.INT4_G128_SYM, 4096, 12288) == fn(F.INT4_G128_ASYM, 4096, 12288)
@@ -141,6 +146,11 @@ def test_quantize_rejects_bad_arguments(q):
                                   None, 0, None, None) == S.INVALID_ARG                 # N % 8
     assert q.qlin_quantize_weight(F.INT4_G128_SYM, FAKE, 128, 1024, 1024, FAKE, FAKE, FAKE, None, L.MMA,
                                   None, 0, None, None) == S.UNSUPPORTED
+    # MXFP4 dual-scale: K % 512, and the coarse-scale buffer is required
+    assert q.qlin_quantize_act(F.MXFP4_DUAL, FAKE, 128, 768, 768, FAKE, FAKE, FAKE, L.MMA, None, 0,
+                               None, None) == S.INVALID_ARG
+    assert q.qlin_quantize_act(F.MXFP4_DUAL, FAKE, 128, 1024, 1024, FAKE, FAKE, None, L.MMA, None, 0,
+                               None, None) == S.INVALID_ARG
 
 
 def test_gemm_rejects_bad_arguments(q):
@@ -174,6 +184,10 @@ def test_gemm_rejects_bad_arguments(q):
     assert g(F.INT8_ROW, F.INT8_ROW, 128, 1024, 1000) == S.INVALID_ARG         # K % 16
     assert g(F.INT8_ROW, F.INT8_ROW, 128, 1024, 1024, ws=None) == S.INVALID_ARG
     assert g(F.INT8_ROW, F.FP8_TOKEN, 128, 1024, 1024) == S.UNSUPPORTED
+    assert g(F.MXFP4_DUAL, F.MXFP4_DUAL, 128, 1024, 1024) == S.UNSUPPORTED        # canonical scales
+    assert g(F.MXFP4_DUAL, F.MXFP4_DUAL, 128, 1024, 768, layout=L.MMA) == S.INVALID_ARG   # K % 512
+    assert g(F.MXFP4_DUAL, F.MXFP4_DUAL, 128, 1024, 1024, layout=L.MMA, wg=None) == S.INVALID_ARG
+    assert g(F.MXFP4_DUAL, F.MXFP4, 128, 1024, 1024, layout=L.MMA) == S.UNSUPPORTED
     assert g(F.FP8_BLOCK128, F.INT8_ROW, 128, 1024, 1024) == S.UNSUPPORTED
     assert g(F.INT4_G128_ASYM, F.BF16, 16, 4096, 4000) == S.INVALID_ARG
     need = q.qlin_gemm_workspace_bytes(F.INT4_G128_ASYM, F.BF16, 16, 4096, 4096)

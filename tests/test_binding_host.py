@@ -52,6 +52,7 @@ PAIRS = [
     ("FP8_TENSOR", "BF16", "CANONICAL", (77, 640, 1040)),
     ("INT4_G128_ASYM", "BF16", "CANONICAL", (33, 136, 128)),
     ("INT4_G128_SYM", "BF16", "CANONICAL", (16, 4096, 4096)),
+    ("MXFP4_DUAL", "MXFP4_DUAL", "MMA", (300, 640, 2560)),
 ]
 
 

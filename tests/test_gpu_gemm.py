@@ -312,6 +312,43 @@ def test_mxfp4_gemm_full_size(q, orc):
     mxfp4_case(q, orc, 20280, 5120, 5120, nrows=256)
 
 
+# ------------------------------------------------------------------ MXFP4 dual-scale
+def mxfp4_dual_case(q, orc, M, N, K, nrows=None, with_bias=False):
+    lin = inputs.mxfp8_linear(K, N, M=M)          # the MXFP8 workload's distributions
+    x, w = lin.make_x(), lin.make_w()
+    F, L = q.Fmt, q.Layout
+    bx = q.quantize_act(F.MXFP4_DUAL, x.cuda(), L.MMA)
+    bw = q.quantize_weight(F.MXFP4_DUAL, w.cuda(), L.MMA)
+    bias = inputs.normal_bf16((1, N), 0.05, 83)[0] if with_bias else None
+    y = q.gemm(F.MXFP4_DUAL, F.MXFP4_DUAL, M, N, K, bx["codes"], bx["scales"], bw["codes"], bw["scales"],
+               layout=L.MMA, x_global=bx["global"], w_global=bw["global"], bias=bias.cuda() if with_bias else None)
+    torch.cuda.synchronize()
+    rows = sample_rows(M, nrows or M)
+    xs = mma_to_canonical(np_u8(bx["scales"]), M, K // 32)[rows]
+    xc = np_f32(bx["global"])[: M * K // 512].reshape(M, K // 512)[rows]
+    xh = orc.dequant_mxfp4_dual(np_u8(bx["codes"]).reshape(M, K // 2)[rows], xs, xc)
+    wh = orc.dequant_mxfp4_dual(np_u8(bw["codes"]).reshape(N, K // 2), mma_to_canonical(np_u8(bw["scales"]), N, K // 32),
+                                np_f32(bw["global"])[: N * K // 512].reshape(N, K // 512))
+    b = orc.bf16_values(bits(bias)[None, :])[0] if with_bias else None
+    return check(orc, y_np(y)[rows], orc.gemm_ref(xh, wh, bias=b), x, w, rows=torch.from_numpy(rows))
+
+
+# ragged M and N tiles, one 512-K block, several blocks, K with an odd number of 512 blocks
+@pytest.mark.parametrize("M,N,K", [(200, 512, 512), (128, 256, 1024), (1, 256, 1536), (300, 640, 2560),
+                                   (513, 1280, 5120)])
+def test_mxfp4_dual_gemm(q, orc, M, N, K):
+    mxfp4_dual_case(q, orc, M, N, K)
+
+
+def test_mxfp4_dual_gemm_bias(q, orc):
+    mxfp4_dual_case(q, orc, 130, 384, 1024, with_bias=True)
+
+
+@pytest.mark.slow
+def test_mxfp4_dual_gemm_full_size(q, orc):
+    mxfp4_dual_case(q, orc, 20280, 5120, 5120, nrows=256)
+
+
 # ------------------------------------------------------------------ W4A16 decode
 def w4a16_case(q, orc, M, K, N, with_bias=False, sym=False):
     lin = inputs.w4a16_linear(M, K, N)

@@ -59,6 +59,8 @@ QUANT_CASES = [
     ("INT8_ROW", "CANONICAL", 3, 20480),
     ("INT4_G128_ASYM", "CANONICAL", 200, 1024),
     ("INT4_G128_SYM", "CANONICAL", 200, 1024),
+    ("MXFP4_DUAL", "CANONICAL", 333, 1536),
+    ("MXFP4_DUAL", "MMA", 333, 1536),
 ]
 
 
@@ -101,6 +103,7 @@ PAIRS = {
     "fp8_block_group128": ("FP8_BLOCK128", "FP8_GROUP128", "CANONICAL"),
     "mxfp8": ("MXFP8", "MXFP8", "MMA"),
     "mxfp4": ("MXFP4", "MXFP4", "MMA"),
+    "mxfp4_dual": ("MXFP4_DUAL", "MXFP4_DUAL", "MMA"),
     "nvfp4": ("NVFP4", "NVFP4", "MMA"),
     "int8": ("INT8_ROW", "INT8_ROW", "CANONICAL"),
     "fp8_tensor_fused_x": ("FP8_TENSOR", "BF16", "CANONICAL"),
@@ -114,6 +117,7 @@ GEMM_CASES = [
     ("fp8_block_group128", 130, 640, 256),
     ("mxfp8", 300, 640, 512),
     ("mxfp4", 130, 384, 512),
+    ("mxfp4_dual", 130, 384, 1024),
     ("nvfp4", 130, 384, 512),
     ("int8", 130, 640, 272),
     ("fp8_tensor_fused_x", 77, 640, 1040),
@@ -136,9 +140,9 @@ def gemm_operands(q, name, M, N, K):
     else:
         bx = q.quantize_act(xf, x, lay)
         xa, xs = bx["codes"], bx["scales"]
-        if xf == q.Fmt.NVFP4:
+        if xf in (q.Fmt.NVFP4, q.Fmt.MXFP4_DUAL):
             kw["x_global"] = bx["global"]
-    if wf == q.Fmt.NVFP4:
+    if wf in (q.Fmt.NVFP4, q.Fmt.MXFP4_DUAL):
         kw["w_global"] = bw["global"]
     if wf in (q.Fmt.INT4_G128_ASYM, q.Fmt.INT4_G128_SYM):
         kw["w_zeros"] = bw["zeros"]

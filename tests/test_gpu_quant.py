@@ -166,6 +166,24 @@ def test_mxfp4(q, orc, rows, K, kind, mma):
         assert np.array_equal(got[: rows * K // 32].reshape(rows, K // 32), sc)
 
 
+@pytest.mark.parametrize("rows,K", [(1, 512), (200, 5120), (130, 13824), (77, 1536), (3, 1024)])
+@pytest.mark.parametrize("kind", ["normal", "edge"])
+@pytest.mark.parametrize("mma", [False, True])
+def test_mxfp4_dual(q, orc, rows, K, kind, mma):
+    x = make(kind, rows, K, 9 * rows + K) if kind == "edge" else inputs.normal_bf16((rows, K), 1.0, rows + 3 * K)
+    b = run(q, q.Fmt.MXFP4_DUAL, x, q.Layout.MMA if mma else None)
+    packed, sc, coarse = orc.quant_mxfp4_dual(bits(x))
+    assert np.array_equal(np_u8(b["codes"]).reshape(rows, K // 2), packed)
+    assert np.array_equal(np_f32(b["global"])[: rows * K // 512].reshape(rows, K // 512).view(np.uint32),
+                          coarse.view(np.uint32))
+    got = np_u8(b["scales"])
+    if mma:
+        assert np.array_equal(mma_to_canonical(got, rows, K // 32), sc)
+        assert not mma_padding_rows(got, rows, K // 32).any()
+    else:
+        assert np.array_equal(got[: rows * K // 32].reshape(rows, K // 32), sc)
+
+
 @pytest.mark.parametrize("N,K", [(72, 256), (4096, 4096), (12288, 4096), (64, 12288)])
 @pytest.mark.parametrize("kind", ["normal", "edge"])
 def test_int4_g128(q, orc, N, K, kind):

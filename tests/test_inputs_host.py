@@ -57,6 +57,8 @@ def test_next_rows_reuse_the_workload_shapes():
         assert sorted((lin.K, lin.N, lin.M) for lin in lins[g]) == sorted(
             (K, N, 4096) for (K, N) in inputs.FP8_MLP_SHAPES)
     assert [(lin.M, lin.K, lin.N) for lin in lins["fp8_tensor_fused"]] == [(128, 1024, 1024)]
+    assert sorted((lin.K, lin.N, lin.M) for lin in lins["mxfp4_dual"]) == sorted(
+        (K, N, 20280) for (K, N) in inputs.MXFP8_SHAPES)
     assert sorted((lin.K, lin.N, lin.M) for lin in lins["w4a16_sym"]) == sorted(
         (K, N, M) for (K, N) in inputs.W4A16_SHAPES for M in (1, 16))
 
