@@ -243,6 +243,15 @@ class Job:
         return (lin.M * lin.K * 2 + q.qlin_codes_bytes(self.xf, lin.M, lin.K)
                 + q.qlin_scales_bytes(self.xf, self.layout, lin.M, lin.K) + q.qlin_global_bytes(self.xf, lin.M, lin.K))
 
+    def second_read_bytes(self, op) -> int:
+        """Bytes the per-tensor formats read once more: their tensor amax is a
+        pass of its own before any code exists (the two-pass floor)."""
+        F = self.q.Fmt
+        fmt = self.wf if op == "quant_w" else self.xf
+        if fmt not in (F.FP8_TENSOR, F.NVFP4) or (op == "quant_x" and self.xb is None):
+            return 0
+        return (self.lin.N if op == "quant_w" else self.lin.M) * self.lin.K * 2
+
     def gemm_bytes(self) -> int:
         """Algorithmic HBM bytes of the GEMM: operands once + output once."""
         lin, q = self.lin, self.q
@@ -528,10 +537,11 @@ def cold_rows(jobs, dev, hbm_peak, iters=20, warm=3):
     for j, op, ms in meas:
         name = kernel_name(j, op)
         nbytes = j.gemm_bytes() if op == "gemm" else (j.bytes_w_quant() if op == "quant_w" else j.bytes_x_quant())
-        r = rows.setdefault(name, {"calls": 0, "ms": 0.0, "bytes": 0})
+        r = rows.setdefault(name, {"calls": 0, "ms": 0.0, "bytes": 0, "floor": 0})
         r["calls"] += 1
         r["ms"] += ms
         r["bytes"] += nbytes
+        r["floor"] += nbytes + (0 if op == "gemm" else j.second_read_bytes(op))
         if op == "gemm":
             w4.append({"M": j.lin.M, "K": j.lin.K, "N": j.lin.N, "us": round(ms * 1e3, 2),
                        "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1),
@@ -541,6 +551,9 @@ def cold_rows(jobs, dev, hbm_peak, iters=20, warm=3):
         gbs = r["bytes"] / (r["ms"] * 1e-3) / 1e9
         out[name] = {"calls": r["calls"], "ms_sum_of_medians": round(r["ms"], 4), "gbs": round(gbs, 1),
                      "hbm_frac": round(gbs / hbm_peak, 3)}
+        if r["floor"] > r["bytes"]:
+            # two passes over the input: the fraction of the two-pass floor (input read twice)
+            out[name]["hbm_frac_two_pass_floor"] = round(r["floor"] / (r["ms"] * 1e-3) / 1e9 / hbm_peak, 3)
     return {"rows": out, "w4a16_calls": w4,
             "method": (f"each call alone, after reading a 512 MiB buffer (L2 about 126 MB); median of {iters} "
                        f"calls after {warm}")}

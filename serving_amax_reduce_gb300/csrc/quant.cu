@@ -84,34 +84,57 @@ __device__ __forceinline__ float e4m3_value(uint32_t code) {
     return f;
 }
 
+// Four fp32 -> four E4M3 codes in one word (a, b in the low half, lo first).
+__device__ __forceinline__ uint32_t cvt_e4m3x4(float a, float b, float c, float d) {
+    uint32_t r;
+    asm("{\n\t.reg .b16 t0, t1;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 t0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 t1, %4, %3;\n\t"
+        "mov.b32 %0, {t0, t1};\n}"
+        : "=r"(r)
+        : "f"(a), "f"(b), "f"(c), "f"(d));
+    return r;
+}
+
 // 8 bf16 (one 16-byte vector) times r -> 8 E4M3 codes.
 __device__ __forceinline__ uint2 enc8_e4m3(const uint4& v, float r) {
-    uint32_t c0 = cvt_e4m3x2(__fmul_rn(bf16_lo(v.x), r), __fmul_rn(bf16_hi(v.x), r));
-    uint32_t c1 = cvt_e4m3x2(__fmul_rn(bf16_lo(v.y), r), __fmul_rn(bf16_hi(v.y), r));
-    uint32_t c2 = cvt_e4m3x2(__fmul_rn(bf16_lo(v.z), r), __fmul_rn(bf16_hi(v.z), r));
-    uint32_t c3 = cvt_e4m3x2(__fmul_rn(bf16_lo(v.w), r), __fmul_rn(bf16_hi(v.w), r));
-    return make_uint2(c0 | (c1 << 16), c2 | (c3 << 16));
+    return make_uint2(cvt_e4m3x4(__fmul_rn(bf16_lo(v.x), r), __fmul_rn(bf16_hi(v.x), r), __fmul_rn(bf16_lo(v.y), r),
+                                 __fmul_rn(bf16_hi(v.y), r)),
+                      cvt_e4m3x4(__fmul_rn(bf16_lo(v.z), r), __fmul_rn(bf16_hi(v.z), r), __fmul_rn(bf16_lo(v.w), r),
+                                 __fmul_rn(bf16_hi(v.w), r)));
+}
+
+// Eight fp32 (pairs lo, hi in each of the four slots) -> eight E2M1 codes
+// in one word, pair i in byte i (lo in its low nibble): four conversions into
+// byte registers, packed by one vector move.
+__device__ __forceinline__ uint32_t cvt_e2m1x8(float l0, float h0, float l1, float h1, float l2, float h2, float l3,
+                                               float h3) {
+    uint32_t r;
+    asm("{\n\t.reg .b8 t0, t1, t2, t3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 t0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 t1, %4, %3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 t2, %6, %5;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 t3, %8, %7;\n\t"
+        "mov.b32 %0, {t0, t1, t2, t3};\n}"
+        : "=r"(r)
+        : "f"(l0), "f"(h0), "f"(l1), "f"(h1), "f"(l2), "f"(h2), "f"(l3), "f"(h3));
+    return r;
 }
 
 // 8 bf16 times r -> 8 E2M1 codes packed in 4 bytes.
 __device__ __forceinline__ uint32_t enc8_e2m1(const uint4& v, float r) {
-    uint32_t b0 = cvt_e2m1x2(__fmul_rn(bf16_lo(v.x), r), __fmul_rn(bf16_hi(v.x), r));
-    uint32_t b1 = cvt_e2m1x2(__fmul_rn(bf16_lo(v.y), r), __fmul_rn(bf16_hi(v.y), r));
-    uint32_t b2 = cvt_e2m1x2(__fmul_rn(bf16_lo(v.z), r), __fmul_rn(bf16_hi(v.z), r));
-    uint32_t b3 = cvt_e2m1x2(__fmul_rn(bf16_lo(v.w), r), __fmul_rn(bf16_hi(v.w), r));
-    return b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
+    return cvt_e2m1x8(__fmul_rn(bf16_lo(v.x), r), __fmul_rn(bf16_hi(v.x), r), __fmul_rn(bf16_lo(v.y), r),
+                      __fmul_rn(bf16_hi(v.y), r), __fmul_rn(bf16_lo(v.z), r), __fmul_rn(bf16_hi(v.z), r),
+                      __fmul_rn(bf16_lo(v.w), r), __fmul_rn(bf16_hi(v.w), r));
 }
 
 // 8 bf16 times r (rounded), then times the power of two m (exact) -> 8
 // E2M1 codes packed in 4 bytes: the two steps of the dual-scale rule.
 __device__ __forceinline__ uint32_t enc8_e2m1_2(const uint4& v, float r, float m) {
-    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
-    uint32_t out = 0;
-#pragma unroll
-    for (int i = 0; i < 4; i++)
-        out |= cvt_e2m1x2(__fmul_rn(__fmul_rn(bf16_lo(u[i]), r), m), __fmul_rn(__fmul_rn(bf16_hi(u[i]), r), m))
-               << (8 * i);
-    return out;
+    return cvt_e2m1x8(__fmul_rn(__fmul_rn(bf16_lo(v.x), r), m), __fmul_rn(__fmul_rn(bf16_hi(v.x), r), m),
+                      __fmul_rn(__fmul_rn(bf16_lo(v.y), r), m), __fmul_rn(__fmul_rn(bf16_hi(v.y), r), m),
+                      __fmul_rn(__fmul_rn(bf16_lo(v.z), r), m), __fmul_rn(__fmul_rn(bf16_hi(v.z), r), m),
+                      __fmul_rn(__fmul_rn(bf16_lo(v.w), r), m), __fmul_rn(__fmul_rn(bf16_hi(v.w), r), m));
 }
 
 __device__ __forceinline__ float warp_max(float v) {
@@ -187,6 +210,17 @@ __device__ __forceinline__ int64_t mma_scale_offset(int64_t row, int64_t j, int6
     const int64_t tile = row >> 7, rr = row & 127;
     return ((tile * chunks_per_row + (j >> 2)) << 9) + ((rr & 31) << 4) + ((rr >> 5) << 2) + (j & 3);
 }
+
+// The same split into a per-row base and a per-scale part, so that a warp
+// working on one row computes the 64-bit base once: offset(row, j) =
+// scale_row_base(row) + scale_col_part(j) for either layout (gs = scales per
+// row in the canonical layout, chunks = 4-scale chunks per row in the tiling).
+__device__ __forceinline__ int64_t scale_row_base(int64_t row, int64_t gs, int64_t chunks, int mma) {
+    if (!mma) return row * gs;
+    const int64_t rr = row & 127;
+    return (((row >> 7) * chunks) << 9) + ((rr & 31) << 4) + ((rr >> 5) << 2);
+}
+__device__ __forceinline__ int scale_col_part(int j, int mma) { return mma ? (((j >> 2) << 9) + (j & 3)) : j; }
 
 // ---------------------------------------------------------------- row tasks
 // The element-wise formats walk "tasks": 32 consecutive 16-byte vectors
@@ -431,8 +465,8 @@ __global__ void __launch_bounds__(256) k_mx(const uint16_t* __restrict__ x, int 
         const int c = c0 + 32 * u;
         v[u] = (live && c < nvr) ? ld16(src + 8 * c) : make_uint4(0, 0, 0, 0);
     }
-    const int64_t chunks = K >> 7;
     uint8_t* crow = codes + (int64_t)row * (FP4 ? (K >> 1) : K);
+    uint8_t* srow = scales + scale_row_base(row, K >> 5, K >> 7, mma);
 #pragma unroll
     for (int u = 0; u < kChunkU; u++) {
         const int c = c0 + 32 * u;
@@ -449,11 +483,7 @@ __global__ void __launch_bounds__(256) k_mx(const uint16_t* __restrict__ x, int 
             if (FP4) reinterpret_cast<uint32_t*>(crow)[c] = enc8_e2m1(v[u], mult);
             else reinterpret_cast<uint2*>(crow)[c] = enc8_e4m3(v[u], mult);
         }
-        if ((c & 3) == 0) {
-            const int64_t j = c >> 2;
-            const int64_t off = mma ? mma_scale_offset(row, j, chunks) : (int64_t)row * (K >> 5) + j;
-            scales[off] = (uint8_t)(e + 127);
-        }
+        if ((c & 3) == 0) srow[scale_col_part(c >> 2, mma)] = (uint8_t)(e + 127);
     }
 }
 
@@ -479,8 +509,8 @@ __global__ void __launch_bounds__(256) k_mx_dual(const uint16_t* __restrict__ x,
         const int c = c0 + 32 * u;
         v[u] = (live && c < nvr) ? ld16(src + 8 * c) : make_uint4(0, 0, 0, 0);
     }
-    const int64_t chunks = K >> 7;
     uint32_t* crow = reinterpret_cast<uint32_t*>(codes + (int64_t)row * (K >> 1));
+    uint8_t* srow = scales + scale_row_base(row, K >> 5, K >> 7, mma);
 #pragma unroll
     for (int blk = 0; blk < 2; blk++) {
         const float A = warp_max(fmaxf(absmax8_bf16x2(v[2 * blk]), absmax8_bf16x2(v[2 * blk + 1])));
@@ -504,11 +534,7 @@ __global__ void __launch_bounds__(256) k_mx_dual(const uint16_t* __restrict__ x,
             e = min(e, 127);
             const float mult = __uint_as_float((uint32_t)(127 - e) << 23);   // 2^-e, e <= 126 here
             if (live) crow[c] = enc8_e2m1_2(v[u], rc, mult);
-            if ((c & 3) == 0) {
-                const int64_t j = c >> 2;
-                const int64_t off = mma ? mma_scale_offset(row, j, chunks) : (int64_t)row * (K >> 5) + j;
-                scales[off] = (uint8_t)(e + 127);
-            }
+            if ((c & 3) == 0) srow[scale_col_part(c >> 2, mma)] = (uint8_t)(e + 127);
         }
     }
 }
@@ -542,7 +568,6 @@ __global__ void __launch_bounds__(256) k_nvfp4_encode(const uint16_t* __restrict
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int nvr = K >> 3, nch = (nvr + kChunk - 1) / kChunk;
     const uint32_t ids = (uint32_t)((rows_pad + 7) / 8) * (uint32_t)nch;
-    const int64_t chunks = K >> 6;
     for (uint32_t id = blockIdx.x; id < ids; id += gridDim.x) {
         const uint32_t rb = id / (uint32_t)nch;
         const int row = (int)rb * 8 + warp;
@@ -557,6 +582,7 @@ __global__ void __launch_bounds__(256) k_nvfp4_encode(const uint16_t* __restrict
             v[u] = (live && c < nvr) ? ld16(src + 8 * c) : make_uint4(0, 0, 0, 0);
         }
         uint32_t* crow = reinterpret_cast<uint32_t*>(codes + (int64_t)row * (K >> 1));
+        uint8_t* srow = scales + scale_row_base(row, K >> 4, K >> 6, mma);
 #pragma unroll
         for (int u = 0; u < kChunkU; u++) {
             const int c = c0 + 32 * u;
@@ -565,11 +591,7 @@ __global__ void __launch_bounds__(256) k_nvfp4_encode(const uint16_t* __restrict
             if (c >= nvr) continue;
             const uint32_t sb = cvt_e4m3x2(__fmul_rn(b, qm), 0.0f) & 0xFFu;   // non-negative: UE4M3
             if (live) crow[c] = enc8_e2m1(v[u], rb_of[sb]);
-            if ((c & 1) == 0) {
-                const int64_t j = c >> 1;
-                const int64_t off = mma ? mma_scale_offset(row, j, chunks) : (int64_t)row * (K >> 4) + j;
-                scales[off] = (uint8_t)sb;
-            }
+            if ((c & 1) == 0) srow[scale_col_part(c >> 1, mma)] = (uint8_t)sb;
         }
     }
 }
@@ -666,8 +688,8 @@ int sm_count() {
 
 // Grid of the per-tensor task walks (8 warps per CTA, kUnroll tasks per warp
 // per round): the FP8 per-tensor encode pass begins by folding the partial
-// maxima, so it stays persistent with 8 CTAs per SM and that prologue runs
-// once per resident CTA.  Tasks of one tensor, or -1 when their count does
+// maxima, so it stays persistent with one resident wave of CTAs and that
+// prologue runs once per resident CTA.  Tasks of one tensor, or -1 when their count does
 // not fit the 32-bit walk.
 int64_t task_count(int64_t rows, int64_t K) {
     const int64_t t = rows * (((K >> 3) + 31) / 32);
@@ -676,9 +698,25 @@ int64_t task_count(int64_t rows, int64_t K) {
 
 int64_t task_rounds(int64_t tasks) { return (tasks + 8 * kUnroll - 1) / (8 * kUnroll); }
 
-int task_grid_persistent(int64_t tasks) {
+// CTAs of a kernel that fit on one SM at once (256 threads, no dynamic shared
+// memory), asked of the runtime once per kernel; a persistent grid larger
+// than one resident wave would leave its last CTAs to start late.
+template <typename Kern>
+int resident_ctas(Kern k, int& cache) {
+    if (!cache) {
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, 256, 0) != cudaSuccess || n < 1) {
+            (void)cudaGetLastError();
+            n = 4;
+        }
+        cache = n;
+    }
+    return cache;
+}
+
+int task_grid_persistent(int64_t tasks, int per_sm) {
     int64_t b = task_rounds(tasks);
-    const int64_t cap = (int64_t)sm_count() * 8;
+    const int64_t cap = (int64_t)sm_count() * per_sm;
     if (b > cap) b = cap;
     return (int)(b < 1 ? 1 : b);
 }
@@ -742,7 +780,9 @@ cudaError_t launch_fp8_tensor(const uint16_t* x, int64_t rows, int64_t K, int64_
     const int64_t tasks = task_count(rows, K);
     if (tasks < 0) return cudaErrorInvalidValue;
     k_amax_partial<<<nparts, 256, 0, st>>>(x, rows, K, ld, partials);
-    k_fp8_tensor_encode<<<task_grid_persistent(tasks), 256, 0, st>>>(x, rows, K, ld, codes, scale, partials, nparts);
+    static int per_sm = 0;
+    k_fp8_tensor_encode<<<task_grid_persistent(tasks, resident_ctas(k_fp8_tensor_encode, per_sm)), 256, 0, st>>>(
+        x, rows, K, ld, codes, scale, partials, nparts);
     return cudaGetLastError();
 }
 
@@ -794,7 +834,8 @@ cudaError_t launch_nvfp4(const uint16_t* x, int64_t rows, int64_t K, int64_t ld,
     const int64_t rows_pad = mma_layout ? (rows + 127) / 128 * 128 : rows;
     const dim3 g = chunk_grid(rows_pad, K);
     const int64_t ids = (int64_t)g.x * g.y;
-    int64_t grid = (int64_t)sm_count() * 8;
+    static int per_sm = 0;       // one resident wave of the persistent encode pass
+    int64_t grid = (int64_t)sm_count() * resident_ctas(k_nvfp4_encode, per_sm);
     if (grid > ids) grid = ids;
     k_amax_partial<<<nparts, 256, 0, st>>>(x, rows, K, ld, partials);
     k_nvfp4_encode<<<(unsigned)grid, 256, 0, st>>>(x, (int)rows, (int)rows_pad, (int)K, ld, codes, scales, global,
