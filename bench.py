@@ -749,6 +749,53 @@ def cpu_baseline():
             "seconds": round(secs, 2), "host": host_cpu()}
 
 
+CPU_ALL_SECONDS = 12.0        # wall time of the all-core oracle leg
+
+
+def _oracle_worker(args):
+    """One process of the all-core oracle leg: its own copy of the sample, BLAS
+    on one thread, passes until `seconds` of wall time after the common start."""
+    rows_x, rows_w, seconds, barrier = args
+    import oracle
+    try:
+        from threadpoolctl import threadpool_limits
+        threadpool_limits(1)
+    except Exception:
+        pass
+    sample = oracle_sample_inputs(rows_x, rows_w)
+    oracle_sample_pass(sample)                      # warm: loads the library, touches the inputs
+    barrier.wait()
+    t0 = time.perf_counter()
+    flops = passes = 0
+    while time.perf_counter() - t0 < seconds:
+        f, _ = oracle_sample_pass(sample)
+        flops += f
+        passes += 1
+    return flops, passes, time.perf_counter() - t0
+
+
+def cpu_baseline_all_cores(procs=None, seconds=CPU_ALL_SECONDS):
+    """The same oracle passes on every host core: one process per core (spawned,
+    never forked from a process that has used the GPU), each with one BLAS
+    thread and its own copy of the sample; throughput = all their flops over the
+    longest process's wall time."""
+    import multiprocessing as mp
+    import oracle
+    oracle.build()
+    procs = procs or os.cpu_count() or 1
+    ctx = mp.get_context("spawn")
+    with ctx.Manager() as mgr:
+        barrier = mgr.Barrier(procs)
+        with ctx.Pool(procs) as pool:
+            res = pool.map(_oracle_worker, [(SAMPLE_CPU[0], SAMPLE_CPU[1], seconds, barrier)] * procs)
+    flops = sum(r[0] for r in res)
+    wall = max(r[2] for r in res)
+    return {"value": round(flops / wall / 1e12, 6), "unit": "TFLOP/s", "cores": procs,
+            "sample": (f"{procs} processes x one BLAS thread, each {min(r[1] for r in res)}-{max(r[1] for r in res)} "
+                       f"passes of the same sample in {wall:.1f} s"),
+            "seconds": round(wall, 2)}
+
+
 def run_reference(args, rank, world):
     import oracle
     oracle.build()
@@ -792,6 +839,7 @@ def main():
     res, _ = run_native(args, rank, world, local_rank)
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.next:
         res["cpu_baseline"] = cpu_baseline()
+        res["cpu_baseline"]["all_cores"] = cpu_baseline_all_cores()
     if args.rows_json and rank == 0:
         json.dump(res, open(args.rows_json, "w"), indent=1)
     if rank == 0:
