@@ -120,7 +120,9 @@ def config_block(args):
                               "(12288,4096)}",
                               "mxfp4 dual-scale W4A4 M20280 (K,N){(5120,13824),(13824,5120),(5120,5120)}"],
                 "step": "per linear: weight quantize + activation quantize + quantized GEMM",
-                "l2": "inputs larger than L2", "parallelism": f"replicas x{args.gpus}"}
+                "l2": ("step: bf16 inputs larger than L2 between reuses; each GEMM reads the codes its quantizer "
+                       "has just written, as in serving; HBM-bound rows also timed call by call after an L2 flush "
+                       "(rows.*.cold)"), "parallelism": f"replicas x{args.gpus}"}
     return {
         "workload": WORKLOAD,
         "workloads": ["fp8_tensor M128 K1024 N1024",
@@ -129,8 +131,9 @@ def config_block(args):
                       "mxfp8 M20280 (K,N){(5120,13824),(13824,5120),(5120,5120)}",
                       "mixed M32768: 4x nvfp4 3072x3072 + 4x fp8_block (3072<->12288)"],
         "step": "per linear: weight quantize + activation quantize + quantized GEMM",
-        "l2": ("step: inputs larger than L2 (each step streams several GB through the 126 MB L2 between "
-               "reuses); HBM-bound rows also timed call by call after an L2 flush (rows.*.cold)"),
+        "l2": ("step: bf16 inputs larger than L2 between reuses (each step streams several GB through the "
+               "126 MB L2); each GEMM reads the codes its quantizer has just written, as in serving; HBM-bound "
+               "rows also timed call by call after an L2 flush (rows.*.cold)"),
         "parallelism": f"replicas x{args.gpus}",
     }
 
@@ -503,7 +506,7 @@ def run_native(args, rank, world, local_rank):
     return res, jobs
 
 
-def cold_rows(jobs, dev, hbm_peak, iters=20, warm=3):
+def cold_rows(jobs, dev, hbm_peak, iters=20, warm=10):
     """Each HBM-bound call (every quantizer, the W4A16 GEMMs) timed alone with
     a cold L2: before every timed call a 512 MiB buffer (over 4x the L2) is
     read through, which leaves only its own clean lines in L2.  CUDA events
