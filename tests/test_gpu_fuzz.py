@@ -101,6 +101,30 @@ def test_gemm_random_shapes(q, orc, kind, i):
     GEMMS[kind](q, orc, M, N, K)
 
 
+# Pairs whose kernels take any N (the W scales of the tensor-core tiling are padded to 128 rows,
+# Y is stored by TMA with its columns clipped at N): N is drawn freely, Y then needs a padded
+# leading dimension for its 16-byte rows, as a caller with such N would pass it.
+RAGGED_N = ["fp8_tensor", "mxfp8", "mxfp4", "mxfp4_dual", "nvfp4", "int8", "fp8_tensor_fused_x"]
+
+
+@pytest.mark.parametrize("i", range(3))
+@pytest.mark.parametrize("kind", RAGGED_N)
+def test_gemm_random_shapes_any_n(q, orc, kind, i, monkeypatch):
+    M, _, K = draw(kind, 3571 * i + sum(map(ord, kind)))
+    N = int(np.random.default_rng(9001 * i + len(kind)).integers(1, 1031))
+    orig = q.gemm
+
+    def gemm_padded_y(*args, **kw):
+        if kw.get("y") is None:
+            m, n = args[2], args[3]
+            ld = (n + 7) // 8 * 8 + 8
+            kw["y"] = torch.full((m, ld), float("nan"), dtype=torch.bfloat16, device="cuda")[:, :n]
+        return orig(*args, **kw)
+
+    monkeypatch.setattr(q, "gemm", gemm_padded_y)
+    GEMMS[kind](q, orc, M, N, K)
+
+
 QUANTS = {
     "q_row": lambda q, orc, rows, K, i: (Qt.test_fp8_token(q, orc, rows, K, "outlier"),
                                          Qt.test_int8_row(q, orc, rows, K, "outlier", i % 2 == 1)),
