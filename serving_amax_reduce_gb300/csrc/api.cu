@@ -33,7 +33,7 @@ qlin_status launch_status(cudaError_t e) {
 qlin_status check_quant_shape(qlin_format fmt, qlin_scale_layout layout, int64_t rows, int64_t K) {
     if (rows < 1 || K < 8 || (K & 7) || rows > 0x7FFFFFFFll || K > 0x7FFFFFFFll) return QLIN_ERR_INVALID_ARG;
     if (layout != QLIN_SCALE_CANONICAL && layout != QLIN_SCALE_MMA) return QLIN_ERR_INVALID_ARG;
-    // the element-wise walks number their 256-element row tasks in 32 bits
+    // the tensor-amax walks number their 256-element row tasks in 32 bits
     const int64_t rows_pad = layout == QLIN_SCALE_MMA ? ceil_div(rows, 128) * 128 : rows;
     if (rows_pad * ceil_div(K, 256) > 0x7FFFFFFFll) return QLIN_ERR_INVALID_ARG;
     if (layout == QLIN_SCALE_MMA && fmt != QLIN_MXFP8 && fmt != QLIN_MXFP4 && fmt != QLIN_NVFP4 &&

@@ -223,9 +223,10 @@ __device__ __forceinline__ int64_t scale_row_base(int64_t row, int64_t gs, int64
 __device__ __forceinline__ int scale_col_part(int j, int mma) { return mma ? (((j >> 2) << 9) + (j & 3)) : j; }
 
 // ---------------------------------------------------------------- row tasks
-// The element-wise formats walk "tasks": 32 consecutive 16-byte vectors
-// (256 elements) of one row, one task per warp and one vector per lane, so
-// each row is read in 512-byte coalesced segments.  A warp keeps kUnroll tasks
+// The tensor-amax passes (per-tensor FP8, the NVFP4 global scale) walk
+// "tasks": 32 consecutive 16-byte vectors (256 elements) of one row, one task
+// per warp and one vector per lane, so each row is read in 512-byte coalesced
+// segments.  A warp keeps kUnroll tasks
 // in flight; row and column come from one 32-bit division per task.  The
 // task count fits in 32 bits for any tensor that fits in device memory (the
 // host checks).
