@@ -272,10 +272,10 @@ class Job:
 # differs from the code the counters came from.
 MEASURED_TRAFFIC = {
     "gemm_fp8_block": {
-        "dram_bytes": 78314240 + 57053952,
+        "dram_bytes": 79111424 + 57217536,
         "alg_bytes": 4096 * 3072 + 4096 * 4 + 12288 * 3072 + 96 * 24 * 4 + 4096 * 12288 * 2,
         "source": "serving_amax_reduce_gb300/csrc/gemm_tc.cu",
-        "code_sha256": "94df25cd32d726672027b2e4f9887380803dd05cacb4249e5c5460152f3a44df",
+        "code_sha256": "ebd934a7683c28caf72361b589f8d86b869f76bf665250e200083087fc3b87f3",
         "captured": "M4096 K3072 N12288 (one bench launch)",
     },
 }

@@ -37,8 +37,10 @@
  *     sets that kernel's shared-memory size on the device current at the
  *     time, and later calls skip the step.  A call on another device of the
  *     same process then fails to launch and returns QLIN_ERR_CUDA; nothing is
- *     written.  Make that first call on one thread; once each pair has run,
- *     calls from several host threads (on their own streams) are safe.
+ *     written.  Calls from several host threads at once, each on its own
+ *     stream and buffers, are safe, first calls included: the one-time
+ *     setups (device queries, driver entry-point lookups, kernel attributes)
+ *     are thread-safe and idempotent.
  *
  * Numeric rules (bit-exact; the pages name the formats but print no formula,
  * so these are the plainest readings of the public format definitions):

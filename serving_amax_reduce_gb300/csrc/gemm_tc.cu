@@ -60,6 +60,8 @@
 //                   accumulator at the end of the tile.  Codes, s_x and the MMA
 //                   sequence equal those of qlin_quantize_act + the per-tensor
 //                   GEMM, so Y is the same bits; one launch instead of three.
+#include <atomic>
+
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -947,28 +949,26 @@ __global__ void __launch_bounds__(Cfg<KIND>::THREADS, 1)
 
 // ---------------------------------------------------------------- host side
 int num_sms() {
-    static int n = 0;
-    if (!n) {
+    static const int n = [] {     // initialised once, thread-safe
         int dev = 0, v = 0;
         if (cudaGetDevice(&dev) == cudaSuccess &&
             cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
-            n = v;
-        else
-            n = kNumSMs;
-    }
+            return v;
+        return kNumSMs;
+    }();
     return n;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
+    static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {     // looked up once, thread-safe
         void* ptr = nullptr;
         cudaDriverEntryPointQueryResult q;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
                 cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-    }
+            return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+        return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+    }();
     return fn;
 }
 
@@ -1040,8 +1040,9 @@ cudaError_t launch_tc(const GemmArgs& a, cudaStream_t st) {
     p.status = a.dev_status;
     p.x_group = a.x_group128 ? 1 : 0;
     p.xb = static_cast<const uint16_t*>(a.x);
-    static bool attr_set = false;
-    if (!attr_set) {
+    // Several threads may run this setup at once; it is idempotent.
+    static std::atomic<bool> attr_set{false};
+    if (!attr_set.load(std::memory_order_acquire)) {
         // The in-kernel setmaxnreg split assumes the launch allocation of
         // REGS_LAUNCH registers per thread; refuse to launch otherwise.
         cudaFuncAttributes fa;
@@ -1050,7 +1051,7 @@ cudaError_t launch_tc(const GemmArgs& a, cudaStream_t st) {
         if (fa.numRegs != C::REGS_LAUNCH) return cudaErrorInvalidConfiguration;
         e = cudaFuncSetAttribute(k_gemm_tc<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
         if (e != cudaSuccess) return e;
-        attr_set = true;
+        attr_set.store(true, std::memory_order_release);
     }
     const int64_t ntiles = ((a.N + C::BN - 1) / C::BN) * ((a.M + BM - 1) / BM);
     const int grid = (int)(ntiles < num_sms() ? ntiles : num_sms());   // persistent: one CTA per SM

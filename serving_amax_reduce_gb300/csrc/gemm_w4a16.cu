@@ -34,6 +34,8 @@
 // Split-K: the CTAs of one thread-block cluster share an output tile and
 // each take a contiguous range of groups; their fp32 partial tiles are summed
 // through distributed shared memory, so the kernel needs no global scratch.
+#include <atomic>
+
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -662,15 +664,15 @@ __global__ void __launch_bounds__(256, 2) k_w4a16_mma(const W4MmaParams p) {
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
+    static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {     // looked up once, thread-safe
         void* ptr = nullptr;
         cudaDriverEntryPointQueryResult q;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
                 cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-    }
+            return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+        return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+    }();
     return fn;
 }
 
@@ -721,11 +723,12 @@ cudaError_t launch_mp(const GemmArgs& a, cudaStream_t st) {
     p.y = a.y;
     p.status = a.dev_status;
 
-    static bool attr_set = false;
-    if (!attr_set) {
+    // Several threads may run this setup at once; it is idempotent.
+    static std::atomic<bool> attr_set{false};
+    if (!attr_set.load(std::memory_order_acquire)) {
         cudaError_t e = cudaFuncSetAttribute(k_w4a16<MP>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
         if (e != cudaSuccess) return e;
-        attr_set = true;
+        attr_set.store(true, std::memory_order_release);
     }
     const int64_t ntiles = (a.N + 127) / 128, mtiles = (a.M + MP - 1) / MP;
     const int cs = pick_split(ntiles * mtiles, p.groups);
@@ -774,11 +777,12 @@ cudaError_t launch_w4a16_mma(const GemmArgs& a, cudaStream_t st) {
     p.y = a.y;
     const int64_t ntiles = (a.N + 127) / 128, mtiles = (a.M + 15) / 16;
     const int cs = pick_split_mma(ntiles * mtiles, p.groups);
-    static bool attr_set = false;
-    if (!attr_set) {
+    // Several threads may run this setup at once; it is idempotent.
+    static std::atomic<bool> attr_set{false};
+    if (!attr_set.load(std::memory_order_acquire)) {
         cudaError_t e = cudaFuncSetAttribute(k_w4a16_mma, cudaFuncAttributeMaxDynamicSharedMemorySize, kMmaSmem);
         if (e != cudaSuccess) return e;
-        attr_set = true;
+        attr_set.store(true, std::memory_order_release);
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)cs, (unsigned)ntiles, (unsigned)mtiles);

@@ -42,23 +42,26 @@ Cached g_partials[kMaxDevices] = {};
 unsigned long long current_context_id() {
     using GetCurrent = CUresult (*)(CUcontext*);
     using GetId = CUresult (*)(CUcontext, unsigned long long*);
-    static GetCurrent get_current = nullptr;
-    static GetId get_id = nullptr;
-    static bool looked_up = false;
-    if (!looked_up) {
+    struct Entry {
+        GetCurrent get_current = nullptr;
+        GetId get_id = nullptr;
+    };
+    static const Entry e = [] {     // looked up once, thread-safe
+        Entry r;
         void* p = nullptr;
         cudaDriverEntryPointQueryResult q;
         if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
-            get_current = reinterpret_cast<GetCurrent>(p);
+            r.get_current = reinterpret_cast<GetCurrent>(p);
         if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
-            get_id = reinterpret_cast<GetId>(p);
-        looked_up = true;
-    }
+            r.get_id = reinterpret_cast<GetId>(p);
+        return r;
+    }();
     CUcontext c = nullptr;
     unsigned long long id = 0;
-    if (!get_current || !get_id || get_current(&c) != CUDA_SUCCESS || !c || get_id(c, &id) != CUDA_SUCCESS) return 0;
+    if (!e.get_current || !e.get_id || e.get_current(&c) != CUDA_SUCCESS || !c || e.get_id(c, &id) != CUDA_SUCCESS)
+        return 0;
     return id;
 }
 

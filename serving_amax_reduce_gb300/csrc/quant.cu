@@ -22,6 +22,8 @@
 // (__fmul_rn, __fdiv_rn, __fsub_rn), this file is compiled with
 // -fmad=false -ftz=false -prec-div=true, and the E4M3/E2M1 conversions are
 // the hardware cvt.rn.satfinite instructions.
+#include <atomic>
+
 #include <cuda_bf16.h>
 
 #include "qlin_internal.h"
@@ -675,15 +677,13 @@ __global__ void __launch_bounds__(128) k_int4_g128(const uint16_t* __restrict__ 
 }
 
 int sm_count() {
-    static int n = 0;
-    if (!n) {
+    static const int n = [] {     // initialised once, thread-safe
         int dev = 0, v = 0;
         if (cudaGetDevice(&dev) == cudaSuccess &&
             cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
-            n = v;
-        else
-            n = kNumSMs;
-    }
+            return v;
+        return kNumSMs;
+    }();
     return n;
 }
 
@@ -703,16 +703,16 @@ int64_t task_rounds(int64_t tasks) { return (tasks + 8 * kUnroll - 1) / (8 * kUn
 // memory), asked of the runtime once per kernel; a persistent grid larger
 // than one resident wave would leave its last CTAs to start late.
 template <typename Kern>
-int resident_ctas(Kern k, int& cache) {
-    if (!cache) {
-        int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, 256, 0) != cudaSuccess || n < 1) {
+int resident_ctas(Kern k, std::atomic<int>& cache) {
+    int c = cache.load(std::memory_order_relaxed);
+    if (!c) {     // several threads may ask at once; they all get the same answer
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&c, k, 256, 0) != cudaSuccess || c < 1) {
             (void)cudaGetLastError();
-            n = 4;
+            c = 4;
         }
-        cache = n;
+        cache.store(c, std::memory_order_relaxed);
     }
-    return cache;
+    return c;
 }
 
 int task_grid_persistent(int64_t tasks, int per_sm) {
@@ -781,7 +781,7 @@ cudaError_t launch_fp8_tensor(const uint16_t* x, int64_t rows, int64_t K, int64_
     const int64_t tasks = task_count(rows, K);
     if (tasks < 0) return cudaErrorInvalidValue;
     k_amax_partial<<<nparts, 256, 0, st>>>(x, rows, K, ld, partials);
-    static int per_sm = 0;
+    static std::atomic<int> per_sm{0};
     k_fp8_tensor_encode<<<task_grid_persistent(tasks, resident_ctas(k_fp8_tensor_encode, per_sm)), 256, 0, st>>>(
         x, rows, K, ld, codes, scale, partials, nparts);
     return cudaGetLastError();
@@ -835,7 +835,7 @@ cudaError_t launch_nvfp4(const uint16_t* x, int64_t rows, int64_t K, int64_t ld,
     const int64_t rows_pad = mma_layout ? (rows + 127) / 128 * 128 : rows;
     const dim3 g = chunk_grid(rows_pad, K);
     const int64_t ids = (int64_t)g.x * g.y;
-    static int per_sm = 0;       // one resident wave of the persistent encode pass
+    static std::atomic<int> per_sm{0};       // one resident wave of the persistent encode pass
     int64_t grid = (int64_t)sm_count() * resident_ctas(k_nvfp4_encode, per_sm);
     if (grid > ids) grid = ids;
     k_amax_partial<<<nparts, 256, 0, st>>>(x, rows, K, ld, partials);

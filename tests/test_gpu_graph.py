@@ -7,7 +7,9 @@ GEMM alone when X stays bf16) into a graph on preallocated buffers.  Replaying
 the graph after new X values are copied into the same input buffer must give,
 bit for bit, what the eager calls give on those values (the kernels are
 deterministic), and differ from the first input's result.  The same calls on a
-side stream, ordered only by events, give the same bits again.
+side stream, ordered only by events, give the same bits again, and so do
+several host threads driving the library at once on their own streams, in a
+warm process and in a fresh one whose first calls all come from those threads.
 """
 import pytest
 import torch
@@ -110,3 +112,97 @@ def test_graph_replay_and_side_stream_match_eager(q, name, wname, xname, lname, 
     torch.cuda.synchronize()
     assert torch.equal(layer.y.view(torch.int16), y2.view(torch.int16)), "side-stream result differs"
     assert q.read_device_status() == 0
+
+
+
+def _threads_run(layers, reps):
+    """Every layer on its own host thread and stream, all released at once;
+    returns the exceptions the threads raised."""
+    import threading
+
+    start, errors = threading.Barrier(len(layers)), []
+
+    def work(layer):
+        try:
+            s = torch.cuda.Stream()
+            start.wait()
+            with torch.cuda.stream(s):
+                for _ in range(reps):
+                    layer.y.zero_()
+                    layer.run()
+            s.synchronize()
+        except Exception as e:       # reported by the caller, from the main thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=work, args=(lay,)) for lay in layers]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    torch.cuda.synchronize()
+    return errors
+
+
+# FP8 block x per-token twice (two threads on one kernel), NVFP4, W4A16 on tcgen05
+THREAD_CASES = [CASES[1], CASES[1], CASES[6], CASES[10]]
+
+
+def _thread_layers(q):
+    layers = []
+    for j, (_, wname, xname, lname, M, N, K) in enumerate(THREAD_CASES):
+        layer = Layer(q, wname, xname, lname, M, N, K)
+        layer.xin.copy_(inputs.normal_bf16((M, K), 1.0, 205 + j).to(DEV))
+        layers.append(layer)
+    return layers
+
+
+def test_host_threads_on_own_streams(q):
+    """Several host threads drive the library at once (ctypes releases the GIL
+    around each call), each on its own stream and buffers; every result equals
+    the one computed alone."""
+    layers = _thread_layers(q)
+    want = []
+    for layer in layers:
+        layer.run()
+        torch.cuda.synchronize()
+        want.append(layer.y.clone())
+    errors = _threads_run(layers, 20)
+    assert not errors, errors
+    for layer, y in zip(layers, want):
+        assert torch.equal(layer.y.view(torch.int16), y.view(torch.int16))
+    assert q.read_device_status() == 0
+
+
+_COLD_CHILD = """
+import sys, torch
+sys.path[:0] = [sys.argv[1], sys.argv[2]]
+import test_gpu_graph as T
+from gpu_util import require_gpu
+q = require_gpu()
+layers = T._thread_layers(q)
+errors = T._threads_run(layers, 3)          # the first call of every kernel happens here, on four threads
+assert not errors, errors
+got = [lay.y.clone() for lay in layers]
+for lay, y in zip(layers, got):
+    lay.y.zero_()
+    lay.run()
+    torch.cuda.synchronize()
+    assert torch.equal(lay.y.view(torch.int16), y.view(torch.int16)), "threaded first calls differ"
+assert q.read_device_status() == 0
+print("ok")
+"""
+
+
+def test_first_calls_from_several_threads(q):
+    """The library's one-time setups (device queries, the tensor-map encoder
+    lookup, kernel attributes) run on whichever thread calls first: in a fresh
+    process whose first calls all come from four threads at once, the results
+    equal the serial ones."""
+    import os
+    import subprocess
+    import sys
+
+    here = os.path.dirname(os.path.abspath(__file__))
+    r = subprocess.run([sys.executable, "-c", _COLD_CHILD, here, os.path.dirname(here)],
+                       capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout[-2000:] + r.stderr[-2000:]
