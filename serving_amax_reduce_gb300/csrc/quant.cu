@@ -416,7 +416,10 @@ constexpr int kChunk = 32 * kChunkU;           // vectors per warp chunk (1024 e
 
 // ---------------------------------------------------------------- 1 x 128 groups
 // Sixteen lanes own one 128-element group; the group amax comes from four
-// xor-shuffles inside the 16 lanes.  K % 128 == 0.
+// xor-shuffles inside the 16 lanes.  A half-warp holds kChunkU groups; lane
+// l works out the scale and multiplier (two divisions) of group l & 3 only,
+// and the others take them by shuffle.  K % 128 == 0.
+static_assert(kChunkU == 4, "one group per lane & 3");
 __global__ void __launch_bounds__(256) k_fp8_group128(const uint16_t* __restrict__ x, int rows, int K, int64_t ld,
                                                       uint8_t* __restrict__ codes, float* __restrict__ scales) {
     const int lane = threadIdx.x & 31;
@@ -430,17 +433,25 @@ __global__ void __launch_bounds__(256) k_fp8_group128(const uint16_t* __restrict
         const int c = c0 + 32 * u;
         v[u] = c < nvr ? ld16(src + 8 * c) : make_uint4(0, 0, 0, 0);
     }
+    float a[kChunkU];
+#pragma unroll
+    for (int u = 0; u < kChunkU; u++) {
+        a[u] = absmax8_bf16x2(v[u]);
+#pragma unroll
+        for (int o = 1; o < 16; o <<= 1) a[u] = fmaxf(a[u], __shfl_xor_sync(0xFFFFFFFFu, a[u], o));
+    }
+    const int mine = lane & 3;
+    const float am = mine == 0 ? a[0] : mine == 1 ? a[1] : mine == 2 ? a[2] : a[3];
+    float sc_m, r_m;
+    fp8_params(am, sc_m, r_m);
     uint2* dst = reinterpret_cast<uint2*>(codes + (int64_t)row * K);
     float* srow = scales + (int64_t)row * (K >> 7);
 #pragma unroll
     for (int u = 0; u < kChunkU; u++) {
         const int c = c0 + 32 * u;
-        float a = absmax8_bf16x2(v[u]);
-#pragma unroll
-        for (int o = 1; o < 16; o <<= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
+        const float r = __shfl_sync(0xFFFFFFFFu, r_m, (lane & 16) | u);
+        const float sc = __shfl_sync(0xFFFFFFFFu, sc_m, (lane & 16) | u);
         if (c >= nvr) continue;
-        float sc, r;
-        fp8_params(a, sc, r);
         dst[c] = enc8_e4m3(v[u], r);
         if ((c & 15) == 0) srow[c >> 4] = sc;
     }
