@@ -611,9 +611,22 @@ __global__ void __launch_bounds__(256) k_nvfp4_encode(const uint16_t* __restrict
 }
 
 // ---------------------------------------------------------------- int4 g128
-// One thread per output channel and 128-K group: it reads the group's 256
+// 16-byte global -> shared copy that bypasses the registers (zero-filled when
+// src_bytes is 0); completion through cp.async.wait_group, no spin.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
+                 "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+
+constexpr int kInt4Pitch = 272;   // bytes per staged row: 256 + 16, so 8 lanes reading 8 rows hit 8 bank groups
+
+// One thread per output channel and 128-K group: it takes the group's 256
 // contiguous bytes of its weight row (16 vectors), so min/max, the scale, the
 // zero point and the 16 packed words are all computed once, by one thread.
+// The CTA's 128 x 128 tile is first copied into shared memory with coalesced
+// 16-byte copies (a warp moves two 256-byte row segments per instruction)
+// instead of each lane loading from its own row.
 // A warp covers 32 consecutive channels, so each qweight row store (fixed
 // k-octet, consecutive n) and each scale store is coalesced; the zero points
 // of 8 channels are OR-ed into one word across 8 lanes.
@@ -624,13 +637,23 @@ template <bool SYM>
 __global__ void __launch_bounds__(128) k_int4_g128(const uint16_t* __restrict__ w, int64_t N, int64_t K,
                                                    int64_t ld, int32_t* __restrict__ qweight,
                                                    uint16_t* __restrict__ scales, int32_t* __restrict__ qzeros) {
+    __shared__ __align__(16) uint8_t tile[128 * kInt4Pitch];
     const int64_t nb = (N + 127) >> 7, g = (int64_t)blockIdx.x / nb, k0 = g * 128;
-    const int64_t n = ((int64_t)blockIdx.x - g * nb) * 128 + threadIdx.x;
+    const int64_t n0 = ((int64_t)blockIdx.x - g * nb) * 128, n = n0 + threadIdx.x;
     const int lane = threadIdx.x & 31;
     const bool valid = n < N;
+    // copy j of thread t: row 8 j + t / 16, 16-byte column t % 16 (rows past N zero-filled)
+#pragma unroll
+    for (int j = 0; j < 16; j++) {
+        const int r = 8 * j + (threadIdx.x >> 4), c = threadIdx.x & 15;
+        const bool in = n0 + r < N;
+        cp_async16(tile + r * kInt4Pitch + 16 * c, w + (in ? n0 + r : 0) * ld + k0 + 8 * c, in ? 16u : 0u);
+    }
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+    __syncthreads();
     uint4 v[16];
 #pragma unroll
-    for (int o = 0; o < 16; o++) v[o] = valid ? ld16(w + n * ld + k0 + 8 * o) : make_uint4(0, 0, 0, 0);
+    for (int o = 0; o < 16; o++) v[o] = *reinterpret_cast<const uint4*>(tile + threadIdx.x * kInt4Pitch + 16 * o);
     // min and max on bf16 pairs (exact), four independent chains of each,
     // then combined
     __nv_bfloat162 mn2[4], mx2[4];
