@@ -214,6 +214,20 @@ def test_block128_and_int4_grids_cover_their_tiles():
         assert len(pairs) == (K // 128) * N and set(pairs.values()) == {1}
 
 
+def test_int4_tile_staging_covers_the_tile_and_reads_without_bank_conflicts():
+    # k_int4_g128 copies: copy j of thread t -> row 8 j + t / 16, 16-byte column t % 16
+    seen = Counter((8 * j + t // 16, t % 16) for t in range(128) for j in range(16))
+    assert len(seen) == 128 * 16 and set(seen.values()) == {1}
+    pitch = 272                                   # kInt4Pitch
+    assert pitch % 16 == 0 and pitch >= 256
+    # thread t then reads row t at t * pitch + 16 o; a 16-byte shared load is served a quarter
+    # warp (8 lanes) at a time, and those 8 lanes must fall in 8 different groups of 4 banks
+    for o in range(16):
+        for q0 in range(0, 128, 8):
+            groups = {((t * pitch + 16 * o) // 4 % 32) // 4 for t in range(q0, q0 + 8)}
+            assert len(groups) == 8
+
+
 def mma_scale_offset(row, j, chunks):
     """quant.cu, mma_scale_offset: the QLIN_SCALE_MMA tiling."""
     tile, rr = row >> 7, row & 127
