@@ -40,7 +40,9 @@
  *     written.  Calls from several host threads at once, each on its own
  *     stream and buffers, are safe, first calls included: the one-time
  *     setups (device queries, driver entry-point lookups, kernel attributes)
- *     are thread-safe and idempotent.
+ *     are thread-safe and idempotent.  The exception is
+ *     qlin_quantize_fp8_tensor_noalloc, whose calls share one device array:
+ *     calls that overlap on the GPU must not be issued (see its entry).
  *
  * Numeric rules (bit-exact; the pages name the formats but print no formula,
  * so these are the plainest readings of the public format definitions):
