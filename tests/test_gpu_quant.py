@@ -314,6 +314,34 @@ def test_leading_dimension_is_honoured(q, orc):
         assert np.array_equal(np_u8(b["codes"]).reshape(96, 2048), codes)
 
 
+STRIDED = [  # format name, weight side, scale layout
+    ("FP8_TENSOR", False, "CANONICAL"), ("FP8_TOKEN", False, "CANONICAL"), ("FP8_GROUP128", False, "CANONICAL"),
+    ("INT8_ROW", False, "CANONICAL"), ("MXFP8", False, "MMA"), ("MXFP4", False, "MMA"), ("NVFP4", False, "MMA"),
+    ("MXFP4_DUAL", False, "MMA"), ("FP8_BLOCK128", True, "CANONICAL"), ("INT4_G128_ASYM", True, "CANONICAL"),
+    ("INT4_G128_SYM", True, "CANONICAL"), ("MXFP8", True, "CANONICAL"), ("NVFP4", True, "CANONICAL"),
+]
+
+
+@pytest.mark.parametrize("name,weight,lname", STRIDED, ids=[f"{n}-{'w' if w else 'x'}-{l}" for n, w, l in STRIDED])
+def test_every_quantizer_honours_the_leading_dimension(q, name, weight, lname):
+    """Every format, on a strided view (ld = 4096 > K = 2048, starting 1024 columns in) of a
+    tensor with a large-magnitude band outside the view: codes, scales, zero points and global
+    scales equal, bit for bit, those of the contiguous copy."""
+    big = inputs.outlier_channel_bf16(128, 4096, 7)
+    big[:, :1024] *= 1000                                  # outside the view; must not leak into its amax
+    view = big.cuda()[:, 1024:3072]
+    assert view.stride(0) == 4096 and not view.is_contiguous()
+    fn = q.quantize_weight if weight else q.quantize_act
+    fmt, lay = q.Fmt[name], q.Layout[lname]
+    a = fn(fmt, view, lay)
+    b = fn(fmt, view.contiguous(), lay)
+    torch.cuda.synchronize()
+    assert set(a) == set(b)
+    for key in ("codes", "scales", "zeros", "global"):     # the outputs (the workspace is scratch)
+        if a.get(key) is not None:
+            assert torch.equal(a[key].view(torch.uint8), b[key].view(torch.uint8)), key
+
+
 @pytest.mark.slow
 def test_full_size_activation_quantizers(q, orc):
     """The workloads' largest activations: MXFP8 X [20280, 13824] and NVFP4 X
