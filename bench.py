@@ -64,6 +64,9 @@ def parse_args():
                     help="measure the next rows instead (MXFP4 W4A4 on the MXFP8 workload's shapes, FP8 "
                          "1x128-group and INT8 W8A8 on the DiT MLP shapes, the per-tensor FP8 linear with "
                          "its activation quantization fused into the GEMM)")
+    ap.add_argument("--vendor", action="store_true",
+                    help="time the vendor library's own low-precision GEMMs (cuBLASLt through "
+                         "torch._scaled_mm) on the workloads' GEMM shapes, as context; prints one JSON line")
     return ap.parse_args()
 
 
@@ -828,8 +831,87 @@ def run_reference(args, rank, world):
             "e2e": {"value": round(v, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+# ---------------------------------------------------------------- vendor library, as context
+def run_vendor(iters: int = 20, warm: int = 5):
+    """cuBLASLt's GEMMs for the same formats and shapes, timed with CUDA events
+    on warm operands (inputs random, scales constant: only the time is kept).
+    Formats it does not support on this GPU are reported with the error."""
+    import torch
+    dev = "cuda"
+    f8, sm = torch.float8_e4m3fn, torch._scaled_mm
+    out = {}
+
+    def fp8_codes(rows, K):
+        return torch.randn(rows, K, device=dev).to(f8)
+
+    def swizzled_scales(rows, K, block, byte, dtype):
+        # one scale per `block` elements along K, in the 128-row x 4-scale tiling (sizes rounded up)
+        n = (rows + 127) // 128 * 128 * (((K // block) + 3) // 4 * 4)
+        return torch.full((n,), byte, dtype=torch.uint8, device=dev).view(dtype)
+
+    def fp8_tensor(M, N, K):
+        a, b, one = fp8_codes(M, K), fp8_codes(N, K), torch.tensor(1.0, device=dev)
+        return lambda: sm(a, b.t(), scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+
+    def fp8_block(M, N, K):      # 1 x 128 activation groups, 128 x 128 weight blocks
+        a, b = fp8_codes(M, K), fp8_codes(N, K)
+        sa = torch.ones(M, K // 128, device=dev).t().contiguous().t()     # [M, K/128], column-major
+        sb = torch.ones(N // 128, K // 128, device=dev).t()               # [K/128, N/128]
+        return lambda: sm(a, b.t(), scale_a=sa, scale_b=sb, out_dtype=torch.bfloat16)
+
+    def mxfp8(M, N, K):
+        a, b = fp8_codes(M, K), fp8_codes(N, K)
+        sa = swizzled_scales(M, K, 32, 127, torch.float8_e8m0fnu)
+        sb = swizzled_scales(N, K, 32, 127, torch.float8_e8m0fnu)
+        return lambda: sm(a, b.t(), scale_a=sa, scale_b=sb, out_dtype=torch.bfloat16)
+
+    def nvfp4(M, N, K):
+        a = torch.randint(0, 256, (M, K // 2), dtype=torch.uint8, device=dev).view(torch.float4_e2m1fn_x2)
+        b = torch.randint(0, 256, (N, K // 2), dtype=torch.uint8, device=dev).view(torch.float4_e2m1fn_x2)
+        sa, sb = swizzled_scales(M, K, 16, 0x38, f8), swizzled_scales(N, K, 16, 0x38, f8)
+        return lambda: sm(a, b.t(), scale_a=sa, scale_b=sb, out_dtype=torch.bfloat16)
+
+    def bf16(M, N, K):
+        a = torch.randn(M, K, device=dev).bfloat16()
+        b = torch.randn(N, K, device=dev).bfloat16()
+        return lambda: a @ b.t()
+
+    def case(name, M, N, K, make):
+        try:
+            fn = make(M, N, K)
+            for _ in range(warm):
+                fn()
+            torch.cuda.synchronize()
+            t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            t0.record()
+            for _ in range(iters):
+                fn()
+            t1.record()
+            torch.cuda.synchronize()
+            sec = t0.elapsed_time(t1) / iters * 1e-3
+            out[name] = {"us": round(sec * 1e6, 1), "tflops": round(2.0 * M * N * K / sec / 1e12, 1)}
+        except Exception as ex:      # unsupported format or layout on this GPU / library
+            out[name] = {"unsupported": (type(ex).__name__ + ": " + str(ex)).splitlines()[0][:200]}
+        torch.cuda.empty_cache()
+
+    for (M, K, N) in [(4096, 3072, 12288), (32768, 3072, 12288), (32768, 12288, 3072)]:
+        case(f"fp8_tensor_M{M}_K{K}_N{N}", M, N, K, fp8_tensor)
+        case(f"fp8_block_M{M}_K{K}_N{N}", M, N, K, fp8_block)
+    for (K, N) in [(5120, 13824), (13824, 5120), (5120, 5120)]:
+        case(f"mxfp8_M20280_K{K}_N{N}", 20280, N, K, mxfp8)
+    case("nvfp4_M32768_K3072_N3072", 32768, 3072, 3072, nvfp4)
+    case("fp8_tensor_M8192_K8192_N8192", 8192, 8192, 8192, fp8_tensor)
+    case("bf16_M8192_K8192_N8192", 8192, 8192, 8192, bf16)
+    return {"vendor_reference": out, "library": "cuBLASLt via torch._scaled_mm (torch " + torch.__version__ + ")",
+            "timing": f"CUDA events, mean of {iters} calls after {warm} warm-up calls, operands warm"}
+
+
 def main():
     args = parse_args()
+    if args.vendor:
+        if int(os.environ.get("RANK", 0)) == 0:
+            print(json.dumps(run_vendor()), flush=True)
+        return
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
     local_rank = int(os.environ.get("LOCAL_RANK", 0))
