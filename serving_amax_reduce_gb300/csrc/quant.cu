@@ -68,14 +68,6 @@ __device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
     return r;
 }
 
-// Two fp32 -> two E2M1 codes in one byte, `lo` in the low nibble.
-__device__ __forceinline__ uint32_t cvt_e2m1x2(float lo, float hi) {
-    uint32_t r;
-    asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u32.u8 %0, t;\n}"
-        : "=r"(r) : "f"(hi), "f"(lo));
-    return r;
-}
-
 // One E4M3 code -> its value (exact: every E4M3 value is an fp16 value).
 __device__ __forceinline__ float e4m3_value(uint32_t code) {
     uint32_t h2;
@@ -206,17 +198,13 @@ __device__ __forceinline__ uint2 enc8_row(const uint4& v, float r) {
     else return enc8_e4m3(v, r);
 }
 
-// Byte offset of scale (row, j) in the tensor-core tiling (see qlin.h):
-// 512-byte chunks of 128 rows x 4 scales, ordered [row_tile][chunk].
-__device__ __forceinline__ int64_t mma_scale_offset(int64_t row, int64_t j, int64_t chunks_per_row) {
-    const int64_t tile = row >> 7, rr = row & 127;
-    return ((tile * chunks_per_row + (j >> 2)) << 9) + ((rr & 31) << 4) + ((rr >> 5) << 2) + (j & 3);
-}
-
-// The same split into a per-row base and a per-scale part, so that a warp
-// working on one row computes the 64-bit base once: offset(row, j) =
-// scale_row_base(row) + scale_col_part(j) for either layout (gs = scales per
-// row in the canonical layout, chunks = 4-scale chunks per row in the tiling).
+// Byte offset of scale (row, j).  In the tensor-core tiling (see qlin.h),
+// 512-byte chunks of 128 rows x 4 scales ordered [row_tile][chunk]:
+//   ((row / 128 * chunks + j / 4) << 9) + (row % 32) * 16 + (row % 128 / 32) * 4 + j % 4;
+// in the canonical layout row * gs + j.  Split into a per-row base and a
+// per-scale part, so that a warp working on one row computes the 64-bit base
+// once: offset(row, j) = scale_row_base(row) + scale_col_part(j) (gs = scales
+// per row in the canonical layout, chunks = 4-scale chunks per row in the tiling).
 __device__ __forceinline__ int64_t scale_row_base(int64_t row, int64_t gs, int64_t chunks, int mma) {
     if (!mma) return row * gs;
     const int64_t rr = row & 127;

@@ -229,9 +229,10 @@ def test_int4_tile_staging_covers_the_tile_and_reads_without_bank_conflicts():
 
 
 def mma_scale_offset(row, j, chunks):
-    """quant.cu, mma_scale_offset: the QLIN_SCALE_MMA tiling."""
-    tile, rr = row >> 7, row & 127
-    return ((tile * chunks + (j >> 2)) << 9) + ((rr & 31) << 4) + ((rr >> 5) << 2) + (j & 3)
+    """quant.cu, scale_row_base(row) + scale_col_part(j) in the QLIN_SCALE_MMA tiling."""
+    rr = row & 127
+    base = (((row >> 7) * chunks) << 9) + ((rr & 31) << 4) + ((rr >> 5) << 2)
+    return base + (((j >> 2) << 9) + (j & 3))
 
 
 @pytest.mark.parametrize("rows,nsc", [(1, 4), (333, 16), (256, 40)])
