@@ -366,28 +366,40 @@ __global__ void __launch_bounds__(256) k_fp8_tensor_encode(const uint16_t* __res
     }
 }
 
+// 16-byte global -> shared copy that bypasses the registers (zero-filled when
+// src_bytes is 0); completion through cp.async.wait_group, no spin.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
+                 "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+
 // ---------------------------------------------------------------- 128x128 block
 // One CTA per 128x128 tile: 256 threads x 8 vectors; thread t covers rows
 // t/16 + 16i and the 16-byte column t%16 (256-byte coalesced row segments).
 __global__ void __launch_bounds__(256) k_fp8_block128(const uint16_t* __restrict__ x, int64_t K, int64_t ld,
                                                       uint8_t* __restrict__ codes, float* __restrict__ scales) {
+    // The tile waits in shared memory rather than in registers, so more CTAs (and
+    // more of their loads) fit on an SM.  Each thread reads back only the vectors
+    // it copied itself, so its own cp.async.wait_group is the only wait needed.
+    __shared__ __align__(16) uint4 tile[8][256];
     __shared__ float red[33];
     const int64_t kt = K >> 7, bi = (int64_t)blockIdx.x / kt, bj = (int64_t)blockIdx.x - bi * kt;
     const int r0 = threadIdx.x >> 4, cv = threadIdx.x & 15;
-    const uint16_t* src = x + (bi * 128 + r0) * ld + bj * 128 + cv * 8;
-    uint4 v[8];
+    const uint16_t* src = x + (bi * 128 + r0) * ld + bj * 128 + cv * 8;   // row r0 + 16 i for i = 0..7
+#pragma unroll
+    for (int i = 0; i < 8; i++) cp_async16(&tile[i][threadIdx.x], src + (int64_t)(16 * i) * ld, 16u);
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
     float amax = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 8; i++) {
-        v[i] = ld16(src + (int64_t)(16 * i) * ld);
-        amax = fmaxf(amax, absmax8(v[i]));
-    }
+    for (int i = 0; i < 8; i++) amax = fmaxf(amax, absmax8(tile[i][threadIdx.x]));
     amax = block_max<256>(amax, red);
     float s, r;
     fp8_params(amax, s, r);
     uint8_t* dst = codes + (bi * 128 + r0) * K + bj * 128 + cv * 8;
 #pragma unroll
-    for (int i = 0; i < 8; i++) *reinterpret_cast<uint2*>(dst + (int64_t)(16 * i) * K) = enc8_e4m3(v[i], r);
+    for (int i = 0; i < 8; i++)
+        *reinterpret_cast<uint2*>(dst + (int64_t)(16 * i) * K) = enc8_e4m3(tile[i][threadIdx.x], r);
     if (threadIdx.x == 0) scales[bi * (K >> 7) + bj] = s;
 }
 
@@ -599,14 +611,6 @@ __global__ void __launch_bounds__(256) k_nvfp4_encode(const uint16_t* __restrict
 }
 
 // ---------------------------------------------------------------- int4 g128
-// 16-byte global -> shared copy that bypasses the registers (zero-filled when
-// src_bytes is 0); completion through cp.async.wait_group, no spin.
-__device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t src_bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
-                 "l"(src), "r"(src_bytes)
-                 : "memory");
-}
-
 constexpr int kInt4Pitch = 272;   // bytes per staged row: 256 + 16, so 8 lanes reading 8 rows hit 8 bank groups
 
 // One thread per output channel and 128-K group: it takes the group's 256
