@@ -663,6 +663,179 @@ __global__ void __launch_bounds__(256, 2) k_w4a16_mma(const W4MmaParams p) {
     if (cs > 1) cluster_sync_all();
 }
 
+// M <= 8: the same ring and staging with the roles of the MMA operands swapped.
+// The weights are the A operand (16 channels per instruction, rows c4 and
+// c4 + 8 of two 16-channel m-tiles per warp) and the tokens the B operand (8
+// per instruction), so a 16-K step costs two MMAs per warp instead of four.
+// The K order is the one above: lane q's A values of a step are the pairs
+// (j, j + 4) and (j + 1, j + 5), j = 2 (q % 2), of octet q / 2, and its B values
+// the staged X positions 4q .. 4q + 3 of token c4 (one 8-byte read).
+__global__ void __launch_bounds__(256, 2) k_w4a16_mma8(const W4MmaParams p) {
+    extern __shared__ __align__(16) uint8_t smem_mma[];
+    uint16_t* xs = reinterpret_cast<uint16_t*>(smem_mma);                         // [2 buf][2 parity][16][kXRow]
+    float* red = reinterpret_cast<float*>(smem_mma + 2 * 2 * 16 * kXRow * 2);      // [16][128]
+    uint32_t* wsm = reinterpret_cast<uint32_t*>(smem_mma + 2 * 2 * 16 * kXRow * 2 + 16 * 128 * 4);  // [slot][16][kWRow]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
+    const int slice = warp & 3, par = warp >> 2, c4 = lane >> 2, q = lane & 3;
+    const int cs = (int)gridDim.x, rank = (int)cluster_ctarank();
+    const int n0 = (int)blockIdx.y * 128, m0 = 0;
+    const int g0 = rank * p.groups / cs, g1 = (rank + 1) * p.groups / cs;
+    const int npairs = (g1 - g0 + 1) / 2;
+    // this lane's 4 A-fragment channels (rows c4 and c4 + 8 of m-tiles 0 and 1), CTA-local
+    int chl[2][2];
+#pragma unroll
+    for (int mt = 0; mt < 2; mt++)
+#pragma unroll
+        for (int r = 0; r < 2; r++) chl[mt][r] = slice * 32 + mt * 16 + c4 + 8 * r;
+    const int sh0 = 8 * (q & 1);                         // pair (j, j + 4), j = 2 (q % 2)
+
+    // X of a pair of groups (16 rows x 16 octets each), two octets per thread
+    auto load_x = [&](int pr, uint4 (&xv)[2]) {
+#pragma unroll
+        for (int j = 0; j < 2; j++) {
+            const int idx = tid + 256 * j, pa = idx >> 8, row = (idx >> 4) & 15, oct = idx & 15;
+            const int g = g0 + 2 * pr + pa;
+            const bool in = g < g1 && m0 + row < p.M;
+            xv[j] = in ? __ldg(reinterpret_cast<const uint4*>(p.x + (int64_t)(m0 + row) * p.K + g * 128 + oct * 8))
+                       : make_uint4(0, 0, 0, 0);
+        }
+    };
+    auto store_x = [&](int buf, const uint4 (&xv)[2]) {
+#pragma unroll
+        for (int j = 0; j < 2; j++) {
+            const int idx = tid + 256 * j, pa = idx >> 8, row = (idx >> 4) & 15, oct = idx & 15;
+            *reinterpret_cast<uint4*>(xs + ((buf * 2 + pa) * 16 + row) * kXRow + oct * 8) = permute_x_chunk(xv[j]);
+        }
+    };
+    // weights of a pair of groups into ring slots: 2 x 16 octet rows x 32 chunks of 16 bytes
+    auto issue_w = [&](int pp) {
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+            const int c = tid + 256 * j, pa = c >> 9, row = (c >> 5) & 15, cc = c & 31;
+            const int g = g0 + 2 * pp + pa, slot = 2 * (pp % kWPairs) + pa;
+            const bool in = g < g1 && n0 + cc * 4 < p.N;
+            const int32_t* src = p.qweight + (int64_t)(in ? g * 16 + row : 0) * p.N + (in ? n0 + cc * 4 : 0);
+            cp_async16(wsm + (slot * 16 + row) * kWRow + cc * 4, src, in ? 16u : 0u);
+        }
+        cp_async_commit();
+    };
+
+    float acc[2][4];
+#pragma unroll
+    for (int t = 0; t < 2; t++)
+#pragma unroll
+        for (int i = 0; i < 4; i++) acc[t][i] = 0.0f;
+
+#pragma unroll
+    for (int pp = 0; pp < kWPairs; pp++) issue_w(pp);   // empty pairs still commit, keeping the count
+    uint4 xv[2];
+    load_x(0, xv);
+    store_x(0, xv);
+    if (npairs > 1) load_x(1, xv);
+    for (int pr = 0; pr < npairs; pr++) {
+        const int g = g0 + 2 * pr + par;
+        const int buf = pr & 1;
+        cp_async_wait<kWPairs - 1>();                     // this pair's weights have landed
+        __syncthreads();
+        // this group's zero points and scales for the lane's 4 A rows (channels)
+        __nv_bfloat162 zb[2][2];
+        float sc[2][2];
+        {
+            const bool gin = g < g1;
+#pragma unroll
+            for (int mt = 0; mt < 2; mt++)
+#pragma unroll
+                for (int r = 0; r < 2; r++) {
+                    const int ch = n0 + chl[mt][r];
+                    const bool ok = gin && ch < p.N;
+                    const uint32_t zw = ok ? (uint32_t)__ldg(p.qzeros + (int64_t)g * (p.N / 8) + ch / 8) : 0u;
+                    const uint16_t zbits = (uint16_t)(0x4300u | ((zw >> (4 * (ch & 7))) & 0xFu));
+                    zb[mt][r] = __halves2bfloat162(__ushort_as_bfloat16(zbits), __ushort_as_bfloat16(zbits));
+                    sc[mt][r] = ok ? __uint_as_float((uint32_t)__ldg(p.scales + (int64_t)g * p.N + ch) << 16) : 0.0f;
+                }
+        }
+        float cg[2][4];
+#pragma unroll
+        for (int t = 0; t < 2; t++)
+#pragma unroll
+            for (int i = 0; i < 4; i++) cg[t][i] = 0.0f;
+        const uint16_t* xr = xs + (buf * 2 + par) * 16 * kXRow;
+        const uint32_t* wr = wsm + (2 * (pr % kWPairs) + par) * 16 * kWRow;
+#pragma unroll
+        for (int st = 0; st < 8; st++) {
+            // B: token c4, the staged positions 4q .. 4q + 3 of this 16-K step
+            const uint2 bx = *reinterpret_cast<const uint2*>(xr + c4 * kXRow + 16 * st + 4 * q);
+            const uint32_t* wo = wr + (2 * st + (q >> 1)) * kWRow;
+#pragma unroll
+            for (int mt = 0; mt < 2; mt++) {
+                const uint32_t wa = wo[chl[mt][0]], wb = wo[chl[mt][1]];
+                const uint32_t a0 = dq_pair(wa, sh0, zb[mt][0]), a2 = dq_pair(wa, sh0 + 4, zb[mt][0]);
+                const uint32_t a1 = dq_pair(wb, sh0, zb[mt][1]), a3 = dq_pair(wb, sh0 + 4, zb[mt][1]);
+                mma_16816(cg[mt], a0, a1, a2, a3, bx.x, bx.y);
+            }
+        }
+        // C rows c4, c4 + 8 are channels chl[mt][0], chl[mt][1]; columns 2q, 2q + 1 are tokens
+#pragma unroll
+        for (int mt = 0; mt < 2; mt++) {
+            acc[mt][0] += cg[mt][0] * sc[mt][0];
+            acc[mt][1] += cg[mt][1] * sc[mt][0];
+            acc[mt][2] += cg[mt][2] * sc[mt][1];
+            acc[mt][3] += cg[mt][3] * sc[mt][1];
+        }
+        // stage the next pair's X (the buffer read two pairs ago is free since the barrier above)
+        if (pr + 1 < npairs) store_x(buf ^ 1, xv);
+        if (pr + 2 < npairs) load_x(pr + 2, xv);
+        __syncthreads();                                  // this pair's weight slots are free
+        issue_w(pr + kWPairs);
+    }
+    cp_async_wait<0>();
+
+    // the two group parities into one partial tile red[token][channel], tokens 2q and 2q + 1
+    if (par == 0) {
+#pragma unroll
+        for (int mt = 0; mt < 2; mt++) {
+            red[(2 * q) * 128 + chl[mt][0]] = acc[mt][0];
+            red[(2 * q + 1) * 128 + chl[mt][0]] = acc[mt][1];
+            red[(2 * q) * 128 + chl[mt][1]] = acc[mt][2];
+            red[(2 * q + 1) * 128 + chl[mt][1]] = acc[mt][3];
+        }
+    }
+    __syncthreads();
+    if (par == 1) {
+#pragma unroll
+        for (int mt = 0; mt < 2; mt++) {
+            red[(2 * q) * 128 + chl[mt][0]] += acc[mt][0];
+            red[(2 * q + 1) * 128 + chl[mt][0]] += acc[mt][1];
+            red[(2 * q) * 128 + chl[mt][1]] += acc[mt][2];
+            red[(2 * q + 1) * 128 + chl[mt][1]] += acc[mt][3];
+        }
+    }
+    __syncthreads();
+    // split-K over the cluster: CTA `rank` sums columns [rank*128/cs, (rank+1)*128/cs)
+    if (cs > 1) cluster_sync_all();
+    const int col0 = rank * 128 / cs, col1 = (rank + 1) * 128 / cs, width = col1 - col0;
+    const uint32_t red_s = smem_u32(red);
+    for (int idx = tid; idx < 8 * width; idx += 256) {
+        const int m = idx / width, n = col0 + idx % width;
+        float v = 0.0f;
+        if (cs > 1) {
+            const uint32_t off = red_s + (uint32_t)((m * 128 + n) * 4);
+            float part[8];
+#pragma unroll
+            for (int r = 0; r < 8; r++) part[r] = (r < cs) ? ld_peer_f32(off, (uint32_t)r) : 0.0f;
+#pragma unroll
+            for (int r = 0; r < 8; r++) v += part[r];
+        } else {
+            v = red[m * 128 + n];
+        }
+        if (m0 + m < p.M && n0 + n < p.N) {
+            const float b = p.bias ? __bfloat162float(__ushort_as_bfloat16(p.bias[n0 + n])) : 0.0f;
+            p.y[(int64_t)(m0 + m) * p.ldy + n0 + n] = __bfloat16_as_ushort(__float2bfloat16_rn(v + b));
+        }
+    }
+    if (cs > 1) cluster_sync_all();
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {     // looked up once, thread-safe
         void* ptr = nullptr;
@@ -763,6 +936,7 @@ int pick_split_mma(int64_t tiles, int64_t groups) {
 }
 
 cudaError_t launch_w4a16_mma(const GemmArgs& a, cudaStream_t st) {
+    const bool m8 = a.M <= 8;
     W4MmaParams p{};
     p.M = (int)a.M;
     p.N = (int)a.N;
@@ -781,6 +955,8 @@ cudaError_t launch_w4a16_mma(const GemmArgs& a, cudaStream_t st) {
     static std::atomic<bool> attr_set{false};
     if (!attr_set.load(std::memory_order_acquire)) {
         cudaError_t e = cudaFuncSetAttribute(k_w4a16_mma, cudaFuncAttributeMaxDynamicSharedMemorySize, kMmaSmem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(k_w4a16_mma8, cudaFuncAttributeMaxDynamicSharedMemorySize, kMmaSmem);
         if (e != cudaSuccess) return e;
         attr_set.store(true, std::memory_order_release);
     }
@@ -796,7 +972,7 @@ cudaError_t launch_w4a16_mma(const GemmArgs& a, cudaStream_t st) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, k_w4a16_mma, p);
+    const cudaError_t e = m8 ? cudaLaunchKernelEx(&cfg, k_w4a16_mma8, p) : cudaLaunchKernelEx(&cfg, k_w4a16_mma, p);
     if (e != cudaSuccess) (void)cudaGetLastError();   // a refused launch leaves no error for the next call
     return e;
 }

@@ -370,10 +370,14 @@ def w4a16_case(q, orc, M, K, N, with_bias=False, sym=False):
 
 @pytest.mark.parametrize("M,K,N", [(1, 4096, 4096), (16, 4096, 12288), (64, 12288, 4096), (5, 256, 72),
                                    (100, 512, 256), (200, 1024, 384), (33, 128, 136), (24, 512, 136),
-                                   # split-K over clusters of 2, 4, 5, 6 and 7 CTAs (warp-level kernel),
+                                   # split-K over clusters of 2, 4, 5, 6 and 7 CTAs (warp-level kernels),
                                    # and the tcgen05 kernel at its 4-way cap
                                    (1, 512, 128), (3, 1024, 256), (7, 1280, 128), (16, 1536, 136), (2, 1792, 72),
-                                   (64, 2048, 1024)])
+                                   (64, 2048, 1024),
+                                   # M <= 8 (tokens as the B operand) with clusters of 3 and 6 CTAs, and
+                                   # 8 < M <= 16 with 1, 2, 4, 5, 7 and 8
+                                   (2, 768, 128), (4, 1536, 256), (9, 256, 72), (12, 512, 136), (10, 1024, 256),
+                                   (13, 1280, 128), (11, 1792, 72), (14, 2048, 512)])
 def test_w4a16_gemm(q, orc, M, K, N):
     w4a16_case(q, orc, M, K, N)
 

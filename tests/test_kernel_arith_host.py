@@ -302,13 +302,15 @@ def test_row_quantizer_tests_reach_every_dispatched_variant():
 
 
 def test_w4a16_parity_cases_reach_every_cluster_size():
-    """The W4A16 parity shapes run the warp-level kernel with every split-K
-    cluster size it picks (1 to 8) and the tcgen05 kernel with 1, 2 and 4."""
+    """The W4A16 parity shapes run both warp-level kernels (M <= 8, tokens as
+    the B operand; 8 < M <= 16) with every split-K cluster size they pick (1 to
+    8) and the tcgen05 kernel with 1, 2 and 4."""
     import test_gpu_gemm
     shapes = []
     for mark in test_gpu_gemm.test_w4a16_gemm.pytestmark + test_gpu_gemm.test_w4a16_gemm_bias.pytestmark:
         if mark.name == "parametrize":
             shapes += list(mark.args[1])
-    mma = {pick_split_mma(cdiv(N, 128) * cdiv(M, 16), K // 128) for M, K, N in shapes if M <= 16}
+    mma8 = {pick_split_mma(cdiv(N, 128) * cdiv(M, 16), K // 128) for M, K, N in shapes if M <= 8}
+    mma16 = {pick_split_mma(cdiv(N, 128) * cdiv(M, 16), K // 128) for M, K, N in shapes if 8 < M <= 16}
     tc = {pick_split(cdiv(N, 128) * cdiv(M, 64), K // 128) for M, K, N in shapes if M > 16}
-    assert mma == set(range(1, 9)) and tc == {1, 2, 4}
+    assert mma8 == set(range(1, 9)) and mma16 == set(range(1, 9)) and tc == {1, 2, 4}
